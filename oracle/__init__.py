@@ -1,0 +1,170 @@
+"""CPU oracle for speculative-sampling verification and SSD outcome prediction.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import or run anything in this package; the
+product library never does, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``specv_oracle.c`` (plain fp64 loops, OpenMP over
+batch rows); this module compiles it with gcc and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "specv_oracle.c")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "libspecv_oracle.so")
+
+BF16, FP32 = 0, 1
+ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK = 1, 2, 4, 8
+ROW_ERRORS = ROW_BAD_TOKEN | ROW_NONFINITE | ROW_BAD_TEMP
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+
+
+def build(src: str = SRC, out: str = LIB_PATH, openmp: bool = True,
+          force: bool = False) -> str:
+    """Compile the oracle into a shared library and return its path."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    base = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+            "-fPIC", "-shared", src, "-o", out, "-lm"]
+    if openmp:
+        try:
+            subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                           capture_output=True)
+            return out
+        except subprocess.CalledProcessError:
+            pass
+    subprocess.run(base, check=True, capture_output=True)
+    return out
+
+
+_LIBS: dict = {}
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    path = path or build()
+    if path in _LIBS:
+        return _LIBS[path]
+    lib = ctypes.CDLL(path)
+    lib.specv_oracle_verify.restype = _I
+    lib.specv_oracle_verify.argtypes = [_I, _I, _I, _I, _P, _L, _L, _P, _L, _L,
+                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]
+    lib.specv_oracle_predict.restype = _I
+    lib.specv_oracle_predict.argtypes = [_I, _I, _I, _I, _I, _P, _L, _L, _P, _P,
+                                         _P, _P, _I]
+    lib.specv_oracle_check_hit.restype = None
+    lib.specv_oracle_check_hit.argtypes = [_I, _I, _I, _P, _P, _P, _P]
+    lib.specv_oracle_row_probs.restype = _I
+    lib.specv_oracle_row_probs.argtypes = [_I, _I, _P, ctypes.c_double, _P]
+    _LIBS[path] = lib
+    return lib
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return FP32
+    if a.dtype in (np.int16, np.uint16):
+        return BF16
+    raise TypeError(f"logits must be float32 or int16 bf16 bits, got {a.dtype}")
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_P)
+
+
+def _strides(a: np.ndarray):
+    it = a.itemsize
+    return a.strides[0] // it, a.strides[1] // it
+
+
+def verify(target, draft, tokens, temperature, uniforms, nthreads: int = 1,
+           lib=None) -> dict:
+    """Run the oracle's verification on B batch rows.
+
+    target [B, >=K+1, V], draft [B, >=K, V] (fp32 or int16 bf16 bits, rows
+    contiguous along V), tokens int32 [B, K], temperature fp32 [B], uniforms
+    fp32 [B, K+1].  Returns accept_len, out_tokens, p (=p_i(x_i)),
+    q (=q_i(x_i)), alpha (=sum_v min(p_i, q_i)), status, boundary.
+    """
+    lib = lib or load()
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, K = tokens.shape
+    V = target.shape[-1]
+    assert target.strides[-1] == target.itemsize and draft.strides[-1] == draft.itemsize
+    assert target.dtype == draft.dtype
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    out = dict(
+        accept_len=np.zeros(B, np.int32),
+        out_tokens=np.zeros((B, K + 1), np.int32),
+        p=np.zeros((B, K), np.float64),
+        q=np.zeros((B, K), np.float64),
+        alpha=np.zeros((B, K), np.float64),
+        status=np.zeros(B, np.int32),
+        boundary=np.zeros(B, np.int32),
+    )
+    tbs, trs = _strides(target)
+    dbs, drs = _strides(draft)
+    rc = lib.specv_oracle_verify(
+        B, K, V, _dtype_code(target), _ptr(target), tbs, trs, _ptr(draft), dbs,
+        drs, _ptr(tokens), _ptr(temperature), _ptr(uniforms),
+        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["p"]),
+        _ptr(out["q"]), _ptr(out["alpha"]), _ptr(out["status"]),
+        _ptr(out["boundary"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle verify: bad sizes")
+    return out
+
+
+def predict(draft, tokens, F: int, nthreads: int = 1, lib=None) -> dict:
+    """Top-F outcome keys from draft logits [B, K+1, V]; tokens int32 [B, K]."""
+    lib = lib or load()
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, K = tokens.shape
+    V = draft.shape[-1]
+    assert draft.shape[1] >= K + 1 and draft.strides[-1] == draft.itemsize
+    keys = np.zeros((B, K + 1, F), np.int32)
+    key_logits = np.zeros((B, K + 1, F), np.float32)
+    status = np.zeros(B, np.int32)
+    dbs, drs = _strides(draft)
+    rc = lib.specv_oracle_predict(B, K, V, F, _dtype_code(draft), _ptr(draft),
+                                  dbs, drs, _ptr(tokens), _ptr(keys),
+                                  _ptr(key_logits), _ptr(status), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle predict: bad sizes")
+    return dict(keys=keys, key_logits=key_logits, status=status)
+
+
+def check_hit(keys, accept_len, out_tokens, lib=None) -> np.ndarray:
+    lib = lib or load()
+    keys = np.ascontiguousarray(keys, dtype=np.int32)
+    accept_len = np.ascontiguousarray(accept_len, dtype=np.int32)
+    out_tokens = np.ascontiguousarray(out_tokens, dtype=np.int32)
+    B, K1, F = keys.shape
+    hit = np.zeros(B, np.uint8)
+    lib.specv_oracle_check_hit(B, K1 - 1, F, _ptr(keys), _ptr(accept_len),
+                               _ptr(out_tokens), _ptr(hit))
+    return hit
+
+
+def row_probs(z, T: float, lib=None) -> np.ndarray:
+    """The oracle's a1 distribution of one logit row (fp32 or bf16 bits)."""
+    lib = lib or load()
+    z = np.ascontiguousarray(z)
+    p = np.zeros(z.shape[-1], np.float64)
+    rc = lib.specv_oracle_row_probs(z.shape[-1], _dtype_code(z), _ptr(z),
+                                    float(T), _ptr(p))
+    if rc & ROW_ERRORS:
+        raise ValueError(f"row status {rc}")
+    return p

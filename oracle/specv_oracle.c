@@ -1,0 +1,343 @@
+/*
+ * specv_oracle.c -- plain, slow, double-precision CPU statement of batched
+ * speculative-sampling verification and SSD (Saguaro) outcome prediction.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no source, header, table or helper with the CUDA
+ * library; the two meet only in the seeded input arrays.
+ *
+ * Sources (page title -- section):
+ *   [SSD]  "Speculative Speculative Decoding" (Kumar, Dao, May) -- §2.1
+ *          (accept rule, residual, bonus token, outcome v_T = (k, t*)),
+ *          §3.1 Alg. 1 and the cache hit/miss definition, §4.1.1 (top-F_k
+ *          outcome prediction excluding the sent draft token).
+ *   [DLN]  "Speculative Decoding" (dl-note) -- §2.2 (accept probability),
+ *          §2.3 (residual distribution), §3 (exactness), Appendix (vLLM
+ *          convention: accept iff draft prob > 0 and p/q >= u).
+ *   [CS349D] "Lecture 5 - Speculative Decoding and SpecInfer" -- §2.1
+ *          (greedy and temperature as adjusted distributions), §2.2 (the rule
+ *          u <= p(x)/q(x)), §2.7 (greedy special case), §3.1 (one iteration:
+ *          residual at the first rejection, or a sample from p_{gamma+1}).
+ *
+ * Readings where the pages leave a step open (each one is listed in the
+ * design notes):
+ *   - temperature: p = softmax(z/T) computed as exp((z - max z)/T)/sum; the
+ *     same T for target and draft of a batch row; T = 0 is greedy (one-hot at
+ *     the FIRST maximum).
+ *   - accept test at position i: accept iff q_i(x_i) > 0 and
+ *     p_i(x_i)/q_i(x_i) >= U[i].  q_i(x_i) > 0 holds exactly when the draft
+ *     logit of x_i is finite; the ratio is evaluated as exp(log p - log q) so
+ *     that neither factor underflows.  Greedy rows do not consult U: with
+ *     one-hot p and q the ratio is 1 iff x_i is the argmax of both rows.
+ *   - bonus: r = max(p_n - q_n, 0) after a rejection at n, r = p_K if all K
+ *     drafts are accepted; t* = the smallest v whose running sum of r in
+ *     index order exceeds U[K] * sum(r).  If sum(r) is 0 the draw falls back
+ *     to r = p_n; if rounding leaves no v, t* is the last v with r(v) > 0.
+ *     Both fallbacks set ROW_FALLBACK.  Greedy bonus = argmax of p_n.
+ *   - outcome prediction: keys at lookahead k are the F largest draft logits
+ *     of draft row k, ordered by (logit descending, index ascending), with the
+ *     token x_{k+1} that was sent for verification at that position removed
+ *     (k < K); nothing is removed at k = K.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_BF16 = 0, OR_FP32 = 1 };
+
+/* Per-batch-row status bits (same meaning as the library's, defined here
+ * independently). */
+enum {
+  ROW_BAD_TOKEN = 1,  /* a draft token outside [0, V) */
+  ROW_NONFINITE = 2,  /* NaN or +inf logit, or a row with no finite logit */
+  ROW_BAD_TEMP = 4,   /* temperature < 0, NaN or inf */
+  ROW_FALLBACK = 8    /* bonus draw used a fallback (informational) */
+};
+
+/* Margin inside which an executed accept test or the bonus draw counts as a
+ * boundary case: |U - p/q| < 1e-6, or U*R within 1e-6*R of a running sum. */
+#define BOUNDARY_EPS 1e-6
+
+static double load_logit(const void* base, int dtype, int64_t idx) {
+  if (dtype == OR_FP32) return (double)((const float*)base)[idx];
+  uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* ---------------------------------------------------------------------------
+ * a1  Distribution of one vocabulary row: [CS349D] §2.1 (greedy = one-hot,
+ *     temperature T = softmax(logits / T)).
+ * Fills p[0..V-1], the first argmax, the max logit m and log of the softmax
+ * normaliser S = sum_v exp((z_v - m)/T) (0 for greedy).  Returns status bits.
+ */
+static int row_distribution(const void* base, int dtype, int64_t off, int V,
+                            double T, double* p, int* argmax, double* m_out,
+                            double* logS_out) {
+  int am = -1;
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double z = load_logit(base, dtype, off + v);
+    if (isnan(z) || z == INFINITY) return ROW_NONFINITE;
+    if (z > m) { m = z; am = v; }
+  }
+  if (am < 0) return ROW_NONFINITE; /* every logit is -inf: no distribution */
+  *argmax = am;
+  *m_out = m;
+  if (T == 0.0) {
+    for (int v = 0; v < V; ++v) p[v] = (v == am) ? 1.0 : 0.0;
+    *logS_out = 0.0;
+    return 0;
+  }
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) {
+    p[v] = exp((load_logit(base, dtype, off + v) - m) / T);
+    S += p[v];
+  }
+  for (int v = 0; v < V; ++v) p[v] /= S;
+  *logS_out = log(S);
+  return 0;
+}
+
+/* log p(v) for a temperature row, from the row's max and log-normaliser. */
+static double log_prob(const void* base, int dtype, int64_t off, int v, double T,
+                       double m, double logS) {
+  return (load_logit(base, dtype, off + v) - m) / T - logS;
+}
+
+/* ---------------------------------------------------------------------------
+ * Verification of one batch row.
+ *   a2 accept scan: [DLN] §2.2 and Appendix; [CS349D] §2.2, §2.7, §3.1 step 3.
+ *   a3 bonus: [SSD] §2.1 (residual r ∝ max(p_target - p_draft, 0), target
+ *      itself when all drafts are accepted); [DLN] §2.3; [CS349D] §3.1 step 4.
+ * Scratch: pt[(K+1)*V], qd[K*V], r[V].
+ */
+static void verify_row(int K, int V, int dtype, const void* target,
+                       int64_t t_off, int64_t t_rs, const void* draft,
+                       int64_t d_off, int64_t d_rs, const int32_t* x, double T,
+                       const float* U, int32_t* n_out, int32_t* tok_out,
+                       double* p_out, double* q_out, double* alpha_out,
+                       int32_t* status_out, int32_t* boundary_out, double* pt,
+                       double* qd, double* r) {
+  int status = 0;
+  int boundary = 0;
+  for (int i = 0; i <= K; ++i) tok_out[i] = -1;
+  for (int i = 0; i < K; ++i) { p_out[i] = 0.0; q_out[i] = 0.0; alpha_out[i] = 0.0; }
+  *n_out = 0;
+
+  if (!(T >= 0.0) || isinf(T)) status |= ROW_BAD_TEMP;
+  for (int i = 0; i < K; ++i)
+    if (x[i] < 0 || x[i] >= V) status |= ROW_BAD_TOKEN;
+  if (status) { *status_out = status; *boundary_out = 0; return; }
+
+  int amt[64], amd[64];
+  double mt[64], lst[64], md[64], lsd[64];
+  for (int i = 0; i <= K; ++i)
+    status |= row_distribution(target, dtype, t_off + (int64_t)i * t_rs, V, T,
+                               pt + (int64_t)i * V, &amt[i], &mt[i], &lst[i]);
+  for (int i = 0; i < K; ++i)
+    status |= row_distribution(draft, dtype, d_off + (int64_t)i * d_rs, V, T,
+                               qd + (int64_t)i * V, &amd[i], &md[i], &lsd[i]);
+  if (status) { *status_out = status; *boundary_out = 0; return; }
+
+  /* Per-position p_i(x_i), q_i(x_i) and the overlap sum_v min(p_i, q_i)
+   * ([SSD] §2.1 Theorem 1). */
+  for (int i = 0; i < K; ++i) {
+    const double* p = pt + (int64_t)i * V;
+    const double* q = qd + (int64_t)i * V;
+    p_out[i] = p[x[i]];
+    q_out[i] = q[x[i]];
+    double a = 0.0;
+    for (int v = 0; v < V; ++v) a += (p[v] < q[v]) ? p[v] : q[v];
+    alpha_out[i] = a;
+  }
+
+  /* a2: left-to-right accept test, stop at the first rejection. */
+  int n = K;
+  for (int i = 0; i < K; ++i) {
+    int accept;
+    if (T == 0.0) {
+      accept = (x[i] == amd[i]) && (x[i] == amt[i]);
+    } else {
+      int64_t to = t_off + (int64_t)i * t_rs, dof = d_off + (int64_t)i * d_rs;
+      double zdx = load_logit(draft, dtype, dof + x[i]);
+      if (zdx == -INFINITY) {
+        accept = 0; /* q_i(x_i) = 0: reject */
+      } else {
+        double ratio = exp(log_prob(target, dtype, to, x[i], T, mt[i], lst[i]) -
+                           log_prob(draft, dtype, dof, x[i], T, md[i], lsd[i]));
+        accept = ratio >= (double)U[i];
+        if (fabs((double)U[i] - ratio) < BOUNDARY_EPS) boundary = 1;
+      }
+    }
+    if (!accept) { n = i; break; }
+  }
+
+  /* a3: bonus token. */
+  int tstar;
+  if (T == 0.0) {
+    tstar = amt[n]; /* residual of two one-hots, or p_{K+1}: argmax of p_n */
+  } else {
+    const double* p = pt + (int64_t)n * V;
+    double R = 0.0;
+    if (n < K) {
+      const double* q = qd + (int64_t)n * V;
+      for (int v = 0; v < V; ++v) { r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0; R += r[v]; }
+    } else {
+      for (int v = 0; v < V; ++v) { r[v] = p[v]; R += r[v]; }
+    }
+    if (!(R > 0.0)) {
+      status |= ROW_FALLBACK;
+      R = 0.0;
+      for (int v = 0; v < V; ++v) { r[v] = p[v]; R += r[v]; }
+    }
+    double tau = (double)U[K] * R;
+    double cum = 0.0, prev = 0.0;
+    tstar = -1;
+    for (int v = 0; v < V; ++v) {
+      prev = cum;
+      cum += r[v];
+      if (cum > tau) { tstar = v; break; }
+    }
+    if (tstar < 0) {
+      status |= ROW_FALLBACK;
+      for (int v = V - 1; v >= 0; --v) if (r[v] > 0.0) { tstar = v; break; }
+      boundary = 1;
+    } else if (fabs(tau - prev) < BOUNDARY_EPS * R || fabs(cum - tau) < BOUNDARY_EPS * R) {
+      boundary = 1;
+    }
+  }
+
+  *n_out = n;
+  for (int i = 0; i < n; ++i) tok_out[i] = x[i];
+  tok_out[n] = tstar;
+  *status_out = status;
+  *boundary_out = boundary;
+}
+
+/* Exported: verification of B batch rows.  Logit layouts are
+ *   target[b*t_bs + i*t_rs + v], i in [0, K]     (K+1 target rows)
+ *   draft [b*d_bs + i*d_rs + v], i in [0, K)     (K draft rows)
+ * Outputs: accept_len[B], out_tokens[B*(K+1)] (-1 padded), p_out/q_out/
+ * alpha_out[B*K], row_status[B], boundary[B].  nthreads <= 0 uses all. */
+int specv_oracle_verify(int B, int K, int V, int dtype, const void* target,
+                        int64_t t_bs, int64_t t_rs, const void* draft,
+                        int64_t d_bs, int64_t d_rs, const int32_t* tokens,
+                        const float* temperature, const float* uniforms,
+                        int32_t* accept_len, int32_t* out_tokens, double* p_out,
+                        double* q_out, double* alpha_out, int32_t* row_status,
+                        int32_t* boundary, int nthreads) {
+  if (B < 0 || K < 1 || K > 63 || V < 1) return 1;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int b = 0; b < B; ++b) {
+    double* pt = (double*)malloc(sizeof(double) * (size_t)(K + 1) * V);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)K * V);
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    verify_row(K, V, dtype, target, (int64_t)b * t_bs, t_rs, draft,
+               (int64_t)b * d_bs, d_rs, tokens + (int64_t)b * K,
+               (double)temperature[b], uniforms + (int64_t)b * (K + 1),
+               accept_len + b, out_tokens + (int64_t)b * (K + 1),
+               p_out + (int64_t)b * K, q_out + (int64_t)b * K,
+               alpha_out + (int64_t)b * K, row_status + b, boundary + b, pt, qd, r);
+    free(pt);
+    free(qd);
+    free(r);
+  }
+  (void)nthreads;
+  return 0;
+}
+
+/* Exported: the a1 distribution of one row, for the pins. */
+int specv_oracle_row_probs(int V, int dtype, const void* row, double T,
+                           double* p) {
+  int am;
+  double m, ls;
+  return row_distribution(row, dtype, 0, V, T, p, &am, &m, &ls);
+}
+
+/* ---------------------------------------------------------------------------
+ * a4  Outcome prediction: [SSD] §4.1.1 ("Saguaro verification-outcome
+ *     prediction"): at every lookahead k take the top-F_k tokens of the draft
+ *     logits, excluding the token sent for verification at that position.
+ *     Full sort of the candidates; no partial selection.
+ */
+typedef struct { double z; int v; } cand_t;
+
+static int cand_cmp(const void* a, const void* b) {
+  const cand_t* x = (const cand_t*)a;
+  const cand_t* y = (const cand_t*)b;
+  if (x->z > y->z) return -1;
+  if (x->z < y->z) return 1;
+  return (x->v < y->v) ? -1 : (x->v > y->v);
+}
+
+int specv_oracle_predict(int B, int K, int V, int F, int dtype,
+                         const void* draft, int64_t d_bs, int64_t d_rs,
+                         const int32_t* tokens, int32_t* keys, float* key_logits,
+                         int32_t* row_status, int nthreads) {
+  if (B < 0 || K < 1 || V < 1 || F < 1) return 1;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int b = 0; b < B; ++b) {
+    cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (size_t)V);
+    int status = 0;
+    for (int k = 0; k <= K; ++k) {
+      int32_t* kk = keys + ((int64_t)b * (K + 1) + k) * F;
+      float* kl = key_logits + ((int64_t)b * (K + 1) + k) * F;
+      for (int f = 0; f < F; ++f) { kk[f] = -1; kl[f] = -INFINITY; }
+      int excl = -1;
+      if (k < K) {
+        excl = tokens[(int64_t)b * K + k];
+        if (excl < 0 || excl >= V) { status |= ROW_BAD_TOKEN; continue; }
+      }
+      int64_t off = (int64_t)b * d_bs + (int64_t)k * d_rs;
+      int nc = 0, bad = 0;
+      for (int v = 0; v < V; ++v) {
+        double z = load_logit(draft, dtype, off + v);
+        if (isnan(z) || z == INFINITY) { bad = 1; break; }
+        if (v == excl) continue;
+        c[nc].z = z;
+        c[nc].v = v;
+        ++nc;
+      }
+      if (bad) { status |= ROW_NONFINITE; continue; }
+      qsort(c, (size_t)nc, sizeof(cand_t), cand_cmp);
+      for (int f = 0; f < F && f < nc; ++f) { kk[f] = c[f].v; kl[f] = (float)c[f].z; }
+    }
+    row_status[b] = status;
+    free(c);
+  }
+  (void)nthreads;
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * a5  Cache hit: [SSD] §3.1, hit iff the realised outcome v_T = (k, t*) is in
+ *     the speculation cache S_T, i.e. t* is among the keys predicted for
+ *     accept length k.
+ */
+void specv_oracle_check_hit(int B, int K, int F, const int32_t* keys,
+                            const int32_t* accept_len, const int32_t* out_tokens,
+                            uint8_t* hit) {
+  for (int b = 0; b < B; ++b) {
+    int n = accept_len[b];
+    hit[b] = 0;
+    if (n < 0 || n > K) continue;
+    int t = out_tokens[(int64_t)b * (K + 1) + n];
+    if (t < 0) continue;
+    const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;
+    for (int f = 0; f < F; ++f)
+      if (kk[f] == t) { hit[b] = 1; break; }
+  }
+}

@@ -1,0 +1,485 @@
+"""Pins for the CPU oracle: each check_* raises AssertionError on failure.
+
+Every check ties the oracle to something other than itself: a value printed
+on the pages (tests/golden), a closed form stated there, a library routine
+(scipy softmax, numpy lexsort), an exact rational enumeration of the output
+distribution, or a chi-square test against the target distribution.  The same
+functions are run against oracle builds with a planted mistake, which must
+fail them (test_oracle_mutations.py).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction as Fr
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# helpers
+
+def logits_for(P, T: float = 1.0) -> np.ndarray:
+    """fp32 logits whose softmax at temperature T is P (up to fp32 rounding)."""
+    return np.array([[T * math.log(float(p)) if p > 0 else -np.inf for p in row]
+                     for row in P], dtype=np.float32)
+
+
+def rational_rows(rng, n: int, V: int, lo: int = 1, hi: int = 20):
+    a = rng.integers(lo, hi + 1, size=(n, V))
+    return [[Fr(int(x), int(row.sum())) for x in row] for row in a]
+
+
+def run_verify(lib, P, Q, tokens, uniforms, T: float = 1.0):
+    """Oracle on B rows sharing the logits of P (K+1 rows) and Q (K rows)."""
+    tokens = np.asarray(tokens, np.int32)
+    B, K = tokens.shape
+    zt = logits_for(P, T)
+    zd = logits_for(Q, T)
+    target = np.broadcast_to(zt[None], (B,) + zt.shape)
+    draft = np.broadcast_to(zd[None], (B,) + zd.shape)
+    temp = np.full(B, T, np.float32)
+    return oracle.verify(target, draft, tokens, temp,
+                         np.asarray(uniforms, np.float32), nthreads=0, lib=lib)
+
+
+def enumerate_pieces(P, Q):
+    """Leaves of the verification procedure on which its output is constant.
+
+    Follows the pages' statement of the rule: x_i ~ q_i; accepted on
+    U_i in [0, min(1, p_i(x_i)/q_i(x_i))); after the first rejection at n the
+    bonus is drawn from max(p_n - q_n, 0)/R by inverse CDF, and from p_K when
+    all K are accepted.  Each leaf is (weight, tokens, uniforms) with U at the
+    midpoint of its piece; weights are exact rationals.
+    """
+    K = len(Q)
+    V = len(P[0])
+    leaves = []
+
+    def bonus(xs, us, w, r):
+        R = sum(r)
+        assert R > 0
+        cum = Fr(0)
+        for v in range(V):
+            if r[v] > 0:
+                mid = (cum + r[v] / 2) / R
+                # positions after the first rejection must not matter; they get
+                # a uniform that would reject almost any token, so an oracle
+                # that kept scanning would show it
+                toks = xs + [0] * (K - len(xs))
+                uu = us + [Fr(999, 1000)] * (K - len(us)) + [mid]
+                leaves.append((w * r[v] / R, toks, uu))
+                cum += r[v]
+
+    def rec(i, xs, us, w):
+        if i == K:
+            bonus(xs, us, w, list(P[K]))
+            return
+        for x in range(V):
+            if Q[i][x] == 0:
+                continue
+            wx = w * Q[i][x]
+            a = min(Fr(1), P[i][x] / Q[i][x])
+            if a > 0:
+                rec(i + 1, xs + [x], us + [a / 2], wx * a)
+            if a < 1:
+                r = [max(P[i][v] - Q[i][v], Fr(0)) for v in range(V)]
+                bonus(xs + [x], us + [(a + 1) / 2], wx * (1 - a), r)
+
+    rec(0, [], [], Fr(1))
+    return leaves
+
+
+def exact_output_law(lib, P, Q, T: float = 1.0):
+    """Exact law of (accept length, emitted tokens) of the oracle on (P, Q)."""
+    leaves = enumerate_pieces(P, Q)
+    tokens = np.array([lf[1] for lf in leaves], np.int32)
+    uniforms = np.array([[float(u) for u in lf[2]] for lf in leaves], np.float32)
+    out = run_verify(lib, P, Q, tokens, uniforms, T)
+    return leaves, out
+
+
+# ---------------------------------------------------------------------------
+# a1 distribution
+
+def check_softmax_library(lib):
+    """Oracle p = scipy.special.softmax(z / T) on random rows; greedy one-hot."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(7)
+    for V in (1, 2, 3, 17, 1000):
+        for T in (0.25, 0.7, 1.0, 2.5):
+            z = (rng.standard_normal(V) * 3).astype(np.float32)
+            p = oracle.row_probs(z, T, lib=lib)
+            ref = softmax(z.astype(np.float64) / T)
+            assert np.max(np.abs(p - ref)) < 1e-14, (V, T)
+            assert abs(p.sum() - 1.0) < 1e-12
+    z = np.array([1.0, 3.0, -2.0, 3.0, 0.5], np.float32)
+    p = oracle.row_probs(z, 0.0, lib=lib)
+    assert p.tolist() == [0.0, 1.0, 0.0, 0.0, 0.0], p  # first maximum wins
+    # bf16 bit patterns decode exactly: 1.0, 0.0, -2.0, -inf
+    bits = np.array([0x3F80, 0x0000, 0xC000, 0xFF80], np.uint16).view(np.int16)
+    p = oracle.row_probs(bits, 1.0, lib=lib)
+    ref = softmax(np.array([1.0, 0.0, -2.0, -np.inf]))
+    assert np.max(np.abs(p - ref)) < 1e-15
+
+
+def check_thm1_overlap(lib):
+    """[SSD] Theorem 1: alpha = sum min(p, q) = 1 - 0.5 * ||p - q||_1."""
+    rng = np.random.default_rng(11)
+    for V in (2, 5, 64, 3000):
+        for T in (0.5, 1.0):
+            zt = (rng.standard_normal((2, V)) * 2).astype(np.float32)
+            zd = (zt[:1] + rng.standard_normal((1, V))).astype(np.float32)
+            p = oracle.row_probs(zt[0], T, lib=lib)
+            q = oracle.row_probs(zd[0], T, lib=lib)
+            out = oracle.verify(zt[None], zd[None], np.zeros((1, 1), np.int32),
+                                np.array([T], np.float32),
+                                np.array([[0.5, 0.5]], np.float32), lib=lib)
+            a = out["alpha"][0, 0]
+            assert abs(a - (1.0 - 0.5 * np.abs(p - q).sum())) < 1e-12, (V, T, a)
+
+
+# ---------------------------------------------------------------------------
+# a2 + a3, worked examples from the pages
+
+def check_exercise_1(lib):
+    """Lecture 5 §11 Exercise 1: beta 0.6, residual [1,0,0], accept probs."""
+    ex = golden("cs349d_worked_examples.json")["exercise_1"]
+    P = [ex["p"], ex["p"]]
+    Q = [ex["q"]]
+    acc = ex["accept_prob_per_token"]
+    rows_t, rows_u = [], []
+    for x in range(3):
+        for du in (-2e-3, 2e-3):
+            u = min(acc[x] + du, 0.999)
+            rows_t.append([x])
+            rows_u.append([u, 0.5])
+    out = run_verify(lib, P, Q, rows_t, rows_u)
+    j = 0
+    for x in range(3):
+        for du in (-2e-3, 2e-3):
+            expect_accept = (acc[x] + du) <= acc[x] or acc[x] >= 1.0
+            assert out["accept_len"][j] == (1 if expect_accept else 0), (x, du)
+            if not expect_accept:
+                # residual is one-hot on token 0 whatever the bonus uniform
+                assert out["out_tokens"][j, 0] == 0
+            j += 1
+    assert abs(out["alpha"][0, 0] - ex["acceptance_rate"]) < 1e-6
+    # exact law of the first emitted token equals p
+    leaves, out = exact_output_law(lib, [[Fr(str(v)) for v in ex["p"]]] * 2,
+                                   [[Fr(str(v)) for v in ex["q"]]])
+    law = [Fr(0)] * 3
+    for (w, _, _), t in zip(leaves, out["out_tokens"][:, 0]):
+        law[t] += w
+    assert law == [Fr(str(v)) for v in ex["p"]], law
+
+
+def check_section_2_3(lib):
+    """Lecture 5 §2.3: beta 0.75; B accepted w.p. 0.6; residual A:C = 0.2:0.05."""
+    ex = golden("cs349d_worked_examples.json")["section_2_3_partial"]
+    s = ex["surviving"]
+    P = [ex["p"], ex["p"]]
+    Q = [ex["q"]]
+    out = run_verify(lib, P, Q, [[1], [1], [1], [1]],
+                     [[0.599, 0.5], [0.601, 0.79], [0.601, 0.81], [0.601, 0.0]])
+    assert out["accept_len"].tolist() == [1, 0, 0, 0]
+    a, c = s["residual_ratio_A_to_C"]
+    cut = a / (a + c)  # bonus is A below this uniform, C above
+    assert abs(cut - 0.8) < 1e-12
+    assert out["out_tokens"][1:, 0].tolist() == [0, 2, 0]
+    assert abs(out["alpha"][0, 0] - s["acceptance_rate"]) < 1e-6
+    assert abs(out["p"][0, 0] - s["p_B"]) < 1e-6
+    assert abs(out["p"][0, 0] / out["q"][0, 0] - s["accept_prob_B"]) < 1e-6
+
+
+# ---------------------------------------------------------------------------
+# a2 + a3, exactness by enumeration ([DLN] §3, [CS349D] §2.4, [SSD] §2.1)
+
+def check_exact_enumeration(lib, seed: int = 3, V: int = 5, K: int = 2,
+                            T: float = 1.0, pairs: int = 6):
+    """The emitted token at position i+1, given the first i drafts accepted,
+    has law exactly p_{i+1}; P(accept at i) = sum min(p_i, q_i)."""
+    rng = np.random.default_rng(seed)
+    for _ in range(pairs):
+        P = rational_rows(rng, K + 1, V)
+        Q = rational_rows(rng, K, V)
+        leaves, out = exact_output_law(lib, P, Q, T)
+        n = out["accept_len"]
+        toks = out["out_tokens"]
+        assert out["status"].max() & oracle.ROW_ERRORS == 0
+        for i in range(K + 1):
+            mass = Fr(0)
+            law = [Fr(0)] * V
+            for (w, _, _), ni, tk in zip(leaves, n, toks):
+                if ni >= i:
+                    mass += w
+                    law[tk[i]] += w
+            # P(first i accepted) = prod_j alpha_j
+            alpha = Fr(1)
+            for j in range(i):
+                alpha *= sum(min(P[j][v], Q[j][v]) for v in range(V))
+            assert mass == alpha, (i, float(mass), float(alpha))
+            cond = [l / mass for l in law]
+            assert cond == P[i], (i, [float(c) for c in cond], [float(p) for p in P[i]])
+
+
+def check_chisq(lib, alpha_target: float, draws: int = 1_000_000, V: int = 8,
+                K: int = 3, seed: int = 5):
+    """Monte-Carlo: first emitted token ~ p_1 and (given n >= i) the (i+1)-th
+    ~ p_{i+1}; chi-square p-value above 1e-3 for each position."""
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(seed)
+    P = [rng.dirichlet(np.ones(V)) for _ in range(K + 1)]
+    Q = []
+    for i in range(K):
+        d = np.zeros(V)
+        d[np.argsort(P[i])[:2]] = 0.5  # mass where p is small
+        lo, hi = 0.0, 1.0
+        for _ in range(60):  # bisection on lambda for sum min(p, q) = target
+            lam = 0.5 * (lo + hi)
+            q = lam * P[i] + (1 - lam) * d
+            a = np.minimum(P[i], q).sum()
+            lo, hi = (lam, hi) if a < alpha_target else (lo, lam)
+        Q.append(q)
+    x = np.stack([rng.choice(V, size=draws, p=Q[i] / Q[i].sum()) for i in range(K)], 1)
+    u = rng.random((draws, K + 1), dtype=np.float32)
+    out = run_verify(lib, [list(p) for p in P], [list(q) for q in Q], x, u)
+    n = out["accept_len"]
+    toks = out["out_tokens"]
+    for i in range(K + 1):
+        sel = n >= i
+        obs = np.bincount(toks[sel, i], minlength=V)
+        exp = P[i] / P[i].sum() * sel.sum()
+        pval = chisquare(obs, exp).pvalue
+        assert pval > 1e-3, (alpha_target, i, pval)
+
+
+def check_expected_tokens(lib):
+    """E[n+1] = (1 - a^(g+1))/(1 - a) with i.i.d. rows (Lecture 5 §4.1,
+    survey blog §4.3); the printed speedups S = E/(g c + 1) of Lecture 5 §4.3
+    and Exercises 2-4 follow from the oracle's exact law of n."""
+    fx = golden("cs349d_worked_examples.json")["expected_tokens_and_speedup"]
+    rows = {  # V=2 pairs with an exact overlap alpha
+        0.7: ([Fr(8, 10), Fr(2, 10)], [Fr(5, 10), Fr(5, 10)]),
+        0.8: ([Fr(9, 10), Fr(1, 10)], [Fr(7, 10), Fr(3, 10)]),
+        0.75: ([Fr(7, 8), Fr(1, 8)], [Fr(5, 8), Fr(3, 8)]),
+        0.6: ([Fr(9, 10), Fr(1, 10)], [Fr(5, 10), Fr(5, 10)]),
+        0.1: ([Fr(19, 20), Fr(1, 20)], [Fr(1, 20), Fr(19, 20)]),
+    }
+    cache = {}
+    for case in fx["cases"]:
+        a, g, c = case["alpha"], case["gamma"], case["c"]
+        key = (a, g)
+        if key not in cache:
+            p, q = rows[a]
+            assert sum(min(x, y) for x, y in zip(p, q)) == Fr(str(a))
+            leaves, out = exact_output_law(lib, [p] * (g + 1), [q] * g)
+            E = sum(w * (int(ni) + 1) for (w, _, _), ni in zip(leaves, out["accept_len"]))
+            for k in range(g + 1):
+                pk = sum(w for (w, _, _), ni in zip(leaves, out["accept_len"]) if ni == k)
+                A = Fr(str(a))
+                assert pk == (A ** k * (1 - A) if k < g else A ** g), (a, g, k)
+            cache[key] = E
+        E = cache[key]
+        closed = (1 - Fr(str(a)) ** (g + 1)) / (1 - Fr(str(a)))
+        assert E == closed
+        if "E" in case:
+            assert round(float(E), 3) == case["E"], (case, float(E))
+        S = float(E) / (g * c + 1)
+        # printed to two decimals; Exercise 3 prints 2.41 at gamma=8 where the
+        # closed form gives 2.40495, so allow half a unit in the last digit
+        # plus that 0.005 slip
+        assert abs(S - case["S"]) <= 0.0051, (case, S)
+    bad = fx["contradiction"]
+    E = cache.get((bad["alpha"], bad["gamma"]))
+    assert E is not None and round(float(E), 2) != bad["printed"]
+
+
+def check_wrong_method_a_is_biased(lib):
+    """Lecture 5 §2.6: resampling from p after a rejection is biased.  The
+    oracle's exact law differs from the wrong method's law by a visible TV."""
+    rng = np.random.default_rng(21)
+    tvs = []
+    for _ in range(20):
+        P = rational_rows(rng, 2, 5)
+        Q = rational_rows(rng, 1, 5)
+        alpha = sum(min(P[0][v], Q[0][v]) for v in range(5))
+        wrong = [min(P[0][v], Q[0][v]) + (1 - alpha) * P[0][v] for v in range(5)]
+        leaves, out = exact_output_law(lib, P, Q)
+        law = [Fr(0)] * 5
+        for (w, _, _), t in zip(leaves, out["out_tokens"][:, 0]):
+            law[t] += w
+        assert law == P[0]
+        tvs.append(0.5 * sum(abs(float(a - b)) for a, b in zip(law, wrong)))
+    assert max(tvs) > 0.05
+
+
+# ---------------------------------------------------------------------------
+# greedy and invariants
+
+def check_greedy(lib):
+    """Lecture 5 §2.7: greedy = accept iff the draft's argmax is the target's
+    argmax; the bonus is the target argmax.  Ties go to the first index."""
+    zt = np.array([[1, 3, 3, 2], [5, 0, 0, 5], [0, 1, 2, 2], [4, 4, 0, 0]], np.float32)
+    zd = np.array([[0, 2, 2, 1], [1, 1, 0, 0], [9, 0, 0, 0]], np.float32)
+    # draft argmaxes (first max): 1, 0, 0; target argmaxes: 1, 0, 2, 0
+    tokens = np.array([[1, 0, 0], [1, 0, 0], [1, 3, 0], [2, 0, 0]], np.int32)
+    B = tokens.shape[0]
+    out = oracle.verify(np.broadcast_to(zt[None], (B, 4, 4)),
+                        np.broadcast_to(zd[None], (B, 3, 4)), tokens,
+                        np.zeros(B, np.float32), np.full((B, 4), 0.999, np.float32),
+                        lib=lib)
+    # row 0: x1=1 ok, x2=0 ok, x3=0 (target argmax 2) rejected -> bonus 2
+    assert out["accept_len"][0] == 2 and out["out_tokens"][0].tolist() == [1, 0, 2, -1]
+    # row 2: x2=3 is not the draft argmax (q(x2)=0) -> rejected, bonus argmax p_2 = 0
+    assert out["accept_len"][2] == 1 and out["out_tokens"][2].tolist() == [1, 0, -1, -1]
+    # row 3: x1=2 rejected at once, bonus = target argmax of row 0 = 1
+    assert out["accept_len"][3] == 0 and out["out_tokens"][3].tolist() == [1, -1, -1, -1]
+    # all-accept path: the bonus is the argmax of p_{K+1}
+    tok = np.array([[1, 0, 2]], np.int32)
+    zd2 = zt[:3].copy()
+    out = oracle.verify(zt[None], zd2[None], tok, np.zeros(1, np.float32),
+                        np.zeros((1, 4), np.float32), lib=lib)
+    assert out["accept_len"][0] == 3 and out["out_tokens"][0].tolist() == [1, 0, 2, 0]
+
+
+def check_invariants(lib):
+    """Identical target and draft logits accept every draft; after a rejection
+    with q(x_j) > 0 the bonus differs from x_j; outputs are well formed."""
+    rng = np.random.default_rng(31)
+    B, K, V = 400, 4, 50
+    zt = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    zd = zt[:, :K].copy()
+    temps = rng.choice(np.array([0.0, 0.5, 1.0], np.float32), B)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    tok[temps == 0] = np.argmax(zd[temps == 0], axis=2)
+    u = rng.random((B, K + 1), dtype=np.float32)
+    out = oracle.verify(zt, zd, tok, temps, u, lib=lib)
+    assert (out["accept_len"] == K).all()
+    assert (out["out_tokens"][:, :K] == tok).all()
+    zd = (zt[:, :K] + rng.standard_normal((B, K, V)) * 1.5).astype(np.float32)
+    out = oracle.verify(zt, zd, tok, temps, u, lib=lib)
+    n = out["accept_len"]
+    for b in range(B):
+        nb = n[b]
+        assert 0 <= nb <= K
+        assert (out["out_tokens"][b, :nb] == tok[b, :nb]).all()
+        assert 0 <= out["out_tokens"][b, nb] < V
+        assert (out["out_tokens"][b, nb + 1:] == -1).all()
+        if nb < K and out["q"][b, nb] > 0 and temps[b] > 0:
+            assert out["out_tokens"][b, nb] != tok[b, nb]
+    assert out["status"].max() & oracle.ROW_ERRORS == 0
+
+
+def check_bad_inputs(lib):
+    """Bad tokens, non-finite logits and bad temperatures flag the row and
+    leave accept length 0 with no tokens."""
+    K, V = 2, 6
+    zt = np.zeros((5, K + 1, V), np.float32)
+    zd = np.zeros((5, K, V), np.float32)
+    tok = np.zeros((5, K), np.int32)
+    temps = np.ones(5, np.float32)
+    tok[0, 1] = V
+    zt[1, 2, 3] = np.nan
+    zd[2, 0, 0] = np.inf
+    temps[3] = -1.0
+    zt[4, 1, :] = -np.inf
+    out = oracle.verify(zt, zd, tok, temps, np.full((5, K + 1), 0.5, np.float32), lib=lib)
+    assert out["status"].tolist() == [oracle.ROW_BAD_TOKEN, oracle.ROW_NONFINITE,
+                                      oracle.ROW_NONFINITE, oracle.ROW_BAD_TEMP,
+                                      oracle.ROW_NONFINITE]
+    assert (out["accept_len"] == 0).all() and (out["out_tokens"] == -1).all()
+
+
+def check_fallback_zero_residual(lib):
+    """A draft token with q = p = 0 is rejected and leaves a zero residual;
+    the bonus then falls back to p_n and the row is flagged."""
+    zt = np.array([[[0.0, 1.0, -np.inf, 0.5], [0, 0, 0, 0]]], np.float32)
+    zd = zt[:, :1].copy()
+    out = oracle.verify(zt, zd, np.array([[2]], np.int32), np.ones(1, np.float32),
+                        np.array([[0.3, 0.0]], np.float32), lib=lib)
+    assert out["accept_len"][0] == 0 and out["out_tokens"][0, 0] == 0
+    assert out["status"][0] & oracle.ROW_FALLBACK
+
+
+# ---------------------------------------------------------------------------
+# a4 outcome prediction, a5 hit
+
+def _bf16(x):
+    from speculative_decoding_verification_50_gb300.workloads import f32_to_bf16_bits
+    return f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+def check_predict_library_sort(lib):
+    """Keys = numpy lexsort by (logit desc, index asc) minus the sent token,
+    first F; bf16 rows with many ties exercise the index tie-break."""
+    rng = np.random.default_rng(41)
+    for dtype in ("fp32", "bf16"):
+        for (B, K, V, F) in ((3, 2, 7, 3), (4, 3, 300, 6), (2, 4, 1000, 32), (2, 1, 4, 6)):
+            z = rng.integers(-3, 4, (B, K + 1, V)).astype(np.float32) * 0.5
+            zz = _bf16(z) if dtype == "bf16" else z
+            tok = rng.integers(0, V, (B, K)).astype(np.int32)
+            out = oracle.predict(zz, tok, F, lib=lib)
+            for b in range(B):
+                for k in range(K + 1):
+                    idx = np.arange(V)
+                    if k < K:
+                        idx = idx[idx != tok[b, k]]
+                    order = idx[np.lexsort((idx, -z[b, k, idx]))][:F]
+                    want = np.full(F, -1, np.int32)
+                    want[:len(order)] = order
+                    assert out["keys"][b, k].tolist() == want.tolist(), (dtype, b, k)
+                    got_l = out["key_logits"][b, k][:len(order)]
+                    assert np.array_equal(got_l, z[b, k, order])
+
+
+def check_predict_exclusion(lib):
+    """[SSD] §4.1.1: the token sent for verification at lookahead k (< K) is
+    never a key there; at k = K nothing is excluded."""
+    V, K, F = 20, 3, 4
+    z = np.tile(np.arange(V, dtype=np.float32)[::-1], (1, K + 1, 1))  # token 0 best
+    tok = np.zeros((1, K), np.int32)
+    out = oracle.predict(z, tok, F, lib=lib)
+    for k in range(K):
+        assert out["keys"][0, k].tolist() == [1, 2, 3, 4]
+    assert out["keys"][0, K].tolist() == [0, 1, 2, 3]
+
+
+def check_hit_constructed(lib):
+    """[SSD] §3.1: hit iff t* is among the keys of the realised accept length."""
+    K, F = 3, 2
+    keys = np.array([[[10, 11], [20, 21], [30, 31], [40, 41]]] * 4, np.int32)
+    accept_len = np.array([0, 2, 3, 1], np.int32)
+    out_tokens = np.array([[11, -1, -1, -1], [5, 6, 30, -1], [1, 2, 3, 41], [7, 30, -1, -1]], np.int32)
+    hit = oracle.check_hit(keys, accept_len, out_tokens, lib=lib)
+    assert hit.tolist() == [1, 1, 1, 0]
+
+
+ALL_CHECKS = {
+    "softmax_library": check_softmax_library,
+    "thm1_overlap": check_thm1_overlap,
+    "exercise_1": check_exercise_1,
+    "section_2_3": check_section_2_3,
+    "exact_enumeration": check_exact_enumeration,
+    "exact_enumeration_T07": lambda lib: check_exact_enumeration(lib, seed=4, T=0.7, K=2),
+    "exact_enumeration_K3": lambda lib: check_exact_enumeration(lib, seed=9, V=4, K=3, pairs=2),
+    "expected_tokens": check_expected_tokens,
+    "wrong_method_a_is_biased": check_wrong_method_a_is_biased,
+    "greedy": check_greedy,
+    "invariants": check_invariants,
+    "bad_inputs": check_bad_inputs,
+    "fallback_zero_residual": check_fallback_zero_residual,
+    "predict_library_sort": check_predict_library_sort,
+    "predict_exclusion": check_predict_exclusion,
+    "hit_constructed": check_hit_constructed,
+}

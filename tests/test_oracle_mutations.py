@@ -1,0 +1,94 @@
+"""Negative controls: oracle builds with one planted mistake must fail the pins.
+
+Each mutation rewrites one line of a private copy of the oracle source (the
+committed oracle is never changed), builds it with gcc, and asserts that the
+listed pins reject it.  This shows the pins would catch a dropped term, a
+wrong sign, a wrong index or a transposed operand in the oracle.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_checks as oc
+
+MUTATIONS = {
+    # resample from p after a rejection (Lecture 5 §2.6, "wrong method A")
+    "wrong_method_a": (
+        "for (int v = 0; v < V; ++v) { r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0; R += r[v]; }",
+        "for (int v = 0; v < V; ++v) { r[v] = p[v]; R += r[v]; (void)q; }",
+        ["exact_enumeration", "wrong_method_a_is_biased", "chisq_0.3"]),
+    # residual max(q - p, 0), the garbled form on the survey blog
+    "swapped_residual": (
+        "r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;",
+        "r[v] = q[v] > p[v] ? q[v] - p[v] : 0.0;",
+        ["exact_enumeration"]),
+    "ratio_inverted": (
+        "accept = ratio >= (double)U[i];",
+        "accept = 1.0 / ratio >= (double)U[i];",
+        ["exercise_1", "exact_enumeration"]),
+    "accept_uses_bonus_uniform": (
+        "accept = ratio >= (double)U[i];",
+        "accept = ratio >= (double)U[K];",
+        ["exact_enumeration"]),
+    "cdf_off_by_one": (
+        "if (cum > tau) { tstar = v; break; }",
+        "if (cum > tau) { tstar = v > 0 ? v - 1 : v; break; }",
+        ["exact_enumeration", "section_2_3"]),
+    "temperature_ignored": (
+        "p[v] = exp((load_logit(base, dtype, off + v) - m) / T);",
+        "p[v] = exp(load_logit(base, dtype, off + v) - m);",
+        ["softmax_library", "exact_enumeration_T07"]),
+    "greedy_last_max": (
+        "if (z > m) { m = z; am = v; }",
+        "if (z >= m) { m = z; am = v; }",
+        ["greedy", "softmax_library"]),
+    "no_stop_at_first_rejection": (
+        "if (!accept) { n = i; break; }",
+        "if (!accept) { n = i; }",
+        ["exact_enumeration"]),
+    "bonus_from_wrong_row": (
+        "const double* p = pt + (int64_t)n * V;",
+        "const double* p = pt + (int64_t)(n > 0 ? n - 1 : 0) * V;",
+        ["exact_enumeration"]),
+    "overlap_uses_max": (
+        "a += (p[v] < q[v]) ? p[v] : q[v];",
+        "a += (p[v] > q[v]) ? p[v] : q[v];",
+        ["thm1_overlap", "exercise_1"]),
+    "predict_no_exclusion": (
+        "if (v == excl) continue;",
+        "(void)excl;",
+        ["predict_exclusion", "predict_library_sort"]),
+    "predict_tie_order": (
+        "return (x->v < y->v) ? -1 : (x->v > y->v);",
+        "return (x->v > y->v) ? -1 : (x->v < y->v);",
+        ["predict_library_sort"]),
+    "hit_wrong_length": (
+        "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
+        "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
+        ["hit_constructed"]),
+}
+
+
+def _check(name):
+    if name.startswith("chisq_"):
+        a = float(name.split("_")[1])
+        return lambda lib: oc.check_chisq(lib, a, draws=200_000)
+    return oc.ALL_CHECKS[name]
+
+
+@pytest.mark.parametrize("mut", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(tmp_path, mut):
+    old, new, checks = MUTATIONS[mut]
+    with open(oracle.SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation anchor for {mut} not unique"
+    path = os.path.join(tmp_path, "mutant.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    so = oracle.build(src=path, out=os.path.join(tmp_path, "libmutant.so"),
+                      openmp=False, force=True)
+    lib = oracle.load(so)
+    for name in checks:
+        with pytest.raises(AssertionError):
+            _check(name)(lib)
