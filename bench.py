@@ -1,0 +1,495 @@
+#!/usr/bin/env python3
+"""Throughput of the verification / outcome-prediction hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: specv_verify (row
+statistics, accept test, residual/bonus draw), specv_predict_outcomes (top-F
+keys at every lookahead) and specv_check_hit, all through the C ABI.
+
+Default workload "cfg5-ssd": B=256, K=8, V=152064, fp32 Zipf-like logits
+(config 5) with the draft logits at K+1 lookaheads so the step also predicts
+F=6 outcome keys per lookahead and checks the hit (the full SSD round).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling: batch
+rows r*B .. (r+1)*B-1 of one global batch); no collective touches the data
+path; the timed region is bracketed by barriers and the max over ranks is
+reported.  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from speculative_decoding_verification_50_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verify rows/s (B·(K+1) vocab rows) and achieved HBM GB/s vs GB300 peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "cfg5-ssd": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd", ssd=True, F=6),
+                 "config 5 (B=256, K=8, V=152064, fp32 Zipf-like logits) as a full SSD round: "
+                 "verify + top-6 outcome keys at K+1 lookaheads + hit check"),
+    "cfg5": (wl.SPECS["cfg5"], "config 5 (B=256, K=8, V=152064, fp32 Zipf-like logits), verify only"),
+    "cfg4": (wl.SPECS["cfg4"], "config 4 (B=32, K=4, V=128256, bf16, F=6): verify + predict + hit"),
+    "cfg3": (wl.SPECS["cfg3"], "config 3 (B=64, K=4, V=128256, bf16, T in {0,0.6,1}), verify only"),
+    "cfg2a": (wl.SPECS["cfg2a"], "config 2a (B=1, K=5, V=128256, bf16, greedy), verify only"),
+    "cfg2b": (wl.SPECS["cfg2b"], "config 2b (B=1, K=5, V=128256, bf16, T=0.7), verify only"),
+    "cfg1": (wl.SPECS["cfg1"], "config 1 (B=1, K=4, V=4096, fp32, T=1), verify only"),
+}
+
+VERIFY_SRC = os.path.join(ROOT, "speculative_decoding_verification_50_gb300", "csrc",
+                          "verify_kernels.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (also exercised by tests/test_bench_dist.py on gloo)
+
+def dist_env() -> tuple:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_rows(rank: int, world: int, B: int) -> list:
+    """Weak scaling: rank r owns rows r*B .. r*B+B-1 of a global batch."""
+    return list(range(rank * B, (rank + 1) * B))
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+
+def measured_peak() -> tuple:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("verify_kernels.cuh", "specv_common.cuh"):
+        with open(os.path.join(os.path.dirname(VERIFY_SRC), name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """ncu DRAM bytes per verify launch recorded for this kernel source, or None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0:
+            time.sleep(0.01)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        return "GPU-" + str(u)
+    except Exception:
+        return None
+
+
+def algorithmic_bytes(spec) -> dict:
+    s = spec.elem_bytes
+    verify = spec.B * (2 * spec.K + 1) * spec.V * s
+    predict = spec.B * (spec.K + 1) * spec.V * s if spec.F else 0
+    fused = spec.B * (2 * spec.K + 2) * spec.V * s if spec.F else verify
+    return dict(verify=verify, predict=predict, step_fused=fused)
+
+
+def time_oracle(data, spec, nthreads: int) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    o = oracle.verify(data["target"], data["draft"], data["tokens"], data["temperature"],
+                      data["uniforms"], nthreads=nthreads)
+    if spec.F:
+        p = oracle.predict(data["draft"], data["tokens"], spec.F, nthreads=nthreads)
+        oracle.check_hit(p["keys"], o["accept_len"], o["out_tokens"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(spec, budget_s: float = 12.0) -> dict:
+    """The oracle on a bounded sample of the workload, on this host's cores."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    rows = list(range(min(spec.B, max(1, cores))))
+    data = wl.generate(spec, rows=rows)
+    t = time_oracle(data, spec, cores)
+    per_row = t / len(rows)
+    n = int(min(spec.B, max(len(rows), budget_s / max(per_row, 1e-6))))
+    if n > len(rows):
+        data = wl.generate(spec, rows=list(range(n)))
+        t = time_oracle(data, spec, cores)
+    value = n * (spec.K + 1) / t
+    return {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {spec.B} batch rows of {spec.name} "
+                      f"({'verify+predict+hit' if spec.F else 'verify'}), fp64 C, OpenMP over rows, "
+                      f"{t:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+
+def run_ours(args) -> None:
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from speculative_decoding_verification_50_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_50_gb300 as sv
+    sv.load_library()
+
+    spec, desc = WORKLOADS[args.workload]
+    if args.batch:
+        spec = dataclasses.replace(spec, B=args.batch)
+        desc += f" [B overridden to {args.batch}]"
+    data = wl.generate(spec, rows=shard_rows(rank, world, spec.B))
+    B, K, V, F = spec.B, spec.K, spec.V, spec.F
+    is_bf16 = spec.dtype == wl.BF16
+
+    def host_logits(a):
+        t = torch.from_numpy(a)
+        return t.view(torch.bfloat16) if is_bf16 else t
+
+    h_target = host_logits(data["target"]).pin_memory()
+    h_draft = host_logits(data["draft"]).pin_memory()
+    h_tok = torch.from_numpy(data["tokens"]).pin_memory()
+    h_temp = torch.from_numpy(data["temperature"]).pin_memory()
+    h_unif = torch.from_numpy(data["uniforms"]).pin_memory()
+    d_target = h_target.to(dev)
+    d_draft = h_draft.to(dev)
+    d_tok, d_temp, d_unif = h_tok.to(dev), h_temp.to(dev), h_unif.to(dev)
+
+    i32 = dict(dtype=torch.int32, device=dev)
+    outs = dict(accept_len=torch.empty(B, **i32), out_tokens=torch.empty((B, K + 1), **i32),
+                p_draft=torch.empty((B, K), dtype=torch.float32, device=dev),
+                q_draft=torch.empty((B, K), dtype=torch.float32, device=dev),
+                row_status=torch.empty(B, **i32))
+    lib = sv.load_library()
+    code = sv.SPECV_BF16 if is_bf16 else sv.SPECV_FP32
+    ws_v = torch.empty(max(1, lib.specv_verify_workspace_bytes(B, K, V, code)), dtype=torch.uint8, device=dev)
+    if F:
+        keys = torch.empty((B, K + 1, F), **i32)
+        key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
+        pstat = torch.empty(B, **i32)
+        ws_p = torch.empty(max(1, lib.specv_predict_workspace_bytes(B, K, V, F, code)), dtype=torch.uint8, device=dev)
+        hit = torch.empty(B, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches = [0]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sv.specv_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
+        launches[0] += sv.last_launch_count()
+        if ev is not None:
+            ev[1].record(stream)
+        if F:
+            sv.specv_predict_outcomes(d_draft, d_tok, F, keys=keys, key_logits=key_logits,
+                                      row_status=pstat, workspace=ws_p)
+            launches[0] += sv.last_launch_count()
+            sv.specv_check_hit(keys, outs["accept_len"], outs["out_tokens"], hit=hit)
+            launches[0] += sv.last_launch_count()
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches[0] = 0
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    gpu_launches = launches[0]
+    total_ms = t_start.elapsed_time(t_end)
+    verify_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    rest_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ms_step = reduce_max(total_ms, world, dev) / args.steps
+    rows_total = reduce_sum(float(B * (K + 1)), world, dev)
+    value = rows_total / (ms_step / 1e3)
+
+    # end to end: host inputs in pinned memory, copies inside the timed region
+    e2e_steps = max(2, min(args.steps, 10))
+    h_n = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_ot = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_keys = torch.empty((B, K + 1, F), dtype=torch.int32).pin_memory() if F else None
+    h_hit = torch.empty(B, dtype=torch.uint8).pin_memory() if F else None
+
+    def e2e_step():
+        d_target.copy_(h_target, non_blocking=True)
+        d_draft.copy_(h_draft, non_blocking=True)
+        d_tok.copy_(h_tok, non_blocking=True)
+        d_temp.copy_(h_temp, non_blocking=True)
+        d_unif.copy_(h_unif, non_blocking=True)
+        step()
+        h_n.copy_(outs["accept_len"], non_blocking=True)
+        h_ot.copy_(outs["out_tokens"], non_blocking=True)
+        if F:
+            h_keys.copy_(keys, non_blocking=True)
+            h_hit.copy_(hit, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (h_target, h_draft, h_tok, h_temp, h_unif))
+    d2h = h_n.numel() * 4 + h_ot.numel() * 4 + ((h_keys.numel() * 4 + h_hit.numel()) if F else 0)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    ab = algorithmic_bytes(spec)
+    v_ms = statistics.mean(verify_ms)
+    achieved = ab["verify"] / (v_ms / 1e3) / 1e9
+    step_gbs = ab["step_fused"] / (ms_step / 1e3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    in_bytes = d_target.numel() * d_target.element_size() + d_draft.numel() * d_draft.element_size()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; see workloads.py)",
+        "config": {
+            "workload": f"{args.workload}: {desc}",
+            "B_per_gpu": B, "K": K, "V": V, "logits": spec.dtype, "F": F,
+            "rows_per_step_per_gpu": B * (K + 1),
+            "l2": (f"inputs {in_bytes / 1e9:.2f} GB > {L2_BYTES / 2**20:.0f} MiB L2, no flush"
+                   if in_bytes > L2_BYTES else "inputs fit in L2: numbers are L2-hot"),
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "verify_units_kernel (+ finalize) per specv_verify call",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_kind": f"of {peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "of fallback",
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": ab["verify"],
+            "avg_launch_ms": round(v_ms, 5),
+        },
+        "step_hbm": {"algorithmic_bytes": ab["step_fused"], "achieved_gbs": round(step_gbs, 1),
+                     "frac": round(step_gbs / peak, 4),
+                     "verify_ms": round(v_ms, 5), "predict_hit_ms": round(statistics.mean(rest_ms), 5)},
+        "e2e": {"value": round(rows_total / (e2e_ms / 1e3), 1), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args) -> None:
+    """The oracle (CPU, fp64) as the reference arm, on a bounded sample."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    spec, desc = WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
+    probe = wl.generate(spec, rows=[0])
+    t_row = time_oracle(probe, spec, 1)
+    # whole run (warm-up + timed) within about a minute
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(spec.B, per_step / max(t_row, 1e-6) * min(cores, 8))))
+    data = wl.generate(spec, rows=list(range(n)))
+    for _ in range(args.warmup):
+        time_oracle(data, spec, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(data, spec, cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n * (spec.K + 1) / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; see workloads.py)",
+        "config": {"workload": f"{args.workload}: {desc}", "B_per_gpu": spec.B, "K": spec.K,
+                   "V": spec.V, "logits": spec.dtype, "F": spec.F,
+                   "sample_rows_per_step": n},
+        "cpu_baseline": {"value": round(value, 2), "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {spec.B} batch rows per step, fp64 C oracle, OpenMP"},
+        "e2e": {"value": round(value, 2), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cfg5-ssd", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override B (smaller cases for profiling captures)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

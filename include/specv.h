@@ -1,0 +1,168 @@
+/*
+ * specv.h -- C ABI of the GB300 (sm_103a) speculative-sampling verification
+ * and SSD outcome-prediction library (libspecv.so).
+ *
+ * Sources (page title -- section):
+ *   "Speculative Speculative Decoding" (Kumar, Dao, May): §2.1 (accept test,
+ *     residual r ∝ max(p_target - p_draft, 0), bonus token, verification
+ *     outcome v_T = (k, t*)), §3.1 Algorithm 1 and the cache hit/miss
+ *     definition, §4.1.1 (Saguaro outcome prediction: top-F_k draft tokens per
+ *     lookahead k, excluding the token sent for verification there).
+ *   "Speculative Decoding" (dl-note): §2.2-§2.3 (accept probability, residual
+ *     distribution), Appendix (vLLM argument layout: one uniform per draft
+ *     token, output [B, K+1], draft probability 0 rejects).
+ *   "Lecture 5 - Speculative Decoding and SpecInfer": §2.1 (greedy and
+ *     temperature sampling as adjusted distributions), §2.2 (accept iff
+ *     u <= p(x)/q(x)), §2.7 (greedy special case), §3.1 (one iteration).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller
+ *     allocates and owns every buffer, including the workspace.  The library
+ *     never allocates, frees or synchronises: work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*, NULL = legacy default stream) and the
+ *     outputs are valid once the caller has synchronised that stream.
+ *   - Logits are bf16 (raw 16-bit patterns) or fp32, rows contiguous along
+ *     the vocabulary.  Row (b, i) starts at element b*batch_stride +
+ *     i*row_stride of its tensor; strides are in elements and must be >= V
+ *     (row_stride) and >= rows*row_stride (batch_stride).  A 16-byte aligned
+ *     base and strides whose byte size is a multiple of 16 select the
+ *     vectorised path; any other layout is accepted and read element-wise.
+ *   - Argument errors are detected on the host, before any launch, and
+ *     return SPECV_ERR_INVALID_ARG (nothing is written).  A failed launch
+ *     returns SPECV_ERR_CUDA.  Data errors never trap: they are reported per
+ *     batch row in the optional row_status output (bits below), and a
+ *     flagged row gets accept length 0, tokens -1, and -1 keys.
+ *   - Limits: 1 <= K <= 32, 1 <= V < 2^31, 0 <= B, 1 <= F <= 32.
+ */
+#ifndef SPECV_H
+#define SPECV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPECV_OK = 0,
+  SPECV_ERR_INVALID_ARG = 1, /* bad pointer, size, stride or dtype */
+  SPECV_ERR_UNSUPPORTED = 2, /* valid but outside what this build handles */
+  SPECV_ERR_CUDA = 3,        /* a CUDA launch or attribute call failed */
+  SPECV_ERR_WORKSPACE = 4    /* workspace NULL or smaller than required */
+} specv_status;
+
+typedef enum { SPECV_BF16 = 0, SPECV_FP32 = 1 } specv_dtype;
+
+/* Per-batch-row status bits (row_status outputs). */
+#define SPECV_ROW_BAD_TOKEN 1 /* a draft token outside [0, V) */
+#define SPECV_ROW_NONFINITE 2 /* a NaN or +inf logit, or a row of all -inf */
+#define SPECV_ROW_BAD_TEMP 4  /* temperature < 0, NaN or inf */
+#define SPECV_ROW_FALLBACK 8  /* informational: the bonus draw fell back
+                                 (zero residual mass -> drawn from p_n; or
+                                 rounding left no index -> last v with r>0) */
+
+/*
+ * Verification of B independent batch rows ("Speculative Speculative
+ * Decoding" §2.1; "Lecture 5" §3.1).
+ *
+ * For batch row b with temperature T = temperature[b] (same T for target and
+ * draft; T = 0 is greedy):
+ *   p_i = softmax(target row i / T), i in [0, K]     (one-hot argmax if T=0,
+ *   q_i = softmax(draft row i / T),  i in [0, K)      ties -> lowest index)
+ *   accept length n = the first i with NOT( q_i(x_i) > 0 and
+ *       p_i(x_i) / q_i(x_i) >= uniforms[b, i] ), or K if there is none
+ *       (greedy rows: accept iff x_i is the argmax of both rows i);
+ *   bonus t* = the smallest v whose running sum of r in index order exceeds
+ *       uniforms[b, K] * sum(r), where r = max(p_n - q_n, 0) if n < K and
+ *       r = p_K if n = K (greedy rows: argmax of p_n).
+ * Outputs: accept_len[b] = n; out_tokens[b, 0..K] = x_1..x_n, t*, then -1;
+ *   optional p_draft[b, i] = p_i(x_i), q_draft[b, i] = q_i(x_i) for every
+ *   i < K (fp32); optional row_status[b].
+ */
+typedef struct {
+  int32_t B, K, V;
+  int32_t dtype;                  /* specv_dtype */
+  const void* target_logits;      /* K+1 rows per batch row */
+  int64_t target_batch_stride;    /* elements */
+  int64_t target_row_stride;      /* elements */
+  const void* draft_logits;       /* K rows per batch row (a [B, K+1, V]
+                                     SSD tensor is accepted: row K unused) */
+  int64_t draft_batch_stride;
+  int64_t draft_row_stride;
+  const int32_t* draft_tokens;    /* [B, K] x_1..x_K */
+  const float* temperature;       /* [B] */
+  const float* uniforms;          /* [B, K+1] in [0,1): columns 0..K-1 drive
+                                     the accept tests, column K the bonus */
+  int32_t* accept_len;            /* OUT [B] */
+  int32_t* out_tokens;            /* OUT [B, K+1] */
+  float* p_draft;                 /* OUT, optional (NULL) [B, K] */
+  float* q_draft;                 /* OUT, optional (NULL) [B, K] */
+  int32_t* row_status;            /* OUT, optional (NULL) [B] */
+} specv_verify_args;
+
+/* Bytes of device workspace specv_verify needs for these sizes (0 if B=0). */
+size_t specv_verify_workspace_bytes(int32_t B, int32_t K, int32_t V,
+                                    int32_t dtype);
+
+/* Enqueue verification.  workspace: device memory of at least
+ * specv_verify_workspace_bytes(...) bytes, 256-byte aligned, owned by the
+ * caller, not shared with a concurrently running call. */
+specv_status specv_verify(const specv_verify_args* args, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * SSD outcome prediction ("Speculative Speculative Decoding" §4.1.1).
+ * For every batch row b and lookahead k in [0, K]: keys[b, k, 0..F-1] are the
+ * F largest logits of draft row k, ordered by (logit descending, index
+ * ascending), with the draft token x_{k+1} = draft_tokens[b, k] removed for
+ * k < K (it was sent for verification and cannot be the bonus); nothing is
+ * removed at k = K.  Fewer than F candidates pad with -1.  The ranking is the
+ * same for every temperature > 0 and for greedy, so no temperature is taken.
+ */
+typedef struct {
+  int32_t B, K, V, F;
+  int32_t dtype;
+  const void* draft_logits;       /* K+1 rows per batch row */
+  int64_t draft_batch_stride;
+  int64_t draft_row_stride;
+  const int32_t* draft_tokens;    /* [B, K] */
+  int32_t* keys;                  /* OUT [B, K+1, F] */
+  float* key_logits;              /* OUT, optional [B, K+1, F] (-inf pad) */
+  int32_t* row_status;            /* OUT, optional [B] */
+} specv_predict_args;
+
+size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V,
+                                     int32_t F, int32_t dtype);
+specv_status specv_predict_outcomes(const specv_predict_args* args,
+                                    void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
+ * Cache-hit check ("Speculative Speculative Decoding" §3.1: hit iff the
+ * realised outcome (k, t*) is in the speculation cache).  hit[b] = 1 iff
+ * 0 <= n <= K for n = accept_len[b] and out_tokens[b, n] is one of
+ * keys[b, n, 0..F-1]; otherwise 0.  keys [B, K+1, F], accept_len [B],
+ * out_tokens [B, K+1], hit [B] (uint8), all device pointers.
+ */
+specv_status specv_check_hit(int32_t B, int32_t K, int32_t F,
+                             const int32_t* keys, const int32_t* accept_len,
+                             const int32_t* out_tokens, uint8_t* hit,
+                             void* stream);
+
+/* Static description of a status code. */
+const char* specv_status_string(specv_status s);
+
+/* Message describing the most recent error on the calling host thread
+ * ("" if none).  The string stays valid until that thread's next call. */
+const char* specv_last_error(void);
+
+/* Number of kernel launches the most recent successful call on this host
+ * thread enqueued (for launch accounting in benchmarks). */
+int32_t specv_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECV_H */

@@ -1,0 +1,202 @@
+"""GB300 (sm_103a) speculative-sampling verification and SSD outcome prediction.
+
+Thin Python binding over the C ABI of ``libspecv.so`` (declared in
+``include/specv.h``): it marshals torch tensors into pointers, sizes and
+strides and passes the current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels; there is no Python or CPU fallback, and a
+missing library raises.
+
+Entry points (same names as the C ABI):
+  specv_verify(target, draft, draft_tokens, temperature, uniforms, ...)
+  specv_predict_outcomes(draft, draft_tokens, F, ...)
+  specv_check_hit(keys, accept_len, out_tokens, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import workloads  # noqa: F401  (seeded inputs; no method arithmetic)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecv.so")
+
+SPECV_OK, SPECV_ERR_INVALID_ARG, SPECV_ERR_UNSUPPORTED, SPECV_ERR_CUDA, SPECV_ERR_WORKSPACE = range(5)
+SPECV_BF16, SPECV_FP32 = 0, 1
+ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK = 1, 2, 4, 8
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+
+class VerifyArgs(ctypes.Structure):
+    _fields_ = [("B", _I32), ("K", _I32), ("V", _I32), ("dtype", _I32),
+                ("target_logits", _P), ("target_batch_stride", _I64), ("target_row_stride", _I64),
+                ("draft_logits", _P), ("draft_batch_stride", _I64), ("draft_row_stride", _I64),
+                ("draft_tokens", _P), ("temperature", _P), ("uniforms", _P),
+                ("accept_len", _P), ("out_tokens", _P), ("p_draft", _P), ("q_draft", _P),
+                ("row_status", _P)]
+
+
+class PredictArgs(ctypes.Structure):
+    _fields_ = [("B", _I32), ("K", _I32), ("V", _I32), ("F", _I32), ("dtype", _I32),
+                ("draft_logits", _P), ("draft_batch_stride", _I64), ("draft_row_stride", _I64),
+                ("draft_tokens", _P), ("keys", _P), ("key_logits", _P), ("row_status", _P)]
+
+
+class SpecvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"specv status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libspecv.so (built by __graft_entry__.build()); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    lib.specv_verify_workspace_bytes.restype = ctypes.c_size_t
+    lib.specv_verify_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
+    lib.specv_verify.restype = ctypes.c_int
+    lib.specv_verify.argtypes = [ctypes.POINTER(VerifyArgs), _P, ctypes.c_size_t, _P]
+    lib.specv_predict_workspace_bytes.restype = ctypes.c_size_t
+    lib.specv_predict_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
+    lib.specv_predict_outcomes.restype = ctypes.c_int
+    lib.specv_predict_outcomes.argtypes = [ctypes.POINTER(PredictArgs), _P, ctypes.c_size_t, _P]
+    lib.specv_check_hit.restype = ctypes.c_int
+    lib.specv_check_hit.argtypes = [_I32, _I32, _I32, _P, _P, _P, _P, _P]
+    lib.specv_status_string.restype = ctypes.c_char_p
+    lib.specv_status_string.argtypes = [ctypes.c_int]
+    lib.specv_last_error.restype = ctypes.c_char_p
+    lib.specv_last_error.argtypes = []
+    lib.specv_last_launch_count.restype = _I32
+    lib.specv_last_launch_count.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(rc: int) -> None:
+    if rc != SPECV_OK:
+        lib = load_library()
+        raise SpecvError(rc, lib.specv_last_error().decode() or lib.specv_status_string(rc).decode())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SPECV_BF16
+    if t.dtype == torch.float32:
+        return SPECV_FP32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def last_launch_count() -> int:
+    """Kernel launches enqueued by the most recent call on this thread."""
+    return int(load_library().specv_last_launch_count())
+
+
+def specv_verify(target, draft, draft_tokens, temperature, uniforms, *, accept_len=None,
+                 out_tokens=None, p_draft=None, q_draft=None, row_status=None,
+                 workspace=None, stream=None) -> dict:
+    """Verify B batch rows on the GPU (see include/specv.h, specv_verify).
+
+    target [B, >=K+1, V], draft [B, >=K, V] (bf16 or fp32, CUDA, last dim
+    contiguous); draft_tokens int32 [B, K]; temperature fp32 [B]; uniforms
+    fp32 [B, K+1].  Outputs are allocated when not given.  Returns a dict
+    with accept_len, out_tokens, p_draft, q_draft, row_status.
+    """
+    import torch
+    lib = load_library()
+    B, K = draft_tokens.shape
+    V = target.shape[-1]
+    assert target.dim() == 3 and draft.dim() == 3 and target.shape[0] == B and draft.shape[0] == B
+    assert target.shape[1] >= K + 1 and draft.shape[1] >= K and draft.shape[-1] == V
+    assert target.stride(-1) == 1 and draft.stride(-1) == 1
+    assert target.dtype == draft.dtype
+    assert uniforms.shape == (B, K + 1) and temperature.shape == (B,)
+    dev = target.device
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if p_draft is None:
+        p_draft = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if q_draft is None:
+        q_draft = torch.empty((B, K), dtype=torch.float32, device=dev)
+    if row_status is None:
+        row_status = torch.empty(B, dtype=torch.int32, device=dev)
+    code = _dtype_code(target)
+    need = lib.specv_verify_workspace_bytes(B, K, V, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    args = VerifyArgs(B, K, V, code,
+                      target.data_ptr(), target.stride(0), target.stride(1),
+                      draft.data_ptr(), draft.stride(0), draft.stride(1),
+                      draft_tokens.data_ptr(), temperature.data_ptr(), uniforms.data_ptr(),
+                      accept_len.data_ptr(), out_tokens.data_ptr(),
+                      p_draft.data_ptr(), q_draft.data_ptr(), row_status.data_ptr())
+    _check(lib.specv_verify(ctypes.byref(args), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dict(accept_len=accept_len, out_tokens=out_tokens, p_draft=p_draft,
+                q_draft=q_draft, row_status=row_status)
+
+
+def specv_predict_outcomes(draft, draft_tokens, F: int, *, keys=None, key_logits=None,
+                           row_status=None, workspace=None, stream=None) -> dict:
+    """Top-F outcome keys per lookahead (see include/specv.h).
+
+    draft [B, >=K+1, V] (bf16 or fp32, CUDA); draft_tokens int32 [B, K].
+    Returns keys int32 [B, K+1, F], key_logits fp32, row_status int32 [B].
+    """
+    import torch
+    lib = load_library()
+    B, K = draft_tokens.shape
+    V = draft.shape[-1]
+    assert draft.dim() == 3 and draft.shape[0] == B and draft.shape[1] >= K + 1
+    assert draft.stride(-1) == 1
+    dev = draft.device
+    if keys is None:
+        keys = torch.empty((B, K + 1, F), dtype=torch.int32, device=dev)
+    if key_logits is None:
+        key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
+    if row_status is None:
+        row_status = torch.empty(B, dtype=torch.int32, device=dev)
+    code = _dtype_code(draft)
+    need = lib.specv_predict_workspace_bytes(B, K, V, F, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    args = PredictArgs(B, K, V, F, code, draft.data_ptr(), draft.stride(0), draft.stride(1),
+                       draft_tokens.data_ptr(), keys.data_ptr(), key_logits.data_ptr(),
+                       row_status.data_ptr())
+    _check(lib.specv_predict_outcomes(ctypes.byref(args), _ptr(workspace), workspace.numel(),
+                                      _stream(stream)))
+    return dict(keys=keys, key_logits=key_logits, row_status=row_status)
+
+
+def specv_check_hit(keys, accept_len, out_tokens, *, hit=None, stream=None):
+    """hit[b] = out_tokens[b, n_b] in keys[b, n_b, :] (uint8 [B])."""
+    import torch
+    lib = load_library()
+    B, K1, F = keys.shape
+    assert accept_len.shape == (B,) and out_tokens.shape == (B, K1)
+    if hit is None:
+        hit = torch.empty(B, dtype=torch.uint8, device=keys.device)
+    _check(lib.specv_check_hit(B, K1 - 1, F, _ptr(keys), _ptr(accept_len), _ptr(out_tokens),
+                               _ptr(hit), _stream(stream)))
+    return hit

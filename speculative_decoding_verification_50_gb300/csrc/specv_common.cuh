@@ -1,0 +1,124 @@
+// Device helpers shared by the verification and outcome-prediction kernels.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace specv {
+
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// Row-status bits (meaning fixed by the C ABI header).
+enum : int32_t {
+  kBadToken = 1,
+  kNonFinite = 2,
+  kBadTemp = 4,
+  kFallback = 8,
+  kErrors = kBadToken | kNonFinite | kBadTemp
+};
+
+constexpr float kNegMax = -3.402823466e+38f;  // lowest finite float
+
+__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// 2^x on the SFU (PTX ex2.approx.ftz.f32): 2^-inf = 0, NaN propagates.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Element traits: DT 0 = bf16 (raw 16-bit patterns), 1 = fp32.  A "vector"
+// is 16 bytes: 8 bf16 or 4 fp32 logits.
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<0> {
+  static constexpr int VW = 8;
+  static constexpr int ES = 2;
+  using Vec = uint4;
+  __device__ static float scalar(const void* row, int64_t v) {
+    unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + v);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  __device__ static Vec vec(const void* row, int64_t v) {  // v multiple of 8
+    return __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(row) + v * ES));
+  }
+  __device__ static void unpack(const Vec& w, float (&z)[VW]) {
+    z[0] = __uint_as_float(w.x << 16);
+    z[1] = __uint_as_float(w.x & 0xffff0000u);
+    z[2] = __uint_as_float(w.y << 16);
+    z[3] = __uint_as_float(w.y & 0xffff0000u);
+    z[4] = __uint_as_float(w.z << 16);
+    z[5] = __uint_as_float(w.z & 0xffff0000u);
+    z[6] = __uint_as_float(w.w << 16);
+    z[7] = __uint_as_float(w.w & 0xffff0000u);
+  }
+  // Vector with elements [v, v+VW) clipped to [.., vend); missing -> -inf.
+  __device__ static Vec gather(const void* row, int64_t v, int64_t vend) {
+    uint32_t h[VW];
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      h[k] = (v + k < vend)
+                 ? static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + v + k))
+                 : 0xff80u;
+    }
+    Vec w;
+    w.x = h[0] | (h[1] << 16);
+    w.y = h[2] | (h[3] << 16);
+    w.z = h[4] | (h[5] << 16);
+    w.w = h[6] | (h[7] << 16);
+    return w;
+  }
+};
+
+template <>
+struct Elem<1> {
+  static constexpr int VW = 4;
+  static constexpr int ES = 4;
+  using Vec = float4;
+  __device__ static float scalar(const void* row, int64_t v) {
+    return __ldg(reinterpret_cast<const float*>(row) + v);
+  }
+  __device__ static Vec vec(const void* row, int64_t v) {
+    return __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const char*>(row) + v * ES));
+  }
+  __device__ static void unpack(const Vec& w, float (&z)[VW]) {
+    z[0] = w.x;
+    z[1] = w.y;
+    z[2] = w.z;
+    z[3] = w.w;
+  }
+  __device__ static Vec gather(const void* row, int64_t v, int64_t vend) {
+    float z[VW];
+#pragma unroll
+    for (int k = 0; k < VW; ++k)
+      z[k] = (v + k < vend) ? __ldg(reinterpret_cast<const float*>(row) + v + k) : neg_inf();
+    return make_float4(z[0], z[1], z[2], z[3]);
+  }
+};
+
+// Load vector j of the slice [v0, v1) of `row`: elements v0 + j*VW .. +VW-1,
+// -inf beyond v1.  VEC: the row base and v0 are 16-byte aligned.
+template <int DT, bool VEC>
+__device__ __forceinline__ typename Elem<DT>::Vec load_vec(const void* row, int64_t v0,
+                                                           int64_t v1, int j) {
+  using E = Elem<DT>;
+  const int64_t v = v0 + static_cast<int64_t>(j) * E::VW;
+  if (VEC && v + E::VW <= v1) return E::vec(row, v);
+  return E::gather(row, v, v1);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  return x;  // lane 0 holds the sum
+}
+
+}  // namespace specv

@@ -1,0 +1,128 @@
+"""C-ABI library: loads, exports every declared symbol, validates on the host.
+
+No test here launches a kernel: every call is rejected by host-side argument
+checks before any CUDA call, so these run without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_50_gb300 as sv
+from speculative_decoding_verification_50_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(specv_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("specv_verify", "specv_predict_outcomes", "specv_check_hit"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.specv_status_string(code)
+    assert lib.specv_status_string(99) == b"unknown status"
+
+
+def _args(**kw):
+    a = sv.VerifyArgs()
+    a.B, a.K, a.V, a.dtype = 2, 3, 100, sv.SPECV_FP32
+    for f in ("target_logits", "draft_logits", "draft_tokens", "temperature", "uniforms",
+              "accept_len", "out_tokens"):
+        setattr(a, f, 0x10000)
+    a.target_batch_stride, a.target_row_stride = 400, 100
+    a.draft_batch_stride, a.draft_row_stride = 300, 100
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), sv.SPECV_ERR_INVALID_ARG),
+    (dict(K=33), sv.SPECV_ERR_INVALID_ARG),
+    (dict(V=0), sv.SPECV_ERR_INVALID_ARG),
+    (dict(B=-1), sv.SPECV_ERR_INVALID_ARG),
+    (dict(dtype=7), sv.SPECV_ERR_INVALID_ARG),
+    (dict(target_logits=None), sv.SPECV_ERR_INVALID_ARG),
+    (dict(uniforms=None), sv.SPECV_ERR_INVALID_ARG),
+    (dict(target_row_stride=99), sv.SPECV_ERR_INVALID_ARG),
+    (dict(target_batch_stride=399), sv.SPECV_ERR_INVALID_ARG),
+    (dict(draft_batch_stride=299), sv.SPECV_ERR_INVALID_ARG),
+    (dict(draft_tokens=0x10002), sv.SPECV_ERR_INVALID_ARG),
+])
+def test_verify_rejects_bad_arguments(lib, kw, code):
+    a = _args(**kw)
+    rc = lib.specv_verify(ctypes.byref(a), ctypes.c_void_p(0x100000), 1 << 20, None)
+    assert rc == code
+    assert lib.specv_last_error()
+
+
+def test_verify_null_args(lib):
+    assert lib.specv_verify(None, None, 0, None) == sv.SPECV_ERR_INVALID_ARG
+
+
+def test_verify_workspace_checks(lib):
+    a = _args()
+    need = lib.specv_verify_workspace_bytes(2, 3, 100, sv.SPECV_FP32)
+    assert need >= 2 * 4 * 32 and need % 256 == 0
+    assert lib.specv_verify(ctypes.byref(a), None, need, None) == sv.SPECV_ERR_WORKSPACE
+    assert lib.specv_verify(ctypes.byref(a), ctypes.c_void_p(0x100000), need - 1, None) == sv.SPECV_ERR_WORKSPACE
+    assert lib.specv_verify(ctypes.byref(a), ctypes.c_void_p(0x100010), need, None) == sv.SPECV_ERR_WORKSPACE
+
+
+def test_empty_batch_is_a_no_op(lib):
+    a = _args(B=0, target_logits=None)
+    assert lib.specv_verify(ctypes.byref(a), None, 0, None) == sv.SPECV_OK
+    assert lib.specv_last_launch_count() == 0
+    assert lib.specv_verify_workspace_bytes(0, 3, 100, 1) == 0
+
+
+def test_predict_rejects_bad_arguments(lib):
+    p = sv.PredictArgs(2, 3, 100, 6, sv.SPECV_BF16, 0x10000, 400, 100, 0x10000, 0x10000, 0, 0)
+    for field, val in (("F", 0), ("F", 33), ("K", 0), ("V", 0), ("dtype", 5),
+                       ("keys", None), ("draft_batch_stride", 399), ("draft_row_stride", 50)):
+        q = sv.PredictArgs.from_buffer_copy(p)
+        setattr(q, field, val)
+        assert lib.specv_predict_outcomes(ctypes.byref(q), None, 0, None) == sv.SPECV_ERR_INVALID_ARG, field
+    q = sv.PredictArgs.from_buffer_copy(p)
+    q.row_status = 0x10000
+    assert lib.specv_predict_outcomes(ctypes.byref(q), None, 0, None) == sv.SPECV_ERR_WORKSPACE
+
+
+def test_check_hit_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p(0x10000)
+    assert lib.specv_check_hit(2, 0, 6, P, P, P, P, None) == sv.SPECV_ERR_INVALID_ARG
+    assert lib.specv_check_hit(2, 3, 0, P, P, P, P, None) == sv.SPECV_ERR_INVALID_ARG
+    assert lib.specv_check_hit(2, 3, 6, None, P, P, P, None) == sv.SPECV_ERR_INVALID_ARG
+    assert lib.specv_check_hit(0, 3, 6, None, None, None, None, None) == sv.SPECV_OK
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_50_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "specv_oracle" not in text, f

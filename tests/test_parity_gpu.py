@@ -1,0 +1,322 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Bars (from the method's statement of parity):
+  - accept lengths and tokens bit-exact, except rows the oracle flags as
+    boundary cases (a uniform within 1e-6 of a ratio or CDF boundary), which
+    are counted and reported;
+  - greedy rows exact; outcome keys and hit flags exact;
+  - p_i(x_i), q_i(x_i) within 1e-5 absolute (fp32 against fp64);
+  - row-status error bits exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_verification_50_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+PROB_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def sv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_verification_50_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_50_gb300 as m
+    m.load_library()
+    return m
+
+
+@pytest.fixture(scope="module")
+def olib():
+    return oracle.load(oracle.build())
+
+
+def to_dev(a, dtype_name):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype_name == wl.BF16 and t.dtype == torch.int16:
+        t = t.view(torch.bfloat16)
+    return t.cuda()
+
+
+def gpu_verify(sv, data, target=None, draft=None):
+    spec = data["spec"]
+    tgt = to_dev(data["target"], spec.dtype) if target is None else target
+    dft = to_dev(data["draft"], spec.dtype) if draft is None else draft
+    out = sv.specv_verify(tgt, dft, to_dev(data["tokens"], None),
+                          to_dev(data["temperature"], None), to_dev(data["uniforms"], None))
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def compare_verify(g, o, temps, label=""):
+    """Assert the parity bars; return the number of boundary rows."""
+    err = o["status"] & oracle.ROW_ERRORS
+    assert np.array_equal(g["row_status"] & oracle.ROW_ERRORS, err), label
+    bnd = o["boundary"].astype(bool)
+    ok = ~bnd
+    assert not (bnd & (temps == 0)).any(), "greedy rows are never boundary cases"
+    mism = ok & ((g["accept_len"] != o["accept_len"]) |
+                 (g["out_tokens"] != o["out_tokens"]).any(axis=1))
+    if mism.any():
+        b = int(np.argmax(mism))
+        raise AssertionError(
+            f"{label}: {int(mism.sum())} non-boundary rows differ; first b={b}: "
+            f"gpu n={g['accept_len'][b]} toks={g['out_tokens'][b]} | oracle n={o['accept_len'][b]} "
+            f"toks={o['out_tokens'][b]} T={temps[b]}")
+    fb = ok & (err == 0)
+    assert np.array_equal(g["row_status"][fb] & oracle.ROW_FALLBACK,
+                          o["status"][fb] & oracle.ROW_FALLBACK), label
+    good = err == 0
+    dp = np.abs(g["p_draft"][good] - o["p"][good]).max(initial=0.0)
+    dq = np.abs(g["q_draft"][good] - o["q"][good]).max(initial=0.0)
+    assert dp <= PROB_TOL and dq <= PROB_TOL, (label, dp, dq)
+    same = (g["accept_len"] == o["accept_len"]) & (g["out_tokens"] == o["out_tokens"]).all(axis=1)
+    print(f"[{label}] boundary rows {int(bnd.sum())}/{len(bnd)} (of which identical anyway: "
+          f"{int((bnd & same).sum())}); max |dp| {dp:.2e} |dq| {dq:.2e}")
+    return int(bnd.sum())
+
+
+def oracle_verify(olib, data):
+    return oracle.verify(data["target"], data["draft"], data["tokens"], data["temperature"],
+                         data["uniforms"], nthreads=0, lib=olib)
+
+
+@pytest.mark.parametrize("name", ["cfg1", "cfg2a", "cfg2b", "cfg3"])
+def test_verify_configs(sv, olib, name):
+    data = wl.generate(wl.SPECS[name])
+    g = gpu_verify(sv, data)
+    o = oracle_verify(olib, data)
+    nb = compare_verify(g, o, data["temperature"], name)
+    print(f"{name}: boundary rows {nb}/{len(o['boundary'])}, mean accept "
+          f"{o['accept_len'].mean():.3f}")
+    assert nb <= max(1, len(o["boundary"]) // 50)
+
+
+def test_ssd_round_cfg4(sv, olib):
+    """Config 4: verify on the SSD draft layout [B, K+1, V], predict F=6 keys
+    at every lookahead, hit check against the realised outcome."""
+    spec = wl.SPECS["cfg4"]
+    data = wl.generate(spec)
+    tgt = to_dev(data["target"], spec.dtype)
+    dft = to_dev(data["draft"], spec.dtype)
+    assert dft.shape[1] == spec.K + 1
+    g = gpu_verify(sv, data, tgt, dft)
+    o = oracle_verify(olib, data)
+    compare_verify(g, o, data["temperature"], "cfg4")
+    tok = to_dev(data["tokens"], None)
+    pr = sv.specv_predict_outcomes(dft, tok, spec.F)
+    hit = sv.specv_check_hit(pr["keys"], to_dev(g["accept_len"], None), to_dev(g["out_tokens"], None))
+    torch.cuda.synchronize()
+    op = oracle.predict(data["draft"], data["tokens"], spec.F, nthreads=0, lib=olib)
+    assert np.array_equal(pr["keys"].cpu().numpy(), op["keys"])
+    assert np.array_equal(pr["key_logits"].cpu().numpy(), op["key_logits"])
+    assert np.array_equal(pr["row_status"].cpu().numpy(), op["status"])
+    # the hit flag of the GPU outcome, recomputed by the oracle's definition
+    oh = oracle.check_hit(op["keys"], g["accept_len"], g["out_tokens"], lib=olib)
+    assert np.array_equal(hit.cpu().numpy(), oh)
+    print(f"cfg4: hit rate {oh.mean():.3f}")
+
+
+def test_cfg5_full_size_sampled(sv, olib):
+    """Config 5 at full size (B=256, K=8, V=152064 fp32) in the launch
+    configuration the benchmark times; 24 sampled rows against the oracle,
+    structural properties on every row."""
+    spec = wl.SPECS["cfg5"]
+    data = wl.generate(spec)
+    g = gpu_verify(sv, data)
+    B, K = spec.B, spec.K
+    n = g["accept_len"]
+    assert ((n >= 0) & (n <= K)).all()
+    assert (g["row_status"] & oracle.ROW_ERRORS == 0).all()
+    for b in range(B):
+        assert (g["out_tokens"][b, :n[b]] == data["tokens"][b, :n[b]]).all()
+        assert 0 <= g["out_tokens"][b, n[b]] < spec.V
+        assert (g["out_tokens"][b, n[b] + 1:] == -1).all()
+    rows = np.random.default_rng(0).choice(B, 24, replace=False)
+    sub = {k: (v[rows] if isinstance(v, np.ndarray) and v.shape[:1] == (B,) else v)
+           for k, v in data.items()}
+    o = oracle_verify(olib, sub)
+    gs = {k: v[rows] for k, v in g.items()}
+    nb = compare_verify(gs, o, sub["temperature"], "cfg5")
+    print(f"cfg5: sampled boundary rows {nb}/24; mean accept (all rows) {n.mean():.3f}")
+
+
+def test_predict_full_size_cfg5_layout(sv, olib):
+    """Outcome prediction at V=152064 fp32 with K+1 draft rows, F=6 and F=32."""
+    spec = wl.custom("pred5", B=8, K=8, V=152064, dtype=wl.FP32, kind="zipf",
+                     draft_scale=0.8, ssd=True, seed=wl.SEED_BASE + 5100)
+    data = wl.generate(spec)
+    dft = to_dev(data["draft"], spec.dtype)
+    tok = to_dev(data["tokens"], None)
+    for F in (6, 32):
+        pr = sv.specv_predict_outcomes(dft, tok, F)
+        torch.cuda.synchronize()
+        op = oracle.predict(data["draft"], data["tokens"], F, nthreads=0, lib=olib)
+        assert np.array_equal(pr["keys"].cpu().numpy(), op["keys"]), F
+        assert np.array_equal(pr["key_logits"].cpu().numpy(), op["key_logits"]), F
+
+
+# ---------------------------------------------------------------------------
+# sizes that span several tiles, ragged tails, every cluster width, layouts
+
+RAGGED = [
+    # (B, K, V, dtype, temps)  -- V sets the cluster width: ceil(V/8192), <= 16
+    (3, 2, 1, wl.FP32, (1.0,)),
+    (3, 2, 2, wl.BF16, (0.7,)),
+    (4, 3, 3, wl.FP32, (0.0, 1.0)),
+    (4, 3, 33, wl.BF16, (0.0, 0.6, 1.0)),
+    (5, 4, 4097, wl.FP32, (0.0, 0.6, 1.0)),
+    (5, 4, 8193, wl.BF16, (0.3, 1.5)),
+    (4, 5, 20001, wl.FP32, (1.0,)),
+    (4, 5, 70003, wl.BF16, (0.8,)),
+    (3, 6, 131071, wl.FP32, (0.5, 1.0)),
+    (3, 7, 152064, wl.BF16, (0.0, 1.0)),
+    (4, 32, 4096, wl.FP32, (1.0,)),
+    (2, 1, 128256, wl.BF16, (1.0,)),
+]
+
+
+@pytest.mark.parametrize("B,K,V,dtype,temps", RAGGED)
+def test_verify_ragged(sv, olib, B, K, V, dtype, temps):
+    spec = wl.custom(f"rag{V}", B=B, K=K, V=V, dtype=dtype, temps=temps,
+                     sigma_d=(0.3, 2.0), seed=wl.SEED_BASE + 7000 + V)
+    data = wl.generate(spec)
+    g = gpu_verify(sv, data)
+    o = oracle_verify(olib, data)
+    compare_verify(g, o, data["temperature"], f"V={V}")
+
+
+@pytest.mark.parametrize("dtype", [wl.FP32, wl.BF16])
+@pytest.mark.parametrize("V", [1000, 4101, 40000])
+def test_verify_padded_and_sliced_layouts(sv, olib, dtype, V):
+    """Row stride > V (16-byte aligned rows: vector path with a ragged tail)
+    and a batch slice of a larger tensor (unaligned rows: element path)."""
+    spec = wl.custom(f"pad{V}", B=6, K=3, V=V, dtype=dtype, temps=(0.0, 0.9),
+                     seed=wl.SEED_BASE + 7500 + V)
+    data = wl.generate(spec)
+    pad = (-V) % 16 + 16
+    for layout in ("padded", "offset"):
+        if layout == "padded":
+            t = np.zeros(data["target"].shape[:2] + (V + pad,), data["target"].dtype)
+            d = np.zeros(data["draft"].shape[:2] + (V + pad,), data["draft"].dtype)
+            t[..., :V] = data["target"]
+            d[..., :V] = data["draft"]
+            tt, dd = to_dev(t, dtype)[..., :V], to_dev(d, dtype)[..., :V]
+        else:
+            t = np.zeros(data["target"].shape[:2] + (V + 1,), data["target"].dtype)
+            d = np.zeros(data["draft"].shape[:2] + (V + 1,), data["draft"].dtype)
+            t[..., 1:] = data["target"]
+            d[..., 1:] = data["draft"]
+            tt, dd = to_dev(t, dtype)[..., 1:], to_dev(d, dtype)[..., 1:]
+        g = gpu_verify(sv, data, tt, dd)
+        o = oracle_verify(olib, data)
+        compare_verify(g, o, data["temperature"], f"{layout} V={V}")
+
+
+def _edge_batch(dtype):
+    """Hand-built rows: identical logits, -inf masks, q(x)=0, zero residual,
+    bad token / NaN / +inf / bad temperature, ties, extreme temperatures."""
+    rng = np.random.default_rng(99)
+    K, V = 3, 50
+    B = 12
+    zt = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    zd = (zt[:, :K] + rng.standard_normal((B, K, V))).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    temp = np.ones(B, np.float32)
+    u = rng.random((B, K + 1), dtype=np.float32)
+    zd[0] = zt[0, :K]                       # identical: every draft accepted
+    zt[1, :, 10:] = -np.inf                 # target masked outside [0, 10)
+    zd[2, 0, tok[2, 0]] = -np.inf           # q(x_1) = 0: reject at once
+    zd[3, 0] = zt[3, 0]                     # zero residual -> fallback to p
+    zt[3, 0, tok[3, 0]] = -np.inf
+    zd[3, 0, tok[3, 0]] = -np.inf
+    tok[4, 1] = V                           # bad token
+    zt[5, 2, 7] = np.nan                    # NaN
+    zd[6, 1, 3] = np.inf                    # +inf
+    temp[7] = -0.5                          # bad temperature
+    temp[8] = 0.0                           # greedy with ties
+    zt[8, :, :] = 0.0
+    zd[8, :, :] = 0.0
+    tok[8] = 0
+    temp[9] = 0.05                          # very low temperature
+    temp[10] = 7.0                          # very high temperature
+    zt[11, 1, :] = -np.inf                  # a target row with no finite logit
+    if dtype == wl.BF16:
+        zt = wl.f32_to_bf16_bits(zt)
+        zd = wl.f32_to_bf16_bits(zd)
+    spec = wl.custom("edge", B=B, K=K, V=V, dtype=dtype)
+    return dict(spec=spec, target=zt, draft=zd, tokens=tok, temperature=temp, uniforms=u)
+
+
+@pytest.mark.parametrize("dtype", [wl.FP32, wl.BF16])
+def test_verify_edge_cases(sv, olib, dtype):
+    data = _edge_batch(dtype)
+    g = gpu_verify(sv, data)
+    o = oracle_verify(olib, data)
+    compare_verify(g, o, data["temperature"], "edge")
+    assert o["accept_len"][0] == 3 and g["accept_len"][0] == 3
+    assert g["accept_len"][2] == 0
+    assert g["row_status"][3] & oracle.ROW_FALLBACK
+    assert g["row_status"][4] == oracle.ROW_BAD_TOKEN
+    assert g["row_status"][5] == oracle.ROW_NONFINITE
+    assert g["row_status"][6] == oracle.ROW_NONFINITE
+    assert g["row_status"][7] == oracle.ROW_BAD_TEMP
+    assert g["row_status"][11] == oracle.ROW_NONFINITE
+    assert g["out_tokens"][8].tolist() == [0, 0, 0, 0]
+
+
+def test_empty_batch(sv):
+    z = torch.zeros((0, 4, 16), device="cuda")
+    out = sv.specv_verify(z, z[:, :3], torch.zeros((0, 3), dtype=torch.int32, device="cuda"),
+                          torch.zeros(0, device="cuda"), torch.zeros((0, 4), device="cuda"))
+    assert out["accept_len"].numel() == 0
+    assert sv.last_launch_count() == 0
+
+
+@pytest.mark.parametrize("dtype", [wl.FP32, wl.BF16])
+def test_predict_edge_cases(sv, olib, dtype):
+    """Ties (bf16 grid values), F > V-1, exclusion, bad token, NaN row."""
+    rng = np.random.default_rng(5)
+    B, K, V, F = 4, 3, 37, 8
+    z = (rng.integers(-2, 3, (B, K + 1, V)) * 0.5).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    tok[1, 2] = -3
+    z[2, 1, 5] = np.nan
+    zz = wl.f32_to_bf16_bits(z) if dtype == wl.BF16 else z
+    dft = to_dev(zz, dtype)
+    for F_ in (F, 1, 32):
+        pr = sv.specv_predict_outcomes(dft, to_dev(tok, None), F_)
+        torch.cuda.synchronize()
+        op = oracle.predict(zz, tok, F_, lib=olib)
+        assert np.array_equal(pr["keys"].cpu().numpy(), op["keys"]), F_
+        assert np.array_equal(pr["key_logits"].cpu().numpy(), op["key_logits"]), F_
+        assert np.array_equal(pr["row_status"].cpu().numpy(), op["status"]), F_
+    small = to_dev(zz[:, :, :4], dtype)
+    pr = sv.specv_predict_outcomes(small, to_dev(np.clip(tok, 0, 3), None), 6)
+    op = oracle.predict(np.ascontiguousarray(zz[:, :, :4]), np.clip(tok, 0, 3), 6, lib=olib)
+    assert np.array_equal(pr["keys"].cpu().numpy(), op["keys"])
+
+
+def test_check_hit_matches_definition(sv, olib):
+    rng = np.random.default_rng(8)
+    B, K, F = 200, 4, 3
+    keys = rng.integers(0, 20, (B, K + 1, F)).astype(np.int32)
+    n = rng.integers(-1, K + 2, B).astype(np.int32)
+    toks = rng.integers(-1, 20, (B, K + 1)).astype(np.int32)
+    h = sv.specv_check_hit(to_dev(keys, None), to_dev(n, None), to_dev(toks, None))
+    torch.cuda.synchronize()
+    assert np.array_equal(h.cpu().numpy(), oracle.check_hit(keys, n, toks, lib=olib))
+
+
+def test_repeated_calls_are_deterministic(sv):
+    data = wl.generate(wl.SPECS["cfg3"])
+    a = gpu_verify(sv, data)
+    b = gpu_verify(sv, data)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
