@@ -54,8 +54,8 @@ WORKLOADS = {
     "cfg1": (wl.SPECS["cfg1"], "config 1 (B=1, K=4, V=4096, fp32, T=1), verify only"),
 }
 
-VERIFY_SRC = os.path.join(ROOT, "speculative_decoding_verification_50_gb300", "csrc",
-                          "verify_kernels.cuh")
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_50_gb300", "csrc",
+                          "units_kernel.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -106,8 +106,8 @@ def measured_peak() -> tuple:
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for name in ("verify_kernels.cuh", "specv_common.cuh"):
-        with open(os.path.join(os.path.dirname(VERIFY_SRC), name), "rb") as f:
+    for name in ("units_kernel.cuh", "specv_common.cuh"):
+        with open(os.path.join(os.path.dirname(KERNEL_SRC), name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -284,26 +284,22 @@ def run_ours(args) -> None:
     if F:
         keys = torch.empty((B, K + 1, F), **i32)
         key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
-        pstat = torch.empty(B, **i32)
-        ws_p = torch.empty(max(1, lib.specv_predict_workspace_bytes(B, K, V, F, code)), dtype=torch.uint8, device=dev)
         hit = torch.empty(B, dtype=torch.uint8, device=dev)
+        ws_v = torch.empty(max(1, lib.specv_ssd_workspace_bytes(B, K, V, F, code)), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     launches = [0]
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        sv.specv_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
+        if F:  # the fused SSD round: verify + outcome keys + hit in one pass
+            sv.specv_ssd_round(d_target, d_draft, d_tok, d_temp, d_unif, F, keys=keys,
+                               key_logits=key_logits, hit=hit, workspace=ws_v, **outs)
+        else:
+            sv.specv_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
         launches[0] += sv.last_launch_count()
         if ev is not None:
             ev[1].record(stream)
-        if F:
-            sv.specv_predict_outcomes(d_draft, d_tok, F, keys=keys, key_logits=key_logits,
-                                      row_status=pstat, workspace=ws_p)
-            launches[0] += sv.last_launch_count()
-            sv.specv_check_hit(keys, outs["accept_len"], outs["out_tokens"], hit=hit)
-            launches[0] += sv.last_launch_count()
-        if ev is not None:
             ev[2].record(stream)
 
     def barrier():
@@ -333,7 +329,6 @@ def run_ours(args) -> None:
     gpu_launches = launches[0]
     total_ms = t_start.elapsed_time(t_end)
     verify_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    rest_ms = [e[1].elapsed_time(e[2]) for e in evs]
     ms_step = reduce_max(total_ms, world, dev) / args.steps
     rows_total = reduce_sum(float(B * (K + 1)), world, dev)
     value = rows_total / (ms_step / 1e3)
@@ -380,7 +375,8 @@ def run_ours(args) -> None:
     peak, peak_kind = measured_peak()
     ab = algorithmic_bytes(spec)
     v_ms = statistics.mean(verify_ms)
-    achieved = ab["verify"] / (v_ms / 1e3) / 1e9
+    kernel_bytes = ab["step_fused"] if F else ab["verify"]
+    achieved = kernel_bytes / (v_ms / 1e3) / 1e9
     step_gbs = ab["step_fused"] / (ms_step / 1e3) / 1e9
     traffic = recorded_traffic(args.workload)
     in_bytes = d_target.numel() * d_target.element_size() + d_draft.numel() * d_draft.element_size()
@@ -406,19 +402,20 @@ def run_ours(args) -> None:
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "verify_units_kernel (+ finalize) per specv_verify call",
+            "kernel": ("units_kernel<ssd> + finalize per specv_ssd_round call" if F else
+                       "units_kernel<verify> + finalize per specv_verify call"),
             "achieved": round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_kind": f"of {peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "of fallback",
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": ab["verify"],
+            "algorithmic_bytes_per_launch": kernel_bytes,
             "avg_launch_ms": round(v_ms, 5),
         },
         "step_hbm": {"algorithmic_bytes": ab["step_fused"], "achieved_gbs": round(step_gbs, 1),
                      "frac": round(step_gbs / peak, 4),
-                     "verify_ms": round(v_ms, 5), "predict_hit_ms": round(statistics.mean(rest_ms), 5)},
+                     "call_ms": round(v_ms, 5)},
         "e2e": {"value": round(rows_total / (e2e_ms / 1e3), 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},

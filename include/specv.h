@@ -30,9 +30,13 @@
  *   - Argument errors are detected on the host, before any launch, and
  *     return SPECV_ERR_INVALID_ARG (nothing is written).  A failed launch
  *     returns SPECV_ERR_CUDA.  Data errors never trap: they are reported per
- *     batch row in the optional row_status output (bits below), and a
- *     flagged row gets accept length 0, tokens -1, and -1 keys.
- *   - Limits: 1 <= K <= 32, 1 <= V < 2^31, 0 <= B, 1 <= F <= 32.
+ *     batch row in the optional row_status output (bits below).  A flagged
+ *     batch row gets accept length 0 and tokens -1 (and, in an SSD round, -1
+ *     keys and no hit); specv_predict_outcomes gives -1 keys at the lookaheads
+ *     whose draft row or sent token is invalid.
+ *   - Limits: 1 <= K <= 32, 0 <= B, 1 <= F <= 32, 1 <= V < 2^31 (in practice
+ *     up to about 10^8: beyond that a CTA's table of partial sums no longer
+ *     fits in shared memory and the call returns SPECV_ERR_UNSUPPORTED).
  */
 #ifndef SPECV_H
 #define SPECV_H
@@ -110,6 +114,28 @@ size_t specv_verify_workspace_bytes(int32_t B, int32_t K, int32_t V,
  * caller, not shared with a concurrently running call. */
 specv_status specv_verify(const specv_verify_args* args, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/*
+ * One SSD round in a single pass over the logits ("Speculative Speculative
+ * Decoding" §3.1 Algorithm 1, §4.1.1): verification exactly as specv_verify,
+ * outcome keys exactly as specv_predict_outcomes (so draft_logits must hold
+ * K+1 rows per batch row), and hit[b] as specv_check_hit on the realised
+ * outcome.  Each draft row is read once and serves both q_i and the top-F
+ * keys at lookahead i.  row_status (if given) also reports non-finite
+ * logits in draft row K.
+ */
+typedef struct {
+  specv_verify_args verify;  /* draft rows: K+1 per batch row */
+  int32_t F;                 /* keys per lookahead, 1..32 */
+  int32_t* keys;             /* OUT [B, K+1, F] */
+  float* key_logits;         /* OUT, optional [B, K+1, F] */
+  uint8_t* hit;              /* OUT [B] */
+} specv_ssd_args;
+
+size_t specv_ssd_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F,
+                                 int32_t dtype);
+specv_status specv_ssd_round(const specv_ssd_args* args, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /*
  * SSD outcome prediction ("Speculative Speculative Decoding" §4.1.1).

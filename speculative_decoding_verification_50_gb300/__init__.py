@@ -8,6 +8,7 @@ missing library raises.
 
 Entry points (same names as the C ABI):
   specv_verify(target, draft, draft_tokens, temperature, uniforms, ...)
+  specv_ssd_round(target, draft, draft_tokens, temperature, uniforms, F, ...)
   specv_predict_outcomes(draft, draft_tokens, F, ...)
   specv_check_hit(keys, accept_len, out_tokens, ...)
 """
@@ -39,6 +40,11 @@ class VerifyArgs(ctypes.Structure):
                 ("row_status", _P)]
 
 
+class SsdArgs(ctypes.Structure):
+    _fields_ = [("verify", VerifyArgs), ("F", _I32), ("keys", _P), ("key_logits", _P),
+                ("hit", _P)]
+
+
 class PredictArgs(ctypes.Structure):
     _fields_ = [("B", _I32), ("K", _I32), ("V", _I32), ("F", _I32), ("dtype", _I32),
                 ("draft_logits", _P), ("draft_batch_stride", _I64), ("draft_row_stride", _I64),
@@ -66,6 +72,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specv_verify_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
     lib.specv_verify.restype = ctypes.c_int
     lib.specv_verify.argtypes = [ctypes.POINTER(VerifyArgs), _P, ctypes.c_size_t, _P]
+    lib.specv_ssd_workspace_bytes.restype = ctypes.c_size_t
+    lib.specv_ssd_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
+    lib.specv_ssd_round.restype = ctypes.c_int
+    lib.specv_ssd_round.argtypes = [ctypes.POINTER(SsdArgs), _P, ctypes.c_size_t, _P]
     lib.specv_predict_workspace_bytes.restype = ctypes.c_size_t
     lib.specv_predict_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
     lib.specv_predict_outcomes.restype = ctypes.c_int
@@ -112,22 +122,13 @@ def last_launch_count() -> int:
     return int(load_library().specv_last_launch_count())
 
 
-def specv_verify(target, draft, draft_tokens, temperature, uniforms, *, accept_len=None,
-                 out_tokens=None, p_draft=None, q_draft=None, row_status=None,
-                 workspace=None, stream=None) -> dict:
-    """Verify B batch rows on the GPU (see include/specv.h, specv_verify).
-
-    target [B, >=K+1, V], draft [B, >=K, V] (bf16 or fp32, CUDA, last dim
-    contiguous); draft_tokens int32 [B, K]; temperature fp32 [B]; uniforms
-    fp32 [B, K+1].  Outputs are allocated when not given.  Returns a dict
-    with accept_len, out_tokens, p_draft, q_draft, row_status.
-    """
+def _verify_args(target, draft, draft_tokens, temperature, uniforms, draft_rows, accept_len,
+                 out_tokens, p_draft, q_draft, row_status):
     import torch
-    lib = load_library()
     B, K = draft_tokens.shape
     V = target.shape[-1]
     assert target.dim() == 3 and draft.dim() == 3 and target.shape[0] == B and draft.shape[0] == B
-    assert target.shape[1] >= K + 1 and draft.shape[1] >= K and draft.shape[-1] == V
+    assert target.shape[1] >= K + 1 and draft.shape[1] >= draft_rows and draft.shape[-1] == V
     assert target.stride(-1) == 1 and draft.stride(-1) == 1
     assert target.dtype == draft.dtype
     assert uniforms.shape == (B, K + 1) and temperature.shape == (B,)
@@ -142,19 +143,69 @@ def specv_verify(target, draft, draft_tokens, temperature, uniforms, *, accept_l
         q_draft = torch.empty((B, K), dtype=torch.float32, device=dev)
     if row_status is None:
         row_status = torch.empty(B, dtype=torch.int32, device=dev)
-    code = _dtype_code(target)
-    need = lib.specv_verify_workspace_bytes(B, K, V, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    args = VerifyArgs(B, K, V, code,
+    args = VerifyArgs(B, K, V, _dtype_code(target),
                       target.data_ptr(), target.stride(0), target.stride(1),
                       draft.data_ptr(), draft.stride(0), draft.stride(1),
                       draft_tokens.data_ptr(), temperature.data_ptr(), uniforms.data_ptr(),
                       accept_len.data_ptr(), out_tokens.data_ptr(),
                       p_draft.data_ptr(), q_draft.data_ptr(), row_status.data_ptr())
-    _check(lib.specv_verify(ctypes.byref(args), _ptr(workspace), workspace.numel(), _stream(stream)))
-    return dict(accept_len=accept_len, out_tokens=out_tokens, p_draft=p_draft,
+    outs = dict(accept_len=accept_len, out_tokens=out_tokens, p_draft=p_draft,
                 q_draft=q_draft, row_status=row_status)
+    return args, outs
+
+
+def specv_verify(target, draft, draft_tokens, temperature, uniforms, *, accept_len=None,
+                 out_tokens=None, p_draft=None, q_draft=None, row_status=None,
+                 workspace=None, stream=None) -> dict:
+    """Verify B batch rows on the GPU (see include/specv.h, specv_verify).
+
+    target [B, >=K+1, V], draft [B, >=K, V] (bf16 or fp32, CUDA, last dim
+    contiguous); draft_tokens int32 [B, K]; temperature fp32 [B]; uniforms
+    fp32 [B, K+1].  Outputs are allocated when not given.  Returns a dict
+    with accept_len, out_tokens, p_draft, q_draft, row_status.
+    """
+    import torch
+    lib = load_library()
+    B, K = draft_tokens.shape
+    args, outs = _verify_args(target, draft, draft_tokens, temperature, uniforms, K, accept_len,
+                              out_tokens, p_draft, q_draft, row_status)
+    need = lib.specv_verify_workspace_bytes(B, K, target.shape[-1], args.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=target.device)
+    _check(lib.specv_verify(ctypes.byref(args), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return outs
+
+
+def specv_ssd_round(target, draft, draft_tokens, temperature, uniforms, F: int, *,
+                    accept_len=None, out_tokens=None, p_draft=None, q_draft=None,
+                    row_status=None, keys=None, key_logits=None, hit=None, workspace=None,
+                    stream=None) -> dict:
+    """One fused SSD round (see include/specv.h, specv_ssd_round): verification,
+    top-F outcome keys at every lookahead and the hit flag, in one pass.
+
+    draft must hold K+1 rows per batch row.  Returns the specv_verify outputs
+    plus keys int32 [B, K+1, F], key_logits fp32 [B, K+1, F], hit uint8 [B].
+    """
+    import torch
+    lib = load_library()
+    B, K = draft_tokens.shape
+    args, outs = _verify_args(target, draft, draft_tokens, temperature, uniforms, K + 1,
+                              accept_len, out_tokens, p_draft, q_draft, row_status)
+    dev = target.device
+    if keys is None:
+        keys = torch.empty((B, K + 1, F), dtype=torch.int32, device=dev)
+    if key_logits is None:
+        key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
+    if hit is None:
+        hit = torch.empty(B, dtype=torch.uint8, device=dev)
+    need = lib.specv_ssd_workspace_bytes(B, K, target.shape[-1], F, args.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    sargs = SsdArgs(args, F, keys.data_ptr(), key_logits.data_ptr(), hit.data_ptr())
+    _check(lib.specv_ssd_round(ctypes.byref(sargs), _ptr(workspace), workspace.numel(),
+                               _stream(stream)))
+    outs.update(keys=keys, key_logits=key_logits, hit=hit)
+    return outs
 
 
 def specv_predict_outcomes(draft, draft_tokens, F: int, *, keys=None, key_logits=None,

@@ -1,0 +1,540 @@
+// Kernel B of the hot path: per batch row, from kernel A's chunk records,
+//   a2 the left-to-right accept test u_i <= p_i(x_i)/q_i(x_i) up to the first
+//      rejection n ("Lecture 5 - Speculative Decoding and SpecInfer" §2.2,
+//      §2.7; "Speculative Decoding" dl-note Appendix: draft prob 0 rejects),
+//   a3 the bonus t* by inverse CDF of r = max(p_n - q_n, 0), or of p_K when
+//      all K drafts are accepted ("Speculative Speculative Decoding" §2.1;
+//      dl-note §2.3; Lecture 5 §3.1),
+//   a4 the outcome keys: top-F of the per-chunk candidates at each lookahead
+//      ("Speculative Speculative Decoding" §4.1.1), and
+//   a5 the hit flag: t* among the keys of lookahead n (§3.1).
+//
+// One thread-block cluster of CB CTAs per batch row.  Every CTA combines the
+// records itself (one warp per position, lanes over chunks, fp64 sums) and
+// decides n; the arithmetic and its order are the same everywhere, so all CTAs
+// agree without waiting for one another.  CTA r merges the keys of lookaheads
+// r, r+CB, ... (threshold from the F-th best chunk head, then rank counting).
+// Only row n is read again: every CTA streams its slice of target row n (and
+// draft row n), forms r, and reduces it to per-warp segment sums; the per-CTA
+// totals are exchanged through distributed shared memory, which gives R and the
+// CTA whose range holds U_K * R; that CTA walks its segments and one warp scans
+// the one segment that holds the crossing (a re-read of 32 vectors).  Rank 0
+// writes the outputs.
+#pragma once
+
+#include "stats_kernel.cuh"
+
+namespace specv {
+
+constexpr int kMaxK = 32;
+constexpr int kTileUnroll = 8;  // tiles of r per loop trip in the residual pass
+
+struct PosStats {  // one position's combined row statistics
+  double St, Sd;
+  float Mt, Md;
+  int32_t it, id;
+  int32_t bad;
+  int32_t pad;
+};
+
+struct Dec {  // a batch row's decision (the same in every CTA of its cluster)
+  int32_t n, status, mode, need_scan, token, owner, last_pos, pad;
+  float mt, md, ist, isd;
+  double tau, pre_mine;
+  float px[kMaxK], qx[kMaxK];
+};
+static_assert(sizeof(Dec) % 4 == 0, "Dec copied as words");
+
+struct DecideParams {
+  const void* zt;
+  int64_t t_bs, t_rs;
+  const void* zd;
+  int64_t d_bs, d_rs;
+  const int32_t* tokens;
+  const float* temp;
+  const float* unif;
+  const ChunkRec* recs;
+  const float* cand_v;
+  const int32_t* cand_i;
+  int32_t* accept_len;
+  int32_t* out_tokens;
+  float* p_draft;
+  float* q_draft;
+  int32_t* row_status;
+  int32_t* keys;
+  float* key_logits;
+  uint8_t* hit;
+  int32_t B, K, V, F, nchunk, CB, L;
+};
+
+// Combine the chunk records of one position (warp-wide; result in every lane).
+__device__ __forceinline__ PosStats combine_position(const ChunkRec* R, int nchunk, float c,
+                                                     int lane) {
+  float mt = kNegMax, s_t = 0.f, md = kNegMax, s_d = 0.f;
+  Arg at, ad;
+  at.init();
+  ad.init();
+  for (int q = lane; q < nchunk; q += 32) {
+    const ChunkRec r = R[q];
+    soft_merge(mt, s_t, r.mt, r.st, c);
+    soft_merge(md, s_d, r.md, r.sd, c);
+    at.merge(r.bt, r.it, r.bad);
+    ad.merge(r.bd, r.id, 0);
+  }
+  PosStats p;
+  p.Mt = warp_max_all(mt);
+  p.Md = warp_max_all(md);
+  p.St = warp_dsum_all(static_cast<double>(s_t) * static_cast<double>(ex2((mt - p.Mt) * c)));
+  p.Sd = warp_dsum_all(static_cast<double>(s_d) * static_cast<double>(ex2((md - p.Md) * c)));
+  warp_arg_all(at.best, at.idx);
+  warp_arg_all(ad.best, ad.idx);
+  p.it = at.idx;
+  p.id = ad.idx;
+  p.bad = __any_sync(0xffffffffu, at.bad);
+  p.pad = 0;
+  return p;
+}
+
+// Top-F over the per-chunk candidate lists of one draft row (warp-wide).
+__device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int32_t* ci, int ncand,
+                                                     int F, int lane) {
+  WarpTopF L;
+  L.init();
+  for (int base = 0; base < ncand; base += 32) {
+    const int idx = base + lane;
+    float z = neg_inf();
+    int32_t vi = INT_MAX;
+    if (idx < ncand) {
+      z = cv[idx];
+      vi = ci[idx];
+    }
+    unsigned m = __ballot_sync(0xffffffffu, vi != INT_MAX && key_beats(z, vi, L.tv, L.ti));
+    while (m) {
+      const int src = __ffs(m) - 1;
+      m &= m - 1;
+      const float zz = __shfl_sync(0xffffffffu, z, src);
+      const int32_t ii = __shfl_sync(0xffffffffu, vi, src);
+      L.insert(zz, ii, F, lane);
+    }
+  }
+  return L;
+}
+
+// r values of vector j of a row slice (global memory): mode 0 max(p - q, 0),
+// mode 1 p.  Both products rounded before the subtraction (no contraction), so
+// p(v) = q(v) gives r(v) = 0 exactly, as in the definition.
+template <int DT, bool VEC>
+__device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd, int64_t v0,
+                                             int64_t v1, int j, int mode, float mt, float md,
+                                             float c, float ist, float isd,
+                                             float (&r)[Elem<DT>::VW]) {
+  using E = Elem<DT>;
+  constexpr int VW = E::VW;
+  float zt[VW];
+  E::unpack(load_vec<DT, VEC>(rowt, v0, v1, j), zt);
+  if (mode == 0) {
+    float zd[VW];
+    E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), zd);
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
+      const float q = __fmul_rn(ex2((zd[k] - md) * c), isd);
+      r[k] = fmaxf(__fsub_rn(p, q), 0.f);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < VW; ++k) r[k] = __fmul_rn(ex2((zt[k] - mt) * c), ist);
+  }
+}
+
+template <int DT, bool VEC, int MODE>
+__global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) {
+  using E = Elem<DT>;
+  constexpr int VW = E::VW;
+  constexpr bool kTopF = MODE != kModeVerify;
+  extern __shared__ float segs[];  // [tiles * kWarps] segment sums of r
+  __shared__ PosStats ps[kMaxK + 1];
+  __shared__ Dec dec;
+  __shared__ double cta_total;
+  __shared__ KeyScratch KS;
+  __shared__ int32_t tok_slot;  // rank 0: the token found by the owner CTA
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int CB = P.CB;
+  const int b = static_cast<int>(blockIdx.x / CB);
+  const int K = P.K, F = P.F;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const float T = P.temp[b];
+  const bool greedy = T == 0.f;
+  const bool temp_ok = T >= 0.f && T < pos_inf();
+  const float c = greedy ? 1.f : temp_scale(T);
+  const int64_t u0 = static_cast<int64_t>(b) * (K + 1);
+
+  // ---- every CTA combines the records and decides (identical results) -------
+  for (int i = warp; i <= K; i += kWarps) {
+    const PosStats p = combine_position(P.recs + (u0 + i) * P.nchunk, P.nchunk, c, lane);
+    if (lane == 0) ps[i] = p;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int nf = 0;
+    if (lane <= K && temp_ok) {
+      const PosStats& q = ps[lane];
+      const bool d_full = lane < K;  // draft rows that are normalised
+      const bool d_any = (MODE != kModeVerify) || lane < K;
+      if (greedy) {
+        nf = q.bad || q.it == INT_MAX || (d_full && q.id == INT_MAX);
+      } else {
+        nf = !(q.St >= 1.0) || q.Mt == kNegMax;
+        if (d_full) nf |= !(q.Sd >= 1.0) || q.Md == kNegMax;
+        else if (d_any) nf |= q.Sd != q.Sd;  // draft row K: NaN / +inf only
+      }
+    }
+    const bool acc_lane = lane < K;
+    const int x = acc_lane ? P.tokens[static_cast<int64_t>(b) * K + lane] : -1;
+    int status = temp_ok ? 0 : kBadTemp;
+    if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
+    if (__any_sync(0xffffffffu, acc_lane && (x < 0 || x >= P.V))) status |= kBadToken;
+    const bool ok = !(status & kErrors);
+    bool accept = false;
+    float px = 0.f, qx = 0.f;
+    if (acc_lane && ok) {
+      const PosStats& q = ps[lane];
+      if (greedy) {
+        px = (x == q.it) ? 1.f : 0.f;
+        qx = (x == q.id) ? 1.f : 0.f;
+        accept = (x == q.it) && (x == q.id);
+      } else {
+        const char* rt = static_cast<const char*>(P.zt) +
+                         (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(lane) * P.t_rs) * E::ES;
+        const char* rd = static_cast<const char*>(P.zd) +
+                         (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(lane) * P.d_rs) * E::ES;
+        const float ztx = E::scalar(rt, x);
+        const float zdx = E::scalar(rd, x);
+        const float lt = __fmul_rn(ztx - q.Mt, c);  // log2 of unnormalised p_i(x), q_i(x)
+        const float ld = __fmul_rn(zdx - q.Md, c);
+        const float St = static_cast<float>(q.St), Sd = static_cast<float>(q.Sd);
+        px = __fdiv_rn(ex2(lt), St);
+        qx = __fdiv_rn(ex2(ld), Sd);
+        if (zdx != neg_inf()) {  // q_i(x_i) > 0
+          const float ratio = __fmul_rn(ex2(__fsub_rn(lt, ld)), __fdiv_rn(Sd, St));
+          accept = ratio >= P.unif[u0 + lane];
+        }
+      }
+    }
+    const unsigned rej = __ballot_sync(0xffffffffu, acc_lane && !accept);
+    const int n = ok ? (rej ? __ffs(rej) - 1 : K) : 0;
+    if (lane < K) {
+      dec.px[lane] = px;
+      dec.qx[lane] = qx;
+    }
+    if (lane == 0) {
+      const PosStats& q = ps[n];
+      dec.n = n;
+      dec.status = status;
+      dec.mode = (n < K) ? 0 : 1;
+      dec.need_scan = ok && !greedy;
+      dec.token = (ok && greedy) ? q.it : -1;
+      dec.owner = -1;
+      dec.last_pos = 0;
+      dec.mt = q.Mt;
+      dec.md = q.Md;
+      dec.ist = static_cast<float>(1.0 / q.St);
+      dec.isd = static_cast<float>(1.0 / q.Sd);
+      dec.tau = 0.0;
+      dec.pre_mine = 0.0;
+      tok_slot = dec.token;
+    }
+  }
+  __syncthreads();
+
+  // ---- outcome keys: lookaheads k = rank, rank + CB, ... ---------------------
+  if (kTopF) {
+    const bool ok = !(dec.status & kErrors);
+    for (int k = rank; k <= K; k += CB) {
+      const int64_t u = u0 + k;
+      select_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F, P.nchunk, F, KS);
+      if (threadIdx.x < F) {
+        const bool good = ok && KS.out_i[threadIdx.x] != INT_MAX;
+        const int32_t key = good ? KS.out_i[threadIdx.x] : -1;
+        P.keys[u * F + threadIdx.x] = key;
+        if (P.key_logits) P.key_logits[u * F + threadIdx.x] = good ? KS.out_v[threadIdx.x] : neg_inf();
+      }
+      __syncthreads();
+    }
+    __threadfence();  // keys visible to rank 0 after the cluster barrier below
+  }
+
+  if (dec.need_scan) {
+    const int n = dec.n;
+    const void* rowt = static_cast<const char*>(P.zt) +
+                       (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(n) * P.t_rs) * E::ES;
+    const void* rowd = static_cast<const char*>(P.zd) +
+                       (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(n < K ? n : 0) * P.d_rs) * E::ES;
+    const int64_t v0 = static_cast<int64_t>(rank) * P.L;
+    const int64_t v1 = min(static_cast<int64_t>(P.V), v0 + P.L);
+    const int nv = v1 > v0 ? static_cast<int>((v1 - v0 + VW - 1) / VW) : 0;
+    const int ntl = (nv + kThreads - 1) / kThreads;
+    // ---- residual mass of this slice: per-warp segment sums ----------------
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      const int mode = dec.mode;
+      const float mt = dec.mt, md = dec.md, ist = dec.ist, isd = dec.isd;
+      for (int t0 = 0; t0 < ntl; t0 += kTileUnroll) {
+        float s[kTileUnroll];
+#pragma unroll
+        for (int q = 0; q < kTileUnroll; ++q) {
+          const int j = (t0 + q) * kThreads + threadIdx.x;
+          s[q] = 0.f;
+          if (j < nv) {
+            float r[VW];
+            residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, r);
+#pragma unroll
+            for (int k = 0; k < VW; ++k) s[q] += r[k];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kTileUnroll; ++q) {
+          const float w = warp_sum(s[q]);
+          if (lane == 0 && t0 + q < ntl) segs[(t0 + q) * kWarps + warp] = w;
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        double acc = 0.0;
+        for (int sg = lane; sg < ntl * kWarps; sg += 32) acc += static_cast<double>(segs[sg]);
+        acc = warp_dsum_all(acc);
+        if (lane == 0) cta_total = acc;
+      }
+      cluster_sync();  // (1) per-CTA totals visible
+      if (warp == 0) {
+        const double tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total, lane) : 0.0;
+        double incl = tr;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const double R = __shfl_sync(0xffffffffu, incl, 31);
+        const double tau = static_cast<double>(P.unif[u0 + K]) * R;
+        const unsigned own = __ballot_sync(0xffffffffu, tr > 0.0 && incl > tau);
+        const unsigned pos = __ballot_sync(0xffffffffu, tr > 0.0);
+        const double pm = __shfl_sync(0xffffffffu, incl - tr, rank);
+        if (lane == 0) {
+          dec.tau = tau;
+          dec.pre_mine = pm;
+          if (R > 0.0) {
+            if (own) {
+              dec.owner = __ffs(own) - 1;
+            } else {  // U*R >= R after rounding: the last index with r > 0
+              dec.owner = 31 - __clz(pos);
+              dec.last_pos = 1;
+              dec.status |= kFallback;
+            }
+          } else if (dec.mode == 0) {
+            dec.mode = 1;  // zero residual mass: draw from p_n instead
+            dec.status |= kFallback;
+          }
+        }
+      }
+      cluster_sync();  // (2) totals read everywhere (they may be rewritten)
+      if (dec.owner >= 0 || attempt == 1 || dec.mode == 0) break;
+    }
+
+    // ---- owner CTA: locate the crossing segment, then scan it --------------
+    if (rank == dec.owner && warp == 0) {
+      // lanes own contiguous blocks of segments; a warp scan of the block sums
+      // finds the block that holds the crossing, whose lane walks it
+      const int nseg = ntl * kWarps;
+      const double tau = dec.tau;
+      const int per = (nseg + 31) / 32;
+      const int s0 = min(nseg, lane * per), s1 = min(nseg, s0 + per);
+      double bsum = 0.0;
+      int lastpos = -1;
+      for (int sg = s0; sg < s1; ++sg) {
+        const float g = segs[sg];
+        if (g > 0.f) {
+          bsum += static_cast<double>(g);
+          lastpos = sg;
+        }
+      }
+      double incl = bsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const double bpre = dec.pre_mine + (incl - bsum);
+      const unsigned hitm = dec.last_pos ? 0u : __ballot_sync(0xffffffffu, bsum > 0.0 && bpre + bsum > tau);
+      const unsigned posm = __ballot_sync(0xffffffffu, lastpos >= 0);
+      int seg = -1;
+      double cum_at = 0.0;
+      if (hitm) {
+        const int L = __ffs(hitm) - 1;
+        if (lane == L) {
+          double cum = bpre;
+          for (int sg = s0; sg < s1; ++sg) {
+            const float g = segs[sg];
+            if (g > 0.f) {
+              if (cum + static_cast<double>(g) > tau) {
+                seg = sg;
+                cum_at = cum;
+                break;
+              }
+              cum += static_cast<double>(g);
+            }
+          }
+          if (seg < 0) seg = lastpos;  // rounding inside the block
+        }
+        seg = __shfl_sync(0xffffffffu, seg, L);
+        cum_at = __shfl_sync(0xffffffffu, cum_at, L);
+      }
+      const int lastseg = posm ? __shfl_sync(0xffffffffu, lastpos, 31 - __clz(posm)) : -1;
+      bool lp = dec.last_pos || seg < 0;
+      if (seg < 0) seg = lastseg;
+      const int j = (seg / kWarps) * kThreads + (seg % kWarps) * 32 + lane;
+      float r[VW];
+#pragma unroll
+      for (int k = 0; k < VW; ++k) r[k] = 0.f;
+      if (seg >= 0 && j < nv)
+        residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, dec.mode, dec.mt, dec.md, c, dec.ist,
+                              dec.isd, r);
+      const int32_t base = static_cast<int32_t>(v0) + j * VW;
+      int found = -1;
+      if (!lp) {
+        float vs = 0.f;
+#pragma unroll
+        for (int k = 0; k < VW; ++k) vs += r[k];
+        double incl = static_cast<double>(vs);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const double excl_sum = incl - static_cast<double>(vs);
+        const unsigned m = __ballot_sync(0xffffffffu, vs > 0.f && cum_at + incl > tau);
+        if (m) {
+          if (lane == __ffs(m) - 1) {
+            double run = cum_at + excl_sum;
+            int kk = -1, klast = -1;
+#pragma unroll
+            for (int k = 0; k < VW; ++k) {
+              if (r[k] > 0.f) {
+                run += static_cast<double>(r[k]);
+                klast = k;
+                if (kk < 0 && run > tau) kk = k;
+              }
+            }
+            found = base + (kk >= 0 ? kk : klast);
+          }
+        } else {
+          lp = true;
+        }
+      }
+      if (lp) {
+        int kl = -1;
+#pragma unroll
+        for (int k = 0; k < VW; ++k)
+          if (r[k] > 0.f) kl = k;
+        const unsigned m = __ballot_sync(0xffffffffu, kl >= 0);
+        if (m && lane == 31 - __clz(m)) found = base + kl;
+      }
+      const unsigned mf = __ballot_sync(0xffffffffu, found >= 0);
+      const int tok = mf ? __shfl_sync(0xffffffffu, found, __ffs(mf) - 1) : -1;
+      if (lane == 0) *cluster.map_shared_rank(&tok_slot, 0) = tok;
+    }
+  }
+  // the owner's token (written into rank 0's shared memory after the first
+  // cluster barrier) and every CTA's keys visible to rank 0; every CTA passes
+  // here exactly once when a scan or keys ran.
+  if (dec.need_scan || kTopF) cluster_sync();
+
+  // ---- outputs, written by rank 0 ---------------------------------------------
+  if (rank == 0) {
+    const bool ok = !(dec.status & kErrors);
+    const int n = dec.n;
+    const int t = threadIdx.x;
+    const int32_t token = tok_slot;
+    if (t <= K) {
+      int32_t v = -1;
+      if (ok) v = (t < n) ? P.tokens[static_cast<int64_t>(b) * K + t] : (t == n ? token : -1);
+      P.out_tokens[u0 + t] = v;
+    }
+    if (t < K) {
+      if (P.p_draft) P.p_draft[static_cast<int64_t>(b) * K + t] = dec.px[t];
+      if (P.q_draft) P.q_draft[static_cast<int64_t>(b) * K + t] = dec.qx[t];
+    }
+    if (t == 0) {
+      P.accept_len[b] = ok ? n : 0;
+      if (P.row_status) P.row_status[b] = ok ? (dec.status & kFallback) : (dec.status & kErrors);
+      if (P.hit) {
+        uint8_t h = 0;
+        if (ok && token >= 0)
+          for (int f = 0; f < F; ++f) h |= (P.keys[(u0 + n) * F + f] == token);
+        P.hit[b] = h;
+      }
+    }
+  }
+}
+
+// Outcome keys alone (specv_predict_outcomes): one CTA per batch row, one warp
+// per lookahead.  A lookahead whose sent token is out of range or whose draft
+// row holds NaN / +inf gets -1 keys; the batch row's status ORs them.
+struct PredictKeysParams {
+  const int32_t* tokens;
+  const ChunkRec* recs;
+  const float* cand_v;
+  const int32_t* cand_i;
+  int32_t* keys;
+  float* key_logits;
+  int32_t* row_status;
+  int32_t B, K, V, F, nchunk;
+};
+
+__global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKeysParams P) {
+  __shared__ KeyScratch KS;
+  __shared__ int32_t row_bad;
+  const int b = blockIdx.x;
+  const int K = P.K, F = P.F;
+  const int64_t u0 = static_cast<int64_t>(b) * (K + 1);
+  int status_all = 0;
+  for (int k = 0; k <= K; ++k) {
+    const int64_t u = u0 + k;
+    if (threadIdx.x == 0) row_bad = 0;
+    __syncthreads();
+    for (int q = threadIdx.x; q < P.nchunk; q += kThreads)
+      if (P.recs[u * P.nchunk + q].bad) row_bad = 1;
+    const int x = (k < K) ? P.tokens[static_cast<int64_t>(b) * K + k] : 0;
+    select_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F, P.nchunk, F, KS);
+    const int status = (row_bad ? kNonFinite : 0) | ((x < 0 || x >= P.V) ? kBadToken : 0);
+    if (threadIdx.x < F) {
+      const bool good = status == 0 && KS.out_i[threadIdx.x] != INT_MAX;
+      P.keys[u * F + threadIdx.x] = good ? KS.out_i[threadIdx.x] : -1;
+      if (P.key_logits) P.key_logits[u * F + threadIdx.x] = good ? KS.out_v[threadIdx.x] : neg_inf();
+    }
+    status_all |= status;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0 && P.row_status) P.row_status[b] = status_all;
+}
+
+__global__ void check_hit_kernel(int B, int K, int F, const int32_t* __restrict__ keys,
+                                 const int32_t* __restrict__ accept_len,
+                                 const int32_t* __restrict__ out_tokens,
+                                 uint8_t* __restrict__ hit) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int n = accept_len[b];
+  uint8_t h = 0;
+  if (n >= 0 && n <= K) {
+    const int t = out_tokens[static_cast<int64_t>(b) * (K + 1) + n];
+    if (t >= 0) {
+      const int32_t* kk = keys + (static_cast<int64_t>(b) * (K + 1) + n) * F;
+      for (int f = 0; f < F; ++f) h |= (kk[f] == t);
+    }
+  }
+  hit[b] = h;
+}
+
+}  // namespace specv

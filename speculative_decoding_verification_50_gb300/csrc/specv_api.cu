@@ -6,8 +6,7 @@
 #include <string>
 
 #include "specv.h"
-#include "predict_kernels.cuh"
-#include "verify_kernels.cuh"
+#include "decide_kernel.cuh"
 
 using namespace specv;
 
@@ -36,16 +35,20 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 int elem_bytes(int32_t dtype) { return dtype == SPECV_BF16 ? 2 : 4; }
 int vec_width(int32_t dtype) { return dtype == SPECV_BF16 ? 8 : 4; }
 
-// CTAs per cluster: one per ~8K logits of a row, at most 16.  SPECV_CLUSTER
-// (1..16) overrides it, for tuning runs.
-int pick_cluster(int32_t V) {
+// CTAs per batch row in the decision kernel (a cluster): enough CTAs in
+// total to keep every SM streaming the re-read row, at most 16, and no more
+// than there are 256-vector tiles in a row.  SPECV_CLUSTER (1..16) overrides
+// it, for tuning runs.
+int pick_cluster(int32_t B, int32_t V, int vw) {
   static int env = -2;
   if (env == -2) {
     const char* s = getenv("SPECV_CLUSTER");
     env = s ? atoi(s) : -1;
   }
   if (env >= 1 && env <= 16) return env;
-  int c = (V + 8191) / 8192;
+  int c = (608 + B - 1) / (B > 0 ? B : 1);
+  const int tiles = static_cast<int>((static_cast<int64_t>(V) + kThreads * vw - 1) / (kThreads * vw));
+  if (c > tiles) c = tiles;
   return c < 1 ? 1 : (c > 16 ? 16 : c);
 }
 
@@ -71,7 +74,7 @@ cudaError_t launch_clustered(Kern k, int C, int64_t units, size_t smem, cudaStre
                              const Params& p) {
   cudaError_t e = allow_cluster(k, C);
   if (e != cudaSuccess) return e;
-  if (smem > 0) {
+  if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
@@ -90,9 +93,108 @@ cudaError_t launch_clustered(Kern k, int C, int64_t units, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
-constexpr size_t kMaxSegSmem = 48 * 1024;
-
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Sizes of one call: kernel A chunks, kernel B cluster and slices, workspace.
+struct Plan {
+  int iters;       // loop trips per kernel-A CTA
+  int64_t chunk;   // logits per kernel-A CTA
+  int64_t nchunk;  // chunks per row
+  int CB;          // CTAs per batch row in kernel B
+  int64_t L;       // kernel-B slice per CTA
+  size_t smemB;    // kernel-B dynamic shared memory (segment sums)
+  size_t recs_bytes, cand_bytes;
+};
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+  }
+  return n;
+}
+
+Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
+  Plan pl;
+  const int vw = vec_width(dtype);
+  const int64_t units = static_cast<int64_t>(B > 0 ? B : 0) * (K + 1);
+  // Loop trips per kernel-A CTA: long chunks amortise the per-CTA reductions;
+  // halve them while the grid would be under about two waves (4 CTAs per SM).
+  pl.iters = 8;
+  const int64_t want = 8LL * sm_count();
+  for (;;) {
+    pl.chunk = static_cast<int64_t>(pl.iters) * kVecs * kThreads * vw;
+    pl.nchunk = (static_cast<int64_t>(V) + pl.chunk - 1) / pl.chunk;
+    if (pl.iters == 1 || units * pl.nchunk >= want) break;
+    pl.iters /= 2;
+  }
+  pl.CB = pick_cluster(B, V, vw);
+  pl.L = slice_len(V, pl.CB, vw);
+  const int64_t ntiles = ((pl.L / vw) + kThreads - 1) / kThreads;
+  pl.smemB = static_cast<size_t>(ntiles) * kWarps * sizeof(float);
+  pl.recs_bytes = round_up(static_cast<size_t>(units * pl.nchunk) * sizeof(ChunkRec), 256);
+  pl.cand_bytes = F > 0 ? round_up(static_cast<size_t>(units * pl.nchunk * F) * 4, 256) : 0;
+  return pl;
+}
+
+size_t plan_workspace(const Plan& pl) { return pl.recs_bytes + 2 * pl.cand_bytes; }
+
+constexpr size_t kMaxSegSmem = 200 * 1024;
+
+template <typename Kern, typename Params>
+cudaError_t launch_plain(Kern k, int64_t blocks, cudaStream_t s, const Params& p) {
+  k<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_stats(int dtype, bool vec, int64_t blocks, cudaStream_t s, const StatsParams& p) {
+  if (dtype == SPECV_BF16)
+    return vec ? launch_plain(stats_kernel<0, true, MODE>, blocks, s, p)
+               : launch_plain(stats_kernel<0, false, MODE>, blocks, s, p);
+  return vec ? launch_plain(stats_kernel<1, true, MODE>, blocks, s, p)
+             : launch_plain(stats_kernel<1, false, MODE>, blocks, s, p);
+}
+
+template <int MODE>
+cudaError_t launch_decide(int dtype, bool vec, int CB, int64_t B, size_t smem, cudaStream_t s,
+                          const DecideParams& p) {
+  if (dtype == SPECV_BF16)
+    return vec ? launch_clustered(decide_kernel<0, true, MODE>, CB, B, smem, s, p)
+               : launch_clustered(decide_kernel<0, false, MODE>, CB, B, smem, s, p);
+  return vec ? launch_clustered(decide_kernel<1, true, MODE>, CB, B, smem, s, p)
+             : launch_clustered(decide_kernel<1, false, MODE>, CB, B, smem, s, p);
+}
+
+// Checks shared by specv_verify and specv_ssd_round.
+specv_status check_verify_args(const specv_verify_args* a, int draft_rows) {
+  const int32_t B = a->B, K = a->K, V = a->V;
+  if (B < 0) return fail(SPECV_ERR_INVALID_ARG, "B=%d < 0", B);
+  if (K < 1 || K > 32) return fail(SPECV_ERR_INVALID_ARG, "K=%d outside [1, 32]", K);
+  if (V < 1) return fail(SPECV_ERR_INVALID_ARG, "V=%d < 1", V);
+  if (a->dtype != SPECV_BF16 && a->dtype != SPECV_FP32)
+    return fail(SPECV_ERR_INVALID_ARG, "dtype=%d is not SPECV_BF16 or SPECV_FP32", a->dtype);
+  if (B == 0) return SPECV_OK;
+  if (!a->target_logits || !a->draft_logits || !a->draft_tokens || !a->temperature ||
+      !a->uniforms || !a->accept_len || !a->out_tokens)
+    return fail(SPECV_ERR_INVALID_ARG, "a required pointer is NULL");
+  const int es = elem_bytes(a->dtype);
+  if (!aligned(a->target_logits, es) || !aligned(a->draft_logits, es) ||
+      !aligned(a->draft_tokens, 4) || !aligned(a->temperature, 4) || !aligned(a->uniforms, 4) ||
+      !aligned(a->accept_len, 4) || !aligned(a->out_tokens, 4) || !aligned(a->p_draft, 4) ||
+      !aligned(a->q_draft, 4) || !aligned(a->row_status, 4))
+    return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
+  if (a->target_row_stride < V || a->draft_row_stride < V)
+    return fail(SPECV_ERR_INVALID_ARG, "row stride smaller than V");
+  if (B > 1 && (a->target_batch_stride < K * a->target_row_stride + V ||
+                a->draft_batch_stride < (draft_rows - 1) * a->draft_row_stride + V))
+    return fail(SPECV_ERR_INVALID_ARG, "batch stride too small for K+1 target / %d draft rows",
+                draft_rows);
+  return SPECV_OK;
+}
 
 }  // namespace
 
@@ -114,94 +216,128 @@ const char* specv_last_error(void) { return g_err.c_str(); }
 int32_t specv_last_launch_count(void) { return g_launches; }
 
 size_t specv_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t dtype) {
-  (void)V;
-  (void)dtype;
-  if (B <= 0 || K < 1) return 0;
-  return round_up(static_cast<size_t>(B) * (K + 1) * sizeof(UnitOut), 256);
+  if (B <= 0 || K < 1 || V < 1) return 0;
+  return plan_workspace(make_plan(B, K, V, 0, dtype));
 }
+
+namespace {
+
+specv_status run_verify(const specv_verify_args* a, void* workspace, size_t workspace_bytes,
+                        void* stream, int mode, int32_t F, int32_t* keys, float* key_logits,
+                        uint8_t* hit) {
+  const int32_t B = a->B, K = a->K, V = a->V;
+  const Plan pl = make_plan(B, K, V, mode == kModeSsd ? F : 0, a->dtype);
+  if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
+  const size_t need = plan_workspace(pl);
+  if (!workspace || workspace_bytes < need)
+    return fail(SPECV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  if (!aligned(workspace, 256)) return fail(SPECV_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  const int64_t units = static_cast<int64_t>(B) * (K + 1);
+  if (units * pl.nchunk > 0x7fffffffLL || static_cast<int64_t>(B) * pl.CB > 0x7fffffffLL)
+    return fail(SPECV_ERR_UNSUPPORTED, "B*(K+1) too large");
+  const int es = elem_bytes(a->dtype);
+  const bool vec = vec_ok(a->target_logits, a->target_batch_stride, a->target_row_stride, es) &&
+                   vec_ok(a->draft_logits, a->draft_batch_stride, a->draft_row_stride, es);
+  char* ws = static_cast<char*>(workspace);
+  ChunkRec* recs = reinterpret_cast<ChunkRec*>(ws);
+  float* cand_v = pl.cand_bytes ? reinterpret_cast<float*>(ws + pl.recs_bytes) : nullptr;
+  int32_t* cand_i = pl.cand_bytes ? reinterpret_cast<int32_t*>(ws + pl.recs_bytes + pl.cand_bytes) : nullptr;
+
+  StatsParams sp = {};
+  sp.zt = a->target_logits;
+  sp.t_bs = a->target_batch_stride;
+  sp.t_rs = a->target_row_stride;
+  sp.zd = a->draft_logits;
+  sp.d_bs = a->draft_batch_stride;
+  sp.d_rs = a->draft_row_stride;
+  sp.tokens = a->draft_tokens;
+  sp.temp = a->temperature;
+  sp.recs = recs;
+  sp.cand_v = cand_v;
+  sp.cand_i = cand_i;
+  sp.B = B;
+  sp.K = K;
+  sp.V = V;
+  sp.F = F;
+  sp.nchunk = static_cast<int32_t>(pl.nchunk);
+  sp.chunk = static_cast<int32_t>(pl.chunk);
+  sp.iters = pl.iters;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = mode == kModeSsd ? launch_stats<kModeSsd>(a->dtype, vec, units * pl.nchunk, s, sp)
+                                   : launch_stats<kModeVerify>(a->dtype, vec, units * pl.nchunk, s, sp);
+  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
+
+  DecideParams dp = {};
+  dp.zt = a->target_logits;
+  dp.t_bs = a->target_batch_stride;
+  dp.t_rs = a->target_row_stride;
+  dp.zd = a->draft_logits;
+  dp.d_bs = a->draft_batch_stride;
+  dp.d_rs = a->draft_row_stride;
+  dp.tokens = a->draft_tokens;
+  dp.temp = a->temperature;
+  dp.unif = a->uniforms;
+  dp.recs = recs;
+  dp.cand_v = cand_v;
+  dp.cand_i = cand_i;
+  dp.accept_len = a->accept_len;
+  dp.out_tokens = a->out_tokens;
+  dp.p_draft = a->p_draft;
+  dp.q_draft = a->q_draft;
+  dp.row_status = a->row_status;
+  dp.keys = keys;
+  dp.key_logits = key_logits;
+  dp.hit = hit;
+  dp.B = B;
+  dp.K = K;
+  dp.V = V;
+  dp.F = F;
+  dp.nchunk = static_cast<int32_t>(pl.nchunk);
+  dp.CB = pl.CB;
+  dp.L = static_cast<int32_t>(pl.L);
+  e = mode == kModeSsd ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, pl.smemB, s, dp)
+                       : launch_decide<kModeVerify>(a->dtype, vec, pl.CB, B, pl.smemB, s, dp);
+  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "decision launch: %s", cudaGetErrorString(e));
+  g_launches = 2;
+  return ok();
+}
+
+}  // namespace
 
 specv_status specv_verify(const specv_verify_args* a, void* workspace, size_t workspace_bytes,
                           void* stream) {
   g_launches = 0;
   if (!a) return fail(SPECV_ERR_INVALID_ARG, "args is NULL");
-  const int32_t B = a->B, K = a->K, V = a->V;
-  if (B < 0) return fail(SPECV_ERR_INVALID_ARG, "B=%d < 0", B);
-  if (K < 1 || K > 32) return fail(SPECV_ERR_INVALID_ARG, "K=%d outside [1, 32]", K);
-  if (V < 1) return fail(SPECV_ERR_INVALID_ARG, "V=%d < 1", V);
-  if (a->dtype != SPECV_BF16 && a->dtype != SPECV_FP32)
-    return fail(SPECV_ERR_INVALID_ARG, "dtype=%d is not SPECV_BF16 or SPECV_FP32", a->dtype);
-  if (B == 0) return ok();
-  if (!a->target_logits || !a->draft_logits || !a->draft_tokens || !a->temperature ||
-      !a->uniforms || !a->accept_len || !a->out_tokens)
-    return fail(SPECV_ERR_INVALID_ARG, "a required pointer is NULL");
-  const int es = elem_bytes(a->dtype);
-  if (!aligned(a->target_logits, es) || !aligned(a->draft_logits, es) ||
-      !aligned(a->draft_tokens, 4) || !aligned(a->temperature, 4) || !aligned(a->uniforms, 4) ||
-      !aligned(a->accept_len, 4) || !aligned(a->out_tokens, 4) || !aligned(a->p_draft, 4) ||
-      !aligned(a->q_draft, 4) || !aligned(a->row_status, 4))
+  specv_status st = check_verify_args(a, a->K);
+  if (st != SPECV_OK) return st;
+  if (a->B == 0) return ok();
+  return run_verify(a, workspace, workspace_bytes, stream, kModeVerify, 0, nullptr, nullptr,
+                    nullptr);
+}
+
+size_t specv_ssd_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
+  if (B <= 0 || K < 1 || V < 1 || F < 1) return 0;
+  return plan_workspace(make_plan(B, K, V, F, dtype));
+}
+
+specv_status specv_ssd_round(const specv_ssd_args* a, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  g_launches = 0;
+  if (!a) return fail(SPECV_ERR_INVALID_ARG, "args is NULL");
+  specv_status st = check_verify_args(&a->verify, a->verify.K + 1);
+  if (st != SPECV_OK) return st;
+  if (a->F < 1 || a->F > 32) return fail(SPECV_ERR_INVALID_ARG, "F=%d outside [1, 32]", a->F);
+  if (a->verify.B == 0) return ok();
+  if (!a->keys || !a->hit) return fail(SPECV_ERR_INVALID_ARG, "keys or hit is NULL");
+  if (!aligned(a->keys, 4) || !aligned(a->key_logits, 4))
     return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
-  if (a->target_row_stride < V || a->draft_row_stride < V)
-    return fail(SPECV_ERR_INVALID_ARG, "row stride smaller than V");
-  if (B > 1 && (a->target_batch_stride < K * a->target_row_stride + V ||
-                a->draft_batch_stride < (K - 1) * a->draft_row_stride + V))
-    return fail(SPECV_ERR_INVALID_ARG, "batch stride too small for K+1 target / K draft rows");
-  const size_t need = specv_verify_workspace_bytes(B, K, V, a->dtype);
-  if (!workspace || workspace_bytes < need)
-    return fail(SPECV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
-  if (!aligned(workspace, 256)) return fail(SPECV_ERR_WORKSPACE, "workspace not 256-byte aligned");
-
-  const int C = pick_cluster(V);
-  const int vw = vec_width(a->dtype);
-  const int64_t L = slice_len(V, C, vw);
-  const int64_t ntiles = ((L / vw) + kThreads - 1) / kThreads;
-  const size_t smem = static_cast<size_t>(ntiles) * kWarps * sizeof(float);
-  if (smem > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large for one cluster", V);
-  const int64_t units = static_cast<int64_t>(B) * (K + 1);
-  if (units * C > 0x7fffffffLL) return fail(SPECV_ERR_UNSUPPORTED, "B*(K+1) too large");
-
-  VerifyParams p;
-  p.zt = a->target_logits;
-  p.t_bs = a->target_batch_stride;
-  p.t_rs = a->target_row_stride;
-  p.zd = a->draft_logits;
-  p.d_bs = a->draft_batch_stride;
-  p.d_rs = a->draft_row_stride;
-  p.tokens = a->draft_tokens;
-  p.temp = a->temperature;
-  p.unif = a->uniforms;
-  p.units = static_cast<UnitOut*>(workspace);
-  p.B = B;
-  p.K = K;
-  p.V = V;
-  p.C = C;
-  p.L = static_cast<int32_t>(L);
-
-  const bool vec = vec_ok(a->target_logits, a->target_batch_stride, a->target_row_stride, es) &&
-                   vec_ok(a->draft_logits, a->draft_batch_stride, a->draft_row_stride, es);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (a->dtype == SPECV_BF16)
-    e = vec ? launch_clustered(verify_units_kernel<0, true>, C, units, smem, s, p)
-            : launch_clustered(verify_units_kernel<0, false>, C, units, smem, s, p);
-  else
-    e = vec ? launch_clustered(verify_units_kernel<1, true>, C, units, smem, s, p)
-            : launch_clustered(verify_units_kernel<1, false>, C, units, smem, s, p);
-  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
-  verify_finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(
-      p.units, a->draft_tokens, B, K, a->accept_len, a->out_tokens, a->p_draft, a->q_draft,
-      a->row_status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "finalize launch: %s", cudaGetErrorString(e));
-  g_launches = 2;
-  return ok();
+  return run_verify(&a->verify, workspace, workspace_bytes, stream, kModeSsd, a->F, a->keys,
+                    a->key_logits, a->hit);
 }
 
 size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
-  (void)V;
-  (void)F;
-  (void)dtype;
-  if (B <= 0 || K < 1) return 0;
-  return round_up(static_cast<size_t>(B) * (K + 1) * sizeof(int32_t), 256);
+  if (B <= 0 || K < 1 || V < 1 || F < 1) return 0;
+  return plan_workspace(make_plan(B, K, V, F, dtype));
 }
 
 specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace,
@@ -225,48 +361,50 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   if (a->draft_row_stride < V) return fail(SPECV_ERR_INVALID_ARG, "row stride smaller than V");
   if (B > 1 && a->draft_batch_stride < K * a->draft_row_stride + V)
     return fail(SPECV_ERR_INVALID_ARG, "batch stride too small for K+1 draft rows");
-  const size_t need = a->row_status ? specv_predict_workspace_bytes(B, K, V, F, a->dtype) : 0;
-  if (need && (!workspace || workspace_bytes < need))
+  const Plan pl = make_plan(B, K, V, F, a->dtype);
+  const size_t need = plan_workspace(pl);
+  if (!workspace || workspace_bytes < need)
     return fail(SPECV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
-  if (need && !aligned(workspace, 256))
-    return fail(SPECV_ERR_WORKSPACE, "workspace not 256-byte aligned");
-
-  const int C = pick_cluster(V);
-  const int vw = vec_width(a->dtype);
-  const int64_t L = slice_len(V, C, vw);
+  if (!aligned(workspace, 256)) return fail(SPECV_ERR_WORKSPACE, "workspace not 256-byte aligned");
   const int64_t units = static_cast<int64_t>(B) * (K + 1);
-  if (units * C > 0x7fffffffLL) return fail(SPECV_ERR_UNSUPPORTED, "B*(K+1) too large");
-  PredictParams p;
-  p.zd = a->draft_logits;
-  p.d_bs = a->draft_batch_stride;
-  p.d_rs = a->draft_row_stride;
-  p.tokens = a->draft_tokens;
-  p.keys = a->keys;
-  p.key_logits = a->key_logits;
-  p.unit_status = a->row_status ? static_cast<int32_t*>(workspace) : nullptr;
-  p.B = B;
-  p.K = K;
-  p.V = V;
-  p.F = F;
-  p.C = C;
-  p.L = static_cast<int32_t>(L);
+  if (units * pl.nchunk > 0x7fffffffLL) return fail(SPECV_ERR_UNSUPPORTED, "B*(K+1) too large");
   const bool vec = vec_ok(a->draft_logits, a->draft_batch_stride, a->draft_row_stride, es);
+  char* ws = static_cast<char*>(workspace);
+  StatsParams sp = {};
+  sp.zd = a->draft_logits;
+  sp.d_bs = a->draft_batch_stride;
+  sp.d_rs = a->draft_row_stride;
+  sp.tokens = a->draft_tokens;
+  sp.recs = reinterpret_cast<ChunkRec*>(ws);
+  sp.cand_v = reinterpret_cast<float*>(ws + pl.recs_bytes);
+  sp.cand_i = reinterpret_cast<int32_t*>(ws + pl.recs_bytes + pl.cand_bytes);
+  sp.B = B;
+  sp.K = K;
+  sp.V = V;
+  sp.F = F;
+  sp.nchunk = static_cast<int32_t>(pl.nchunk);
+  sp.chunk = static_cast<int32_t>(pl.chunk);
+  sp.iters = pl.iters;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (a->dtype == SPECV_BF16)
-    e = vec ? launch_clustered(predict_units_kernel<0, true>, C, units, 0, s, p)
-            : launch_clustered(predict_units_kernel<0, false>, C, units, 0, s, p);
-  else
-    e = vec ? launch_clustered(predict_units_kernel<1, true>, C, units, 0, s, p)
-            : launch_clustered(predict_units_kernel<1, false>, C, units, 0, s, p);
-  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "predict launch: %s", cudaGetErrorString(e));
-  g_launches = 1;
-  if (a->row_status) {
-    predict_finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(p.unit_status, B, K, a->row_status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "finalize launch: %s", cudaGetErrorString(e));
-    g_launches = 2;
-  }
+  cudaError_t e = launch_stats<kModePredict>(a->dtype, vec, units * pl.nchunk, s, sp);
+  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
+  PredictKeysParams kp = {};
+  kp.tokens = a->draft_tokens;
+  kp.recs = sp.recs;
+  kp.cand_v = sp.cand_v;
+  kp.cand_i = sp.cand_i;
+  kp.keys = a->keys;
+  kp.key_logits = a->key_logits;
+  kp.row_status = a->row_status;
+  kp.B = B;
+  kp.K = K;
+  kp.V = V;
+  kp.F = F;
+  kp.nchunk = static_cast<int32_t>(pl.nchunk);
+  predict_keys_kernel<<<B, kThreads, 0, s>>>(kp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "keys launch: %s", cudaGetErrorString(e));
+  g_launches = 2;
   return ok();
 }
 

@@ -43,6 +43,11 @@ struct Elem<0> {
   static constexpr int VW = 8;
   static constexpr int ES = 2;
   using Vec = uint4;
+  using Raw = unsigned short;
+  __device__ static Raw raw(const void* row, int64_t v) {
+    return __ldg(reinterpret_cast<const unsigned short*>(row) + v);
+  }
+  __device__ static Raw neg_inf_raw() { return 0xff80u; }
   __device__ static float scalar(const void* row, int64_t v) {
     unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + v);
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
@@ -83,6 +88,11 @@ struct Elem<1> {
   static constexpr int VW = 4;
   static constexpr int ES = 4;
   using Vec = float4;
+  using Raw = float;
+  __device__ static Raw raw(const void* row, int64_t v) {
+    return __ldg(reinterpret_cast<const float*>(row) + v);
+  }
+  __device__ static Raw neg_inf_raw() { return neg_inf(); }
   __device__ static float scalar(const void* row, int64_t v) {
     return __ldg(reinterpret_cast<const float*>(row) + v);
   }
@@ -113,6 +123,71 @@ __device__ __forceinline__ typename Elem<DT>::Vec load_vec(const void* row, int6
   const int64_t v = v0 + static_cast<int64_t>(j) * E::VW;
   if (VEC && v + E::VW <= v1) return E::vec(row, v);
   return E::gather(row, v, v1);
+}
+
+// ---- shared-memory addresses, mbarriers, 1-D bulk (TMA) copies, cluster barrier
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`, giving up after about a second of device
+// time (or 2^26 polls): returns false on timeout instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0; it < (1u << 26); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > 2000000000LL) break;
+  }
+  return false;
+}
+
+// Split cluster barrier: arrive (release) now, wait (acquire) later.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
 }
 
 __device__ __forceinline__ float warp_sum(float x) {

@@ -1,0 +1,291 @@
+// Device building blocks shared by the row-statistics and decision kernels:
+// online softmax statistics, first argmax, warp-distributed top-F lists and
+// deterministic warp reductions.
+#pragma once
+
+#include <climits>
+
+#include "specv_common.cuh"
+
+namespace specv {
+
+constexpr int kMaxF = 32;
+
+template <int VW>
+struct Soft {  // online (max, sum) with VW partial sums for accuracy
+  float m;
+  float s[VW];
+  __device__ __forceinline__ void init() {
+    m = kNegMax;
+#pragma unroll
+    for (int k = 0; k < VW; ++k) s[k] = 0.f;
+  }
+  __device__ __forceinline__ void add(const float (&z)[VW], float c) {
+    float vm = z[0];
+#pragma unroll
+    for (int k = 1; k < VW; ++k) vm = fmaxf(vm, z[k]);  // NaN ignored here
+    if (vm > m) {
+      const float f = ex2((m - vm) * c);
+#pragma unroll
+      for (int k = 0; k < VW; ++k) s[k] *= f;
+      m = vm;
+    }
+#pragma unroll
+    for (int k = 0; k < VW; ++k) s[k] += ex2((z[k] - m) * c);  // NaN -> sum NaN
+  }
+  __device__ __forceinline__ float total() const {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < VW; ++k) t += s[k];
+    return t;
+  }
+};
+
+__device__ __forceinline__ void soft_merge(float& m, float& s, float m2, float s2, float c) {
+  const float M = fmaxf(m, m2);
+  s = s * ex2((m - M) * c) + s2 * ex2((m2 - M) * c);
+  m = M;
+}
+
+struct Arg {  // first argmax
+  float best;
+  int32_t idx;
+  int32_t bad;
+  __device__ __forceinline__ void init() {
+    best = neg_inf();
+    idx = INT_MAX;
+    bad = 0;
+  }
+  template <int VW>
+  __device__ __forceinline__ void add(const float (&z)[VW], int32_t base) {
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      bad |= !(z[k] < pos_inf());  // NaN or +inf
+      if (z[k] > best) {
+        best = z[k];
+        idx = base + k;
+      }
+    }
+  }
+  __device__ __forceinline__ void merge(float b2, int32_t i2, int32_t bad2) {
+    if (b2 > best || (b2 == best && i2 < idx)) {
+      best = b2;
+      idx = i2;
+    }
+    bad |= bad2;
+  }
+};
+
+__device__ __forceinline__ bool key_beats(float av, int32_t ai, float bv, int32_t bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// Sorted top-F list over a warp (lane f holds entry f); the order is (logit
+// descending, index ascending); empty entries are (-inf, INT_MAX).
+struct WarpTopF {
+  float v;
+  int32_t i;
+  float tv;  // entry F-1: the admission threshold, same in every lane
+  int32_t ti;
+  __device__ __forceinline__ void init() {
+    v = neg_inf();
+    i = INT_MAX;
+    tv = neg_inf();
+    ti = INT_MAX;
+  }
+  __device__ __forceinline__ void insert(float cv, int32_t ci, int F, int lane) {
+    const bool ahead = lane < F && key_beats(v, i, cv, ci);
+    const int pos = __popc(__ballot_sync(0xffffffffu, ahead));
+    if (pos >= F) return;
+    const float uv = __shfl_up_sync(0xffffffffu, v, 1);
+    const int32_t ui = __shfl_up_sync(0xffffffffu, i, 1);
+    if (lane > pos && lane < F) {
+      v = uv;
+      i = ui;
+    } else if (lane == pos) {
+      v = cv;
+      i = ci;
+    }
+    tv = __shfl_sync(0xffffffffu, v, F - 1);
+    ti = __shfl_sync(0xffffffffu, i, F - 1);
+  }
+};
+
+// Merge n <= 32 sorted lists lv[r][0..F-1] (shared memory) into out[0..F-1];
+// lane r follows list r.  Called by one full warp.
+__device__ __forceinline__ void merge_lists(const float (*lv)[kMaxF], const int32_t (*li)[kMaxF],
+                                            int n, int F, int lane, float* outv, int32_t* outi) {
+  int ptr = 0;
+  float hv = neg_inf();
+  int32_t hi = INT_MAX;
+  if (lane < n) {
+    hv = lv[lane][0];
+    hi = li[lane][0];
+  }
+  for (int f = 0; f < F; ++f) {
+    float bv = hv;
+    int32_t bi = hi;
+    int bl = lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      if (key_beats(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+        bl = ol;
+      }
+    }
+    if (lane == 0) {
+      outv[f] = bv;
+      outi[f] = bi;
+    }
+    if (lane == bl && bi != INT_MAX) {
+      ++ptr;
+      if (ptr < F) {
+        hv = lv[lane][ptr];
+        hi = li[lane][ptr];
+      } else {
+        hv = neg_inf();
+        hi = INT_MAX;
+      }
+    }
+  }
+}
+
+// (max, sum) of a warp's online-softmax partials: the warp max first, then one
+// rescale per lane and a plain sum tree (no exponential per tree step).  The
+// result is in every lane.  Lanes without data hold (kNegMax, 0).
+__device__ __forceinline__ void warp_soft_all(float& m, float& s, float c) {
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float t = s * ex2((m - M) * c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  m = M;
+  s = t;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_max_all(T x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ double warp_dsum_all(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ void warp_arg_all(float& v, int32_t& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int32_t oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ov > v || (ov == v && oi < i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// ---- CTA-wide top-F selection by rank counting ----------------------------
+// Keys are (value, index) under key_beats; all indices are distinct, so the
+// ranks of distinct entries are distinct.  Empty entries are (-inf, INT_MAX).
+
+constexpr int kCandCap = 512;  // candidates one CTA ranks at once
+
+struct KeyScratch {  // shared-memory scratch of select_keys
+  float v[kCandCap];
+  int32_t i[kCandCap];
+  float out_v[kMaxF];
+  int32_t out_i[kMaxF];
+  float thr_v;
+  int32_t thr_i;
+  int count;
+};
+
+// Top-F of n candidates (cand_v[e], cand_i[e], e < n, in global or shared
+// memory) by rank counting over the ones that reach the threshold key
+// (tv, ti); candidates below it are known not to be in the top-F.  All threads
+// of the CTA call it; the result is in S.out_v / S.out_i (F entries, sorted).
+__device__ __forceinline__ void select_top_f(const float* cand_v, const int32_t* cand_i, int n,
+                                             float tv, int32_t ti, int F, KeyScratch& S) {
+  if (threadIdx.x == 0) S.count = 0;
+  if (threadIdx.x < F) {
+    S.out_v[threadIdx.x] = neg_inf();
+    S.out_i[threadIdx.x] = INT_MAX;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const float v = cand_v[e];
+    const int32_t i = cand_i[e];
+    if (i != INT_MAX && !key_beats(tv, ti, v, i)) {
+      const int slot = atomicAdd(&S.count, 1);
+      if (slot < kCandCap) {
+        S.v[slot] = v;
+        S.i[slot] = i;
+      }
+    }
+  }
+  __syncthreads();
+  const int m = S.count;
+  if (m <= kCandCap) {
+    for (int e = threadIdx.x; e < m; e += blockDim.x) {
+      const float v = S.v[e];
+      const int32_t i = S.i[e];
+      int rank = 0;
+      for (int o = 0; o < m; ++o) rank += key_beats(S.v[o], S.i[o], v, i);
+      if (rank < F) {
+        S.out_v[rank] = v;
+        S.out_i[rank] = i;
+      }
+    }
+  } else {  // too many ties at the threshold: rank against every candidate
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const float v = cand_v[e];
+      const int32_t i = cand_i[e];
+      if (i == INT_MAX) continue;
+      int rank = 0;
+      for (int o = 0; o < n && rank < F; ++o) rank += key_beats(cand_v[o], cand_i[o], v, i);
+      if (rank < F) {
+        S.out_v[rank] = v;
+        S.out_i[rank] = i;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Top-F over n lists of F sorted entries (list r at cv[r*F .. r*F+F-1]).  The
+// F-th best list head bounds the answer from below (F heads reach it), so
+// only entries reaching it are ranked.  All threads of the CTA call it.
+__device__ __forceinline__ void select_keys(const float* cv, const int32_t* ci, int nlists, int F,
+                                            KeyScratch& S) {
+  if (threadIdx.x == 0) {
+    S.thr_v = neg_inf();
+    S.thr_i = INT_MAX;
+  }
+  __syncthreads();
+  if (nlists >= F) {
+    for (int r = threadIdx.x; r < nlists; r += blockDim.x) {
+      const float v = cv[static_cast<int64_t>(r) * F];
+      const int32_t i = ci[static_cast<int64_t>(r) * F];
+      int rank = 0;
+      for (int o = 0; o < nlists; ++o)
+        rank += key_beats(cv[static_cast<int64_t>(o) * F], ci[static_cast<int64_t>(o) * F], v, i);
+      if (rank == F - 1) {
+        S.thr_v = v;
+        S.thr_i = i;
+      }
+    }
+  }
+  __syncthreads();
+  select_top_f(cv, ci, nlists * F, S.thr_v, S.thr_i, F, S);
+}
+
+}  // namespace specv

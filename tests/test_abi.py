@@ -85,7 +85,7 @@ def test_verify_null_args(lib):
 def test_verify_workspace_checks(lib):
     a = _args()
     need = lib.specv_verify_workspace_bytes(2, 3, 100, sv.SPECV_FP32)
-    assert need >= 2 * 4 * 32 and need % 256 == 0
+    assert need >= 2 * 4 * 48 and need % 256 == 0
     assert lib.specv_verify(ctypes.byref(a), None, need, None) == sv.SPECV_ERR_WORKSPACE
     assert lib.specv_verify(ctypes.byref(a), ctypes.c_void_p(0x100000), need - 1, None) == sv.SPECV_ERR_WORKSPACE
     assert lib.specv_verify(ctypes.byref(a), ctypes.c_void_p(0x100010), need, None) == sv.SPECV_ERR_WORKSPACE
@@ -126,3 +126,49 @@ def test_product_path_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "specv_oracle" not in text, f
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The binding's ctypes structs have the C header's sizes and offsets."""
+    import subprocess
+    src = tmp_path / "layout.c"
+    src.write_text(r'''
+#include <stddef.h>
+#include <stdio.h>
+#include "specv.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(specv_verify_args),
+         offsetof(specv_verify_args, target_logits), offsetof(specv_verify_args, draft_tokens),
+         offsetof(specv_verify_args, row_status), sizeof(specv_ssd_args),
+         offsetof(specv_ssd_args, keys), sizeof(specv_predict_args),
+         offsetof(specv_predict_args, row_status));
+  return 0;
+}
+''')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    want = [ctypes.sizeof(sv.VerifyArgs), sv.VerifyArgs.target_logits.offset,
+            sv.VerifyArgs.draft_tokens.offset, sv.VerifyArgs.row_status.offset,
+            ctypes.sizeof(sv.SsdArgs), sv.SsdArgs.keys.offset, ctypes.sizeof(sv.PredictArgs),
+            sv.PredictArgs.row_status.offset]
+    assert got == want
+
+
+def test_ssd_round_rejects_bad_arguments(lib):
+    a = _args()
+    s = sv.SsdArgs(a, 6, 0x10000, 0, 0x10000)
+    for field, val in (("F", 0), ("F", 33), ("keys", None), ("hit", None)):
+        q = sv.SsdArgs.from_buffer_copy(s)
+        setattr(q, field, val)
+        assert lib.specv_ssd_round(ctypes.byref(q), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG, field
+    q = sv.SsdArgs.from_buffer_copy(s)
+    q.verify.draft_batch_stride = 300  # needs K+1 = 4 draft rows of stride 100
+    assert lib.specv_ssd_round(ctypes.byref(q), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+
+
+def test_unsupported_vocabulary_size(lib):
+    V = 2_000_000_000  # per-CTA segment table of the decision kernel would not fit
+    a = _args(V=V, target_row_stride=V, draft_row_stride=V,
+              target_batch_stride=4 * V, draft_batch_stride=3 * V)
+    assert lib.specv_verify(ctypes.byref(a), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_UNSUPPORTED

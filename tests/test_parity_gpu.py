@@ -320,3 +320,100 @@ def test_repeated_calls_are_deterministic(sv):
     b = gpu_verify(sv, data)
     for k in a:
         assert np.array_equal(a[k], b[k]), k
+
+
+# ---------------------------------------------------------------------------
+# the fused SSD round: verification + top-F keys + hit in one pass
+
+def oracle_ssd(olib, data, F):
+    o = oracle_verify(olib, data)
+    op = oracle.predict(data["draft"], data["tokens"], F, nthreads=0, lib=olib)
+    o["status"] = o["status"] | op["status"]
+    err = (o["status"] & oracle.ROW_ERRORS) != 0
+    # a flagged batch row of an SSD round has no outcome (header contract)
+    o["accept_len"][err] = 0
+    o["out_tokens"][err] = -1
+    o["p"][err] = 0.0
+    o["q"][err] = 0.0
+    o["boundary"][err] = 0
+    keys, kl = op["keys"].copy(), op["key_logits"].copy()
+    keys[err] = -1
+    kl[err] = -np.inf
+    return o, keys, kl
+
+
+def gpu_ssd(sv, data, F, target=None, draft=None):
+    spec = data["spec"]
+    tgt = to_dev(data["target"], spec.dtype) if target is None else target
+    dft = to_dev(data["draft"], spec.dtype) if draft is None else draft
+    out = sv.specv_ssd_round(tgt, dft, to_dev(data["tokens"], None),
+                             to_dev(data["temperature"], None), to_dev(data["uniforms"], None), F)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def compare_ssd(olib, g, o, keys, kl, temps, label):
+    compare_verify(g, o, temps, label)
+    assert np.array_equal(g["keys"], keys), label
+    assert np.array_equal(g["key_logits"], kl), label
+    # the hit flag of the GPU's own outcome, by the oracle's definition
+    assert np.array_equal(g["hit"], oracle.check_hit(keys, g["accept_len"], g["out_tokens"], lib=olib)), label
+
+
+def test_ssd_round_cfg4_fused(sv, olib):
+    spec = wl.SPECS["cfg4"]
+    data = wl.generate(spec)
+    g = gpu_ssd(sv, data, spec.F)
+    o, keys, kl = oracle_ssd(olib, data, spec.F)
+    compare_ssd(olib, g, o, keys, kl, data["temperature"], "ssd cfg4")
+    print(f"ssd cfg4: hit rate {g['hit'].mean():.3f}")
+
+
+def test_ssd_round_cfg5_full_size_sampled(sv, olib):
+    """Config 5 sizes with K+1 draft rows and F=6: the benchmark's workload."""
+    import dataclasses
+    spec = dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd", ssd=True, F=6)
+    data = wl.generate(spec)
+    g = gpu_ssd(sv, data, spec.F)
+    rows = np.random.default_rng(1).choice(spec.B, 16, replace=False)
+    sub = {k: (v[rows] if isinstance(v, np.ndarray) and v.shape[:1] == (spec.B,) else v)
+           for k, v in data.items()}
+    o, keys, kl = oracle_ssd(olib, sub, spec.F)
+    gs = {k: v[rows] for k, v in g.items()}
+    compare_ssd(olib, gs, o, keys, kl, sub["temperature"], "ssd cfg5")
+    print(f"ssd cfg5: hit rate (all rows) {g['hit'].mean():.3f}")
+
+
+@pytest.mark.parametrize("B,K,V,dtype,F", [
+    (3, 2, 5, wl.FP32, 3),
+    (4, 3, 33, wl.BF16, 6),
+    (4, 4, 4097, wl.FP32, 1),
+    (3, 5, 20001, wl.BF16, 32),
+    (3, 3, 70003, wl.FP32, 8),
+    (2, 2, 152064, wl.BF16, 6),
+])
+def test_ssd_round_ragged(sv, olib, B, K, V, dtype, F):
+    spec = wl.custom(f"ssd{V}", B=B, K=K, V=V, dtype=dtype, temps=(0.0, 0.7, 1.0),
+                     sigma_d=(0.3, 2.0), ssd=True, F=F, seed=wl.SEED_BASE + 8000 + V)
+    data = wl.generate(spec)
+    g = gpu_ssd(sv, data, F)
+    o, keys, kl = oracle_ssd(olib, data, F)
+    compare_ssd(olib, g, o, keys, kl, data["temperature"], f"ssd V={V}")
+
+
+@pytest.mark.parametrize("dtype", [wl.FP32, wl.BF16])
+def test_ssd_round_edge_cases(sv, olib, dtype):
+    base = _edge_batch(wl.FP32)
+    zt, zd = base["target"], base["draft"]
+    K = zd.shape[1]
+    rng = np.random.default_rng(3)
+    extra = (zt[:, K:K + 1] + rng.standard_normal((zt.shape[0], 1, zt.shape[2]))).astype(np.float32)
+    zd = np.concatenate([zd, extra], axis=1)
+    zd[0, K, 4] = np.nan  # NaN only in draft row K: flags the batch row in an SSD round
+    if dtype == wl.BF16:
+        zt, zd = wl.f32_to_bf16_bits(zt), wl.f32_to_bf16_bits(zd)
+    data = dict(base, target=zt, draft=zd, spec=wl.custom("edge", B=zt.shape[0], K=K, V=zt.shape[2], dtype=dtype))
+    g = gpu_ssd(sv, data, 4)
+    o, keys, kl = oracle_ssd(olib, data, 4)
+    compare_ssd(olib, g, o, keys, kl, data["temperature"], "ssd edge")
+    assert g["row_status"][0] == oracle.ROW_NONFINITE and (g["keys"][0] == -1).all()
