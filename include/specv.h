@@ -116,6 +116,29 @@ specv_status specv_verify(const specv_verify_args* args, void* workspace,
                           size_t workspace_bytes, void* stream);
 
 /*
+ * Verification exactly as specv_verify, without a workspace argument.  The
+ * pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory where they call the library -- a server that reserved
+ * all free GPU memory for its KV cache at start-up, or a host language with no
+ * CUDA allocator binding.  It calls no allocator at all.
+ *
+ * Its scratch is a fixed array of SPECV_NOALLOC_SCRATCH_BYTES bytes of device
+ * memory built into the library; every GPU that loads the library holds one
+ * copy until the process exits.  A call whose specv_verify_workspace_bytes()
+ * exceeds it returns SPECV_ERR_UNSUPPORTED before any launch (8 MiB covers,
+ * e.g., B = 256, K = 8, V = 152064 fp32 with a wide margin).
+ *
+ * The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls on a device share the one
+ * scratch array, which keeps the last call's contents (nothing in it needs to
+ * start at zero): calls that can overlap on the GPU -- other streams, other
+ * host threads -- race and corrupt each other's results, so serialise them.
+ */
+#define SPECV_NOALLOC_SCRATCH_BYTES (8u << 20)
+specv_status specv_verify_noalloc(const specv_verify_args* args, void* stream);
+
+/*
  * One SSD round in a single pass over the logits ("Speculative Speculative
  * Decoding" §3.1 Algorithm 1, §4.1.1): verification exactly as specv_verify,
  * outcome keys exactly as specv_predict_outcomes (so draft_logits must hold

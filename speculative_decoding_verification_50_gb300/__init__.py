@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specv_verify_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
     lib.specv_verify.restype = ctypes.c_int
     lib.specv_verify.argtypes = [ctypes.POINTER(VerifyArgs), _P, ctypes.c_size_t, _P]
+    lib.specv_verify_noalloc.restype = ctypes.c_int
+    lib.specv_verify_noalloc.argtypes = [ctypes.POINTER(VerifyArgs), _P]
     lib.specv_ssd_workspace_bytes.restype = ctypes.c_size_t
     lib.specv_ssd_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
     lib.specv_ssd_round.restype = ctypes.c_int
@@ -173,6 +175,20 @@ def specv_verify(target, draft, draft_tokens, temperature, uniforms, *, accept_l
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=target.device)
     _check(lib.specv_verify(ctypes.byref(args), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return outs
+
+
+def specv_verify_noalloc(target, draft, draft_tokens, temperature, uniforms, *, accept_len=None,
+                         out_tokens=None, p_draft=None, q_draft=None, row_status=None,
+                         stream=None) -> dict:
+    """specv_verify without a workspace: the library's built-in scratch is used
+    (for callers that cannot allocate device memory where they call it; see
+    include/specv.h).  Calls that may overlap on the GPU must be serialised."""
+    lib = load_library()
+    B, K = draft_tokens.shape
+    args, outs = _verify_args(target, draft, draft_tokens, temperature, uniforms, K, accept_len,
+                              out_tokens, p_draft, q_draft, row_status)
+    _check(lib.specv_verify_noalloc(ctypes.byref(args), _stream(stream)))
     return outs
 
 

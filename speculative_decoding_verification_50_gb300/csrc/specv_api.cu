@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <mutex>
 #include <string>
 
 #include "specv.h"
@@ -429,3 +430,63 @@ specv_status specv_check_hit(int32_t B, int32_t K, int32_t F, const int32_t* key
 }
 
 }  // extern "C"
+
+// ---- verification with the library's own scratch (no workspace argument) ----
+//
+// For callers that cannot allocate device memory where they call us: a server
+// that reserved all free GPU memory for its KV cache at start-up, or a host
+// language with no CUDA allocator binding.  The scratch (kernel A's per-chunk
+// records) lives in a fixed array in device memory, one copy per GPU that
+// loads this library, held until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = SPECV_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per
+// device (with that device current) and cached.
+specv_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(SPECV_ERR_UNSUPPORTED, "device index %d beyond %d", dev, kNoAllocMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(SPECV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return SPECV_OK;
+}
+
+}  // namespace
+
+extern "C" specv_status specv_verify_noalloc(const specv_verify_args* a, void* stream) {
+  g_launches = 0;
+  if (!a) return fail(SPECV_ERR_INVALID_ARG, "args is NULL");
+  specv_status st = check_verify_args(a, a->K);
+  if (st != SPECV_OK) return st;
+  if (a->B == 0) return ok();
+  const size_t need = specv_verify_workspace_bytes(a->B, a->K, a->V, a->dtype);
+  if (need > kNoAllocScratchBytes)
+    return fail(SPECV_ERR_UNSUPPORTED,
+                "this call needs %zu bytes of scratch but the built-in scratch holds %zu "
+                "(SPECV_NOALLOC_SCRATCH_BYTES); call specv_verify with a workspace instead",
+                need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  st = noalloc_scratch(&ws);
+  if (st != SPECV_OK) return st;
+  // Every record kernel B reads is written by kernel A earlier in this same
+  // call, so nothing in the scratch has to start at zero.
+  return run_verify(a, ws, kNoAllocScratchBytes, stream, kModeVerify, 0, nullptr, nullptr,
+                    nullptr);
+}
