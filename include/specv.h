@@ -65,6 +65,11 @@ typedef enum { SPECV_BF16 = 0, SPECV_FP32 = 1 } specv_dtype;
 #define SPECV_ROW_FALLBACK 8  /* informational: the bonus draw fell back
                                  (zero residual mass -> drawn from p_n; or
                                  rounding left no index -> last v with r>0) */
+#define SPECV_ROW_DEVICE_TIMEOUT 16 /* a bulk copy of this row's logits into
+                                 shared memory did not complete within about
+                                 a second of device time; the kernel gave up on
+                                 the row instead of waiting forever (not
+                                 expected on a healthy GPU) */
 
 /*
  * Verification of B independent batch rows ("Speculative Speculative
@@ -209,6 +214,13 @@ const char* specv_last_error(void);
 /* Number of kernel launches the most recent successful call on this host
  * thread enqueued (for launch accounting in benchmarks). */
 int32_t specv_last_launch_count(void);
+
+/* Measurement hook.  While `event` (a cudaEvent_t created by the caller) is
+ * set, every specv_verify / specv_ssd_round / specv_predict_outcomes call made
+ * by this host thread records it on its stream between the row-statistics
+ * kernel and the decision kernel, so the two can be timed apart.  NULL clears
+ * it.  The library does not create, own or destroy the event. */
+void specv_set_split_event(void* event);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_PKG, "libspecv.so")
 
 SPECV_OK, SPECV_ERR_INVALID_ARG, SPECV_ERR_UNSUPPORTED, SPECV_ERR_CUDA, SPECV_ERR_WORKSPACE = range(5)
 SPECV_BF16, SPECV_FP32 = 0, 1
-ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK = 1, 2, 4, 8
+ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK, ROW_DEVICE_TIMEOUT = 1, 2, 4, 8, 16
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -90,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specv_last_error.argtypes = []
     lib.specv_last_launch_count.restype = _I32
     lib.specv_last_launch_count.argtypes = []
+    lib.specv_set_split_event.restype = None
+    lib.specv_set_split_event.argtypes = [_P]
     _lib = lib
     return lib
 
@@ -117,6 +119,14 @@ def _stream(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def specv_set_split_event(event) -> None:
+    """Record `event` (a torch.cuda.Event, already recorded once so that it
+    exists, or None) between the library's two kernels on later calls from
+    this thread (measurement hook; see include/specv.h)."""
+    handle = None if event is None else ctypes.c_void_p(event.cuda_event)
+    load_library().specv_set_split_event(handle)
 
 
 def last_launch_count() -> int:

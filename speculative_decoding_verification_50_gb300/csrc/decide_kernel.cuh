@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       const bool d_full = lane < K;  // draft rows that are normalised
       const bool d_any = (MODE != kModeVerify) || lane < K;
       if (greedy) {
-        nf = q.bad || q.it == INT_MAX || (d_full && q.id == INT_MAX);
+        nf = (q.bad & 1) || q.it == INT_MAX || (d_full && q.id == INT_MAX);
       } else {
         nf = !(q.St >= 1.0) || q.Mt == kNegMax;
         if (d_full) nf |= !(q.Sd >= 1.0) || q.Md == kNegMax;
@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
     const int x = acc_lane ? P.tokens[static_cast<int64_t>(b) * K + lane] : -1;
     int status = temp_ok ? 0 : kBadTemp;
     if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
+    if (__any_sync(0xffffffffu, lane <= K && (ps[lane].bad & 2))) status |= kTimeout;
     if (__any_sync(0xffffffffu, acc_lane && (x < 0 || x >= P.V))) status |= kBadToken;
     const bool ok = !(status & kErrors);
     bool accept = false;
@@ -504,10 +505,11 @@ __global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKey
     if (threadIdx.x == 0) row_bad = 0;
     __syncthreads();
     for (int q = threadIdx.x; q < P.nchunk; q += kThreads)
-      if (P.recs[u * P.nchunk + q].bad) row_bad = 1;
+      if (P.recs[u * P.nchunk + q].bad) row_bad |= P.recs[u * P.nchunk + q].bad;
     const int x = (k < K) ? P.tokens[static_cast<int64_t>(b) * K + k] : 0;
     select_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F, P.nchunk, F, KS);
-    const int status = (row_bad ? kNonFinite : 0) | ((x < 0 || x >= P.V) ? kBadToken : 0);
+    const int status = ((row_bad & 1) ? kNonFinite : 0) | ((row_bad & 2) ? kTimeout : 0) |
+                       ((x < 0 || x >= P.V) ? kBadToken : 0);
     if (threadIdx.x < F) {
       const bool good = status == 0 && KS.out_i[threadIdx.x] != INT_MAX;
       P.keys[u * F + threadIdx.x] = good ? KS.out_i[threadIdx.x] : -1;

@@ -15,6 +15,13 @@ namespace {
 
 thread_local std::string g_err;
 thread_local int32_t g_launches = 0;
+thread_local cudaEvent_t g_split_event = nullptr;  // measurement hook
+
+// Records the caller's split event (if any) between the statistics kernel and
+// the decision kernel.
+cudaError_t record_split(cudaStream_t s) {
+  return g_split_event ? cudaEventRecord(g_split_event, s) : cudaSuccess;
+}
 
 specv_status fail(specv_status s, const char* fmt, ...) {
   char buf[512];
@@ -124,12 +131,18 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
   const int64_t units = static_cast<int64_t>(B > 0 ? B : 0) * (K + 1);
   // Loop trips per kernel-A CTA: long chunks amortise the per-CTA reductions;
   // halve them while the grid would be under about two waves (4 CTAs per SM).
-  pl.iters = 8;
+  // SPECV_ITERS (1..64) fixes the trip count, for tuning runs.
+  static int env_iters = -2;
+  if (env_iters == -2) {
+    const char* e = getenv("SPECV_ITERS");
+    env_iters = e ? atoi(e) : -1;
+  }
+  pl.iters = (env_iters >= 1 && env_iters <= 64) ? env_iters : 8;
   const int64_t want = 8LL * sm_count();
   for (;;) {
     pl.chunk = static_cast<int64_t>(pl.iters) * kVecs * kThreads * vw;
     pl.nchunk = (static_cast<int64_t>(V) + pl.chunk - 1) / pl.chunk;
-    if (pl.iters == 1 || units * pl.nchunk >= want) break;
+    if (pl.iters == 1 || env_iters >= 1 || units * pl.nchunk >= want) break;
     pl.iters /= 2;
   }
   pl.CB = pick_cluster(B, V, vw);
@@ -146,18 +159,27 @@ size_t plan_workspace(const Plan& pl) { return pl.recs_bytes + 2 * pl.cand_bytes
 constexpr size_t kMaxSegSmem = 200 * 1024;
 
 template <typename Kern, typename Params>
-cudaError_t launch_plain(Kern k, int64_t blocks, cudaStream_t s, const Params& p) {
-  k<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(p);
+cudaError_t launch_plain(Kern k, int64_t blocks, size_t smem, cudaStream_t s, const Params& p) {
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  k<<<static_cast<unsigned>(blocks), kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
+
+// Shared memory of the TMA ring (aligned rows only): kStages stages of one
+// trip of two rows.
+constexpr size_t kRingSmem = static_cast<size_t>(kStages) * 2 * kTripBytes;
 
 template <int MODE>
 cudaError_t launch_stats(int dtype, bool vec, int64_t blocks, cudaStream_t s, const StatsParams& p) {
   if (dtype == SPECV_BF16)
-    return vec ? launch_plain(stats_kernel<0, true, MODE>, blocks, s, p)
-               : launch_plain(stats_kernel<0, false, MODE>, blocks, s, p);
-  return vec ? launch_plain(stats_kernel<1, true, MODE>, blocks, s, p)
-             : launch_plain(stats_kernel<1, false, MODE>, blocks, s, p);
+    return vec ? launch_plain(stats_kernel<0, true, MODE>, blocks, kRingSmem, s, p)
+               : launch_plain(stats_kernel<0, false, MODE>, blocks, 0, s, p);
+  return vec ? launch_plain(stats_kernel<1, true, MODE>, blocks, kRingSmem, s, p)
+             : launch_plain(stats_kernel<1, false, MODE>, blocks, 0, s, p);
 }
 
 template <int MODE>
@@ -216,6 +238,8 @@ const char* specv_last_error(void) { return g_err.c_str(); }
 
 int32_t specv_last_launch_count(void) { return g_launches; }
 
+void specv_set_split_event(void* event) { g_split_event = static_cast<cudaEvent_t>(event); }
+
 size_t specv_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t dtype) {
   if (B <= 0 || K < 1 || V < 1) return 0;
   return plan_workspace(make_plan(B, K, V, 0, dtype));
@@ -267,6 +291,8 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   cudaError_t e = mode == kModeSsd ? launch_stats<kModeSsd>(a->dtype, vec, units * pl.nchunk, s, sp)
                                    : launch_stats<kModeVerify>(a->dtype, vec, units * pl.nchunk, s, sp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
+  e = record_split(s);
+  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "split event: %s", cudaGetErrorString(e));
 
   DecideParams dp = {};
   dp.zt = a->target_logits;
@@ -389,6 +415,8 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_stats<kModePredict>(a->dtype, vec, units * pl.nchunk, s, sp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
+  e = record_split(s);
+  if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "split event: %s", cudaGetErrorString(e));
   PredictKeysParams kp = {};
   kp.tokens = a->draft_tokens;
   kp.recs = sp.recs;

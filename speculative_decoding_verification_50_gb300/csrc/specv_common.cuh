@@ -18,7 +18,8 @@ enum : int32_t {
   kNonFinite = 2,
   kBadTemp = 4,
   kFallback = 8,
-  kErrors = kBadToken | kNonFinite | kBadTemp
+  kTimeout = 16,  // a staged bulk copy did not land within the wait bound
+  kErrors = kBadToken | kNonFinite | kBadTemp | kTimeout
 };
 
 constexpr float kNegMax = -3.402823466e+38f;  // lowest finite float

@@ -33,7 +33,8 @@ struct ChunkRec {        // 48 bytes per (unit, chunk)
   float mt, st, md, sd;  // temperature rows: max and sum of 2^((z-max)c)
   float bt, bd;          // greedy rows: best logit
   int32_t it, id;        // greedy rows: first index of the best logit
-  int32_t bad;           // greedy rows: NaN or +inf seen (T > 0: shows as a NaN sum)
+  int32_t bad;           // bit 0: NaN or +inf seen in a greedy row (T > 0: shows
+                         // as a NaN sum); bit 1: a staged copy did not land in time
   int32_t pad[3];
 };
 static_assert(sizeof(ChunkRec) == 48, "ChunkRec layout");
@@ -111,6 +112,112 @@ __device__ __forceinline__ void stream_chunk(const void* rowt, const void* rowd,
   }
 }
 
+// ---- TMA ring (16-byte aligned rows) ----------------------------------------
+// A trip is kVecs*256 16-byte vectors of each row; stage s of the ring holds
+// one trip of every streamed row.  Thread 0 keeps up to kStages trips in
+// flight as 1-D bulk copies completing on the stage's mbarrier; all threads
+// consume a stage from shared memory, meet at a CTA barrier, and thread 0
+// refills the stage with the trip kStages ahead.  The vector -> thread mapping
+// is that of the register path, so results are identical.
+constexpr int kStages = 4;
+constexpr int kTripBytes = kVecs * kThreads * 16;  // per row per trip (8 KB)
+
+struct Ring {
+  uint64_t full[kStages];
+};
+
+// Issue trip t of the chunk into stage t % kStages.  Bytes past the last whole
+// 16-byte unit of the chunk are left to the consumers (plain loads).
+__device__ __forceinline__ void ring_issue(Ring& R, unsigned char* stages, int t,
+                                          const char* rowt, const char* rowd, int64_t first,
+                                          int64_t n_bytes_chunk) {
+  const int st = t % kStages;
+  const int64_t off = static_cast<int64_t>(t) * kTripBytes;
+  int64_t bytes = n_bytes_chunk - off;
+  if (bytes > kTripBytes) bytes = kTripBytes;
+  bytes &= ~static_cast<int64_t>(15);
+  if (bytes < 0) bytes = 0;
+  const uint32_t b32 = static_cast<uint32_t>(bytes);
+  mbar_arrive_expect_tx(&R.full[st], b32 * ((rowt ? 1u : 0u) + (rowd ? 1u : 0u)));
+  if (b32) {
+    unsigned char* base = stages + static_cast<int64_t>(st) * 2 * kTripBytes;
+    if (rowt) bulk_load(base, rowt + first + off, b32, &R.full[st]);
+    if (rowd) bulk_load(base + kTripBytes, rowd + first + off, b32, &R.full[st]);
+  }
+}
+
+// Vector k of this thread in stage buffer `buf` for trip t: from shared
+// memory, or element by element from global memory for the ragged tail that
+// no bulk copy covered; -inf beyond the chunk.
+template <int DT>
+__device__ __forceinline__ typename Elem<DT>::Vec ring_vec(const unsigned char* buf, const char* row,
+                                                           int64_t v0, int64_t v1, int t, int k,
+                                                           int64_t covered_elems) {
+  using E = Elem<DT>;
+  const int jl = k * kThreads + threadIdx.x;               // vector within the trip
+  const int64_t e = v0 + (static_cast<int64_t>(t) * kVecs * kThreads + jl) * E::VW;  // first element
+  if (e + E::VW <= v0 + covered_elems) return reinterpret_cast<const typename E::Vec*>(buf)[jl];
+  return E::gather(row, e, v1);
+}
+
+template <int DT, bool GREEDY, bool KT>
+__device__ __forceinline__ bool stream_chunk_tma(Ring& R, unsigned char* stages, const char* rowt,
+                                                 const char* rowd, bool has_d, int64_t v0,
+                                                 int64_t v1, int nv, float c,
+                                                 Soft<Elem<DT>::VW>& st, Soft<Elem<DT>::VW>& sd,
+                                                 Arg& at, Arg& ad) {
+  using E = Elem<DT>;
+  constexpr int VW = E::VW;
+  const int ntr = (nv + kVecs * kThreads - 1) / (kVecs * kThreads);
+  const int64_t first = v0 * E::ES;
+  const int64_t n_bytes = (v1 - v0) * E::ES;
+  const int64_t covered = (n_bytes & ~static_cast<int64_t>(15)) / E::ES;  // elements in bulk copies
+  const char* rt = KT ? rowt : nullptr;
+  const char* rd = has_d ? rowd : nullptr;
+  if (threadIdx.x == 0) {
+    for (int s2 = 0; s2 < kStages; ++s2) mbar_init(&R.full[s2], 1);
+    fence_mbar_init();
+    for (int t = 0; t < ntr && t < kStages; ++t) ring_issue(R, stages, t, rt, rd, first, n_bytes);
+  }
+  __syncthreads();
+  bool ok = true;
+  for (int t = 0; t < ntr; ++t) {
+    const int s2 = t % kStages;
+    if (!mbar_wait_bounded(&R.full[s2], static_cast<uint32_t>((t / kStages) & 1))) ok = false;
+    const unsigned char* base = stages + static_cast<int64_t>(s2) * 2 * kTripBytes;
+#pragma unroll
+    for (int k = 0; k < kVecs; ++k) {
+      const int j = (t * kVecs + k) * kThreads + threadIdx.x;
+      if (j < nv) {
+        float z[VW];
+        const int32_t b0 = static_cast<int32_t>(v0) + j * VW;
+        if (KT) {
+          E::unpack(ring_vec<DT>(base, rowt, v0, v1, t, k, covered), z);
+          if (GREEDY) at.add(z, b0); else st.add(z, c);
+        }
+        if (has_d) {
+          E::unpack(ring_vec<DT>(base + kTripBytes, rowd, v0, v1, t, k, covered), z);
+          if (GREEDY) ad.add(z, b0); else sd.add(z, c);
+        }
+      }
+    }
+    // Stage s2 consumed by every thread.  If any wait gave up, issue nothing
+    // more, give the copies in flight a bounded wait to land, and report.
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0)
+        for (int t2 = t; t2 < ntr && t2 < t + kStages; ++t2)
+          mbar_wait_bounded(&R.full[t2 % kStages], static_cast<uint32_t>((t2 / kStages) & 1));
+      __syncthreads();
+      return false;
+    }
+    if (threadIdx.x == 0 && t + kStages < ntr) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ring_issue(R, stages, t + kStages, rt, rd, first, n_bytes);
+    }
+  }
+  return ok;
+}
+
 template <int DT, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
   using E = Elem<DT>;
@@ -145,14 +252,26 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
   const int64_t v1 = min(static_cast<int64_t>(P.V), v0 + P.chunk);
   const int nv = static_cast<int>((v1 - v0 + VW - 1) / VW);
 
+  const int excl = (kTopF && i < K) ? P.tokens[static_cast<int64_t>(b) * K + i] : -1;
   Soft<VW> st, sd;
   Arg at, ad;
   st.init();
   sd.init();
   at.init();
   ad.init();
-  if (greedy) stream_chunk<DT, VEC, true, kT>(rowt, rowd, has_d, v0, v1, nv, P.iters, c, st, sd, at, ad);
-  else stream_chunk<DT, VEC, false, kT>(rowt, rowd, has_d, v0, v1, nv, P.iters, c, st, sd, at, ad);
+  int copy_bad = 0;  // bit 1: a staged copy did not land in time
+  if (VEC) {
+    extern __shared__ __align__(128) unsigned char stages[];
+    __shared__ Ring ring;
+    const bool ok = greedy
+        ? stream_chunk_tma<DT, true, kT>(ring, stages, rowt, rowd, has_d, v0, v1, nv, c, st, sd, at, ad)
+        : stream_chunk_tma<DT, false, kT>(ring, stages, rowt, rowd, has_d, v0, v1, nv, c, st, sd, at, ad);
+    copy_bad = ok ? 0 : 2;  // every thread of the CTA returns the same verdict
+  } else if (greedy) {
+    stream_chunk<DT, VEC, true, kT>(rowt, rowd, has_d, v0, v1, nv, P.iters, c, st, sd, at, ad);
+  } else {
+    stream_chunk<DT, VEC, false, kT>(rowt, rowd, has_d, v0, v1, nv, P.iters, c, st, sd, at, ad);
+  }
 
   // ---- reduce: warp, then CTA (warp 0 over the eight warp partials) --------
   const float tmax_d = greedy ? ad.best : sd.m;  // this thread's draft maximum
@@ -222,41 +341,48 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
       warp_soft_all(md, s_d, c);
       r.mt = mt; r.st = s_t; r.md = md; r.sd = s_d;
     }
+    r.bad |= copy_bad;
     if (lane == 0) P.recs[blockIdx.x] = r;
   }
 
   if (kTopF) {
-    // Only threads whose maximum reaches the bound can hold a top-F logit:
-    // they read their logits again (L2) and push the qualifying ones into a
-    // shared buffer, ranked in parallel.  Too many qualifiers (ties at the
-    // bound, or no finite bound at F = 32) take the exact warp-list path.
+    // Only threads whose maximum reaches the bound can hold a top-F logit.
+    // Their logits are read again (from L2, just streamed) by their whole
+    // warp -- lane k fetches the candidate thread's k-th vector -- and the
+    // qualifying ones are pushed into a shared buffer, ranked in parallel.
+    // Too many qualifiers (ties at the bound), or no finite bound at all
+    // (F = 32, masked rows), take the exact warp-list path.
     const int F = P.F;
-    const int excl = (i < K) ? P.tokens[static_cast<int64_t>(b) * K + i] : -1;
     float thr = wthr[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) thr = fmaxf(thr, wthr[w]);
-    if (!(thr > kNegMax)) thr = neg_inf();  // no finite bound: admit everything
+    const bool bounded = thr > kNegMax;
     const int ntrips = P.iters * kVecs;
-    if (tmax_d >= thr) {
-      for (int k = 0; k < ntrips; ++k) {
-        const int j = k * kThreads + threadIdx.x;
-        if (j >= nv) break;
-        float z[VW];
-        E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), z);
-        const int32_t base = static_cast<int32_t>(v0) + j * VW;
+    unsigned cm = __ballot_sync(0xffffffffu, bounded && tmax_d >= thr);
+    while (cm) {
+      const int owner = warp * 32 + __ffs(cm) - 1;
+      cm &= cm - 1;
+      for (int k = lane; k < ntrips; k += 32) {
+        const int j = k * kThreads + owner;
+        if (j < nv) {
+          float z[VW];
+          E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), z);
+          const int32_t base = static_cast<int32_t>(v0) + j * VW;
 #pragma unroll
-        for (int e = 0; e < VW; ++e) {
-          const int32_t vi = base + e;
-          if (vi < v1 && vi != excl && z[e] >= thr) {
-            const int slot = atomicAdd(&KS.count, 1);
-            if (slot < kCandCap) {
-              KS.v[slot] = z[e];
-              KS.i[slot] = vi;
+          for (int e = 0; e < VW; ++e) {
+            const int32_t vi = base + e;
+            if (vi < v1 && vi != excl && z[e] >= thr) {
+              const int slot = atomicAdd(&KS.count, 1);
+              if (slot < kCandCap) {
+                KS.v[slot] = z[e];
+                KS.i[slot] = vi;
+              }
             }
           }
         }
       }
     }
+    if (!bounded && threadIdx.x == 0) KS.count = kCandCap + 1;  // exact path below
     __syncthreads();
     const int m = KS.count;
     float* outv = P.cand_v + static_cast<int64_t>(blockIdx.x) * F;
@@ -293,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           const int32_t vi = base + e;
-          const bool pass = j < nv && vi < v1 && vi != excl && z[e] >= thr &&
+          const bool pass = j < nv && vi < v1 && vi != excl && (!bounded || z[e] >= thr) &&
                             key_beats(z[e], vi, L.tv, L.ti);
           unsigned mm = __ballot_sync(0xffffffffu, pass);
           while (mm) {
