@@ -1,5 +1,7 @@
 // C ABI of libspecv (declared in include/specv.h): argument checks, workspace
 // sizing, cluster-size choice and kernel launches on the caller's stream.
+#include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -160,7 +162,7 @@ constexpr size_t kMaxSegSmem = 200 * 1024;
 
 template <typename Kern, typename Params>
 cudaError_t launch_plain(Kern k, int64_t blocks, size_t smem, cudaStream_t s, const Params& p) {
-  if (smem > 48 * 1024) {
+  if (smem > 0) {  // static + dynamic shared memory may pass the 48 KB default
     const cudaError_t e =
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -169,17 +171,63 @@ cudaError_t launch_plain(Kern k, int64_t blocks, size_t smem, cudaStream_t s, co
   return cudaGetLastError();
 }
 
-// Shared memory of the TMA ring (aligned rows only): kStages stages of one
-// trip of two rows.
-constexpr size_t kRingSmem = static_cast<size_t>(kStages) * 2 * kTripBytes;
+// Stages of the persistent path's ring (SPECV_STAGES = 2..8 fixes the count,
+// for tuning runs).
+int ring_stages() {
+  static int n = 0;
+  if (n == 0) {
+    const char* e = getenv("SPECV_STAGES");
+    const int v = e ? atoi(e) : 0;
+    n = (v >= 2 && v <= kMaxStages) ? v : 3;
+  }
+  return n;
+}
+
+// Persistent row-statistics kernel: as many CTAs as are resident at once on
+// the GPU (at most one per work item), each with the ring in dynamic shared
+// memory.  The occupancy query is made once per kernel and ring size.
+template <int DT, int MODE>
+cudaError_t launch_ring(int64_t items, cudaStream_t s, const StatsParams& p) {
+  auto k = stats_ring_kernel<DT, MODE>;
+  const size_t smem = static_cast<size_t>(p.stages) * 2 * kTripBytes;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  static std::atomic<int> occ_cache[kMaxStages + 1];
+  int occ = occ_cache[p.stages].load(std::memory_order_relaxed);
+  if (occ <= 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kRingThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    occ_cache[p.stages].store(occ, std::memory_order_relaxed);
+  }
+  const int64_t grid = std::min<int64_t>(items, static_cast<int64_t>(occ) * sm_count());
+  k<<<static_cast<unsigned>(grid), kRingThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Kernel A for 16-byte aligned layouts: the staged path (one CTA per item) by
+// default, the persistent path when SPECV_PERSIST=1 (for tuning runs); the
+// register path for any other layout.
+bool persistent_path() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("SPECV_PERSIST");
+    v = (e && atoi(e) == 1) ? 1 : 0;
+  }
+  return v == 1;
+}
 
 template <int MODE>
-cudaError_t launch_stats(int dtype, bool vec, int64_t blocks, cudaStream_t s, const StatsParams& p) {
-  if (dtype == SPECV_BF16)
-    return vec ? launch_plain(stats_kernel<0, true, MODE>, blocks, kRingSmem, s, p)
-               : launch_plain(stats_kernel<0, false, MODE>, blocks, 0, s, p);
-  return vec ? launch_plain(stats_kernel<1, true, MODE>, blocks, kRingSmem, s, p)
-             : launch_plain(stats_kernel<1, false, MODE>, blocks, 0, s, p);
+cudaError_t launch_stats(int dtype, bool vec, int64_t items, cudaStream_t s, const StatsParams& p) {
+  const size_t ring_smem = static_cast<size_t>(p.stages) * 2 * kTripBytes;
+  if (dtype == SPECV_BF16) {
+    if (!vec) return launch_plain(stats_kernel<0, false, MODE>, items, 0, s, p);
+    return persistent_path() ? launch_ring<0, MODE>(items, s, p)
+                             : launch_plain(stats_kernel<0, true, MODE>, items, ring_smem, s, p);
+  }
+  if (!vec) return launch_plain(stats_kernel<1, false, MODE>, items, 0, s, p);
+  return persistent_path() ? launch_ring<1, MODE>(items, s, p)
+                           : launch_plain(stats_kernel<1, true, MODE>, items, ring_smem, s, p);
 }
 
 template <int MODE>
@@ -287,6 +335,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.nchunk = static_cast<int32_t>(pl.nchunk);
   sp.chunk = static_cast<int32_t>(pl.chunk);
   sp.iters = pl.iters;
+  sp.stages = ring_stages();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = mode == kModeSsd ? launch_stats<kModeSsd>(a->dtype, vec, units * pl.nchunk, s, sp)
                                    : launch_stats<kModeVerify>(a->dtype, vec, units * pl.nchunk, s, sp);
@@ -412,6 +461,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   sp.nchunk = static_cast<int32_t>(pl.nchunk);
   sp.chunk = static_cast<int32_t>(pl.chunk);
   sp.iters = pl.iters;
+  sp.stages = ring_stages();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_stats<kModePredict>(a->dtype, vec, units * pl.nchunk, s, sp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));

@@ -34,6 +34,44 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Paired fp32 arithmetic (two lanes of one 64-bit register, round to nearest,
+// no fused multiply-add) and three-input max, native on sm_100 and later.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three, NaN inputs ignored (NaN only if all three are NaN)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// max of three, NaN if any input is NaN
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Element traits: DT 0 = bf16 (raw 16-bit patterns), 1 = fp32.  A "vector"
 // is 16 bytes: 8 bf16 or 4 fp32 logits.
 template <int DT>
@@ -177,6 +215,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (clock64() - t0 > 2000000000LL) break;
   }
   return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Named barrier 1 over the kThreads threads of warps 0..kWarps-1 (a CTA's
+// whole block, or its consumer warps when a producer warp runs beside them).
+__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// As cons_sync, returning whether `p` held on any of those threads.
+__device__ __forceinline__ bool cons_sync_or(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred b, 1, 256, a;\n selp.u32 %0, 1, 0, b;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p))
+      : "memory");
+  return r != 0;
 }
 
 // Split cluster barrier: arrive (release) now, wait (acquire) later.

@@ -6,20 +6,26 @@
 // Speculative Decoding" §4.1.1: top-F draft tokens at each lookahead, the token
 // sent for verification there excluded).
 //
-// A unit is one (batch row b, position i), i in [0, K]; a CTA owns one chunk of
-// the unit's rows (target row i and/or draft row i): `iters` trips of kVecs
-// 16-byte vectors per row per thread.  The loop is software-pipelined: the next
-// trip's loads are in flight while the current trip is consumed, so a thread
-// keeps 2*kVecs vectors per row outstanding; there is no shared staging and no
-// cluster, so CTAs are small and many.
+// A unit is one (batch row b, position i), i in [0, K]; a work item is one
+// chunk of the unit's rows (target row i and/or draft row i): `iters` trips of
+// kVecs 16-byte vectors per row per thread of a 256-thread group.  Three ways
+// to stream a chunk, all with the same vector -> thread mapping (so the same
+// results):
+//   - register path (any layout): one CTA per item, element-wise loads,
+//     software-pipelined;
+//   - staged path (16-byte aligned rows): one CTA per item; thread 0 keeps a
+//     ring of 1-D bulk copies (TMA) of the next trips in flight into shared
+//     memory while the CTA consumes the current one;
+//   - persistent path (16-byte aligned rows): every CTA loops over items and
+//     a producer warp keeps the ring filled across item boundaries.
 //
-// Per chunk the CTA writes a ChunkRec: online (max, sum 2^((z-max) log2(e)/T))
-// of each row, or its first argmax for greedy rows.  With outcome prediction it
-// also writes the chunk's own top-F of the draft row: the (F+1)-th largest of a
-// warp's per-thread maxima bounds the chunk's top-F from below, so only the few
-// threads whose maximum reaches the bound read their logits again (from L2,
-// just streamed) and push the qualifying ones into shared memory, where they
-// are ranked in parallel.
+// Per chunk the consumers write a ChunkRec: online (max, sum 2^((z-max) log2(e)/T))
+// of each row, or its first argmax for greedy rows.  With outcome prediction
+// they also write the chunk's own top-F of the draft row: the (F+1)-th largest
+// per-thread maximum of a warp bounds the chunk's top-F from below, so only the
+// few threads whose maximum reaches the bound read their share again (from
+// L2, just streamed; one round trip per warp) and push the qualifying logits
+// into shared memory, where they are ranked in parallel.
 #pragma once
 
 #include "specv_device.cuh"
@@ -28,6 +34,8 @@ namespace specv {
 
 enum : int { kModeVerify = 0, kModeSsd = 1, kModePredict = 2 };
 constexpr int kVecs = 2;  // 16-byte vectors per row per thread per loop trip
+constexpr int kMaxStages = 8;
+constexpr int kTripBytes = kVecs * kThreads * 16;  // one row's share of a trip (8 KB)
 
 struct ChunkRec {        // 48 bytes per (unit, chunk)
   float mt, st, md, sd;  // temperature rows: max and sum of 2^((z-max)c)
@@ -50,12 +58,133 @@ struct StatsParams {
   float* cand_v;      // [units * nchunk * F] (predict / ssd)
   int32_t* cand_i;
   int32_t B, K, V, F, nchunk, chunk, iters;  // chunk = iters * kVecs * 256 * VW logits
+  int32_t stages;     // ring stages of the staged paths, 2..kMaxStages
 };
 
 // log2(e)/T for a valid temperature; greedy rows and bad temperatures use 1.
 __device__ __forceinline__ float temp_scale(float T) {
   return (T > 0.f && T < pos_inf()) ? __fdiv_rn(1.44269504088896341f, T) : 1.f;
 }
+
+// ---- a thread's accumulators -------------------------------------------------
+// A thread streams its share of a chunk one trip at a time: a group of N =
+// kVecs*VW logits of each row (kVecs vectors; logits base[k] .. base[k]+VW-1
+// in vector k, in increasing index order).  Per group the max is taken once
+// (three-input max) and the sums are rescaled once, branch-free; the
+// exponents are computed in paired fp32 lanes.
+
+template <int N>
+__device__ __forceinline__ float group_max(const float (&z)[N], float init) {
+  float r = init;
+#pragma unroll
+  for (int k = 0; k + 1 < N; k += 2) r = max3(r, z[k], z[k + 1]);
+  return r;
+}
+
+template <int N>
+__device__ __forceinline__ float group_max_nan(const float (&z)[N]) {
+  float r = z[0];
+#pragma unroll
+  for (int k = 1; k + 1 < N; k += 2) r = max3_nan(r, z[k], z[k + 1]);
+  return (N % 2 == 0) ? max3_nan(r, z[N - 1], z[N - 1]) : r;
+}
+
+// Temperature rows: online max m and sum of 2^((z-m)c), as four partial sums
+// held in two pairs.  A NaN logit makes the sum NaN; a +inf logit makes it
+// NaN as well (inf - inf); a row of -inf leaves m = kNegMax and the sum 0.
+template <int N>
+struct SoftG {
+  float m;
+  uint64_t s0, s1;
+  __device__ __forceinline__ void init() {
+    m = kNegMax;
+    s0 = s1 = f2(0.f, 0.f);
+  }
+  __device__ __forceinline__ void add(const float (&z)[N], float c) {
+    static_assert(N % 4 == 0, "groups of whole pairs of pairs");
+    const float mn = group_max(z, m);
+    const float f = ex2(__fmul_rn(__fsub_rn(m, mn), c));  // exactly 1 when m is unchanged
+    const uint64_t ff = f2(f, f);
+    s0 = f2_mul(s0, ff);
+    s1 = f2_mul(s1, ff);
+    const uint64_t mm = f2(mn, mn), cc = f2(c, c);
+#pragma unroll
+    for (int k = 0; k < N; k += 4) {
+      float a, b, d, e;
+      f2_split(f2_mul(f2_sub(f2(z[k], z[k + 1]), mm), cc), a, b);
+      f2_split(f2_mul(f2_sub(f2(z[k + 2], z[k + 3]), mm), cc), d, e);
+      s0 = f2_add(s0, f2(ex2(a), ex2(b)));
+      s1 = f2_add(s1, f2(ex2(d), ex2(e)));
+    }
+    m = mn;
+  }
+  __device__ __forceinline__ float total() const {
+    float a, b, d, e;
+    f2_split(s0, a, b);
+    f2_split(s1, d, e);
+    return (a + b) + (d + e);
+  }
+};
+
+// Greedy rows: first argmax, and whether a NaN or +inf was seen.
+template <int N>
+struct ArgG {
+  float best;
+  int32_t idx;
+  int32_t bad;
+  __device__ __forceinline__ void init() {
+    best = neg_inf();
+    idx = INT_MAX;
+    bad = 0;
+  }
+  template <int VW>
+  __device__ __forceinline__ void add(const float (&z)[N], const int32_t (&base)[N / VW]) {
+    const float vm = group_max_nan(z);  // NaN if any logit is NaN
+    bad |= !(vm < pos_inf());
+    if (vm > best) {  // a new best: the first logit of the group equal to it
+      int32_t id = INT_MAX;
+#pragma unroll
+      for (int k = N - 1; k >= 0; --k)
+        if (z[k] == vm) id = base[k / VW] + k % VW;
+      best = vm;
+      idx = id;
+    }
+  }
+};
+
+template <int VW>
+struct Acc {
+  static constexpr int N = kVecs * VW;
+  SoftG<N> st, sd;  // temperature rows: target, draft
+  ArgG<N> at, ad;   // greedy rows: target, draft
+  __device__ __forceinline__ void init() {
+    st.init();
+    sd.init();
+    at.init();
+    ad.init();
+  }
+  template <bool GREEDY, bool DRAFT>
+  __device__ __forceinline__ void add(const float (&z)[N], const int32_t (&base)[kVecs], float c) {
+    if (GREEDY) (DRAFT ? ad : at).template add<VW>(z, base);
+    else (DRAFT ? sd : st).add(z, c);
+  }
+};
+
+// Unpacks vector k of a trip into its slot of the group (or -inf when absent).
+template <int DT>
+__device__ __forceinline__ void put_vec(float* z, const typename Elem<DT>::Vec& w) {
+  float y[Elem<DT>::VW];
+  Elem<DT>::unpack(w, y);
+#pragma unroll
+  for (int e = 0; e < Elem<DT>::VW; ++e) z[e] = y[e];
+}
+template <int DT>
+__device__ __forceinline__ void put_none(float* z) {
+#pragma unroll
+  for (int e = 0; e < Elem<DT>::VW; ++e) z[e] = neg_inf();
+}
+
+// ---- register path ------------------------------------------------------------
 
 template <int DT, bool VEC>
 __device__ __forceinline__ void load_trip(const void* row, int64_t v0, int64_t v1, int nv, int it,
@@ -67,29 +196,26 @@ __device__ __forceinline__ void load_trip(const void* row, int64_t v0, int64_t v
   }
 }
 
-template <int DT, bool GREEDY>
+template <int DT, bool GREEDY, bool DRAFT>
 __device__ __forceinline__ void consume_trip(const typename Elem<DT>::Vec (&w)[kVecs], int nv,
-                                             int it, int64_t v0, float c,
-                                             Soft<Elem<DT>::VW>& s, Arg& a) {
-  using E = Elem<DT>;
-  constexpr int VW = E::VW;
+                                             int it, int64_t v0, float c, Acc<Elem<DT>::VW>& A) {
+  constexpr int VW = Elem<DT>::VW;
+  float z[kVecs * VW];
+  int32_t base[kVecs];
 #pragma unroll
   for (int k = 0; k < kVecs; ++k) {
     const int j = (it * kVecs + k) * kThreads + threadIdx.x;
-    if (j < nv) {
-      float z[VW];
-      E::unpack(w[k], z);
-      if (GREEDY) a.add(z, static_cast<int32_t>(v0) + j * VW); else s.add(z, c);
-    }
+    base[k] = static_cast<int32_t>(v0) + j * VW;
+    if (j < nv) put_vec<DT>(z + k * VW, w[k]); else put_none<DT>(z + k * VW);
   }
+  A.template add<GREEDY, DRAFT>(z, base, c);
 }
 
 // Streams the CTA's chunk of one or two rows (software-pipelined).
 template <int DT, bool VEC, bool GREEDY, bool KT>
 __device__ __forceinline__ void stream_chunk(const void* rowt, const void* rowd, bool has_d,
                                              int64_t v0, int64_t v1, int nv, int iters, float c,
-                                             Soft<Elem<DT>::VW>& st, Soft<Elem<DT>::VW>& sd,
-                                             Arg& at, Arg& ad) {
+                                             Acc<Elem<DT>::VW>& A) {
   using Vec = typename Elem<DT>::Vec;
   Vec at0[kVecs], ad0[kVecs], at1[kVecs], ad1[kVecs];
   if (KT) load_trip<DT, VEC>(rowt, v0, v1, nv, 0, at0);
@@ -99,209 +225,112 @@ __device__ __forceinline__ void stream_chunk(const void* rowt, const void* rowd,
       if (KT) load_trip<DT, VEC>(rowt, v0, v1, nv, it + 1, at1);
       if (has_d) load_trip<DT, VEC>(rowd, v0, v1, nv, it + 1, ad1);
     }
-    if (KT) consume_trip<DT, GREEDY>(at0, nv, it, v0, c, st, at);
-    if (has_d) consume_trip<DT, GREEDY>(ad0, nv, it, v0, c, sd, ad);
+    if (KT) consume_trip<DT, GREEDY, false>(at0, nv, it, v0, c, A);
+    if (has_d) consume_trip<DT, GREEDY, true>(ad0, nv, it, v0, c, A);
     if (it + 1 < iters) {
       if (it + 2 < iters) {
         if (KT) load_trip<DT, VEC>(rowt, v0, v1, nv, it + 2, at0);
         if (has_d) load_trip<DT, VEC>(rowd, v0, v1, nv, it + 2, ad0);
       }
-      if (KT) consume_trip<DT, GREEDY>(at1, nv, it + 1, v0, c, st, at);
-      if (has_d) consume_trip<DT, GREEDY>(ad1, nv, it + 1, v0, c, sd, ad);
+      if (KT) consume_trip<DT, GREEDY, false>(at1, nv, it + 1, v0, c, A);
+      if (has_d) consume_trip<DT, GREEDY, true>(ad1, nv, it + 1, v0, c, A);
     }
   }
 }
 
-// ---- TMA ring (16-byte aligned rows) ----------------------------------------
-// A trip is kVecs*256 16-byte vectors of each row; stage s of the ring holds
-// one trip of every streamed row.  Thread 0 keeps up to kStages trips in
-// flight as 1-D bulk copies completing on the stage's mbarrier; all threads
-// consume a stage from shared memory, meet at a CTA barrier, and thread 0
-// refills the stage with the trip kStages ahead.  The vector -> thread mapping
-// is that of the register path, so results are identical.
-constexpr int kStages = 4;
-constexpr int kTripBytes = kVecs * kThreads * 16;  // per row per trip (8 KB)
-
-struct Ring {
-  uint64_t full[kStages];
+// ---- one chunk of one unit ----------------------------------------------------
+// Work item `item` = (unit u = item / nchunk, chunk item % nchunk); unit u is
+// (batch row b, position i) = (u / (K+1), u % (K+1)).
+struct Chunk {
+  int b, i;
+  const char* rowt;  // target row i, or null when it is not streamed
+  const char* rowd;  // draft row i, or null when there is none
+  int64_t v0, v1;    // the chunk covers logits [v0, v1) of its rows
+  int nv;            // 16-byte vectors covering them (the last may be partial)
 };
 
-// Issue trip t of the chunk into stage t % kStages.  Bytes past the last whole
-// 16-byte unit of the chunk are left to the consumers (plain loads).
-__device__ __forceinline__ void ring_issue(Ring& R, unsigned char* stages, int t,
-                                          const char* rowt, const char* rowd, int64_t first,
-                                          int64_t n_bytes_chunk) {
-  const int st = t % kStages;
-  const int64_t off = static_cast<int64_t>(t) * kTripBytes;
-  int64_t bytes = n_bytes_chunk - off;
-  if (bytes > kTripBytes) bytes = kTripBytes;
-  bytes &= ~static_cast<int64_t>(15);
-  if (bytes < 0) bytes = 0;
-  const uint32_t b32 = static_cast<uint32_t>(bytes);
-  mbar_arrive_expect_tx(&R.full[st], b32 * ((rowt ? 1u : 0u) + (rowd ? 1u : 0u)));
-  if (b32) {
-    unsigned char* base = stages + static_cast<int64_t>(st) * 2 * kTripBytes;
-    if (rowt) bulk_load(base, rowt + first + off, b32, &R.full[st]);
-    if (rowd) bulk_load(base + kTripBytes, rowd + first + off, b32, &R.full[st]);
-  }
-}
-
-// Vector k of this thread in stage buffer `buf` for trip t: from shared
-// memory, or element by element from global memory for the ragged tail that
-// no bulk copy covered; -inf beyond the chunk.
-template <int DT>
-__device__ __forceinline__ typename Elem<DT>::Vec ring_vec(const unsigned char* buf, const char* row,
-                                                           int64_t v0, int64_t v1, int t, int k,
-                                                           int64_t covered_elems) {
+template <int DT, int MODE>
+__device__ __forceinline__ Chunk chunk_at(const StatsParams& P, int64_t item) {
   using E = Elem<DT>;
-  const int jl = k * kThreads + threadIdx.x;               // vector within the trip
-  const int64_t e = v0 + (static_cast<int64_t>(t) * kVecs * kThreads + jl) * E::VW;  // first element
-  if (e + E::VW <= v0 + covered_elems) return reinterpret_cast<const typename E::Vec*>(buf)[jl];
-  return E::gather(row, e, v1);
+  Chunk C;
+  const int64_t u = item / P.nchunk;
+  const int ch = static_cast<int>(item % P.nchunk);
+  C.b = static_cast<int>(u / (P.K + 1));
+  C.i = static_cast<int>(u % (P.K + 1));
+  const bool has_d = (MODE == kModeVerify) ? (C.i < P.K) : true;
+  C.rowt = (MODE != kModePredict)
+               ? static_cast<const char*>(P.zt) +
+                     (static_cast<int64_t>(C.b) * P.t_bs + static_cast<int64_t>(C.i) * P.t_rs) * E::ES
+               : nullptr;
+  C.rowd = has_d ? static_cast<const char*>(P.zd) +
+                       (static_cast<int64_t>(C.b) * P.d_bs + static_cast<int64_t>(C.i) * P.d_rs) * E::ES
+                 : nullptr;
+  C.v0 = static_cast<int64_t>(ch) * P.chunk;
+  C.v1 = min(static_cast<int64_t>(P.V), C.v0 + P.chunk);
+  C.nv = static_cast<int>((C.v1 - C.v0 + E::VW - 1) / E::VW);
+  return C;
 }
 
-template <int DT, bool GREEDY, bool KT>
-__device__ __forceinline__ bool stream_chunk_tma(Ring& R, unsigned char* stages, const char* rowt,
-                                                 const char* rowd, bool has_d, int64_t v0,
-                                                 int64_t v1, int nv, float c,
-                                                 Soft<Elem<DT>::VW>& st, Soft<Elem<DT>::VW>& sd,
-                                                 Arg& at, Arg& ad) {
-  using E = Elem<DT>;
-  constexpr int VW = E::VW;
-  const int ntr = (nv + kVecs * kThreads - 1) / (kVecs * kThreads);
-  const int64_t first = v0 * E::ES;
-  const int64_t n_bytes = (v1 - v0) * E::ES;
-  const int64_t covered = (n_bytes & ~static_cast<int64_t>(15)) / E::ES;  // elements in bulk copies
-  const char* rt = KT ? rowt : nullptr;
-  const char* rd = has_d ? rowd : nullptr;
-  if (threadIdx.x == 0) {
-    for (int s2 = 0; s2 < kStages; ++s2) mbar_init(&R.full[s2], 1);
-    fence_mbar_init();
-    for (int t = 0; t < ntr && t < kStages; ++t) ring_issue(R, stages, t, rt, rd, first, n_bytes);
+// Shared scratch of a chunk's epilogue.
+struct EpiSmem {
+  ChunkRec wrec[kWarps];
+  float wthr[kWarps];
+  float wl_v[kWarps][kMaxF];
+  int32_t wl_i[kWarps][kMaxF];
+  KeyScratch KS;
+};
+
+__device__ __forceinline__ void push_key(KeyScratch& KS, float v, int32_t i) {
+  const int slot = atomicAdd(&KS.count, 1);
+  if (slot < kCandCap) {
+    KS.v[slot] = v;
+    KS.i[slot] = i;
   }
-  __syncthreads();
-  bool ok = true;
-  for (int t = 0; t < ntr; ++t) {
-    const int s2 = t % kStages;
-    if (!mbar_wait_bounded(&R.full[s2], static_cast<uint32_t>((t / kStages) & 1))) ok = false;
-    const unsigned char* base = stages + static_cast<int64_t>(s2) * 2 * kTripBytes;
-#pragma unroll
-    for (int k = 0; k < kVecs; ++k) {
-      const int j = (t * kVecs + k) * kThreads + threadIdx.x;
-      if (j < nv) {
-        float z[VW];
-        const int32_t b0 = static_cast<int32_t>(v0) + j * VW;
-        if (KT) {
-          E::unpack(ring_vec<DT>(base, rowt, v0, v1, t, k, covered), z);
-          if (GREEDY) at.add(z, b0); else st.add(z, c);
-        }
-        if (has_d) {
-          E::unpack(ring_vec<DT>(base + kTripBytes, rowd, v0, v1, t, k, covered), z);
-          if (GREEDY) ad.add(z, b0); else sd.add(z, c);
-        }
-      }
-    }
-    // Stage s2 consumed by every thread.  If any wait gave up, issue nothing
-    // more, give the copies in flight a bounded wait to land, and report.
-    if (__syncthreads_or(!ok)) {
-      if (threadIdx.x == 0)
-        for (int t2 = t; t2 < ntr && t2 < t + kStages; ++t2)
-          mbar_wait_bounded(&R.full[t2 % kStages], static_cast<uint32_t>((t2 / kStages) & 1));
-      __syncthreads();
-      return false;
-    }
-    if (threadIdx.x == 0 && t + kStages < ntr) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      ring_issue(R, stages, t + kStages, rt, rd, first, n_bytes);
-    }
-  }
-  return ok;
 }
 
+// Epilogue of chunk `item`, run by the kThreads threads of warps 0..7 after
+// they have streamed it: reduces their accumulators into the chunk's ChunkRec
+// (warp, then warp 0 over the eight warp partials) and, with outcome
+// prediction, writes the chunk's top-F draft candidates.  `ok` is false on a
+// thread whose staged copies did not all land.  Ends with a barrier, so the
+// scratch is free for the next chunk.
 template <int DT, bool VEC, int MODE>
-__global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
+__device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& C, int64_t item,
+                                             bool greedy, float c, Acc<Elem<DT>::VW>& A, bool ok,
+                                             EpiSmem& S) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
-  constexpr bool kT = MODE != kModePredict;
   constexpr bool kTopF = MODE != kModeVerify;
-  __shared__ ChunkRec wrec[kWarps];
-  __shared__ float wthr[kWarps];
-  __shared__ float wl_v[kWarps][kMaxF];
-  __shared__ int32_t wl_i[kWarps][kMaxF];
-  __shared__ KeyScratch KS;
-
-  const int64_t u = blockIdx.x / P.nchunk;
-  const int ch = static_cast<int>(blockIdx.x % P.nchunk);
-  const int K = P.K;
-  const int b = static_cast<int>(u / (K + 1));
-  const int i = static_cast<int>(u % (K + 1));
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const bool has_d = (MODE == kModeVerify) ? (i < K) : true;
-  const float T = kT ? P.temp[b] : 0.f;
-  const bool greedy = !kT || T == 0.f;
-  const float c = greedy ? 1.f : temp_scale(T);
-
-  const char* rowt = kT ? static_cast<const char*>(P.zt) +
-                              (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(i) * P.t_rs) * E::ES
-                        : nullptr;
-  const char* rowd = has_d ? static_cast<const char*>(P.zd) +
-                                 (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(i) * P.d_rs) * E::ES
-                           : nullptr;
-  const int64_t v0 = static_cast<int64_t>(ch) * P.chunk;
-  const int64_t v1 = min(static_cast<int64_t>(P.V), v0 + P.chunk);
-  const int nv = static_cast<int>((v1 - v0 + VW - 1) / VW);
-
-  const int excl = (kTopF && i < K) ? P.tokens[static_cast<int64_t>(b) * K + i] : -1;
-  Soft<VW> st, sd;
-  Arg at, ad;
-  st.init();
-  sd.init();
-  at.init();
-  ad.init();
-  int copy_bad = 0;  // bit 1: a staged copy did not land in time
-  if (VEC) {
-    extern __shared__ __align__(128) unsigned char stages[];
-    __shared__ Ring ring;
-    const bool ok = greedy
-        ? stream_chunk_tma<DT, true, kT>(ring, stages, rowt, rowd, has_d, v0, v1, nv, c, st, sd, at, ad)
-        : stream_chunk_tma<DT, false, kT>(ring, stages, rowt, rowd, has_d, v0, v1, nv, c, st, sd, at, ad);
-    copy_bad = ok ? 0 : 2;  // every thread of the CTA returns the same verdict
-  } else if (greedy) {
-    stream_chunk<DT, VEC, true, kT>(rowt, rowd, has_d, v0, v1, nv, P.iters, c, st, sd, at, ad);
-  } else {
-    stream_chunk<DT, VEC, false, kT>(rowt, rowd, has_d, v0, v1, nv, P.iters, c, st, sd, at, ad);
-  }
-
-  // ---- reduce: warp, then CTA (warp 0 over the eight warp partials) --------
-  const float tmax_d = greedy ? ad.best : sd.m;  // this thread's draft maximum
   if (greedy) {
-    float bt = at.best, bd = ad.best;
-    int32_t it = at.idx, id = ad.idx;
+    float bt = A.at.best, bd = A.ad.best;
+    int32_t it = A.at.idx, id = A.ad.idx;
     warp_arg_all(bt, it);
     warp_arg_all(bd, id);
-    const int bad = __any_sync(0xffffffffu, at.bad | ad.bad);
+    const int bad = __any_sync(0xffffffffu, A.at.bad | A.ad.bad);
     if (lane == 0) {
-      wrec[warp].bt = bt; wrec[warp].it = it; wrec[warp].bd = bd; wrec[warp].id = id;
-      wrec[warp].bad = bad;
+      S.wrec[warp].bt = bt; S.wrec[warp].it = it; S.wrec[warp].bd = bd; S.wrec[warp].id = id;
+      S.wrec[warp].bad = bad;
     }
   } else {
-    float mt = st.m, s_t = st.total(), md = sd.m, s_d = sd.total();
+    float mt = A.st.m, s_t = A.st.total(), md = A.sd.m, s_d = A.sd.total();
     warp_soft_all(mt, s_t, c);
     warp_soft_all(md, s_d, c);
     if (lane == 0) {
-      wrec[warp].mt = mt; wrec[warp].st = s_t; wrec[warp].md = md; wrec[warp].sd = s_d;
+      S.wrec[warp].mt = mt; S.wrec[warp].st = s_t; S.wrec[warp].md = md; S.wrec[warp].sd = s_d;
     }
   }
   if (kTopF) {
-    if (threadIdx.x == 0) KS.count = 0;
+    if (threadIdx.x == 0) S.KS.count = 0;
     if (threadIdx.x < P.F) {
-      KS.out_v[threadIdx.x] = neg_inf();
-      KS.out_i[threadIdx.x] = INT_MAX;
+      S.KS.out_v[threadIdx.x] = neg_inf();
+      S.KS.out_i[threadIdx.x] = INT_MAX;
     }
-    // (F+1)-th largest per-thread max of this warp: a lower bound on the
-    // chunk's (F+1)-th largest draft logit, hence on its top-F without x.
-    float s = tmax_d;
+    // (F+1)-th largest per-thread maximum of this warp (bitonic sort of the
+    // 32 maxima): F+1 distinct logits reach it, so at least F of them are not
+    // the excluded token -- a lower bound on the chunk's top-F without it.
+    float s = greedy ? A.ad.best : A.sd.m;  // this thread's draft maximum
 #pragma unroll
     for (int k2 = 2; k2 <= 32; k2 <<= 1) {
 #pragma unroll
@@ -312,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
       }
     }
     const float tw = (P.F < 32) ? __shfl_sync(0xffffffffu, s, P.F) : neg_inf();
-    if (lane == 0) wthr[warp] = tw;
+    if (lane == 0) S.wthr[warp] = tw;
   }
-  __syncthreads();
+  const bool copy_bad = cons_sync_or(!ok);  // a chunk copy gave up on some thread
   if (warp == 0) {
     ChunkRec r;
     r.mt = kNegMax; r.st = 0.f; r.md = kNegMax; r.sd = 0.f;
@@ -325,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
       int32_t it = INT_MAX, id = INT_MAX;
       int bad = 0;
       if (lane < kWarps) {
-        bt = wrec[lane].bt; it = wrec[lane].it; bd = wrec[lane].bd; id = wrec[lane].id;
-        bad = wrec[lane].bad;
+        bt = S.wrec[lane].bt; it = S.wrec[lane].it; bd = S.wrec[lane].bd; id = S.wrec[lane].id;
+        bad = S.wrec[lane].bad;
       }
       warp_arg_all(bt, it);
       warp_arg_all(bd, id);
@@ -335,73 +364,86 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
     } else {
       float mt = kNegMax, s_t = 0.f, md = kNegMax, s_d = 0.f;
       if (lane < kWarps) {
-        mt = wrec[lane].mt; s_t = wrec[lane].st; md = wrec[lane].md; s_d = wrec[lane].sd;
+        mt = S.wrec[lane].mt; s_t = S.wrec[lane].st; md = S.wrec[lane].md; s_d = S.wrec[lane].sd;
       }
       warp_soft_all(mt, s_t, c);
       warp_soft_all(md, s_d, c);
       r.mt = mt; r.st = s_t; r.md = md; r.sd = s_d;
     }
-    r.bad |= copy_bad;
-    if (lane == 0) P.recs[blockIdx.x] = r;
+    if (copy_bad) r.bad |= 2;
+    if (lane == 0) P.recs[item] = r;
   }
 
   if (kTopF) {
-    // Only threads whose maximum reaches the bound can hold a top-F logit.
-    // Their logits are read again (from L2, just streamed) by their whole
-    // warp -- lane k fetches the candidate thread's k-th vector -- and the
-    // qualifying ones are pushed into a shared buffer, ranked in parallel.
-    // Too many qualifiers (ties at the bound), or no finite bound at all
-    // (F = 32, masked rows), take the exact warp-list path.
+    // Every draft logit of the chunk at or above the bound, the excluded token
+    // left out, goes into a shared buffer ranked in parallel.  Only threads
+    // whose maximum reaches the bound can hold one; their shares are read
+    // again (from L2, just streamed) by their whole warp at once -- lane l
+    // fetches vector l, l+32, ... of the list (candidate, vector k) -- so the
+    // warp pays one round trip for all its candidates.  Too many qualifiers
+    // (ties at the bound), or no finite bound at all (F = 32, masked rows),
+    // take the exact warp-list path.
     const int F = P.F;
-    float thr = wthr[0];
+    const int excl = (C.i < P.K) ? P.tokens[static_cast<int64_t>(C.b) * P.K + C.i] : -1;
+    float thr = S.wthr[0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) thr = fmaxf(thr, wthr[w]);
+    for (int w = 1; w < kWarps; ++w) thr = fmaxf(thr, S.wthr[w]);
     const bool bounded = thr > kNegMax;
-    const int ntrips = P.iters * kVecs;
-    unsigned cm = __ballot_sync(0xffffffffu, bounded && tmax_d >= thr);
-    while (cm) {
-      const int owner = warp * 32 + __ffs(cm) - 1;
-      cm &= cm - 1;
-      for (int k = lane; k < ntrips; k += 32) {
-        const int j = k * kThreads + owner;
-        if (j < nv) {
+    const int ntrips = P.iters * kVecs;  // vectors per thread per row
+    const float tmax_d = greedy ? A.ad.best : A.sd.m;
+    const unsigned cm = __ballot_sync(0xffffffffu, bounded && tmax_d >= thr);
+    const int todo = __popc(cm) * ntrips;
+    for (int r0 = 0; r0 < todo; r0 += 4 * 32) {
+      typename E::Vec w[4];
+      int jv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int idx = r0 + q * 32 + lane;
+        jv[q] = -1;
+        if (idx < todo) {
+          const int cand = idx / ntrips;
+          const int owner = warp * 32 + static_cast<int>(__fns(cm, 0, cand + 1));
+          const int j = (idx - cand * ntrips) * kThreads + owner;
+          if (j < C.nv) {
+            jv[q] = j;
+            w[q] = load_vec<DT, VEC>(C.rowd, C.v0, C.v1, j);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (jv[q] >= 0) {
           float z[VW];
-          E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), z);
-          const int32_t base = static_cast<int32_t>(v0) + j * VW;
+          E::unpack(w[q], z);
+          const int32_t base = static_cast<int32_t>(C.v0) + jv[q] * VW;
 #pragma unroll
           for (int e = 0; e < VW; ++e) {
             const int32_t vi = base + e;
-            if (vi < v1 && vi != excl && z[e] >= thr) {
-              const int slot = atomicAdd(&KS.count, 1);
-              if (slot < kCandCap) {
-                KS.v[slot] = z[e];
-                KS.i[slot] = vi;
-              }
-            }
+            if (vi < C.v1 && vi != excl && z[e] >= thr) push_key(S.KS, z[e], vi);
           }
         }
       }
     }
-    if (!bounded && threadIdx.x == 0) KS.count = kCandCap + 1;  // exact path below
-    __syncthreads();
-    const int m = KS.count;
-    float* outv = P.cand_v + static_cast<int64_t>(blockIdx.x) * F;
-    int32_t* outi = P.cand_i + static_cast<int64_t>(blockIdx.x) * F;
+    if (!bounded && threadIdx.x == 0) S.KS.count = kCandCap + 1;  // exact path below
+    cons_sync();
+    const int m = S.KS.count;
+    float* outv = P.cand_v + item * F;
+    int32_t* outi = P.cand_i + item * F;
     if (m <= kCandCap) {
       for (int e = threadIdx.x; e < m; e += kThreads) {
-        const float v = KS.v[e];
-        const int32_t ii = KS.i[e];
+        const float v = S.KS.v[e];
+        const int32_t ii = S.KS.i[e];
         int rank = 0;
-        for (int o = 0; o < m; ++o) rank += key_beats(KS.v[o], KS.i[o], v, ii);
+        for (int o = 0; o < m; ++o) rank += key_beats(S.KS.v[o], S.KS.i[o], v, ii);
         if (rank < F) {
-          KS.out_v[rank] = v;
-          KS.out_i[rank] = ii;
+          S.KS.out_v[rank] = v;
+          S.KS.out_i[rank] = ii;
         }
       }
-      __syncthreads();
+      cons_sync();
       if (threadIdx.x < F) {
-        outv[threadIdx.x] = KS.out_v[threadIdx.x];
-        outi[threadIdx.x] = KS.out_i[threadIdx.x];
+        outv[threadIdx.x] = S.KS.out_v[threadIdx.x];
+        outi[threadIdx.x] = S.KS.out_i[threadIdx.x];
       }
     } else {
       WarpTopF L;
@@ -409,17 +451,17 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
       for (int k = 0; k < ntrips; ++k) {
         const int j = k * kThreads + threadIdx.x;
         float z[VW];
-        if (j < nv) {
-          E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), z);
+        if (j < C.nv) {
+          E::unpack(load_vec<DT, VEC>(C.rowd, C.v0, C.v1, j), z);
         } else {
 #pragma unroll
           for (int e = 0; e < VW; ++e) z[e] = neg_inf();
         }
-        const int32_t base = static_cast<int32_t>(v0) + j * VW;
+        const int32_t base = static_cast<int32_t>(C.v0) + j * VW;
 #pragma unroll
         for (int e = 0; e < VW; ++e) {
           const int32_t vi = base + e;
-          const bool pass = j < nv && vi < v1 && vi != excl && (!bounded || z[e] >= thr) &&
+          const bool pass = j < C.nv && vi < C.v1 && vi != excl && (!bounded || z[e] >= thr) &&
                             key_beats(z[e], vi, L.tv, L.ti);
           unsigned mm = __ballot_sync(0xffffffffu, pass);
           while (mm) {
@@ -432,12 +474,283 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
         }
       }
       if (lane < F) {
-        wl_v[warp][lane] = L.v;
-        wl_i[warp][lane] = L.i;
+        S.wl_v[warp][lane] = L.v;
+        S.wl_i[warp][lane] = L.i;
+      }
+      cons_sync();
+      if (warp == 0) merge_lists(S.wl_v, S.wl_i, kWarps, F, lane, outv, outi);
+    }
+  }
+  cons_sync();
+}
+
+// ---- staged paths: bulk copies into a ring of shared-memory stages --------------
+// Stage s holds one trip of each streamed row: the target's share at offset 0,
+// the draft's at kTripBytes.
+
+struct RingBars {
+  uint64_t full[kMaxStages];   // completes when stage s has landed
+  uint64_t empty[kMaxStages];  // persistent path: all consumer warps are done with stage s
+  int abort;                   // persistent path: set once a wait has given up
+};
+
+__device__ __forceinline__ int ring_trips(int nv) {
+  return (nv + kVecs * kThreads - 1) / (kVecs * kThreads);
+}
+
+// Copies trip t of chunk C into stage s, completing on `full`.  Whole 16-byte
+// units only (the consumers load a ragged tail themselves); the expected byte
+// count is armed even when nothing is copied, so the phase completes anyway.
+template <int DT>
+__device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, int s, int t,
+                                           const Chunk& C) {
+  using E = Elem<DT>;
+  const int64_t off = static_cast<int64_t>(t) * kTripBytes;
+  int64_t bytes = (C.v1 - C.v0) * E::ES - off;
+  if (bytes > kTripBytes) bytes = kTripBytes;
+  if (bytes < 0) bytes = 0;
+  const uint32_t b32 = static_cast<uint32_t>(bytes) & ~15u;
+  const uint32_t nrows = (C.rowt ? 1u : 0u) + (C.rowd ? 1u : 0u);
+  mbar_arrive_expect_tx(full, b32 * nrows);
+  if (b32) {
+    unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
+    const int64_t src = C.v0 * E::ES + off;
+    if (C.rowt) bulk_load(base, C.rowt + src, b32, full);
+    if (C.rowd) bulk_load(base + kTripBytes, C.rowd + src, b32, full);
+  }
+}
+
+// Accumulates this thread's vectors of trip t from the stage at `base`; a
+// vector past the last whole 16-byte unit of the chunk (`covered` = first
+// logit not copied) is gathered from global memory instead.
+template <int DT, bool GREEDY, bool KT>
+__device__ __forceinline__ void consume_stage(const unsigned char* base, int t, const Chunk& C,
+                                              int64_t covered, float c, Acc<Elem<DT>::VW>& A) {
+  using E = Elem<DT>;
+  using Vec = typename E::Vec;
+  constexpr int VW = E::VW;
+  constexpr int N = kVecs * VW;
+  const int j0 = t * kVecs * kThreads + threadIdx.x;  // this thread's first vector of the trip
+  int32_t b[kVecs];
+#pragma unroll
+  for (int k = 0; k < kVecs; ++k) b[k] = static_cast<int32_t>(C.v0) + (j0 + k * kThreads) * VW;
+  // Whole trip in shared memory: the common case, no per-vector checks.
+  const bool whole = C.v0 + static_cast<int64_t>(j0 + (kVecs - 1) * kThreads + 1) * VW <= covered;
+  if (KT) {
+    float z[N];
+    const Vec* src = reinterpret_cast<const Vec*>(base);
+#pragma unroll
+    for (int k = 0; k < kVecs; ++k) {
+      const int j = j0 + k * kThreads;
+      const int64_t e = C.v0 + static_cast<int64_t>(j) * VW;
+      if (whole || e + VW <= covered) put_vec<DT>(z + k * VW, src[k * kThreads + threadIdx.x]);
+      else if (j < C.nv) put_vec<DT>(z + k * VW, E::gather(C.rowt, e, C.v1));
+      else put_none<DT>(z + k * VW);
+    }
+    A.template add<GREEDY, false>(z, b, c);
+  }
+  if (C.rowd) {
+    float z[N];
+    const Vec* src = reinterpret_cast<const Vec*>(base + kTripBytes);
+#pragma unroll
+    for (int k = 0; k < kVecs; ++k) {
+      const int j = j0 + k * kThreads;
+      const int64_t e = C.v0 + static_cast<int64_t>(j) * VW;
+      if (whole || e + VW <= covered) put_vec<DT>(z + k * VW, src[k * kThreads + threadIdx.x]);
+      else if (j < C.nv) put_vec<DT>(z + k * VW, E::gather(C.rowd, e, C.v1));
+      else put_none<DT>(z + k * VW);
+    }
+    A.template add<GREEDY, true>(z, b, c);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ int64_t covered_end(const Chunk& C) {
+  using E = Elem<DT>;
+  return C.v0 + ((((C.v1 - C.v0) * E::ES) & ~static_cast<int64_t>(15)) / E::ES);
+}
+
+// Staged path, one CTA per item: thread 0 keeps up to S trips in flight and
+// refills a stage after the CTA barrier that closes its consumption.  Returns
+// false (on every thread) if a wait gave up; the copies then in flight get a
+// bounded wait before returning.
+template <int DT, bool GREEDY, bool KT>
+__device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* ring, int S,
+                                                    const Chunk& C, float c, Acc<Elem<DT>::VW>& A) {
+  const int ntr = ring_trips(C.nv);
+  const int64_t covered = covered_end<DT>(C);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&R.full[s], 1);
+    fence_mbar_init();
+    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C);
+  }
+  __syncthreads();
+  bool ok = true;
+  int s = 0;
+  uint32_t ph = 0;
+  for (int t = 0; t < ntr; ++t) {
+    if (!mbar_wait_bounded(&R.full[s], ph)) ok = false;
+    consume_stage<DT, GREEDY, KT>(ring + static_cast<int64_t>(s) * 2 * kTripBytes, t, C,
+                                        covered, c, A);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        int s2 = s;
+        uint32_t p2 = ph;
+        for (int t2 = t; t2 < ntr && t2 < t + S; ++t2) {
+          mbar_wait_bounded(&R.full[s2], p2);
+          if (++s2 == S) {
+            s2 = 0;
+            p2 ^= 1u;
+          }
+        }
       }
       __syncthreads();
-      if (warp == 0) merge_lists(wl_v, wl_i, kWarps, F, lane, outv, outi);
+      return false;
     }
+    if (threadIdx.x == 0 && t + S < ntr) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ring_issue<DT>(&R.full[s], ring, s, t + S, C);
+    }
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  return ok;
+}
+
+// Register path (VEC = false: any layout) or staged path (VEC = true: 16-byte
+// aligned rows, P.stages stages of dynamic shared memory); one CTA per item.
+template <int DT, bool VEC, int MODE>
+__global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
+  constexpr bool kT = MODE != kModePredict;
+  __shared__ EpiSmem S;
+  const Chunk C = chunk_at<DT, MODE>(P, blockIdx.x);
+  const float T = kT ? P.temp[C.b] : 0.f;
+  const bool greedy = !kT || T == 0.f;
+  const float c = greedy ? 1.f : temp_scale(T);
+  Acc<Elem<DT>::VW> A;
+  A.init();
+  bool ok = true;
+  if (VEC) {
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ RingBars R;
+    ok = greedy ? stream_chunk_staged<DT, true, kT>(R, ring, P.stages, C, c, A)
+                : stream_chunk_staged<DT, false, kT>(R, ring, P.stages, C, c, A);
+  } else if (greedy) {
+    stream_chunk<DT, false, true, kT>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
+                                             P.iters, c, A);
+  } else {
+    stream_chunk<DT, false, false, kT>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
+                                              P.iters, c, A);
+  }
+  chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S);
+}
+
+// ---- persistent path ------------------------------------------------------------
+// kThreads consumer threads (warps 0-7) plus one producer warp (warp 8).  A CTA
+// takes the items blockIdx.x, blockIdx.x + gridDim.x, ... in order.  Lane 0 of
+// the producer warp walks the same sequence of trips and copies the g-th into
+// stage g mod S, once all eight consumer warps have arrived on that stage's
+// empty barrier; the consumers run a chunk's epilogue while the copies of the
+// next chunk are already in flight.  Every wait is bounded: after a timeout
+// the CTA issues no more copies, flags every chunk it still owns (ChunkRec.bad
+// bit 1) and still writes all their records.
+constexpr int kRingThreads = kThreads + 32;
+
+template <int DT, int MODE>
+__device__ __forceinline__ void ring_produce(const StatsParams& P, RingBars& R, unsigned char* ring,
+                                             int64_t items) {
+  const int S = P.stages;
+  volatile int* abort = &R.abort;
+  int64_t g = 0;  // trips issued so far; the next goes to stage s with parity ph
+  int s = 0;
+  uint32_t ph = 0;
+  for (int64_t item = blockIdx.x; item < items && !*abort; item += gridDim.x) {
+    const Chunk C = chunk_at<DT, MODE>(P, item);
+    const int ntr = ring_trips(C.nv);
+    for (int t = 0; t < ntr; ++t) {
+      if (*abort || !mbar_wait_bounded(&R.empty[s], ph ^ 1u)) {
+        *abort = 1;
+        break;
+      }
+      ring_issue<DT>(&R.full[s], ring, s, t, C);
+      ++g;
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  if (*abort) {
+    // The copies that may still be in flight (the last S trips issued) get a
+    // bounded wait to land before the CTA can exit.
+    for (int64_t g2 = g > S ? g - S : 0; g2 < g; ++g2)
+      mbar_wait_bounded(&R.full[g2 % S], static_cast<uint32_t>((g2 / S) & 1));
+  }
+}
+
+// Consumes the trips of one chunk; returns false if any of them was not waited
+// for successfully (its data are then garbage and the chunk is flagged).
+template <int DT, bool GREEDY, bool KT>
+__device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* ring, int S, int& s,
+                                             uint32_t& ph, const Chunk& C, float c,
+                                             Acc<Elem<DT>::VW>& A) {
+  volatile int* abort = &R.abort;
+  const int ntr = ring_trips(C.nv);
+  const int64_t covered = covered_end<DT>(C);
+  bool ok = true;
+  for (int t = 0; t < ntr; ++t) {
+    if (*abort) {
+      ok = false;
+    } else if (!mbar_wait_bounded(&R.full[s], ph)) {
+      ok = false;
+      *abort = 1;
+    }
+    consume_stage<DT, GREEDY, KT>(ring + static_cast<int64_t>(s) * 2 * kTripBytes, t, C,
+                                        covered, c, A);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[s]);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  return ok;
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const StatsParams P) {
+  constexpr bool kT = MODE != kModePredict;
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ RingBars R;
+  __shared__ EpiSmem S;
+  const int64_t items = static_cast<int64_t>(P.B) * (P.K + 1) * P.nchunk;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P.stages; ++s) {
+      mbar_init(&R.full[s], 1);
+      mbar_init(&R.empty[s], kWarps);
+    }
+    R.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x >= kThreads) {
+    if (threadIdx.x == kThreads) ring_produce<DT, MODE>(P, R, ring, items);
+    return;
+  }
+  int s = 0;  // stage and parity of the next trip to consume
+  uint32_t ph = 0;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const Chunk C = chunk_at<DT, MODE>(P, item);
+    const float T = kT ? P.temp[C.b] : 0.f;
+    const bool greedy = !kT || T == 0.f;
+    const float c = greedy ? 1.f : temp_scale(T);
+    Acc<Elem<DT>::VW> A;
+    A.init();
+    const bool ok = greedy ? ring_consume<DT, true, kT>(R, ring, P.stages, s, ph, C, c, A)
+                           : ring_consume<DT, false, kT>(R, ring, P.stages, s, ph, C, c, A);
+    chunk_finish<DT, true, MODE>(P, C, item, greedy, c, A, ok, S);
   }
 }
 
