@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Throughput of the verification / outcome-prediction hot path on GB300.
 
-One step = one pass of the whole hot path over one batch: specv_verify (row
-statistics, accept test, residual/bonus draw), specv_predict_outcomes (top-F
-keys at every lookahead) and specv_check_hit, all through the C ABI.
+One step = one pass of the whole hot path over one batch through the C ABI:
+specv_ssd_round (row statistics, accept test, residual/bonus draw, top-F
+outcome keys at every lookahead and the hit check, fused over one read of the
+logits) for the SSD workloads, specv_verify for the verify-only ones.
 
 Default workload "cfg5-ssd": B=256, K=8, V=152064, fp32 Zipf-like logits
 (config 5) with the draft logits at K+1 lookaheads so the step also predicts

@@ -65,6 +65,8 @@ struct DecideParams {
   float* key_logits;
   uint8_t* hit;
   int32_t B, K, V, F, nchunk, CB, L;
+  int32_t stages;    // ring stages of the staged residual pass (aligned rows); 0: none
+  int32_t ring_off;  // byte offset of that ring in dynamic shared memory
 };
 
 // Combine the chunk records of one position (warp-wide; result in every lane).
@@ -120,21 +122,14 @@ __device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int3
   return L;
 }
 
-// r values of vector j of a row slice (global memory): mode 0 max(p - q, 0),
-// mode 1 p.  Both products rounded before the subtraction (no contraction), so
-// p(v) = q(v) gives r(v) = 0 exactly, as in the definition.
-template <int DT, bool VEC>
-__device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd, int64_t v0,
-                                             int64_t v1, int j, int mode, float mt, float md,
-                                             float c, float ist, float isd,
-                                             float (&r)[Elem<DT>::VW]) {
-  using E = Elem<DT>;
-  constexpr int VW = E::VW;
-  float zt[VW];
-  E::unpack(load_vec<DT, VEC>(rowt, v0, v1, j), zt);
+// r values of one vector from its target (and draft) logits: mode 0
+// max(p - q, 0), mode 1 p.  Both products rounded before the subtraction (no
+// contraction), so p(v) = q(v) gives r(v) = 0 exactly, as in the definition.
+template <int VW>
+__device__ __forceinline__ void residual_from(const float (&zt)[VW], const float (&zd)[VW], int mode,
+                                              float mt, float md, float c, float ist, float isd,
+                                              float (&r)[VW]) {
   if (mode == 0) {
-    float zd[VW];
-    E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), zd);
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
       const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
@@ -145,6 +140,105 @@ __device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd,
 #pragma unroll
     for (int k = 0; k < VW; ++k) r[k] = __fmul_rn(ex2((zt[k] - mt) * c), ist);
   }
+}
+
+// r values of vector j of a row slice, read from global memory.
+template <int DT, bool VEC>
+__device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd, int64_t v0,
+                                             int64_t v1, int j, int mode, float mt, float md,
+                                             float c, float ist, float isd,
+                                             float (&r)[Elem<DT>::VW]) {
+  using E = Elem<DT>;
+  constexpr int VW = E::VW;
+  float zt[VW], zd[VW];
+  E::unpack(load_vec<DT, VEC>(rowt, v0, v1, j), zt);
+  if (mode == 0) E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), zd);
+  residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
+}
+
+// Staged residual pass (16-byte aligned rows): the slice C of target row n
+// (and draft row n in mode 0) streams through the same bulk-copy ring as the
+// row-statistics kernel; trip t holds tiles 2t and 2t+1 (tile = one 16-byte
+// vector per thread).  ring_start arms the ring and issues the first trips (by
+// thread 0; call before other work, then a CTA barrier); ring_residual
+// consumes them and writes the per-warp segment sums of r, tile-major, as the
+// register path does.  Returns false if a wait gave up (after a bounded wait
+// for the copies still in flight).
+template <int DT>
+__device__ __forceinline__ void ring_start(RingBars& R, unsigned char* ring, int S, const Chunk& C) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&R.full[s], 1);
+    fence_mbar_init();
+    const int ntr = ring_trips(C.nv);
+    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, int S, const Chunk& C,
+                                              int mode, float mt, float md, float c, float ist,
+                                              float isd, float* segs, int ntl) {
+  using E = Elem<DT>;
+  using Vec = typename E::Vec;
+  constexpr int VW = E::VW;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int ntr = ring_trips(C.nv);
+  const int64_t covered = covered_end<DT>(C);
+  bool ok = true;
+  int s = 0;
+  uint32_t ph = 0;
+  for (int t = 0; t < ntr; ++t) {
+    if (!mbar_wait_bounded(&R.full[s], ph)) ok = false;
+    const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
+#pragma unroll
+    for (int k = 0; k < kVecs; ++k) {
+      const int tile = t * kVecs + k;
+      const int j = tile * kThreads + threadIdx.x;
+      float sum = 0.f;
+      if (j < C.nv) {
+        const int64_t e = C.v0 + static_cast<int64_t>(j) * VW;
+        const int jl = k * kThreads + threadIdx.x;
+        float zt[VW], zd[VW], r[VW];
+        if (e + VW <= covered) {
+          E::unpack(reinterpret_cast<const Vec*>(base)[jl], zt);
+          if (mode == 0) E::unpack(reinterpret_cast<const Vec*>(base + kTripBytes)[jl], zd);
+        } else {
+          E::unpack(E::gather(C.rowt, e, C.v1), zt);
+          if (mode == 0) E::unpack(E::gather(C.rowd, e, C.v1), zd);
+        }
+        residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
+#pragma unroll
+        for (int q = 0; q < VW; ++q) sum += r[q];
+      }
+      const float w = warp_sum(sum);
+      if (lane == 0 && tile < ntl) segs[tile * kWarps + warp] = w;
+    }
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        int s2 = s;
+        uint32_t p2 = ph;
+        for (int t2 = t; t2 < ntr && t2 < t + S; ++t2) {
+          mbar_wait_bounded(&R.full[s2], p2);
+          if (++s2 == S) {
+            s2 = 0;
+            p2 ^= 1u;
+          }
+        }
+      }
+      __syncthreads();
+      return false;
+    }
+    if (threadIdx.x == 0 && t + S < ntr) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      ring_issue<DT>(&R.full[s], ring, s, t + S, C);
+    }
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  return ok;
 }
 
 template <int DT, bool VEC, int MODE>
@@ -158,6 +252,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   __shared__ double cta_total;
   __shared__ KeyScratch KS;
   __shared__ int32_t tok_slot;  // rank 0: the token found by the owner CTA
+  __shared__ int32_t copy_fail;  // rank 0: a CTA's staged copies did not land in time
+  __shared__ RingBars ring_bars;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -247,9 +343,32 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       dec.tau = 0.0;
       dec.pre_mine = 0.0;
       tok_slot = dec.token;
+      copy_fail = 0;
     }
   }
   __syncthreads();
+
+  // ---- this CTA's slice of row n; aligned rows start streaming it now, so the
+  // copies run while the keys are merged ------------------------------------
+  const int n_dec = dec.n;
+  Chunk RC;
+  RC.b = b;
+  RC.i = n_dec;
+  RC.rowt = static_cast<const char*>(P.zt) +
+            (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(n_dec) * P.t_rs) * E::ES;
+  RC.rowd = static_cast<const char*>(P.zd) +
+            (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(n_dec < K ? n_dec : 0) * P.d_rs) * E::ES;
+  RC.v0 = static_cast<int64_t>(rank) * P.L;
+  RC.v1 = min(static_cast<int64_t>(P.V), RC.v0 + P.L);
+  RC.nv = RC.v1 > RC.v0 ? static_cast<int>((RC.v1 - RC.v0 + VW - 1) / VW) : 0;
+  unsigned char* ring = reinterpret_cast<unsigned char*>(segs) + P.ring_off;
+  const bool staged = VEC && dec.need_scan && P.stages > 0;
+  if (staged) {
+    Chunk SC = RC;
+    if (dec.mode != 0) SC.rowd = nullptr;  // mode 1 reads p_n only
+    ring_start<DT>(ring_bars, ring, P.stages, SC);
+    __syncthreads();
+  }
 
   // ---- outcome keys: lookaheads k = rank, rank + CB, ... ---------------------
   if (kTopF) {
@@ -269,19 +388,22 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   }
 
   if (dec.need_scan) {
-    const int n = dec.n;
-    const void* rowt = static_cast<const char*>(P.zt) +
-                       (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(n) * P.t_rs) * E::ES;
-    const void* rowd = static_cast<const char*>(P.zd) +
-                       (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(n < K ? n : 0) * P.d_rs) * E::ES;
-    const int64_t v0 = static_cast<int64_t>(rank) * P.L;
-    const int64_t v1 = min(static_cast<int64_t>(P.V), v0 + P.L);
-    const int nv = v1 > v0 ? static_cast<int>((v1 - v0 + VW - 1) / VW) : 0;
+    const void* rowt = RC.rowt;
+    const void* rowd = RC.rowd;
+    const int64_t v0 = RC.v0;
+    const int64_t v1 = RC.v1;
+    const int nv = RC.nv;
     const int ntl = (nv + kThreads - 1) / kThreads;
+    bool copies_ok = true;
     // ---- residual mass of this slice: per-warp segment sums ----------------
     for (int attempt = 0; attempt < 2; ++attempt) {
       const int mode = dec.mode;
       const float mt = dec.mt, md = dec.md, ist = dec.ist, isd = dec.isd;
+      if (staged && attempt == 0) {
+        Chunk SC = RC;
+        if (mode != 0) SC.rowd = nullptr;
+        copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd, segs, ntl);
+      } else
       for (int t0 = 0; t0 < ntl; t0 += kTileUnroll) {
         float s[kTileUnroll];
 #pragma unroll
@@ -308,7 +430,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         acc = warp_dsum_all(acc);
         if (lane == 0) cta_total = acc;
       }
-      cluster_sync();  // (1) per-CTA totals visible
+      cluster_sync();  // (1) per-CTA totals visible; every CTA of the cluster has started
+      if (!copies_ok && threadIdx.x == 0) *cluster.map_shared_rank(&copy_fail, 0) = 1;
       if (warp == 0) {
         const double tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total, lane) : 0.0;
         double incl = tr;
@@ -453,7 +576,10 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
 
   // ---- outputs, written by rank 0 ---------------------------------------------
   if (rank == 0) {
-    const bool ok = !(dec.status & kErrors);
+    // A slice whose staged copies did not land makes the row an error row
+    // (read after the barrier above, so the same on every thread).
+    const int status = dec.status | (copy_fail ? kTimeout : 0);
+    const bool ok = !(status & kErrors);
     const int n = dec.n;
     const int t = threadIdx.x;
     const int32_t token = tok_slot;
@@ -463,12 +589,17 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       P.out_tokens[u0 + t] = v;
     }
     if (t < K) {
-      if (P.p_draft) P.p_draft[static_cast<int64_t>(b) * K + t] = dec.px[t];
-      if (P.q_draft) P.q_draft[static_cast<int64_t>(b) * K + t] = dec.qx[t];
+      if (P.p_draft) P.p_draft[static_cast<int64_t>(b) * K + t] = ok ? dec.px[t] : 0.f;
+      if (P.q_draft) P.q_draft[static_cast<int64_t>(b) * K + t] = ok ? dec.qx[t] : 0.f;
     }
+    if (kTopF && copy_fail)
+      for (int e = t; e < (K + 1) * F; e += kThreads) {
+        P.keys[u0 * F + e] = -1;
+        if (P.key_logits) P.key_logits[u0 * F + e] = neg_inf();
+      }
     if (t == 0) {
       P.accept_len[b] = ok ? n : 0;
-      if (P.row_status) P.row_status[b] = ok ? (dec.status & kFallback) : (dec.status & kErrors);
+      if (P.row_status) P.row_status[b] = ok ? (status & kFallback) : (status & kErrors);
       if (P.hit) {
         uint8_t h = 0;
         if (ok && token >= 0)

@@ -49,6 +49,8 @@ int vec_width(int32_t dtype) { return dtype == SPECV_BF16 ? 8 : 4; }
 // total to keep every SM streaming the re-read row, at most 16, and no more
 // than there are 256-vector tiles in a row.  SPECV_CLUSTER (1..16) overrides
 // it, for tuning runs.
+int sm_count();
+
 int pick_cluster(int32_t B, int32_t V, int vw) {
   static int env = -2;
   if (env == -2) {
@@ -56,7 +58,12 @@ int pick_cluster(int32_t B, int32_t V, int vw) {
     env = s ? atoi(s) : -1;
   }
   if (env >= 1 && env <= 16) return env;
-  int c = (608 + B - 1) / (B > 0 ? B : 1);
+  // About four CTAs per SM over the whole grid, rounded down to a power of
+  // two: clusters of 2^k CTAs pack onto the GPCs without gaps.
+  const int want = 4 * sm_count();
+  int c = (want + B - 1) / (B > 0 ? B : 1);
+  if (c > 16) c = 16;
+  while (c & (c - 1)) c &= c - 1;
   const int tiles = static_cast<int>((static_cast<int64_t>(V) + kThreads * vw - 1) / (kThreads * vw));
   if (c > tiles) c = tiles;
   return c < 1 ? 1 : (c > 16 ? 16 : c);
@@ -84,7 +91,7 @@ cudaError_t launch_clustered(Kern k, int C, int64_t units, size_t smem, cudaStre
                              const Params& p) {
   cudaError_t e = allow_cluster(k, C);
   if (e != cudaSuccess) return e;
-  if (smem > 48 * 1024) {
+  if (smem > 0) {  // static + dynamic shared memory may pass the 48 KB default
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
@@ -178,7 +185,7 @@ int ring_stages() {
   if (n == 0) {
     const char* e = getenv("SPECV_STAGES");
     const int v = e ? atoi(e) : 0;
-    n = (v >= 2 && v <= kMaxStages) ? v : 3;
+    n = (v >= 2 && v <= kMaxStages) ? v : 2;
   }
   return n;
 }
@@ -371,8 +378,18 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   dp.nchunk = static_cast<int32_t>(pl.nchunk);
   dp.CB = pl.CB;
   dp.L = static_cast<int32_t>(pl.L);
-  e = mode == kModeSsd ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, pl.smemB, s, dp)
-                       : launch_decide<kModeVerify>(a->dtype, vec, pl.CB, B, pl.smemB, s, dp);
+  // Aligned rows stream the residual slice through a ring placed after the
+  // segment sums in dynamic shared memory.
+  // (Very long rows whose segment table leaves no room for it read directly.)
+  dp.ring_off = static_cast<int32_t>(round_up(pl.smemB, 128));
+  dp.stages = ring_stages();
+  size_t smemB = dp.ring_off + static_cast<size_t>(dp.stages) * 2 * kTripBytes;
+  if (!vec || smemB > kMaxSegSmem) {
+    dp.stages = 0;
+    smemB = pl.smemB;
+  }
+  e = mode == kModeSsd ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, smemB, s, dp)
+                       : launch_decide<kModeVerify>(a->dtype, vec, pl.CB, B, smemB, s, dp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "decision launch: %s", cudaGetErrorString(e));
   g_launches = 2;
   return ok();
