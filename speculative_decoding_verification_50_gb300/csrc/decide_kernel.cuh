@@ -185,33 +185,52 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
   const int warp = threadIdx.x >> 5;
   const int ntr = ring_trips(C.nv);
   const int64_t covered = covered_end<DT>(C);
+  const int nwhole = whole_trips<DT>(C, covered);
   bool ok = true;
   int s = 0;
   uint32_t ph = 0;
   for (int t = 0; t < ntr; ++t) {
     if (!mbar_wait_bounded(&R.full[s], ph)) ok = false;
     const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
+    float sum[kVecs];
+    if (t < nwhole) {  // whole trip in shared memory: no bounds checks
+#pragma unroll
+      for (int k = 0; k < kVecs; ++k) {
+        const int jl = k * kThreads + threadIdx.x;
+        float zt[VW], zd[VW], r[VW];
+        E::unpack(reinterpret_cast<const Vec*>(base)[jl], zt);
+        if (mode == 0) E::unpack(reinterpret_cast<const Vec*>(base + kTripBytes)[jl], zd);
+        residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
+        sum[k] = 0.f;
+#pragma unroll
+        for (int q = 0; q < VW; ++q) sum[k] += r[q];
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kVecs; ++k) {
+        const int j = (t * kVecs + k) * kThreads + threadIdx.x;
+        sum[k] = 0.f;
+        if (j < C.nv) {
+          const int64_t e = C.v0 + static_cast<int64_t>(j) * VW;
+          const int jl = k * kThreads + threadIdx.x;
+          float zt[VW], zd[VW], r[VW];
+          if (e + VW <= covered) {
+            E::unpack(reinterpret_cast<const Vec*>(base)[jl], zt);
+            if (mode == 0) E::unpack(reinterpret_cast<const Vec*>(base + kTripBytes)[jl], zd);
+          } else {
+            E::unpack(E::gather(C.rowt, e, C.v1), zt);
+            if (mode == 0) E::unpack(E::gather(C.rowd, e, C.v1), zd);
+          }
+          residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
+#pragma unroll
+          for (int q = 0; q < VW; ++q) sum[k] += r[q];
+        }
+      }
+    }
 #pragma unroll
     for (int k = 0; k < kVecs; ++k) {
       const int tile = t * kVecs + k;
-      const int j = tile * kThreads + threadIdx.x;
-      float sum = 0.f;
-      if (j < C.nv) {
-        const int64_t e = C.v0 + static_cast<int64_t>(j) * VW;
-        const int jl = k * kThreads + threadIdx.x;
-        float zt[VW], zd[VW], r[VW];
-        if (e + VW <= covered) {
-          E::unpack(reinterpret_cast<const Vec*>(base)[jl], zt);
-          if (mode == 0) E::unpack(reinterpret_cast<const Vec*>(base + kTripBytes)[jl], zd);
-        } else {
-          E::unpack(E::gather(C.rowt, e, C.v1), zt);
-          if (mode == 0) E::unpack(E::gather(C.rowd, e, C.v1), zd);
-        }
-        residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
-#pragma unroll
-        for (int q = 0; q < VW; ++q) sum += r[q];
-      }
-      const float w = warp_sum(sum);
+      const float w = warp_sum(sum[k]);
       if (lane == 0 && tile < ntl) segs[tile * kWarps + warp] = w;
     }
     if (__syncthreads_or(!ok)) {

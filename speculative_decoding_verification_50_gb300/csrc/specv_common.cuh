@@ -206,12 +206,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, letting the hardware suspend the thread for up to about
+// `ns` nanoseconds while the phase is incomplete (woken early when it completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar`, giving up after about a second of device
-// time (or 2^26 polls): returns false on timeout instead of spinning forever.
+// time (or 2^20 suspended polls): returns false on timeout instead of waiting
+// forever.  The common case -- the phase already complete -- costs one poll;
+// otherwise the thread sleeps in the hardware wait rather than spinning.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  for (uint32_t it = 0; it < (1u << 26); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t it = 0; it < (1u << 20); ++it) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (clock64() - t0 > 2000000000LL) break;
   }
   return false;

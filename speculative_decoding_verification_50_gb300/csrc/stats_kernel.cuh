@@ -520,6 +520,41 @@ __device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, 
   }
 }
 
+// Accumulates this thread's vectors of trip t, which lies wholly inside the
+// copied part of the chunk: no bounds checks (the common case).
+template <int DT, bool GREEDY, bool KT>
+__device__ __forceinline__ void consume_stage_whole(const unsigned char* base, int t, const Chunk& C,
+                                                    float c, Acc<Elem<DT>::VW>& A) {
+  using E = Elem<DT>;
+  using Vec = typename E::Vec;
+  constexpr int VW = E::VW;
+  constexpr int N = kVecs * VW;
+  const int j0 = t * kVecs * kThreads + threadIdx.x;
+  int32_t b[kVecs];
+#pragma unroll
+  for (int k = 0; k < kVecs; ++k) b[k] = static_cast<int32_t>(C.v0) + (j0 + k * kThreads) * VW;
+  if (KT) {
+    float z[N];
+    const Vec* src = reinterpret_cast<const Vec*>(base);
+#pragma unroll
+    for (int k = 0; k < kVecs; ++k) put_vec<DT>(z + k * VW, src[k * kThreads + threadIdx.x]);
+    A.template add<GREEDY, false>(z, b, c);
+  }
+  if (C.rowd) {
+    float z[N];
+    const Vec* src = reinterpret_cast<const Vec*>(base + kTripBytes);
+#pragma unroll
+    for (int k = 0; k < kVecs; ++k) put_vec<DT>(z + k * VW, src[k * kThreads + threadIdx.x]);
+    A.template add<GREEDY, true>(z, b, c);
+  }
+}
+
+// Trips of chunk C that lie wholly inside its copied part (for every thread).
+template <int DT>
+__device__ __forceinline__ int whole_trips(const Chunk& C, int64_t covered) {
+  return static_cast<int>(((covered - C.v0) / Elem<DT>::VW) / (kVecs * kThreads));
+}
+
 // Accumulates this thread's vectors of trip t from the stage at `base`; a
 // vector past the last whole 16-byte unit of the chunk (`covered` = first
 // logit not copied) is gathered from global memory instead.
@@ -588,10 +623,12 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
   bool ok = true;
   int s = 0;
   uint32_t ph = 0;
+  const int nwhole = whole_trips<DT>(C, covered);
   for (int t = 0; t < ntr; ++t) {
     if (!mbar_wait_bounded(&R.full[s], ph)) ok = false;
-    consume_stage<DT, GREEDY, KT>(ring + static_cast<int64_t>(s) * 2 * kTripBytes, t, C,
-                                        covered, c, A);
+    const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
+    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT>(base, t, C, c, A);
+    else consume_stage<DT, GREEDY, KT>(base, t, C, covered, c, A);
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         int s2 = s;
@@ -699,6 +736,7 @@ __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* r
   volatile int* abort = &R.abort;
   const int ntr = ring_trips(C.nv);
   const int64_t covered = covered_end<DT>(C);
+  const int nwhole = whole_trips<DT>(C, covered);
   bool ok = true;
   for (int t = 0; t < ntr; ++t) {
     if (*abort) {
@@ -707,8 +745,9 @@ __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* r
       ok = false;
       *abort = 1;
     }
-    consume_stage<DT, GREEDY, KT>(ring + static_cast<int64_t>(s) * 2 * kTripBytes, t, C,
-                                        covered, c, A);
+    const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
+    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT>(base, t, C, c, A);
+    else consume_stage<DT, GREEDY, KT>(base, t, C, covered, c, A);
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[s]);
     if (++s == S) {
