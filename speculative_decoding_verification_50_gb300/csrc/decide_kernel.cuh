@@ -12,8 +12,8 @@
 // One thread-block cluster of CB CTAs per batch row.  Every CTA combines the
 // records itself (one warp per position, lanes over chunks, fp64 sums) and
 // decides n; the arithmetic and its order are the same everywhere, so all CTAs
-// agree without waiting for one another.  CTA r merges the keys of lookaheads
-// r, r+CB, ... (threshold from the F-th best chunk head, then rank counting).
+// agree without waiting for one another.  Warp w of CTA r merges the chunk
+// candidate lists of lookahead r + w*CB (and r + (w+8)*CB, ...) into its keys.
 // Only row n is read again: every CTA streams its slice of target row n (and
 // draft row n), forms r, and reduces it to per-warp segment sums; the per-CTA
 // totals are exchanged through distributed shared memory, which gives R and the
@@ -269,7 +269,6 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   __shared__ PosStats ps[kMaxK + 1];
   __shared__ Dec dec;
   __shared__ double cta_total;
-  __shared__ KeyScratch KS;
   __shared__ int32_t tok_slot;  // rank 0: the token found by the owner CTA
   __shared__ int32_t copy_fail;  // rank 0: a CTA's staged copies did not land in time
   __shared__ RingBars ring_bars;
@@ -390,18 +389,19 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   }
 
   // ---- outcome keys: lookaheads k = rank, rank + CB, ... ---------------------
+  // One warp per lookahead, all at once: warp w of CTA r merges lookaheads
+  // r + w*CB, r + (w + 8)*CB, ... (the chunk lists into the row's top-F).
   if (kTopF) {
     const bool ok = !(dec.status & kErrors);
-    for (int k = rank; k <= K; k += CB) {
+    for (int k = rank + warp * CB; k <= K; k += CB * kWarps) {
       const int64_t u = u0 + k;
-      select_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F, P.nchunk, F, KS);
-      if (threadIdx.x < F) {
-        const bool good = ok && KS.out_i[threadIdx.x] != INT_MAX;
-        const int32_t key = good ? KS.out_i[threadIdx.x] : -1;
-        P.keys[u * F + threadIdx.x] = key;
-        if (P.key_logits) P.key_logits[u * F + threadIdx.x] = good ? KS.out_v[threadIdx.x] : neg_inf();
+      const WarpTopF L = merge_candidates(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
+                                          static_cast<int>(P.nchunk) * F, F, lane);
+      if (lane < F) {
+        const bool good = ok && L.i != INT_MAX;
+        P.keys[u * F + lane] = good ? L.i : -1;
+        if (P.key_logits) P.key_logits[u * F + lane] = good ? L.v : neg_inf();
       }
-      __syncthreads();
     }
     __threadfence();  // keys visible to rank 0 after the cluster barrier below
   }
@@ -644,30 +644,32 @@ struct PredictKeysParams {
 };
 
 __global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKeysParams P) {
-  __shared__ KeyScratch KS;
-  __shared__ int32_t row_bad;
+  __shared__ int32_t status_all;
   const int b = blockIdx.x;
   const int K = P.K, F = P.F;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int64_t u0 = static_cast<int64_t>(b) * (K + 1);
-  int status_all = 0;
-  for (int k = 0; k <= K; ++k) {
+  if (threadIdx.x == 0) status_all = 0;
+  __syncthreads();
+  for (int k = warp; k <= K; k += kWarps) {
     const int64_t u = u0 + k;
-    if (threadIdx.x == 0) row_bad = 0;
-    __syncthreads();
-    for (int q = threadIdx.x; q < P.nchunk; q += kThreads)
-      if (P.recs[u * P.nchunk + q].bad) row_bad |= P.recs[u * P.nchunk + q].bad;
+    int bad = 0;
+    for (int q = lane; q < P.nchunk; q += 32) bad |= P.recs[u * P.nchunk + q].bad;
+    bad = __reduce_or_sync(0xffffffffu, bad);
     const int x = (k < K) ? P.tokens[static_cast<int64_t>(b) * K + k] : 0;
-    select_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F, P.nchunk, F, KS);
-    const int status = ((row_bad & 1) ? kNonFinite : 0) | ((row_bad & 2) ? kTimeout : 0) |
+    const int status = ((bad & 1) ? kNonFinite : 0) | ((bad & 2) ? kTimeout : 0) |
                        ((x < 0 || x >= P.V) ? kBadToken : 0);
-    if (threadIdx.x < F) {
-      const bool good = status == 0 && KS.out_i[threadIdx.x] != INT_MAX;
-      P.keys[u * F + threadIdx.x] = good ? KS.out_i[threadIdx.x] : -1;
-      if (P.key_logits) P.key_logits[u * F + threadIdx.x] = good ? KS.out_v[threadIdx.x] : neg_inf();
+    const WarpTopF L = merge_candidates(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
+                                        P.nchunk * F, F, lane);
+    if (lane < F) {
+      const bool good = status == 0 && L.i != INT_MAX;
+      P.keys[u * F + lane] = good ? L.i : -1;
+      if (P.key_logits) P.key_logits[u * F + lane] = good ? L.v : neg_inf();
     }
-    status_all |= status;
-    __syncthreads();
+    if (lane == 0 && status) atomicOr(&status_all, status);
   }
+  __syncthreads();
   if (threadIdx.x == 0 && P.row_status) P.row_status[b] = status_all;
 }
 

@@ -199,93 +199,12 @@ __device__ __forceinline__ void warp_arg_all(float& v, int32_t& i) {
 
 constexpr int kCandCap = 512;  // candidates one CTA ranks at once
 
-struct KeyScratch {  // shared-memory scratch of select_keys
-  float v[kCandCap];
+struct KeyScratch {  // shared-memory scratch of a chunk's top-F selection
+  float v[kCandCap];   // qualifying candidates, unordered
   int32_t i[kCandCap];
-  float out_v[kMaxF];
+  float out_v[kMaxF];  // the top-F, in key order
   int32_t out_i[kMaxF];
-  float thr_v;
-  int32_t thr_i;
-  int count;
+  int count;           // candidates pushed (may pass kCandCap)
 };
-
-// Top-F of n candidates (cand_v[e], cand_i[e], e < n, in global or shared
-// memory) by rank counting over the ones that reach the threshold key
-// (tv, ti); candidates below it are known not to be in the top-F.  All threads
-// of the CTA call it; the result is in S.out_v / S.out_i (F entries, sorted).
-__device__ __forceinline__ void select_top_f(const float* cand_v, const int32_t* cand_i, int n,
-                                             float tv, int32_t ti, int F, KeyScratch& S) {
-  if (threadIdx.x == 0) S.count = 0;
-  if (threadIdx.x < F) {
-    S.out_v[threadIdx.x] = neg_inf();
-    S.out_i[threadIdx.x] = INT_MAX;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
-    const float v = cand_v[e];
-    const int32_t i = cand_i[e];
-    if (i != INT_MAX && !key_beats(tv, ti, v, i)) {
-      const int slot = atomicAdd(&S.count, 1);
-      if (slot < kCandCap) {
-        S.v[slot] = v;
-        S.i[slot] = i;
-      }
-    }
-  }
-  __syncthreads();
-  const int m = S.count;
-  if (m <= kCandCap) {
-    for (int e = threadIdx.x; e < m; e += blockDim.x) {
-      const float v = S.v[e];
-      const int32_t i = S.i[e];
-      int rank = 0;
-      for (int o = 0; o < m; ++o) rank += key_beats(S.v[o], S.i[o], v, i);
-      if (rank < F) {
-        S.out_v[rank] = v;
-        S.out_i[rank] = i;
-      }
-    }
-  } else {  // too many ties at the threshold: rank against every candidate
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      const float v = cand_v[e];
-      const int32_t i = cand_i[e];
-      if (i == INT_MAX) continue;
-      int rank = 0;
-      for (int o = 0; o < n && rank < F; ++o) rank += key_beats(cand_v[o], cand_i[o], v, i);
-      if (rank < F) {
-        S.out_v[rank] = v;
-        S.out_i[rank] = i;
-      }
-    }
-  }
-  __syncthreads();
-}
-
-// Top-F over n lists of F sorted entries (list r at cv[r*F .. r*F+F-1]).  The
-// F-th best list head bounds the answer from below (F heads reach it), so
-// only entries reaching it are ranked.  All threads of the CTA call it.
-__device__ __forceinline__ void select_keys(const float* cv, const int32_t* ci, int nlists, int F,
-                                            KeyScratch& S) {
-  if (threadIdx.x == 0) {
-    S.thr_v = neg_inf();
-    S.thr_i = INT_MAX;
-  }
-  __syncthreads();
-  if (nlists >= F) {
-    for (int r = threadIdx.x; r < nlists; r += blockDim.x) {
-      const float v = cv[static_cast<int64_t>(r) * F];
-      const int32_t i = ci[static_cast<int64_t>(r) * F];
-      int rank = 0;
-      for (int o = 0; o < nlists; ++o)
-        rank += key_beats(cv[static_cast<int64_t>(o) * F], ci[static_cast<int64_t>(o) * F], v, i);
-      if (rank == F - 1) {
-        S.thr_v = v;
-        S.thr_i = i;
-      }
-    }
-  }
-  __syncthreads();
-  select_top_f(cv, ci, nlists * F, S.thr_v, S.thr_i, F, S);
-}
 
 }  // namespace specv
