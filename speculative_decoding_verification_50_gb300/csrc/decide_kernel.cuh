@@ -10,16 +10,16 @@
 //   a5 the hit flag: t* among the keys of lookahead n (§3.1).
 //
 // One thread-block cluster of CB CTAs per batch row.  Every CTA combines the
-// records itself (one warp per position, lanes over chunks, fp64 sums) and
+// records itself (half a warp per position, lanes over chunks, fp64 sums) and
 // decides n; the arithmetic and its order are the same everywhere, so all CTAs
-// agree without waiting for one another.  Warp w of CTA r merges the chunk
-// candidate lists of lookahead r + w*CB (and r + (w+8)*CB, ...) into its keys.
-// Only row n is read again: every CTA streams its slice of target row n (and
-// draft row n), forms r, and reduces it to per-warp segment sums; the per-CTA
-// totals are exchanged through distributed shared memory, which gives R and the
-// CTA whose range holds U_K * R; that CTA walks its segments and one warp scans
-// the one segment that holds the crossing (a re-read of 32 vectors).  Rank 0
-// writes the outputs.
+// agree without waiting for one another.  Only row n is read again: every CTA
+// streams its slice of target row n (and draft row n) through a bulk-copy
+// ring, forms r, and reduces it to per-warp segment sums; the per-CTA totals
+// are exchanged through distributed shared memory, which gives R and the CTA
+// whose range holds U_K * R; that CTA walks its segments and one warp scans
+// the one segment that holds the crossing (a re-read of 32 vectors).  Meanwhile
+// warps 1..7 of every CTA merge the chunk candidate lists into the outcome
+// keys (one warp per lookahead).  Rank 0 writes the outputs.
 #pragma once
 
 #include "stats_kernel.cuh"
@@ -69,14 +69,15 @@ struct DecideParams {
   int32_t ring_off;  // byte offset of that ring in dynamic shared memory
 };
 
-// Combine the chunk records of one position (warp-wide; result in every lane).
-__device__ __forceinline__ PosStats combine_position(const ChunkRec* R, int nchunk, float c,
-                                                     int lane) {
+// Combine the chunk records of one position over an aligned group of W lanes
+// (`sub` = lane within the group; result in every lane of the group).
+template <int W>
+__device__ __forceinline__ PosStats combine_position(const ChunkRec* R, int nchunk, float c, int sub) {
   float mt = kNegMax, s_t = 0.f, md = kNegMax, s_d = 0.f;
   Arg at, ad;
   at.init();
   ad.init();
-  for (int q = lane; q < nchunk; q += 32) {
+  for (int q = sub; q < nchunk; q += W) {
     const ChunkRec r = R[q];
     soft_merge(mt, s_t, r.mt, r.st, c);
     soft_merge(md, s_d, r.md, r.sd, c);
@@ -84,17 +85,71 @@ __device__ __forceinline__ PosStats combine_position(const ChunkRec* R, int nchu
     ad.merge(r.bd, r.id, 0);
   }
   PosStats p;
-  p.Mt = warp_max_all(mt);
-  p.Md = warp_max_all(md);
-  p.St = warp_dsum_all(static_cast<double>(s_t) * static_cast<double>(ex2((mt - p.Mt) * c)));
-  p.Sd = warp_dsum_all(static_cast<double>(s_d) * static_cast<double>(ex2((md - p.Md) * c)));
-  warp_arg_all(at.best, at.idx);
-  warp_arg_all(ad.best, ad.idx);
+  p.Mt = warp_max_all<float, W>(mt);
+  p.Md = warp_max_all<float, W>(md);
+  p.St = warp_dsum_all<W>(static_cast<double>(s_t) * static_cast<double>(ex2((mt - p.Mt) * c)));
+  p.Sd = warp_dsum_all<W>(static_cast<double>(s_d) * static_cast<double>(ex2((md - p.Md) * c)));
+  warp_arg_all<W>(at.best, at.idx);
+  warp_arg_all<W>(ad.best, ad.idx);
   p.it = at.idx;
   p.id = ad.idx;
-  p.bad = __any_sync(0xffffffffu, at.bad);
+  // bad flags of the whole group (OR over W lanes)
+  int bad = at.bad;
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  p.bad = bad;
   p.pad = 0;
   return p;
+}
+
+// Top-F keys of one draft row from its per-chunk candidate lists, by one warp
+// (lanes < F end with the keys of rank `lane`; (-inf, INT_MAX) where the row
+// has fewer than F).  Up to kWarpCand candidates are staged in the warp's
+// shared scratch and ranked by counting (independent comparisons); larger sets
+// are merged by warp insertion.
+constexpr int kWarpCand = 64;
+struct WarpKeys {
+  float v[kWarpCand];
+  int32_t i[kWarpCand];
+  float ov[kMaxF];
+  int32_t oi[kMaxF];
+};
+
+__device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int32_t* ci, int ncand,
+                                                     int F, int lane);
+
+__device__ __forceinline__ WarpTopF warp_keys(const float* cv, const int32_t* ci, int ncand, int F,
+                                              int lane, WarpKeys& S) {
+  if (ncand > kWarpCand) return merge_candidates(cv, ci, ncand, F, lane);
+  for (int e = lane; e < ncand; e += 32) {
+    S.v[e] = cv[e];
+    S.i[e] = ci[e];
+  }
+  if (lane < F) {
+    S.ov[lane] = neg_inf();
+    S.oi[lane] = INT_MAX;
+  }
+  __syncwarp();
+  for (int e = lane; e < ncand; e += 32) {
+    const float v = S.v[e];
+    const int32_t i = S.i[e];
+    if (i == INT_MAX) continue;  // an empty slot of a short list
+    int rank = 0;
+    for (int o = 0; o < ncand; ++o) rank += key_beats(S.v[o], S.i[o], v, i);
+    if (rank < F) {
+      S.ov[rank] = v;
+      S.oi[rank] = i;
+    }
+  }
+  __syncwarp();
+  WarpTopF L;
+  L.init();
+  if (lane < F) {
+    L.v = S.ov[lane];
+    L.i = S.oi[lane];
+  }
+  __syncwarp();  // the scratch may be reused by this warp's next row
+  return L;
 }
 
 // Top-F over the per-chunk candidate lists of one draft row (warp-wide).
@@ -268,10 +323,15 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   extern __shared__ float segs[];  // [tiles * kWarps] segment sums of r
   __shared__ PosStats ps[kMaxK + 1];
   __shared__ Dec dec;
-  __shared__ double cta_total;
+  __shared__ double cta_total[2];  // this CTA's residual mass, per attempt
   __shared__ int32_t tok_slot;  // rank 0: the token found by the owner CTA
   __shared__ int32_t copy_fail;  // rank 0: a CTA's staged copies did not land in time
   __shared__ RingBars ring_bars;
+  __shared__ int32_t pre_x[kMaxK];  // draft tokens, their logits and the uniforms,
+  __shared__ float pre_zt[kMaxK];   // fetched while the records are combined
+  __shared__ float pre_zd[kMaxK];
+  __shared__ float pre_u[kMaxK];
+  __shared__ WarpKeys wkeys[kTopF ? kWarps : 1];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -287,9 +347,30 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   const int64_t u0 = static_cast<int64_t>(b) * (K + 1);
 
   // ---- every CTA combines the records and decides (identical results) -------
-  for (int i = warp; i <= K; i += kWarps) {
-    const PosStats p = combine_position(P.recs + (u0 + i) * P.nchunk, P.nchunk, c, lane);
-    if (lane == 0) ps[i] = p;
+  // The last warp first fetches what the decision needs besides the records.
+  if (warp == kWarps - 1) {
+    for (int i = lane; i < K; i += 32) {
+      const int x = P.tokens[static_cast<int64_t>(b) * K + i];
+      float zt = 0.f, zd = 0.f;
+      if (x >= 0 && x < P.V) {
+        zt = E::scalar(static_cast<const char*>(P.zt) +
+                           (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(i) * P.t_rs) * E::ES,
+                       x);
+        zd = E::scalar(static_cast<const char*>(P.zd) +
+                           (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(i) * P.d_rs) * E::ES,
+                       x);
+      }
+      pre_x[i] = x;
+      pre_zt[i] = zt;
+      pre_zd[i] = zd;
+      pre_u[i] = P.unif[u0 + i];
+    }
+  }
+  // Half a warp per position: positions 2w and 2w+1 on warp w, 16 per pass.
+  for (int i0 = 2 * warp; i0 <= K; i0 += 2 * kWarps) {
+    const int i = i0 + (lane >> 4);
+    const PosStats p = combine_position<16>(P.recs + (u0 + min(i, K)) * P.nchunk, P.nchunk, c, lane & 15);
+    if ((lane & 15) == 0 && i <= K) ps[i] = p;
   }
   __syncthreads();
   if (warp == 0) {
@@ -307,7 +388,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       }
     }
     const bool acc_lane = lane < K;
-    const int x = acc_lane ? P.tokens[static_cast<int64_t>(b) * K + lane] : -1;
+    const int x = acc_lane ? pre_x[lane] : -1;
     int status = temp_ok ? 0 : kBadTemp;
     if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
     if (__any_sync(0xffffffffu, lane <= K && (ps[lane].bad & 2))) status |= kTimeout;
@@ -322,12 +403,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         qx = (x == q.id) ? 1.f : 0.f;
         accept = (x == q.it) && (x == q.id);
       } else {
-        const char* rt = static_cast<const char*>(P.zt) +
-                         (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(lane) * P.t_rs) * E::ES;
-        const char* rd = static_cast<const char*>(P.zd) +
-                         (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(lane) * P.d_rs) * E::ES;
-        const float ztx = E::scalar(rt, x);
-        const float zdx = E::scalar(rd, x);
+        const float ztx = pre_zt[lane];
+        const float zdx = pre_zd[lane];
         const float lt = __fmul_rn(ztx - q.Mt, c);  // log2 of unnormalised p_i(x), q_i(x)
         const float ld = __fmul_rn(zdx - q.Md, c);
         const float St = static_cast<float>(q.St), Sd = static_cast<float>(q.Sd);
@@ -335,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         qx = __fdiv_rn(ex2(ld), Sd);
         if (zdx != neg_inf()) {  // q_i(x_i) > 0
           const float ratio = __fmul_rn(ex2(__fsub_rn(lt, ld)), __fdiv_rn(Sd, St));
-          accept = ratio >= P.unif[u0 + lane];
+          accept = ratio >= pre_u[lane];
         }
       }
     }
@@ -388,24 +465,6 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
     __syncthreads();
   }
 
-  // ---- outcome keys: lookaheads k = rank, rank + CB, ... ---------------------
-  // One warp per lookahead, all at once: warp w of CTA r merges lookaheads
-  // r + w*CB, r + (w + 8)*CB, ... (the chunk lists into the row's top-F).
-  if (kTopF) {
-    const bool ok = !(dec.status & kErrors);
-    for (int k = rank + warp * CB; k <= K; k += CB * kWarps) {
-      const int64_t u = u0 + k;
-      const WarpTopF L = merge_candidates(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
-                                          static_cast<int>(P.nchunk) * F, F, lane);
-      if (lane < F) {
-        const bool good = ok && L.i != INT_MAX;
-        P.keys[u * F + lane] = good ? L.i : -1;
-        if (P.key_logits) P.key_logits[u * F + lane] = good ? L.v : neg_inf();
-      }
-    }
-    __threadfence();  // keys visible to rank 0 after the cluster barrier below
-  }
-
   if (dec.need_scan) {
     const void* rowt = RC.rowt;
     const void* rowd = RC.rowd;
@@ -447,12 +506,12 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         double acc = 0.0;
         for (int sg = lane; sg < ntl * kWarps; sg += 32) acc += static_cast<double>(segs[sg]);
         acc = warp_dsum_all(acc);
-        if (lane == 0) cta_total = acc;
+        if (lane == 0) cta_total[attempt] = acc;
       }
       cluster_sync();  // (1) per-CTA totals visible; every CTA of the cluster has started
       if (!copies_ok && threadIdx.x == 0) *cluster.map_shared_rank(&copy_fail, 0) = 1;
       if (warp == 0) {
-        const double tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total, lane) : 0.0;
+        const double tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total[attempt], lane) : 0.0;
         double incl = tr;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -481,7 +540,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
           }
         }
       }
-      cluster_sync();  // (2) totals read everywhere (they may be rewritten)
+      __syncthreads();  // the decision on the owner, made by warp 0, seen by the CTA
       if (dec.owner >= 0 || attempt == 1 || dec.mode == 0) break;
     }
 
@@ -588,9 +647,26 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       if (lane == 0) *cluster.map_shared_rank(&tok_slot, 0) = tok;
     }
   }
-  // the owner's token (written into rank 0's shared memory after the first
-  // cluster barrier) and every CTA's keys visible to rank 0; every CTA passes
-  // here exactly once when a scan or keys ran.
+  // ---- outcome keys, while the owner CTA's warp 0 scans: warps 1..7 of CTA
+  // r merge lookaheads r, r + CB, ... (one warp each, all at once) -----------
+  if (kTopF && warp > 0) {
+    const bool ok = !(dec.status & kErrors);
+    for (int k = rank + (warp - 1) * CB; k <= K; k += CB * (kWarps - 1)) {
+      const int64_t u = u0 + k;
+      const WarpTopF L = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
+                                   static_cast<int>(P.nchunk) * F, F, lane, wkeys[warp]);
+      if (lane < F) {
+        const bool good = ok && L.i != INT_MAX;
+        P.keys[u * F + lane] = good ? L.i : -1;
+        if (P.key_logits) P.key_logits[u * F + lane] = good ? L.v : neg_inf();
+      }
+    }
+  }
+  // The barrier's release/acquire ordering (cluster scope) makes the owner's
+  // token (written into rank 0's shared memory after the first cluster
+  // barrier) and every CTA's key writes (global memory) visible to rank 0; no
+  // CTA exits while another may still read its shared memory.  Every CTA
+  // passes here exactly once when a scan or keys ran.
   if (dec.need_scan || kTopF) cluster_sync();
 
   // ---- outputs, written by rank 0 ---------------------------------------------
@@ -645,6 +721,7 @@ struct PredictKeysParams {
 
 __global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKeysParams P) {
   __shared__ int32_t status_all;
+  __shared__ WarpKeys wkeys[kWarps];
   const int b = blockIdx.x;
   const int K = P.K, F = P.F;
   const int lane = threadIdx.x & 31;
@@ -660,8 +737,8 @@ __global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKey
     const int x = (k < K) ? P.tokens[static_cast<int64_t>(b) * K + k] : 0;
     const int status = ((bad & 1) ? kNonFinite : 0) | ((bad & 2) ? kTimeout : 0) |
                        ((x < 0 || x >= P.V) ? kBadToken : 0);
-    const WarpTopF L = merge_candidates(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
-                                        P.nchunk * F, F, lane);
+    const WarpTopF L = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
+                                 P.nchunk * F, F, lane, wkeys[warp]);
     if (lane < F) {
       const bool good = status == 0 && L.i != INT_MAX;
       P.keys[u * F + lane] = good ? L.i : -1;

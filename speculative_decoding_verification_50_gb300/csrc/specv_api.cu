@@ -190,6 +190,19 @@ int ring_stages() {
   return n;
 }
 
+// Stages of the decision kernel's residual ring (SPECV_STAGES_B = 2..8 fixes
+// the count, for tuning runs).  Its grid is small (B x cluster CTAs), so each
+// CTA keeps more of its slice in flight than a row-statistics CTA does.
+int ring_stages_b() {
+  static int n = 0;
+  if (n == 0) {
+    const char* e = getenv("SPECV_STAGES_B");
+    const int v = e ? atoi(e) : 0;
+    n = (v >= 2 && v <= kMaxStages) ? v : 2;
+  }
+  return n;
+}
+
 // Persistent row-statistics kernel: as many CTAs as are resident at once on
 // the GPU (at most one per work item), each with the ring in dynamic shared
 // memory.  The occupancy query is made once per kernel and ring size.
@@ -382,7 +395,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   // segment sums in dynamic shared memory.
   // (Very long rows whose segment table leaves no room for it read directly.)
   dp.ring_off = static_cast<int32_t>(round_up(pl.smemB, 128));
-  dp.stages = ring_stages();
+  dp.stages = ring_stages_b();
   size_t smemB = dp.ring_off + static_cast<size_t>(dp.stages) * 2 * kTripBytes;
   if (!vec || smemB > kMaxSegSmem) {
     dp.stages = 0;

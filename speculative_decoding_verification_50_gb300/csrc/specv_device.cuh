@@ -168,22 +168,26 @@ __device__ __forceinline__ void warp_soft_all(float& m, float& s, float c) {
   s = t;
 }
 
-template <typename T>
+// Reductions over aligned groups of W lanes (W = 32: the whole warp), every
+// lane of a group ending with the group's result.  All 32 lanes must call.
+template <typename T, int W = 32>
 __device__ __forceinline__ T warp_max_all(T x) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
+  for (int o = W / 2; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
 }
 
+template <int W = 32>
 __device__ __forceinline__ double warp_dsum_all(double x) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  for (int o = W / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
 
+template <int W = 32>
 __device__ __forceinline__ void warp_arg_all(float& v, int32_t& i) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
+  for (int o = W / 2; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, v, o);
     const int32_t oi = __shfl_xor_sync(0xffffffffu, i, o);
     if (ov > v || (ov == v && oi < i)) {
