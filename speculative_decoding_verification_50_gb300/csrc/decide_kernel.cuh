@@ -366,6 +366,9 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       pre_u[i] = P.unif[u0 + i];
     }
   }
+  // Everything above reads only the call's inputs; the records below are
+  // the row-statistics kernel's output, so wait for it to complete here.
+  pdl_wait_primary();
   // Half a warp per position: positions 2w and 2w+1 on warp w, 16 per pass.
   for (int i0 = 2 * warp; i0 <= K; i0 += 2 * kWarps) {
     const int i = i0 + (lane >> 4);
@@ -728,6 +731,7 @@ __global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKey
   const int warp = threadIdx.x >> 5;
   const int64_t u0 = static_cast<int64_t>(b) * (K + 1);
   if (threadIdx.x == 0) status_all = 0;
+  pdl_wait_primary();  // records and candidates come from the row-statistics kernel
   __syncthreads();
   for (int k = warp; k <= K; k += kWarps) {
     const int64_t u = u0 + k;

@@ -100,13 +100,17 @@ cudaError_t launch_clustered(Kern k, int C, int64_t units, size_t smem, cudaStre
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // The kernel waits (griddepcontrol.wait) for the one before it on the
+  // stream, so it may be scheduled while that one drains.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(C);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
@@ -510,8 +514,19 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   kp.V = V;
   kp.F = F;
   kp.nchunk = static_cast<int32_t>(pl.nchunk);
-  predict_keys_kernel<<<B, kThreads, 0, s>>>(kp);
-  e = cudaGetLastError();
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, predict_keys_kernel, kp);
+  }
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "keys launch: %s", cudaGetErrorString(e));
   g_launches = 2;
   return ok();

@@ -251,6 +251,17 @@ __device__ __forceinline__ bool cons_sync_or(bool p) {
   return r != 0;
 }
 
+// Programmatic dependent launch: a kernel lets the next kernel on its stream
+// (launched with programmatic stream serialization) start early, and that
+// kernel waits for this one's completion -- memory included -- before it
+// touches this one's outputs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Split cluster barrier: arrive (release) now, wait (acquire) later.
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");

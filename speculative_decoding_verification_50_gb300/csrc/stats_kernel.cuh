@@ -662,6 +662,7 @@ template <int DT, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
   constexpr bool kT = MODE != kModePredict;
   __shared__ EpiSmem S;
+  pdl_launch_dependents();  // the decision kernel may be scheduled once every CTA has started
   const Chunk C = chunk_at<DT, MODE>(P, blockIdx.x);
   const float T = kT ? P.temp[C.b] : 0.f;
   const bool greedy = !kT || T == 0.f;
@@ -765,6 +766,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const Stats
   __shared__ RingBars R;
   __shared__ EpiSmem S;
   const int64_t items = static_cast<int64_t>(P.B) * (P.K + 1) * P.nchunk;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < P.stages; ++s) {
       mbar_init(&R.full[s], 1);
