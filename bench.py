@@ -482,7 +482,7 @@ def run_reference(args) -> None:
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)  # about 1 s timed at cfg5
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="cfg5-ssd", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
