@@ -61,8 +61,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.specv_oracle_verify.argtypes = [_I, _I, _I, _I, _P, _L, _L, _P, _L, _L,
                                         _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]
     lib.specv_oracle_predict.restype = _I
-    lib.specv_oracle_predict.argtypes = [_I, _I, _I, _I, _I, _P, _L, _L, _P, _P,
+    lib.specv_oracle_predict.argtypes = [_I, _I, _I, _I, _I, _P, _L, _L, _P, _P, _P,
                                          _P, _P, _I]
+    lib.specv_oracle_geometric_fanout.restype = _I
+    lib.specv_oracle_geometric_fanout.argtypes = [_I, ctypes.c_double, ctypes.c_double, _I, _I,
+                                                  _P, _P]
     lib.specv_oracle_check_hit.restype = None
     lib.specv_oracle_check_hit.argtypes = [_I, _I, _I, _P, _P, _P, _P]
     lib.specv_oracle_row_probs.restype = _I
@@ -127,8 +130,12 @@ def verify(target, draft, tokens, temperature, uniforms, nthreads: int = 1,
     return out
 
 
-def predict(draft, tokens, F: int, nthreads: int = 1, lib=None) -> dict:
-    """Top-F outcome keys from draft logits [B, K+1, V]; tokens int32 [B, K]."""
+def predict(draft, tokens, F: int, nthreads: int = 1, lib=None, fanout=None) -> dict:
+    """Top-F outcome keys from draft logits [B, K+1, V]; tokens int32 [B, K].
+
+    fanout (optional, K+1 ints in [0, F]): keep only the first fanout[k] keys
+    at lookahead k (the rest are -1).
+    """
     lib = lib or load()
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     B, K = tokens.shape
@@ -138,12 +145,27 @@ def predict(draft, tokens, F: int, nthreads: int = 1, lib=None) -> dict:
     key_logits = np.zeros((B, K + 1, F), np.float32)
     status = np.zeros(B, np.int32)
     dbs, drs = _strides(draft)
+    fan = None if fanout is None else np.ascontiguousarray(fanout, dtype=np.int32)
+    assert fan is None or fan.shape == (K + 1,)
     rc = lib.specv_oracle_predict(B, K, V, F, _dtype_code(draft), _ptr(draft),
-                                  dbs, drs, _ptr(tokens), _ptr(keys),
-                                  _ptr(key_logits), _ptr(status), int(nthreads))
+                                  dbs, drs, _ptr(tokens), None if fan is None else _ptr(fan),
+                                  _ptr(keys), _ptr(key_logits), _ptr(status), int(nthreads))
     if rc != 0:
         raise ValueError("oracle predict: bad sizes")
     return dict(keys=keys, key_logits=key_logits, status=status)
+
+
+def geometric_fanout(K: int, a: float, r: float, budget: int, max_f: int = 32,
+                     lib=None) -> tuple:
+    """[SSD] Theorem 12 fan-out: (integer F_k [K+1], real F_k [K+1])."""
+    lib = lib or load()
+    real = np.zeros(K + 1, np.float64)
+    fk = np.zeros(K + 1, np.int32)
+    rc = lib.specv_oracle_geometric_fanout(int(K), float(a), float(r), int(budget), int(max_f),
+                                           _ptr(real), _ptr(fk))
+    if rc != 0:
+        raise ValueError("oracle geometric_fanout: bad arguments")
+    return fk, real
 
 
 def check_hit(keys, accept_len, out_tokens, lib=None) -> np.ndarray:

@@ -282,9 +282,13 @@ static int cand_cmp(const void* a, const void* b) {
 
 int specv_oracle_predict(int B, int K, int V, int F, int dtype,
                          const void* draft, int64_t d_bs, int64_t d_rs,
-                         const int32_t* tokens, int32_t* keys, float* key_logits,
+                         const int32_t* tokens, const int32_t* fanout,
+                         int32_t* keys, float* key_logits,
                          int32_t* row_status, int nthreads) {
   if (B < 0 || K < 1 || V < 1 || F < 1) return 1;
+  if (fanout)
+    for (int k = 0; k <= K; ++k)
+      if (fanout[k] < 0 || fanout[k] > F) return 1;
 #ifdef _OPENMP
   if (nthreads <= 0) nthreads = omp_get_max_threads();
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
@@ -313,12 +317,60 @@ int specv_oracle_predict(int B, int K, int V, int F, int dtype,
       }
       if (bad) { status |= ROW_NONFINITE; continue; }
       qsort(c, (size_t)nc, sizeof(cand_t), cand_cmp);
-      for (int f = 0; f < F && f < nc; ++f) { kk[f] = c[f].v; kl[f] = (float)c[f].z; }
+      /* per-lookahead fan-out F_k (SSD Theorem 12) keeps the first F_k keys */
+      const int Fk = fanout ? fanout[k] : F;
+      for (int f = 0; f < Fk && f < nc; ++f) { kk[f] = c[f].v; kl[f] = (float)c[f].z; }
     }
     row_status[b] = status;
     free(c);
   }
   (void)nthreads;
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * f1  Geometric fan-out: [SSD] Theorem 12 (Saguaro cache shape), proved in
+ *     Appendix A.2 (Theorem 18).  For a drafter with acceptance rate a and an
+ *     r-th power-law cache hit rate (miss probability F^-r), the F_k that
+ *     maximise the hit rate under sum_k F_k <= budget are
+ *       F_k = F_0 a^{k/(1+r)}                       for k < K,
+ *       F_K = F_0 a^{K/(1+r)} (1 - a)^{-1/(1+r)},
+ *       F_0 = budget / (a^{K/(1+r)} (1-a)^{-1/(1+r)}
+ *                       + (1 - a^{K/(1+r)}) / (1 - a^{1/(1+r)})),
+ *     so that the F_k sum to the budget.  The pages leave integer rounding
+ *     open; the reading taken here: floor every F_k, give the budget left
+ *     over to the lookaheads with the largest fractional parts (lower k first
+ *     on ties), then cap each at max_f.  real[] (optional) receives F_k.
+ *     Returns 0, or 1 on arguments outside 0 < a < 1, r > 0, K >= 1,
+ *     budget >= 0, max_f >= 0.
+ */
+int specv_oracle_geometric_fanout(int K, double a, double r, int budget, int max_f,
+                                  double* real, int32_t* fk) {
+  if (K < 1 || !(a > 0.0 && a < 1.0) || !(r > 0.0) || budget < 0 || max_f < 0) return 1;
+  const double g = 1.0 / (1.0 + r);
+  const double aK = pow(a, K * g);
+  const double F0 = budget / (aK * pow(1.0 - a, -g) + (1.0 - aK) / (1.0 - pow(a, g)));
+  double* x = (double*)malloc(sizeof(double) * (size_t)(K + 1));
+  int used = 0;
+  for (int k = 0; k <= K; ++k) {
+    x[k] = (k < K) ? F0 * pow(a, k * g) : F0 * aK * pow(1.0 - a, -g);
+    if (real) real[k] = x[k];
+    fk[k] = (int32_t)floor(x[k]);
+    used += fk[k];
+  }
+  for (int left = budget - used; left > 0; --left) {
+    int best = -1;
+    double best_frac = -1.0;
+    for (int k = 0; k <= K; ++k) {
+      const double frac = x[k] - floor(x[k]);
+      if (fk[k] == (int32_t)floor(x[k]) && frac > best_frac) { best = k; best_frac = frac; }
+    }
+    if (best < 0) break;
+    fk[best] += 1;
+  }
+  for (int k = 0; k <= K; ++k)
+    if (fk[k] > max_f) fk[k] = max_f;
+  free(x);
   return 0;
 }
 

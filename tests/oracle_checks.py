@@ -465,6 +465,75 @@ def check_hit_constructed(lib):
     assert hit.tolist() == [1, 1, 1, 0]
 
 
+def _hit_objective(F, a: float, r: float):
+    """[SSD] Appendix A.2: the hit rate the fan-out maximises under an r-th
+    power-law miss model, a^K (1 - F_K^-r) + sum_{k<K} a^k (1-a) (1 - F_k^-r)."""
+    K = len(F) - 1
+    w = np.array([a ** k * (1 - a) for k in range(K)] + [a ** K])
+    return float(np.sum(w * (1.0 - np.asarray(F, float) ** (-r))))
+
+
+def check_fanout_optimal(lib):
+    """[SSD] Theorem 12: the closed-form F_k sum to the budget, satisfy the
+    Lagrange condition of Appendix A.2 (equal marginal hit rate at every k)
+    and match a library constrained optimiser (scipy SLSQP) on the objective."""
+    from scipy.optimize import minimize
+    for (K, a, r, budget) in [(4, 0.7, 1.0, 24), (8, 0.5, 0.7, 64), (3, 0.9, 2.0, 10),
+                              (6, 0.3, 1.5, 40)]:
+        _, x = oracle.geometric_fanout(K, a, r, budget, lib=lib)
+        assert abs(x.sum() - budget) < 1e-9 * budget
+        marg = [a ** k * (1 - a) * r * x[k] ** (-r - 1) for k in range(K)] + \
+               [a ** K * r * x[K] ** (-r - 1)]
+        assert np.ptp(marg) < 1e-9 * max(marg), (K, a, r, marg)
+        res = minimize(lambda F: -_hit_objective(F, a, r), np.full(K + 1, budget / (K + 1)),
+                       method="SLSQP", bounds=[(1e-3, budget)] * (K + 1),
+                       constraints=[{"type": "eq", "fun": lambda F: F.sum() - budget}],
+                       options={"ftol": 1e-14, "maxiter": 500})
+        assert res.success
+        np.testing.assert_allclose(x, res.x, rtol=2e-3, atol=2e-3)
+        assert _hit_objective(x, a, r) >= _hit_objective(res.x, a, r) - 1e-10
+    # the values of the formula at a = 0.7, r = 1, K = 4, budget = 24 (worked
+    # out from Theorem 12, not printed on the pages): 5.97 5.00 4.18 3.50 5.35
+    _, x = oracle.geometric_fanout(4, 0.7, 1.0, 24, lib=lib)
+    np.testing.assert_allclose(x, [5.97, 5.00, 4.18, 3.50, 5.35], atol=0.006)
+
+
+def check_fanout_rounding(lib):
+    """Integer fan-out (our reading of Theorem 12, which leaves rounding open):
+    floor, then the leftover budget to the largest fractional parts (lower k on
+    ties), then the cap; every F_k within 1 of the real value; sum = budget."""
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        K = int(rng.integers(1, 10))
+        a = float(rng.uniform(0.05, 0.95))
+        r = float(rng.uniform(0.2, 3.0))
+        budget = int(rng.integers(0, 200))
+        fk, x = oracle.geometric_fanout(K, a, r, budget, max_f=10 ** 6, lib=lib)
+        fl = np.floor(x).astype(int)
+        assert fk.sum() == budget and np.all(fk >= fl) and np.all(fk <= fl + 1)
+        frac = x - fl
+        up, down = frac[fk > fl], frac[fk == fl]
+        if len(up) and len(down):
+            assert up.min() >= down.max()
+        capped, _ = oracle.geometric_fanout(K, a, r, budget, max_f=3, lib=lib)
+        np.testing.assert_array_equal(capped, np.minimum(fk, 3))
+
+
+def check_predict_fanout(lib):
+    """Per-lookahead fan-out keeps the first F_k keys of each lookahead (the
+    rest -1): a prefix of the uniform top-F list."""
+    rng = np.random.default_rng(13)
+    B, K, V, F = 3, 4, 50, 6
+    z = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    full = oracle.predict(z, tok, F, lib=lib)
+    fan = np.array([6, 0, 3, 1, 5], np.int32)
+    part = oracle.predict(z, tok, F, lib=lib, fanout=fan)
+    for k in range(K + 1):
+        np.testing.assert_array_equal(part["keys"][:, k, :fan[k]], full["keys"][:, k, :fan[k]])
+        assert np.all(part["keys"][:, k, fan[k]:] == -1)
+
+
 ALL_CHECKS = {
     "softmax_library": check_softmax_library,
     "thm1_overlap": check_thm1_overlap,
@@ -482,4 +551,7 @@ ALL_CHECKS = {
     "predict_library_sort": check_predict_library_sort,
     "predict_exclusion": check_predict_exclusion,
     "hit_constructed": check_hit_constructed,
+    "fanout_optimal": check_fanout_optimal,
+    "fanout_rounding": check_fanout_rounding,
+    "predict_fanout": check_predict_fanout,
 }

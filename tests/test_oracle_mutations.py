@@ -63,6 +63,25 @@ MUTATIONS = {
         "return (x->v < y->v) ? -1 : (x->v > y->v);",
         "return (x->v > y->v) ? -1 : (x->v < y->v);",
         ["predict_library_sort"]),
+    # Theorem 12 with the (1 - a) factor of F_K dropped
+    "fanout_no_tail_factor": (
+        "x[k] = (k < K) ? F0 * pow(a, k * g) : F0 * aK * pow(1.0 - a, -g);",
+        "x[k] = (k < K) ? F0 * pow(a, k * g) : F0 * aK;",
+        ["fanout_optimal"]),
+    # exponent k/r instead of k/(1+r)
+    "fanout_wrong_exponent": (
+        "const double g = 1.0 / (1.0 + r);",
+        "const double g = 1.0 / r;",
+        ["fanout_optimal"]),
+    # leftover budget to the smallest fractional parts
+    "fanout_rounds_wrong_way": (
+        "if (fk[k] == (int32_t)floor(x[k]) && frac > best_frac) { best = k; best_frac = frac; }",
+        "if (fk[k] == (int32_t)floor(x[k]) && (best < 0 || frac < best_frac)) { best = k; best_frac = frac; }",
+        ["fanout_rounding"]),
+    "predict_fanout_ignored": (
+        "const int Fk = fanout ? fanout[k] : F;",
+        "const int Fk = F; (void)fanout;",
+        ["predict_fanout"]),
     "hit_wrong_length": (
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
