@@ -154,10 +154,14 @@ specv_status specv_verify_noalloc(const specv_verify_args* args, void* stream);
  */
 typedef struct {
   specv_verify_args verify;  /* draft rows: K+1 per batch row */
-  int32_t F;                 /* keys per lookahead, 1..32 */
+  int32_t F;                 /* keys per lookahead, 1..32 (the width of keys) */
   int32_t* keys;             /* OUT [B, K+1, F] */
   float* key_logits;         /* OUT, optional [B, K+1, F] */
   uint8_t* hit;              /* OUT [B] */
+  const int32_t* fanout;     /* optional HOST array [K+1]: keep only the first
+                                fanout[k] keys at lookahead k (0..F; the rest
+                                are -1), e.g. from specv_geometric_fanout.
+                                NULL: F keys at every lookahead. */
 } specv_ssd_args;
 
 size_t specv_ssd_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F,
@@ -184,6 +188,7 @@ typedef struct {
   int32_t* keys;                  /* OUT [B, K+1, F] */
   float* key_logits;              /* OUT, optional [B, K+1, F] (-inf pad) */
   int32_t* row_status;            /* OUT, optional [B] */
+  const int32_t* fanout;          /* optional HOST [K+1], as in specv_ssd_args */
 } specv_predict_args;
 
 size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V,
@@ -191,6 +196,24 @@ size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V,
 specv_status specv_predict_outcomes(const specv_predict_args* args,
                                     void* workspace, size_t workspace_bytes,
                                     void* stream);
+
+/*
+ * Geometric fan-out ("Speculative Speculative Decoding" Theorem 12, proved in
+ * Appendix A.2).  For a drafter with per-token acceptance rate a (0 < a < 1)
+ * whose cache-miss probability at fan-out F is F^-r (r > 0), the fan-outs
+ * maximising the hit rate under sum_k F_k <= budget are
+ *   F_k = F_0 a^{k/(1+r)} for k < K,   F_K = F_0 a^{K/(1+r)} (1-a)^{-1/(1+r)},
+ * with F_0 chosen so that they sum to budget.  The pages leave integer
+ * rounding open: fanout[k] = floor(F_k), plus one for the lookaheads with the
+ * largest fractional parts (lower k first on ties) until the budget is used,
+ * then capped at max_f (so the sum is budget unless the cap binds).
+ * Host-only: fanout (OUT [K+1]) and real (OUT, optional [K+1], the F_k before
+ * rounding) are host arrays; no GPU work.  SPECV_ERR_INVALID_ARG on K outside
+ * [1, 32], a outside (0, 1), r <= 0, budget < 0, max_f outside [0, 32] or a
+ * NULL fanout.
+ */
+specv_status specv_geometric_fanout(int32_t K, double a, double r, int32_t budget,
+                                    int32_t max_f, int32_t* fanout, double* real);
 
 /*
  * Cache-hit check ("Speculative Speculative Decoding" §3.1: hit iff the

@@ -42,13 +42,14 @@ class VerifyArgs(ctypes.Structure):
 
 class SsdArgs(ctypes.Structure):
     _fields_ = [("verify", VerifyArgs), ("F", _I32), ("keys", _P), ("key_logits", _P),
-                ("hit", _P)]
+                ("hit", _P), ("fanout", _P)]
 
 
 class PredictArgs(ctypes.Structure):
     _fields_ = [("B", _I32), ("K", _I32), ("V", _I32), ("F", _I32), ("dtype", _I32),
                 ("draft_logits", _P), ("draft_batch_stride", _I64), ("draft_row_stride", _I64),
-                ("draft_tokens", _P), ("keys", _P), ("key_logits", _P), ("row_status", _P)]
+                ("draft_tokens", _P), ("keys", _P), ("key_logits", _P), ("row_status", _P),
+                ("fanout", _P)]
 
 
 class SpecvError(RuntimeError):
@@ -82,6 +83,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specv_predict_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
     lib.specv_predict_outcomes.restype = ctypes.c_int
     lib.specv_predict_outcomes.argtypes = [ctypes.POINTER(PredictArgs), _P, ctypes.c_size_t, _P]
+    lib.specv_geometric_fanout.restype = ctypes.c_int
+    lib.specv_geometric_fanout.argtypes = [_I32, ctypes.c_double, ctypes.c_double, _I32, _I32,
+                                           _P, _P]
     lib.specv_check_hit.restype = ctypes.c_int
     lib.specv_check_hit.argtypes = [_I32, _I32, _I32, _P, _P, _P, _P, _P]
     lib.specv_status_string.restype = ctypes.c_char_p
@@ -202,15 +206,27 @@ def specv_verify_noalloc(target, draft, draft_tokens, temperature, uniforms, *, 
     return outs
 
 
+def _fanout_arg(fanout, K: int):
+    """A host int32 array [K+1] kept alive by the caller, or None."""
+    if fanout is None:
+        return None, None
+    vals = [int(x) for x in fanout]
+    assert len(vals) == K + 1, "fanout needs K+1 entries"
+    arr = (_I32 * (K + 1))(*vals)
+    return arr, ctypes.cast(arr, _P)
+
+
 def specv_ssd_round(target, draft, draft_tokens, temperature, uniforms, F: int, *,
                     accept_len=None, out_tokens=None, p_draft=None, q_draft=None,
                     row_status=None, keys=None, key_logits=None, hit=None, workspace=None,
-                    stream=None) -> dict:
+                    fanout=None, stream=None) -> dict:
     """One fused SSD round (see include/specv.h, specv_ssd_round): verification,
     top-F outcome keys at every lookahead and the hit flag, in one pass.
 
     draft must hold K+1 rows per batch row.  Returns the specv_verify outputs
     plus keys int32 [B, K+1, F], key_logits fp32 [B, K+1, F], hit uint8 [B].
+    fanout (optional, K+1 ints in [0, F], e.g. from specv_geometric_fanout)
+    keeps only the first fanout[k] keys at lookahead k.
     """
     import torch
     lib = load_library()
@@ -227,7 +243,8 @@ def specv_ssd_round(target, draft, draft_tokens, temperature, uniforms, F: int, 
     need = lib.specv_ssd_workspace_bytes(B, K, target.shape[-1], F, args.dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    sargs = SsdArgs(args, F, keys.data_ptr(), key_logits.data_ptr(), hit.data_ptr())
+    fan_keep, fan_ptr = _fanout_arg(fanout, K)
+    sargs = SsdArgs(args, F, keys.data_ptr(), key_logits.data_ptr(), hit.data_ptr(), fan_ptr)
     _check(lib.specv_ssd_round(ctypes.byref(sargs), _ptr(workspace), workspace.numel(),
                                _stream(stream)))
     outs.update(keys=keys, key_logits=key_logits, hit=hit)
@@ -235,7 +252,7 @@ def specv_ssd_round(target, draft, draft_tokens, temperature, uniforms, F: int, 
 
 
 def specv_predict_outcomes(draft, draft_tokens, F: int, *, keys=None, key_logits=None,
-                           row_status=None, workspace=None, stream=None) -> dict:
+                           row_status=None, workspace=None, fanout=None, stream=None) -> dict:
     """Top-F outcome keys per lookahead (see include/specv.h).
 
     draft [B, >=K+1, V] (bf16 or fp32, CUDA); draft_tokens int32 [B, K].
@@ -258,12 +275,23 @@ def specv_predict_outcomes(draft, draft_tokens, F: int, *, keys=None, key_logits
     need = lib.specv_predict_workspace_bytes(B, K, V, F, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    fan_keep, fan_ptr = _fanout_arg(fanout, K)
     args = PredictArgs(B, K, V, F, code, draft.data_ptr(), draft.stride(0), draft.stride(1),
                        draft_tokens.data_ptr(), keys.data_ptr(), key_logits.data_ptr(),
-                       row_status.data_ptr())
+                       row_status.data_ptr(), fan_ptr)
     _check(lib.specv_predict_outcomes(ctypes.byref(args), _ptr(workspace), workspace.numel(),
                                       _stream(stream)))
     return dict(keys=keys, key_logits=key_logits, row_status=row_status)
+
+
+def specv_geometric_fanout(K: int, a: float, r: float, budget: int, max_f: int = 32) -> tuple:
+    """Theorem 12 fan-out (see include/specv.h): (integer F_k list, real F_k list)."""
+    lib = load_library()
+    fk = (_I32 * (K + 1))()
+    real = (ctypes.c_double * (K + 1))()
+    _check(lib.specv_geometric_fanout(int(K), float(a), float(r), int(budget), int(max_f),
+                                      ctypes.cast(fk, _P), ctypes.cast(real, _P)))
+    return list(fk), list(real)
 
 
 def specv_check_hit(keys, accept_len, out_tokens, *, hit=None, stream=None):

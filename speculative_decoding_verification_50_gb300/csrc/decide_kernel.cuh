@@ -65,6 +65,7 @@ struct DecideParams {
   float* key_logits;
   uint8_t* hit;
   int32_t B, K, V, F, nchunk, CB, L;
+  int32_t fk[kMaxK + 1];  // keys kept at lookahead k (F when the fan-out is uniform)
   int32_t stages;    // ring stages of the staged residual pass (aligned rows); 0: none
   int32_t ring_off;  // byte offset of that ring in dynamic shared memory
 };
@@ -659,7 +660,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       const WarpTopF L = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
                                    static_cast<int>(P.nchunk) * F, F, lane, wkeys[warp]);
       if (lane < F) {
-        const bool good = ok && L.i != INT_MAX;
+        const bool good = ok && lane < P.fk[k] && L.i != INT_MAX;
         P.keys[u * F + lane] = good ? L.i : -1;
         if (P.key_logits) P.key_logits[u * F + lane] = good ? L.v : neg_inf();
       }
@@ -720,6 +721,7 @@ struct PredictKeysParams {
   float* key_logits;
   int32_t* row_status;
   int32_t B, K, V, F, nchunk;
+  int32_t fk[kMaxK + 1];  // keys kept at lookahead k
 };
 
 __global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKeysParams P) {
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKey
     const WarpTopF L = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
                                  P.nchunk * F, F, lane, wkeys[warp]);
     if (lane < F) {
-      const bool good = status == 0 && L.i != INT_MAX;
+      const bool good = status == 0 && lane < P.fk[k] && L.i != INT_MAX;
       P.keys[u * F + lane] = good ? L.i : -1;
       if (P.key_logits) P.key_logits[u * F + lane] = good ? L.v : neg_inf();
     }

@@ -1,6 +1,7 @@
 // C ABI of libspecv (declared in include/specv.h): argument checks, workspace
 // sizing, cluster-size choice and kernel launches on the caller's stream.
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -321,7 +322,7 @@ namespace {
 
 specv_status run_verify(const specv_verify_args* a, void* workspace, size_t workspace_bytes,
                         void* stream, int mode, int32_t F, int32_t* keys, float* key_logits,
-                        uint8_t* hit) {
+                        uint8_t* hit, const int32_t* fanout) {
   const int32_t B = a->B, K = a->K, V = a->V;
   const Plan pl = make_plan(B, K, V, mode == kModeSsd ? F : 0, a->dtype);
   if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
@@ -395,6 +396,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   dp.nchunk = static_cast<int32_t>(pl.nchunk);
   dp.CB = pl.CB;
   dp.L = static_cast<int32_t>(pl.L);
+  for (int k = 0; k <= K; ++k) dp.fk[k] = fanout ? fanout[k] : F;
   // Aligned rows stream the residual slice through a ring placed after the
   // segment sums in dynamic shared memory.
   // (Very long rows whose segment table leaves no room for it read directly.)
@@ -422,7 +424,7 @@ specv_status specv_verify(const specv_verify_args* a, void* workspace, size_t wo
   if (st != SPECV_OK) return st;
   if (a->B == 0) return ok();
   return run_verify(a, workspace, workspace_bytes, stream, kModeVerify, 0, nullptr, nullptr,
-                    nullptr);
+                    nullptr, nullptr);
 }
 
 size_t specv_ssd_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
@@ -441,8 +443,12 @@ specv_status specv_ssd_round(const specv_ssd_args* a, void* workspace, size_t wo
   if (!a->keys || !a->hit) return fail(SPECV_ERR_INVALID_ARG, "keys or hit is NULL");
   if (!aligned(a->keys, 4) || !aligned(a->key_logits, 4))
     return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
+  if (a->fanout)
+    for (int k = 0; k <= a->verify.K; ++k)
+      if (a->fanout[k] < 0 || a->fanout[k] > a->F)
+        return fail(SPECV_ERR_INVALID_ARG, "fanout[%d]=%d outside [0, F=%d]", k, a->fanout[k], a->F);
   return run_verify(&a->verify, workspace, workspace_bytes, stream, kModeSsd, a->F, a->keys,
-                    a->key_logits, a->hit);
+                    a->key_logits, a->hit, a->fanout);
 }
 
 size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
@@ -461,6 +467,10 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   if (F < 1 || F > 32) return fail(SPECV_ERR_INVALID_ARG, "F=%d outside [1, 32]", F);
   if (a->dtype != SPECV_BF16 && a->dtype != SPECV_FP32)
     return fail(SPECV_ERR_INVALID_ARG, "dtype=%d is not SPECV_BF16 or SPECV_FP32", a->dtype);
+  if (a->fanout)
+    for (int k = 0; k <= K; ++k)
+      if (a->fanout[k] < 0 || a->fanout[k] > F)
+        return fail(SPECV_ERR_INVALID_ARG, "fanout[%d]=%d outside [0, F=%d]", k, a->fanout[k], F);
   if (B == 0) return ok();
   if (!a->draft_logits || !a->draft_tokens || !a->keys)
     return fail(SPECV_ERR_INVALID_ARG, "a required pointer is NULL");
@@ -514,6 +524,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   kp.V = V;
   kp.F = F;
   kp.nchunk = static_cast<int32_t>(pl.nchunk);
+  for (int k = 0; k <= K; ++k) kp.fk[k] = a->fanout ? a->fanout[k] : F;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
@@ -529,6 +540,52 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "keys launch: %s", cudaGetErrorString(e));
   g_launches = 2;
+  return ok();
+}
+
+// Theorem 12 of "Speculative Speculative Decoding": F_k = F_0 q^k (k < K) and
+// F_K = F_0 q^K t with q = a^{1/(1+r)}, t = (1-a)^{-1/(1+r)}; the budget
+// fixes F_0 = budget / (q^K t + sum_{k<K} q^k).  Rounded by largest remainder.
+specv_status specv_geometric_fanout(int32_t K, double a, double r, int32_t budget, int32_t max_f,
+                                    int32_t* fanout, double* real) {
+  if (K < 1 || K > 32) return fail(SPECV_ERR_INVALID_ARG, "K=%d outside [1, 32]", K);
+  if (!(a > 0.0 && a < 1.0)) return fail(SPECV_ERR_INVALID_ARG, "a=%g outside (0, 1)", a);
+  if (!(r > 0.0) || !(r < 1e300)) return fail(SPECV_ERR_INVALID_ARG, "r=%g is not positive", r);
+  if (budget < 0) return fail(SPECV_ERR_INVALID_ARG, "budget=%d < 0", budget);
+  if (max_f < 0 || max_f > 32) return fail(SPECV_ERR_INVALID_ARG, "max_f=%d outside [0, 32]", max_f);
+  if (!fanout) return fail(SPECV_ERR_INVALID_ARG, "fanout is NULL");
+  const double q = std::pow(a, 1.0 / (1.0 + r));
+  const double t = std::pow(1.0 - a, -1.0 / (1.0 + r));
+  double head = 0.0, qk = 1.0;  // sum_{k<K} q^k
+  for (int k = 0; k < K; ++k) {
+    head += qk;
+    qk *= q;
+  }
+  const double f0 = static_cast<double>(budget) / (qk * t + head);
+  double x[33];
+  int32_t whole[33];
+  int64_t left = budget;
+  double w = f0;
+  for (int k = 0; k <= K; ++k) {
+    x[k] = (k < K) ? w : w * t;
+    w *= q;
+    whole[k] = static_cast<int32_t>(std::floor(x[k]));
+    left -= whole[k];
+    fanout[k] = whole[k];
+    if (real) real[k] = x[k];
+  }
+  // the leftover budget, one each, to the largest fractional parts
+  while (left > 0) {
+    int pick = -1;
+    for (int k = 0; k <= K; ++k) {
+      if (fanout[k] != whole[k]) continue;
+      if (pick < 0 || x[k] - whole[k] > x[pick] - whole[pick]) pick = k;
+    }
+    if (pick < 0) break;
+    ++fanout[pick];
+    --left;
+  }
+  for (int k = 0; k <= K; ++k) fanout[k] = std::min(fanout[k], max_f);
   return ok();
 }
 
@@ -611,5 +668,5 @@ extern "C" specv_status specv_verify_noalloc(const specv_verify_args* a, void* s
   // Every record kernel B reads is written by kernel A earlier in this same
   // call, so nothing in the scratch has to start at zero.
   return run_verify(a, ws, kNoAllocScratchBytes, stream, kModeVerify, 0, nullptr, nullptr,
-                    nullptr);
+                    nullptr, nullptr);
 }

@@ -137,11 +137,12 @@ def test_struct_layouts_match_the_header(tmp_path):
 #include <stdio.h>
 #include "specv.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(specv_verify_args),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(specv_verify_args),
          offsetof(specv_verify_args, target_logits), offsetof(specv_verify_args, draft_tokens),
          offsetof(specv_verify_args, row_status), sizeof(specv_ssd_args),
          offsetof(specv_ssd_args, keys), sizeof(specv_predict_args),
-         offsetof(specv_predict_args, row_status));
+         offsetof(specv_predict_args, row_status), offsetof(specv_ssd_args, fanout),
+         offsetof(specv_predict_args, fanout));
   return 0;
 }
 ''')
@@ -151,7 +152,8 @@ int main(void) {
     want = [ctypes.sizeof(sv.VerifyArgs), sv.VerifyArgs.target_logits.offset,
             sv.VerifyArgs.draft_tokens.offset, sv.VerifyArgs.row_status.offset,
             ctypes.sizeof(sv.SsdArgs), sv.SsdArgs.keys.offset, ctypes.sizeof(sv.PredictArgs),
-            sv.PredictArgs.row_status.offset]
+            sv.PredictArgs.row_status.offset, sv.SsdArgs.fanout.offset,
+            sv.PredictArgs.fanout.offset]
     assert got == want
 
 
@@ -172,3 +174,49 @@ def test_unsupported_vocabulary_size(lib):
     a = _args(V=V, target_row_stride=V, draft_row_stride=V,
               target_batch_stride=4 * V, draft_batch_stride=3 * V)
     assert lib.specv_verify(ctypes.byref(a), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_UNSUPPORTED
+
+
+def test_ssd_round_and_predict_reject_bad_fanout(lib):
+    a = _args()
+    for bad in ([1, 2, 7, 1], [1, -1, 0, 0]):  # F = 6: entries must lie in [0, 6]
+        arr = (ctypes.c_int32 * 4)(*bad)
+        s = sv.SsdArgs(a, 6, 0x10000, 0, 0x10000, ctypes.cast(arr, ctypes.c_void_p))
+        assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+        p = sv.PredictArgs(2, 3, 100, 6, sv.SPECV_BF16, 0x10000, 400, 100, 0x10000, 0x10000, 0, 0,
+                           ctypes.cast(arr, ctypes.c_void_p))
+        assert lib.specv_predict_outcomes(ctypes.byref(p), None, 0, None) == sv.SPECV_ERR_INVALID_ARG
+
+
+def test_geometric_fanout_matches_the_oracle(lib):
+    """Host-only entry point: the library's Theorem 12 fan-out equals the
+    oracle's, real values to 1e-12 and integers exactly (up to exact ties of
+    fractional parts, where either choice is the same reading)."""
+    import numpy as np
+    import oracle
+    olib = oracle.load()
+    rng = np.random.default_rng(21)
+    for _ in range(300):
+        K = int(rng.integers(1, 33))
+        a = float(rng.uniform(0.01, 0.99))
+        r = float(rng.uniform(0.1, 4.0))
+        budget = int(rng.integers(0, 400))
+        max_f = int(rng.integers(0, 33))
+        fk, real = sv.specv_geometric_fanout(K, a, r, budget, max_f)
+        ofk, oreal = oracle.geometric_fanout(K, a, r, budget, max_f, lib=olib)
+        np.testing.assert_allclose(real, oreal, rtol=1e-12, atol=1e-12)
+        if list(fk) != list(ofk):
+            frac = np.sort(oreal - np.floor(oreal))
+            assert np.min(np.diff(frac)) < 1e-9, (K, a, r, budget, fk, ofk)
+    fk, real = sv.specv_geometric_fanout(4, 0.7, 1.0, 24)
+    assert fk == [6, 5, 4, 4, 5] and abs(sum(real) - 24) < 1e-12
+
+
+def test_geometric_fanout_rejects_bad_arguments(lib):
+    out = (ctypes.c_int32 * 40)()
+    ptr = ctypes.cast(out, ctypes.c_void_p)
+    for args in ((0, 0.5, 1.0, 10, 8), (33, 0.5, 1.0, 10, 8), (4, 0.0, 1.0, 10, 8),
+                 (4, 1.0, 1.0, 10, 8), (4, 0.5, 0.0, 10, 8), (4, 0.5, 1.0, -1, 8),
+                 (4, 0.5, 1.0, 10, 33)):
+        assert lib.specv_geometric_fanout(*args, ptr, None) == sv.SPECV_ERR_INVALID_ARG, args
+    assert lib.specv_geometric_fanout(4, 0.5, 1.0, 10, 8, None, None) == sv.SPECV_ERR_INVALID_ARG
+    assert lib.specv_geometric_fanout(4, 0.5, 1.0, 10, 8, ptr, None) == sv.SPECV_OK

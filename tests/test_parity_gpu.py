@@ -325,9 +325,9 @@ def test_repeated_calls_are_deterministic(sv):
 # ---------------------------------------------------------------------------
 # the fused SSD round: verification + top-F keys + hit in one pass
 
-def oracle_ssd(olib, data, F):
+def oracle_ssd(olib, data, F, fanout=None):
     o = oracle_verify(olib, data)
-    op = oracle.predict(data["draft"], data["tokens"], F, nthreads=0, lib=olib)
+    op = oracle.predict(data["draft"], data["tokens"], F, nthreads=0, lib=olib, fanout=fanout)
     o["status"] = o["status"] | op["status"]
     err = (o["status"] & oracle.ROW_ERRORS) != 0
     # a flagged batch row of an SSD round has no outcome (header contract)
@@ -342,12 +342,13 @@ def oracle_ssd(olib, data, F):
     return o, keys, kl
 
 
-def gpu_ssd(sv, data, F, target=None, draft=None):
+def gpu_ssd(sv, data, F, target=None, draft=None, fanout=None):
     spec = data["spec"]
     tgt = to_dev(data["target"], spec.dtype) if target is None else target
     dft = to_dev(data["draft"], spec.dtype) if draft is None else draft
     out = sv.specv_ssd_round(tgt, dft, to_dev(data["tokens"], None),
-                             to_dev(data["temperature"], None), to_dev(data["uniforms"], None), F)
+                             to_dev(data["temperature"], None), to_dev(data["uniforms"], None), F,
+                             fanout=fanout)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}
 
@@ -382,6 +383,45 @@ def test_ssd_round_cfg5_full_size_sampled(sv, olib):
     gs = {k: v[rows] for k, v in g.items()}
     compare_ssd(olib, gs, o, keys, kl, sub["temperature"], "ssd cfg5")
     print(f"ssd cfg5: hit rate (all rows) {g['hit'].mean():.3f}")
+
+
+@pytest.mark.parametrize("a,r,budget", [(0.6, 1.0, 30), (0.9, 0.5, 12), (0.3, 2.0, 5)])
+def test_ssd_round_geometric_fanout(sv, olib, a, r, budget):
+    """Config 4 with the Theorem 12 fan-out: F_k keys at lookahead k (the rest
+    -1) and the hit flag against those keys."""
+    spec = wl.SPECS["cfg4"]
+    data = wl.generate(spec)
+    fan, _ = sv.specv_geometric_fanout(spec.K, a, r, budget)
+    F = max(1, max(fan))
+    g = gpu_ssd(sv, data, F, fanout=fan)
+    o, keys, kl = oracle_ssd(olib, data, F, fanout=fan)
+    compare_ssd(olib, g, o, keys, kl, data["temperature"], f"ssd fanout {fan}")
+    for k, f in enumerate(fan):
+        assert (g["keys"][:, k, f:] == -1).all()
+    pr = sv.specv_predict_outcomes(to_dev(data["draft"], spec.dtype), to_dev(data["tokens"], None),
+                                   F, fanout=fan)
+    torch.cuda.synchronize()
+    op = oracle.predict(data["draft"], data["tokens"], F, nthreads=0, lib=olib, fanout=fan)
+    assert np.array_equal(pr["keys"].cpu().numpy(), op["keys"])
+    assert np.array_equal(pr["key_logits"].cpu().numpy(), op["key_logits"])
+    print(f"fanout {fan}: hit rate {g['hit'].mean():.3f}")
+
+
+def test_ssd_round_cfg5_geometric_fanout_sampled(sv, olib):
+    """Config 5 sizes, K+1 draft rows, Theorem 12 fan-out over a budget of 48
+    keys (a = 0.5, r = 1): 16 sampled rows against the oracle."""
+    import dataclasses
+    spec = dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd", ssd=True, F=6)
+    data = wl.generate(spec)
+    fan, _ = sv.specv_geometric_fanout(spec.K, 0.5, 1.0, 48)
+    F = max(fan)
+    g = gpu_ssd(sv, data, F, fanout=fan)
+    rows = np.random.default_rng(2).choice(spec.B, 16, replace=False)
+    sub = {k: (v[rows] if isinstance(v, np.ndarray) and v.shape[:1] == (spec.B,) else v)
+           for k, v in data.items()}
+    o, keys, kl = oracle_ssd(olib, sub, F, fanout=fan)
+    gs = {k: v[rows] for k, v in g.items()}
+    compare_ssd(olib, gs, o, keys, kl, sub["temperature"], "ssd cfg5 fanout")
 
 
 @pytest.mark.parametrize("B,K,V,dtype,F", [
