@@ -47,6 +47,9 @@ WORKLOADS = {
     "cfg5-ssd": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd", ssd=True, F=6),
                  "config 5 (B=256, K=8, V=152064, fp32 Zipf-like logits) as a full SSD round: "
                  "verify + top-6 outcome keys at K+1 lookaheads + hit check"),
+    "cfg5-ssd-geo": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd-geo", ssd=True, F=6),
+                     "config 5 as a full SSD round with the Theorem 12 geometric fan-out "
+                     "(a=0.5, r=1, 54 keys over the K+1 lookaheads) + hit check"),
     "cfg5": (wl.SPECS["cfg5"], "config 5 (B=256, K=8, V=152064, fp32 Zipf-like logits), verify only"),
     "cfg4": (wl.SPECS["cfg4"], "config 4 (B=32, K=4, V=128256, bf16, F=6): verify + predict + hit"),
     "cfg3": (wl.SPECS["cfg3"], "config 3 (B=64, K=4, V=128256, bf16, T in {0,0.6,1}), verify only"),
@@ -54,6 +57,10 @@ WORKLOADS = {
     "cfg2b": (wl.SPECS["cfg2b"], "config 2b (B=1, K=5, V=128256, bf16, T=0.7), verify only"),
     "cfg1": (wl.SPECS["cfg1"], "config 1 (B=1, K=4, V=4096, fp32, T=1), verify only"),
 }
+
+# Workloads whose keys follow the geometric fan-out: (acceptance rate a,
+# power-law exponent r, key budget over the K+1 lookaheads).
+GEOMETRIC = {"cfg5-ssd-geo": (0.5, 1.0, 54)}
 
 KERNEL_DIR = os.path.join(ROOT, "speculative_decoding_verification_50_gb300", "csrc")
 # Sources of the row-statistics kernel, the one the roofline reports on.
@@ -258,6 +265,11 @@ def run_ours(args) -> None:
     if args.batch:
         spec = dataclasses.replace(spec, B=args.batch)
         desc += f" [B overridden to {args.batch}]"
+    fanout = None
+    if args.workload in GEOMETRIC:
+        fanout, _ = sv.specv_geometric_fanout(spec.K, *GEOMETRIC[args.workload], max_f=32)
+        spec = dataclasses.replace(spec, F=max(1, max(fanout)))
+        desc += f" [F_k = {fanout}]"
     data = wl.generate(spec, rows=shard_rows(rank, world, spec.B))
     B, K, V, F = spec.B, spec.K, spec.V, spec.F
     is_bf16 = spec.dtype == wl.BF16
@@ -297,7 +309,8 @@ def run_ours(args) -> None:
             ev[0].record(stream)
         if F:  # the fused SSD round: verify + outcome keys + hit in one pass
             sv.specv_ssd_round(d_target, d_draft, d_tok, d_temp, d_unif, F, keys=keys,
-                               key_logits=key_logits, hit=hit, workspace=ws_v, **outs)
+                               key_logits=key_logits, hit=hit, workspace=ws_v, fanout=fanout,
+                               **outs)
         else:
             sv.specv_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
         launches[0] += sv.last_launch_count()
@@ -404,6 +417,7 @@ def run_ours(args) -> None:
         "config": {
             "workload": f"{args.workload}: {desc}",
             "B_per_gpu": B, "K": K, "V": V, "logits": spec.dtype, "F": F,
+            **({"fanout": fanout} if fanout else {}),
             "rows_per_step_per_gpu": B * (K + 1),
             "l2": (f"inputs {in_bytes / 1e9:.2f} GB > {L2_BYTES / 2**20:.0f} MiB L2, no flush"
                    if in_bytes > L2_BYTES else "inputs fit in L2: numbers are L2-hot"),

@@ -152,21 +152,52 @@ struct ArgG {
   }
 };
 
+// Outcome prediction: the group holding this thread's largest draft logit,
+// kept in registers (m1, its trip t1, its logits z), and the largest maximum
+// of the thread's other groups (m2), all updated without a branch.  A thread
+// whose m2 is below a bound holds every logit at or above it in z.
+template <int N>
+struct BestGroup {
+  float m1, m2;
+  int t1;
+  float z[N];
+  __device__ __forceinline__ void init() {
+    m1 = m2 = neg_inf();
+    t1 = 0;
+#pragma unroll
+    for (int k = 0; k < N; ++k) z[k] = neg_inf();
+  }
+  __device__ __forceinline__ void add(const float (&zz)[N], int t) {
+    const float vm = group_max(zz, neg_inf());  // NaN ignored
+    const bool nb = vm > m1;
+    m2 = nb ? m1 : fmaxf(m2, vm);
+    t1 = nb ? t : t1;
+    m1 = nb ? vm : m1;
+#pragma unroll
+    for (int k = 0; k < N; ++k) z[k] = nb ? zz[k] : z[k];
+  }
+};
+
 template <int VW>
 struct Acc {
   static constexpr int N = kVecs * VW;
-  SoftG<N> st, sd;  // temperature rows: target, draft
-  ArgG<N> at, ad;   // greedy rows: target, draft
+  SoftG<N> st, sd;   // temperature rows: target, draft
+  ArgG<N> at, ad;    // greedy rows: target, draft
+  BestGroup<N> kd;   // draft row, outcome prediction
   __device__ __forceinline__ void init() {
     st.init();
     sd.init();
     at.init();
     ad.init();
+    kd.init();
   }
-  template <bool GREEDY, bool DRAFT>
-  __device__ __forceinline__ void add(const float (&z)[N], const int32_t (&base)[kVecs], float c) {
+  // Group of trip t of the target (DRAFT = false) or draft row.
+  template <bool GREEDY, bool DRAFT, bool TOPF>
+  __device__ __forceinline__ void add(const float (&z)[N], const int32_t (&base)[kVecs], float c,
+                                      int t) {
     if (GREEDY) (DRAFT ? ad : at).template add<VW>(z, base);
     else (DRAFT ? sd : st).add(z, c);
+    if (DRAFT && TOPF) kd.add(z, t);
   }
 };
 
@@ -196,7 +227,7 @@ __device__ __forceinline__ void load_trip(const void* row, int64_t v0, int64_t v
   }
 }
 
-template <int DT, bool GREEDY, bool DRAFT>
+template <int DT, bool GREEDY, bool DRAFT, bool TOPF>
 __device__ __forceinline__ void consume_trip(const typename Elem<DT>::Vec (&w)[kVecs], int nv,
                                              int it, int64_t v0, float c, Acc<Elem<DT>::VW>& A) {
   constexpr int VW = Elem<DT>::VW;
@@ -208,11 +239,11 @@ __device__ __forceinline__ void consume_trip(const typename Elem<DT>::Vec (&w)[k
     base[k] = static_cast<int32_t>(v0) + j * VW;
     if (j < nv) put_vec<DT>(z + k * VW, w[k]); else put_none<DT>(z + k * VW);
   }
-  A.template add<GREEDY, DRAFT>(z, base, c);
+  A.template add<GREEDY, DRAFT, TOPF>(z, base, c, it);
 }
 
 // Streams the CTA's chunk of one or two rows (software-pipelined).
-template <int DT, bool VEC, bool GREEDY, bool KT>
+template <int DT, bool VEC, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ void stream_chunk(const void* rowt, const void* rowd, bool has_d,
                                              int64_t v0, int64_t v1, int nv, int iters, float c,
                                              Acc<Elem<DT>::VW>& A) {
@@ -225,15 +256,15 @@ __device__ __forceinline__ void stream_chunk(const void* rowt, const void* rowd,
       if (KT) load_trip<DT, VEC>(rowt, v0, v1, nv, it + 1, at1);
       if (has_d) load_trip<DT, VEC>(rowd, v0, v1, nv, it + 1, ad1);
     }
-    if (KT) consume_trip<DT, GREEDY, false>(at0, nv, it, v0, c, A);
-    if (has_d) consume_trip<DT, GREEDY, true>(ad0, nv, it, v0, c, A);
+    if (KT) consume_trip<DT, GREEDY, false, TOPF>(at0, nv, it, v0, c, A);
+    if (has_d) consume_trip<DT, GREEDY, true, TOPF>(ad0, nv, it, v0, c, A);
     if (it + 1 < iters) {
       if (it + 2 < iters) {
         if (KT) load_trip<DT, VEC>(rowt, v0, v1, nv, it + 2, at0);
         if (has_d) load_trip<DT, VEC>(rowd, v0, v1, nv, it + 2, ad0);
       }
-      if (KT) consume_trip<DT, GREEDY, false>(at1, nv, it + 1, v0, c, A);
-      if (has_d) consume_trip<DT, GREEDY, true>(ad1, nv, it + 1, v0, c, A);
+      if (KT) consume_trip<DT, GREEDY, false, TOPF>(at1, nv, it + 1, v0, c, A);
+      if (has_d) consume_trip<DT, GREEDY, true, TOPF>(ad1, nv, it + 1, v0, c, A);
     }
   }
 }
@@ -274,7 +305,8 @@ __device__ __forceinline__ Chunk chunk_at(const StatsParams& P, int64_t item) {
 // Shared scratch of a chunk's epilogue.
 struct EpiSmem {
   ChunkRec wrec[kWarps];
-  float wthr[kWarps];
+  float wthr[kWarps];    // each warp's g-th largest per-thread maximum
+  float wthr_f[kWarps];  // each warp's (F+1)-th largest
   float wl_v[kWarps][kMaxF];
   int32_t wl_i[kWarps][kMaxF];
   KeyScratch KS;
@@ -327,10 +359,12 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
       S.KS.out_v[threadIdx.x] = neg_inf();
       S.KS.out_i[threadIdx.x] = INT_MAX;
     }
-    // (F+1)-th largest per-thread maximum of this warp (bitonic sort of the
-    // 32 maxima): F+1 distinct logits reach it, so at least F of them are not
-    // the excluded token -- a lower bound on the chunk's top-F without it.
-    float s = greedy ? A.ad.best : A.sd.m;  // this thread's draft maximum
+    // Bound: with g = ceil((F+1)/8), every warp holds g distinct logits at or
+    // above its g-th largest per-thread maximum (bitonic sort of the 32
+    // maxima), so at least 8g >= F+1 distinct logits reach the smallest of
+    // the eight, and at least F of them are not the excluded token: a lower
+    // bound on the chunk's top-F without it.
+    float s = A.kd.m1;  // this thread's draft maximum
 #pragma unroll
     for (int k2 = 2; k2 <= 32; k2 <<= 1) {
 #pragma unroll
@@ -340,8 +374,14 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
         s = take_max ? fmaxf(s, o) : fminf(s, o);
       }
     }
-    const float tw = (P.F < 32) ? __shfl_sync(0xffffffffu, s, P.F) : neg_inf();
-    if (lane == 0) S.wthr[warp] = tw;
+    const float tw = __shfl_sync(0xffffffffu, s, (P.F + kWarps) / kWarps - 1);
+    // Fallback when some warp holds fewer than g finite maxima (a short last
+    // chunk): the largest, over warps, of a warp's (F+1)-th largest maximum.
+    const float tf = (P.F < 32) ? __shfl_sync(0xffffffffu, s, P.F) : neg_inf();
+    if (lane == 0) {
+      S.wthr[warp] = tw;
+      S.wthr_f[warp] = tf;
+    }
   }
   const bool copy_bad = cons_sync_or(!ok);  // a chunk copy gave up on some thread
   if (warp == 0) {
@@ -377,21 +417,35 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
   if (kTopF) {
     // Every draft logit of the chunk at or above the bound, the excluded token
     // left out, goes into a shared buffer ranked in parallel.  Only threads
-    // whose maximum reaches the bound can hold one; their shares are read
-    // again (from L2, just streamed) by their whole warp at once -- lane l
-    // fetches vector l, l+32, ... of the list (candidate, vector k) -- so the
-    // warp pays one round trip for all its candidates.  Too many qualifiers
-    // (ties at the bound), or no finite bound at all (F = 32, masked rows),
-    // take the exact warp-list path.
+    // whose maximum reaches the bound can hold one.  If the thread's other
+    // groups all stay below the bound, its qualifying logits are all in the
+    // group it kept in registers and it pushes them from there; otherwise
+    // (rare) its share is read again by its whole warp at once -- lane l
+    // fetches vector l, l+32, ... of the list (candidate, vector k).  Too many
+    // qualifiers (ties at the bound), or no finite bound at all (masked rows,
+    // chunks with fewer than F+1 finite logits), take the exact warp-list path.
     const int F = P.F;
     const int excl = (C.i < P.K) ? P.tokens[static_cast<int64_t>(C.b) * P.K + C.i] : -1;
-    float thr = S.wthr[0];
+    float thr = S.wthr[0], thr_f = S.wthr_f[0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) thr = fmaxf(thr, S.wthr[w]);
+    for (int w = 1; w < kWarps; ++w) {
+      thr = fminf(thr, S.wthr[w]);
+      thr_f = fmaxf(thr_f, S.wthr_f[w]);
+    }
+    if (!(thr > kNegMax)) thr = thr_f;
     const bool bounded = thr > kNegMax;
     const int ntrips = P.iters * kVecs;  // vectors per thread per row
-    const float tmax_d = greedy ? A.ad.best : A.sd.m;
-    const unsigned cm = __ballot_sync(0xffffffffu, bounded && tmax_d >= thr);
+    const bool cand = bounded && A.kd.m1 >= thr;
+    const bool reread = cand && A.kd.m2 >= thr;
+    if (cand && !reread) {
+      const int j0 = A.kd.t1 * kVecs * kThreads + threadIdx.x;
+#pragma unroll
+      for (int k = 0; k < kVecs * VW; ++k) {
+        const int32_t vi = static_cast<int32_t>(C.v0) + (j0 + (k / VW) * kThreads) * VW + k % VW;
+        if (A.kd.z[k] >= thr && vi != excl) push_key(S.KS, A.kd.z[k], vi);
+      }
+    }
+    const unsigned cm = __ballot_sync(0xffffffffu, reread);
     const int todo = __popc(cm) * ntrips;
     for (int r0 = 0; r0 < todo; r0 += 4 * 32) {
       typename E::Vec w[4];
@@ -522,7 +576,7 @@ __device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, 
 
 // Accumulates this thread's vectors of trip t, which lies wholly inside the
 // copied part of the chunk: no bounds checks (the common case).
-template <int DT, bool GREEDY, bool KT>
+template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ void consume_stage_whole(const unsigned char* base, int t, const Chunk& C,
                                                     float c, Acc<Elem<DT>::VW>& A) {
   using E = Elem<DT>;
@@ -538,14 +592,14 @@ __device__ __forceinline__ void consume_stage_whole(const unsigned char* base, i
     const Vec* src = reinterpret_cast<const Vec*>(base);
 #pragma unroll
     for (int k = 0; k < kVecs; ++k) put_vec<DT>(z + k * VW, src[k * kThreads + threadIdx.x]);
-    A.template add<GREEDY, false>(z, b, c);
+    A.template add<GREEDY, false, TOPF>(z, b, c, t);
   }
   if (C.rowd) {
     float z[N];
     const Vec* src = reinterpret_cast<const Vec*>(base + kTripBytes);
 #pragma unroll
     for (int k = 0; k < kVecs; ++k) put_vec<DT>(z + k * VW, src[k * kThreads + threadIdx.x]);
-    A.template add<GREEDY, true>(z, b, c);
+    A.template add<GREEDY, true, TOPF>(z, b, c, t);
   }
 }
 
@@ -558,7 +612,7 @@ __device__ __forceinline__ int whole_trips(const Chunk& C, int64_t covered) {
 // Accumulates this thread's vectors of trip t from the stage at `base`; a
 // vector past the last whole 16-byte unit of the chunk (`covered` = first
 // logit not copied) is gathered from global memory instead.
-template <int DT, bool GREEDY, bool KT>
+template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ void consume_stage(const unsigned char* base, int t, const Chunk& C,
                                               int64_t covered, float c, Acc<Elem<DT>::VW>& A) {
   using E = Elem<DT>;
@@ -582,7 +636,7 @@ __device__ __forceinline__ void consume_stage(const unsigned char* base, int t, 
       else if (j < C.nv) put_vec<DT>(z + k * VW, E::gather(C.rowt, e, C.v1));
       else put_none<DT>(z + k * VW);
     }
-    A.template add<GREEDY, false>(z, b, c);
+    A.template add<GREEDY, false, TOPF>(z, b, c, t);
   }
   if (C.rowd) {
     float z[N];
@@ -595,7 +649,7 @@ __device__ __forceinline__ void consume_stage(const unsigned char* base, int t, 
       else if (j < C.nv) put_vec<DT>(z + k * VW, E::gather(C.rowd, e, C.v1));
       else put_none<DT>(z + k * VW);
     }
-    A.template add<GREEDY, true>(z, b, c);
+    A.template add<GREEDY, true, TOPF>(z, b, c, t);
   }
 }
 
@@ -609,7 +663,7 @@ __device__ __forceinline__ int64_t covered_end(const Chunk& C) {
 // refills a stage after the CTA barrier that closes its consumption.  Returns
 // false (on every thread) if a wait gave up; the copies then in flight get a
 // bounded wait before returning.
-template <int DT, bool GREEDY, bool KT>
+template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* ring, int S,
                                                     const Chunk& C, float c, Acc<Elem<DT>::VW>& A) {
   const int ntr = ring_trips(C.nv);
@@ -627,8 +681,8 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
   for (int t = 0; t < ntr; ++t) {
     if (!mbar_wait_bounded(&R.full[s], ph)) ok = false;
     const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
-    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT>(base, t, C, c, A);
-    else consume_stage<DT, GREEDY, KT>(base, t, C, covered, c, A);
+    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A);
+    else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A);
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         int s2 = s;
@@ -661,6 +715,7 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
 template <int DT, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
   constexpr bool kT = MODE != kModePredict;
+  constexpr bool kTopF = MODE != kModeVerify;
   __shared__ EpiSmem S;
   pdl_launch_dependents();  // the decision kernel may be scheduled once every CTA has started
   const Chunk C = chunk_at<DT, MODE>(P, blockIdx.x);
@@ -673,13 +728,13 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const 
   if (VEC) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ RingBars R;
-    ok = greedy ? stream_chunk_staged<DT, true, kT>(R, ring, P.stages, C, c, A)
-                : stream_chunk_staged<DT, false, kT>(R, ring, P.stages, C, c, A);
+    ok = greedy ? stream_chunk_staged<DT, true, kT, kTopF>(R, ring, P.stages, C, c, A)
+                : stream_chunk_staged<DT, false, kT, kTopF>(R, ring, P.stages, C, c, A);
   } else if (greedy) {
-    stream_chunk<DT, false, true, kT>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
+    stream_chunk<DT, false, true, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
                                              P.iters, c, A);
   } else {
-    stream_chunk<DT, false, false, kT>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
+    stream_chunk<DT, false, false, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
                                               P.iters, c, A);
   }
   chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S);
@@ -730,7 +785,7 @@ __device__ __forceinline__ void ring_produce(const StatsParams& P, RingBars& R, 
 
 // Consumes the trips of one chunk; returns false if any of them was not waited
 // for successfully (its data are then garbage and the chunk is flagged).
-template <int DT, bool GREEDY, bool KT>
+template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* ring, int S, int& s,
                                              uint32_t& ph, const Chunk& C, float c,
                                              Acc<Elem<DT>::VW>& A) {
@@ -747,8 +802,8 @@ __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* r
       *abort = 1;
     }
     const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
-    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT>(base, t, C, c, A);
-    else consume_stage<DT, GREEDY, KT>(base, t, C, covered, c, A);
+    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A);
+    else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A);
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[s]);
     if (++s == S) {
@@ -762,6 +817,7 @@ __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* r
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const StatsParams P) {
   constexpr bool kT = MODE != kModePredict;
+  constexpr bool kTopF = MODE != kModeVerify;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ RingBars R;
   __shared__ EpiSmem S;
@@ -789,8 +845,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const Stats
     const float c = greedy ? 1.f : temp_scale(T);
     Acc<Elem<DT>::VW> A;
     A.init();
-    const bool ok = greedy ? ring_consume<DT, true, kT>(R, ring, P.stages, s, ph, C, c, A)
-                           : ring_consume<DT, false, kT>(R, ring, P.stages, s, ph, C, c, A);
+    const bool ok = greedy ? ring_consume<DT, true, kT, kTopF>(R, ring, P.stages, s, ph, C, c, A)
+                           : ring_consume<DT, false, kT, kTopF>(R, ring, P.stages, s, ph, C, c, A);
     chunk_finish<DT, true, MODE>(P, C, item, greedy, c, A, ok, S);
   }
 }
