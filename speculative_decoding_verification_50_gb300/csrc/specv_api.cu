@@ -144,7 +144,7 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
   const int vw = vec_width(dtype);
   const int64_t units = static_cast<int64_t>(B > 0 ? B : 0) * (K + 1);
   // Loop trips per kernel-A CTA: long chunks amortise the per-CTA reductions;
-  // halve them while the grid would be under about two waves (4 CTAs per SM).
+  // halve them while there would be fewer than four chunks per SM.
   // SPECV_ITERS (1..64) fixes the trip count, for tuning runs.
   static int env_iters = -2;
   if (env_iters == -2) {
@@ -152,7 +152,7 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
     env_iters = e ? atoi(e) : -1;
   }
   pl.iters = (env_iters >= 1 && env_iters <= 64) ? env_iters : 8;
-  const int64_t want = 8LL * sm_count();
+  const int64_t want = 4LL * sm_count();
   for (;;) {
     pl.chunk = static_cast<int64_t>(pl.iters) * kVecs * kThreads * vw;
     pl.nchunk = (static_cast<int64_t>(V) + pl.chunk - 1) / pl.chunk;
