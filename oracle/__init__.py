@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libspecv_oracle.so")
 
 BF16, FP32 = 0, 1
 ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK = 1, 2, 4, 8
+ROW_BAD_COUNT = 32  # a per-row draft count outside [0, Kmax]
 ROW_ERRORS = ROW_BAD_TOKEN | ROW_NONFINITE | ROW_BAD_TEMP
 
 _P = ctypes.c_void_p
@@ -59,7 +60,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     lib.specv_oracle_verify.restype = _I
     lib.specv_oracle_verify.argtypes = [_I, _I, _I, _I, _P, _L, _L, _P, _L, _L,
-                                        _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I]
+                                        _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I]
+    lib.specv_oracle_verify_ragged.restype = _I
+    lib.specv_oracle_verify_ragged.argtypes = [_I, _I, _I, _I, _P, _L, _P, _L, _P, _P, _P, _P,
+                                               _I, _P, _P, _P, _P, _P, _P, _P, _I]
     lib.specv_oracle_predict.restype = _I
     lib.specv_oracle_predict.argtypes = [_I, _I, _I, _I, _I, _P, _L, _L, _P, _P, _P,
                                          _P, _P, _I]
@@ -92,18 +96,22 @@ def _strides(a: np.ndarray):
 
 
 def verify(target, draft, tokens, temperature, uniforms, nthreads: int = 1,
-           lib=None) -> dict:
+           lib=None, no_draft: bool = False) -> dict:
     """Run the oracle's verification on B batch rows.
 
     target [B, >=K+1, V], draft [B, >=K, V] (fp32 or int16 bf16 bits, rows
     contiguous along V), tokens int32 [B, K], temperature fp32 [B], uniforms
     fp32 [B, K+1].  Returns accept_len, out_tokens, p (=p_i(x_i)),
     q (=q_i(x_i)), alpha (=sum_v min(p_i, q_i)), status, boundary.
+    no_draft: the draft distributions are one-hot at the sent tokens (the
+    draft tensor is then ignored; pass the target).
     """
     lib = lib or load()
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     B, K = tokens.shape
     V = target.shape[-1]
+    if no_draft:
+        draft = target
     assert target.strides[-1] == target.itemsize and draft.strides[-1] == draft.itemsize
     assert target.dtype == draft.dtype
     temperature = np.ascontiguousarray(temperature, dtype=np.float32)
@@ -121,12 +129,54 @@ def verify(target, draft, tokens, temperature, uniforms, nthreads: int = 1,
     dbs, drs = _strides(draft)
     rc = lib.specv_oracle_verify(
         B, K, V, _dtype_code(target), _ptr(target), tbs, trs, _ptr(draft), dbs,
-        drs, _ptr(tokens), _ptr(temperature), _ptr(uniforms),
+        drs, _ptr(tokens), _ptr(temperature), _ptr(uniforms), int(bool(no_draft)),
         _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["p"]),
         _ptr(out["q"]), _ptr(out["alpha"]), _ptr(out["status"]),
         _ptr(out["boundary"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle verify: bad sizes")
+    return out
+
+
+def verify_ragged(target, draft, cu, tokens, temperature, uniforms, Kmax: int,
+                  nthreads: int = 1, lib=None, no_draft: bool = False) -> dict:
+    """Verification with K_b = cu[b] - cu[b-1] drafts per row, packed rows.
+
+    target [cu[-1] + B, V] (K_b + 1 rows per batch row, in order), draft
+    [cu[-1], V] (ignored with no_draft), cu int32 [B] inclusive prefix sums,
+    tokens int32 [cu[-1]], temperature fp32 [B], uniforms fp32 [cu[-1] + B].
+    Returns accept_len [B], out_tokens [B, Kmax+1], p/q/alpha [cu[-1]],
+    status [B], boundary [B].
+    """
+    lib = lib or load()
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    B = cu.shape[0]
+    T = int(cu[-1]) if B else 0
+    target = np.ascontiguousarray(target)
+    draft = target if no_draft else np.ascontiguousarray(draft)
+    V = target.shape[-1]
+    assert target.dtype == draft.dtype
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    out = dict(
+        accept_len=np.zeros(B, np.int32),
+        out_tokens=np.zeros((B, Kmax + 1), np.int32),
+        p=np.zeros(max(T, 1), np.float64),
+        q=np.zeros(max(T, 1), np.float64),
+        alpha=np.zeros(max(T, 1), np.float64),
+        status=np.zeros(B, np.int32),
+        boundary=np.zeros(B, np.int32),
+    )
+    rc = lib.specv_oracle_verify_ragged(
+        B, Kmax, V, _dtype_code(target), _ptr(target), V, _ptr(draft), V, _ptr(cu),
+        _ptr(tokens), _ptr(temperature), _ptr(uniforms), int(bool(no_draft)),
+        _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["p"]), _ptr(out["q"]),
+        _ptr(out["alpha"]), _ptr(out["status"]), _ptr(out["boundary"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle verify_ragged: bad sizes")
+    for k in ("p", "q", "alpha"):
+        out[k] = out[k][:T]
     return out
 
 

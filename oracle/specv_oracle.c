@@ -121,7 +121,7 @@ static double log_prob(const void* base, int dtype, int64_t off, int v, double T
 static void verify_row(int K, int V, int dtype, const void* target,
                        int64_t t_off, int64_t t_rs, const void* draft,
                        int64_t d_off, int64_t d_rs, const int32_t* x, double T,
-                       const float* U, int32_t* n_out, int32_t* tok_out,
+                       const float* U, int no_draft, int32_t* n_out, int32_t* tok_out,
                        double* p_out, double* q_out, double* alpha_out,
                        int32_t* status_out, int32_t* boundary_out, double* pt,
                        double* qd, double* r) {
@@ -141,9 +141,17 @@ static void verify_row(int K, int V, int dtype, const void* target,
   for (int i = 0; i <= K; ++i)
     status |= row_distribution(target, dtype, t_off + (int64_t)i * t_rs, V, T,
                                pt + (int64_t)i * V, &amt[i], &mt[i], &lst[i]);
-  for (int i = 0; i < K; ++i)
+  for (int i = 0; i < K; ++i) {
+    if (no_draft) {
+      /* [DLN] Appendix, NO_DRAFT_PROBS: the draft probability of the sent
+       * token is taken as 1, i.e. q_i is one-hot at x_i. */
+      for (int v = 0; v < V; ++v) qd[(int64_t)i * V + v] = (v == x[i]) ? 1.0 : 0.0;
+      amd[i] = x[i];
+      continue;
+    }
     status |= row_distribution(draft, dtype, d_off + (int64_t)i * d_rs, V, T,
                                qd + (int64_t)i * V, &amd[i], &md[i], &lsd[i]);
+  }
   if (status) { *status_out = status; *boundary_out = 0; return; }
 
   /* Per-position p_i(x_i), q_i(x_i) and the overlap sum_v min(p_i, q_i)
@@ -166,12 +174,13 @@ static void verify_row(int K, int V, int dtype, const void* target,
       accept = (x[i] == amd[i]) && (x[i] == amt[i]);
     } else {
       int64_t to = t_off + (int64_t)i * t_rs, dof = d_off + (int64_t)i * d_rs;
-      double zdx = load_logit(draft, dtype, dof + x[i]);
+      double zdx = no_draft ? 0.0 : load_logit(draft, dtype, dof + x[i]);
       if (zdx == -INFINITY) {
         accept = 0; /* q_i(x_i) = 0: reject */
       } else {
-        double ratio = exp(log_prob(target, dtype, to, x[i], T, mt[i], lst[i]) -
-                           log_prob(draft, dtype, dof, x[i], T, md[i], lsd[i]));
+        /* log q_i(x_i) = 0 without draft probabilities (q one-hot at x_i) */
+        double lq = no_draft ? 0.0 : log_prob(draft, dtype, dof, x[i], T, md[i], lsd[i]);
+        double ratio = exp(log_prob(target, dtype, to, x[i], T, mt[i], lst[i]) - lq);
         accept = ratio >= (double)U[i];
         if (fabs((double)U[i] - ratio) < BOUNDARY_EPS) boundary = 1;
       }
@@ -229,7 +238,7 @@ static void verify_row(int K, int V, int dtype, const void* target,
 int specv_oracle_verify(int B, int K, int V, int dtype, const void* target,
                         int64_t t_bs, int64_t t_rs, const void* draft,
                         int64_t d_bs, int64_t d_rs, const int32_t* tokens,
-                        const float* temperature, const float* uniforms,
+                        const float* temperature, const float* uniforms, int no_draft,
                         int32_t* accept_len, int32_t* out_tokens, double* p_out,
                         double* q_out, double* alpha_out, int32_t* row_status,
                         int32_t* boundary, int nthreads) {
@@ -244,10 +253,58 @@ int specv_oracle_verify(int B, int K, int V, int dtype, const void* target,
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     verify_row(K, V, dtype, target, (int64_t)b * t_bs, t_rs, draft,
                (int64_t)b * d_bs, d_rs, tokens + (int64_t)b * K,
-               (double)temperature[b], uniforms + (int64_t)b * (K + 1),
+               (double)temperature[b], uniforms + (int64_t)b * (K + 1), no_draft,
                accept_len + b, out_tokens + (int64_t)b * (K + 1),
                p_out + (int64_t)b * K, q_out + (int64_t)b * K,
                alpha_out + (int64_t)b * K, row_status + b, boundary + b, pt, qd, r);
+    free(pt);
+    free(qd);
+    free(r);
+  }
+  (void)nthreads;
+  return 0;
+}
+
+/* Exported: verification with a per-row draft count ([DLN] Appendix,
+ * cu_num_draft_tokens).  Row b has K_b = cu[b] - cu[b-1] drafts (cu[-1] = 0),
+ * 0 <= K_b <= Kmax, packed along one axis:
+ *   draft row (b, i)  at draft [(cu[b-1] + i) * d_rs],      i < K_b
+ *   target row (b, i) at target[(cu[b-1] + b + i) * t_rs],  i <= K_b
+ *   tokens x_{b,i} at tokens[cu[b-1] + i]; uniforms at uniforms[cu[b-1] + b + i],
+ *   i <= K_b (the last drives the bonus).
+ * Outputs: accept_len[B], out_tokens[B*(Kmax+1)] (-1 padded), p_out/q_out/
+ * alpha_out[num_tokens] (packed like the tokens), row_status[B] (bit 32: K_b
+ * outside [0, Kmax]), boundary[B].  cu is a host array here. */
+int specv_oracle_verify_ragged(int B, int Kmax, int V, int dtype, const void* target,
+                               int64_t t_rs, const void* draft, int64_t d_rs,
+                               const int32_t* cu, const int32_t* tokens,
+                               const float* temperature, const float* uniforms, int no_draft,
+                               int32_t* accept_len, int32_t* out_tokens, double* p_out,
+                               double* q_out, double* alpha_out, int32_t* row_status,
+                               int32_t* boundary, int nthreads) {
+  if (B < 0 || Kmax < 0 || Kmax > 63 || V < 1) return 1;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int b = 0; b < B; ++b) {
+    const int64_t c0 = b == 0 ? 0 : cu[b - 1];
+    const int kb = (int)(cu[b] - c0);
+    int32_t* ot = out_tokens + (int64_t)b * (Kmax + 1);
+    for (int i = 0; i <= Kmax; ++i) ot[i] = -1;
+    if (kb < 0 || kb > Kmax) {
+      accept_len[b] = 0;
+      row_status[b] = 32;
+      boundary[b] = 0;
+      continue;
+    }
+    double* pt = (double*)malloc(sizeof(double) * (size_t)(kb + 1) * V);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)(kb > 0 ? kb : 1) * V);
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    verify_row(kb, V, dtype, target, (c0 + b) * t_rs, t_rs, draft, c0 * d_rs, d_rs,
+               tokens + c0, (double)temperature[b], uniforms + c0 + b, no_draft,
+               accept_len + b, ot, p_out + c0, q_out + c0, alpha_out + c0,
+               row_status + b, boundary + b, pt, qd, r);
     free(pt);
     free(qd);
     free(r);

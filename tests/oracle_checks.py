@@ -534,6 +534,111 @@ def check_predict_fanout(lib):
         assert np.all(part["keys"][:, k, fan[k]:] == -1)
 
 
+def check_no_draft_is_one_hot_draft(lib):
+    """[DLN] Appendix, NO_DRAFT_PROBS: the draft probability of the sent token
+    is 1, so verification without draft logits equals verification whose draft
+    rows are one-hot at the sent tokens (logit 0 there, -inf elsewhere) --
+    whose exact output law is pinned by the enumeration checks."""
+    rng = np.random.default_rng(31)
+    B, K, V = 24, 3, 9
+    zt = rng.normal(0, 1.5, (B, K + 1, V)).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    tok[::3] = np.argmax(zt[::3, :K], axis=-1)  # some drafts the target likes
+    temp = rng.choice([0.0, 0.7, 1.0], B).astype(np.float32)
+    U = rng.uniform(0, 1, (B, K + 1)).astype(np.float32)
+    onehot = np.full((B, K, V), -np.inf, np.float32)
+    for b in range(B):
+        for i in range(K):
+            onehot[b, i, tok[b, i]] = 0.0
+    a = oracle.verify(zt, None, tok, temp, U, lib=lib, no_draft=True)
+    b_ = oracle.verify(zt, onehot, tok, temp, U, lib=lib)
+    for k in ("accept_len", "out_tokens", "status"):
+        np.testing.assert_array_equal(a[k], b_[k])
+    np.testing.assert_allclose(a["p"], b_["p"], rtol=1e-12)
+    np.testing.assert_array_equal(a["q"], 1.0)
+    np.testing.assert_allclose(a["alpha"], a["p"], rtol=1e-12)  # sum min(p, one-hot) = p(x)
+
+
+def check_no_draft_exact_law(lib):
+    """Deterministic drafts ([DLN] Appendix, NO_DRAFT_PROBS: q one-hot at the
+    sent token), run without draft logits: the emitted token at position i+1,
+    given the first i accepted, has law exactly p_{i+1}, and the first i are
+    accepted with probability prod_j p_j(x_j)."""
+    rng = np.random.default_rng(33)
+    V, K = 5, 2
+    for _ in range(4):
+        P = rational_rows(rng, K + 1, V)
+        xs = rng.integers(0, V, K)
+        Q = [[Fr(1) if v == xs[i] else Fr(0) for v in range(V)] for i in range(K)]
+        leaves = enumerate_pieces(P, Q)
+        tokens = np.array([lf[1] for lf in leaves], np.int32)
+        uniforms = np.array([[float(u) for u in lf[2]] for lf in leaves], np.float32)
+        B = len(leaves)
+        zt = logits_for(P)
+        target = np.broadcast_to(zt[None], (B,) + zt.shape)
+        out = oracle.verify(target, None, tokens, np.ones(B, np.float32), uniforms,
+                            nthreads=0, lib=lib, no_draft=True)
+        assert out["status"].max() & oracle.ROW_ERRORS == 0
+        for i in range(K + 1):
+            mass = Fr(0)
+            law = [Fr(0)] * V
+            for (w, _, _), ni, tk in zip(leaves, out["accept_len"], out["out_tokens"]):
+                if ni >= i:
+                    mass += w
+                    law[tk[i]] += w
+            alpha = Fr(1)
+            for j in range(i):
+                alpha *= P[j][int(xs[j])]
+            assert mass == alpha, (i, float(mass), float(alpha))
+            assert [l / mass for l in law] == P[i], i
+
+
+def check_ragged_matches_rows(lib):
+    """Per-row draft counts ([DLN] Appendix, cu_num_draft_tokens): each packed
+    row verifies exactly as that row alone with K = K_b; a row with no drafts
+    draws its bonus from p_0 by the inverse CDF (numpy searchsorted); a count
+    outside [0, Kmax] flags the row."""
+    rng = np.random.default_rng(32)
+    B, Kmax, V = 10, 4, 11
+    kb = rng.integers(0, Kmax + 1, B)
+    kb[1] = 0
+    cu = np.cumsum(kb).astype(np.int32)
+    T_ = int(cu[-1])
+    zt = rng.normal(0, 1.5, (T_ + B, V)).astype(np.float32)
+    zd = (np.repeat(zt[:1], T_, 0) * 0 + rng.normal(0, 1.5, (T_, V))).astype(np.float32)
+    tok = rng.integers(0, V, T_).astype(np.int32)
+    temp = rng.choice([0.0, 0.8, 1.0], B).astype(np.float32)
+    U = rng.uniform(0, 1, T_ + B).astype(np.float32)
+    out = oracle.verify_ragged(zt, zd, cu, tok, temp, U, Kmax, lib=lib)
+    for b in range(B):
+        c0 = 0 if b == 0 else int(cu[b - 1])
+        k = int(kb[b])
+        rows_t = zt[c0 + b: c0 + b + k + 1][None]
+        ot = out["out_tokens"][b]
+        assert np.all(ot[k + 1:] == -1)
+        if k == 0:
+            p0 = oracle.row_probs(rows_t[0, 0], float(temp[b]), lib=lib)
+            t = int(np.argmax(p0)) if temp[b] == 0 else \
+                int(np.searchsorted(np.cumsum(p0), float(U[c0 + b]) * p0.sum(), side="right"))
+            assert out["accept_len"][b] == 0 and ot[0] == t, (b, ot, t)
+            continue
+        one = oracle.verify(rows_t, zd[c0:c0 + k][None], tok[c0:c0 + k][None], temp[b:b + 1],
+                            U[c0 + b: c0 + b + k + 1][None], lib=lib)
+        assert out["accept_len"][b] == one["accept_len"][0]
+        np.testing.assert_array_equal(ot[:k + 1], one["out_tokens"][0])
+        np.testing.assert_array_equal(out["p"][c0:c0 + k], one["p"][0])
+        assert out["status"][b] == one["status"][0]
+    bad = cu.copy()
+    bad[3] = bad[2] + Kmax + 1  # K_3 too large (later rows shift, still read in bounds
+    bad[4:] = np.maximum(bad[4:], bad[3])  # of the arrays below)
+    big_t = np.concatenate([zt, zt, zt])
+    big_d = np.concatenate([zd, zd, zd])
+    o2 = oracle.verify_ragged(big_t, big_d, bad, np.concatenate([tok, tok, tok]), temp,
+                              np.concatenate([U, U, U]), Kmax, lib=lib)
+    assert o2["status"][3] == oracle.ROW_BAD_COUNT and o2["accept_len"][3] == 0
+    assert np.all(o2["out_tokens"][3] == -1)
+
+
 ALL_CHECKS = {
     "softmax_library": check_softmax_library,
     "thm1_overlap": check_thm1_overlap,
@@ -554,4 +659,7 @@ ALL_CHECKS = {
     "fanout_optimal": check_fanout_optimal,
     "fanout_rounding": check_fanout_rounding,
     "predict_fanout": check_predict_fanout,
+    "no_draft_one_hot": check_no_draft_is_one_hot_draft,
+    "no_draft_exact_law": check_no_draft_exact_law,
+    "ragged_rows": check_ragged_matches_rows,
 }

@@ -82,6 +82,16 @@ MUTATIONS = {
         "const int Fk = fanout ? fanout[k] : F;",
         "const int Fk = F; (void)fanout;",
         ["predict_fanout"]),
+    # NO_DRAFT_PROBS with a uniform instead of a one-hot draft distribution
+    "no_draft_not_one_hot": (
+        "for (int v = 0; v < V; ++v) qd[(int64_t)i * V + v] = (v == x[i]) ? 1.0 : 0.0;",
+        "for (int v = 0; v < V; ++v) qd[(int64_t)i * V + v] = 1.0 / V;",
+        ["no_draft_one_hot", "no_draft_exact_law"]),
+    # ragged rows: target rows placed without the per-row bonus-row shift
+    "ragged_target_offset": (
+        "verify_row(kb, V, dtype, target, (c0 + b) * t_rs, t_rs, draft, c0 * d_rs, d_rs,",
+        "verify_row(kb, V, dtype, target, c0 * t_rs, t_rs, draft, c0 * d_rs, d_rs,",
+        ["ragged_rows"]),
     "hit_wrong_length": (
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
