@@ -65,6 +65,9 @@ typedef enum { SPECV_BF16 = 0, SPECV_FP32 = 1 } specv_dtype;
 #define SPECV_ROW_FALLBACK 8  /* informational: the bonus draw fell back
                                  (zero residual mass -> drawn from p_n; or
                                  rounding left no index -> last v with r>0) */
+#define SPECV_ROW_BAD_COUNT 32 /* per-row draft counts (cu_num_draft_tokens)
+                                 give this row a count outside [0, K] or rows
+                                 past num_draft_tokens; the row is read nowhere */
 #define SPECV_ROW_DEVICE_TIMEOUT 16 /* a bulk copy of this row's logits into
                                  shared memory did not complete within about
                                  a second of device time; the kernel gave up on
@@ -108,7 +111,31 @@ typedef struct {
   float* p_draft;                 /* OUT, optional (NULL) [B, K] */
   float* q_draft;                 /* OUT, optional (NULL) [B, K] */
   int32_t* row_status;            /* OUT, optional (NULL) [B] */
+  /* Per-row draft counts ("Speculative Decoding" dl-note, Appendix:
+   * cu_num_draft_tokens).  Optional DEVICE [B]: inclusive prefix sums of the
+   * draft counts K_b, 0 <= K_b <= K.  NULL: every row has K drafts in the
+   * strided layout above.  When given, rows are packed along one axis and the
+   * batch strides are ignored (c = cu[b-1], 0 for b = 0):
+   *   target row (b, i), i <= K_b:  target_logits + (c + b + i) * target_row_stride
+   *   draft row (b, i),  i <  K_b:  draft_logits + (c + i) * draft_row_stride
+   *   draft_tokens[c + i], p_draft[c + i], q_draft[c + i]   (i < K_b)
+   *   uniforms[c + b + i], i <= K_b (entry K_b drives the bonus);
+   * accept_len and out_tokens keep their [B] and [B, K+1] shapes.  A row whose
+   * counts fall outside [0, K] or past num_draft_tokens is flagged
+   * SPECV_ROW_BAD_COUNT and read nowhere (its p_draft/q_draft are not
+   * written).  Verification only (specv_verify, specv_verify_noalloc). */
+  const int32_t* cu_num_draft_tokens;
+  int32_t num_draft_tokens;       /* with cu: cu[B-1], the draft rows the packed
+                                     buffers hold (target rows: that + B) */
+  int32_t flags;                  /* SPECV_NO_DRAFT_PROBS or 0 */
 } specv_verify_args;
+
+/* flags: no draft distribution (dl-note Appendix, NO_DRAFT_PROBS: n-gram or
+ * suffix drafts).  draft_logits must be NULL; q_i is taken one-hot at x_i, so
+ * a draft is accepted iff p_i(x_i) >= uniforms[b, i] (greedy rows: iff x_i is
+ * the argmax of p_i), q_draft reports 1, and after a rejection at n the bonus
+ * is drawn from r = p_n with r(x_n) = 0.  Verification only. */
+#define SPECV_NO_DRAFT_PROBS 1
 
 /* Bytes of device workspace specv_verify needs for these sizes (0 if B=0). */
 size_t specv_verify_workspace_bytes(int32_t B, int32_t K, int32_t V,

@@ -23,7 +23,8 @@ LIB_PATH = os.path.join(BUILD_DIR, "libspecv_oracle.so")
 BF16, FP32 = 0, 1
 ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK = 1, 2, 4, 8
 ROW_BAD_COUNT = 32  # a per-row draft count outside [0, Kmax]
-ROW_ERRORS = ROW_BAD_TOKEN | ROW_NONFINITE | ROW_BAD_TEMP
+ROW_ERRORS = ROW_BAD_TOKEN | ROW_NONFINITE | ROW_BAD_TEMP | ROW_BAD_COUNT
+
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

@@ -25,6 +25,8 @@ LIB_PATH = os.path.join(_PKG, "libspecv.so")
 SPECV_OK, SPECV_ERR_INVALID_ARG, SPECV_ERR_UNSUPPORTED, SPECV_ERR_CUDA, SPECV_ERR_WORKSPACE = range(5)
 SPECV_BF16, SPECV_FP32 = 0, 1
 ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK, ROW_DEVICE_TIMEOUT = 1, 2, 4, 8, 16
+ROW_BAD_COUNT = 32
+SPECV_NO_DRAFT_PROBS = 1
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -37,7 +39,8 @@ class VerifyArgs(ctypes.Structure):
                 ("draft_logits", _P), ("draft_batch_stride", _I64), ("draft_row_stride", _I64),
                 ("draft_tokens", _P), ("temperature", _P), ("uniforms", _P),
                 ("accept_len", _P), ("out_tokens", _P), ("p_draft", _P), ("q_draft", _P),
-                ("row_status", _P)]
+                ("row_status", _P), ("cu_num_draft_tokens", _P), ("num_draft_tokens", _I32),
+                ("flags", _I32)]
 
 
 class SsdArgs(ctypes.Structure):
@@ -143,10 +146,11 @@ def _verify_args(target, draft, draft_tokens, temperature, uniforms, draft_rows,
     import torch
     B, K = draft_tokens.shape
     V = target.shape[-1]
-    assert target.dim() == 3 and draft.dim() == 3 and target.shape[0] == B and draft.shape[0] == B
-    assert target.shape[1] >= K + 1 and draft.shape[1] >= draft_rows and draft.shape[-1] == V
-    assert target.stride(-1) == 1 and draft.stride(-1) == 1
-    assert target.dtype == draft.dtype
+    assert target.dim() == 3 and target.shape[0] == B and target.shape[1] >= K + 1
+    assert target.stride(-1) == 1
+    if draft is not None:  # None: no draft probabilities (SPECV_NO_DRAFT_PROBS)
+        assert draft.dim() == 3 and draft.shape[0] == B and draft.shape[1] >= draft_rows
+        assert draft.shape[-1] == V and draft.stride(-1) == 1 and target.dtype == draft.dtype
     assert uniforms.shape == (B, K + 1) and temperature.shape == (B,)
     dev = target.device
     if accept_len is None:
@@ -161,10 +165,12 @@ def _verify_args(target, draft, draft_tokens, temperature, uniforms, draft_rows,
         row_status = torch.empty(B, dtype=torch.int32, device=dev)
     args = VerifyArgs(B, K, V, _dtype_code(target),
                       target.data_ptr(), target.stride(0), target.stride(1),
-                      draft.data_ptr(), draft.stride(0), draft.stride(1),
+                      None if draft is None else draft.data_ptr(),
+                      0 if draft is None else draft.stride(0), 0 if draft is None else draft.stride(1),
                       draft_tokens.data_ptr(), temperature.data_ptr(), uniforms.data_ptr(),
                       accept_len.data_ptr(), out_tokens.data_ptr(),
-                      p_draft.data_ptr(), q_draft.data_ptr(), row_status.data_ptr())
+                      p_draft.data_ptr(), q_draft.data_ptr(), row_status.data_ptr(),
+                      None, 0, SPECV_NO_DRAFT_PROBS if draft is None else 0)
     outs = dict(accept_len=accept_len, out_tokens=out_tokens, p_draft=p_draft,
                 q_draft=q_draft, row_status=row_status)
     return args, outs
@@ -176,9 +182,10 @@ def specv_verify(target, draft, draft_tokens, temperature, uniforms, *, accept_l
     """Verify B batch rows on the GPU (see include/specv.h, specv_verify).
 
     target [B, >=K+1, V], draft [B, >=K, V] (bf16 or fp32, CUDA, last dim
-    contiguous); draft_tokens int32 [B, K]; temperature fp32 [B]; uniforms
-    fp32 [B, K+1].  Outputs are allocated when not given.  Returns a dict
-    with accept_len, out_tokens, p_draft, q_draft, row_status.
+    contiguous) or None for drafts without probabilities (SPECV_NO_DRAFT_PROBS);
+    draft_tokens int32 [B, K]; temperature fp32 [B]; uniforms fp32 [B, K+1].
+    Outputs are allocated when not given.  Returns a dict with accept_len,
+    out_tokens, p_draft, q_draft, row_status.
     """
     import torch
     lib = load_library()
@@ -190,6 +197,52 @@ def specv_verify(target, draft, draft_tokens, temperature, uniforms, *, accept_l
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=target.device)
     _check(lib.specv_verify(ctypes.byref(args), _ptr(workspace), workspace.numel(), _stream(stream)))
     return outs
+
+
+def specv_verify_ragged(target, draft, cu_num_draft_tokens, draft_tokens, temperature, uniforms,
+                        K: int, *, num_draft_tokens: int | None = None, accept_len=None,
+                        out_tokens=None, p_draft=None, q_draft=None, row_status=None,
+                        workspace=None, stream=None) -> dict:
+    """Verification with a per-row draft count (see include/specv.h,
+    cu_num_draft_tokens): rows packed along one axis.
+
+    target [N + B, V] (K_b + 1 rows per batch row, in order), draft [N, V] or
+    None (no draft probabilities), cu_num_draft_tokens int32 [B] (inclusive
+    prefix sums, on the device), draft_tokens int32 [N], temperature fp32 [B],
+    uniforms fp32 [N + B]; K = the largest count allowed.  N defaults to
+    draft_tokens.numel().  Returns accept_len [B], out_tokens [B, K+1],
+    p_draft / q_draft [N], row_status [B].
+    """
+    import torch
+    lib = load_library()
+    B = cu_num_draft_tokens.shape[0]
+    N = draft_tokens.numel() if num_draft_tokens is None else int(num_draft_tokens)
+    V = target.shape[-1]
+    assert target.dim() == 2 and target.stride(-1) == 1 and target.shape[0] >= N + B
+    if draft is not None:
+        assert draft.dim() == 2 and draft.stride(-1) == 1 and draft.shape[0] >= N
+        assert draft.shape[-1] == V and draft.dtype == target.dtype
+    assert draft_tokens.numel() >= N and uniforms.numel() >= N + B and temperature.shape == (B,)
+    dev = target.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    accept_len = torch.empty(B, **i32) if accept_len is None else accept_len
+    out_tokens = torch.empty((B, K + 1), **i32) if out_tokens is None else out_tokens
+    p_draft = torch.zeros(max(N, 1), dtype=torch.float32, device=dev) if p_draft is None else p_draft
+    q_draft = torch.zeros(max(N, 1), dtype=torch.float32, device=dev) if q_draft is None else q_draft
+    row_status = torch.empty(B, **i32) if row_status is None else row_status
+    args = VerifyArgs(B, K, V, _dtype_code(target), target.data_ptr(), 0, target.stride(0),
+                      None if draft is None else draft.data_ptr(), 0,
+                      0 if draft is None else draft.stride(0),
+                      draft_tokens.data_ptr(), temperature.data_ptr(), uniforms.data_ptr(),
+                      accept_len.data_ptr(), out_tokens.data_ptr(), p_draft.data_ptr(),
+                      q_draft.data_ptr(), row_status.data_ptr(), cu_num_draft_tokens.data_ptr(),
+                      N, SPECV_NO_DRAFT_PROBS if draft is None else 0)
+    need = lib.specv_verify_workspace_bytes(B, K, V, args.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(lib.specv_verify(ctypes.byref(args), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dict(accept_len=accept_len, out_tokens=out_tokens, p_draft=p_draft, q_draft=q_draft,
+                row_status=row_status)
 
 
 def specv_verify_noalloc(target, draft, draft_tokens, temperature, uniforms, *, accept_len=None,

@@ -38,7 +38,7 @@ struct PosStats {  // one position's combined row statistics
 };
 
 struct Dec {  // a batch row's decision (the same in every CTA of its cluster)
-  int32_t n, status, mode, need_scan, token, owner, last_pos, pad;
+  int32_t n, status, mode, need_scan, token, owner, last_pos, xn;
   float mt, md, ist, isd;
   double tau, pre_mine;
   float px[kMaxK], qx[kMaxK];
@@ -68,6 +68,9 @@ struct DecideParams {
   int32_t fk[kMaxK + 1];  // keys kept at lookahead k (F when the fan-out is uniform)
   int32_t stages;    // ring stages of the staged residual pass (aligned rows); 0: none
   int32_t ring_off;  // byte offset of that ring in dynamic shared memory
+  const int32_t* cu; // per-row draft counts (inclusive prefix sums), or null
+  int32_t ntok;      // with cu: packed draft rows the buffers hold
+  int32_t no_draft;  // no draft logits: q_i is one-hot at x_i
 };
 
 // Combine the chunk records of one position over an aligned group of W lanes
@@ -178,14 +181,20 @@ __device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int3
   return L;
 }
 
-// r values of one vector from its target (and draft) logits: mode 0
-// max(p - q, 0), mode 1 p.  Both products rounded before the subtraction (no
-// contraction), so p(v) = q(v) gives r(v) = 0 exactly, as in the definition.
+// r values of one vector (logits e0 .. e0+VW-1) from its target (and draft)
+// logits: mode 0 max(p - q, 0); mode 1 p; mode 2 (no draft probabilities: q
+// one-hot at the rejected token xn) p with r(xn) = 0.  Both products rounded
+// before the subtraction (no contraction), so p(v) = q(v) gives r(v) = 0
+// exactly, as in the definition.
 template <int VW>
 __device__ __forceinline__ void residual_from(const float (&zt)[VW], const float (&zd)[VW], int mode,
                                               float mt, float md, float c, float ist, float isd,
-                                              float (&r)[VW]) {
-  if (mode == 0) {
+                                              int64_t e0, int xn, float (&r)[VW]) {
+  if (mode == 2) {
+#pragma unroll
+    for (int k = 0; k < VW; ++k)
+      r[k] = (e0 + k == xn) ? 0.f : __fmul_rn(ex2((zt[k] - mt) * c), ist);
+  } else if (mode == 0) {
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
       const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
@@ -202,14 +211,14 @@ __device__ __forceinline__ void residual_from(const float (&zt)[VW], const float
 template <int DT, bool VEC>
 __device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd, int64_t v0,
                                              int64_t v1, int j, int mode, float mt, float md,
-                                             float c, float ist, float isd,
+                                             float c, float ist, float isd, int xn,
                                              float (&r)[Elem<DT>::VW]) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   float zt[VW], zd[VW];
   E::unpack(load_vec<DT, VEC>(rowt, v0, v1, j), zt);
   if (mode == 0) E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), zd);
-  residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
+  residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, v0 + static_cast<int64_t>(j) * VW, xn, r);
 }
 
 // Staged residual pass (16-byte aligned rows): the slice C of target row n
@@ -233,7 +242,7 @@ __device__ __forceinline__ void ring_start(RingBars& R, unsigned char* ring, int
 template <int DT>
 __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, int S, const Chunk& C,
                                               int mode, float mt, float md, float c, float ist,
-                                              float isd, float* segs, int ntl) {
+                                              float isd, int xn, float* segs, int ntl) {
   using E = Elem<DT>;
   using Vec = typename E::Vec;
   constexpr int VW = E::VW;
@@ -256,7 +265,8 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
         float zt[VW], zd[VW], r[VW];
         E::unpack(reinterpret_cast<const Vec*>(base)[jl], zt);
         if (mode == 0) E::unpack(reinterpret_cast<const Vec*>(base + kTripBytes)[jl], zd);
-        residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
+        const int64_t e0 = C.v0 + static_cast<int64_t>((t * kVecs + k) * kThreads + threadIdx.x) * VW;
+        residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, e0, xn, r);
         sum[k] = 0.f;
 #pragma unroll
         for (int q = 0; q < VW; ++q) sum[k] += r[q];
@@ -277,7 +287,7 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
             E::unpack(E::gather(C.rowt, e, C.v1), zt);
             if (mode == 0) E::unpack(E::gather(C.rowd, e, C.v1), zd);
           }
-          residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, r);
+          residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, e, xn, r);
 #pragma unroll
           for (int q = 0; q < VW; ++q) sum[k] += r[q];
         }
@@ -345,44 +355,46 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   const bool greedy = T == 0.f;
   const bool temp_ok = T >= 0.f && T < pos_inf();
   const float c = greedy ? 1.f : temp_scale(T);
-  const int64_t u0 = static_cast<int64_t>(b) * (K + 1);
+  const int64_t u0 = static_cast<int64_t>(b) * (K + 1);  // records, outputs: [B, K+1]
+  const RowLayout L = row_layout(P.cu, P.ntok, b, K, P.t_bs, P.t_rs, P.d_bs, P.d_rs);
+  const int kb = L.kb < 0 ? 0 : L.kb;  // this row's drafts
+  const bool nd = P.no_draft != 0;
 
   // ---- every CTA combines the records and decides (identical results) -------
   // The last warp first fetches what the decision needs besides the records.
   if (warp == kWarps - 1) {
-    for (int i = lane; i < K; i += 32) {
-      const int x = P.tokens[static_cast<int64_t>(b) * K + i];
+    for (int i = lane; i < kb; i += 32) {
+      const int x = P.tokens[L.tok0 + i];
       float zt = 0.f, zd = 0.f;
       if (x >= 0 && x < P.V) {
-        zt = E::scalar(static_cast<const char*>(P.zt) +
-                           (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(i) * P.t_rs) * E::ES,
+        zt = E::scalar(static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(i) * P.t_rs) * E::ES,
                        x);
-        zd = E::scalar(static_cast<const char*>(P.zd) +
-                           (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(i) * P.d_rs) * E::ES,
-                       x);
+        if (!nd)
+          zd = E::scalar(static_cast<const char*>(P.zd) + (L.d_off + static_cast<int64_t>(i) * P.d_rs) * E::ES,
+                         x);
       }
       pre_x[i] = x;
       pre_zt[i] = zt;
       pre_zd[i] = zd;
-      pre_u[i] = P.unif[u0 + i];
+      pre_u[i] = P.unif[L.u_off + i];
     }
   }
   // Everything above reads only the call's inputs; the records below are
   // the row-statistics kernel's output, so wait for it to complete here.
   pdl_wait_primary();
   // Half a warp per position: positions 2w and 2w+1 on warp w, 16 per pass.
-  for (int i0 = 2 * warp; i0 <= K; i0 += 2 * kWarps) {
+  for (int i0 = 2 * warp; i0 <= kb; i0 += 2 * kWarps) {
     const int i = i0 + (lane >> 4);
-    const PosStats p = combine_position<16>(P.recs + (u0 + min(i, K)) * P.nchunk, P.nchunk, c, lane & 15);
-    if ((lane & 15) == 0 && i <= K) ps[i] = p;
+    const PosStats p = combine_position<16>(P.recs + (u0 + min(i, kb)) * P.nchunk, P.nchunk, c, lane & 15);
+    if ((lane & 15) == 0 && i <= kb) ps[i] = p;
   }
   __syncthreads();
   if (warp == 0) {
     int nf = 0;
-    if (lane <= K && temp_ok) {
+    if (lane <= kb && temp_ok) {
       const PosStats& q = ps[lane];
-      const bool d_full = lane < K;  // draft rows that are normalised
-      const bool d_any = (MODE != kModeVerify) || lane < K;
+      const bool d_full = lane < kb && !nd;  // draft rows that are normalised
+      const bool d_any = (MODE != kModeVerify) || d_full;
       if (greedy) {
         nf = (q.bad & 1) || q.it == INT_MAX || (d_full && q.id == INT_MAX);
       } else {
@@ -391,21 +403,27 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         else if (d_any) nf |= q.Sd != q.Sd;  // draft row K: NaN / +inf only
       }
     }
-    const bool acc_lane = lane < K;
+    const bool acc_lane = lane < kb;
     const int x = acc_lane ? pre_x[lane] : -1;
     int status = temp_ok ? 0 : kBadTemp;
+    if (L.kb < 0) status |= kBadCount;
     if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
-    if (__any_sync(0xffffffffu, lane <= K && (ps[lane].bad & 2))) status |= kTimeout;
+    if (__any_sync(0xffffffffu, lane <= kb && (ps[lane].bad & 2))) status |= kTimeout;
     if (__any_sync(0xffffffffu, acc_lane && (x < 0 || x >= P.V))) status |= kBadToken;
     const bool ok = !(status & kErrors);
     bool accept = false;
     float px = 0.f, qx = 0.f;
     if (acc_lane && ok) {
       const PosStats& q = ps[lane];
-      if (greedy) {
+      if (greedy) {  // one-hot p and q (q at x itself without draft logits)
         px = (x == q.it) ? 1.f : 0.f;
-        qx = (x == q.id) ? 1.f : 0.f;
-        accept = (x == q.it) && (x == q.id);
+        qx = (nd || x == q.id) ? 1.f : 0.f;
+        accept = (x == q.it) && (nd || x == q.id);
+      } else if (nd) {  // q_i(x_i) = 1: accept iff p_i(x_i) >= u
+        const float lt = __fmul_rn(pre_zt[lane] - q.Mt, c);
+        px = __fdiv_rn(ex2(lt), static_cast<float>(q.St));
+        qx = 1.f;
+        accept = px >= pre_u[lane];
       } else {
         const float ztx = pre_zt[lane];
         const float zdx = pre_zd[lane];
@@ -421,8 +439,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       }
     }
     const unsigned rej = __ballot_sync(0xffffffffu, acc_lane && !accept);
-    const int n = ok ? (rej ? __ffs(rej) - 1 : K) : 0;
-    if (lane < K) {
+    const int n = ok ? (rej ? __ffs(rej) - 1 : kb) : 0;
+    if (lane < kb) {
       dec.px[lane] = px;
       dec.qx[lane] = qx;
     }
@@ -430,7 +448,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       const PosStats& q = ps[n];
       dec.n = n;
       dec.status = status;
-      dec.mode = (n < K) ? 0 : 1;
+      dec.mode = (n < kb) ? (nd ? 2 : 0) : 1;
+      dec.xn = (n < kb) ? pre_x[n] : -1;
       dec.need_scan = ok && !greedy;
       dec.token = (ok && greedy) ? q.it : -1;
       dec.owner = -1;
@@ -453,10 +472,10 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   Chunk RC;
   RC.b = b;
   RC.i = n_dec;
-  RC.rowt = static_cast<const char*>(P.zt) +
-            (static_cast<int64_t>(b) * P.t_bs + static_cast<int64_t>(n_dec) * P.t_rs) * E::ES;
-  RC.rowd = static_cast<const char*>(P.zd) +
-            (static_cast<int64_t>(b) * P.d_bs + static_cast<int64_t>(n_dec < K ? n_dec : 0) * P.d_rs) * E::ES;
+  RC.rowt = static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(n_dec) * P.t_rs) * E::ES;
+  RC.rowd = (dec.mode == 0)  // draft row n, read only for the residual max(p - q, 0)
+                ? static_cast<const char*>(P.zd) + (L.d_off + static_cast<int64_t>(n_dec) * P.d_rs) * E::ES
+                : nullptr;
   RC.v0 = static_cast<int64_t>(rank) * P.L;
   RC.v1 = min(static_cast<int64_t>(P.V), RC.v0 + P.L);
   RC.nv = RC.v1 > RC.v0 ? static_cast<int>((RC.v1 - RC.v0 + VW - 1) / VW) : 0;
@@ -484,7 +503,8 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       if (staged && attempt == 0) {
         Chunk SC = RC;
         if (mode != 0) SC.rowd = nullptr;
-        copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd, segs, ntl);
+        copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd,
+                                      dec.xn, segs, ntl);
       } else
       for (int t0 = 0; t0 < ntl; t0 += kTileUnroll) {
         float s[kTileUnroll];
@@ -494,7 +514,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
           s[q] = 0.f;
           if (j < nv) {
             float r[VW];
-            residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, r);
+            residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, dec.xn, r);
 #pragma unroll
             for (int k = 0; k < VW; ++k) s[q] += r[k];
           }
@@ -523,7 +543,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
           if (lane >= o) incl += y;
         }
         const double R = __shfl_sync(0xffffffffu, incl, 31);
-        const double tau = static_cast<double>(P.unif[u0 + K]) * R;
+        const double tau = static_cast<double>(P.unif[L.u_off + kb]) * R;  // the bonus uniform
         const unsigned own = __ballot_sync(0xffffffffu, tr > 0.0 && incl > tau);
         const unsigned pos = __ballot_sync(0xffffffffu, tr > 0.0);
         const double pm = __shfl_sync(0xffffffffu, incl - tr, rank);
@@ -538,14 +558,14 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
               dec.last_pos = 1;
               dec.status |= kFallback;
             }
-          } else if (dec.mode == 0) {
+          } else if (dec.mode != 1) {
             dec.mode = 1;  // zero residual mass: draw from p_n instead
             dec.status |= kFallback;
           }
         }
       }
       __syncthreads();  // the decision on the owner, made by warp 0, seen by the CTA
-      if (dec.owner >= 0 || attempt == 1 || dec.mode == 0) break;
+      if (dec.owner >= 0 || attempt == 1 || dec.mode != 1) break;
     }
 
     // ---- owner CTA: locate the crossing segment, then scan it --------------
@@ -605,7 +625,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       for (int k = 0; k < VW; ++k) r[k] = 0.f;
       if (seg >= 0 && j < nv)
         residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, dec.mode, dec.mt, dec.md, c, dec.ist,
-                              dec.isd, r);
+                              dec.isd, dec.xn, r);
       const int32_t base = static_cast<int32_t>(v0) + j * VW;
       int found = -1;
       if (!lp) {
@@ -684,12 +704,12 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
     const int32_t token = tok_slot;
     if (t <= K) {
       int32_t v = -1;
-      if (ok) v = (t < n) ? P.tokens[static_cast<int64_t>(b) * K + t] : (t == n ? token : -1);
+      if (ok) v = (t < n) ? pre_x[t] : (t == n ? token : -1);
       P.out_tokens[u0 + t] = v;
     }
     if (t < K) {
-      if (P.p_draft) P.p_draft[static_cast<int64_t>(b) * K + t] = ok ? dec.px[t] : 0.f;
-      if (P.q_draft) P.q_draft[static_cast<int64_t>(b) * K + t] = ok ? dec.qx[t] : 0.f;
+      if (t < kb && P.p_draft) P.p_draft[L.tok0 + t] = ok ? dec.px[t] : 0.f;
+      if (t < kb && P.q_draft) P.q_draft[L.tok0 + t] = ok ? dec.qx[t] : 0.f;
     }
     if (kTopF && copy_fail)
       for (int e = t; e < (K + 1) * F; e += kThreads) {

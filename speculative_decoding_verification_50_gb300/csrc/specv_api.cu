@@ -273,20 +273,29 @@ specv_status check_verify_args(const specv_verify_args* a, int draft_rows) {
   if (V < 1) return fail(SPECV_ERR_INVALID_ARG, "V=%d < 1", V);
   if (a->dtype != SPECV_BF16 && a->dtype != SPECV_FP32)
     return fail(SPECV_ERR_INVALID_ARG, "dtype=%d is not SPECV_BF16 or SPECV_FP32", a->dtype);
+  if (a->flags & ~SPECV_NO_DRAFT_PROBS) return fail(SPECV_ERR_INVALID_ARG, "unknown flags 0x%x", a->flags);
+  const bool nd = (a->flags & SPECV_NO_DRAFT_PROBS) != 0;
+  if (a->cu_num_draft_tokens && a->num_draft_tokens < 0)
+    return fail(SPECV_ERR_INVALID_ARG, "num_draft_tokens=%d < 0", a->num_draft_tokens);
   if (B == 0) return SPECV_OK;
-  if (!a->target_logits || !a->draft_logits || !a->draft_tokens || !a->temperature ||
-      !a->uniforms || !a->accept_len || !a->out_tokens)
+  if (nd != (a->draft_logits == nullptr))
+    return fail(SPECV_ERR_INVALID_ARG, "draft_logits must be NULL exactly when SPECV_NO_DRAFT_PROBS is set");
+  if (!a->target_logits || !a->draft_tokens || !a->temperature || !a->uniforms ||
+      !a->accept_len || !a->out_tokens)
     return fail(SPECV_ERR_INVALID_ARG, "a required pointer is NULL");
   const int es = elem_bytes(a->dtype);
+  if (!aligned(a->cu_num_draft_tokens, 4))
+    return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
   if (!aligned(a->target_logits, es) || !aligned(a->draft_logits, es) ||
       !aligned(a->draft_tokens, 4) || !aligned(a->temperature, 4) || !aligned(a->uniforms, 4) ||
       !aligned(a->accept_len, 4) || !aligned(a->out_tokens, 4) || !aligned(a->p_draft, 4) ||
       !aligned(a->q_draft, 4) || !aligned(a->row_status, 4))
     return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
-  if (a->target_row_stride < V || a->draft_row_stride < V)
+  if (a->target_row_stride < V || (!nd && a->draft_row_stride < V))
     return fail(SPECV_ERR_INVALID_ARG, "row stride smaller than V");
+  if (a->cu_num_draft_tokens) return SPECV_OK;  // packed rows: no batch strides
   if (B > 1 && (a->target_batch_stride < K * a->target_row_stride + V ||
-                a->draft_batch_stride < (draft_rows - 1) * a->draft_row_stride + V))
+                (!nd && a->draft_batch_stride < (draft_rows - 1) * a->draft_row_stride + V)))
     return fail(SPECV_ERR_INVALID_ARG, "batch stride too small for K+1 target / %d draft rows",
                 draft_rows);
   return SPECV_OK;
@@ -334,8 +343,12 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   if (units * pl.nchunk > 0x7fffffffLL || static_cast<int64_t>(B) * pl.CB > 0x7fffffffLL)
     return fail(SPECV_ERR_UNSUPPORTED, "B*(K+1) too large");
   const int es = elem_bytes(a->dtype);
-  const bool vec = vec_ok(a->target_logits, a->target_batch_stride, a->target_row_stride, es) &&
-                   vec_ok(a->draft_logits, a->draft_batch_stride, a->draft_row_stride, es);
+  // Packed rows have no batch stride: row alignment follows from the row stride.
+  const bool packed = a->cu_num_draft_tokens != nullptr;
+  const bool nd = (a->flags & SPECV_NO_DRAFT_PROBS) != 0;
+  const bool vec =
+      vec_ok(a->target_logits, packed ? 0 : a->target_batch_stride, a->target_row_stride, es) &&
+      (nd || vec_ok(a->draft_logits, packed ? 0 : a->draft_batch_stride, a->draft_row_stride, es));
   char* ws = static_cast<char*>(workspace);
   ChunkRec* recs = reinterpret_cast<ChunkRec*>(ws);
   float* cand_v = pl.cand_bytes ? reinterpret_cast<float*>(ws + pl.recs_bytes) : nullptr;
@@ -361,6 +374,8 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.chunk = static_cast<int32_t>(pl.chunk);
   sp.iters = pl.iters;
   sp.stages = ring_stages();
+  sp.cu = a->cu_num_draft_tokens;
+  sp.ntok = a->num_draft_tokens;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = mode == kModeSsd ? launch_stats<kModeSsd>(a->dtype, vec, units * pl.nchunk, s, sp)
                                    : launch_stats<kModeVerify>(a->dtype, vec, units * pl.nchunk, s, sp);
@@ -400,6 +415,9 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   // Aligned rows stream the residual slice through a ring placed after the
   // segment sums in dynamic shared memory.
   // (Very long rows whose segment table leaves no room for it read directly.)
+  dp.cu = a->cu_num_draft_tokens;
+  dp.ntok = a->num_draft_tokens;
+  dp.no_draft = (a->flags & SPECV_NO_DRAFT_PROBS) ? 1 : 0;
   dp.ring_off = static_cast<int32_t>(round_up(pl.smemB, 128));
   dp.stages = ring_stages_b();
   size_t smemB = dp.ring_off + static_cast<size_t>(dp.stages) * 2 * kTripBytes;
@@ -439,6 +457,10 @@ specv_status specv_ssd_round(const specv_ssd_args* a, void* workspace, size_t wo
   specv_status st = check_verify_args(&a->verify, a->verify.K + 1);
   if (st != SPECV_OK) return st;
   if (a->F < 1 || a->F > 32) return fail(SPECV_ERR_INVALID_ARG, "F=%d outside [1, 32]", a->F);
+  if (a->verify.flags & SPECV_NO_DRAFT_PROBS)
+    return fail(SPECV_ERR_INVALID_ARG, "an SSD round ranks draft logits: SPECV_NO_DRAFT_PROBS does not apply");
+  if (a->verify.cu_num_draft_tokens)
+    return fail(SPECV_ERR_UNSUPPORTED, "per-row draft counts are supported by specv_verify only");
   if (a->verify.B == 0) return ok();
   if (!a->keys || !a->hit) return fail(SPECV_ERR_INVALID_ARG, "keys or hit is NULL");
   if (!aligned(a->keys, 4) || !aligned(a->key_logits, 4))

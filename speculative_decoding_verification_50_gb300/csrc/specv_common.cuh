@@ -19,7 +19,8 @@ enum : int32_t {
   kBadTemp = 4,
   kFallback = 8,
   kTimeout = 16,  // a staged bulk copy did not land within the wait bound
-  kErrors = kBadToken | kNonFinite | kBadTemp | kTimeout
+  kBadCount = 32, // per-row draft counts outside [0, K] or past the packed rows
+  kErrors = kBadToken | kNonFinite | kBadTemp | kTimeout | kBadCount
 };
 
 constexpr float kNegMax = -3.402823466e+38f;  // lowest finite float

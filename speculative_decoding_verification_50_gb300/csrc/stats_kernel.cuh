@@ -59,7 +59,46 @@ struct StatsParams {
   int32_t* cand_i;
   int32_t B, K, V, F, nchunk, chunk, iters;  // chunk = iters * kVecs * 256 * VW logits
   int32_t stages;     // ring stages of the staged paths, 2..kMaxStages
+  const int32_t* cu;  // per-row draft counts (inclusive prefix sums), or null
+  int32_t ntok;       // with cu: packed draft rows the buffers hold
 };
+
+// Where batch row b's logit rows, draft tokens and uniforms live: the strided
+// [B, K(+1), V] layout, or rows packed by per-row draft counts ("Speculative
+// Decoding" dl-note Appendix, cu_num_draft_tokens): K_b = cu[b] - cu[b-1]
+// drafts, target row i at (cu[b-1] + b + i), draft row i at cu[b-1] + i,
+// tokens at cu[b-1] + i, uniforms at cu[b-1] + b + i.  Counts outside
+// [0, K] or past the ntok packed rows give kb = -1: the row is read nowhere.
+struct RowLayout {
+  int kb;          // drafts of the row (K when strided), -1 if its counts are bad
+  int64_t t_off;   // element offset of its target row 0
+  int64_t d_off;   // element offset of its draft row 0
+  int64_t tok0;    // index of its first draft token (and of its p/q outputs)
+  int64_t u_off;   // index of its first uniform
+};
+
+__device__ __forceinline__ RowLayout row_layout(const int32_t* cu, int ntok, int b, int K,
+                                                int64_t t_bs, int64_t t_rs, int64_t d_bs,
+                                                int64_t d_rs) {
+  RowLayout L;
+  if (!cu) {
+    L.kb = K;
+    L.t_off = static_cast<int64_t>(b) * t_bs;
+    L.d_off = static_cast<int64_t>(b) * d_bs;
+    L.tok0 = static_cast<int64_t>(b) * K;
+    L.u_off = static_cast<int64_t>(b) * (K + 1);
+    return L;
+  }
+  const int64_t c0 = b > 0 ? cu[b - 1] : 0, c1 = cu[b];
+  const bool ok = c0 >= 0 && c1 >= c0 && c1 - c0 <= K && c1 <= ntok;
+  L.kb = ok ? static_cast<int>(c1 - c0) : -1;
+  const int64_t base = ok ? c0 : 0;
+  L.t_off = (base + b) * t_rs;
+  L.d_off = base * d_rs;
+  L.tok0 = base;
+  L.u_off = base + b;
+  return L;
+}
 
 // log2(e)/T for a valid temperature; greedy rows and bad temperatures use 1.
 __device__ __forceinline__ float temp_scale(float T) {
@@ -288,16 +327,18 @@ __device__ __forceinline__ Chunk chunk_at(const StatsParams& P, int64_t item) {
   const int ch = static_cast<int>(item % P.nchunk);
   C.b = static_cast<int>(u / (P.K + 1));
   C.i = static_cast<int>(u % (P.K + 1));
-  const bool has_d = (MODE == kModeVerify) ? (C.i < P.K) : true;
-  C.rowt = (MODE != kModePredict)
-               ? static_cast<const char*>(P.zt) +
-                     (static_cast<int64_t>(C.b) * P.t_bs + static_cast<int64_t>(C.i) * P.t_rs) * E::ES
+  const RowLayout L = row_layout(P.cu, P.ntok, C.b, P.K, P.t_bs, P.t_rs, P.d_bs, P.d_rs);
+  const bool live = C.i <= L.kb;  // positions past the row's drafts hold no rows
+  // Verification reads draft rows i < K_b (none without draft logits);
+  // prediction reads draft rows 0..K.
+  const bool has_d = live && ((MODE == kModeVerify) ? (C.i < L.kb && P.zd != nullptr) : true);
+  C.rowt = (MODE != kModePredict && live)
+               ? static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(C.i) * P.t_rs) * E::ES
                : nullptr;
-  C.rowd = has_d ? static_cast<const char*>(P.zd) +
-                       (static_cast<int64_t>(C.b) * P.d_bs + static_cast<int64_t>(C.i) * P.d_rs) * E::ES
+  C.rowd = has_d ? static_cast<const char*>(P.zd) + (L.d_off + static_cast<int64_t>(C.i) * P.d_rs) * E::ES
                  : nullptr;
   C.v0 = static_cast<int64_t>(ch) * P.chunk;
-  C.v1 = min(static_cast<int64_t>(P.V), C.v0 + P.chunk);
+  C.v1 = live ? min(static_cast<int64_t>(P.V), C.v0 + P.chunk) : C.v0;
   C.nv = static_cast<int>((C.v1 - C.v0 + E::VW - 1) / E::VW);
   return C;
 }
@@ -587,7 +628,7 @@ __device__ __forceinline__ void consume_stage_whole(const unsigned char* base, i
   int32_t b[kVecs];
 #pragma unroll
   for (int k = 0; k < kVecs; ++k) b[k] = static_cast<int32_t>(C.v0) + (j0 + k * kThreads) * VW;
-  if (KT) {
+  if (KT && C.rowt) {
     float z[N];
     const Vec* src = reinterpret_cast<const Vec*>(base);
 #pragma unroll

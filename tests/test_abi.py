@@ -220,3 +220,35 @@ def test_geometric_fanout_rejects_bad_arguments(lib):
         assert lib.specv_geometric_fanout(*args, ptr, None) == sv.SPECV_ERR_INVALID_ARG, args
     assert lib.specv_geometric_fanout(4, 0.5, 1.0, 10, 8, None, None) == sv.SPECV_ERR_INVALID_ARG
     assert lib.specv_geometric_fanout(4, 0.5, 1.0, 10, 8, ptr, None) == sv.SPECV_OK
+
+
+def test_verify_flags_and_packed_rows_are_checked(lib):
+    # unknown flag bits
+    assert lib.specv_verify(ctypes.byref(_args(flags=2)), ctypes.c_void_p(0x100000), 1 << 20,
+                            None) == sv.SPECV_ERR_INVALID_ARG
+    # SPECV_NO_DRAFT_PROBS needs draft_logits NULL, and NULL needs the flag
+    assert lib.specv_verify(ctypes.byref(_args(flags=sv.SPECV_NO_DRAFT_PROBS)),
+                            ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+    assert lib.specv_verify(ctypes.byref(_args(draft_logits=None)), ctypes.c_void_p(0x100000),
+                            1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+    # packed rows: a negative row count, a misaligned count array
+    assert lib.specv_verify(ctypes.byref(_args(cu_num_draft_tokens=0x10000, num_draft_tokens=-1)),
+                            ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+    assert lib.specv_verify(ctypes.byref(_args(cu_num_draft_tokens=0x10002, num_draft_tokens=4)),
+                            ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+    # packed rows ignore the batch strides (0 is fine); the workspace check comes next
+    a = _args(cu_num_draft_tokens=0x10000, num_draft_tokens=4, target_batch_stride=0,
+              draft_batch_stride=0)
+    assert lib.specv_verify(ctypes.byref(a), None, 0, None) == sv.SPECV_ERR_WORKSPACE
+
+
+def test_ssd_round_refuses_verification_only_modes(lib):
+    a = _args(draft_batch_stride=400)
+    s = sv.SsdArgs(a, 6, 0x10000, 0, 0x10000)
+    s.verify.flags = sv.SPECV_NO_DRAFT_PROBS
+    s.verify.draft_logits = None
+    assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+    s = sv.SsdArgs(a, 6, 0x10000, 0, 0x10000)
+    s.verify.cu_num_draft_tokens = 0x10000
+    s.verify.num_draft_tokens = 4
+    assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_UNSUPPORTED
