@@ -50,6 +50,11 @@ WORKLOADS = {
     "cfg5-ssd-geo": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd-geo", ssd=True, F=6),
                      "config 5 as a full SSD round with the Theorem 12 geometric fan-out "
                      "(a=0.5, r=1, 54 keys over the K+1 lookaheads) + hit check"),
+    "cfg5-ragged": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ragged"),
+                    "config 5 with per-row draft counts K_b in 0..8 (seeded), rows packed "
+                    "by cu_num_draft_tokens, verify only"),
+    "cfg5-nodraft": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-nodraft"),
+                     "config 5 without draft logits (SPECV_NO_DRAFT_PROBS), verify only"),
     "cfg5": (wl.SPECS["cfg5"], "config 5 (B=256, K=8, V=152064, fp32 Zipf-like logits), verify only"),
     "cfg4": (wl.SPECS["cfg4"], "config 4 (B=32, K=4, V=128256, bf16, F=6): verify + predict + hit"),
     "cfg3": (wl.SPECS["cfg3"], "config 3 (B=64, K=4, V=128256, bf16, T in {0,0.6,1}), verify only"),
@@ -57,6 +62,10 @@ WORKLOADS = {
     "cfg2b": (wl.SPECS["cfg2b"], "config 2b (B=1, K=5, V=128256, bf16, T=0.7), verify only"),
     "cfg1": (wl.SPECS["cfg1"], "config 1 (B=1, K=4, V=4096, fp32, T=1), verify only"),
 }
+
+# Workloads in another layout: rows packed by per-row draft counts, or
+# verification without draft logits.
+LAYOUT = {"cfg5-ragged": "ragged", "cfg5-nodraft": "nodraft"}
 
 # Workloads whose keys follow the geometric fan-out: (acceptance rate a,
 # power-law exponent r, key budget over the K+1 lookaheads).
@@ -212,31 +221,65 @@ def algorithmic_bytes(spec) -> dict:
     return dict(verify=verify, predict=predict, step_fused=fused)
 
 
-def time_oracle(data, spec, nthreads: int) -> float:
+def draft_counts(first_row: int, n: int, K: int) -> np.ndarray:
+    """Seeded per-row draft counts in 0..K; row b's count depends on b only."""
+    return np.array([np.random.default_rng((20261202, b)).integers(0, K + 1)
+                     for b in range(first_row, first_row + n)], np.int64)
+
+
+def lay_out(data, spec, mode, first_row: int = 0) -> dict:
+    """The call's inputs in the workload's layout, with its target rows (the
+    metric's rows) and its algorithmic bytes (every row it must normalise)."""
+    B, K, V, s = data["tokens"].shape[0], spec.K, spec.V, spec.elem_bytes
+    lay = dict(target=data["target"], draft=data["draft"], tokens=data["tokens"],
+               temperature=data["temperature"], uniforms=data["uniforms"], cu=None)
+    if mode == "ragged":
+        kb = draft_counts(first_row, B, K)
+        lay.update(
+            cu=np.cumsum(kb).astype(np.int32),
+            target=np.concatenate([data["target"][b, :kb[b] + 1] for b in range(B)]),
+            draft=np.concatenate([data["draft"][b, :kb[b]] for b in range(B)]),
+            tokens=np.concatenate([data["tokens"][b, :kb[b]] for b in range(B)]).astype(np.int32),
+            uniforms=np.concatenate([np.append(data["uniforms"][b, :kb[b]], data["uniforms"][b, -1])
+                                     for b in range(B)]).astype(np.float32))
+        lay.update(rows=int((kb + 1).sum()), bytes=int((2 * kb + 1).sum()) * V * s)
+    elif mode == "nodraft":
+        lay.update(draft=None, rows=B * (K + 1), bytes=B * (K + 1) * V * s)
+    else:
+        ab = algorithmic_bytes(dataclasses.replace(spec, B=B))
+        lay.update(rows=B * (K + 1), bytes=ab["step_fused"] if spec.F else ab["verify"])
+    return lay
+
+
+def time_oracle(lay, spec, nthreads: int, mode=None) -> float:
     import oracle
     t0 = time.perf_counter()
-    o = oracle.verify(data["target"], data["draft"], data["tokens"], data["temperature"],
-                      data["uniforms"], nthreads=nthreads)
+    if mode == "ragged":
+        oracle.verify_ragged(lay["target"], lay["draft"], lay["cu"], lay["tokens"],
+                             lay["temperature"], lay["uniforms"], spec.K, nthreads=nthreads)
+        return time.perf_counter() - t0
+    o = oracle.verify(lay["target"], lay["draft"], lay["tokens"], lay["temperature"],
+                      lay["uniforms"], nthreads=nthreads, no_draft=(mode == "nodraft"))
     if spec.F:
-        p = oracle.predict(data["draft"], data["tokens"], spec.F, nthreads=nthreads)
+        p = oracle.predict(lay["draft"], lay["tokens"], spec.F, nthreads=nthreads)
         oracle.check_hit(p["keys"], o["accept_len"], o["out_tokens"])
     return time.perf_counter() - t0
 
 
-def cpu_baseline(spec, budget_s: float = 12.0) -> dict:
+def cpu_baseline(spec, budget_s: float = 12.0, mode=None) -> dict:
     """The oracle on a bounded sample of the workload, on this host's cores."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
     rows = list(range(min(spec.B, max(1, cores))))
-    data = wl.generate(spec, rows=rows)
-    t = time_oracle(data, spec, cores)
+    lay = lay_out(wl.generate(spec, rows=rows), spec, mode)
+    t = time_oracle(lay, spec, cores, mode)
     per_row = t / len(rows)
     n = int(min(spec.B, max(len(rows), budget_s / max(per_row, 1e-6))))
     if n > len(rows):
-        data = wl.generate(spec, rows=list(range(n)))
-        t = time_oracle(data, spec, cores)
-    value = n * (spec.K + 1) / t
+        lay = lay_out(wl.generate(spec, rows=list(range(n))), spec, mode)
+        t = time_oracle(lay, spec, cores, mode)
+    value = lay["rows"] / t
     return {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {spec.B} batch rows of {spec.name} "
                       f"({'verify+predict+hit' if spec.F else 'verify'}), fp64 C, OpenMP over rows, "
@@ -270,7 +313,9 @@ def run_ours(args) -> None:
         fanout, _ = sv.specv_geometric_fanout(spec.K, *GEOMETRIC[args.workload], max_f=32)
         spec = dataclasses.replace(spec, F=max(1, max(fanout)))
         desc += f" [F_k = {fanout}]"
+    mode = LAYOUT.get(args.workload)
     data = wl.generate(spec, rows=shard_rows(rank, world, spec.B))
+    lay = lay_out(data, spec, mode, first_row=rank * spec.B)
     B, K, V, F = spec.B, spec.K, spec.V, spec.F
     is_bf16 = spec.dtype == wl.BF16
 
@@ -278,19 +323,22 @@ def run_ours(args) -> None:
         t = torch.from_numpy(a)
         return t.view(torch.bfloat16) if is_bf16 else t
 
-    h_target = host_logits(data["target"]).pin_memory()
-    h_draft = host_logits(data["draft"]).pin_memory()
-    h_tok = torch.from_numpy(data["tokens"]).pin_memory()
-    h_temp = torch.from_numpy(data["temperature"]).pin_memory()
-    h_unif = torch.from_numpy(data["uniforms"]).pin_memory()
+    h_target = host_logits(lay["target"]).pin_memory()
+    h_draft = host_logits(lay["draft"]).pin_memory() if lay["draft"] is not None else None
+    h_tok = torch.from_numpy(lay["tokens"]).pin_memory()
+    h_temp = torch.from_numpy(lay["temperature"]).pin_memory()
+    h_unif = torch.from_numpy(lay["uniforms"]).pin_memory()
+    h_cu = torch.from_numpy(lay["cu"]).pin_memory() if lay["cu"] is not None else None
     d_target = h_target.to(dev)
-    d_draft = h_draft.to(dev)
+    d_draft = h_draft.to(dev) if h_draft is not None else None
     d_tok, d_temp, d_unif = h_tok.to(dev), h_temp.to(dev), h_unif.to(dev)
+    d_cu = h_cu.to(dev) if h_cu is not None else None
+    pq_shape = (max(1, h_tok.numel()),) if mode == "ragged" else (B, K)
 
     i32 = dict(dtype=torch.int32, device=dev)
     outs = dict(accept_len=torch.empty(B, **i32), out_tokens=torch.empty((B, K + 1), **i32),
-                p_draft=torch.empty((B, K), dtype=torch.float32, device=dev),
-                q_draft=torch.empty((B, K), dtype=torch.float32, device=dev),
+                p_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
+                q_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
                 row_status=torch.empty(B, **i32))
     lib = sv.load_library()
     code = sv.SPECV_BF16 if is_bf16 else sv.SPECV_FP32
@@ -311,6 +359,9 @@ def run_ours(args) -> None:
             sv.specv_ssd_round(d_target, d_draft, d_tok, d_temp, d_unif, F, keys=keys,
                                key_logits=key_logits, hit=hit, workspace=ws_v, fanout=fanout,
                                **outs)
+        elif mode == "ragged":
+            sv.specv_verify_ragged(d_target, d_draft, d_cu, d_tok, d_temp, d_unif, K,
+                                   workspace=ws_v, **outs)
         else:
             sv.specv_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
         launches[0] += sv.last_launch_count()
@@ -350,7 +401,7 @@ def run_ours(args) -> None:
     stats_ms = [e[0].elapsed_time(e[1]) for e in evs]
     decide_ms = [e[1].elapsed_time(e[2]) for e in evs]
     ms_step = reduce_max(total_ms, world, dev) / args.steps
-    rows_total = reduce_sum(float(B * (K + 1)), world, dev)
+    rows_total = reduce_sum(float(lay["rows"]), world, dev)
     value = rows_total / (ms_step / 1e3)
 
     # end to end: host inputs in pinned memory, copies inside the timed region
@@ -362,7 +413,10 @@ def run_ours(args) -> None:
 
     def e2e_step():
         d_target.copy_(h_target, non_blocking=True)
-        d_draft.copy_(h_draft, non_blocking=True)
+        if d_draft is not None:
+            d_draft.copy_(h_draft, non_blocking=True)
+        if d_cu is not None:
+            d_cu.copy_(h_cu, non_blocking=True)
         d_tok.copy_(h_tok, non_blocking=True)
         d_temp.copy_(h_temp, non_blocking=True)
         d_unif.copy_(h_unif, non_blocking=True)
@@ -383,7 +437,8 @@ def run_ours(args) -> None:
     e1.record(stream)
     barrier()
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in (h_target, h_draft, h_tok, h_temp, h_unif))
+    h2d = sum(t.numel() * t.element_size()
+              for t in (h_target, h_draft, h_tok, h_temp, h_unif, h_cu) if t is not None)
     d2h = h_n.numel() * 4 + h_ot.numel() * 4 + ((h_keys.numel() * 4 + h_hit.numel()) if F else 0)
 
     if rank != 0:
@@ -393,14 +448,14 @@ def run_ours(args) -> None:
         return
 
     peak, peak_kind = measured_peak()
-    ab = algorithmic_bytes(spec)
     v_ms = statistics.mean(call_ms)
     a_ms = statistics.mean(stats_ms)
-    kernel_bytes = ab["step_fused"] if F else ab["verify"]
+    kernel_bytes = lay["bytes"]
     achieved = kernel_bytes / (a_ms / 1e3) / 1e9
     call_gbs = kernel_bytes / (v_ms / 1e3) / 1e9
     traffic = recorded_traffic(args.workload)
-    in_bytes = d_target.numel() * d_target.element_size() + d_draft.numel() * d_draft.element_size()
+    in_bytes = d_target.numel() * d_target.element_size() + \
+        (d_draft.numel() * d_draft.element_size() if d_draft is not None else 0)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -418,7 +473,7 @@ def run_ours(args) -> None:
             "workload": f"{args.workload}: {desc}",
             "B_per_gpu": B, "K": K, "V": V, "logits": spec.dtype, "F": F,
             **({"fanout": fanout} if fanout else {}),
-            "rows_per_step_per_gpu": B * (K + 1),
+            "rows_per_step_per_gpu": lay["rows"],
             "l2": (f"inputs {in_bytes / 1e9:.2f} GB > {L2_BYTES / 2**20:.0f} MiB L2, no flush"
                    if in_bytes > L2_BYTES else "inputs fit in L2: numbers are L2-hot"),
         },
@@ -447,7 +502,7 @@ def run_ours(args) -> None:
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec)
+        line["cpu_baseline"] = cpu_baseline(spec, mode=mode)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -462,20 +517,23 @@ def run_reference(args) -> None:
     import oracle
     oracle.build()
     spec, desc = WORKLOADS[args.workload]
+    mode = LAYOUT.get(args.workload)
+    if args.workload in GEOMETRIC:  # the oracle's cost does not depend on the split of F
+        spec = dataclasses.replace(spec, F=16)
     cores = os.cpu_count() or 1
-    probe = wl.generate(spec, rows=[0])
-    t_row = time_oracle(probe, spec, 1)
+    probe = lay_out(wl.generate(spec, rows=[0]), spec, mode)
+    t_row = time_oracle(probe, spec, 1, mode)
     # whole run (warm-up + timed) within about a minute
     per_step = 60.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(spec.B, per_step / max(t_row, 1e-6) * min(cores, 8))))
-    data = wl.generate(spec, rows=list(range(n)))
+    lay = lay_out(wl.generate(spec, rows=list(range(n))), spec, mode)
     for _ in range(args.warmup):
-        time_oracle(data, spec, cores)
+        time_oracle(lay, spec, cores, mode)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        time_oracle(data, spec, cores)
+        time_oracle(lay, spec, cores, mode)
     dt = (time.perf_counter() - t0) / args.steps
-    value = n * (spec.K + 1) / dt
+    value = lay["rows"] / dt
     line = {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": world,
