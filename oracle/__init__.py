@@ -61,7 +61,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     lib.specv_oracle_verify.restype = _I
     lib.specv_oracle_verify.argtypes = [_I, _I, _I, _I, _P, _L, _L, _P, _L, _L,
-                                        _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I]
+                                        _P, _P, _P, _I, _I, ctypes.c_double,
+                                        _P, _P, _P, _P, _P, _P, _P, _I]
+    lib.specv_oracle_saguaro_probs.restype = _I
+    lib.specv_oracle_saguaro_probs.argtypes = [_I, _I, _P, ctypes.c_double, _I, ctypes.c_double, _P]
+    lib.specv_oracle_saguaro_sample.restype = _I
+    lib.specv_oracle_saguaro_sample.argtypes = [_I, _I, _I, _P, _L, _P, _I, ctypes.c_double, _P,
+                                                _P, _P, _P]
     lib.specv_oracle_verify_ragged.restype = _I
     lib.specv_oracle_verify_ragged.argtypes = [_I, _I, _I, _I, _P, _L, _P, _L, _P, _P, _P, _P,
                                                _I, _P, _P, _P, _P, _P, _P, _P, _I]
@@ -97,7 +103,7 @@ def _strides(a: np.ndarray):
 
 
 def verify(target, draft, tokens, temperature, uniforms, nthreads: int = 1,
-           lib=None, no_draft: bool = False) -> dict:
+           lib=None, no_draft: bool = False, saguaro=None) -> dict:
     """Run the oracle's verification on B batch rows.
 
     target [B, >=K+1, V], draft [B, >=K, V] (fp32 or int16 bf16 bits, rows
@@ -106,6 +112,7 @@ def verify(target, draft, tokens, temperature, uniforms, nthreads: int = 1,
     q (=q_i(x_i)), alpha (=sum_v min(p_i, q_i)), status, boundary.
     no_draft: the draft distributions are one-hot at the sent tokens (the
     draft tensor is then ignored; pass the target).
+    saguaro=(F, C): the drafts were sampled from sigma_{F,C}(z/T), so that is q.
     """
     lib = lib or load()
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
@@ -131,11 +138,42 @@ def verify(target, draft, tokens, temperature, uniforms, nthreads: int = 1,
     rc = lib.specv_oracle_verify(
         B, K, V, _dtype_code(target), _ptr(target), tbs, trs, _ptr(draft), dbs,
         drs, _ptr(tokens), _ptr(temperature), _ptr(uniforms), int(bool(no_draft)),
+        int(saguaro[0]) if saguaro else 0, float(saguaro[1]) if saguaro else 1.0,
         _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["p"]),
         _ptr(out["q"]), _ptr(out["alpha"]), _ptr(out["status"]),
         _ptr(out["boundary"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle verify: bad sizes")
+    return out
+
+
+def saguaro_probs(z, T: float, F: int, C: float, lib=None) -> np.ndarray:
+    """The oracle's sigma_{F,C}(z/T) of one logit row."""
+    lib = lib or load()
+    z = np.ascontiguousarray(z)
+    p = np.zeros(z.shape[-1], np.float64)
+    rc = lib.specv_oracle_saguaro_probs(z.shape[-1], _dtype_code(z), _ptr(z), float(T), int(F),
+                                        float(C), _ptr(p))
+    if rc & ROW_ERRORS:
+        raise ValueError(f"row status {rc}")
+    return p
+
+
+def saguaro_sample(z, temperature, F: int, C: float, uniforms, lib=None) -> dict:
+    """[SSD] §4.2.1 draft-side sampling: tokens [B] drawn from sigma_{F,C}(z/T)
+    by inverse CDF of uniforms [B], with q = sigma(token) and row status."""
+    lib = lib or load()
+    z = np.ascontiguousarray(z)
+    B, V = z.shape
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    out = dict(tokens=np.zeros(B, np.int32), q=np.zeros(B, np.float64),
+               status=np.zeros(B, np.int32))
+    rc = lib.specv_oracle_saguaro_sample(B, V, _dtype_code(z), _ptr(z), V, _ptr(temperature),
+                                         int(F), float(C), _ptr(uniforms), _ptr(out["tokens"]),
+                                         _ptr(out["q"]), _ptr(out["status"]))
+    if rc != 0:
+        raise ValueError("oracle saguaro_sample: bad arguments")
     return out
 
 

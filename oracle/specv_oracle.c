@@ -105,6 +105,41 @@ static int row_distribution(const void* base, int dtype, int64_t off, int V,
   return 0;
 }
 
+/* Candidates of a row, ordered by (logit descending, index ascending). */
+typedef struct { double z; int v; } cand_t;
+
+static int cand_cmp(const void* a, const void* b) {
+  const cand_t* x = (const cand_t*)a;
+  const cand_t* y = (const cand_t*)b;
+  if (x->z > y->z) return -1;
+  if (x->z < y->z) return 1;
+  return (x->v < y->v) ? -1 : (x->v > y->v);
+}
+
+/* ---------------------------------------------------------------------------
+ * f2  Saguaro sampling scheme: [SSD] §4.2.1.  sigma_{F,C}(z) is proportional
+ *     to C * exp(z_t) for the F tokens with the largest logits (top_F(z), in
+ *     the key order above) and to exp(z_t) for every other token.  With a
+ *     temperature the scheme applies to z / T (top_F is the same); greedy rows
+ *     (T = 0) are left one-hot.  In: p[] = softmax(z/T) of the row (from
+ *     row_distribution).  Out: p[] = sigma_{F,C}(z/T).  Returns 0, or
+ *     ROW_NONFINITE when no mass is left (C = 0 and nothing outside top_F).
+ */
+static int saguaro_reweight(const void* base, int dtype, int64_t off, int V, int F, double C,
+                            double* p, cand_t* c) {
+  for (int v = 0; v < V; ++v) {
+    c[v].z = load_logit(base, dtype, off + v);
+    c[v].v = v;
+  }
+  qsort(c, (size_t)V, sizeof(cand_t), cand_cmp);
+  for (int f = 0; f < F && f < V; ++f) p[c[f].v] *= C;
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) S += p[v];
+  if (!(S > 0.0)) return ROW_NONFINITE;
+  for (int v = 0; v < V; ++v) p[v] /= S;
+  return 0;
+}
+
 /* log p(v) for a temperature row, from the row's max and log-normaliser. */
 static double log_prob(const void* base, int dtype, int64_t off, int v, double T,
                        double m, double logS) {
@@ -121,7 +156,8 @@ static double log_prob(const void* base, int dtype, int64_t off, int v, double T
 static void verify_row(int K, int V, int dtype, const void* target,
                        int64_t t_off, int64_t t_rs, const void* draft,
                        int64_t d_off, int64_t d_rs, const int32_t* x, double T,
-                       const float* U, int no_draft, int32_t* n_out, int32_t* tok_out,
+                       const float* U, int no_draft, int sg_F, double sg_C,
+                       int32_t* n_out, int32_t* tok_out,
                        double* p_out, double* q_out, double* alpha_out,
                        int32_t* status_out, int32_t* boundary_out, double* pt,
                        double* qd, double* r) {
@@ -151,6 +187,13 @@ static void verify_row(int K, int V, int dtype, const void* target,
     }
     status |= row_distribution(draft, dtype, d_off + (int64_t)i * d_rs, V, T,
                                qd + (int64_t)i * V, &amd[i], &md[i], &lsd[i]);
+    /* Saguaro drafts were sampled from sigma_{F,C}: that is q ([SSD] §4.2.1) */
+    if (sg_F > 0 && T > 0.0 && !status) {
+      cand_t* cs = (cand_t*)malloc(sizeof(cand_t) * (size_t)V);
+      status |= saguaro_reweight(draft, dtype, d_off + (int64_t)i * d_rs, V, sg_F, sg_C,
+                                 qd + (int64_t)i * V, cs);
+      free(cs);
+    }
   }
   if (status) { *status_out = status; *boundary_out = 0; return; }
 
@@ -179,7 +222,9 @@ static void verify_row(int K, int V, int dtype, const void* target,
         accept = 0; /* q_i(x_i) = 0: reject */
       } else {
         /* log q_i(x_i) = 0 without draft probabilities (q one-hot at x_i) */
-        double lq = no_draft ? 0.0 : log_prob(draft, dtype, dof, x[i], T, md[i], lsd[i]);
+        double lq = no_draft ? 0.0
+                    : sg_F > 0 ? log(qd[(int64_t)i * V + x[i]])
+                               : log_prob(draft, dtype, dof, x[i], T, md[i], lsd[i]);
         double ratio = exp(log_prob(target, dtype, to, x[i], T, mt[i], lst[i]) - lq);
         accept = ratio >= (double)U[i];
         if (fabs((double)U[i] - ratio) < BOUNDARY_EPS) boundary = 1;
@@ -239,10 +284,11 @@ int specv_oracle_verify(int B, int K, int V, int dtype, const void* target,
                         int64_t t_bs, int64_t t_rs, const void* draft,
                         int64_t d_bs, int64_t d_rs, const int32_t* tokens,
                         const float* temperature, const float* uniforms, int no_draft,
+                        int sg_F, double sg_C,
                         int32_t* accept_len, int32_t* out_tokens, double* p_out,
                         double* q_out, double* alpha_out, int32_t* row_status,
                         int32_t* boundary, int nthreads) {
-  if (B < 0 || K < 1 || K > 63 || V < 1) return 1;
+  if (B < 0 || K < 1 || K > 63 || V < 1 || sg_F < 0 || !(sg_C >= 0.0 && sg_C <= 1.0)) return 1;
 #ifdef _OPENMP
   if (nthreads <= 0) nthreads = omp_get_max_threads();
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
@@ -253,7 +299,7 @@ int specv_oracle_verify(int B, int K, int V, int dtype, const void* target,
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     verify_row(K, V, dtype, target, (int64_t)b * t_bs, t_rs, draft,
                (int64_t)b * d_bs, d_rs, tokens + (int64_t)b * K,
-               (double)temperature[b], uniforms + (int64_t)b * (K + 1), no_draft,
+               (double)temperature[b], uniforms + (int64_t)b * (K + 1), no_draft, sg_F, sg_C,
                accept_len + b, out_tokens + (int64_t)b * (K + 1),
                p_out + (int64_t)b * K, q_out + (int64_t)b * K,
                alpha_out + (int64_t)b * K, row_status + b, boundary + b, pt, qd, r);
@@ -302,7 +348,7 @@ int specv_oracle_verify_ragged(int B, int Kmax, int V, int dtype, const void* ta
     double* qd = (double*)malloc(sizeof(double) * (size_t)(kb > 0 ? kb : 1) * V);
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
     verify_row(kb, V, dtype, target, (c0 + b) * t_rs, t_rs, draft, c0 * d_rs, d_rs,
-               tokens + c0, (double)temperature[b], uniforms + c0 + b, no_draft,
+               tokens + c0, (double)temperature[b], uniforms + c0 + b, no_draft, 0, 1.0,
                accept_len + b, ot, p_out + c0, q_out + c0, alpha_out + c0,
                row_status + b, boundary + b, pt, qd, r);
     free(pt);
@@ -311,6 +357,61 @@ int specv_oracle_verify_ragged(int B, int Kmax, int V, int dtype, const void* ta
   }
   (void)nthreads;
   return 0;
+}
+
+/* Exported: draft-side Saguaro sampling ([SSD] §4.2.1): for each of B rows
+ * (z[b*z_bs + v]), the token t = the smallest v whose running sum of
+ * sigma_{F,C}(z/T) exceeds U[b] (T = 0: the first argmax), and q_out[b] =
+ * sigma(t).  F = 0 samples softmax(z/T) itself. */
+int specv_oracle_saguaro_sample(int B, int V, int dtype, const void* z, int64_t z_bs,
+                                const float* temperature, int F, double C, const float* U,
+                                int32_t* tokens, double* q_out, int32_t* row_status) {
+  if (B < 0 || V < 1 || F < 0 || !(C >= 0.0 && C <= 1.0)) return 1;
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  cand_t* cs = (cand_t*)malloc(sizeof(cand_t) * (size_t)V);
+  for (int b = 0; b < B; ++b) {
+    const double T = (double)temperature[b];
+    int am;
+    double m, ls;
+    int st = (!(T >= 0.0) || isinf(T)) ? ROW_BAD_TEMP : 0;
+    if (!st) st = row_distribution(z, dtype, (int64_t)b * z_bs, V, T, p, &am, &m, &ls);
+    if (!st && F > 0 && T > 0.0) st = saguaro_reweight(z, dtype, (int64_t)b * z_bs, V, F, C, p, cs);
+    tokens[b] = -1;
+    q_out[b] = 0.0;
+    row_status[b] = st;
+    if (st) continue;
+    if (T == 0.0) {
+      tokens[b] = am;
+      q_out[b] = 1.0;
+      continue;
+    }
+    double cum = 0.0;
+    for (int v = 0; v < V; ++v) {
+      cum += p[v];
+      if (cum > (double)U[b]) { tokens[b] = v; break; }
+    }
+    if (tokens[b] < 0) {  /* U at the top end after rounding: the last v with mass */
+      for (int v = V - 1; v >= 0; --v) if (p[v] > 0.0) { tokens[b] = v; break; }
+      row_status[b] |= ROW_FALLBACK;
+    }
+    q_out[b] = p[tokens[b]];
+  }
+  free(p);
+  free(cs);
+  return 0;
+}
+
+/* Exported: sigma_{F,C}(z/T) of one row, for the pins. */
+int specv_oracle_saguaro_probs(int V, int dtype, const void* row, double T, int F, double C,
+                               double* p) {
+  int am;
+  double m, ls;
+  int st = row_distribution(row, dtype, 0, V, T, p, &am, &m, &ls);
+  if (st || T == 0.0 || F == 0) return st;
+  cand_t* cs = (cand_t*)malloc(sizeof(cand_t) * (size_t)V);
+  st = saguaro_reweight(row, dtype, 0, V, F, C, p, cs);
+  free(cs);
+  return st;
 }
 
 /* Exported: the a1 distribution of one row, for the pins. */
@@ -327,15 +428,6 @@ int specv_oracle_row_probs(int V, int dtype, const void* row, double T,
  *     logits, excluding the token sent for verification at that position.
  *     Full sort of the candidates; no partial selection.
  */
-typedef struct { double z; int v; } cand_t;
-
-static int cand_cmp(const void* a, const void* b) {
-  const cand_t* x = (const cand_t*)a;
-  const cand_t* y = (const cand_t*)b;
-  if (x->z > y->z) return -1;
-  if (x->z < y->z) return 1;
-  return (x->v < y->v) ? -1 : (x->v > y->v);
-}
 
 int specv_oracle_predict(int B, int K, int V, int F, int dtype,
                          const void* draft, int64_t d_bs, int64_t d_rs,

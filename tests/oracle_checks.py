@@ -639,6 +639,131 @@ def check_ragged_matches_rows(lib):
     assert np.all(o2["out_tokens"][3] == -1)
 
 
+def _top_mask(z, F):
+    """numpy lexsort: the F largest logits, ties to the lower index."""
+    order = np.lexsort((np.arange(len(z)), -z.astype(np.float64)))
+    m = np.zeros(len(z), bool)
+    m[order[:F]] = True
+    return m
+
+
+def check_saguaro_library(lib):
+    """[SSD] §4.2.1: sigma_{F,C}(z/T) = scipy softmax(z/T + log(C) on top_F(z))."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(41)
+    for _ in range(40):
+        V = int(rng.integers(2, 40))
+        z = (rng.integers(-3, 4, V) * 0.5 if rng.random() < 0.3 else rng.normal(0, 2, V)).astype(np.float32)
+        T = float(rng.choice([0.5, 1.0, 2.0]))
+        F = int(rng.integers(1, V))
+        C = float(rng.choice([0.1, 47 / 147, 0.5, 1.0]))
+        want = softmax(z.astype(np.float64) / T + np.where(_top_mask(z, F), np.log(C), 0.0))
+        np.testing.assert_allclose(oracle.saguaro_probs(z, T, F, C, lib=lib), want, rtol=1e-12,
+                                   atol=1e-15)
+
+
+def check_saguaro_thm19(lib):
+    """[SSD] Theorem 19 (Appendix A.3): p_d = (.49,.49,.01,.01) with F = 2 and
+    C = 47/147 becomes (.47,.47,.03,.03); the acceptance rate against
+    p_t = (.48,.48,.02,.02) is 0.98 with either; after a rejection the bonus
+    lands in the cache (top-2 of the draft) always with Saguaro, never without."""
+    zd = np.log(np.array([0.49, 0.49, 0.01, 0.01])).astype(np.float32)
+    zt = np.log(np.array([0.48, 0.48, 0.02, 0.02])).astype(np.float32)
+    q = oracle.saguaro_probs(zd, 1.0, 2, 47 / 147, lib=lib)
+    np.testing.assert_allclose(q, [0.47, 0.47, 0.03, 0.03], atol=2e-7)
+    # sampling from it: inverse CDF at U
+    s = oracle.saguaro_sample(np.stack([zd] * 4), np.ones(4, np.float32), 2, 47 / 147,
+                              np.array([0.2, 0.6, 0.95, 0.99], np.float32), lib=lib)
+    assert list(s["tokens"]) == [0, 1, 2, 3]
+    np.testing.assert_allclose(s["q"], [0.47, 0.47, 0.03, 0.03], atol=2e-7)
+    B = 64
+    rng = np.random.default_rng(19)
+    U = rng.uniform(0, 1, (B, 2)).astype(np.float32)
+    U[:, 0] = 0.999  # reject whenever p/q < 1
+    tgt = np.broadcast_to(np.stack([zt, zt])[None], (B, 2, 4))
+    dft = np.broadcast_to(zd[None, None], (B, 1, 4))
+    for sg, tok, in_cache in (((2, 47 / 147), 2, True), (None, 0, False)):
+        toks = np.full((B, 1), tok, np.int32)
+        o = oracle.verify(tgt, dft, toks, np.ones(B, np.float32), U, lib=lib, saguaro=sg)
+        np.testing.assert_allclose(o["alpha"][:, 0], 0.98, atol=2e-7)
+        assert (o["accept_len"] == 0).all()  # p/q = 2/3 (Saguaro) or 0.98 (plain) < 0.999
+        bonus = o["out_tokens"][:, 0]
+        assert (np.isin(bonus, [0, 1]) == in_cache).all(), (sg, bonus)
+
+
+def check_saguaro_thm15_monotone(lib):
+    """[SSD] Theorem 15: with the cache S = top_F(z_d), the share of residual
+    mass max(p_t - sigma_{F,C}, 0) inside S is non-increasing in C."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(15)
+    Cs = np.linspace(0.0, 1.0, 21)
+    for _ in range(30):
+        V = int(rng.integers(4, 30))
+        zd = rng.normal(0, 1.5, V).astype(np.float32)
+        zt = (zd + rng.normal(0, 1.0, V)).astype(np.float32)
+        F = int(rng.integers(1, V - 1))
+        pt = softmax(zt.astype(np.float64))
+        S = _top_mask(zd, F)
+        hit = []
+        for C in Cs:
+            if C == 0.0 and S.all():
+                continue
+            u = np.maximum(pt - oracle.saguaro_probs(zd, 1.0, F, float(C), lib=lib), 0.0)
+            hit.append(u[S].sum() / u.sum() if u.sum() > 0 else 1.0)
+        assert all(a >= b - 1e-12 for a, b in zip(hit, hit[1:])), hit
+
+
+def check_saguaro_exact_law(lib):
+    """Verification of drafts sampled from sigma_{F,C}: the output law is
+    exactly the target's (the enumeration weights drafts by sigma)."""
+    rng = np.random.default_rng(42)
+    V, K, F, C = 5, 2, 2, Fr(1, 3)
+    for _ in range(3):
+        P = rational_rows(rng, K + 1, V)
+        Pd = rational_rows(rng, K, V)
+        Q = []
+        for row in Pd:
+            zr = np.array([math.log(float(x)) for x in row])
+            m = _top_mask(zr, F)
+            w = [x * (C if m[v] else 1) for v, x in enumerate(row)]
+            tot = sum(w)
+            Q.append([x / tot for x in w])
+        leaves = enumerate_pieces(P, Q)
+        tokens = np.array([lf[1] for lf in leaves], np.int32)
+        uniforms = np.array([[float(u) for u in lf[2]] for lf in leaves], np.float32)
+        B = len(leaves)
+        zt, zd = logits_for(P), logits_for(Pd)
+        out = oracle.verify(np.broadcast_to(zt[None], (B,) + zt.shape),
+                            np.broadcast_to(zd[None], (B,) + zd.shape), tokens,
+                            np.ones(B, np.float32), uniforms, nthreads=0, lib=lib,
+                            saguaro=(F, float(C)))
+        for i in range(K + 1):
+            mass = Fr(0)
+            law = [Fr(0)] * V
+            for (w, _, _), ni, tk in zip(leaves, out["accept_len"], out["out_tokens"]):
+                if ni >= i:
+                    mass += w
+                    law[tk[i]] += w
+            assert [l / mass for l in law] == P[i], i
+
+
+def check_saguaro_sampler_inverse_cdf(lib):
+    """Draft-side sampling = numpy searchsorted on the cumulative sigma."""
+    rng = np.random.default_rng(43)
+    B, V = 50, 23
+    z = rng.normal(0, 2, (B, V)).astype(np.float32)
+    T = rng.choice([0.0, 0.7, 1.0], B).astype(np.float32)
+    U = rng.uniform(0, 1, B).astype(np.float32)
+    out = oracle.saguaro_sample(z, T, 3, 0.25, U, lib=lib)
+    for b in range(B):
+        if T[b] == 0:
+            assert out["tokens"][b] == int(np.argmax(z[b]))
+            continue
+        q = oracle.saguaro_probs(z[b], float(T[b]), 3, 0.25, lib=lib)
+        t = int(np.searchsorted(np.cumsum(q), float(U[b]), side="right"))
+        assert out["tokens"][b] == min(t, V - 1) and abs(out["q"][b] - q[out["tokens"][b]]) < 1e-15
+
+
 ALL_CHECKS = {
     "softmax_library": check_softmax_library,
     "thm1_overlap": check_thm1_overlap,
@@ -662,4 +787,9 @@ ALL_CHECKS = {
     "no_draft_one_hot": check_no_draft_is_one_hot_draft,
     "no_draft_exact_law": check_no_draft_exact_law,
     "ragged_rows": check_ragged_matches_rows,
+    "saguaro_library": check_saguaro_library,
+    "saguaro_thm19": check_saguaro_thm19,
+    "saguaro_thm15": check_saguaro_thm15_monotone,
+    "saguaro_exact_law": check_saguaro_exact_law,
+    "saguaro_sampler": check_saguaro_sampler_inverse_cdf,
 }

@@ -92,6 +92,20 @@ MUTATIONS = {
         "verify_row(kb, V, dtype, target, (c0 + b) * t_rs, t_rs, draft, c0 * d_rs, d_rs,",
         "verify_row(kb, V, dtype, target, c0 * t_rs, t_rs, draft, c0 * d_rs, d_rs,",
         ["ragged_rows"]),
+    # Saguaro sampling down-weighting the F smallest logits
+    "saguaro_bottom_f": (
+        "for (int f = 0; f < F && f < V; ++f) p[c[f].v] *= C;",
+        "for (int f = 0; f < F && f < V; ++f) p[c[V - 1 - f].v] *= C;",
+        ["saguaro_library", "saguaro_thm19"]),
+    "saguaro_not_renormalised": (
+        "if (!(S > 0.0)) return ROW_NONFINITE;\n  for (int v = 0; v < V; ++v) p[v] /= S;",
+        "if (!(S > 0.0)) return ROW_NONFINITE;",
+        ["saguaro_library"]),
+    # accept test with the plain draft probability after Saguaro sampling
+    "saguaro_plain_q_in_accept": (
+        ": sg_F > 0 ? log(qd[(int64_t)i * V + x[i]])",
+        ": sg_F > 0 ? log_prob(draft, dtype, dof, x[i], T, md[i], lsd[i])",
+        ["saguaro_exact_law"]),
     "hit_wrong_length": (
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
