@@ -189,6 +189,13 @@ typedef struct {
                                 fanout[k] keys at lookahead k (0..F; the rest
                                 are -1), e.g. from specv_geometric_fanout.
                                 NULL: F keys at every lookahead. */
+  int32_t saguaro_F;         /* 0, or the drafts were sampled with Saguaro
+                                sampling sigma_{saguaro_F, saguaro_C} (see
+                                specv_saguaro_sample; 1 <= saguaro_F <= F): the
+                                accept test and the residual then use
+                                q_i = sigma(draft row i / T) instead of
+                                softmax (greedy rows unaffected) */
+  float saguaro_C;           /* in [0, 1] */
 } specv_ssd_args;
 
 size_t specv_ssd_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F,
@@ -223,6 +230,39 @@ size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V,
 specv_status specv_predict_outcomes(const specv_predict_args* args,
                                     void* workspace, size_t workspace_bytes,
                                     void* stream);
+
+/*
+ * Draft-side Saguaro sampling ("Speculative Speculative Decoding" §4.2.1):
+ * for each of B draft rows z (one lookahead of the drafter), with T =
+ * temperature[b]:
+ *   sigma_{F,C}(z/T)(t) is proportional to C * exp(z_t/T) for the F tokens of
+ *   largest logit (ties to the lower index) and to exp(z_t/T) otherwise;
+ *   tokens[b] = the smallest t whose running sum of sigma in index order
+ *   exceeds uniforms[b] (T = 0: the first argmax, sigma not applied);
+ *   q[b] = sigma(tokens[b]) (1 for greedy rows).
+ * F = 0 samples softmax(z/T) itself.  A row with no mass left (C = 0 and every
+ * finite logit in the top F) or a NaN / +inf logit gets token -1 and
+ * SPECV_ROW_NONFINITE; a bad temperature SPECV_ROW_BAD_TEMP.  The drafts drawn
+ * this way are verified with specv_ssd_args.saguaro_F / saguaro_C set to the
+ * same F and C.
+ */
+typedef struct {
+  int32_t B, V;
+  int32_t dtype;             /* specv_dtype */
+  const void* logits;        /* row b at logits + b * row_stride (elements) */
+  int64_t row_stride;        /* >= V */
+  const float* temperature;  /* [B] */
+  int32_t F;                 /* 0..32 */
+  float C;                   /* [0, 1] */
+  const float* uniforms;     /* [B] in [0, 1) */
+  int32_t* tokens;           /* OUT [B] */
+  float* q;                  /* OUT, optional [B] */
+  int32_t* row_status;       /* OUT, optional [B] */
+} specv_saguaro_args;
+
+size_t specv_saguaro_workspace_bytes(int32_t B, int32_t V, int32_t F, int32_t dtype);
+specv_status specv_saguaro_sample(const specv_saguaro_args* args, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /*
  * Geometric fan-out ("Speculative Speculative Decoding" Theorem 12, proved in

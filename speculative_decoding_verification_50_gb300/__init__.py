@@ -45,7 +45,13 @@ class VerifyArgs(ctypes.Structure):
 
 class SsdArgs(ctypes.Structure):
     _fields_ = [("verify", VerifyArgs), ("F", _I32), ("keys", _P), ("key_logits", _P),
-                ("hit", _P), ("fanout", _P)]
+                ("hit", _P), ("fanout", _P), ("saguaro_F", _I32), ("saguaro_C", ctypes.c_float)]
+
+
+class SaguaroArgs(ctypes.Structure):
+    _fields_ = [("B", _I32), ("V", _I32), ("dtype", _I32), ("logits", _P), ("row_stride", _I64),
+                ("temperature", _P), ("F", _I32), ("C", ctypes.c_float), ("uniforms", _P),
+                ("tokens", _P), ("q", _P), ("row_status", _P)]
 
 
 class PredictArgs(ctypes.Structure):
@@ -86,6 +92,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specv_predict_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
     lib.specv_predict_outcomes.restype = ctypes.c_int
     lib.specv_predict_outcomes.argtypes = [ctypes.POINTER(PredictArgs), _P, ctypes.c_size_t, _P]
+    lib.specv_saguaro_workspace_bytes.restype = ctypes.c_size_t
+    lib.specv_saguaro_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
+    lib.specv_saguaro_sample.restype = ctypes.c_int
+    lib.specv_saguaro_sample.argtypes = [ctypes.POINTER(SaguaroArgs), _P, ctypes.c_size_t, _P]
     lib.specv_geometric_fanout.restype = ctypes.c_int
     lib.specv_geometric_fanout.argtypes = [_I32, ctypes.c_double, ctypes.c_double, _I32, _I32,
                                            _P, _P]
@@ -272,14 +282,16 @@ def _fanout_arg(fanout, K: int):
 def specv_ssd_round(target, draft, draft_tokens, temperature, uniforms, F: int, *,
                     accept_len=None, out_tokens=None, p_draft=None, q_draft=None,
                     row_status=None, keys=None, key_logits=None, hit=None, workspace=None,
-                    fanout=None, stream=None) -> dict:
+                    fanout=None, saguaro=None, stream=None) -> dict:
     """One fused SSD round (see include/specv.h, specv_ssd_round): verification,
     top-F outcome keys at every lookahead and the hit flag, in one pass.
 
     draft must hold K+1 rows per batch row.  Returns the specv_verify outputs
     plus keys int32 [B, K+1, F], key_logits fp32 [B, K+1, F], hit uint8 [B].
     fanout (optional, K+1 ints in [0, F], e.g. from specv_geometric_fanout)
-    keeps only the first fanout[k] keys at lookahead k.
+    keeps only the first fanout[k] keys at lookahead k.  saguaro=(F_s, C): the
+    drafts were sampled from sigma_{F_s,C} (specv_saguaro_sample), so the
+    accept test and the residual use it as q.
     """
     import torch
     lib = load_library()
@@ -297,7 +309,9 @@ def specv_ssd_round(target, draft, draft_tokens, temperature, uniforms, F: int, 
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     fan_keep, fan_ptr = _fanout_arg(fanout, K)
-    sargs = SsdArgs(args, F, keys.data_ptr(), key_logits.data_ptr(), hit.data_ptr(), fan_ptr)
+    sg_F, sg_C = saguaro if saguaro else (0, 1.0)
+    sargs = SsdArgs(args, F, keys.data_ptr(), key_logits.data_ptr(), hit.data_ptr(), fan_ptr,
+                    int(sg_F), float(sg_C))
     _check(lib.specv_ssd_round(ctypes.byref(sargs), _ptr(workspace), workspace.numel(),
                                _stream(stream)))
     outs.update(keys=keys, key_logits=key_logits, hit=hit)
@@ -335,6 +349,31 @@ def specv_predict_outcomes(draft, draft_tokens, F: int, *, keys=None, key_logits
     _check(lib.specv_predict_outcomes(ctypes.byref(args), _ptr(workspace), workspace.numel(),
                                       _stream(stream)))
     return dict(keys=keys, key_logits=key_logits, row_status=row_status)
+
+
+def specv_saguaro_sample(logits, temperature, F: int, C: float, uniforms, *, tokens=None, q=None,
+                         row_status=None, workspace=None, stream=None) -> dict:
+    """Draft-side Saguaro sampling (see include/specv.h): one token per row of
+    logits [B, V] (bf16 or fp32, CUDA) from sigma_{F,C}(z/T) by inverse CDF of
+    uniforms [B].  Returns tokens int32 [B], q fp32 [B], row_status int32 [B]."""
+    import torch
+    lib = load_library()
+    assert logits.dim() == 2 and logits.stride(-1) == 1
+    B, V = logits.shape
+    dev = logits.device
+    tokens = torch.empty(B, dtype=torch.int32, device=dev) if tokens is None else tokens
+    q = torch.empty(B, dtype=torch.float32, device=dev) if q is None else q
+    row_status = torch.empty(B, dtype=torch.int32, device=dev) if row_status is None else row_status
+    code = _dtype_code(logits)
+    need = lib.specv_saguaro_workspace_bytes(B, V, int(F), code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    args = SaguaroArgs(B, V, code, logits.data_ptr(), logits.stride(0), temperature.data_ptr(),
+                       int(F), float(C), uniforms.data_ptr(), tokens.data_ptr(), q.data_ptr(),
+                       row_status.data_ptr())
+    _check(lib.specv_saguaro_sample(ctypes.byref(args), _ptr(workspace), workspace.numel(),
+                                    _stream(stream)))
+    return dict(tokens=tokens, q=q, row_status=row_status)
 
 
 def specv_geometric_fanout(K: int, a: float, r: float, budget: int, max_f: int = 32) -> tuple:

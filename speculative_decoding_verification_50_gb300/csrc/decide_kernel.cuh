@@ -40,6 +40,9 @@ struct PosStats {  // one position's combined row statistics
 struct Dec {  // a batch row's decision (the same in every CTA of its cluster)
   int32_t n, status, mode, need_scan, token, owner, last_pos, xn;
   float mt, md, ist, isd;
+  float sgc, zl;  // residual weights: C on the keys at or above (zl, il)
+  int32_t il, pad2;
+  double R;       // total residual mass (the sampler normalises its q by it)
   double tau, pre_mine;
   float px[kMaxK], qx[kMaxK];
 };
@@ -71,6 +74,8 @@ struct DecideParams {
   const int32_t* cu; // per-row draft counts (inclusive prefix sums), or null
   int32_t ntok;      // with cu: packed draft rows the buffers hold
   int32_t no_draft;  // no draft logits: q_i is one-hot at x_i
+  int32_t sg_F;      // Saguaro sampling: the drafts came from sigma_{sg_F, sg_C}
+  float sg_C;        //   (0: plain softmax drafts); the sampler's own F and C
 };
 
 // Combine the chunk records of one position over an aligned group of W lanes
@@ -186,19 +191,37 @@ __device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int3
 // one-hot at the rejected token xn) p with r(xn) = 0.  Both products rounded
 // before the subtraction (no contraction), so p(v) = q(v) gives r(v) = 0
 // exactly, as in the definition.
+// Saguaro weights ([SSD] §4.2.1): a logit z at index e is among the row's
+// top-F_s, and is weighted by C, iff its key (z, e) is at or above the F_s-th
+// key (zl, il) in (logit desc, index asc) order.  zl = +inf: no weights.
+struct SgW {
+  float C, zl;
+  int32_t il;
+  __device__ __forceinline__ bool in(float z, int64_t e) const {
+    return z > zl || (z == zl && e <= il);
+  }
+};
+
 template <int VW>
 __device__ __forceinline__ void residual_from(const float (&zt)[VW], const float (&zd)[VW], int mode,
                                               float mt, float md, float c, float ist, float isd,
-                                              int64_t e0, int xn, float (&r)[VW]) {
+                                              int64_t e0, int xn, const SgW& w, float (&r)[VW]) {
   if (mode == 2) {
 #pragma unroll
     for (int k = 0; k < VW; ++k)
       r[k] = (e0 + k == xn) ? 0.f : __fmul_rn(ex2((zt[k] - mt) * c), ist);
-  } else if (mode == 0) {
+  } else if (mode == 3) {  // the sampler: sigma_{F,C} of the row itself
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
       const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
-      const float q = __fmul_rn(ex2((zd[k] - md) * c), isd);
+      r[k] = w.in(zt[k], e0 + k) ? __fmul_rn(p, w.C) : p;
+    }
+  } else if (mode == 0) {  // q is sigma_{F,C} of the draft row when weighted
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
+      float q = __fmul_rn(ex2((zd[k] - md) * c), isd);
+      if (w.in(zd[k], e0 + k)) q = __fmul_rn(q, w.C);
       r[k] = fmaxf(__fsub_rn(p, q), 0.f);
     }
   } else {
@@ -211,14 +234,14 @@ __device__ __forceinline__ void residual_from(const float (&zt)[VW], const float
 template <int DT, bool VEC>
 __device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd, int64_t v0,
                                              int64_t v1, int j, int mode, float mt, float md,
-                                             float c, float ist, float isd, int xn,
+                                             float c, float ist, float isd, int xn, const SgW& w,
                                              float (&r)[Elem<DT>::VW]) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   float zt[VW], zd[VW];
   E::unpack(load_vec<DT, VEC>(rowt, v0, v1, j), zt);
   if (mode == 0) E::unpack(load_vec<DT, VEC>(rowd, v0, v1, j), zd);
-  residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, v0 + static_cast<int64_t>(j) * VW, xn, r);
+  residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, v0 + static_cast<int64_t>(j) * VW, xn, w, r);
 }
 
 // Staged residual pass (16-byte aligned rows): the slice C of target row n
@@ -242,7 +265,7 @@ __device__ __forceinline__ void ring_start(RingBars& R, unsigned char* ring, int
 template <int DT>
 __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, int S, const Chunk& C,
                                               int mode, float mt, float md, float c, float ist,
-                                              float isd, int xn, float* segs, int ntl) {
+                                              float isd, int xn, const SgW& w, float* segs, int ntl) {
   using E = Elem<DT>;
   using Vec = typename E::Vec;
   constexpr int VW = E::VW;
@@ -266,7 +289,7 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
         E::unpack(reinterpret_cast<const Vec*>(base)[jl], zt);
         if (mode == 0) E::unpack(reinterpret_cast<const Vec*>(base + kTripBytes)[jl], zd);
         const int64_t e0 = C.v0 + static_cast<int64_t>((t * kVecs + k) * kThreads + threadIdx.x) * VW;
-        residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, e0, xn, r);
+        residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, e0, xn, w, r);
         sum[k] = 0.f;
 #pragma unroll
         for (int q = 0; q < VW; ++q) sum[k] += r[q];
@@ -287,7 +310,7 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
             E::unpack(E::gather(C.rowt, e, C.v1), zt);
             if (mode == 0) E::unpack(E::gather(C.rowd, e, C.v1), zd);
           }
-          residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, e, xn, r);
+          residual_from<VW>(zt, zd, mode, mt, md, c, ist, isd, e, xn, w, r);
 #pragma unroll
           for (int q = 0; q < VW; ++q) sum[k] += r[q];
         }
@@ -330,19 +353,25 @@ template <int DT, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
-  constexpr bool kTopF = MODE != kModeVerify;
+  constexpr bool kTopF = MODE == kModeSsd;      // outcome keys and hit
+  constexpr bool kSample = MODE == kModeSample;  // draft-side Saguaro sampling
   extern __shared__ float segs[];  // [tiles * kWarps] segment sums of r
   __shared__ PosStats ps[kMaxK + 1];
   __shared__ Dec dec;
   __shared__ double cta_total[2];  // this CTA's residual mass, per attempt
   __shared__ int32_t tok_slot;  // rank 0: the token found by the owner CTA
+  __shared__ float q_slot;      // rank 0 (sampler): sigma of that token
+  __shared__ float sg_d[kMaxK + 1];    // Saguaro: weighted mass of the top-F_s,
+  __shared__ float sg_zl[kMaxK + 1];   //   its F_s-th key (zl, il), and whether
+  __shared__ int32_t sg_il[kMaxK + 1]; //   the sent token is among them
+  __shared__ int32_t sg_xin[kMaxK + 1];
   __shared__ int32_t copy_fail;  // rank 0: a CTA's staged copies did not land in time
   __shared__ RingBars ring_bars;
   __shared__ int32_t pre_x[kMaxK];  // draft tokens, their logits and the uniforms,
   __shared__ float pre_zt[kMaxK];   // fetched while the records are combined
   __shared__ float pre_zd[kMaxK];
   __shared__ float pre_u[kMaxK];
-  __shared__ WarpKeys wkeys[kTopF ? kWarps : 1];
+  __shared__ WarpKeys wkeys[(kTopF || kSample) ? kWarps : 1];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -389,9 +418,56 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
     if ((lane & 15) == 0 && i <= kb) ps[i] = p;
   }
   __syncthreads();
+
+  // ---- Saguaro sampling ([SSD] §4.2.1): the drafts of an SSD round came from
+  // sigma_{F_s,C}, and the sampler draws from it.  Per draft row: its top-F_s
+  // keys (the lookahead's merged candidates, which exclude the sent token x,
+  // with x put back in key order), their mass in units of 2^((z - Md) c), and
+  // the F_s-th key.  One warp per row.  Greedy rows are left one-hot.
+  const bool sg_on = (kSample || (kTopF && P.sg_F > 0)) && !greedy && temp_ok;
+  if (sg_on) {
+    const int nrows = kSample ? 1 : kb;
+    for (int i = warp; i < nrows; i += kWarps) {
+      const int64_t u = u0 + i;
+      const WarpTopF Lk = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
+                                    static_cast<int>(P.nchunk) * F, F, lane, wkeys[warp]);
+      const int fs = P.sg_F;
+      const int x = kSample ? -1 : pre_x[i];
+      const float zx = kSample ? neg_inf() : pre_zd[i];
+      const int pos = (x >= 0) ? __popc(__ballot_sync(0xffffffffu, lane < F && key_beats(Lk.v, Lk.i, zx, x)))
+                               : F;
+      const bool xin = x >= 0 && pos < fs;
+      const int fl = xin ? fs - 1 : fs;  // list entries inside the top-F_s
+      const float Md = ps[i].Md;
+      float d = (lane < fl && Lk.i != INT_MAX) ? ex2((Lk.v - Md) * c) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      if (xin) d += ex2((zx - Md) * c);
+      // the F_s-th key of the list with x inserted at pos
+      const int src = (!xin) ? fs - 1 : (pos == fs - 1 ? -1 : fs - 2);
+      const float lv = __shfl_sync(0xffffffffu, Lk.v, src < 0 ? 0 : src);
+      const int32_t li = __shfl_sync(0xffffffffu, Lk.i, src < 0 ? 0 : src);
+      if (lane == 0) {
+        sg_d[i] = d;
+        sg_zl[i] = src < 0 ? zx : lv;
+        sg_il[i] = src < 0 ? x : li;
+        sg_xin[i] = xin;
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 0) {
     int nf = 0;
-    if (lane <= kb && temp_ok) {
+    // Saguaro: the weighted normaliser of draft row i, sum - (1 - C) * top-F_s mass
+    const float sgC = sg_on ? P.sg_C : 1.f;
+    auto sdp = [&](int i) -> double {
+      return sg_on ? ps[i].Sd - (1.0 - static_cast<double>(sgC)) * static_cast<double>(sg_d[i]) : ps[i].Sd;
+    };
+    if (kSample && temp_ok && lane == 0) {  // the sampled row sits in the draft fields
+      const PosStats& q = ps[0];
+      nf = greedy ? ((q.bad & 1) || q.id == INT_MAX)
+                  : (!(q.Sd >= 1.0) || q.Md == kNegMax || !(sdp(0) > 0.0));
+    } else if (!kSample && lane <= kb && temp_ok) {
       const PosStats& q = ps[lane];
       const bool d_full = lane < kb && !nd;  // draft rows that are normalised
       const bool d_any = (MODE != kModeVerify) || d_full;
@@ -399,7 +475,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         nf = (q.bad & 1) || q.it == INT_MAX || (d_full && q.id == INT_MAX);
       } else {
         nf = !(q.St >= 1.0) || q.Mt == kNegMax;
-        if (d_full) nf |= !(q.Sd >= 1.0) || q.Md == kNegMax;
+        if (d_full) nf |= !(q.Sd >= 1.0) || q.Md == kNegMax || !(sdp(lane) > 0.0);
         else if (d_any) nf |= q.Sd != q.Sd;  // draft row K: NaN / +inf only
       }
     }
@@ -429,11 +505,12 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         const float zdx = pre_zd[lane];
         const float lt = __fmul_rn(ztx - q.Mt, c);  // log2 of unnormalised p_i(x), q_i(x)
         const float ld = __fmul_rn(zdx - q.Md, c);
-        const float St = static_cast<float>(q.St), Sd = static_cast<float>(q.Sd);
+        const float St = static_cast<float>(q.St), Sd = static_cast<float>(sdp(lane));
+        const float wx = (sg_on && sg_xin[lane]) ? sgC : 1.f;  // Saguaro weight of x_i
         px = __fdiv_rn(ex2(lt), St);
-        qx = __fdiv_rn(ex2(ld), Sd);
-        if (zdx != neg_inf()) {  // q_i(x_i) > 0
-          const float ratio = __fmul_rn(ex2(__fsub_rn(lt, ld)), __fdiv_rn(Sd, St));
+        qx = __fdiv_rn(__fmul_rn(ex2(ld), wx), Sd);
+        if (zdx != neg_inf() && wx > 0.f) {  // q_i(x_i) > 0
+          const float ratio = __fdiv_rn(__fmul_rn(ex2(__fsub_rn(lt, ld)), __fdiv_rn(Sd, St)), wx);
           accept = ratio >= pre_u[lane];
         }
       }
@@ -448,19 +525,26 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       const PosStats& q = ps[n];
       dec.n = n;
       dec.status = status;
-      dec.mode = (n < kb) ? (nd ? 2 : 0) : 1;
+      dec.mode = kSample ? 3 : (n < kb) ? (nd ? 2 : 0) : 1;
       dec.xn = (n < kb) ? pre_x[n] : -1;
       dec.need_scan = ok && !greedy;
-      dec.token = (ok && greedy) ? q.it : -1;
+      dec.token = (ok && greedy) ? (kSample ? q.id : q.it) : -1;
       dec.owner = -1;
       dec.last_pos = 0;
-      dec.mt = q.Mt;
+      // the sampler's row statistics are the draft fields of position 0
+      dec.mt = kSample ? q.Md : q.Mt;
       dec.md = q.Md;
-      dec.ist = static_cast<float>(1.0 / q.St);
-      dec.isd = static_cast<float>(1.0 / q.Sd);
+      dec.ist = static_cast<float>(1.0 / (kSample ? sdp(0) : q.St));
+      dec.isd = static_cast<float>(1.0 / ((n < kb) ? sdp(n) : q.Sd));
+      // Saguaro weights on the residual: the draft row n (mode 0) or the row (mode 3)
+      const bool weighted = sg_on && (kSample || (n < kb && !nd));
+      dec.sgc = weighted ? sgC : 1.f;
+      dec.zl = weighted ? sg_zl[n] : pos_inf();
+      dec.il = weighted ? sg_il[n] : -1;
       dec.tau = 0.0;
       dec.pre_mine = 0.0;
       tok_slot = dec.token;
+      q_slot = (ok && greedy) ? 1.f : 0.f;
       copy_fail = 0;
     }
   }
@@ -472,7 +556,9 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   Chunk RC;
   RC.b = b;
   RC.i = n_dec;
-  RC.rowt = static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(n_dec) * P.t_rs) * E::ES;
+  RC.rowt = kSample  // the sampler reads its one row through the target slot
+                ? static_cast<const char*>(P.zd) + L.d_off * E::ES
+                : static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(n_dec) * P.t_rs) * E::ES;
   RC.rowd = (dec.mode == 0)  // draft row n, read only for the residual max(p - q, 0)
                 ? static_cast<const char*>(P.zd) + (L.d_off + static_cast<int64_t>(n_dec) * P.d_rs) * E::ES
                 : nullptr;
@@ -489,6 +575,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   }
 
   if (dec.need_scan) {
+    const SgW sgw{dec.sgc, dec.zl, dec.il};
     const void* rowt = RC.rowt;
     const void* rowd = RC.rowd;
     const int64_t v0 = RC.v0;
@@ -504,7 +591,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         Chunk SC = RC;
         if (mode != 0) SC.rowd = nullptr;
         copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd,
-                                      dec.xn, segs, ntl);
+                                      dec.xn, sgw, segs, ntl);
       } else
       for (int t0 = 0; t0 < ntl; t0 += kTileUnroll) {
         float s[kTileUnroll];
@@ -514,7 +601,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
           s[q] = 0.f;
           if (j < nv) {
             float r[VW];
-            residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, dec.xn, r);
+            residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, dec.xn, sgw, r);
 #pragma unroll
             for (int k = 0; k < VW; ++k) s[q] += r[k];
           }
@@ -550,6 +637,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         if (lane == 0) {
           dec.tau = tau;
           dec.pre_mine = pm;
+          dec.R = R;
           if (R > 0.0) {
             if (own) {
               dec.owner = __ffs(own) - 1;
@@ -625,9 +713,10 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       for (int k = 0; k < VW; ++k) r[k] = 0.f;
       if (seg >= 0 && j < nv)
         residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, dec.mode, dec.mt, dec.md, c, dec.ist,
-                              dec.isd, dec.xn, r);
+                              dec.isd, dec.xn, sgw, r);
       const int32_t base = static_cast<int32_t>(v0) + j * VW;
       int found = -1;
+      float rv = 0.f;  // r at the found logit (the sampler reports it as sigma(t))
       if (!lp) {
         float vs = 0.f;
 #pragma unroll
@@ -652,7 +741,11 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
                 if (kk < 0 && run > tau) kk = k;
               }
             }
-            found = base + (kk >= 0 ? kk : klast);
+            const int ksel = kk >= 0 ? kk : klast;
+            found = base + ksel;
+#pragma unroll
+            for (int k = 0; k < VW; ++k)
+              if (k == ksel) rv = r[k];
           }
         } else {
           lp = true;
@@ -664,11 +757,22 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         for (int k = 0; k < VW; ++k)
           if (r[k] > 0.f) kl = k;
         const unsigned m = __ballot_sync(0xffffffffu, kl >= 0);
-        if (m && lane == 31 - __clz(m)) found = base + kl;
+        if (m && lane == 31 - __clz(m)) {
+          found = base + kl;
+#pragma unroll
+          for (int k = 0; k < VW; ++k)
+            if (k == kl) rv = r[k];
+        }
       }
       const unsigned mf = __ballot_sync(0xffffffffu, found >= 0);
       const int tok = mf ? __shfl_sync(0xffffffffu, found, __ffs(mf) - 1) : -1;
-      if (lane == 0) *cluster.map_shared_rank(&tok_slot, 0) = tok;
+      const float rq = mf ? __shfl_sync(0xffffffffu, rv, __ffs(mf) - 1) : 0.f;
+      if (lane == 0) {
+        *cluster.map_shared_rank(&tok_slot, 0) = tok;
+        // sigma(t) = r(t) / R: the pass's own total, free of the cancellation
+        // in the weighted normaliser
+        if (kSample) *cluster.map_shared_rank(&q_slot, 0) = static_cast<float>(rq / dec.R);
+      }
     }
   }
   // ---- outcome keys, while the owner CTA's warp 0 scans: warps 1..7 of CTA
@@ -717,7 +821,11 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         if (P.key_logits) P.key_logits[u0 * F + e] = neg_inf();
       }
     if (t == 0) {
-      P.accept_len[b] = ok ? n : 0;
+      if (kSample) {
+        if (P.q_draft) P.q_draft[b] = ok ? q_slot : 0.f;  // sigma(token)
+      } else {
+        P.accept_len[b] = ok ? n : 0;
+      }
       if (P.row_status) P.row_status[b] = ok ? (status & kFallback) : (status & kErrors);
       if (P.hit) {
         uint8_t h = 0;

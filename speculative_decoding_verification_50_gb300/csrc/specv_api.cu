@@ -329,11 +329,15 @@ size_t specv_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t dty
 
 namespace {
 
+// Both kernels for one call: verification, an SSD round, or (kModeSample, K =
+// 0, the drafter's rows as draft rows) Saguaro sampling.  sg_F/sg_C: the
+// Saguaro sampling scheme of the drafts (sg_F = 0: none).
 specv_status run_verify(const specv_verify_args* a, void* workspace, size_t workspace_bytes,
                         void* stream, int mode, int32_t F, int32_t* keys, float* key_logits,
-                        uint8_t* hit, const int32_t* fanout) {
+                        uint8_t* hit, const int32_t* fanout, int32_t sg_F = 0, float sg_C = 1.f) {
   const int32_t B = a->B, K = a->K, V = a->V;
-  const Plan pl = make_plan(B, K, V, mode == kModeSsd ? F : 0, a->dtype);
+  const bool cands = mode == kModeSsd || mode == kModeSample;
+  const Plan pl = make_plan(B, K, V, cands ? F : 0, a->dtype);
   if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need)
@@ -377,8 +381,9 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.cu = a->cu_num_draft_tokens;
   sp.ntok = a->num_draft_tokens;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = mode == kModeSsd ? launch_stats<kModeSsd>(a->dtype, vec, units * pl.nchunk, s, sp)
-                                   : launch_stats<kModeVerify>(a->dtype, vec, units * pl.nchunk, s, sp);
+  cudaError_t e = mode == kModeSsd      ? launch_stats<kModeSsd>(a->dtype, vec, units * pl.nchunk, s, sp)
+                  : mode == kModeSample ? launch_stats<kModeSample>(a->dtype, vec, units * pl.nchunk, s, sp)
+                                        : launch_stats<kModeVerify>(a->dtype, vec, units * pl.nchunk, s, sp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
   e = record_split(s);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "split event: %s", cudaGetErrorString(e));
@@ -418,6 +423,8 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   dp.cu = a->cu_num_draft_tokens;
   dp.ntok = a->num_draft_tokens;
   dp.no_draft = (a->flags & SPECV_NO_DRAFT_PROBS) ? 1 : 0;
+  dp.sg_F = sg_F;
+  dp.sg_C = sg_C;
   dp.ring_off = static_cast<int32_t>(round_up(pl.smemB, 128));
   dp.stages = ring_stages_b();
   size_t smemB = dp.ring_off + static_cast<size_t>(dp.stages) * 2 * kTripBytes;
@@ -425,8 +432,9 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
     dp.stages = 0;
     smemB = pl.smemB;
   }
-  e = mode == kModeSsd ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, smemB, s, dp)
-                       : launch_decide<kModeVerify>(a->dtype, vec, pl.CB, B, smemB, s, dp);
+  e = mode == kModeSsd      ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, smemB, s, dp)
+      : mode == kModeSample ? launch_decide<kModeSample>(a->dtype, vec, pl.CB, B, smemB, s, dp)
+                            : launch_decide<kModeVerify>(a->dtype, vec, pl.CB, B, smemB, s, dp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "decision launch: %s", cudaGetErrorString(e));
   g_launches = 2;
   return ok();
@@ -469,8 +477,13 @@ specv_status specv_ssd_round(const specv_ssd_args* a, void* workspace, size_t wo
     for (int k = 0; k <= a->verify.K; ++k)
       if (a->fanout[k] < 0 || a->fanout[k] > a->F)
         return fail(SPECV_ERR_INVALID_ARG, "fanout[%d]=%d outside [0, F=%d]", k, a->fanout[k], a->F);
+  if (a->saguaro_F < 0 || a->saguaro_F > a->F)
+    return fail(SPECV_ERR_INVALID_ARG, "saguaro_F=%d outside [0, F=%d]", a->saguaro_F, a->F);
+  if (a->saguaro_F > 0 && !(a->saguaro_C >= 0.f && a->saguaro_C <= 1.f))
+    return fail(SPECV_ERR_INVALID_ARG, "saguaro_C=%g outside [0, 1]", a->saguaro_C);
   return run_verify(&a->verify, workspace, workspace_bytes, stream, kModeSsd, a->F, a->keys,
-                    a->key_logits, a->hit, a->fanout);
+                    a->key_logits, a->hit, a->fanout, a->saguaro_F,
+                    a->saguaro_F > 0 ? a->saguaro_C : 1.f);
 }
 
 size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
@@ -563,6 +576,54 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "keys launch: %s", cudaGetErrorString(e));
   g_launches = 2;
   return ok();
+}
+
+size_t specv_saguaro_workspace_bytes(int32_t B, int32_t V, int32_t F, int32_t dtype) {
+  if (B <= 0 || V < 1 || F < 0 || F > 32) return 0;
+  return plan_workspace(make_plan(B, 0, V, F > 0 ? F : 1, dtype));
+}
+
+// Saguaro sampling runs the verification pipeline with no drafts (K = 0):
+// kernel A streams each row once (statistics and its top-F candidates), and
+// kernel B draws the token from sigma_{F,C} by inverse CDF of the uniform.
+specv_status specv_saguaro_sample(const specv_saguaro_args* a, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  g_launches = 0;
+  if (!a) return fail(SPECV_ERR_INVALID_ARG, "args is NULL");
+  const int32_t B = a->B, V = a->V;
+  if (B < 0) return fail(SPECV_ERR_INVALID_ARG, "B=%d < 0", B);
+  if (V < 1) return fail(SPECV_ERR_INVALID_ARG, "V=%d < 1", V);
+  if (a->dtype != SPECV_BF16 && a->dtype != SPECV_FP32)
+    return fail(SPECV_ERR_INVALID_ARG, "dtype=%d is not SPECV_BF16 or SPECV_FP32", a->dtype);
+  if (a->F < 0 || a->F > 32) return fail(SPECV_ERR_INVALID_ARG, "F=%d outside [0, 32]", a->F);
+  if (!(a->C >= 0.f && a->C <= 1.f)) return fail(SPECV_ERR_INVALID_ARG, "C=%g outside [0, 1]", a->C);
+  if (B == 0) return ok();
+  if (!a->logits || !a->temperature || !a->uniforms || !a->tokens)
+    return fail(SPECV_ERR_INVALID_ARG, "a required pointer is NULL");
+  const int es = elem_bytes(a->dtype);
+  if (!aligned(a->logits, es) || !aligned(a->temperature, 4) || !aligned(a->uniforms, 4) ||
+      !aligned(a->tokens, 4) || !aligned(a->q, 4) || !aligned(a->row_status, 4))
+    return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
+  if (a->row_stride < V) return fail(SPECV_ERR_INVALID_ARG, "row stride smaller than V");
+  specv_verify_args v = {};
+  v.B = B;
+  v.K = 0;
+  v.V = V;
+  v.dtype = a->dtype;
+  v.target_logits = a->logits;  // read through the draft slot; kept valid for the checks
+  v.target_batch_stride = a->row_stride;
+  v.target_row_stride = a->row_stride;
+  v.draft_logits = a->logits;
+  v.draft_batch_stride = a->row_stride;
+  v.draft_row_stride = a->row_stride;
+  v.temperature = a->temperature;
+  v.uniforms = a->uniforms;
+  v.out_tokens = a->tokens;
+  v.q_draft = a->q;
+  v.row_status = a->row_status;
+  const int32_t F = a->F > 0 ? a->F : 1;
+  return run_verify(&v, workspace, workspace_bytes, stream, kModeSample, F, nullptr, nullptr,
+                    nullptr, nullptr, a->F, a->F > 0 ? a->C : 1.f);
 }
 
 // Theorem 12 of "Speculative Speculative Decoding": F_k = F_0 q^k (k < K) and

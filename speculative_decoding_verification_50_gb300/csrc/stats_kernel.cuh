@@ -32,7 +32,14 @@
 
 namespace specv {
 
-enum : int { kModeVerify = 0, kModeSsd = 1, kModePredict = 2 };
+// verify: target and draft rows; ssd: plus draft row K and candidates;
+// predict: draft rows 0..K, candidates, no temperature; sample: one draft row
+// per batch row (K = 0) with its temperature and candidates (no exclusion).
+enum : int { kModeVerify = 0, kModeSsd = 1, kModePredict = 2, kModeSample = 3 };
+
+// Streams target rows; uses the temperature.
+__host__ __device__ constexpr bool mode_has_target(int m) { return m == kModeVerify || m == kModeSsd; }
+__host__ __device__ constexpr bool mode_has_temp(int m) { return m != kModePredict; }
 constexpr int kVecs = 2;  // 16-byte vectors per row per thread per loop trip
 constexpr int kMaxStages = 8;
 constexpr int kTripBytes = kVecs * kThreads * 16;  // one row's share of a trip (8 KB)
@@ -332,7 +339,7 @@ __device__ __forceinline__ Chunk chunk_at(const StatsParams& P, int64_t item) {
   // Verification reads draft rows i < K_b (none without draft logits);
   // prediction reads draft rows 0..K.
   const bool has_d = live && ((MODE == kModeVerify) ? (C.i < L.kb && P.zd != nullptr) : true);
-  C.rowt = (MODE != kModePredict && live)
+  C.rowt = (mode_has_target(MODE) && live)
                ? static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(C.i) * P.t_rs) * E::ES
                : nullptr;
   C.rowd = has_d ? static_cast<const char*>(P.zd) + (L.d_off + static_cast<int64_t>(C.i) * P.d_rs) * E::ES
@@ -755,13 +762,13 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
 // aligned rows, P.stages stages of dynamic shared memory); one CTA per item.
 template <int DT, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
-  constexpr bool kT = MODE != kModePredict;
+  constexpr bool kT = mode_has_target(MODE);
   constexpr bool kTopF = MODE != kModeVerify;
   __shared__ EpiSmem S;
   pdl_launch_dependents();  // the decision kernel may be scheduled once every CTA has started
   const Chunk C = chunk_at<DT, MODE>(P, blockIdx.x);
-  const float T = kT ? P.temp[C.b] : 0.f;
-  const bool greedy = !kT || T == 0.f;
+  const float T = mode_has_temp(MODE) ? P.temp[C.b] : 0.f;
+  const bool greedy = !mode_has_temp(MODE) || T == 0.f;
   const float c = greedy ? 1.f : temp_scale(T);
   Acc<Elem<DT>::VW> A;
   A.init();
@@ -857,7 +864,7 @@ __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* r
 
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const StatsParams P) {
-  constexpr bool kT = MODE != kModePredict;
+  constexpr bool kT = mode_has_target(MODE);
   constexpr bool kTopF = MODE != kModeVerify;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ RingBars R;
@@ -881,8 +888,8 @@ __global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const Stats
   uint32_t ph = 0;
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
     const Chunk C = chunk_at<DT, MODE>(P, item);
-    const float T = kT ? P.temp[C.b] : 0.f;
-    const bool greedy = !kT || T == 0.f;
+    const float T = mode_has_temp(MODE) ? P.temp[C.b] : 0.f;
+    const bool greedy = !mode_has_temp(MODE) || T == 0.f;
     const float c = greedy ? 1.f : temp_scale(T);
     Acc<Elem<DT>::VW> A;
     A.init();

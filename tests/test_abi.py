@@ -137,12 +137,14 @@ def test_struct_layouts_match_the_header(tmp_path):
 #include <stdio.h>
 #include "specv.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(specv_verify_args),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(specv_verify_args),
          offsetof(specv_verify_args, target_logits), offsetof(specv_verify_args, draft_tokens),
          offsetof(specv_verify_args, row_status), sizeof(specv_ssd_args),
          offsetof(specv_ssd_args, keys), sizeof(specv_predict_args),
          offsetof(specv_predict_args, row_status), offsetof(specv_ssd_args, fanout),
-         offsetof(specv_predict_args, fanout));
+         offsetof(specv_predict_args, fanout), offsetof(specv_ssd_args, saguaro_C),
+         sizeof(specv_saguaro_args), offsetof(specv_saguaro_args, C),
+         offsetof(specv_saguaro_args, row_status));
   return 0;
 }
 ''')
@@ -153,7 +155,9 @@ int main(void) {
             sv.VerifyArgs.draft_tokens.offset, sv.VerifyArgs.row_status.offset,
             ctypes.sizeof(sv.SsdArgs), sv.SsdArgs.keys.offset, ctypes.sizeof(sv.PredictArgs),
             sv.PredictArgs.row_status.offset, sv.SsdArgs.fanout.offset,
-            sv.PredictArgs.fanout.offset]
+            sv.PredictArgs.fanout.offset, sv.SsdArgs.saguaro_C.offset,
+            ctypes.sizeof(sv.SaguaroArgs), sv.SaguaroArgs.C.offset,
+            sv.SaguaroArgs.row_status.offset]
     assert got == want
 
 
@@ -252,3 +256,24 @@ def test_ssd_round_refuses_verification_only_modes(lib):
     s.verify.cu_num_draft_tokens = 0x10000
     s.verify.num_draft_tokens = 4
     assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_UNSUPPORTED
+
+
+def test_saguaro_arguments_are_checked(lib):
+    P = 0x10000
+    base = sv.SaguaroArgs(4, 100, sv.SPECV_FP32, P, 100, P, 6, 0.25, P, P, 0, 0)
+    for field, val in (("F", -1), ("F", 33), ("C", 1.5), ("C", -0.1), ("V", 0), ("dtype", 9),
+                       ("logits", None), ("tokens", None), ("row_stride", 99), ("logits", 0x10002)):
+        a = sv.SaguaroArgs.from_buffer_copy(base)
+        setattr(a, field, val)
+        assert lib.specv_saguaro_sample(ctypes.byref(a), ctypes.c_void_p(0x100000), 1 << 20,
+                                        None) == sv.SPECV_ERR_INVALID_ARG, field
+    a = sv.SaguaroArgs.from_buffer_copy(base)
+    assert lib.specv_saguaro_sample(ctypes.byref(a), None, 0, None) == sv.SPECV_ERR_WORKSPACE
+    assert lib.specv_saguaro_workspace_bytes(4, 100, 6, sv.SPECV_FP32) > 0
+    a.B = 0
+    assert lib.specv_saguaro_sample(ctypes.byref(a), None, 0, None) == sv.SPECV_OK
+    # an SSD round whose Saguaro F exceeds its key width, or C outside [0, 1]
+    s = sv.SsdArgs(_args(draft_batch_stride=400), 6, 0x10000, 0, 0x10000, None, 7, 0.5)
+    assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+    s = sv.SsdArgs(_args(draft_batch_stride=400), 6, 0x10000, 0, 0x10000, None, 3, 1.5)
+    assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
