@@ -50,6 +50,12 @@ WORKLOADS = {
     "cfg5-ssd-geo": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd-geo", ssd=True, F=6),
                      "config 5 as a full SSD round with the Theorem 12 geometric fan-out "
                      "(a=0.5, r=1, 54 keys over the K+1 lookaheads) + hit check"),
+    "cfg5-ssd-saguaro": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ssd-saguaro", ssd=True, F=6),
+                         "config 5 as a full SSD round whose drafts came from Saguaro sampling "
+                         "sigma_{6,0.3} (q = sigma in the accept test and the residual)"),
+    "cfg5-sample": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-sample", ssd=True),
+                    "Saguaro draft-side sampling sigma_{6,0.3} of the B*(K+1) = 2304 draft rows "
+                    "of a config 5 round (V=152064 fp32), one token per row"),
     "cfg5-ragged": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-ragged"),
                     "config 5 with per-row draft counts K_b in 0..8 (seeded), rows packed "
                     "by cu_num_draft_tokens, verify only"),
@@ -65,7 +71,10 @@ WORKLOADS = {
 
 # Workloads in another layout: rows packed by per-row draft counts, or
 # verification without draft logits.
-LAYOUT = {"cfg5-ragged": "ragged", "cfg5-nodraft": "nodraft"}
+LAYOUT = {"cfg5-ragged": "ragged", "cfg5-nodraft": "nodraft", "cfg5-sample": "sample"}
+
+# Saguaro sampling (F_s, C) of the drafts (SSD rounds) or of the sampler.
+SAGUARO = {"cfg5-ssd-saguaro": (6, 0.3), "cfg5-sample": (6, 0.3)}
 
 # Workloads whose keys follow the geometric fan-out: (acceptance rate a,
 # power-law exponent r, key budget over the K+1 lookaheads).
@@ -245,40 +254,51 @@ def lay_out(data, spec, mode, first_row: int = 0) -> dict:
         lay.update(rows=int((kb + 1).sum()), bytes=int((2 * kb + 1).sum()) * V * s)
     elif mode == "nodraft":
         lay.update(draft=None, rows=B * (K + 1), bytes=B * (K + 1) * V * s)
+    elif mode == "sample":  # every draft row of the round, one draw each
+        rows = data["draft"].reshape(-1, V)
+        n = rows.shape[0]
+        lay.update(target=None, draft=rows, tokens=np.zeros(0, np.int32),
+                   temperature=np.repeat(data["temperature"], K + 1).astype(np.float32),
+                   uniforms=np.resize(data["uniforms"].reshape(-1), n).astype(np.float32),
+                   rows=n, bytes=n * V * s)
     else:
         ab = algorithmic_bytes(dataclasses.replace(spec, B=B))
         lay.update(rows=B * (K + 1), bytes=ab["step_fused"] if spec.F else ab["verify"])
     return lay
 
 
-def time_oracle(lay, spec, nthreads: int, mode=None) -> float:
+def time_oracle(lay, spec, nthreads: int, mode=None, saguaro=None) -> float:
     import oracle
     t0 = time.perf_counter()
+    if mode == "sample":
+        oracle.saguaro_sample(lay["draft"], lay["temperature"], *saguaro, lay["uniforms"])
+        return time.perf_counter() - t0
     if mode == "ragged":
         oracle.verify_ragged(lay["target"], lay["draft"], lay["cu"], lay["tokens"],
                              lay["temperature"], lay["uniforms"], spec.K, nthreads=nthreads)
         return time.perf_counter() - t0
     o = oracle.verify(lay["target"], lay["draft"], lay["tokens"], lay["temperature"],
-                      lay["uniforms"], nthreads=nthreads, no_draft=(mode == "nodraft"))
+                      lay["uniforms"], nthreads=nthreads, no_draft=(mode == "nodraft"),
+                      saguaro=saguaro)
     if spec.F:
         p = oracle.predict(lay["draft"], lay["tokens"], spec.F, nthreads=nthreads)
         oracle.check_hit(p["keys"], o["accept_len"], o["out_tokens"])
     return time.perf_counter() - t0
 
 
-def cpu_baseline(spec, budget_s: float = 12.0, mode=None) -> dict:
+def cpu_baseline(spec, budget_s: float = 12.0, mode=None, saguaro=None) -> dict:
     """The oracle on a bounded sample of the workload, on this host's cores."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
     rows = list(range(min(spec.B, max(1, cores))))
     lay = lay_out(wl.generate(spec, rows=rows), spec, mode)
-    t = time_oracle(lay, spec, cores, mode)
+    t = time_oracle(lay, spec, cores, mode, saguaro)
     per_row = t / len(rows)
     n = int(min(spec.B, max(len(rows), budget_s / max(per_row, 1e-6))))
     if n > len(rows):
         lay = lay_out(wl.generate(spec, rows=list(range(n))), spec, mode)
-        t = time_oracle(lay, spec, cores, mode)
+        t = time_oracle(lay, spec, cores, mode, saguaro)
     value = lay["rows"] / t
     return {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {spec.B} batch rows of {spec.name} "
@@ -314,6 +334,7 @@ def run_ours(args) -> None:
         spec = dataclasses.replace(spec, F=max(1, max(fanout)))
         desc += f" [F_k = {fanout}]"
     mode = LAYOUT.get(args.workload)
+    saguaro = SAGUARO.get(args.workload)
     data = wl.generate(spec, rows=shard_rows(rank, world, spec.B))
     lay = lay_out(data, spec, mode, first_row=rank * spec.B)
     B, K, V, F = spec.B, spec.K, spec.V, spec.F
@@ -323,26 +344,32 @@ def run_ours(args) -> None:
         t = torch.from_numpy(a)
         return t.view(torch.bfloat16) if is_bf16 else t
 
-    h_target = host_logits(lay["target"]).pin_memory()
+    h_target = host_logits(lay["target"]).pin_memory() if lay["target"] is not None else None
     h_draft = host_logits(lay["draft"]).pin_memory() if lay["draft"] is not None else None
     h_tok = torch.from_numpy(lay["tokens"]).pin_memory()
     h_temp = torch.from_numpy(lay["temperature"]).pin_memory()
     h_unif = torch.from_numpy(lay["uniforms"]).pin_memory()
     h_cu = torch.from_numpy(lay["cu"]).pin_memory() if lay["cu"] is not None else None
-    d_target = h_target.to(dev)
+    d_target = h_target.to(dev) if h_target is not None else None
     d_draft = h_draft.to(dev) if h_draft is not None else None
     d_tok, d_temp, d_unif = h_tok.to(dev), h_temp.to(dev), h_unif.to(dev)
     d_cu = h_cu.to(dev) if h_cu is not None else None
-    pq_shape = (max(1, h_tok.numel()),) if mode == "ragged" else (B, K)
+    pq_shape = (max(1, h_tok.numel()),) if mode == "ragged" else \
+        (lay["rows"],) if mode == "sample" else (B, K)
 
     i32 = dict(dtype=torch.int32, device=dev)
+    n_out = lay["rows"] if mode == "sample" else B
     outs = dict(accept_len=torch.empty(B, **i32), out_tokens=torch.empty((B, K + 1), **i32),
                 p_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
                 q_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
-                row_status=torch.empty(B, **i32))
+                row_status=torch.empty(n_out, **i32))
     lib = sv.load_library()
     code = sv.SPECV_BF16 if is_bf16 else sv.SPECV_FP32
     ws_v = torch.empty(max(1, lib.specv_verify_workspace_bytes(B, K, V, code)), dtype=torch.uint8, device=dev)
+    if mode == "sample":
+        ws_v = torch.empty(max(1, lib.specv_saguaro_workspace_bytes(lay["rows"], V, saguaro[0], code)),
+                           dtype=torch.uint8, device=dev)
+        s_tok = torch.empty(lay["rows"], **i32)
     if F:
         keys = torch.empty((B, K + 1, F), **i32)
         key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
@@ -355,10 +382,14 @@ def run_ours(args) -> None:
         if ev is not None:
             sv.specv_set_split_event(ev[1])  # recorded between the two kernels
             ev[0].record(stream)
-        if F:  # the fused SSD round: verify + outcome keys + hit in one pass
+        if mode == "sample":
+            sv.specv_saguaro_sample(d_draft, d_temp, *saguaro, d_unif, tokens=s_tok,
+                                    q=outs["q_draft"], row_status=outs["row_status"],
+                                    workspace=ws_v)
+        elif F:  # the fused SSD round: verify + outcome keys + hit in one pass
             sv.specv_ssd_round(d_target, d_draft, d_tok, d_temp, d_unif, F, keys=keys,
                                key_logits=key_logits, hit=hit, workspace=ws_v, fanout=fanout,
-                               **outs)
+                               saguaro=saguaro, **outs)
         elif mode == "ragged":
             sv.specv_verify_ragged(d_target, d_draft, d_cu, d_tok, d_temp, d_unif, K,
                                    workspace=ws_v, **outs)
@@ -410,9 +441,11 @@ def run_ours(args) -> None:
     h_ot = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
     h_keys = torch.empty((B, K + 1, F), dtype=torch.int32).pin_memory() if F else None
     h_hit = torch.empty(B, dtype=torch.uint8).pin_memory() if F else None
+    h_st = torch.empty(lay["rows"], dtype=torch.int32).pin_memory() if mode == "sample" else None
 
     def e2e_step():
-        d_target.copy_(h_target, non_blocking=True)
+        if d_target is not None:
+            d_target.copy_(h_target, non_blocking=True)
         if d_draft is not None:
             d_draft.copy_(h_draft, non_blocking=True)
         if d_cu is not None:
@@ -421,8 +454,11 @@ def run_ours(args) -> None:
         d_temp.copy_(h_temp, non_blocking=True)
         d_unif.copy_(h_unif, non_blocking=True)
         step()
-        h_n.copy_(outs["accept_len"], non_blocking=True)
-        h_ot.copy_(outs["out_tokens"], non_blocking=True)
+        if mode == "sample":
+            h_st.copy_(s_tok, non_blocking=True)
+        else:
+            h_n.copy_(outs["accept_len"], non_blocking=True)
+            h_ot.copy_(outs["out_tokens"], non_blocking=True)
         if F:
             h_keys.copy_(keys, non_blocking=True)
             h_hit.copy_(hit, non_blocking=True)
@@ -439,7 +475,8 @@ def run_ours(args) -> None:
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
     h2d = sum(t.numel() * t.element_size()
               for t in (h_target, h_draft, h_tok, h_temp, h_unif, h_cu) if t is not None)
-    d2h = h_n.numel() * 4 + h_ot.numel() * 4 + ((h_keys.numel() * 4 + h_hit.numel()) if F else 0)
+    d2h = (h_st.numel() * 4 if mode == "sample" else
+           h_n.numel() * 4 + h_ot.numel() * 4 + ((h_keys.numel() * 4 + h_hit.numel()) if F else 0))
 
     if rank != 0:
         if world > 1:
@@ -454,7 +491,7 @@ def run_ours(args) -> None:
     achieved = kernel_bytes / (a_ms / 1e3) / 1e9
     call_gbs = kernel_bytes / (v_ms / 1e3) / 1e9
     traffic = recorded_traffic(args.workload)
-    in_bytes = d_target.numel() * d_target.element_size() + \
+    in_bytes = (d_target.numel() * d_target.element_size() if d_target is not None else 0) + \
         (d_draft.numel() * d_draft.element_size() if d_draft is not None else 0)
     line = {
         "metric": METRIC,
@@ -480,7 +517,8 @@ def run_ours(args) -> None:
         "roofline": {
             "bound": "hbm",
             "kernel": (f"stats_kernel<{'bf16' if is_bf16 else 'fp32'},"
-                       f"{'ssd' if F else 'verify'}> (reads every logit once)"),
+                       f"{'sample' if mode == 'sample' else 'ssd' if F else 'verify'}> "
+                       f"(reads every logit once)"),
             "achieved": round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
@@ -491,7 +529,8 @@ def run_ours(args) -> None:
             "algorithmic_bytes_per_launch": kernel_bytes,
             "avg_launch_ms": round(a_ms, 5),
         },
-        "call": {"api": "specv_ssd_round" if F else "specv_verify", "launches": 2,
+        "call": {"api": ("specv_saguaro_sample" if mode == "sample" else
+                         "specv_ssd_round" if F else "specv_verify"), "launches": 2,
                  "ms": round(v_ms, 5), "stats_ms": round(a_ms, 5),
                  "decide_ms": round(statistics.mean(decide_ms), 5),
                  "gbs_algorithmic": round(call_gbs, 1), "frac": round(call_gbs / peak, 4)},
@@ -502,7 +541,7 @@ def run_ours(args) -> None:
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec, mode=mode)
+        line["cpu_baseline"] = cpu_baseline(spec, mode=mode, saguaro=saguaro)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -518,20 +557,21 @@ def run_reference(args) -> None:
     oracle.build()
     spec, desc = WORKLOADS[args.workload]
     mode = LAYOUT.get(args.workload)
+    saguaro = SAGUARO.get(args.workload)
     if args.workload in GEOMETRIC:  # the oracle's cost does not depend on the split of F
         spec = dataclasses.replace(spec, F=16)
     cores = os.cpu_count() or 1
     probe = lay_out(wl.generate(spec, rows=[0]), spec, mode)
-    t_row = time_oracle(probe, spec, 1, mode)
+    t_row = time_oracle(probe, spec, 1, mode, saguaro)
     # whole run (warm-up + timed) within about a minute
     per_step = 60.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(spec.B, per_step / max(t_row, 1e-6) * min(cores, 8))))
     lay = lay_out(wl.generate(spec, rows=list(range(n))), spec, mode)
     for _ in range(args.warmup):
-        time_oracle(lay, spec, cores, mode)
+        time_oracle(lay, spec, cores, mode, saguaro)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        time_oracle(lay, spec, cores, mode)
+        time_oracle(lay, spec, cores, mode, saguaro)
     dt = (time.perf_counter() - t0) / args.steps
     value = lay["rows"] / dt
     line = {

@@ -367,9 +367,12 @@ int specv_oracle_saguaro_sample(int B, int V, int dtype, const void* z, int64_t 
                                 const float* temperature, int F, double C, const float* U,
                                 int32_t* tokens, double* q_out, int32_t* row_status) {
   if (B < 0 || V < 1 || F < 0 || !(C >= 0.0 && C <= 1.0)) return 1;
-  double* p = (double*)malloc(sizeof(double) * (size_t)V);
-  cand_t* cs = (cand_t*)malloc(sizeof(cand_t) * (size_t)V);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
   for (int b = 0; b < B; ++b) {
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    cand_t* cs = (cand_t*)malloc(sizeof(cand_t) * (size_t)V);
     const double T = (double)temperature[b];
     int am;
     double m, ls;
@@ -379,10 +382,13 @@ int specv_oracle_saguaro_sample(int B, int V, int dtype, const void* z, int64_t 
     tokens[b] = -1;
     q_out[b] = 0.0;
     row_status[b] = st;
-    if (st) continue;
-    if (T == 0.0) {
-      tokens[b] = am;
-      q_out[b] = 1.0;
+    if (st || T == 0.0) {
+      if (!st) {
+        tokens[b] = am;
+        q_out[b] = 1.0;
+      }
+      free(p);
+      free(cs);
       continue;
     }
     double cum = 0.0;
@@ -395,9 +401,9 @@ int specv_oracle_saguaro_sample(int B, int V, int dtype, const void* z, int64_t 
       row_status[b] |= ROW_FALLBACK;
     }
     q_out[b] = p[tokens[b]];
+    free(p);
+    free(cs);
   }
-  free(p);
-  free(cs);
   return 0;
 }
 
