@@ -30,7 +30,7 @@ constexpr int kMaxK = 32;
 constexpr int kTileUnroll = 8;  // tiles of r per loop trip in the residual pass
 
 struct PosStats {  // one position's combined row statistics
-  double St, Sd;
+  FF St, Sd;  // softmax normalisers, in units of 2^((z - M) c)
   float Mt, Md;
   int32_t it, id;
   int32_t bad;
@@ -41,9 +41,10 @@ struct Dec {  // a batch row's decision (the same in every CTA of its cluster)
   int32_t n, status, mode, need_scan, token, owner, last_pos, xn;
   float mt, md, ist, isd;
   float sgc, zl;  // residual weights: C on the keys at or above (zl, il)
-  int32_t il, pad2;
-  double R;       // total residual mass (the sampler normalises its q by it)
-  double tau, pre_mine;
+  int32_t il;
+  int32_t full_pass;  // the sampler's draw reads the whole row (see below)
+  FF R;          // total residual mass (the sampler normalises its q by it)
+  FF tau, pre_mine;
   float px[kMaxK], qx[kMaxK];
 };
 static_assert(sizeof(Dec) % 4 == 0, "Dec copied as words");
@@ -68,6 +69,7 @@ struct DecideParams {
   float* key_logits;
   uint8_t* hit;
   int32_t B, K, V, F, nchunk, CB, L;
+  int32_t chunk;     // logits per chunk record of the row-statistics kernel
   int32_t fk[kMaxK + 1];  // keys kept at lookahead k (F when the fan-out is uniform)
   int32_t stages;    // ring stages of the staged residual pass (aligned rows); 0: none
   int32_t ring_off;  // byte offset of that ring in dynamic shared memory
@@ -76,6 +78,7 @@ struct DecideParams {
   int32_t no_draft;  // no draft logits: q_i is one-hot at x_i
   int32_t sg_F;      // Saguaro sampling: the drafts came from sigma_{sg_F, sg_C}
   float sg_C;        //   (0: plain softmax drafts); the sampler's own F and C
+  int32_t local_draw;  // draws from a whole row read only the chunk holding U * R
 };
 
 // Combine the chunk records of one position over an aligned group of W lanes
@@ -96,8 +99,8 @@ __device__ __forceinline__ PosStats combine_position(const ChunkRec* R, int nchu
   PosStats p;
   p.Mt = warp_max_all<float, W>(mt);
   p.Md = warp_max_all<float, W>(md);
-  p.St = warp_dsum_all<W>(static_cast<double>(s_t) * static_cast<double>(ex2((mt - p.Mt) * c)));
-  p.Sd = warp_dsum_all<W>(static_cast<double>(s_d) * static_cast<double>(ex2((md - p.Md) * c)));
+  p.St = warp_ffsum_all<W>(ff_mul(s_t, ex2((mt - p.Mt) * c)));
+  p.Sd = warp_ffsum_all<W>(ff_mul(s_d, ex2((md - p.Md) * c)));
   warp_arg_all<W>(at.best, at.idx);
   warp_arg_all<W>(ad.best, ad.idx);
   p.it = at.idx;
@@ -161,6 +164,40 @@ __device__ __forceinline__ WarpTopF warp_keys(const float* cv, const int32_t* ci
   return L;
 }
 
+// The same ranking with the whole CTA (the sampler's one row): four threads
+// per candidate, each counting the candidates that beat it in a quarter of
+// the list.  ncand <= kWarpCand; the top F land in S.ov / S.oi.
+static_assert(kThreads == 4 * kWarpCand, "four threads per candidate");
+__device__ __forceinline__ void cta_rank_keys(const float* cv, const int32_t* ci, int ncand, int F,
+                                              WarpKeys& S) {
+  const int t = threadIdx.x;
+  if (t < ncand) {
+    S.v[t] = cv[t];
+    S.i[t] = ci[t];
+  }
+  if (t < F) {
+    S.ov[t] = neg_inf();
+    S.oi[t] = INT_MAX;
+  }
+  __syncthreads();
+  const int e = t >> 2, o0 = (t & 3) * (kWarpCand / 4), o1 = min(ncand, o0 + kWarpCand / 4);
+  float v = neg_inf();
+  int32_t i = INT_MAX;
+  int rank = 0;
+  if (e < ncand) {
+    v = S.v[e];
+    i = S.i[e];
+    for (int o = o0; o < o1; ++o) rank += key_beats(S.v[o], S.i[o], v, i);
+  }
+  rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+  rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+  if ((t & 3) == 0 && e < ncand && i != INT_MAX && rank < F) {
+    S.ov[rank] = v;
+    S.oi[rank] = i;
+  }
+  __syncthreads();
+}
+
 // Top-F over the per-chunk candidate lists of one draft row (warp-wide).
 __device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int32_t* ci, int ncand,
                                                      int F, int lane) {
@@ -216,7 +253,14 @@ __device__ __forceinline__ void residual_from(const float (&zt)[VW], const float
       const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
       r[k] = w.in(zt[k], e0 + k) ? __fmul_rn(p, w.C) : p;
     }
-  } else if (mode == 0) {  // q is sigma_{F,C} of the draft row when weighted
+  } else if (mode == 0 && w.zl == pos_inf()) {  // plain softmax drafts
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
+      const float q = __fmul_rn(ex2((zd[k] - md) * c), isd);
+      r[k] = fmaxf(__fsub_rn(p, q), 0.f);
+    }
+  } else if (mode == 0) {  // q is sigma_{F,C} of the draft row
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
       const float p = __fmul_rn(ex2((zt[k] - mt) * c), ist);
@@ -349,8 +393,214 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
   return ok;
 }
 
+constexpr int kDrawTiles = 8 * kVecs;  // 256-vector tiles in the longest chunk (8 trips)
+static_assert(kDrawTiles <= 32, "one lane per tile");
+
+struct DrawSmem {
+  float tile[kDrawTiles][kWarps];  // per-warp sums of r in each tile of the chunk
+  FF R;        // the row's total mass
+  FF tau_in;   // U * R less the mass before the chosen chunk
+  FF before;   // the chunk's mass before the chosen warp of the chosen tile
+  int32_t pick;    // the chunk, then the token, holding U * R
+  int32_t tsel;    // the tile holding it
+  int32_t wsel;    // the warp of that tile holding it
+  int32_t fallback;
+  float q;
+};
+
+// A draw from a whole row's own distribution, r(v) = w(v) 2^((z_v - M) c) with
+// w = C on the row's top-F_s keys (the sampler) or 1 (the bonus after all K
+// drafts are accepted), by inverse CDF of U ("Speculative Speculative
+// Decoding" §2.1; §4.2.1).  The row-statistics kernel's chunk records give
+// every chunk's mass, so the prefix over chunks finds the chunk holding U * R
+// and only that chunk is read again: its 256-vector tiles give per-warp sums,
+// a scan over tiles and then warps narrows U * R to 32 vectors, and a warp
+// scan to one.  Every sum is float-float.  All threads of one CTA call it;
+// returns the token, with S.q = r(t) / R and S.fallback set when rounding
+// left U * R past the end (the last logit with r > 0 is taken).
+template <int DT, bool VEC>
+__device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V, bool draft_fields,
+                          float M, float c, const char* row, float U, const float* kv,
+                          const int32_t* ki, int nk, const SgW& w, DrawSmem& S) {
+  using E = Elem<DT>;
+  constexpr int VW = E::VW;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  // ---- warp 0: chunk masses, lanes over contiguous blocks of chunks --------
+  if (warp == 0) {
+    const FF one_m_c = two_sum(1.f, -w.C);
+    const int per = (nchunk + 31) / 32;
+    const int j0 = min(nchunk, lane * per), j1 = min(nchunk, j0 + per);
+    auto mass = [&](int j) -> FF {
+      const ChunkRec r = recs[j];
+      const float m = draft_fields ? r.md : r.mt, sm = draft_fields ? r.sd : r.st;
+      FF x = ff_mul(sm, ex2((m - M) * c));
+      for (int k = 0; k < nk; ++k)  // the weighted keys of this chunk
+        if (ki[k] / chunk == j) x = ff_add(x, ff_neg(ff_mul(one_m_c, ex2((kv[k] - M) * c))));
+      return x.hi > 0.f ? x : ff(0.f);
+    };
+    FF mine = ff(0.f);
+    for (int j = j0; j < j1; ++j) mine = ff_add(mine, mass(j));
+    const FF incl = warp_ffscan(mine, lane);
+    const FF R = shfl(incl, 31);
+    const FF tau = ff_mul(R, U);
+    const unsigned hit = __ballot_sync(0xffffffffu, mine.hi > 0.f && ff_gt(incl, tau));
+    const unsigned pos = __ballot_sync(0xffffffffu, mine.hi > 0.f);
+    const bool last = hit == 0;  // U * R at or past the end after rounding
+    const int owner = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    if (lane == 0) {
+      S.pick = -1;
+      S.R = R;
+      S.fallback = last ? 1 : 0;
+    }
+    __syncwarp();
+    if (lane == owner) {
+      FF run = ff_add(incl, ff_neg(mine));
+      int pick = -1;
+      FF tin = ff(0.f);
+      for (int j = j0; j < j1; ++j) {
+        const FF x = mass(j);
+        if (x.hi > 0.f) {
+          const FF nx = ff_add(run, x);
+          if (!last && ff_gt(nx, tau)) {
+            pick = j;
+            tin = ff_add(tau, ff_neg(run));
+            break;
+          }
+          pick = j;  // the last chunk with mass so far
+          tin = x;
+          run = nx;
+        }
+      }
+      S.pick = pick;
+      S.tau_in = tin;
+    }
+  }
+  __syncthreads();
+  const int jc = S.pick;
+  if (jc < 0) return -1;  // no mass at all (flagged by the caller's checks)
+  // ---- every thread: vector t of each 256-vector tile of the chunk, loaded
+  // in batches of four per thread (each batch held in registers until it
+  // lands); per-warp sums of r per tile --------------------------------------
+  const int64_t e0 = static_cast<int64_t>(jc) * chunk, e1 = min(static_cast<int64_t>(V), e0 + chunk);
+  const int nvc = static_cast<int>((e1 - e0 + VW - 1) / VW);
+  const int ntile = (nvc + kThreads - 1) / kThreads;  // <= kDrawTiles (the caller checks)
+  auto rfrom = [&](const typename E::Vec& v, int j, float (&r)[VW]) {
+    float z[VW];
+    E::unpack(v, z);
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      const float p = ex2((z[k] - M) * c);
+      r[k] = w.in(z[k], e0 + static_cast<int64_t>(j) * VW + k) ? __fmul_rn(p, w.C) : p;
+    }
+  };
+  auto rvals = [&](int j, float (&r)[VW]) { rfrom(load_vec<DT, VEC>(row, e0, e1, j), j, r); };
+  constexpr int kBatch = 4;
+#pragma unroll
+  for (int h = 0; h < kDrawTiles; h += kBatch) {
+    typename E::Vec raw[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int j = (h + q) * kThreads + t;
+      if (h + q < ntile && j < nvc) raw[q] = load_vec<DT, VEC>(row, e0, e1, j);
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = h + q, j = i * kThreads + t;
+      float rsum = 0.f;
+      if (i < ntile && j < nvc) {
+        float r[VW];
+        rfrom(raw[q], j, r);
+#pragma unroll
+        for (int k = 0; k < VW; ++k) rsum += r[k];
+      }
+      const float ws = warp_sum(rsum);
+      if (lane == 0) S.tile[i][warp] = ws;
+    }
+  }
+  __syncthreads();
+  // ---- warp 0: lane i sums tile i; a scan over tiles, then a walk over the
+  // chosen tile's warps, locates the 32 vectors holding U * R -----------------
+  if (warp == 0) {
+    const FF tin = S.tau_in;
+    const bool fb = S.fallback != 0;
+    FF ti = ff(0.f);
+    if (lane < ntile)
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) ti = ff_add(ti, S.tile[lane][w2]);
+    const FF incl = warp_ffscan(ti, lane);
+    const unsigned hit = fb ? 0u : __ballot_sync(0xffffffffu, ti.hi > 0.f && ff_gt(incl, tin));
+    const unsigned pos = __ballot_sync(0xffffffffu, ti.hi > 0.f);
+    const bool last = hit == 0;
+    const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    if (lane == sel) {
+      FF run = ff_add(incl, ff_neg(ti));
+      int ws = -1;
+      FF wb = run;
+      for (int w2 = 0; w2 < kWarps; ++w2) {
+        const float g = S.tile[lane][w2];
+        if (g > 0.f) {
+          const FF nx = ff_add(run, g);
+          ws = w2;
+          wb = run;
+          if (!last && ff_gt(nx, tin)) break;
+          run = nx;
+        }
+      }
+      S.tsel = ws >= 0 ? lane : -1;
+      S.wsel = ws;
+      S.before = wb;
+      S.fallback = last ? 1 : 0;
+    }
+    if (lane == 0 && sel < 0) S.tsel = -1;
+  }
+  __syncthreads();
+  const int ts = S.tsel;
+  if (ts < 0) return -1;
+  // ---- the chosen warp: a scan of its lanes' r sums in the chosen tile, then
+  // the crossing lane walks its vector ---------------------------------------
+  if (warp == S.wsel) {
+    const int j = ts * kThreads + t;
+    float r[VW];
+#pragma unroll
+    for (int k = 0; k < VW; ++k) r[k] = 0.f;
+    if (j < nvc) rvals(j, r);
+    float vs = 0.f;
+#pragma unroll
+    for (int k = 0; k < VW; ++k) vs += r[k];
+    const FF tin = S.tau_in;
+    const bool fb = S.fallback != 0;
+    const FF incl = ff_add(S.before, warp_ffscan(ff(vs), lane));
+    const unsigned hit = fb ? 0u : __ballot_sync(0xffffffffu, vs > 0.f && ff_gt(incl, tin));
+    const unsigned pos = __ballot_sync(0xffffffffu, vs > 0.f);
+    const bool lastel = hit == 0;  // past the end, or rounding inside the tile
+    const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    if (lane == sel) {
+      FF run = ff_add(incl, -vs);
+      int kk = -1, kl = -1;
+#pragma unroll
+      for (int k = 0; k < VW; ++k)
+        if (r[k] > 0.f) {
+          run = ff_add(run, r[k]);
+          kl = k;
+          if (!lastel && kk < 0 && ff_gt(run, tin)) kk = k;
+        }
+      const int ksel = kk >= 0 ? kk : kl;  // rounding within the vector: its last r > 0
+      float rt = 0.f;
+#pragma unroll
+      for (int k = 0; k < VW; ++k)
+        if (k == ksel) rt = r[k];
+      S.pick = ksel >= 0 ? static_cast<int>(e0 + static_cast<int64_t>(j) * VW + ksel) : -1;
+      S.q = __fdiv_rn(rt, S.R.hi);
+      S.fallback = (fb || kk < 0) ? 1 : 0;
+    }
+    if (lane == 0 && sel < 0) S.pick = -1;
+  }
+  __syncthreads();
+  return S.pick;
+}
+
 template <int DT, bool VEC, int MODE>
-__global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) {
+__global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams P) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   constexpr bool kTopF = MODE == kModeSsd;      // outcome keys and hit
@@ -358,13 +608,17 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   extern __shared__ float segs[];  // [tiles * kWarps] segment sums of r
   __shared__ PosStats ps[kMaxK + 1];
   __shared__ Dec dec;
-  __shared__ double cta_total[2];  // this CTA's residual mass, per attempt
+  __shared__ FF cta_total[2];  // this CTA's residual mass, per attempt
   __shared__ int32_t tok_slot;  // rank 0: the token found by the owner CTA
   __shared__ float q_slot;      // rank 0 (sampler): sigma of that token
   __shared__ float sg_d[kMaxK + 1];    // Saguaro: weighted mass of the top-F_s,
   __shared__ float sg_zl[kMaxK + 1];   //   its F_s-th key (zl, il), and whether
   __shared__ int32_t sg_il[kMaxK + 1]; //   the sent token is among them
   __shared__ int32_t sg_xin[kMaxK + 1];
+  __shared__ float sg_kv[kMaxF];        // the sampler: its row's top-F_s keys
+  __shared__ int32_t sg_ki[kMaxF];
+  __shared__ int32_t sg_nk;
+  __shared__ DrawSmem draw;
   __shared__ int32_t copy_fail;  // rank 0: a CTA's staged copies did not land in time
   __shared__ RingBars ring_bars;
   __shared__ int32_t pre_x[kMaxK];  // draft tokens, their logits and the uniforms,
@@ -427,10 +681,21 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   const bool sg_on = (kSample || (kTopF && P.sg_F > 0)) && !greedy && temp_ok;
   if (sg_on) {
     const int nrows = kSample ? 1 : kb;
+    const int ncand = static_cast<int>(P.nchunk) * F;
+    const bool cta_rank = kSample && ncand <= kWarpCand;  // the sampler: all warps rank
+    if (cta_rank) cta_rank_keys(P.cand_v + u0 * ncand, P.cand_i + u0 * ncand, ncand, F, wkeys[0]);
     for (int i = warp; i < nrows; i += kWarps) {
       const int64_t u = u0 + i;
-      const WarpTopF Lk = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
-                                    static_cast<int>(P.nchunk) * F, F, lane, wkeys[warp]);
+      WarpTopF Lk;
+      if (cta_rank) {
+        Lk.init();
+        if (lane < F) {
+          Lk.v = wkeys[0].ov[lane];
+          Lk.i = wkeys[0].oi[lane];
+        }
+      } else {
+        Lk = warp_keys(P.cand_v + u * ncand, P.cand_i + u * ncand, ncand, F, lane, wkeys[warp]);
+      }
       const int fs = P.sg_F;
       const int x = kSample ? -1 : pre_x[i];
       const float zx = kSample ? neg_inf() : pre_zd[i];
@@ -453,6 +718,15 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         sg_il[i] = src < 0 ? x : li;
         sg_xin[i] = xin;
       }
+      if (kSample) {  // the keys themselves, for the chunk-local draw
+        const bool valid = lane < fs && Lk.i != INT_MAX;
+        if (valid) {
+          sg_kv[lane] = Lk.v;
+          sg_ki[lane] = Lk.i;
+        }
+        const unsigned vm = __ballot_sync(0xffffffffu, valid);
+        if (lane == 0) sg_nk = __popc(vm);
+      }
     }
     __syncthreads();
   }
@@ -460,13 +734,14 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
     int nf = 0;
     // Saguaro: the weighted normaliser of draft row i, sum - (1 - C) * top-F_s mass
     const float sgC = sg_on ? P.sg_C : 1.f;
-    auto sdp = [&](int i) -> double {
-      return sg_on ? ps[i].Sd - (1.0 - static_cast<double>(sgC)) * static_cast<double>(sg_d[i]) : ps[i].Sd;
+    const FF one_m_c = two_sum(1.f, -sgC);  // 1 - C, exactly
+    auto sdp = [&](int i) -> FF {
+      return sg_on ? ff_add(ps[i].Sd, ff_neg(ff_mul(one_m_c, sg_d[i]))) : ps[i].Sd;
     };
     if (kSample && temp_ok && lane == 0) {  // the sampled row sits in the draft fields
       const PosStats& q = ps[0];
       nf = greedy ? ((q.bad & 1) || q.id == INT_MAX)
-                  : (!(q.Sd >= 1.0) || q.Md == kNegMax || !(sdp(0) > 0.0));
+                  : (!(q.Sd.hi >= 1.f) || q.Md == kNegMax || !(sdp(0).hi > 0.f));
     } else if (!kSample && lane <= kb && temp_ok) {
       const PosStats& q = ps[lane];
       const bool d_full = lane < kb && !nd;  // draft rows that are normalised
@@ -474,9 +749,9 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       if (greedy) {
         nf = (q.bad & 1) || q.it == INT_MAX || (d_full && q.id == INT_MAX);
       } else {
-        nf = !(q.St >= 1.0) || q.Mt == kNegMax;
-        if (d_full) nf |= !(q.Sd >= 1.0) || q.Md == kNegMax || !(sdp(lane) > 0.0);
-        else if (d_any) nf |= q.Sd != q.Sd;  // draft row K: NaN / +inf only
+        nf = !(q.St.hi >= 1.f) || q.Mt == kNegMax;
+        if (d_full) nf |= !(q.Sd.hi >= 1.f) || q.Md == kNegMax || !(sdp(lane).hi > 0.f);
+        else if (d_any) nf |= q.Sd.hi != q.Sd.hi;  // draft row K: NaN / +inf only
       }
     }
     const bool acc_lane = lane < kb;
@@ -497,7 +772,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         accept = (x == q.it) && (nd || x == q.id);
       } else if (nd) {  // q_i(x_i) = 1: accept iff p_i(x_i) >= u
         const float lt = __fmul_rn(pre_zt[lane] - q.Mt, c);
-        px = __fdiv_rn(ex2(lt), static_cast<float>(q.St));
+        px = __fdiv_rn(ex2(lt), q.St.hi);
         qx = 1.f;
         accept = px >= pre_u[lane];
       } else {
@@ -505,7 +780,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         const float zdx = pre_zd[lane];
         const float lt = __fmul_rn(ztx - q.Mt, c);  // log2 of unnormalised p_i(x), q_i(x)
         const float ld = __fmul_rn(zdx - q.Md, c);
-        const float St = static_cast<float>(q.St), Sd = static_cast<float>(sdp(lane));
+        const float St = q.St.hi, Sd = sdp(lane).hi;
         const float wx = (sg_on && sg_xin[lane]) ? sgC : 1.f;  // Saguaro weight of x_i
         px = __fdiv_rn(ex2(lt), St);
         qx = __fdiv_rn(__fmul_rn(ex2(ld), wx), Sd);
@@ -534,21 +809,52 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       // the sampler's row statistics are the draft fields of position 0
       dec.mt = kSample ? q.Md : q.Mt;
       dec.md = q.Md;
-      dec.ist = static_cast<float>(1.0 / (kSample ? sdp(0) : q.St));
-      dec.isd = static_cast<float>(1.0 / ((n < kb) ? sdp(n) : q.Sd));
+      dec.ist = __fdiv_rn(1.f, (kSample ? sdp(0) : q.St).hi);
+      dec.isd = __fdiv_rn(1.f, ((n < kb) ? sdp(n) : q.Sd).hi);
       // Saguaro weights on the residual: the draft row n (mode 0) or the row (mode 3)
       const bool weighted = sg_on && (kSample || (n < kb && !nd));
       dec.sgc = weighted ? sgC : 1.f;
       dec.zl = weighted ? sg_zl[n] : pos_inf();
       dec.il = weighted ? sg_il[n] : -1;
-      dec.tau = 0.0;
-      dec.pre_mine = 0.0;
+      // The chunk-local draw takes the weighted mass from the chunk sums less
+      // (1 - C) x the keys' mass; when that correction is most of the row's
+      // mass the difference loses fp32 precision, and the draw reads the whole
+      // row instead (its residual total is then summed from the weighted
+      // values themselves).
+      dec.full_pass = (kSample && sg_on) ? (__fmul_rn(one_m_c.hi, sg_d[0]) > 0.5f * q.Sd.hi) : 0;
+      dec.tau = ff(0.f);
+      dec.pre_mine = ff(0.f);
       tok_slot = dec.token;
       q_slot = (ok && greedy) ? 1.f : 0.f;
       copy_fail = 0;
     }
   }
   __syncthreads();
+
+  // ---- a draw from a whole row's own distribution (the bonus after K accepted
+  // drafts, the sampler) needs only the one chunk holding U * R: rank 0 finds
+  // it from the chunk records and reads that chunk alone -----------------------
+  // (P.local_draw: the host's choice, made when a chunk is shorter than one
+  // CTA's slice of the row and holds at most kDrawTiles tiles)
+  const bool local_draw = dec.need_scan && P.local_draw && (dec.mode == 1 || (dec.mode == 3 && !dec.full_pass));
+  const bool scan = dec.need_scan && !local_draw;  // the residual pass over row n
+  if (local_draw && rank == 0) {
+    const int nn = dec.n;
+    const char* row = kSample ? static_cast<const char*>(P.zd) + L.d_off * E::ES
+                              : static_cast<const char*>(P.zt) +
+                                    (L.t_off + static_cast<int64_t>(nn) * P.t_rs) * E::ES;
+    const SgW w = kSample ? SgW{dec.sgc, dec.zl, dec.il} : SgW{1.f, pos_inf(), -1};
+    const int tok = chunk_draw<DT, VEC>(P.recs + (u0 + nn) * P.nchunk, P.nchunk, P.chunk, P.V,
+                                        kSample, dec.mt, c, row,
+                                        P.unif[L.u_off + kb], sg_kv, sg_ki,
+                                        (kSample && sg_on) ? sg_nk : 0, w, draw);
+    if (threadIdx.x == 0) {
+      tok_slot = tok;
+      q_slot = draw.q;
+      if (draw.fallback) dec.status |= kFallback;
+    }
+    __syncthreads();
+  }
 
   // ---- this CTA's slice of row n; aligned rows start streaming it now, so the
   // copies run while the keys are merged ------------------------------------
@@ -566,7 +872,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   RC.v1 = min(static_cast<int64_t>(P.V), RC.v0 + P.L);
   RC.nv = RC.v1 > RC.v0 ? static_cast<int>((RC.v1 - RC.v0 + VW - 1) / VW) : 0;
   unsigned char* ring = reinterpret_cast<unsigned char*>(segs) + P.ring_off;
-  const bool staged = VEC && dec.need_scan && P.stages > 0;
+  const bool staged = VEC && scan && P.stages > 0;
   if (staged) {
     Chunk SC = RC;
     if (dec.mode != 0) SC.rowd = nullptr;  // mode 1 reads p_n only
@@ -574,7 +880,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
     __syncthreads();
   }
 
-  if (dec.need_scan) {
+  if (scan) {
     const SgW sgw{dec.sgc, dec.zl, dec.il};
     const void* rowt = RC.rowt;
     const void* rowd = RC.rowd;
@@ -614,31 +920,26 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       }
       __syncthreads();
       if (warp == 0) {
-        double acc = 0.0;
-        for (int sg = lane; sg < ntl * kWarps; sg += 32) acc += static_cast<double>(segs[sg]);
-        acc = warp_dsum_all(acc);
+        FF acc = ff(0.f);
+        for (int sg = lane; sg < ntl * kWarps; sg += 32) acc = ff_add(acc, segs[sg]);
+        acc = warp_ffsum_all(acc);
         if (lane == 0) cta_total[attempt] = acc;
       }
       cluster_sync();  // (1) per-CTA totals visible; every CTA of the cluster has started
       if (!copies_ok && threadIdx.x == 0) *cluster.map_shared_rank(&copy_fail, 0) = 1;
       if (warp == 0) {
-        const double tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total[attempt], lane) : 0.0;
-        double incl = tr;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const double R = __shfl_sync(0xffffffffu, incl, 31);
-        const double tau = static_cast<double>(P.unif[L.u_off + kb]) * R;  // the bonus uniform
-        const unsigned own = __ballot_sync(0xffffffffu, tr > 0.0 && incl > tau);
-        const unsigned pos = __ballot_sync(0xffffffffu, tr > 0.0);
-        const double pm = __shfl_sync(0xffffffffu, incl - tr, rank);
+        const FF tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total[attempt], lane) : ff(0.f);
+        const FF incl = warp_ffscan(tr, lane);
+        const FF R = shfl(incl, 31);
+        const FF tau = ff_mul(R, P.unif[L.u_off + kb]);  // the bonus uniform
+        const unsigned own = __ballot_sync(0xffffffffu, tr.hi > 0.f && ff_gt(incl, tau));
+        const unsigned pos = __ballot_sync(0xffffffffu, tr.hi > 0.f);
+        const FF pm = shfl(ff_add(incl, ff_neg(tr)), rank);
         if (lane == 0) {
           dec.tau = tau;
           dec.pre_mine = pm;
           dec.R = R;
-          if (R > 0.0) {
+          if (R.hi > 0.f) {
             if (own) {
               dec.owner = __ffs(own) - 1;
             } else {  // U*R >= R after rounding: the last index with r > 0
@@ -661,48 +962,45 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
       // lanes own contiguous blocks of segments; a warp scan of the block sums
       // finds the block that holds the crossing, whose lane walks it
       const int nseg = ntl * kWarps;
-      const double tau = dec.tau;
+      const FF tau = dec.tau;
       const int per = (nseg + 31) / 32;
       const int s0 = min(nseg, lane * per), s1 = min(nseg, s0 + per);
-      double bsum = 0.0;
+      FF bsum = ff(0.f);
       int lastpos = -1;
       for (int sg = s0; sg < s1; ++sg) {
         const float g = segs[sg];
         if (g > 0.f) {
-          bsum += static_cast<double>(g);
+          bsum = ff_add(bsum, g);
           lastpos = sg;
         }
       }
-      double incl = bsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const double bpre = dec.pre_mine + (incl - bsum);
-      const unsigned hitm = dec.last_pos ? 0u : __ballot_sync(0xffffffffu, bsum > 0.0 && bpre + bsum > tau);
+      const FF incl = warp_ffscan(bsum, lane);
+      const FF bpre = ff_add(dec.pre_mine, ff_add(incl, ff_neg(bsum)));
+      const unsigned hitm = dec.last_pos ? 0u
+                                         : __ballot_sync(0xffffffffu, bsum.hi > 0.f && ff_gt(ff_add(bpre, bsum), tau));
       const unsigned posm = __ballot_sync(0xffffffffu, lastpos >= 0);
       int seg = -1;
-      double cum_at = 0.0;
+      FF cum_at = ff(0.f);
       if (hitm) {
         const int L = __ffs(hitm) - 1;
         if (lane == L) {
-          double cum = bpre;
+          FF cum = bpre;
           for (int sg = s0; sg < s1; ++sg) {
             const float g = segs[sg];
             if (g > 0.f) {
-              if (cum + static_cast<double>(g) > tau) {
+              const FF nx = ff_add(cum, g);
+              if (ff_gt(nx, tau)) {
                 seg = sg;
                 cum_at = cum;
                 break;
               }
-              cum += static_cast<double>(g);
+              cum = nx;
             }
           }
           if (seg < 0) seg = lastpos;  // rounding inside the block
         }
         seg = __shfl_sync(0xffffffffu, seg, L);
-        cum_at = __shfl_sync(0xffffffffu, cum_at, L);
+        cum_at = shfl(cum_at, L);
       }
       const int lastseg = posm ? __shfl_sync(0xffffffffu, lastpos, 31 - __clz(posm)) : -1;
       bool lp = dec.last_pos || seg < 0;
@@ -721,24 +1019,19 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         float vs = 0.f;
 #pragma unroll
         for (int k = 0; k < VW; ++k) vs += r[k];
-        double incl = static_cast<double>(vs);
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const double excl_sum = incl - static_cast<double>(vs);
-        const unsigned m = __ballot_sync(0xffffffffu, vs > 0.f && cum_at + incl > tau);
+        const FF incl = warp_ffscan(ff(vs), lane);
+        const FF excl_sum = ff_add(incl, -vs);
+        const unsigned m = __ballot_sync(0xffffffffu, vs > 0.f && ff_gt(ff_add(cum_at, incl), tau));
         if (m) {
           if (lane == __ffs(m) - 1) {
-            double run = cum_at + excl_sum;
+            FF run = ff_add(cum_at, excl_sum);
             int kk = -1, klast = -1;
 #pragma unroll
             for (int k = 0; k < VW; ++k) {
               if (r[k] > 0.f) {
-                run += static_cast<double>(r[k]);
+                run = ff_add(run, r[k]);
                 klast = k;
-                if (kk < 0 && run > tau) kk = k;
+                if (kk < 0 && ff_gt(run, tau)) kk = k;
               }
             }
             const int ksel = kk >= 0 ? kk : klast;
@@ -771,7 +1064,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
         *cluster.map_shared_rank(&tok_slot, 0) = tok;
         // sigma(t) = r(t) / R: the pass's own total, free of the cancellation
         // in the weighted normaliser
-        if (kSample) *cluster.map_shared_rank(&q_slot, 0) = static_cast<float>(rq / dec.R);
+        if (kSample) *cluster.map_shared_rank(&q_slot, 0) = __fdiv_rn(rq, dec.R.hi);
       }
     }
   }
@@ -795,7 +1088,7 @@ __global__ void __launch_bounds__(kThreads) decide_kernel(const DecideParams P) 
   // barrier) and every CTA's key writes (global memory) visible to rank 0; no
   // CTA exits while another may still read its shared memory.  Every CTA
   // passes here exactly once when a scan or keys ran.
-  if (dec.need_scan || kTopF) cluster_sync();
+  if (scan || kTopF) cluster_sync();
 
   // ---- outputs, written by rank 0 ---------------------------------------------
   if (rank == 0) {

@@ -416,6 +416,17 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   dp.nchunk = static_cast<int32_t>(pl.nchunk);
   dp.CB = pl.CB;
   dp.L = static_cast<int32_t>(pl.L);
+  dp.chunk = static_cast<int32_t>(pl.chunk);
+  // A draw from a whole row reads one chunk on rank 0 instead of a slice on
+  // every CTA of the cluster: worth it when the chunk is the shorter read.
+  // SPECV_LOCAL_DRAW=0/1 overrides, for tuning runs.
+  static int env_local = -2;
+  if (env_local == -2) {
+    const char* e = getenv("SPECV_LOCAL_DRAW");
+    env_local = e ? atoi(e) : -1;
+  }
+  const bool fits = pl.chunk <= static_cast<int64_t>(kDrawTiles) * kThreads * vec_width(a->dtype);
+  dp.local_draw = fits && (env_local >= 0 ? env_local != 0 : pl.chunk < pl.L);
   for (int k = 0; k <= K; ++k) dp.fk[k] = fanout ? fanout[k] : F;
   // Aligned rows stream the residual slice through a ring placed after the
   // segment sums in dynamic shared memory.

@@ -177,10 +177,92 @@ __device__ __forceinline__ T warp_max_all(T x) {
   return x;
 }
 
+// ---- float-float ("double-word") arithmetic -------------------------------
+// The sums that locate an inverse-CDF draw need more than fp32's 24 bits, and
+// this part's FP64 pipe is narrow: a dependent chain of double adds costs
+// about a hundred times a chain of fp32 adds.  A value is kept as an
+// unevaluated sum hi + lo of two floats with |lo| <= ulp(hi) / 2, built from
+// the error-free transformations TwoSum (Knuth, TAOCP vol. 2, 4.2.2),
+// FastTwoSum (Dekker 1971) and the fma-based TwoProd; the add and the
+// multiply by a float follow the "accurate" double-word algorithms of Joldes,
+// Muller and Popescu (ACM TOMS 44(2), 2017), relative error below 2^-44.
+// Explicit round-to-nearest intrinsics keep the compiler from contracting or
+// reassociating the steps.
+struct FF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ FF ff(float a) { return FF{a, 0.f}; }
+
+__device__ __forceinline__ FF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bv = __fsub_rn(s, a);
+  const float av = __fsub_rn(s, bv);
+  return FF{s, __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv))};
+}
+
+__device__ __forceinline__ FF fast_two_sum(float a, float b) {  // |a| >= |b| (or a == 0)
+  const float s = __fadd_rn(a, b);
+  return FF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ FF ff_add(FF x, FF y) {
+  const FF s = two_sum(x.hi, y.hi);
+  const FF t = two_sum(x.lo, y.lo);
+  const FF v = fast_two_sum(s.hi, __fadd_rn(s.lo, t.hi));
+  return fast_two_sum(v.hi, __fadd_rn(t.lo, v.lo));
+}
+
+__device__ __forceinline__ FF ff_add(FF x, float y) {
+  const FF s = two_sum(x.hi, y);
+  return fast_two_sum(s.hi, __fadd_rn(x.lo, s.lo));
+}
+
+__device__ __forceinline__ FF ff_neg(FF x) { return FF{-x.hi, -x.lo}; }
+
+__device__ __forceinline__ FF ff_mul(FF x, float y) {
+  const float p = __fmul_rn(x.hi, y);
+  const float e = __fmaf_rn(x.hi, y, -p);  // exact: x.hi * y = p + e
+  return fast_two_sum(p, __fmaf_rn(x.lo, y, e));
+}
+
+// the exact product of two floats
+__device__ __forceinline__ FF ff_mul(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return FF{p, __fmaf_rn(a, b, -p)};
+}
+
+// x > y for normalised pairs (|lo| <= ulp(hi) / 2)
+__device__ __forceinline__ bool ff_gt(FF x, FF y) {
+  return x.hi > y.hi || (x.hi == y.hi && x.lo > y.lo);
+}
+
+__device__ __forceinline__ FF shfl_xor(FF x, int o) {
+  return FF{__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)};
+}
+
+__device__ __forceinline__ FF shfl_up(FF x, int o) {
+  return FF{__shfl_up_sync(0xffffffffu, x.hi, o), __shfl_up_sync(0xffffffffu, x.lo, o)};
+}
+
+__device__ __forceinline__ FF shfl(FF x, int src) {
+  return FF{__shfl_sync(0xffffffffu, x.hi, src), __shfl_sync(0xffffffffu, x.lo, src)};
+}
+
 template <int W = 32>
-__device__ __forceinline__ double warp_dsum_all(double x) {
+__device__ __forceinline__ FF warp_ffsum_all(FF x) {
 #pragma unroll
-  for (int o = W / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  for (int o = W / 2; o > 0; o >>= 1) x = ff_add(x, shfl_xor(x, o));
+  return x;
+}
+
+// inclusive prefix sum over the warp's lanes (Hillis-Steele)
+__device__ __forceinline__ FF warp_ffscan(FF x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const FF y = shfl_up(x, o);
+    if (lane >= o) x = ff_add(x, y);
+  }
   return x;
 }
 
