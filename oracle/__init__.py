@@ -81,6 +81,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.specv_oracle_check_hit.argtypes = [_I, _I, _I, _P, _P, _P, _P]
     lib.specv_oracle_row_probs.restype = _I
     lib.specv_oracle_row_probs.argtypes = [_I, _I, _P, ctypes.c_double, _P]
+    lib.specv_oracle_mss.restype = _I
+    lib.specv_oracle_mss.argtypes = [_I, _I, _I, _I, _P, _L, _P, _L, _P, _P, _P, _P, _I,
+                                     _P, _P, _P, _P, _P, _I]
+    lib.specv_oracle_mss_law.restype = _I
+    lib.specv_oracle_mss_law.argtypes = [_I, _P, _P, _P, _I, _I, _P, _P]
     _LIBS[path] = lib
     return lib
 
@@ -279,3 +284,54 @@ def row_probs(z, T: float, lib=None) -> np.ndarray:
     if rc & ROW_ERRORS:
         raise ValueError(f"row status {rc}")
     return p
+
+
+def mss(target, draft, cands, temperature, uniforms, num_cands=None, naive: bool = False,
+        nthreads: int = 1, lib=None) -> dict:
+    """[CS349D] §6.4 multi-step speculative sampling (naive=False) or naive
+    sampling (naive=True) at B token-tree nodes.
+
+    target, draft [B, V] (one row each per node; fp32 or int16 bf16 bits),
+    cands int32 [B, M], num_cands int32 [B] or None (all M), temperature fp32
+    [B], uniforms fp32 [B, M+1] (u_j for candidate j, column M for the draw).
+    Returns accepted [B] (candidate index or -1), token [B], accept_prob
+    [B, M], status [B], boundary [B].
+    """
+    lib = lib or load()
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    assert target.dtype == draft.dtype and target.ndim == 2 and draft.shape == target.shape
+    B, V = target.shape
+    cands = np.ascontiguousarray(cands, dtype=np.int32).reshape(B, -1)
+    M = cands.shape[1]
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, M + 1)
+    nc = None if num_cands is None else np.ascontiguousarray(num_cands, dtype=np.int32)
+    out = dict(accepted=np.zeros(B, np.int32), token=np.zeros(B, np.int32),
+               accept_prob=np.zeros((B, M), np.float64), status=np.zeros(B, np.int32),
+               boundary=np.zeros(B, np.int32))
+    rc = lib.specv_oracle_mss(B, M, V, _dtype_code(target), _ptr(target), V, _ptr(draft), V,
+                              _ptr(cands), _ptr(nc) if nc is not None else None,
+                              _ptr(temperature), _ptr(uniforms), int(bool(naive)),
+                              _ptr(out["accepted"]), _ptr(out["token"]), _ptr(out["accept_prob"]),
+                              _ptr(out["status"]), _ptr(out["boundary"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle mss: bad sizes")
+    return out
+
+
+def mss_law(p, q, cands, naive: bool = False, lib=None):
+    """Exact law of the node's output token for one candidate tuple, given the
+    distributions p, q (fp64 [V]); returns (law [V], P(some candidate
+    accepted)).  Raises if a reachable residual has no mass."""
+    lib = lib or load()
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    x = np.ascontiguousarray(cands, dtype=np.int32)
+    law = np.zeros(p.shape[0], np.float64)
+    pa = np.zeros(1, np.float64)
+    rc = lib.specv_oracle_mss_law(p.shape[0], _ptr(p), _ptr(q), _ptr(x), x.shape[0],
+                                  int(bool(naive)), _ptr(law), _ptr(pa))
+    if rc != 0:
+        raise ValueError("oracle mss_law: a reachable residual has no mass")
+    return law, float(pa[0])

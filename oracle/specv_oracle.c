@@ -18,7 +18,9 @@
  *   [CS349D] "Lecture 5 - Speculative Decoding and SpecInfer" -- §2.1
  *          (greedy and temperature as adjusted distributions), §2.2 (the rule
  *          u <= p(x)/q(x)), §2.7 (greedy special case), §3.1 (one iteration:
- *          residual at the first rejection, or a sample from p_{gamma+1}).
+ *          residual at the first rejection, or a sample from p_{gamma+1}),
+ *          §6.4 (multi-step speculative sampling over several candidates at
+ *          one token-tree node, and naive sampling).
  *
  * Readings where the pages leave a step open (each one is listed in the
  * design notes):
@@ -547,4 +549,191 @@ void specv_oracle_check_hit(int B, int K, int F, const int32_t* keys,
     for (int f = 0; f < F; ++f)
       if (kk[f] == t) { hit[b] = 1; break; }
   }
+}
+
+/* ---------------------------------------------------------------------------
+ * a6  Multi-step speculative sampling (MSS) at one node of a token tree,
+ *     [CS349D] §6.4 (SpecInfer Theorem 4.2 / 4.3).  The node's candidates
+ *     x_1..x_m (children drawn independently from the draft distribution q of
+ *     the node) are tested in order: x_j is accepted iff q(x_j) > 0 and
+ *     p_j(x_j) / q(x_j) >= u_j, with p_1 = p (the target distribution of the
+ *     node) and, after each rejection, p_{j+1} = norm(max(0, p_j - q)).  If
+ *     all m are rejected the token is drawn from p_{m+1} by inverse CDF of
+ *     the node's last uniform.  One candidate is plain speculative sampling.
+ *     Naive sampling (NS, same section), the rule for candidates that were
+ *     not drawn from q (e.g. the top-k of q): one draw y ~ p by inverse CDF of
+ *     the last uniform, a candidate is accepted iff it equals y.
+ *
+ * Readings (listed in the design notes):
+ *   - T = 0 (greedy): the first candidate equal to argmax p is accepted, else
+ *     the token is argmax p ([CS349D] §6.4, greedy verification follows the
+ *     target's argmax); NS gives the same result.
+ *   - a residual with no mass (p_j <= q everywhere, reachable only through
+ *     rounding or q(x_j) = 0) ends the testing: the token is drawn from p and
+ *     ROW_FALLBACK is set, as for the single-draft bonus.
+ *   - accept_prob[j] = min(1, p_j(x_j)/q(x_j)) for every tested candidate
+ *     (0 when q(x_j) = 0), 0 for the untested ones and under NS.
+ */
+
+/* Inverse-CDF draw from the unnormalised r[0..V-1] with uniform U: the
+ * smallest v whose running sum exceeds U*sum(r); the last v with r > 0 when
+ * rounding leaves none (sets *fb).  *bd is set when U*sum(r) lies within
+ * BOUNDARY_EPS*sum(r) of a running sum next to the chosen v. */
+static int icdf_draw(const double* r, int V, double U, int* fb, int* bd) {
+  double R = 0.0;
+  for (int v = 0; v < V; ++v) R += r[v];
+  double tau = U * R, cum = 0.0, prev = 0.0;
+  for (int v = 0; v < V; ++v) {
+    prev = cum;
+    cum += r[v];
+    if (cum > tau) {
+      if (fabs(tau - prev) < BOUNDARY_EPS * R || fabs(cum - tau) < BOUNDARY_EPS * R) *bd = 1;
+      return v;
+    }
+  }
+  *fb = 1;
+  *bd = 1;
+  for (int v = V - 1; v >= 0; --v) if (r[v] > 0.0) return v;
+  return -1;
+}
+
+/* One node from its distributions p, q (T > 0).  Scratch pj[V], r[V]. */
+static void mss_node(int V, const double* p, const double* q, const int32_t* x, int m,
+                     const float* U, int M, int naive, int32_t* acc_out, int32_t* tok_out,
+                     double* aprob, int* status, int* boundary, double* pj, double* r) {
+  int fb = 0;
+  *acc_out = -1;
+  for (int j = 0; j < M; ++j) aprob[j] = 0.0;
+  if (naive) {
+    *tok_out = icdf_draw(p, V, (double)U[M], &fb, boundary);
+    for (int j = 0; j < m; ++j)
+      if (x[j] == *tok_out) { *acc_out = j; break; }
+    if (fb) *status |= ROW_FALLBACK;
+    return;
+  }
+  memcpy(pj, p, sizeof(double) * (size_t)V);
+  for (int j = 0; j < m; ++j) {
+    const double qx = q[x[j]];
+    const double ratio = qx > 0.0 ? pj[x[j]] / qx : 0.0;
+    aprob[j] = ratio < 1.0 ? ratio : 1.0;
+    if (qx > 0.0 && fabs((double)U[j] - ratio) < BOUNDARY_EPS) *boundary = 1;
+    if (qx > 0.0 && ratio >= (double)U[j]) {
+      *acc_out = j;
+      *tok_out = x[j];
+      return;
+    }
+    /* rejected: p_{j+1} = norm(max(0, p_j - q)) */
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) { r[v] = pj[v] > q[v] ? pj[v] - q[v] : 0.0; Z += r[v]; }
+    if (!(Z > 0.0)) {  /* no residual mass: draw from p itself */
+      *status |= ROW_FALLBACK;
+      *tok_out = icdf_draw(p, V, (double)U[M], &fb, boundary);
+      if (fb) *status |= ROW_FALLBACK;
+      return;
+    }
+    for (int v = 0; v < V; ++v) pj[v] = r[v] / Z;
+  }
+  *tok_out = icdf_draw(pj, V, (double)U[M], &fb, boundary);
+  if (fb) *status |= ROW_FALLBACK;
+}
+
+/* Exported: MSS (naive = 0) or NS (naive = 1) at B nodes.  Layouts:
+ *   target[b*t_rs + v], draft[b*d_rs + v]      one row each per node
+ *   cands[b*M + j], j < m_b = num_cands ? num_cands[b] : M (0 <= m_b <= M)
+ *   uniforms[b*(M+1) + j]: u_j for candidate j < M, u_M for the draw
+ * Outputs: accepted[B] (candidate index or -1), token[B], accept_prob[B*M],
+ * row_status[B] (ROW_BAD_TOKEN also for a count outside [0, M]), boundary[B]. */
+int specv_oracle_mss(int B, int M, int V, int dtype, const void* target, int64_t t_rs,
+                     const void* draft, int64_t d_rs, const int32_t* cands,
+                     const int32_t* num_cands, const float* temperature, const float* uniforms,
+                     int naive, int32_t* accepted, int32_t* token, double* accept_prob,
+                     int32_t* row_status, int32_t* boundary, int nthreads) {
+  if (B < 0 || M < 0 || M > 32 || V < 1) return 1;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int b = 0; b < B; ++b) {
+    const int32_t* x = cands + (int64_t)b * M;
+    const float* U = uniforms + (int64_t)b * (M + 1);
+    const double T = (double)temperature[b];
+    const int m = num_cands ? num_cands[b] : M;
+    int st = 0, bd = 0;
+    accepted[b] = -1;
+    token[b] = -1;
+    for (int j = 0; j < M; ++j) accept_prob[(int64_t)b * M + j] = 0.0;
+    if (!(T >= 0.0) || isinf(T)) st |= ROW_BAD_TEMP;
+    if (m < 0 || m > M) st |= ROW_BAD_TOKEN;
+    else
+      for (int j = 0; j < m; ++j)
+        if (x[j] < 0 || x[j] >= V) st |= ROW_BAD_TOKEN;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V * 4);
+    double *q = p + V, *pj = p + 2 * (size_t)V, *r = p + 3 * (size_t)V;
+    int amt = -1, amd = -1;
+    double mt, lst, md, lsd;
+    if (!st) st |= row_distribution(target, dtype, (int64_t)b * t_rs, V, T, p, &amt, &mt, &lst);
+    if (!st) st |= row_distribution(draft, dtype, (int64_t)b * d_rs, V, T, q, &amd, &md, &lsd);
+    if (!st) {
+      if (T == 0.0) {
+        token[b] = amt;
+        for (int j = 0; j < m; ++j) {
+          if (!naive) accept_prob[(int64_t)b * M + j] = (x[j] == amt) ? 1.0 : 0.0;
+          if (x[j] == amt) { accepted[b] = j; break; }
+        }
+      } else {
+        mss_node(V, p, q, x, m, U, M, naive, accepted + b, token + b,
+                 accept_prob + (int64_t)b * M, &st, &bd, pj, r);
+      }
+    }
+    row_status[b] = st;
+    boundary[b] = bd;
+    free(p);
+  }
+  (void)nthreads;
+  return 0;
+}
+
+/* Exported, for the pins: the exact law of the node's output token given one
+ * candidate tuple x[0..m-1] and the distributions p, q (not logits):
+ *   law[y] = sum_j (prod_{i<j} (1 - a_i)) a_j [y = x_j] + prod_j (1 - a_j) p_{m+1}(y)
+ * with a_j = min(1, p_j(x_j)/q(x_j)) (0 if q(x_j) = 0) for MSS, and
+ * law = p for NS.  Also the probability that some candidate is accepted.
+ * Returns 1 if a residual has no mass (the law is then undefined). */
+int specv_oracle_mss_law(int V, const double* p, const double* q, const int32_t* x, int m,
+                         int naive, double* law, double* p_accept) {
+  if (naive) {
+    double pa = 0.0;
+    for (int v = 0; v < V; ++v) {
+      law[v] = p[v];
+      int in = 0;
+      for (int j = 0; j < m; ++j) in |= (x[j] == v);
+      if (in) pa += p[v];
+    }
+    *p_accept = pa;
+    return 0;
+  }
+  double* pj = (double*)malloc(sizeof(double) * (size_t)V * 2);
+  double* r = pj + V;
+  memcpy(pj, p, sizeof(double) * (size_t)V);
+  for (int v = 0; v < V; ++v) law[v] = 0.0;
+  double reach = 1.0; /* probability that candidates 1..j-1 were all rejected */
+  for (int j = 0; j < m; ++j) {
+    const double qx = q[x[j]];
+    double a = qx > 0.0 ? pj[x[j]] / qx : 0.0;
+    if (a > 1.0) a = 1.0;
+    law[x[j]] += reach * a;
+    reach *= 1.0 - a;
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) { r[v] = pj[v] > q[v] ? pj[v] - q[v] : 0.0; Z += r[v]; }
+    if (!(Z > 0.0)) {
+      free(pj);
+      *p_accept = 1.0 - reach;
+      return reach > 0.0 ? 1 : 0;  /* unreachable residual: harmless */
+    }
+    for (int v = 0; v < V; ++v) pj[v] = r[v] / Z;
+  }
+  for (int v = 0; v < V; ++v) law[v] += reach * pj[v];
+  *p_accept = 1.0 - reach;
+  free(pj);
+  return 0;
 }

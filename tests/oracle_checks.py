@@ -764,6 +764,193 @@ def check_saguaro_sampler_inverse_cdf(lib):
         assert out["tokens"][b] == min(t, V - 1) and abs(out["q"][b] - q[out["tokens"][b]]) < 1e-15
 
 
+# ---------------------------------------------------------------------------
+# Multi-step speculative sampling at a token-tree node ([CS349D] §6.4)
+
+def mss_pieces(P, Q, m: int):
+    """Leaves of MSS with m candidates drawn i.i.d. from Q, in exact rationals.
+
+    Each leaf is (probability, candidates, uniforms, token): the candidates
+    occur with probability prod Q(x_j); u_j in [0, a_j) accepts x_j, with
+    a_j = min(1, P_j(x_j)/Q(x_j)) and P_{j+1} = norm(max(0, P_j - Q)); when
+    all m are rejected, u_m picks the token of P_{m+1} by its CDF.  The
+    uniforms are interval midpoints, so a correct MSS takes the leaf's token.
+    """
+    import itertools
+    V = len(P)
+    half = Fr(1, 2)
+    leaves = []
+    for x in itertools.product(range(V), repeat=m):
+        w = Fr(1)
+        for xi in x:
+            w *= Q[xi]
+        if w == 0:
+            continue
+        pj = list(P)
+        reach = Fr(1)
+        pre = []
+        for j in range(m):
+            a = min(Fr(1), pj[x[j]] / Q[x[j]])
+            if a > 0:
+                leaves.append((w * reach * a, x, pre + [a / 2] + [half] * (m - j), x[j]))
+            if a == 1:
+                reach = Fr(0)
+                break
+            pre.append((a + 1) / 2)
+            reach *= 1 - a
+            r = [max(Fr(0), pj[v] - Q[v]) for v in range(V)]
+            Z = sum(r)
+            pj = [rv / Z for rv in r]
+        if reach > 0:
+            cum = Fr(0)
+            for y in range(V):
+                if pj[y] > 0:
+                    leaves.append((w * reach * pj[y], x, pre + [cum + pj[y] / 2], y))
+                cum += pj[y]
+    return leaves
+
+
+def check_mss_exact_enumeration(lib, seed: int = 11, V: int = 5, pairs: int = 3):
+    """Theorem 4.2: over candidates drawn i.i.d. from q, the MSS output law is
+    exactly p.  The oracle, run on every leaf of the exact enumeration, takes
+    each leaf's token, and the leaves' law is P in exact rationals (m = 1..3)."""
+    rng = np.random.default_rng(seed)
+    for _ in range(pairs):
+        P = rational_rows(rng, 1, V)[0]
+        Q = rational_rows(rng, 1, V)[0]
+        for m in (1, 2, 3):
+            leaves = mss_pieces(P, Q, m)
+            law = [Fr(0)] * V
+            for w, _, _, y in leaves:
+                law[y] += w
+            assert law == P, m
+            B = len(leaves)
+            zt, zq = logits_for([P])[0], logits_for([Q])[0]
+            out = oracle.mss(np.broadcast_to(zt, (B, V)), np.broadcast_to(zq, (B, V)),
+                             np.array([lf[1] for lf in leaves], np.int32),
+                             np.ones(B, np.float32),
+                             np.array([[float(u) for u in lf[2]] for lf in leaves], np.float32),
+                             nthreads=0, lib=lib)
+            assert not (out["status"] & oracle.ROW_ERRORS).any()
+            got = out["token"]
+            want = np.array([lf[3] for lf in leaves])
+            assert np.array_equal(got, want), (m, np.nonzero(got != want)[0][:5])
+            acc = out["accepted"]
+            for i, (w, x, us, y) in enumerate(leaves):
+                assert acc[i] == -1 or x[acc[i]] == y
+
+
+def _dirichlet_pairs(seed: int, n: int, V: int = 5):
+    rng = np.random.default_rng(seed)
+    return [(rng.dirichlet(np.ones(V)), rng.dirichlet(np.ones(V))) for _ in range(n)]
+
+
+def check_mss_law_thm42_thm43(lib):
+    """The exact-law routine: sum over candidate tuples weighted by prod q is p
+    (Theorem 4.2), and MSS accepts at least as often as naive sampling
+    (Theorem 4.3), on 200 random pairs over V = 5 with m = 1..3."""
+    import itertools
+    V = 5
+    for p, q in _dirichlet_pairs(5, 200, V):
+        for m in (1, 2, 3):
+            tot = np.zeros(V)
+            pm = pn = 0.0
+            for x in itertools.product(range(V), repeat=m):
+                w = float(np.prod(q[list(x)]))
+                law, pa = oracle.mss_law(p, q, np.array(x), lib=lib)
+                _, pan = oracle.mss_law(p, q, np.array(x), naive=True, lib=lib)
+                tot += w * law
+                pm += w * pa
+                pn += w * pan
+            assert np.abs(tot - p).max() < 1e-12, m
+            assert pm >= pn - 1e-12, (m, pm, pn)
+
+
+def check_mss_topk_misuse(lib):
+    """[CS349D] §6.4: candidates taken deterministically as the top-k of q with
+    the same ratio rule do not give p (mean TV 0.24-0.34 on the pages' pairs,
+    whose family is not stated; Dirichlet(1) pairs over V = 5 give about 0.30,
+    0.36, 0.40 for k = 1, 2, 3), while naive sampling with the same candidates
+    gives p exactly."""
+    for k in (1, 2, 3):
+        tv = []
+        for p, q in _dirichlet_pairs(6, 300):
+            x = np.argsort(-q, kind="stable")[:k]
+            law, _ = oracle.mss_law(p, q, x, lib=lib)
+            tv.append(0.5 * np.abs(law - p).sum())
+            lawn, pan = oracle.mss_law(p, q, x, naive=True, lib=lib)
+            assert np.abs(lawn - p).max() < 1e-15 and abs(pan - p[x].sum()) < 1e-15
+        assert 0.2 < float(np.mean(tv)) < 0.5, (k, np.mean(tv))
+
+
+def check_mss_single_candidate_is_sd(lib):
+    """One candidate is plain speculative sampling: the same accept decision
+    and token as verification with K = 1 after a rejection."""
+    rng = np.random.default_rng(12)
+    B, V = 400, 37
+    zt = rng.normal(0, 2, (B, V)).astype(np.float32)
+    zq = (zt + rng.normal(0, 1, (B, V))).astype(np.float32)
+    T = rng.choice([0.7, 1.0, 1.3], B).astype(np.float32)
+    x = rng.integers(0, V, (B, 1)).astype(np.int32)
+    U = rng.uniform(0, 1, (B, 2)).astype(np.float32)
+    o = oracle.mss(zt, zq, x, T, U, lib=lib)
+    tgt = np.stack([zt, zt], axis=1)  # K + 1 = 2 target rows (row 1 unused on rejection)
+    v = oracle.verify(tgt, zq[:, None, :], x, T, U, lib=lib)
+    assert np.array_equal(o["accepted"] == 0, v["accept_len"] == 1)
+    rej = v["accept_len"] == 0
+    assert np.array_equal(o["token"][rej], v["out_tokens"][rej, 0])
+    assert np.array_equal(o["token"][~rej], x[~rej, 0])
+    assert np.allclose(o["accept_prob"][:, 0], np.minimum(1.0, v["p"][:, 0] / v["q"][:, 0]))
+
+
+def check_mss_naive_and_greedy(lib):
+    """Naive sampling: the token is the inverse-CDF draw from p (numpy
+    searchsorted on the library softmax) and a candidate is accepted iff it is
+    that token.  T = 0: the first candidate equal to argmax p, else argmax p."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(13)
+    B, V, M = 300, 29, 3
+    zt = rng.normal(0, 2, (B, V)).astype(np.float32)
+    zq = (zt + rng.normal(0, 1, (B, V))).astype(np.float32)
+    T = rng.choice([0.0, 0.8, 1.0], B).astype(np.float32)
+    x = rng.integers(0, V, (B, M)).astype(np.int32)
+    x[::4, 1] = np.argmax(zt[::4], axis=1)  # some nodes hold the argmax
+    U = rng.uniform(0, 1, (B, M + 1)).astype(np.float32)
+    for naive in (False, True):
+        o = oracle.mss(zt, zq, x, T, U, naive=naive, lib=lib)
+        for b in range(B):
+            if T[b] == 0:
+                am = int(np.argmax(zt[b]))
+                hits = np.nonzero(x[b] == am)[0]
+                assert o["token"][b] == am and o["accepted"][b] == (hits[0] if len(hits) else -1)
+            elif naive:
+                p = softmax(zt[b].astype(np.float64) / T[b])
+                y = min(int(np.searchsorted(np.cumsum(p), float(U[b, M]), side="right")), V - 1)
+                assert o["token"][b] == y
+                hits = np.nonzero(x[b] == y)[0]
+                assert o["accepted"][b] == (hits[0] if len(hits) else -1)
+                assert (o["accept_prob"][b] == 0).all()
+
+
+def check_mss_bad_inputs(lib):
+    """Out-of-range candidates, counts outside [0, M] and bad temperatures flag
+    the node and produce no token."""
+    V, M = 7, 2
+    z = np.zeros((4, V), np.float32)
+    x = np.array([[1, 2], [1, 9], [1, 2], [1, 2]], np.int32)
+    T = np.array([1.0, 1.0, -1.0, 1.0], np.float32)
+    nc = np.array([2, 2, 2, 3], np.int32)
+    o = oracle.mss(z, z, x, T, np.full((4, M + 1), 0.5, np.float32), num_cands=nc, lib=lib)
+    assert o["status"][0] == 0 and o["token"][0] >= 0
+    assert o["status"][1] & oracle.ROW_BAD_TOKEN and o["token"][1] == -1
+    assert o["status"][2] & oracle.ROW_BAD_TEMP and o["token"][2] == -1
+    assert o["status"][3] & oracle.ROW_BAD_TOKEN and o["token"][3] == -1
+    # a node with no candidates draws from p (naive and MSS alike)
+    o0 = oracle.mss(z[:1], z[:1], x[:1], T[:1], np.full((1, M + 1), 0.5, np.float32),
+                    num_cands=np.array([0], np.int32), lib=lib)
+    assert o0["accepted"][0] == -1 and o0["token"][0] == 3  # uniform p on 7: U = .5 -> v = 3
+
+
 ALL_CHECKS = {
     "softmax_library": check_softmax_library,
     "thm1_overlap": check_thm1_overlap,
@@ -792,4 +979,10 @@ ALL_CHECKS = {
     "saguaro_thm15": check_saguaro_thm15_monotone,
     "saguaro_exact_law": check_saguaro_exact_law,
     "saguaro_sampler": check_saguaro_sampler_inverse_cdf,
+    "mss_exact_enumeration": check_mss_exact_enumeration,
+    "mss_law_thm42_thm43": check_mss_law_thm42_thm43,
+    "mss_topk_misuse": check_mss_topk_misuse,
+    "mss_single_candidate": check_mss_single_candidate_is_sd,
+    "mss_naive_and_greedy": check_mss_naive_and_greedy,
+    "mss_bad_inputs": check_mss_bad_inputs,
 }

@@ -106,6 +106,36 @@ MUTATIONS = {
         ": sg_F > 0 ? log(qd[(int64_t)i * V + x[i]])",
         ": sg_F > 0 ? log_prob(draft, dtype, dof, x[i], T, md[i], lsd[i])",
         ["saguaro_exact_law"]),
+    # MSS: the target left at p after a rejection (no residual step)
+    "mss_no_residual_update": (
+        "    for (int v = 0; v < V; ++v) pj[v] = r[v] / Z;\n  }\n  *tok_out = icdf_draw(pj",
+        "    (void)Z;\n  }\n  *tok_out = icdf_draw(pj",
+        ["mss_exact_enumeration"]),
+    # MSS: every candidate tested against p instead of the current residual
+    "mss_ratio_from_p": (
+        "const double ratio = qx > 0.0 ? pj[x[j]] / qx : 0.0;",
+        "const double ratio = qx > 0.0 ? p[x[j]] / qx : 0.0;",
+        ["mss_exact_enumeration"]),
+    # MSS: all candidates rejected, but the token drawn from p
+    "mss_final_draw_from_p": (
+        "*tok_out = icdf_draw(pj, V, (double)U[M], &fb, boundary);",
+        "*tok_out = icdf_draw(p, V, (double)U[M], &fb, boundary);",
+        ["mss_exact_enumeration"]),
+    # MSS: candidate j tested with the draw's uniform
+    "mss_accept_uses_draw_uniform": (
+        "if (qx > 0.0 && ratio >= (double)U[j]) {",
+        "if (qx > 0.0 && ratio >= (double)U[M]) {",
+        ["mss_exact_enumeration"]),
+    # the exact-law routine without the residual step
+    "mss_law_no_residual": (
+        "    for (int v = 0; v < V; ++v) pj[v] = r[v] / Z;\n  }\n  for (int v = 0; v < V; ++v) law[v] += reach * pj[v];",
+        "    (void)Z;\n  }\n  for (int v = 0; v < V; ++v) law[v] += reach * pj[v];",
+        ["mss_law_thm42_thm43"]),
+    # naive sampling drawing from q
+    "mss_naive_draws_from_q": (
+        "*tok_out = icdf_draw(p, V, (double)U[M], &fb, boundary);\n    for (int j = 0; j < m; ++j)",
+        "*tok_out = icdf_draw(q, V, (double)U[M], &fb, boundary);\n    for (int j = 0; j < m; ++j)",
+        ["mss_naive_and_greedy"]),
     "hit_wrong_length": (
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
