@@ -58,7 +58,8 @@ enum {
   ROW_BAD_TOKEN = 1,  /* a draft token outside [0, V) */
   ROW_NONFINITE = 2,  /* NaN or +inf logit, or a row with no finite logit */
   ROW_BAD_TEMP = 4,   /* temperature < 0, NaN or inf */
-  ROW_FALLBACK = 8    /* bonus draw used a fallback (informational) */
+  ROW_FALLBACK = 8,   /* bonus draw used a fallback (informational) */
+  ROW_BAD_COUNT = 32  /* a per-row draft or candidate count out of range */
 };
 
 /* Margin inside which an executed accept test or the bonus draw counts as a
@@ -342,7 +343,7 @@ int specv_oracle_verify_ragged(int B, int Kmax, int V, int dtype, const void* ta
     for (int i = 0; i <= Kmax; ++i) ot[i] = -1;
     if (kb < 0 || kb > Kmax) {
       accept_len[b] = 0;
-      row_status[b] = 32;
+      row_status[b] = ROW_BAD_COUNT;
       boundary[b] = 0;
       continue;
     }
@@ -642,7 +643,7 @@ static void mss_node(int V, const double* p, const double* q, const int32_t* x, 
  *   cands[b*M + j], j < m_b = num_cands ? num_cands[b] : M (0 <= m_b <= M)
  *   uniforms[b*(M+1) + j]: u_j for candidate j < M, u_M for the draw
  * Outputs: accepted[B] (candidate index or -1), token[B], accept_prob[B*M],
- * row_status[B] (ROW_BAD_TOKEN also for a count outside [0, M]), boundary[B]. */
+ * row_status[B] (ROW_BAD_COUNT for a count outside [0, M]), boundary[B]. */
 int specv_oracle_mss(int B, int M, int V, int dtype, const void* target, int64_t t_rs,
                      const void* draft, int64_t d_rs, const int32_t* cands,
                      const int32_t* num_cands, const float* temperature, const float* uniforms,
@@ -663,7 +664,7 @@ int specv_oracle_mss(int B, int M, int V, int dtype, const void* target, int64_t
     token[b] = -1;
     for (int j = 0; j < M; ++j) accept_prob[(int64_t)b * M + j] = 0.0;
     if (!(T >= 0.0) || isinf(T)) st |= ROW_BAD_TEMP;
-    if (m < 0 || m > M) st |= ROW_BAD_TOKEN;
+    if (m < 0 || m > M) st |= ROW_BAD_COUNT;
     else
       for (int j = 0; j < m; ++j)
         if (x[j] < 0 || x[j] >= V) st |= ROW_BAD_TOKEN;

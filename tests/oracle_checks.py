@@ -933,8 +933,8 @@ def check_mss_naive_and_greedy(lib):
 
 
 def check_mss_bad_inputs(lib):
-    """Out-of-range candidates, counts outside [0, M] and bad temperatures flag
-    the node and produce no token."""
+    """Out-of-range candidates (ROW_BAD_TOKEN), counts outside [0, M]
+    (ROW_BAD_COUNT) and bad temperatures flag the node and produce no token."""
     V, M = 7, 2
     z = np.zeros((4, V), np.float32)
     x = np.array([[1, 2], [1, 9], [1, 2], [1, 2]], np.int32)
@@ -944,7 +944,7 @@ def check_mss_bad_inputs(lib):
     assert o["status"][0] == 0 and o["token"][0] >= 0
     assert o["status"][1] & oracle.ROW_BAD_TOKEN and o["token"][1] == -1
     assert o["status"][2] & oracle.ROW_BAD_TEMP and o["token"][2] == -1
-    assert o["status"][3] & oracle.ROW_BAD_TOKEN and o["token"][3] == -1
+    assert o["status"][3] & oracle.ROW_BAD_COUNT and o["token"][3] == -1
     # a node with no candidates draws from p (naive and MSS alike)
     o0 = oracle.mss(z[:1], z[:1], x[:1], T[:1], np.full((1, M + 1), 0.5, np.float32),
                     num_cands=np.array([0], np.int32), lib=lib)
