@@ -61,6 +61,9 @@ WORKLOADS = {
                     "by cu_num_draft_tokens, verify only"),
     "cfg5-nodraft": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-nodraft"),
                      "config 5 without draft logits (SPECV_NO_DRAFT_PROBS), verify only"),
+    "cfg5-mss": (dataclasses.replace(wl.SPECS["cfg5"], name="cfg5-mss", B=2048),
+                 "multi-step speculative sampling (MSS) at 2048 token-tree nodes, 3 candidate "
+                 "children each drawn from q, config 5 logits (V=152064 fp32)"),
     "cfg5": (wl.SPECS["cfg5"], "config 5 (B=256, K=8, V=152064, fp32 Zipf-like logits), verify only"),
     "cfg4": (wl.SPECS["cfg4"], "config 4 (B=32, K=4, V=128256, bf16, F=6): verify + predict + hit"),
     "cfg3": (wl.SPECS["cfg3"], "config 3 (B=64, K=4, V=128256, bf16, T in {0,0.6,1}), verify only"),
@@ -71,7 +74,11 @@ WORKLOADS = {
 
 # Workloads in another layout: rows packed by per-row draft counts, or
 # verification without draft logits.
-LAYOUT = {"cfg5-ragged": "ragged", "cfg5-nodraft": "nodraft", "cfg5-sample": "sample"}
+LAYOUT = {"cfg5-ragged": "ragged", "cfg5-nodraft": "nodraft", "cfg5-sample": "sample",
+          "cfg5-mss": "mss"}
+
+# Candidates per token-tree node of the MSS workloads.
+MSS_M = {"cfg5-mss": 3}
 
 # Saguaro sampling (F_s, C) of the drafts (SSD rounds) or of the sampler.
 SAGUARO = {"cfg5-ssd-saguaro": (6, 0.3), "cfg5-sample": (6, 0.3)}
@@ -236,9 +243,21 @@ def draft_counts(first_row: int, n: int, K: int) -> np.ndarray:
                      for b in range(first_row, first_row + n)], np.int64)
 
 
+def gen_data(spec, rows, mode, workload: str) -> dict:
+    """Seeded inputs of the given batch rows (token-tree nodes for MSS)."""
+    if mode == "mss":
+        return wl.generate_mss(spec, MSS_M[workload], rows=rows)
+    return wl.generate(spec, rows=rows)
+
+
 def lay_out(data, spec, mode, first_row: int = 0) -> dict:
     """The call's inputs in the workload's layout, with its target rows (the
     metric's rows) and its algorithmic bytes (every row it must normalise)."""
+    if mode == "mss":  # one target and one draft row per node; a node is a metric row
+        n, s = data["target"].shape[0], spec.elem_bytes
+        return dict(target=data["target"], draft=data["draft"], tokens=data["candidates"],
+                    temperature=data["temperature"], uniforms=data["uniforms"], cu=None,
+                    rows=n, bytes=2 * n * spec.V * s)
     B, K, V, s = data["tokens"].shape[0], spec.K, spec.V, spec.elem_bytes
     lay = dict(target=data["target"], draft=data["draft"], tokens=data["tokens"],
                temperature=data["temperature"], uniforms=data["uniforms"], cu=None)
@@ -270,6 +289,10 @@ def lay_out(data, spec, mode, first_row: int = 0) -> dict:
 def time_oracle(lay, spec, nthreads: int, mode=None, saguaro=None) -> float:
     import oracle
     t0 = time.perf_counter()
+    if mode == "mss":
+        oracle.mss(lay["target"], lay["draft"], lay["tokens"], lay["temperature"], lay["uniforms"],
+                   nthreads=nthreads)
+        return time.perf_counter() - t0
     if mode == "sample":
         oracle.saguaro_sample(lay["draft"], lay["temperature"], *saguaro, lay["uniforms"])
         return time.perf_counter() - t0
@@ -286,23 +309,24 @@ def time_oracle(lay, spec, nthreads: int, mode=None, saguaro=None) -> float:
     return time.perf_counter() - t0
 
 
-def cpu_baseline(spec, budget_s: float = 12.0, mode=None, saguaro=None) -> dict:
+def cpu_baseline(spec, budget_s: float = 12.0, mode=None, saguaro=None, workload: str = "") -> dict:
     """The oracle on a bounded sample of the workload, on this host's cores."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
     rows = list(range(min(spec.B, max(1, cores))))
-    lay = lay_out(wl.generate(spec, rows=rows), spec, mode)
+    lay = lay_out(gen_data(spec, rows, mode, workload), spec, mode)
     t = time_oracle(lay, spec, cores, mode, saguaro)
     per_row = t / len(rows)
     n = int(min(spec.B, max(len(rows), budget_s / max(per_row, 1e-6))))
     if n > len(rows):
-        lay = lay_out(wl.generate(spec, rows=list(range(n))), spec, mode)
+        lay = lay_out(gen_data(spec, list(range(n)), mode, workload), spec, mode)
         t = time_oracle(lay, spec, cores, mode, saguaro)
     value = lay["rows"] / t
     return {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {spec.B} batch rows of {spec.name} "
-                      f"({'verify+predict+hit' if spec.F else 'verify'}), fp64 C, OpenMP over rows, "
+                      f"({'MSS' if mode == 'mss' else 'verify+predict+hit' if spec.F else 'verify'}), "
+                      f"fp64 C, OpenMP over rows, "
                       f"{t:.1f} s"}
 
 
@@ -335,7 +359,7 @@ def run_ours(args) -> None:
         desc += f" [F_k = {fanout}]"
     mode = LAYOUT.get(args.workload)
     saguaro = SAGUARO.get(args.workload)
-    data = wl.generate(spec, rows=shard_rows(rank, world, spec.B))
+    data = gen_data(spec, shard_rows(rank, world, spec.B), mode, args.workload)
     lay = lay_out(data, spec, mode, first_row=rank * spec.B)
     B, K, V, F = spec.B, spec.K, spec.V, spec.F
     is_bf16 = spec.dtype == wl.BF16
@@ -370,6 +394,13 @@ def run_ours(args) -> None:
         ws_v = torch.empty(max(1, lib.specv_saguaro_workspace_bytes(lay["rows"], V, saguaro[0], code)),
                            dtype=torch.uint8, device=dev)
         s_tok = torch.empty(lay["rows"], **i32)
+    if mode == "mss":
+        Mc = MSS_M[args.workload]
+        outs = dict(accepted=torch.empty(B, **i32), out_token=torch.empty(B, **i32),
+                    accept_prob=torch.empty((B, Mc), dtype=torch.float32, device=dev),
+                    row_status=torch.empty(B, **i32))
+        ws_v = torch.empty(max(1, lib.specv_mss_workspace_bytes(B, Mc, V, code)),
+                           dtype=torch.uint8, device=dev)
     if F:
         keys = torch.empty((B, K + 1, F), **i32)
         key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
@@ -386,6 +417,8 @@ def run_ours(args) -> None:
             sv.specv_saguaro_sample(d_draft, d_temp, *saguaro, d_unif, tokens=s_tok,
                                     q=outs["q_draft"], row_status=outs["row_status"],
                                     workspace=ws_v)
+        elif mode == "mss":
+            sv.specv_mss_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
         elif F:  # the fused SSD round: verify + outcome keys + hit in one pass
             sv.specv_ssd_round(d_target, d_draft, d_tok, d_temp, d_unif, F, keys=keys,
                                key_logits=key_logits, hit=hit, workspace=ws_v, fanout=fanout,
@@ -450,6 +483,7 @@ def run_ours(args) -> None:
     h_keys = torch.empty((B, K + 1, F), dtype=torch.int32).pin_memory() if F else None
     h_hit = torch.empty(B, dtype=torch.uint8).pin_memory() if F else None
     h_st = torch.empty(lay["rows"], dtype=torch.int32).pin_memory() if mode == "sample" else None
+    h_tm = torch.empty(B, dtype=torch.int32).pin_memory() if mode == "mss" else None
 
     def e2e_step():
         if d_target is not None:
@@ -464,6 +498,9 @@ def run_ours(args) -> None:
         step()
         if mode == "sample":
             h_st.copy_(s_tok, non_blocking=True)
+        elif mode == "mss":
+            h_n.copy_(outs["accepted"], non_blocking=True)
+            h_tm.copy_(outs["out_token"], non_blocking=True)
         else:
             h_n.copy_(outs["accept_len"], non_blocking=True)
             h_ot.copy_(outs["out_tokens"], non_blocking=True)
@@ -483,7 +520,7 @@ def run_ours(args) -> None:
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
     h2d = sum(t.numel() * t.element_size()
               for t in (h_target, h_draft, h_tok, h_temp, h_unif, h_cu) if t is not None)
-    d2h = (h_st.numel() * 4 if mode == "sample" else
+    d2h = (h_st.numel() * 4 if mode == "sample" else 2 * B * 4 if mode == "mss" else
            h_n.numel() * 4 + h_ot.numel() * 4 + ((h_keys.numel() * 4 + h_hit.numel()) if F else 0))
 
     if rank != 0:
@@ -517,6 +554,7 @@ def run_ours(args) -> None:
         "config": {
             "workload": f"{args.workload}: {desc}",
             "B_per_gpu": B, "K": K, "V": V, "logits": spec.dtype, "F": F,
+            **({"M": MSS_M[args.workload], "nodes": B} if mode == "mss" else {}),
             **({"fanout": fanout} if fanout else {}),
             "rows_per_step_per_gpu": lay["rows"],
             "l2": (f"inputs {in_bytes / 1e9:.2f} GB > {L2_BYTES / 2**20:.0f} MiB L2, no flush"
@@ -525,7 +563,7 @@ def run_ours(args) -> None:
         "roofline": {
             "bound": "hbm",
             "kernel": (f"stats_kernel<{'bf16' if is_bf16 else 'fp32'},"
-                       f"{'sample' if mode == 'sample' else 'ssd' if F else 'verify'}> "
+                       f"{mode if mode in ('sample', 'mss') else 'ssd' if F else 'verify'}> "
                        f"(reads every logit once)"),
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -538,6 +576,7 @@ def run_ours(args) -> None:
             "avg_launch_ms": round(a_ms, 5),
         },
         "call": {"api": ("specv_saguaro_sample" if mode == "sample" else
+                         "specv_mss_verify" if mode == "mss" else
                          "specv_ssd_round" if F else "specv_verify"), "launches": 2,
                  "ms": round(ms_step, 5),
                  "ms_split": round(v_ms, 5), "stats_ms": round(a_ms, 5),
@@ -550,7 +589,7 @@ def run_ours(args) -> None:
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec, mode=mode, saguaro=saguaro)
+        line["cpu_baseline"] = cpu_baseline(spec, mode=mode, saguaro=saguaro, workload=args.workload)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -570,12 +609,12 @@ def run_reference(args) -> None:
     if args.workload in GEOMETRIC:  # the oracle's cost does not depend on the split of F
         spec = dataclasses.replace(spec, F=16)
     cores = os.cpu_count() or 1
-    probe = lay_out(wl.generate(spec, rows=[0]), spec, mode)
+    probe = lay_out(gen_data(spec, [0], mode, args.workload), spec, mode)
     t_row = time_oracle(probe, spec, 1, mode, saguaro)
     # whole run (warm-up + timed) within about a minute
     per_step = 60.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(spec.B, per_step / max(t_row, 1e-6) * min(cores, 8))))
-    lay = lay_out(wl.generate(spec, rows=list(range(n))), spec, mode)
+    lay = lay_out(gen_data(spec, list(range(n)), mode, args.workload), spec, mode)
     for _ in range(args.warmup):
         time_oracle(lay, spec, cores, mode, saguaro)
     t0 = time.perf_counter()

@@ -265,6 +265,60 @@ specv_status specv_saguaro_sample(const specv_saguaro_args* args, void* workspac
                                   size_t workspace_bytes, void* stream);
 
 /*
+ * Multi-step speculative sampling (MSS) at B token-tree nodes ("Lecture 5 -
+ * Speculative Decoding and SpecInfer" §6.4; SpecInfer Theorems 4.2, 4.3).
+ * Node b has a target row z_t and a draft row z_d (the draft model's logits
+ * at that node), p = softmax(z_t/T), q = softmax(z_d/T), T = temperature[b],
+ * and m_b candidate children x_0..x_{m_b-1} (candidates[b, 0..m_b-1]) that
+ * the drafter drew independently from q.  The candidates are tested in
+ * order: x_j is accepted iff q(x_j) > 0 and p_j(x_j)/q(x_j) >= u_j, where
+ * p_0 = p and, after each rejection, p_{j+1} = norm(max(0, p_j - q)).  The
+ * first accepted x_j is the node's token (accepted[b] = j); when all m_b are
+ * rejected the token is the smallest v whose running sum of p_{m_b} exceeds
+ * u_M (accepted[b] = -1).  u_j = uniforms[b, j], u_M = uniforms[b, M].  The
+ * token's law is exactly p for any q; one candidate is plain speculative
+ * sampling.  Greedy nodes (T = 0): the first candidate equal to argmax p is
+ * accepted, else the token is argmax p (first maximum).
+ * SPECV_MSS_NAIVE in flags: naive sampling, the correct rule when the
+ * candidates were NOT drawn from q (e.g. the top-k of q): the token is drawn
+ * from p by u_M and accepted[b] is the first j with x_j equal to it, or -1.
+ * accept_prob[b, j] = min(1, p_j(x_j)/q(x_j)) for every tested candidate, 0
+ * for the others (and under SPECV_MSS_NAIVE).
+ * Row status: SPECV_ROW_BAD_TOKEN (a candidate outside [0, V)),
+ * SPECV_ROW_BAD_COUNT (m_b outside [0, M]), SPECV_ROW_NONFINITE,
+ * SPECV_ROW_BAD_TEMP, SPECV_ROW_DEVICE_TIMEOUT: the node gets token -1 and
+ * accepted -1.  SPECV_ROW_FALLBACK (informational): a residual had no mass
+ * (p_j <= q everywhere, reachable only by rounding), so the token was drawn
+ * from p, or rounding left u_M past the end of the running sum.
+ * All pointers are device pointers; target and draft rows 16-byte aligned
+ * (base and strides) take the staged path, any other layout a slower one.
+ * Each rejection costs one pass over the node's two rows.
+ */
+#define SPECV_MSS_NAIVE 1
+
+typedef struct {
+  int32_t B, M, V;             /* nodes; candidates per node (1..32); vocabulary */
+  int32_t dtype;               /* specv_dtype */
+  const void* target_logits;   /* node b's row at target_logits + b * target_row_stride */
+  int64_t target_row_stride;   /* elements, >= V */
+  const void* draft_logits;    /* node b's row at draft_logits + b * draft_row_stride */
+  int64_t draft_row_stride;    /* elements, >= V */
+  const int32_t* candidates;   /* [B, M] */
+  const int32_t* num_candidates; /* optional [B]: m_b (NULL: every node has M) */
+  const float* temperature;    /* [B] */
+  const float* uniforms;       /* [B, M+1] in [0, 1) */
+  int32_t flags;               /* 0 or SPECV_MSS_NAIVE */
+  int32_t* accepted;           /* OUT [B] */
+  int32_t* out_token;          /* OUT [B] */
+  float* accept_prob;          /* OUT, optional [B, M] */
+  int32_t* row_status;         /* OUT, optional [B] */
+} specv_mss_args;
+
+size_t specv_mss_workspace_bytes(int32_t B, int32_t M, int32_t V, int32_t dtype);
+specv_status specv_mss_verify(const specv_mss_args* args, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * Geometric fan-out ("Speculative Speculative Decoding" Theorem 12, proved in
  * Appendix A.2).  For a drafter with per-token acceptance rate a (0 < a < 1)
  * whose cache-miss probability at fan-out F is F^-r (r > 0), the fan-outs
@@ -306,7 +360,8 @@ const char* specv_last_error(void);
 int32_t specv_last_launch_count(void);
 
 /* Measurement hook.  While `event` (a cudaEvent_t created by the caller) is
- * set, every specv_verify / specv_ssd_round / specv_predict_outcomes call made
+ * set, every specv_verify / specv_ssd_round / specv_predict_outcomes /
+ * specv_saguaro_sample / specv_mss_verify call made
  * by this host thread records it on its stream between the row-statistics
  * kernel and the decision kernel, so the two can be timed apart.  NULL clears
  * it.  The library does not create, own or destroy the event. */

@@ -27,6 +27,7 @@ SPECV_BF16, SPECV_FP32 = 0, 1
 ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TEMP, ROW_FALLBACK, ROW_DEVICE_TIMEOUT = 1, 2, 4, 8, 16
 ROW_BAD_COUNT = 32
 SPECV_NO_DRAFT_PROBS = 1
+SPECV_MSS_NAIVE = 1
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -52,6 +53,15 @@ class SaguaroArgs(ctypes.Structure):
     _fields_ = [("B", _I32), ("V", _I32), ("dtype", _I32), ("logits", _P), ("row_stride", _I64),
                 ("temperature", _P), ("F", _I32), ("C", ctypes.c_float), ("uniforms", _P),
                 ("tokens", _P), ("q", _P), ("row_status", _P)]
+
+
+class MssArgs(ctypes.Structure):
+    _fields_ = [("B", _I32), ("M", _I32), ("V", _I32), ("dtype", _I32),
+                ("target_logits", _P), ("target_row_stride", _I64),
+                ("draft_logits", _P), ("draft_row_stride", _I64),
+                ("candidates", _P), ("num_candidates", _P), ("temperature", _P), ("uniforms", _P),
+                ("flags", _I32), ("accepted", _P), ("out_token", _P), ("accept_prob", _P),
+                ("row_status", _P)]
 
 
 class PredictArgs(ctypes.Structure):
@@ -96,6 +106,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specv_saguaro_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
     lib.specv_saguaro_sample.restype = ctypes.c_int
     lib.specv_saguaro_sample.argtypes = [ctypes.POINTER(SaguaroArgs), _P, ctypes.c_size_t, _P]
+    lib.specv_mss_workspace_bytes.restype = ctypes.c_size_t
+    lib.specv_mss_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
+    lib.specv_mss_verify.restype = ctypes.c_int
+    lib.specv_mss_verify.argtypes = [ctypes.POINTER(MssArgs), _P, ctypes.c_size_t, _P]
     lib.specv_geometric_fanout.restype = ctypes.c_int
     lib.specv_geometric_fanout.argtypes = [_I32, ctypes.c_double, ctypes.c_double, _I32, _I32,
                                            _P, _P]
@@ -374,6 +388,44 @@ def specv_saguaro_sample(logits, temperature, F: int, C: float, uniforms, *, tok
     _check(lib.specv_saguaro_sample(ctypes.byref(args), _ptr(workspace), workspace.numel(),
                                     _stream(stream)))
     return dict(tokens=tokens, q=q, row_status=row_status)
+
+
+def specv_mss_verify(target, draft, candidates, temperature, uniforms, *, num_candidates=None,
+                     naive: bool = False, accepted=None, out_token=None, accept_prob=None,
+                     row_status=None, workspace=None, stream=None) -> dict:
+    """Multi-step speculative sampling at B token-tree nodes (see
+    include/specv.h): target, draft [B, V] (bf16 or fp32, CUDA; rows may be
+    strided), candidates int32 [B, M], num_candidates int32 [B] or None,
+    temperature fp32 [B], uniforms fp32 [B, M+1].  naive=True: naive sampling.
+    Returns accepted int32 [B], out_token int32 [B], accept_prob fp32 [B, M],
+    row_status int32 [B]."""
+    import torch
+    lib = load_library()
+    assert target.dim() == 2 and draft.dim() == 2 and target.shape == draft.shape
+    assert target.stride(-1) == 1 and draft.stride(-1) == 1 and target.dtype == draft.dtype
+    B, V = target.shape
+    M = candidates.shape[1]
+    dev = target.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    accepted = torch.empty(B, **i32) if accepted is None else accepted
+    out_token = torch.empty(B, **i32) if out_token is None else out_token
+    accept_prob = (torch.empty((B, M), dtype=torch.float32, device=dev)
+                   if accept_prob is None else accept_prob)
+    row_status = torch.empty(B, **i32) if row_status is None else row_status
+    code = _dtype_code(target)
+    need = lib.specv_mss_workspace_bytes(B, M, V, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    args = MssArgs(B, M, V, code, target.data_ptr(), target.stride(0), draft.data_ptr(),
+                   draft.stride(0), candidates.data_ptr(),
+                   num_candidates.data_ptr() if num_candidates is not None else None,
+                   temperature.data_ptr(), uniforms.data_ptr(),
+                   SPECV_MSS_NAIVE if naive else 0, accepted.data_ptr(), out_token.data_ptr(),
+                   accept_prob.data_ptr(), row_status.data_ptr())
+    _check(lib.specv_mss_verify(ctypes.byref(args), _ptr(workspace), workspace.numel(),
+                                _stream(stream)))
+    return dict(accepted=accepted, out_token=out_token, accept_prob=accept_prob,
+                row_status=row_status)
 
 
 def specv_geometric_fanout(K: int, a: float, r: float, budget: int, max_f: int = 32) -> tuple:

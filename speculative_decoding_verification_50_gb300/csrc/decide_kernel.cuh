@@ -46,6 +46,15 @@ struct Dec {  // a batch row's decision (the same in every CTA of its cluster)
   FF R;          // total residual mass (the sampler normalises its q by it)
   FF tau, pre_mine;
   float px[kMaxK], qx[kMaxK];
+  // MSS at a token-tree node: the residual after j rejections is
+  // max(0, p - c_j q) / D_j with c_0 = 0, D_0 = 1, c_{j+1} = c_j + D_j and
+  // D_j = sum_v max(0, p - c_j q) (one pass over the node's rows each).
+  FF cff;        // c_j of the current pass
+  float cq;      // c_j as a float (the residual's multiplier of q)
+  int32_t next;  // the candidate tested after the current pass
+  int32_t acc;   // the accepted candidate, or -1
+  int32_t again; // another pass is needed
+  float ap[kMaxK];  // min(1, p_j(x_j)/q(x_j)) of the tested candidates
 };
 static_assert(sizeof(Dec) % 4 == 0, "Dec copied as words");
 
@@ -79,6 +88,11 @@ struct DecideParams {
   int32_t sg_F;      // Saguaro sampling: the drafts came from sigma_{sg_F, sg_C}
   float sg_C;        //   (0: plain softmax drafts); the sampler's own F and C
   int32_t local_draw;  // draws from a whole row read only the chunk holding U * R
+  // MSS (K = M candidates per node, one target and one draft row each)
+  const int32_t* ncand;  // per-node candidate counts, or null (all M)
+  int32_t naive;         // naive sampling: one draw from p, candidates matched to it
+  int32_t* mss_acc;      // [B] accepted candidate or -1
+  float* mss_ap;         // optional [B, M] accept probabilities
 };
 
 // Combine the chunk records of one position over an aligned group of W lanes
@@ -605,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   constexpr int VW = E::VW;
   constexpr bool kTopF = MODE == kModeSsd;      // outcome keys and hit
   constexpr bool kSample = MODE == kModeSample;  // draft-side Saguaro sampling
+  constexpr bool kMss = MODE == kModeMss;        // candidates at token-tree nodes
   extern __shared__ float segs[];  // [tiles * kWarps] segment sums of r
   __shared__ PosStats ps[kMaxK + 1];
   __shared__ Dec dec;
@@ -638,9 +653,17 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   const bool greedy = T == 0.f;
   const bool temp_ok = T >= 0.f && T < pos_inf();
   const float c = greedy ? 1.f : temp_scale(T);
-  const int64_t u0 = static_cast<int64_t>(b) * (K + 1);  // records, outputs: [B, K+1]
+  // records, outputs: [B, K+1] (an MSS node has one position)
+  const int64_t u0 = kMss ? static_cast<int64_t>(b) : static_cast<int64_t>(b) * (K + 1);
   const RowLayout L = row_layout(P.cu, P.ntok, b, K, P.t_bs, P.t_rs, P.d_bs, P.d_rs);
-  const int kb = L.kb < 0 ? 0 : L.kb;  // this row's drafts
+  int kb_in = L.kb;  // this row's drafts (an MSS node's candidates); -1: bad count
+  if (kMss && P.ncand) {
+    const int m = P.ncand[b];
+    kb_in = (m >= 0 && m <= K) ? m : -1;
+  }
+  const int kb = kb_in < 0 ? 0 : kb_in;
+  const int npos = kMss ? 0 : kb;     // positions with records: 0..npos
+  const int u_draw = kMss ? K : kb;   // the uniform of the final draw
   const bool nd = P.no_draft != 0;
 
   // ---- every CTA combines the records and decides (identical results) -------
@@ -650,11 +673,9 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
       const int x = P.tokens[L.tok0 + i];
       float zt = 0.f, zd = 0.f;
       if (x >= 0 && x < P.V) {
-        zt = E::scalar(static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(i) * P.t_rs) * E::ES,
-                       x);
-        if (!nd)
-          zd = E::scalar(static_cast<const char*>(P.zd) + (L.d_off + static_cast<int64_t>(i) * P.d_rs) * E::ES,
-                         x);
+        const int64_t ri = kMss ? 0 : i;  // every candidate of a node sits on its one row
+        zt = E::scalar(static_cast<const char*>(P.zt) + (L.t_off + ri * P.t_rs) * E::ES, x);
+        if (!nd) zd = E::scalar(static_cast<const char*>(P.zd) + (L.d_off + ri * P.d_rs) * E::ES, x);
       }
       pre_x[i] = x;
       pre_zt[i] = zt;
@@ -666,10 +687,10 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   // the row-statistics kernel's output, so wait for it to complete here.
   pdl_wait_primary();
   // Half a warp per position: positions 2w and 2w+1 on warp w, 16 per pass.
-  for (int i0 = 2 * warp; i0 <= kb; i0 += 2 * kWarps) {
+  for (int i0 = 2 * warp; i0 <= npos; i0 += 2 * kWarps) {
     const int i = i0 + (lane >> 4);
-    const PosStats p = combine_position<16>(P.recs + (u0 + min(i, kb)) * P.nchunk, P.nchunk, c, lane & 15);
-    if ((lane & 15) == 0 && i <= kb) ps[i] = p;
+    const PosStats p = combine_position<16>(P.recs + (u0 + min(i, npos)) * P.nchunk, P.nchunk, c, lane & 15);
+    if ((lane & 15) == 0 && i <= npos) ps[i] = p;
   }
   __syncthreads();
 
@@ -730,7 +751,87 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     }
     __syncthreads();
   }
-  if (warp == 0) {
+  // ---- MSS at a token-tree node ([CS349D] §6.4): warp 0 tests the first
+  // candidate; each rejection is followed by a residual pass below ------------
+  if (kMss && warp == 0) {
+    const PosStats& q = ps[0];
+    int nf = 0;
+    if (lane == 0 && temp_ok)
+      nf = greedy ? ((q.bad & 1) || q.it == INT_MAX || q.id == INT_MAX)
+                  : (!(q.St.hi >= 1.f) || q.Mt == kNegMax || !(q.Sd.hi >= 1.f) || q.Md == kNegMax);
+    const bool cl = lane < kb;
+    const int x = cl ? pre_x[lane] : -1;
+    int status = temp_ok ? 0 : kBadTemp;
+    if (kb_in < 0) status |= kBadCount;
+    if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
+    if (q.bad & 2) status |= kTimeout;
+    if (__any_sync(0xffffffffu, cl && (x < 0 || x >= P.V))) status |= kBadToken;
+    const bool ok = !(status & kErrors);
+    const bool naive = P.naive != 0;
+    // t_j = p(x_j) / q(x_j), from the log2 difference so neither factor
+    // underflows; q(x_j) > 0 iff its draft logit is finite
+    float t = 0.f;
+    bool qpos = false;
+    if (cl && ok && !greedy) {
+      const float lt = __fmul_rn(pre_zt[lane] - q.Mt, c);
+      const float ld = __fmul_rn(pre_zd[lane] - q.Md, c);
+      qpos = pre_zd[lane] != neg_inf();
+      t = qpos ? __fmul_rn(ex2(__fsub_rn(lt, ld)), __fdiv_rn(q.Sd.hi, q.St.hi)) : 0.f;
+    }
+    const unsigned hitg = __ballot_sync(0xffffffffu, ok && cl && greedy && x == q.it);
+    const int acc_g = hitg ? __ffs(hitg) - 1 : -1;
+    const bool a0 = __shfl_sync(0xffffffffu, cl && qpos && t >= pre_u[lane < kMaxK ? lane : 0], 0);
+    float ap = 0.f;
+    if (ok && cl && !naive) ap = greedy ? (lane == acc_g ? 1.f : 0.f) : (lane == 0 ? fminf(t, 1.f) : 0.f);
+    dec.ap[lane] = ap;
+    dec.px[lane] = t;
+    dec.qx[lane] = qpos ? 1.f : 0.f;
+    if (lane == 0) {
+      int acc = -1, token = -1, mode = 1, need = 0;
+      if (ok) {
+        if (greedy) {
+          acc = acc_g;
+          token = q.it;
+        } else if (naive || kb == 0) {
+          need = 1;  // a draw from p itself
+        } else if (a0) {
+          acc = 0;
+          token = pre_x[0];
+        } else {
+          need = 1;  // residual max(0, p - c_1 q), c_1 = 1
+          mode = 0;
+        }
+      }
+      dec.n = 0;
+      dec.status = status;
+      dec.mode = mode;
+      dec.xn = -1;
+      dec.need_scan = need;
+      dec.token = token;
+      dec.acc = acc;
+      dec.owner = -1;
+      dec.last_pos = 0;
+      dec.mt = q.Mt;
+      dec.md = q.Md;
+      dec.ist = __fdiv_rn(1.f, q.St.hi);
+      dec.isd = __fdiv_rn(1.f, q.Sd.hi);
+      dec.sgc = 1.f;
+      dec.zl = pos_inf();
+      dec.il = -1;
+      dec.full_pass = 0;
+      dec.tau = ff(0.f);
+      dec.pre_mine = ff(0.f);
+      dec.R = ff(0.f);
+      dec.cff = ff(1.f);
+      dec.cq = 1.f;
+      dec.next = 1;
+      dec.again = 0;
+      tok_slot = token;
+      q_slot = 0.f;
+      copy_fail = 0;
+    }
+  }
+  if (!kMss && warp == 0) {
     int nf = 0;
     // Saguaro: the weighted normaliser of draft row i, sum - (1 - C) * top-F_s mass
     const float sgC = sg_on ? P.sg_C : 1.f;
@@ -757,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     const bool acc_lane = lane < kb;
     const int x = acc_lane ? pre_x[lane] : -1;
     int status = temp_ok ? 0 : kBadTemp;
-    if (L.kb < 0) status |= kBadCount;
+    if (kb_in < 0) status |= kBadCount;
     if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
     if (__any_sync(0xffffffffu, lane <= kb && (ps[lane].bad & 2))) status |= kTimeout;
     if (__any_sync(0xffffffffu, acc_lane && (x < 0 || x >= P.V))) status |= kBadToken;
@@ -846,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     const SgW w = kSample ? SgW{dec.sgc, dec.zl, dec.il} : SgW{1.f, pos_inf(), -1};
     const int tok = chunk_draw<DT, VEC>(P.recs + (u0 + nn) * P.nchunk, P.nchunk, P.chunk, P.V,
                                         kSample, dec.mt, c, row,
-                                        P.unif[L.u_off + kb], sg_kv, sg_ki,
+                                        P.unif[L.u_off + u_draw], sg_kv, sg_ki,
                                         (kSample && sg_on) ? sg_nk : 0, w, draw);
     if (threadIdx.x == 0) {
       tok_slot = tok;
@@ -889,11 +990,14 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     const int nv = RC.nv;
     const int ntl = (nv + kThreads - 1) / kThreads;
     bool copies_ok = true;
-    // ---- residual mass of this slice: per-warp segment sums ----------------
-    for (int attempt = 0; attempt < 2; ++attempt) {
+    // ---- residual mass of this slice: per-warp segment sums.  One pass, plus
+    // one when a zero mass falls back to p; an MSS node one per rejection ----
+    const int max_pass = kMss ? kb + 2 : 2;
+    for (int pass = 0; pass < max_pass; ++pass) {
       const int mode = dec.mode;
-      const float mt = dec.mt, md = dec.md, ist = dec.ist, isd = dec.isd;
-      if (staged && attempt == 0) {
+      const float mt = dec.mt, md = dec.md, ist = dec.ist;
+      const float isd = kMss ? __fmul_rn(dec.isd, dec.cq) : dec.isd;  // MSS: c_j q
+      if (staged && pass == 0) {
         Chunk SC = RC;
         if (mode != 0) SC.rowd = nullptr;
         copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd,
@@ -923,15 +1027,15 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
         FF acc = ff(0.f);
         for (int sg = lane; sg < ntl * kWarps; sg += 32) acc = ff_add(acc, segs[sg]);
         acc = warp_ffsum_all(acc);
-        if (lane == 0) cta_total[attempt] = acc;
+        if (lane == 0) cta_total[pass & 1] = acc;
       }
       cluster_sync();  // (1) per-CTA totals visible; every CTA of the cluster has started
       if (!copies_ok && threadIdx.x == 0) *cluster.map_shared_rank(&copy_fail, 0) = 1;
       if (warp == 0) {
-        const FF tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total[attempt], lane) : ff(0.f);
+        const FF tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total[pass & 1], lane) : ff(0.f);
         const FF incl = warp_ffscan(tr, lane);
         const FF R = shfl(incl, 31);
-        const FF tau = ff_mul(R, P.unif[L.u_off + kb]);  // the bonus uniform
+        const FF tau = ff_mul(R, P.unif[L.u_off + u_draw]);  // the bonus uniform
         const unsigned own = __ballot_sync(0xffffffffu, tr.hi > 0.f && ff_gt(incl, tau));
         const unsigned pos = __ballot_sync(0xffffffffu, tr.hi > 0.f);
         const FF pm = shfl(ff_add(incl, ff_neg(tr)), rank);
@@ -939,7 +1043,25 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
           dec.tau = tau;
           dec.pre_mine = pm;
           dec.R = R;
-          if (R.hi > 0.f) {
+          dec.again = 0;
+          if (kMss && mode == 0 && dec.next < kb && R.hi > 0.f) {
+            // MSS: R = D_j; candidate j is accepted iff
+            // p_j(x_j)/q(x_j) = max(0, t_j - c_j) / D_j >= u_j
+            const int j = dec.next;
+            const FF d = ff_add(ff(dec.px[j]), ff_neg(dec.cff));
+            const float a = (dec.qx[j] > 0.f && d.hi > 0.f) ? __fdiv_rn(d.hi, R.hi) : 0.f;
+            dec.ap[j] = fminf(a, 1.f);
+            if (dec.qx[j] > 0.f && a >= pre_u[j]) {
+              dec.acc = j;
+              dec.token = pre_x[j];
+              tok_slot = pre_x[j];
+            } else {  // rejected: c_{j+1} = c_j + D_j, one more pass
+              dec.cff = ff_add(dec.cff, R);
+              dec.cq = dec.cff.hi;
+              dec.next = j + 1;
+              dec.again = 1;
+            }
+          } else if (R.hi > 0.f) {
             if (own) {
               dec.owner = __ffs(own) - 1;
             } else {  // U*R >= R after rounding: the last index with r > 0
@@ -950,11 +1072,12 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
           } else if (dec.mode != 1) {
             dec.mode = 1;  // zero residual mass: draw from p_n instead
             dec.status |= kFallback;
+            dec.again = 1;
           }
         }
       }
       __syncthreads();  // the decision on the owner, made by warp 0, seen by the CTA
-      if (dec.owner >= 0 || attempt == 1 || dec.mode != 1) break;
+      if (!dec.again) break;
     }
 
     // ---- owner CTA: locate the crossing segment, then scan it --------------
@@ -1011,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
       for (int k = 0; k < VW; ++k) r[k] = 0.f;
       if (seg >= 0 && j < nv)
         residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, dec.mode, dec.mt, dec.md, c, dec.ist,
-                              dec.isd, dec.xn, sgw, r);
+                              kMss ? __fmul_rn(dec.isd, dec.cq) : dec.isd, dec.xn, sgw, r);
       const int32_t base = static_cast<int32_t>(v0) + j * VW;
       int found = -1;
       float rv = 0.f;  // r at the found logit (the sampler reports it as sigma(t))
@@ -1091,7 +1214,28 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   if (scan || kTopF) cluster_sync();
 
   // ---- outputs, written by rank 0 ---------------------------------------------
-  if (rank == 0) {
+  if (kMss && rank == 0) {  // a node: its token, the accepted candidate, accept probabilities
+    const int status = dec.status | (copy_fail ? kTimeout : 0);
+    const bool ok = !(status & kErrors);
+    const int t = threadIdx.x;
+    const int32_t token = ok ? tok_slot : -1;
+    if (t == 0) {
+      int acc = ok ? dec.acc : -1;
+      if (ok && P.naive) {  // naive sampling: the first candidate equal to the draw
+        acc = -1;
+        for (int j = 0; j < kb; ++j)
+          if (pre_x[j] == token) {
+            acc = j;
+            break;
+          }
+      }
+      P.out_tokens[b] = token;
+      P.mss_acc[b] = acc;
+      if (P.row_status) P.row_status[b] = ok ? (status & kFallback) : (status & kErrors);
+    }
+    if (P.mss_ap && t < K) P.mss_ap[static_cast<int64_t>(b) * K + t] = (ok && t < kb) ? dec.ap[t] : 0.f;
+  }
+  if (!kMss && rank == 0) {
     // A slice whose staged copies did not land makes the row an error row
     // (read after the barrier above, so the same on every thread).
     const int status = dec.status | (copy_fail ? kTimeout : 0);

@@ -52,7 +52,7 @@ int vec_width(int32_t dtype) { return dtype == SPECV_BF16 ? 8 : 4; }
 // it, for tuning runs.
 int sm_count();
 
-int pick_cluster(int32_t B, int32_t V, int vw) {
+int pick_cluster(int32_t B, int32_t V, int vw, int min_c = 1) {
   static int env = -2;
   if (env == -2) {
     const char* s = getenv("SPECV_CLUSTER");
@@ -63,6 +63,7 @@ int pick_cluster(int32_t B, int32_t V, int vw) {
   // two: clusters of 2^k CTAs pack onto the GPCs without gaps.
   const int want = 4 * sm_count();
   int c = (want + B - 1) / (B > 0 ? B : 1);
+  if (c < min_c) c = min_c;
   if (c > 16) c = 16;
   while (c & (c - 1)) c &= c - 1;
   const int tiles = static_cast<int>((static_cast<int64_t>(V) + kThreads * vw - 1) / (kThreads * vw));
@@ -139,7 +140,10 @@ int sm_count() {
   return n;
 }
 
-Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
+// min_cb: the smallest cluster; an MSS node may stream its rows once per
+// rejection, and two CTAs per node halve each pass (measured best at 2048
+// nodes of 152064 fp32 logits: 1 -> 0.69 ms, 2 -> 0.58, 4 -> 0.60, 8 -> 0.61).
+Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int min_cb = 1) {
   Plan pl;
   const int vw = vec_width(dtype);
   const int64_t units = static_cast<int64_t>(B > 0 ? B : 0) * (K + 1);
@@ -159,7 +163,7 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
     if (pl.iters == 1 || env_iters >= 1 || units * pl.nchunk >= want) break;
     pl.iters /= 2;
   }
-  pl.CB = pick_cluster(B, V, vw);
+  pl.CB = pick_cluster(B, V, vw, min_cb);
   pl.L = slice_len(V, pl.CB, vw);
   const int64_t ntiles = ((pl.L / vw) + kThreads - 1) / kThreads;
   pl.smemB = static_cast<size_t>(ntiles) * kWarps * sizeof(float);
@@ -329,21 +333,32 @@ size_t specv_verify_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t dty
 
 namespace {
 
-// Both kernels for one call: verification, an SSD round, or (kModeSample, K =
-// 0, the drafter's rows as draft rows) Saguaro sampling.  sg_F/sg_C: the
+// What an MSS call adds to the verification arguments.
+struct MssExtra {
+  const int32_t* ncand;
+  int32_t naive;
+  int32_t* acc;
+  float* ap;
+};
+
+// Both kernels for one call: verification, an SSD round, (kModeSample, K =
+// 0, the drafter's rows as draft rows) Saguaro sampling, or (kModeMss, K = M
+// candidates, one target and one draft row per node) MSS.  sg_F/sg_C: the
 // Saguaro sampling scheme of the drafts (sg_F = 0: none).
 specv_status run_verify(const specv_verify_args* a, void* workspace, size_t workspace_bytes,
                         void* stream, int mode, int32_t F, int32_t* keys, float* key_logits,
-                        uint8_t* hit, const int32_t* fanout, int32_t sg_F = 0, float sg_C = 1.f) {
+                        uint8_t* hit, const int32_t* fanout, int32_t sg_F = 0, float sg_C = 1.f,
+                        const MssExtra* mx = nullptr) {
   const int32_t B = a->B, K = a->K, V = a->V;
+  const int32_t Ka = mode == kModeMss ? 0 : K;  // positions per row in the statistics kernel
   const bool cands = mode == kModeSsd || mode == kModeSample;
-  const Plan pl = make_plan(B, K, V, cands ? F : 0, a->dtype);
+  const Plan pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, mode == kModeMss ? 2 : 1);
   if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need)
     return fail(SPECV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
   if (!aligned(workspace, 256)) return fail(SPECV_ERR_WORKSPACE, "workspace not 256-byte aligned");
-  const int64_t units = static_cast<int64_t>(B) * (K + 1);
+  const int64_t units = static_cast<int64_t>(B) * (Ka + 1);
   if (units * pl.nchunk > 0x7fffffffLL || static_cast<int64_t>(B) * pl.CB > 0x7fffffffLL)
     return fail(SPECV_ERR_UNSUPPORTED, "B*(K+1) too large");
   const int es = elem_bytes(a->dtype);
@@ -371,7 +386,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.cand_v = cand_v;
   sp.cand_i = cand_i;
   sp.B = B;
-  sp.K = K;
+  sp.K = Ka;
   sp.V = V;
   sp.F = F;
   sp.nchunk = static_cast<int32_t>(pl.nchunk);
@@ -381,9 +396,11 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.cu = a->cu_num_draft_tokens;
   sp.ntok = a->num_draft_tokens;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = mode == kModeSsd      ? launch_stats<kModeSsd>(a->dtype, vec, units * pl.nchunk, s, sp)
-                  : mode == kModeSample ? launch_stats<kModeSample>(a->dtype, vec, units * pl.nchunk, s, sp)
-                                        : launch_stats<kModeVerify>(a->dtype, vec, units * pl.nchunk, s, sp);
+  const int64_t items = units * pl.nchunk;
+  cudaError_t e = mode == kModeSsd      ? launch_stats<kModeSsd>(a->dtype, vec, items, s, sp)
+                  : mode == kModeSample ? launch_stats<kModeSample>(a->dtype, vec, items, s, sp)
+                  : mode == kModeMss    ? launch_stats<kModeMss>(a->dtype, vec, items, s, sp)
+                                        : launch_stats<kModeVerify>(a->dtype, vec, items, s, sp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
   e = record_split(s);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "split event: %s", cudaGetErrorString(e));
@@ -443,8 +460,15 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
     dp.stages = 0;
     smemB = pl.smemB;
   }
+  if (mx) {
+    dp.ncand = mx->ncand;
+    dp.naive = mx->naive;
+    dp.mss_acc = mx->acc;
+    dp.mss_ap = mx->ap;
+  }
   e = mode == kModeSsd      ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, smemB, s, dp)
       : mode == kModeSample ? launch_decide<kModeSample>(a->dtype, vec, pl.CB, B, smemB, s, dp)
+      : mode == kModeMss    ? launch_decide<kModeMss>(a->dtype, vec, pl.CB, B, smemB, s, dp)
                             : launch_decide<kModeVerify>(a->dtype, vec, pl.CB, B, smemB, s, dp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "decision launch: %s", cudaGetErrorString(e));
   g_launches = 2;
@@ -635,6 +659,55 @@ specv_status specv_saguaro_sample(const specv_saguaro_args* a, void* workspace,
   const int32_t F = a->F > 0 ? a->F : 1;
   return run_verify(&v, workspace, workspace_bytes, stream, kModeSample, F, nullptr, nullptr,
                     nullptr, nullptr, a->F, a->F > 0 ? a->C : 1.f);
+}
+
+size_t specv_mss_workspace_bytes(int32_t B, int32_t M, int32_t V, int32_t dtype) {
+  if (B <= 0 || M < 1 || V < 1) return 0;
+  return plan_workspace(make_plan(B, 0, V, 0, dtype, 2));
+}
+
+specv_status specv_mss_verify(const specv_mss_args* a, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  g_launches = 0;
+  if (!a) return fail(SPECV_ERR_INVALID_ARG, "args is NULL");
+  const int32_t B = a->B, M = a->M, V = a->V;
+  if (B < 0) return fail(SPECV_ERR_INVALID_ARG, "B=%d < 0", B);
+  if (M < 1 || M > 32) return fail(SPECV_ERR_INVALID_ARG, "M=%d outside [1, 32]", M);
+  if (V < 1) return fail(SPECV_ERR_INVALID_ARG, "V=%d < 1", V);
+  if (a->dtype != SPECV_BF16 && a->dtype != SPECV_FP32)
+    return fail(SPECV_ERR_INVALID_ARG, "dtype=%d is not SPECV_BF16 or SPECV_FP32", a->dtype);
+  if (a->flags & ~SPECV_MSS_NAIVE) return fail(SPECV_ERR_INVALID_ARG, "unknown flags 0x%x", a->flags);
+  if (B == 0) return ok();
+  if (!a->target_logits || !a->draft_logits || !a->candidates || !a->temperature ||
+      !a->uniforms || !a->accepted || !a->out_token)
+    return fail(SPECV_ERR_INVALID_ARG, "a required pointer is NULL");
+  const int es = elem_bytes(a->dtype);
+  if (!aligned(a->target_logits, es) || !aligned(a->draft_logits, es) || !aligned(a->candidates, 4) ||
+      !aligned(a->num_candidates, 4) || !aligned(a->temperature, 4) || !aligned(a->uniforms, 4) ||
+      !aligned(a->accepted, 4) || !aligned(a->out_token, 4) || !aligned(a->accept_prob, 4) ||
+      !aligned(a->row_status, 4))
+    return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
+  if (a->target_row_stride < V || a->draft_row_stride < V)
+    return fail(SPECV_ERR_INVALID_ARG, "row stride smaller than V");
+  specv_verify_args v = {};
+  v.B = B;
+  v.K = M;
+  v.V = V;
+  v.dtype = a->dtype;
+  v.target_logits = a->target_logits;
+  v.target_batch_stride = a->target_row_stride;  // one row per node
+  v.target_row_stride = a->target_row_stride;
+  v.draft_logits = a->draft_logits;
+  v.draft_batch_stride = a->draft_row_stride;
+  v.draft_row_stride = a->draft_row_stride;
+  v.draft_tokens = a->candidates;
+  v.temperature = a->temperature;
+  v.uniforms = a->uniforms;
+  v.out_tokens = a->out_token;
+  v.row_status = a->row_status;
+  const MssExtra mx{a->num_candidates, (a->flags & SPECV_MSS_NAIVE) ? 1 : 0, a->accepted, a->accept_prob};
+  return run_verify(&v, workspace, workspace_bytes, stream, kModeMss, 0, nullptr, nullptr, nullptr,
+                    nullptr, 0, 1.f, &mx);
 }
 
 // Theorem 12 of "Speculative Speculative Decoding": F_k = F_0 q^k (k < K) and

@@ -34,11 +34,17 @@ namespace specv {
 
 // verify: target and draft rows; ssd: plus draft row K and candidates;
 // predict: draft rows 0..K, candidates, no temperature; sample: one draft row
-// per batch row (K = 0) with its temperature and candidates (no exclusion).
-enum : int { kModeVerify = 0, kModeSsd = 1, kModePredict = 2, kModeSample = 3 };
+// per batch row (K = 0) with its temperature and candidates (no exclusion);
+// mss: one target and one draft row per token-tree node (K = 0).
+enum : int { kModeVerify = 0, kModeSsd = 1, kModePredict = 2, kModeSample = 3, kModeMss = 4 };
 
-// Streams target rows; uses the temperature.
-__host__ __device__ constexpr bool mode_has_target(int m) { return m == kModeVerify || m == kModeSsd; }
+// Streams target rows; keeps top-F candidates; uses the temperature.
+__host__ __device__ constexpr bool mode_has_target(int m) {
+  return m == kModeVerify || m == kModeSsd || m == kModeMss;
+}
+__host__ __device__ constexpr bool mode_has_topf(int m) {
+  return m == kModeSsd || m == kModePredict || m == kModeSample;
+}
 __host__ __device__ constexpr bool mode_has_temp(int m) { return m != kModePredict; }
 constexpr int kVecs = 2;  // 16-byte vectors per row per thread per loop trip
 constexpr int kMaxStages = 8;
@@ -380,7 +386,7 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
                                              EpiSmem& S) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
-  constexpr bool kTopF = MODE != kModeVerify;
+  constexpr bool kTopF = mode_has_topf(MODE);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if (greedy) {
@@ -763,7 +769,7 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
 template <int DT, bool VEC, int MODE>
 __global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
   constexpr bool kT = mode_has_target(MODE);
-  constexpr bool kTopF = MODE != kModeVerify;
+  constexpr bool kTopF = mode_has_topf(MODE);
   __shared__ EpiSmem S;
   pdl_launch_dependents();  // the decision kernel may be scheduled once every CTA has started
   const Chunk C = chunk_at<DT, MODE>(P, blockIdx.x);
@@ -865,7 +871,7 @@ __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* r
 template <int DT, int MODE>
 __global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const StatsParams P) {
   constexpr bool kT = mode_has_target(MODE);
-  constexpr bool kTopF = MODE != kModeVerify;
+  constexpr bool kTopF = mode_has_topf(MODE);
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ RingBars R;
   __shared__ EpiSmem S;

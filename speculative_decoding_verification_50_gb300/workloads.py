@@ -219,3 +219,75 @@ def generate(spec: Spec, rows=None, threads: int | None = None) -> dict:
     out["spec"] = spec
     out["rows"] = np.asarray(rows, dtype=np.int64)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Token-tree nodes for multi-step speculative sampling
+
+def _fill_node(spec: Spec, M: int, b: int, out: dict, j: int) -> None:
+    """Node b: one target row and one draft row drawn by spec's recipe (its
+    kind, temperature set and draft noise), M candidate children drawn
+    independently from softmax(z_d/T) by the Gumbel-max trick (a greedy node
+    proposes the draft argmax first, then draws at T = 1), and M+1 uniforms."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([spec.seed, b, 0x3155])))
+    V = spec.V
+    T = float(spec.temps[rng.integers(len(spec.temps))]) if len(spec.temps) > 1 else float(spec.temps[0])
+    lo, hi = spec.sigma_d
+    sigma_d = float(rng.uniform(lo, hi)) if hi > lo else float(lo)
+    if spec.kind == "zipf":
+        base = -1.1 * np.log(np.arange(1, V + 1, dtype=np.float64))
+        zt = rng.permuted((base + rng.normal(0.0, 0.5, size=V)).astype(np.float32))
+    else:
+        zt = rng.standard_normal(size=V, dtype=np.float32) * np.float32(spec.sigma_t)
+        if spec.kind == "boosted":
+            zt[rng.choice(V, size=spec.boost_ids, replace=False)] += np.float32(spec.boost)
+    zt_stored = _store(zt, spec.dtype)
+    zd = np.float32(spec.draft_scale) * _stored_as_f32(zt_stored, spec.dtype) + \
+        rng.standard_normal(size=V, dtype=np.float32) * np.float32(sigma_d)
+    zd_stored = _store(zd, spec.dtype)
+    zd_exact = _stored_as_f32(zd_stored, spec.dtype)
+    cands = np.empty(M, dtype=np.int32)
+    for i in range(M):
+        if T == 0.0:
+            cands[i] = int(np.argmax(zd_exact)) if i == 0 else _gumbel_argmax(rng, zd_exact, 1.0)
+        else:
+            cands[i] = _gumbel_argmax(rng, zd_exact, T)
+    out["target"][j] = zt_stored
+    out["draft"][j] = zd_stored
+    out["candidates"][j] = cands
+    out["temperature"][j] = np.float32(T)
+    out["uniforms"][j] = rng.random(M + 1, dtype=np.float32)
+
+
+def generate_mss(spec: Spec, M: int, B: int | None = None, rows=None,
+                 threads: int | None = None) -> dict:
+    """Materialise B token-tree nodes (default spec.B) for multi-step
+    speculative sampling with M candidates each.  Returns numpy arrays
+      target [n, V], draft [n, V]   fp32, or int16 bf16 bits
+      candidates [n, M]             int32, drawn i.i.d. from the draft softmax
+      temperature [n]               fp32 (0 = greedy)
+      uniforms [n, M+1]             fp32 in [0,1): u_j for candidate j, column
+                                    M for the final draw
+    Node b's bytes do not depend on which nodes are generated."""
+    B = spec.B if B is None else B
+    rows = list(range(B)) if rows is None else [int(r) for r in rows]
+    n = len(rows)
+    st = np.int16 if spec.dtype == BF16 else np.float32
+    out = {
+        "target": np.empty((n, spec.V), dtype=st),
+        "draft": np.empty((n, spec.V), dtype=st),
+        "candidates": np.empty((n, M), dtype=np.int32),
+        "temperature": np.empty(n, dtype=np.float32),
+        "uniforms": np.empty((n, M + 1), dtype=np.float32),
+    }
+    if threads is None:
+        threads = min(16, os.cpu_count() or 1)
+    items = list(enumerate(rows))
+    if threads <= 1 or n <= 1:
+        for j, b in items:
+            _fill_node(spec, M, b, out, j)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda it: _fill_node(spec, M, it[1], out, it[0]), items))
+    out["rows"] = np.asarray(rows, dtype=np.int64)
+    return out

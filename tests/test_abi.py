@@ -137,14 +137,17 @@ def test_struct_layouts_match_the_header(tmp_path):
 #include <stdio.h>
 #include "specv.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(specv_verify_args),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n",
+         sizeof(specv_verify_args),
          offsetof(specv_verify_args, target_logits), offsetof(specv_verify_args, draft_tokens),
          offsetof(specv_verify_args, row_status), sizeof(specv_ssd_args),
          offsetof(specv_ssd_args, keys), sizeof(specv_predict_args),
          offsetof(specv_predict_args, row_status), offsetof(specv_ssd_args, fanout),
          offsetof(specv_predict_args, fanout), offsetof(specv_ssd_args, saguaro_C),
          sizeof(specv_saguaro_args), offsetof(specv_saguaro_args, C),
-         offsetof(specv_saguaro_args, row_status));
+         offsetof(specv_saguaro_args, row_status), sizeof(specv_mss_args),
+         offsetof(specv_mss_args, candidates), offsetof(specv_mss_args, flags),
+         offsetof(specv_mss_args, row_status));
   return 0;
 }
 ''')
@@ -157,7 +160,8 @@ int main(void) {
             sv.PredictArgs.row_status.offset, sv.SsdArgs.fanout.offset,
             sv.PredictArgs.fanout.offset, sv.SsdArgs.saguaro_C.offset,
             ctypes.sizeof(sv.SaguaroArgs), sv.SaguaroArgs.C.offset,
-            sv.SaguaroArgs.row_status.offset]
+            sv.SaguaroArgs.row_status.offset, ctypes.sizeof(sv.MssArgs),
+            sv.MssArgs.candidates.offset, sv.MssArgs.flags.offset, sv.MssArgs.row_status.offset]
     assert got == want
 
 
@@ -277,3 +281,26 @@ def test_saguaro_arguments_are_checked(lib):
     assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
     s = sv.SsdArgs(_args(draft_batch_stride=400), 6, 0x10000, 0, 0x10000, None, 3, 1.5)
     assert lib.specv_ssd_round(ctypes.byref(s), ctypes.c_void_p(0x100000), 1 << 20, None) == sv.SPECV_ERR_INVALID_ARG
+
+
+def test_mss_arguments_are_checked(lib):
+    P = 0x10000
+    base = sv.MssArgs(4, 3, 100, sv.SPECV_FP32, P, 100, P, 100, P, None, P, P, 0, P, P, None, None)
+    for field, val in (("M", 0), ("M", 33), ("V", 0), ("dtype", 9), ("flags", 2),
+                       ("target_logits", None), ("draft_logits", None), ("candidates", None),
+                       ("uniforms", None), ("accepted", None), ("out_token", None),
+                       ("target_row_stride", 99), ("draft_row_stride", 99),
+                       ("candidates", 0x10002), ("num_candidates", 0x10002)):
+        a = sv.MssArgs.from_buffer_copy(base)
+        setattr(a, field, val)
+        assert lib.specv_mss_verify(ctypes.byref(a), ctypes.c_void_p(0x100000), 1 << 20,
+                                    None) == sv.SPECV_ERR_INVALID_ARG, field
+    a = sv.MssArgs.from_buffer_copy(base)
+    assert lib.specv_mss_verify(ctypes.byref(a), None, 0, None) == sv.SPECV_ERR_WORKSPACE
+    assert lib.specv_mss_workspace_bytes(4, 3, 100, sv.SPECV_FP32) > 0
+    assert lib.specv_mss_workspace_bytes(4, 0, 100, sv.SPECV_FP32) == 0
+    a.B = 0
+    assert lib.specv_mss_verify(ctypes.byref(a), None, 0, None) == sv.SPECV_OK
+    a.flags = sv.SPECV_MSS_NAIVE
+    assert lib.specv_mss_verify(ctypes.byref(a), None, 0, None) == sv.SPECV_OK
+    assert lib.specv_mss_verify(None, None, 0, None) == sv.SPECV_ERR_INVALID_ARG
