@@ -7,11 +7,12 @@ accept probability lies within ACC_TOL of its uniform (the library forms
 p_j(x_j)/q(x_j) = max(0, t_j - c_j) / D_j from fp32 logits, the oracle
 p_j by fp64 arrays); accept probabilities within ACC_TOL.
 
-ACC_TOL: t_j = p(x_j)/q(x_j) comes from fp32 logits with a few ulps of
-error (relative 1e-7), c_j and D_j are float-float sums of fp32 terms
-(relative 1e-7), so |delta a_j| <= 1e-7 (t_j + c_j + a_j D_j) / D_j, below
-2e-5 while t_j, c_j <= 10 and D_j >= 0.1, as on these workloads' nodes
-(measured: below 3e-6).
+ACC_TOL = 1e-5, the bar for probabilities: t_j = p(x_j)/q(x_j) comes from
+fp32 logits with a few ulps of error (relative 1e-7), c_j and D_j are
+float-float sums of fp32 terms (relative 1e-7), so |delta a_j| <= 1e-7
+(t_j + c_j + a_j D_j) / D_j, below 1e-5 while t_j, c_j <= 10 and D_j >= 0.2
+(measured: below 3e-6).  A uniform within ACC_TOL of a_j may decide either
+way, like a boundary row.
 """
 import numpy as np
 import pytest
@@ -47,7 +48,7 @@ def to_dev(a, bf16=False):
     return t.cuda()
 
 
-ACC_TOL = 2e-5
+ACC_TOL = 1e-5
 
 
 def run_pair(sv, olib, data, bf16, naive=False, num_candidates=None):
@@ -150,16 +151,17 @@ def test_mss_counts_and_bad_inputs(sv, olib):
 
 
 def test_mss_cfg5_sizes_sampled(sv, olib):
-    """Config 5 distributions (V = 152064 fp32, zipf logits, T = 1): 512
-    nodes with three candidates; 24 sampled nodes against the oracle."""
+    """The benchmark's MSS workload (2048 nodes, three candidates, V = 152064
+    fp32, config 5 logits, T = 1) in the launch configuration bench.py
+    times; 32 sampled nodes against the oracle."""
     spec = wl.SPECS["cfg5"]
-    data = wl.generate_mss(spec, 3, B=512)
+    data = wl.generate_mss(spec, 3, B=2048)
     g = sv.specv_mss_verify(to_dev(data["target"]), to_dev(data["draft"]),
                             to_dev(data["candidates"]), to_dev(data["temperature"]),
                             to_dev(data["uniforms"]))
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in g.items()}
-    rows = np.random.default_rng(7).choice(512, 24, replace=False)
+    rows = np.random.default_rng(7).choice(2048, 32, replace=False)
     sub = {k: data[k][rows] for k in ("target", "draft", "candidates", "temperature", "uniforms")}
     o = oracle.mss(sub["target"], sub["draft"], sub["candidates"], sub["temperature"],
                    sub["uniforms"], nthreads=0, lib=olib)
