@@ -767,7 +767,7 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
 // Register path (VEC = false: any layout) or staged path (VEC = true: 16-byte
 // aligned rows, P.stages stages of dynamic shared memory); one CTA per item.
 template <int DT, bool VEC, int MODE>
-__global__ void __launch_bounds__(kThreads, DT == 0 ? 3 : 4) stats_kernel(const StatsParams P) {
+__global__ void __launch_bounds__(kThreads, DT == 0 ? 4 : 5) stats_kernel(const StatsParams P) {
   constexpr bool kT = mode_has_target(MODE);
   constexpr bool kTopF = mode_has_topf(MODE);
   __shared__ EpiSmem S;
