@@ -609,9 +609,12 @@ __device__ __forceinline__ int ring_trips(int nv) {
 // Copies trip t of chunk C into stage s, completing on `full`.  Whole 16-byte
 // units only (the consumers load a ragged tail themselves); the expected byte
 // count is armed even when nothing is copied, so the phase completes anyway.
+// A stage holds the trip of both rows (target at +0, draft at +kTripBytes);
+// with `one` (a chunk of a single row) stages are kTripBytes apart and hold
+// that row alone, so the same ring carries twice as many trips.
 template <int DT>
 __device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, int s, int t,
-                                           const Chunk& C) {
+                                           const Chunk& C, bool one = false) {
   using E = Elem<DT>;
   const int64_t off = static_cast<int64_t>(t) * kTripBytes;
   int64_t bytes = (C.v1 - C.v0) * E::ES - off;
@@ -621,10 +624,14 @@ __device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, 
   const uint32_t nrows = (C.rowt ? 1u : 0u) + (C.rowd ? 1u : 0u);
   mbar_arrive_expect_tx(full, b32 * nrows);
   if (b32) {
-    unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
     const int64_t src = C.v0 * E::ES + off;
-    if (C.rowt) bulk_load(base, C.rowt + src, b32, full);
-    if (C.rowd) bulk_load(base + kTripBytes, C.rowd + src, b32, full);
+    if (one) {
+      bulk_load(ring + static_cast<int64_t>(s) * kTripBytes, (C.rowt ? C.rowt : C.rowd) + src, b32, full);
+    } else {
+      unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
+      if (C.rowt) bulk_load(base, C.rowt + src, b32, full);
+      if (C.rowd) bulk_load(base + kTripBytes, C.rowd + src, b32, full);
+    }
   }
 }
 
@@ -632,7 +639,7 @@ __device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, 
 // copied part of the chunk: no bounds checks (the common case).
 template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ void consume_stage_whole(const unsigned char* base, int t, const Chunk& C,
-                                                    float c, Acc<Elem<DT>::VW>& A) {
+                                                    float c, Acc<Elem<DT>::VW>& A, int doff) {
   using E = Elem<DT>;
   using Vec = typename E::Vec;
   constexpr int VW = E::VW;
@@ -650,7 +657,7 @@ __device__ __forceinline__ void consume_stage_whole(const unsigned char* base, i
   }
   if (C.rowd) {
     float z[N];
-    const Vec* src = reinterpret_cast<const Vec*>(base + kTripBytes);
+    const Vec* src = reinterpret_cast<const Vec*>(base + doff);
 #pragma unroll
     for (int k = 0; k < kVecs; ++k) put_vec<DT>(z + k * VW, src[k * kThreads + threadIdx.x]);
     A.template add<GREEDY, true, TOPF>(z, b, c, t);
@@ -668,7 +675,8 @@ __device__ __forceinline__ int whole_trips(const Chunk& C, int64_t covered) {
 // logit not copied) is gathered from global memory instead.
 template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ void consume_stage(const unsigned char* base, int t, const Chunk& C,
-                                              int64_t covered, float c, Acc<Elem<DT>::VW>& A) {
+                                              int64_t covered, float c, Acc<Elem<DT>::VW>& A,
+                                              int doff) {
   using E = Elem<DT>;
   using Vec = typename E::Vec;
   constexpr int VW = E::VW;
@@ -679,7 +687,7 @@ __device__ __forceinline__ void consume_stage(const unsigned char* base, int t, 
   for (int k = 0; k < kVecs; ++k) b[k] = static_cast<int32_t>(C.v0) + (j0 + k * kThreads) * VW;
   // Whole trip in shared memory: the common case, no per-vector checks.
   const bool whole = C.v0 + static_cast<int64_t>(j0 + (kVecs - 1) * kThreads + 1) * VW <= covered;
-  if (KT) {
+  if (KT && C.rowt) {
     float z[N];
     const Vec* src = reinterpret_cast<const Vec*>(base);
 #pragma unroll
@@ -694,7 +702,7 @@ __device__ __forceinline__ void consume_stage(const unsigned char* base, int t, 
   }
   if (C.rowd) {
     float z[N];
-    const Vec* src = reinterpret_cast<const Vec*>(base + kTripBytes);
+    const Vec* src = reinterpret_cast<const Vec*>(base + doff);
 #pragma unroll
     for (int k = 0; k < kVecs; ++k) {
       const int j = j0 + k * kThreads;
@@ -718,14 +726,20 @@ __device__ __forceinline__ int64_t covered_end(const Chunk& C) {
 // false (on every thread) if a wait gave up; the copies then in flight get a
 // bounded wait before returning.
 template <int DT, bool GREEDY, bool KT, bool TOPF>
-__device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* ring, int S,
+__device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* ring, int S2,
                                                     const Chunk& C, float c, Acc<Elem<DT>::VW>& A) {
   const int ntr = ring_trips(C.nv);
   const int64_t covered = covered_end<DT>(C);
+  // A chunk of a single row (a draft row alone, or a target row with no
+  // draft) splits each two-row stage in two: twice the trips in flight.
+  const bool one = !(C.rowt && C.rowd);
+  const int S = one ? min(2 * S2, kMaxStages) : S2;
+  const int64_t sb = one ? kTripBytes : 2 * kTripBytes;  // stage stride
+  const int doff = one ? 0 : kTripBytes;                 // draft row within a stage
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&R.full[s], 1);
     fence_mbar_init();
-    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C);
+    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C, one);
   }
   __syncthreads();
   bool ok = true;
@@ -734,9 +748,9 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
   const int nwhole = whole_trips<DT>(C, covered);
   for (int t = 0; t < ntr; ++t) {
     if (!mbar_wait_bounded(&R.full[s], ph)) ok = false;
-    const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
-    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A);
-    else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A);
+    const unsigned char* base = ring + static_cast<int64_t>(s) * sb;
+    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A, doff);
+    else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A, doff);
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         int s2 = s;
@@ -754,7 +768,7 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
     }
     if (threadIdx.x == 0 && t + S < ntr) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      ring_issue<DT>(&R.full[s], ring, s, t + S, C);
+      ring_issue<DT>(&R.full[s], ring, s, t + S, C, one);
     }
     if (++s == S) {
       s = 0;
@@ -856,8 +870,8 @@ __device__ __forceinline__ bool ring_consume(RingBars& R, const unsigned char* r
       *abort = 1;
     }
     const unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
-    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A);
-    else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A);
+    if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A, kTripBytes);
+    else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A, kTripBytes);
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[s]);
     if (++s == S) {
