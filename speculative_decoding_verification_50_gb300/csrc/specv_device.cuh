@@ -154,16 +154,18 @@ __device__ __forceinline__ void merge_lists(const float (*lv)[kMaxF], const int3
   }
 }
 
-// (max, sum) of a warp's online-softmax partials: the warp max first, then one
-// rescale per lane and a plain sum tree (no exponential per tree step).  The
-// result is in every lane.  Lanes without data hold (kNegMax, 0).
+// (max, sum) of the online-softmax partials of an aligned group of W lanes
+// (the whole warp by default): the group max first, then one rescale per lane
+// and a plain sum tree (no exponential per tree step).  The result is in every
+// lane of the group.  Lanes without data hold (kNegMax, 0).
+template <int W = 32>
 __device__ __forceinline__ void warp_soft_all(float& m, float& s, float c) {
   float M = m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  for (int o = W / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float t = s * ex2((m - M) * c);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  for (int o = W / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
   m = M;
   s = t;
 }

@@ -399,10 +399,10 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
       S.wrec[warp].bt = bt; S.wrec[warp].it = it; S.wrec[warp].bd = bd; S.wrec[warp].id = id;
       S.wrec[warp].bad = bad;
     }
-  } else {
+  } else {  // (a row the chunk does not have keeps its empty statistics)
     float mt = A.st.m, s_t = A.st.total(), md = A.sd.m, s_d = A.sd.total();
-    warp_soft_all(mt, s_t, c);
-    warp_soft_all(md, s_d, c);
+    if (C.rowt) warp_soft_all(mt, s_t, c);
+    if (C.rowd) warp_soft_all(md, s_d, c);
     if (lane == 0) {
       S.wrec[warp].mt = mt; S.wrec[warp].st = s_t; S.wrec[warp].md = md; S.wrec[warp].sd = s_d;
     }
@@ -419,19 +419,30 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     // the eight, and at least F of them are not the excluded token: a lower
     // bound on the chunk's top-F without it.
     float s = A.kd.m1;  // this thread's draft maximum
+    float tw, tf;
+    if (P.F < kWarps) {
+      // g = 1: the warp's largest maximum.  A warp with no finite maximum
+      // (a short chunk) leaves the bound unset and the chunk takes the exact
+      // path below.
 #pragma unroll
-    for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+      for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, o));
+      tw = s;
+      tf = neg_inf();
+    } else {
 #pragma unroll
-      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, s, j2);
-        const bool take_max = ((lane & k2) == 0) == ((lane & j2) == 0);
-        s = take_max ? fmaxf(s, o) : fminf(s, o);
+      for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+#pragma unroll
+        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+          const float o = __shfl_xor_sync(0xffffffffu, s, j2);
+          const bool take_max = ((lane & k2) == 0) == ((lane & j2) == 0);
+          s = take_max ? fmaxf(s, o) : fminf(s, o);
+        }
       }
+      tw = __shfl_sync(0xffffffffu, s, (P.F + kWarps) / kWarps - 1);
+      // Fallback when some warp holds fewer than g finite maxima (a short last
+      // chunk): the largest, over warps, of a warp's (F+1)-th largest maximum.
+      tf = (P.F < 32) ? __shfl_sync(0xffffffffu, s, P.F) : neg_inf();
     }
-    const float tw = __shfl_sync(0xffffffffu, s, (P.F + kWarps) / kWarps - 1);
-    // Fallback when some warp holds fewer than g finite maxima (a short last
-    // chunk): the largest, over warps, of a warp's (F+1)-th largest maximum.
-    const float tf = (P.F < 32) ? __shfl_sync(0xffffffffu, s, P.F) : neg_inf();
     if (lane == 0) {
       S.wthr[warp] = tw;
       S.wthr_f[warp] = tf;
@@ -460,8 +471,8 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
       if (lane < kWarps) {
         mt = S.wrec[lane].mt; s_t = S.wrec[lane].st; md = S.wrec[lane].md; s_d = S.wrec[lane].sd;
       }
-      warp_soft_all(mt, s_t, c);
-      warp_soft_all(md, s_d, c);
+      if (C.rowt) warp_soft_all<kWarps>(mt, s_t, c);
+      if (C.rowd) warp_soft_all<kWarps>(md, s_d, c);
       r.mt = mt; r.st = s_t; r.md = md; r.sd = s_d;
     }
     if (copy_bad) r.bad |= 2;
