@@ -290,8 +290,6 @@ constexpr int kCandCap = 512;  // candidates one CTA ranks at once
 struct KeyScratch {  // shared-memory scratch of a chunk's top-F selection
   float v[kCandCap];   // qualifying candidates, unordered
   int32_t i[kCandCap];
-  float out_v[kMaxF];  // the top-F, in key order
-  int32_t out_i[kMaxF];
   int count;           // candidates pushed (may pass kCandCap)
 };
 

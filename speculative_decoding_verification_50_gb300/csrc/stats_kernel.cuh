@@ -356,6 +356,13 @@ __device__ __forceinline__ Chunk chunk_at(const StatsParams& P, int64_t item) {
   return C;
 }
 
+// The draft token sent for verification at the chunk's position, excluded
+// from its outcome keys (none at position K, or without candidates).
+template <int MODE>
+__device__ __forceinline__ int excluded_token(const StatsParams& P, const Chunk& C) {
+  return (mode_has_topf(MODE) && C.i < P.K) ? P.tokens[static_cast<int64_t>(C.b) * P.K + C.i] : -1;
+}
+
 // Shared scratch of a chunk's epilogue.
 struct EpiSmem {
   ChunkRec wrec[kWarps];
@@ -383,7 +390,7 @@ __device__ __forceinline__ void push_key(KeyScratch& KS, float v, int32_t i) {
 template <int DT, bool VEC, int MODE>
 __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& C, int64_t item,
                                              bool greedy, float c, Acc<Elem<DT>::VW>& A, bool ok,
-                                             EpiSmem& S) {
+                                             EpiSmem& S, int excl) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   constexpr bool kTopF = mode_has_topf(MODE);
@@ -409,10 +416,6 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
   }
   if (kTopF) {
     if (threadIdx.x == 0) S.KS.count = 0;
-    if (threadIdx.x < P.F) {
-      S.KS.out_v[threadIdx.x] = neg_inf();
-      S.KS.out_i[threadIdx.x] = INT_MAX;
-    }
     // Bound: with g = ceil((F+1)/8), every warp holds g distinct logits at or
     // above its g-th largest per-thread maximum (bitonic sort of the 32
     // maxima), so at least 8g >= F+1 distinct logits reach the smallest of
@@ -490,7 +493,6 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     // qualifiers (ties at the bound), or no finite bound at all (masked rows,
     // chunks with fewer than F+1 finite logits), take the exact warp-list path.
     const int F = P.F;
-    const int excl = (C.i < P.K) ? P.tokens[static_cast<int64_t>(C.b) * P.K + C.i] : -1;
     float thr = S.wthr[0], thr_f = S.wthr_f[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) {
@@ -549,20 +551,21 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     float* outv = P.cand_v + item * F;
     int32_t* outi = P.cand_i + item * F;
     if (m <= kCandCap) {
+      // distinct indices: the ranks are 0..m-1, each written once; slots
+      // m..F-1 (fewer candidates than F) are padded
       for (int e = threadIdx.x; e < m; e += kThreads) {
         const float v = S.KS.v[e];
         const int32_t ii = S.KS.i[e];
         int rank = 0;
         for (int o = 0; o < m; ++o) rank += key_beats(S.KS.v[o], S.KS.i[o], v, ii);
         if (rank < F) {
-          S.KS.out_v[rank] = v;
-          S.KS.out_i[rank] = ii;
+          outv[rank] = v;
+          outi[rank] = ii;
         }
       }
-      cons_sync();
-      if (threadIdx.x < F) {
-        outv[threadIdx.x] = S.KS.out_v[threadIdx.x];
-        outi[threadIdx.x] = S.KS.out_i[threadIdx.x];
+      if (threadIdx.x >= m && threadIdx.x < F) {
+        outv[threadIdx.x] = neg_inf();
+        outi[threadIdx.x] = INT_MAX;
       }
     } else {
       WarpTopF L;
@@ -801,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 4 : 5) stats_kernel(const 
   const float T = mode_has_temp(MODE) ? P.temp[C.b] : 0.f;
   const bool greedy = !mode_has_temp(MODE) || T == 0.f;
   const float c = greedy ? 1.f : temp_scale(T);
+  const int excl = excluded_token<MODE>(P, C);  // fetched now, used by the epilogue
   Acc<Elem<DT>::VW> A;
   A.init();
   bool ok = true;
@@ -816,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 4 : 5) stats_kernel(const 
     stream_chunk<DT, false, false, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
                                               P.iters, c, A);
   }
-  chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S);
+  chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S, excl);
 }
 
 // ---- persistent path ------------------------------------------------------------
@@ -926,7 +930,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) stats_ring_kernel(const Stats
     A.init();
     const bool ok = greedy ? ring_consume<DT, true, kT, kTopF>(R, ring, P.stages, s, ph, C, c, A)
                            : ring_consume<DT, false, kT, kTopF>(R, ring, P.stages, s, ph, C, c, A);
-    chunk_finish<DT, true, MODE>(P, C, item, greedy, c, A, ok, S);
+    chunk_finish<DT, true, MODE>(P, C, item, greedy, c, A, ok, S, excluded_token<MODE>(P, C));
   }
 }
 
