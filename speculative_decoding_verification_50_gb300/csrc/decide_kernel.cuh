@@ -407,7 +407,7 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
   return ok;
 }
 
-constexpr int kDrawTiles = 8 * kVecs;  // 256-vector tiles in the longest chunk (8 trips)
+constexpr int kDrawTiles = 16 * kVecs;  // 256-vector tiles in the longest chunk (16 trips)
 static_assert(kDrawTiles <= 32, "one lane per tile");
 
 struct DrawSmem {
@@ -508,9 +508,8 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
     }
   };
   auto rvals = [&](int j, float (&r)[VW]) { rfrom(load_vec<DT, VEC>(row, e0, e1, j), j, r); };
-  constexpr int kBatch = 4;
-#pragma unroll
-  for (int h = 0; h < kDrawTiles; h += kBatch) {
+  constexpr int kBatch = 4;  // (8 spills registers elsewhere in the kernel)
+  for (int h = 0; h < ntile; h += kBatch) {
     typename E::Vec raw[kBatch];
 #pragma unroll
     for (int q = 0; q < kBatch; ++q) {
