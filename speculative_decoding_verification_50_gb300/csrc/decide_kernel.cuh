@@ -1081,39 +1081,44 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
 
     // ---- owner CTA: locate the crossing segment, then scan it --------------
     if (rank == dec.owner && warp == 0) {
-      // lanes own contiguous blocks of segments; a warp scan of the block sums
-      // finds the block that holds the crossing, whose lane walks it
+      // lanes own contiguous blocks of segments; a float-float warp scan of
+      // the block sums finds the block that holds the crossing.  Inside it
+      // the walk runs in fp32, relative to the block's start: U*R less the
+      // mass before the block, rounded once, against the same additions that
+      // formed the block sum (so a crossing found by the scan is found again,
+      // and what rounding can move lies within a few ulps of the block's mass)
       const int nseg = ntl * kWarps;
       const FF tau = dec.tau;
       const int per = (nseg + 31) / 32;
       const int s0 = min(nseg, lane * per), s1 = min(nseg, s0 + per);
-      FF bsum = ff(0.f);
+      float bsum = 0.f;
       int lastpos = -1;
       for (int sg = s0; sg < s1; ++sg) {
         const float g = segs[sg];
         if (g > 0.f) {
-          bsum = ff_add(bsum, g);
+          bsum += g;
           lastpos = sg;
         }
       }
-      const FF incl = warp_ffscan(bsum, lane);
-      const FF bpre = ff_add(dec.pre_mine, ff_add(incl, ff_neg(bsum)));
+      const FF incl = warp_ffscan(ff(bsum), lane);
+      const FF bpre = ff_add(dec.pre_mine, ff_add(incl, -bsum));
       const unsigned hitm = dec.last_pos ? 0u
-                                         : __ballot_sync(0xffffffffu, bsum.hi > 0.f && ff_gt(ff_add(bpre, bsum), tau));
+                                         : __ballot_sync(0xffffffffu, bsum > 0.f && ff_gt(ff_add(bpre, bsum), tau));
       const unsigned posm = __ballot_sync(0xffffffffu, lastpos >= 0);
       int seg = -1;
-      FF cum_at = ff(0.f);
+      float tseg = 0.f;  // U*R less the mass before the chosen segment
       if (hitm) {
         const int L = __ffs(hitm) - 1;
         if (lane == L) {
-          FF cum = bpre;
+          const float t = ff_add(tau, ff_neg(bpre)).hi;
+          float cum = 0.f;
           for (int sg = s0; sg < s1; ++sg) {
             const float g = segs[sg];
             if (g > 0.f) {
-              const FF nx = ff_add(cum, g);
-              if (ff_gt(nx, tau)) {
+              const float nx = cum + g;
+              if (nx > t) {
                 seg = sg;
-                cum_at = cum;
+                tseg = t - cum;
                 break;
               }
               cum = nx;
@@ -1122,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
           if (seg < 0) seg = lastpos;  // rounding inside the block
         }
         seg = __shfl_sync(0xffffffffu, seg, L);
-        cum_at = shfl(cum_at, L);
+        tseg = __shfl_sync(0xffffffffu, tseg, L);
       }
       const int lastseg = posm ? __shfl_sync(0xffffffffu, lastpos, 31 - __clz(posm)) : -1;
       bool lp = dec.last_pos || seg < 0;
@@ -1138,22 +1143,28 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
       int found = -1;
       float rv = 0.f;  // r at the found logit (the sampler reports it as sigma(t))
       if (!lp) {
+        // the segment's 32 vectors: an fp32 scan relative to the segment start
         float vs = 0.f;
 #pragma unroll
         for (int k = 0; k < VW; ++k) vs += r[k];
-        const FF incl = warp_ffscan(ff(vs), lane);
-        const FF excl_sum = ff_add(incl, -vs);
-        const unsigned m = __ballot_sync(0xffffffffu, vs > 0.f && ff_gt(ff_add(cum_at, incl), tau));
+        float inc = vs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        const float exc = __shfl_up_sync(0xffffffffu, inc, 1);
+        const unsigned m = __ballot_sync(0xffffffffu, vs > 0.f && inc > tseg);
         if (m) {
           if (lane == __ffs(m) - 1) {
-            FF run = ff_add(cum_at, excl_sum);
+            float run = lane > 0 ? exc : 0.f;
             int kk = -1, klast = -1;
 #pragma unroll
             for (int k = 0; k < VW; ++k) {
               if (r[k] > 0.f) {
-                run = ff_add(run, r[k]);
+                run += r[k];
                 klast = k;
-                if (kk < 0 && ff_gt(run, tau)) kk = k;
+                if (kk < 0 && run > tseg) kk = k;
               }
             }
             const int ksel = kk >= 0 ? kk : klast;
