@@ -414,7 +414,7 @@ struct DrawSmem {
   float tile[kDrawTiles][kWarps];  // per-warp sums of r in each tile of the chunk
   FF R;        // the row's total mass
   FF tau_in;   // U * R less the mass before the chosen chunk
-  FF before;   // the chunk's mass before the chosen warp of the chosen tile
+  float tw;    // U * R less the mass before the chosen warp of the chosen tile
   int32_t pick;    // the chunk, then the token, holding U * R
   int32_t tsel;    // the tile holding it
   int32_t wsel;    // the warp of that tile holding it
@@ -531,37 +531,39 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
     }
   }
   __syncthreads();
-  // ---- warp 0: lane i sums tile i; a scan over tiles, then a walk over the
-  // chosen tile's warps, locates the 32 vectors holding U * R -----------------
+  // ---- warp 0: lane i sums tile i; a float-float scan over tiles, then an
+  // fp32 walk over the chosen tile's warps relative to the tile's start (the
+  // same additions that formed the tile sum), locates the 32 vectors holding
+  // U * R -----------------------------------------------------------------
   if (warp == 0) {
     const FF tin = S.tau_in;
     const bool fb = S.fallback != 0;
-    FF ti = ff(0.f);
+    float ti = 0.f;
     if (lane < ntile)
 #pragma unroll
-      for (int w2 = 0; w2 < kWarps; ++w2) ti = ff_add(ti, S.tile[lane][w2]);
-    const FF incl = warp_ffscan(ti, lane);
-    const unsigned hit = fb ? 0u : __ballot_sync(0xffffffffu, ti.hi > 0.f && ff_gt(incl, tin));
-    const unsigned pos = __ballot_sync(0xffffffffu, ti.hi > 0.f);
+      for (int w2 = 0; w2 < kWarps; ++w2) ti += S.tile[lane][w2];
+    const FF incl = warp_ffscan(ff(ti), lane);
+    const unsigned hit = fb ? 0u : __ballot_sync(0xffffffffu, ti > 0.f && ff_gt(incl, tin));
+    const unsigned pos = __ballot_sync(0xffffffffu, ti > 0.f);
     const bool last = hit == 0;
     const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
     if (lane == sel) {
-      FF run = ff_add(incl, ff_neg(ti));
+      const float t = ff_add(tin, ff_neg(ff_add(incl, -ti))).hi;  // relative to the tile's start
+      float run = 0.f, wb = 0.f;
       int ws = -1;
-      FF wb = run;
       for (int w2 = 0; w2 < kWarps; ++w2) {
         const float g = S.tile[lane][w2];
+        const float nx = run + g;
         if (g > 0.f) {
-          const FF nx = ff_add(run, g);
           ws = w2;
           wb = run;
-          if (!last && ff_gt(nx, tin)) break;
-          run = nx;
+          if (!last && nx > t) break;
         }
+        run = nx;
       }
       S.tsel = ws >= 0 ? lane : -1;
       S.wsel = ws;
-      S.before = wb;
+      S.tw = t - wb;
       S.fallback = last ? 1 : 0;
     }
     if (lane == 0 && sel < 0) S.tsel = -1;
@@ -580,22 +582,28 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
     float vs = 0.f;
 #pragma unroll
     for (int k = 0; k < VW; ++k) vs += r[k];
-    const FF tin = S.tau_in;
+    const float tw = S.tw;  // relative to the warp's first vector of the tile
     const bool fb = S.fallback != 0;
-    const FF incl = ff_add(S.before, warp_ffscan(ff(vs), lane));
-    const unsigned hit = fb ? 0u : __ballot_sync(0xffffffffu, vs > 0.f && ff_gt(incl, tin));
+    float inc = vs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const float exc = __shfl_up_sync(0xffffffffu, inc, 1);
+    const unsigned hit = fb ? 0u : __ballot_sync(0xffffffffu, vs > 0.f && inc > tw);
     const unsigned pos = __ballot_sync(0xffffffffu, vs > 0.f);
     const bool lastel = hit == 0;  // past the end, or rounding inside the tile
     const int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
     if (lane == sel) {
-      FF run = ff_add(incl, -vs);
+      float run = lane > 0 ? exc : 0.f;
       int kk = -1, kl = -1;
 #pragma unroll
       for (int k = 0; k < VW; ++k)
         if (r[k] > 0.f) {
-          run = ff_add(run, r[k]);
+          run += r[k];
           kl = k;
-          if (!lastel && kk < 0 && ff_gt(run, tin)) kk = k;
+          if (!lastel && kk < 0 && run > tw) kk = k;
         }
       const int ksel = kk >= 0 ? kk : kl;  // rounding within the vector: its last r > 0
       float rt = 0.f;
