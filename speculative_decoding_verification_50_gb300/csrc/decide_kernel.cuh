@@ -88,6 +88,7 @@ struct DecideParams {
   int32_t sg_F;      // Saguaro sampling: the drafts came from sigma_{sg_F, sg_C}
   float sg_C;        //   (0: plain softmax drafts); the sampler's own F and C
   int32_t local_draw;  // draws from a whole row read only the chunk holding U * R
+  int32_t half;        // the sampler's records carry each chunk's first half apart
   // MSS (K = M candidates per node, one target and one draft row each)
   const int32_t* ncand;  // per-node candidate counts, or null (all M)
   int32_t naive;         // naive sampling: one draw from p, candidates matched to it
@@ -435,21 +436,32 @@ struct DrawSmem {
 template <int DT, bool VEC>
 __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V, bool draft_fields,
                           float M, float c, const char* row, float U, const float* kv,
-                          const int32_t* ki, int nk, const SgW& w, DrawSmem& S) {
+                          const int32_t* ki, int nk, const SgW& w, bool halves, DrawSmem& S) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  // With halves the records also carry each chunk's first half (the sampler's
+  // chunks, in the target fields): the draw then locates and reads a half.
+  const int nloc = halves ? 2 * nchunk : nchunk;
+  const int32_t span = halves ? chunk / 2 : chunk;  // logits per located piece
   // ---- warp 0: chunk masses, lanes over contiguous blocks of chunks --------
   if (warp == 0) {
     const FF one_m_c = two_sum(1.f, -w.C);
-    const int per = (nchunk + 31) / 32;
-    const int j0 = min(nchunk, lane * per), j1 = min(nchunk, j0 + per);
+    const int per = (nloc + 31) / 32;
+    const int j0 = min(nloc, lane * per), j1 = min(nloc, j0 + per);
     auto mass = [&](int j) -> FF {
-      const ChunkRec r = recs[j];
-      const float m = draft_fields ? r.md : r.mt, sm = draft_fields ? r.sd : r.st;
-      FF x = ff_mul(sm, ex2((m - M) * c));
-      for (int k = 0; k < nk; ++k)  // the weighted keys of this chunk
-        if (ki[k] / chunk == j) x = ff_add(x, ff_neg(ff_mul(one_m_c, ex2((kv[k] - M) * c))));
+      FF x;
+      if (halves) {  // piece j is half j % 2 of chunk j / 2; the second is the rest
+        const ChunkRec r = recs[j >> 1];
+        const FF first = ff_mul(r.st, ex2((r.mt - M) * c));
+        x = (j & 1) ? ff_add(ff_mul(r.sd, ex2((r.md - M) * c)), ff_neg(first)) : first;
+      } else {
+        const ChunkRec r = recs[j];
+        const float m = draft_fields ? r.md : r.mt, sm = draft_fields ? r.sd : r.st;
+        x = ff_mul(sm, ex2((m - M) * c));
+      }
+      for (int k = 0; k < nk; ++k)  // the weighted keys of this piece
+        if (ki[k] / span == j) x = ff_add(x, ff_neg(ff_mul(one_m_c, ex2((kv[k] - M) * c))));
       return x.hi > 0.f ? x : ff(0.f);
     };
     FF mine = ff(0.f);
@@ -495,7 +507,7 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
   // ---- every thread: vector t of each 256-vector tile of the chunk, loaded
   // in batches of four per thread (each batch held in registers until it
   // lands); per-warp sums of r per tile --------------------------------------
-  const int64_t e0 = static_cast<int64_t>(jc) * chunk, e1 = min(static_cast<int64_t>(V), e0 + chunk);
+  const int64_t e0 = static_cast<int64_t>(jc) * span, e1 = min(static_cast<int64_t>(V), e0 + span);
   const int nvc = static_cast<int>((e1 - e0 + VW - 1) / VW);
   const int ntile = (nvc + kThreads - 1) / kThreads;  // <= kDrawTiles (the caller checks)
   auto rfrom = [&](const typename E::Vec& v, int j, float (&r)[VW]) {
@@ -955,7 +967,8 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     const int tok = chunk_draw<DT, VEC>(P.recs + (u0 + nn) * P.nchunk, P.nchunk, P.chunk, P.V,
                                         kSample, dec.mt, c, row,
                                         P.unif[L.u_off + u_draw], sg_kv, sg_ki,
-                                        (kSample && sg_on) ? sg_nk : 0, w, draw);
+                                        (kSample && sg_on) ? sg_nk : 0, w, kSample && P.half > 0,
+                                        draw);
     if (threadIdx.x == 0) {
       tok_slot = tok;
       q_slot = draw.q;

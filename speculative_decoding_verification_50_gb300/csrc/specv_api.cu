@@ -416,6 +416,10 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.chunk = static_cast<int32_t>(pl.chunk);
   sp.iters = pl.iters;
   sp.stages = ring_stages();
+  // The sampler's staged chunks record their first half apart, so its draw
+  // reads half a chunk (two equal halves: an even trip count).
+  sp.half = (mode == kModeSample && vec && !persistent_path() && pl.iters >= 2 && pl.iters % 2 == 0)
+                ? pl.iters / 2 : 0;
   sp.cu = a->cu_num_draft_tokens;
   sp.ntok = a->num_draft_tokens;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -467,6 +471,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   }
   const bool fits = pl.chunk <= static_cast<int64_t>(kDrawTiles) * kThreads * vec_width(a->dtype);
   dp.local_draw = fits && (env_local >= 0 ? env_local != 0 : pl.chunk < pl.L);
+  dp.half = sp.half;
   for (int k = 0; k <= K; ++k) dp.fk[k] = fanout ? fanout[k] : F;
   // Aligned rows stream the residual slice through a ring placed after the
   // segment sums in dynamic shared memory.

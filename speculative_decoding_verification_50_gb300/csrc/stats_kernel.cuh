@@ -51,7 +51,9 @@ constexpr int kMaxStages = 8;
 constexpr int kTripBytes = kVecs * kThreads * 16;  // one row's share of a trip (8 KB)
 
 struct ChunkRec {        // 48 bytes per (unit, chunk)
-  float mt, st, md, sd;  // temperature rows: max and sum of 2^((z-max)c)
+  float mt, st, md, sd;  // temperature rows: max and sum of 2^((z-max)c); a
+                         // sampler chunk split in halves keeps its first
+                         // half's draft statistics in mt, st
   float bt, bd;          // greedy rows: best logit
   int32_t it, id;        // greedy rows: first index of the best logit
   int32_t bad;           // bit 0: NaN or +inf seen in a greedy row (T > 0: shows
@@ -72,6 +74,7 @@ struct StatsParams {
   int32_t* cand_i;
   int32_t B, K, V, F, nchunk, chunk, iters;  // chunk = iters * kVecs * 256 * VW logits
   int32_t stages;     // ring stages of the staged paths, 2..kMaxStages
+  int32_t half;       // sampler rows: trips in a chunk's first half, recorded apart (0: none)
   const int32_t* cu;  // per-row draft counts (inclusive prefix sums), or null
   int32_t ntok;       // with cu: packed draft rows the buffers hold
 };
@@ -390,7 +393,7 @@ __device__ __forceinline__ void push_key(KeyScratch& KS, float v, int32_t i) {
 template <int DT, bool VEC, int MODE>
 __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& C, int64_t item,
                                              bool greedy, float c, Acc<Elem<DT>::VW>& A, bool ok,
-                                             EpiSmem& S, int excl) {
+                                             EpiSmem& S, int excl, const float2* snap = nullptr) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   constexpr bool kTopF = mode_has_topf(MODE);
@@ -408,7 +411,15 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     }
   } else {  // (a row the chunk does not have keeps its empty statistics)
     float mt = A.st.m, s_t = A.st.total(), md = A.sd.m, s_d = A.sd.total();
-    if (C.rowt) warp_soft_all(mt, s_t, c);
+    if (snap) {  // the draft's first half in the target slots, the whole chunk in the draft's
+      const float2 h = snap[threadIdx.x];
+      mt = h.x;
+      s_t = h.y;
+      const float M = fmaxf(mt, md);
+      s_d = s_t * ex2((mt - M) * c) + s_d * ex2((md - M) * c);
+      md = M;
+    }
+    if (C.rowt || snap) warp_soft_all(mt, s_t, c);
     if (C.rowd) warp_soft_all(md, s_d, c);
     if (lane == 0) {
       S.wrec[warp].mt = mt; S.wrec[warp].st = s_t; S.wrec[warp].md = md; S.wrec[warp].sd = s_d;
@@ -474,7 +485,7 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
       if (lane < kWarps) {
         mt = S.wrec[lane].mt; s_t = S.wrec[lane].st; md = S.wrec[lane].md; s_d = S.wrec[lane].sd;
       }
-      if (C.rowt) warp_soft_all<kWarps>(mt, s_t, c);
+      if (C.rowt || snap) warp_soft_all<kWarps>(mt, s_t, c);
       if (C.rowd) warp_soft_all<kWarps>(md, s_d, c);
       r.mt = mt; r.st = s_t; r.md = md; r.sd = s_d;
     }
@@ -739,9 +750,13 @@ __device__ __forceinline__ int64_t covered_end(const Chunk& C) {
 // refills a stage after the CTA barrier that closes its consumption.  Returns
 // false (on every thread) if a wait gave up; the copies then in flight get a
 // bounded wait before returning.
+// half > 0: after `half` trips the draft row's running statistics move to
+// snap[threadIdx.x] and start again, so the chunk's first half is recorded
+// apart (all of it if the chunk is that short).
 template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* ring, int S2,
-                                                    const Chunk& C, float c, Acc<Elem<DT>::VW>& A) {
+                                                    const Chunk& C, float c, Acc<Elem<DT>::VW>& A,
+                                                    int half = 0, float2* snap = nullptr) {
   const int ntr = ring_trips(C.nv);
   const int64_t covered = covered_end<DT>(C);
   // A chunk of a single row (a draft row alone, or a target row with no
@@ -765,6 +780,10 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
     const unsigned char* base = ring + static_cast<int64_t>(s) * sb;
     if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A, doff);
     else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A, doff);
+    if (!GREEDY && half > 0 && t + 1 == half) {
+      snap[threadIdx.x] = make_float2(A.sd.m, A.sd.total());
+      A.sd.init();
+    }
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         int s2 = s;
@@ -789,6 +808,10 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
       ph ^= 1u;
     }
   }
+  if (!GREEDY && half > 0 && ntr < half) {  // a short chunk: all of it is the first half
+    snap[threadIdx.x] = make_float2(A.sd.m, A.sd.total());
+    A.sd.init();
+  }
   return ok;
 }
 
@@ -808,11 +831,15 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 4 : 5) stats_kernel(const 
   Acc<Elem<DT>::VW> A;
   A.init();
   bool ok = true;
+  // the sampler's chunks may record their first half apart (staged path)
+  __shared__ float2 snap[MODE == kModeSample ? kThreads : 1];
+  const bool halves = MODE == kModeSample && VEC && !greedy && P.half > 0;
   if (VEC) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ RingBars R;
     ok = greedy ? stream_chunk_staged<DT, true, kT, kTopF>(R, ring, P.stages, C, c, A)
-                : stream_chunk_staged<DT, false, kT, kTopF>(R, ring, P.stages, C, c, A);
+                : stream_chunk_staged<DT, false, kT, kTopF>(R, ring, P.stages, C, c, A,
+                                                            halves ? P.half : 0, snap);
   } else if (greedy) {
     stream_chunk<DT, false, true, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
                                              P.iters, c, A);
@@ -820,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 4 : 5) stats_kernel(const 
     stream_chunk<DT, false, false, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
                                               P.iters, c, A);
   }
-  chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S, excl);
+  chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S, excl, halves ? snap : nullptr);
 }
 
 // ---- persistent path ------------------------------------------------------------
