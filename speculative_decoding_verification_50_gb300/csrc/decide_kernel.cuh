@@ -7,19 +7,23 @@
 //      dl-note §2.3; Lecture 5 §3.1),
 //   a4 the outcome keys: top-F of the per-chunk candidates at each lookahead
 //      ("Speculative Speculative Decoding" §4.1.1), and
-//   a5 the hit flag: t* among the keys of lookahead n (§3.1).
+//   a5 the hit flag: t* among the keys of lookahead n (§3.1);
+// in its other modes the Saguaro sampler's draw from sigma_{F,C} (§4.2.1)
+// and multi-step speculative sampling at token-tree nodes (Lecture 5 §6.4).
 //
 // One thread-block cluster of CB CTAs per batch row.  Every CTA combines the
-// records itself (half a warp per position, lanes over chunks, fp64 sums) and
-// decides n; the arithmetic and its order are the same everywhere, so all CTAs
-// agree without waiting for one another.  Only row n is read again: every CTA
-// streams its slice of target row n (and draft row n) through a bulk-copy
-// ring, forms r, and reduces it to per-warp segment sums; the per-CTA totals
-// are exchanged through distributed shared memory, which gives R and the CTA
-// whose range holds U_K * R; that CTA walks its segments and one warp scans
-// the one segment that holds the crossing (a re-read of 32 vectors).  Meanwhile
-// warps 1..7 of every CTA merge the chunk candidate lists into the outcome
-// keys (one warp per lookahead).  Rank 0 writes the outputs.
+// records itself (half a warp per position, lanes over chunks, float-float
+// sums) and decides n; the arithmetic and its order are the same everywhere,
+// so all CTAs agree without waiting for one another.  Only row n is read
+// again: every CTA streams its slice of target row n (and draft row n) through
+// a bulk-copy ring, forms r, and reduces it to per-warp segment sums; the
+// per-CTA totals are exchanged through distributed shared memory, which gives
+// R and the CTA whose range holds U_K * R; that CTA walks its segments and one
+// warp scans the one segment that holds the crossing (a re-read of 32
+// vectors).  A draw from a whole row's own distribution reads only the chunk
+// (or half-chunk) holding U * R instead.  Meanwhile warps 1..7 of every CTA
+// merge the chunk candidate lists into the outcome keys (one warp per
+// lookahead).  Rank 0 writes the outputs.
 #pragma once
 
 #include "stats_kernel.cuh"

@@ -21,11 +21,13 @@
 //
 // Per chunk the consumers write a ChunkRec: online (max, sum 2^((z-max) log2(e)/T))
 // of each row, or its first argmax for greedy rows.  With outcome prediction
-// they also write the chunk's own top-F of the draft row: the (F+1)-th largest
-// per-thread maximum of a warp bounds the chunk's top-F from below, so only the
-// few threads whose maximum reaches the bound read their share again (from
-// L2, just streamed; one round trip per warp) and push the qualifying logits
-// into shared memory, where they are ranked in parallel.
+// they also write the chunk's own top-F of the draft row: the per-warp
+// maxima bound the chunk's top-F from below, each thread keeps the group
+// holding its maximum in registers, so only the few threads with a second
+// group above the bound read their share again (from L2, just streamed; one
+// round trip per warp), and the qualifying logits are ranked in parallel in
+// shared memory.  A chunk of a single row streams through half-size ring
+// stages (twice the trips in flight).
 #pragma once
 
 #include "specv_device.cuh"
