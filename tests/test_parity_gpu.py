@@ -457,3 +457,22 @@ def test_ssd_round_edge_cases(sv, olib, dtype):
     o, keys, kl = oracle_ssd(olib, data, 4)
     compare_ssd(olib, g, o, keys, kl, data["temperature"], "ssd edge")
     assert g["row_status"][0] == oracle.ROW_NONFINITE and (g["keys"][0] == -1).all()
+
+
+@pytest.mark.parametrize("dtype", [wl.FP32, wl.BF16])
+def test_extreme_temperatures(sv, olib, dtype):
+    """Temperatures far from 1 (0.001, 0.02, 20, 10000): the exponent
+    (z - max) log2(e)/T spans hundreds, or nearly vanishes.  Same bars."""
+    spec = wl.custom(f"temps{dtype}", B=32, K=4, V=20000, dtype=dtype,
+                     temps=(0.001, 0.02, 20.0, 10000.0), sigma_d=(0.3, 2.0),
+                     seed=wl.SEED_BASE + 33000)
+    data = wl.generate(spec)
+    g = gpu_verify(sv, data)
+    o = oracle_verify(olib, data)
+    compare_verify(g, o, data["temperature"], f"temps {dtype}")
+    ssd = wl.custom(f"temps-ssd{dtype}", B=16, K=4, V=20000, dtype=dtype, F=6, ssd=True,
+                    temps=(0.001, 20.0, 10000.0), sigma_d=(0.3, 2.0), seed=wl.SEED_BASE + 33100)
+    d2 = wl.generate(ssd)
+    g2 = gpu_ssd(sv, d2, 6)
+    o2, keys, kl = oracle_ssd(olib, d2, 6)
+    compare_ssd(olib, g2, o2, keys, kl, d2["temperature"], f"temps ssd {dtype}")
