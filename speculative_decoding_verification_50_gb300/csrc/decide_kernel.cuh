@@ -315,6 +315,14 @@ __device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd,
 // consumes them and writes the per-warp segment sums of r, tile-major, as the
 // register path does.  Returns false if a wait gave up (after a bounded wait
 // for the copies still in flight).
+// Invalidates the ring's barriers, before ring_start arms them for another
+// pass (every wait on them has ended and every copy has landed).
+__device__ __forceinline__ void ring_reset(RingBars& R, int S) {
+  if (threadIdx.x == 0)
+    for (int s = 0; s < S; ++s)
+      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&R.full[s])) : "memory");
+}
+
 template <int DT>
 __device__ __forceinline__ void ring_start(RingBars& R, unsigned char* ring, int S, const Chunk& C) {
   if (threadIdx.x == 0) {
@@ -1021,11 +1029,19 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
       const int mode = dec.mode;
       const float mt = dec.mt, md = dec.md, ist = dec.ist;
       const float isd = kMss ? __fmul_rn(dec.isd, dec.cq) : dec.isd;  // MSS: c_j q
-      if (staged && pass == 0) {
+      // (a CTA whose copies gave up reads its later passes directly: its ring
+      // may still have a copy in flight, and the row is an error row anyway)
+      if (staged && (pass == 0 || copies_ok)) {
         Chunk SC = RC;
         if (mode != 0) SC.rowd = nullptr;
+        if (pass > 0) {  // another pass over the slice (an MSS rejection, a fallback)
+          __syncthreads();
+          ring_reset(ring_bars, P.stages);
+          ring_start<DT>(ring_bars, ring, P.stages, SC);
+          __syncthreads();
+        }
         copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd,
-                                      dec.xn, sgw, segs, ntl);
+                                      dec.xn, sgw, segs, ntl) && copies_ok;
       } else
       for (int t0 = 0; t0 < ntl; t0 += kTileUnroll) {
         float s[kTileUnroll];
