@@ -168,3 +168,27 @@ def test_mss_cfg5_sizes_sampled(sv, olib):
     gs = {k: g[k][rows] for k in g}
     compare(gs, o, sub, "cfg5 sampled")
     print("cfg5 nodes: accepted hist", np.bincount(g["accepted"] + 1, minlength=4).tolist())
+
+
+@pytest.mark.parametrize("V,dtype", [(20001, wl.FP32), (4097, wl.BF16)])
+@pytest.mark.parametrize("naive", [False, True])
+def test_mss_unaligned_rows(sv, olib, V, dtype, naive):
+    """Rows whose stride is not a multiple of 16 bytes take the register
+    path (element loads, every pass read directly)."""
+    spec = wl.custom(f"mssu{V}", B=24, K=1, V=V, dtype=dtype, temps=(0.0, 0.7, 1.0),
+                     sigma_d=(0.5, 2.5), seed=wl.SEED_BASE + 34000 + V)
+    data = wl.generate_mss(spec, 3)
+    bf = dtype == wl.BF16
+
+    def padded(a):  # stride V + 1 elements
+        t = to_dev(np.pad(a, ((0, 0), (0, 1))), bf)
+        return t[:, :V]
+
+    g = sv.specv_mss_verify(padded(data["target"]), padded(data["draft"]),
+                            to_dev(data["candidates"]), to_dev(data["temperature"]),
+                            to_dev(data["uniforms"]), naive=naive)
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in g.items()}
+    o = oracle.mss(data["target"], data["draft"], data["candidates"], data["temperature"],
+                   data["uniforms"], naive=naive, nthreads=0, lib=olib)
+    compare(g, o, data, f"unaligned V={V} naive={naive}")
