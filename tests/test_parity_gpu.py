@@ -476,3 +476,37 @@ def test_extreme_temperatures(sv, olib, dtype):
     g2 = gpu_ssd(sv, d2, 6)
     o2, keys, kl = oracle_ssd(olib, d2, 6)
     compare_ssd(olib, g2, o2, keys, kl, d2["temperature"], f"temps ssd {dtype}")
+
+
+def test_maximum_sizes(sv, olib):
+    """The largest K and F the library takes (32, 32) in an SSD round, MSS
+    with 32 candidates, and a batch of 8192 rows (16384 units) against the
+    oracle."""
+    spec = wl.custom("maxkf", B=3, K=32, V=4097, dtype=wl.BF16, F=32, ssd=True,
+                     temps=(0.0, 1.0, 1.5), sigma_d=(0.2, 0.6), seed=wl.SEED_BASE + 35000)
+    data = wl.generate(spec)
+    g = gpu_ssd(sv, data, 32)
+    o, keys, kl = oracle_ssd(olib, data, 32)
+    compare_ssd(olib, g, o, keys, kl, data["temperature"], "K=32 F=32")
+
+    ms = wl.custom("maxm", B=16, K=1, V=300, dtype=wl.FP32, temps=(0.0, 1.0),
+                   sigma_d=(1.0, 3.0), seed=wl.SEED_BASE + 35100)
+    m = wl.generate_mss(ms, 32)
+    nc = np.random.default_rng(1).integers(0, 33, 16).astype(np.int32)
+    r = sv.specv_mss_verify(to_dev(m["target"], wl.FP32), to_dev(m["draft"], wl.FP32),
+                            to_dev(m["candidates"], None), to_dev(m["temperature"], None),
+                            to_dev(m["uniforms"], None), num_candidates=to_dev(nc, None))
+    torch.cuda.synchronize()
+    om = oracle.mss(m["target"], m["draft"], m["candidates"], m["temperature"], m["uniforms"],
+                    num_cands=nc, nthreads=0, lib=olib)
+    ok = om["boundary"] == 0
+    assert np.array_equal(r["out_token"].cpu().numpy()[ok], om["token"][ok])
+    assert np.array_equal(r["accepted"].cpu().numpy()[ok], om["accepted"][ok])
+    assert np.abs(r["accept_prob"].cpu().numpy() - om["accept_prob"]).max() <= 1e-5
+
+    big = wl.custom("bigb", B=8192, K=1, V=64, dtype=wl.FP32, temps=(0.0, 0.8, 1.0),
+                    sigma_d=(0.5, 2.0), seed=wl.SEED_BASE + 35200)
+    db = wl.generate(big)
+    gb = gpu_verify(sv, db)
+    ob = oracle_verify(olib, db)
+    compare_verify(gb, ob, db["temperature"], "B=8192")
