@@ -72,7 +72,10 @@ typedef enum { SPECV_BF16 = 0, SPECV_FP32 = 1 } specv_dtype;
                                  shared memory did not complete within about
                                  a second of device time; the kernel gave up on
                                  the row instead of waiting forever (not
-                                 expected on a healthy GPU) */
+                                 expected on a healthy GPU; for tests, the
+                                 environment variable SPECV_TEST_STALL="A:<i>"
+                                 or "B:<b>", read once per process, makes one
+                                 such wait run out) */
 
 /*
  * Verification of B independent batch rows ("Speculative Speculative

@@ -93,6 +93,8 @@ struct DecideParams {
   float sg_C;        //   (0: plain softmax drafts); the sampler's own F and C
   int32_t local_draw;  // draws from a whole row read only the chunk holding U * R
   int32_t half;        // the sampler's records carry each chunk's first half apart
+  int32_t stall;       // test hook: 1 + the batch row whose first residual stage (rank 0)
+                       // waits for 16 bytes no copy brings, so its wait runs out (0: none)
   // MSS (K = M candidates per node, one target and one draft row each)
   const int32_t* ncand;  // per-node candidate counts, or null (all M)
   int32_t naive;         // naive sampling: one draw from p, candidates matched to it
@@ -314,7 +316,8 @@ __device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd,
 // thread 0; call before other work, then a CTA barrier); ring_residual
 // consumes them and writes the per-warp segment sums of r, tile-major, as the
 // register path does.  Returns false if a wait gave up (after a bounded wait
-// for the copies still in flight).
+// for the copies still in flight).  With `stall` (a test hook) stage 0 also
+// waits for 16 bytes that no copy brings.
 // Invalidates the ring's barriers, before ring_start arms them for another
 // pass (every wait on them has ended and every copy has landed).
 __device__ __forceinline__ void ring_reset(RingBars& R, int S) {
@@ -324,10 +327,12 @@ __device__ __forceinline__ void ring_reset(RingBars& R, int S) {
 }
 
 template <int DT>
-__device__ __forceinline__ void ring_start(RingBars& R, unsigned char* ring, int S, const Chunk& C) {
+__device__ __forceinline__ void ring_start(RingBars& R, unsigned char* ring, int S, const Chunk& C,
+                                           bool stall = false) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&R.full[s], 1);
     fence_mbar_init();
+    if (stall) mbar_expect_tx(&R.full[0], 16);
     const int ntr = ring_trips(C.nv);
     for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C);
   }
@@ -1009,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   if (staged) {
     Chunk SC = RC;
     if (dec.mode != 0) SC.rowd = nullptr;  // mode 1 reads p_n only
-    ring_start<DT>(ring_bars, ring, P.stages, SC);
+    ring_start<DT>(ring_bars, ring, P.stages, SC, P.stall == b + 1 && rank == 0);
     __syncthreads();
   }
 

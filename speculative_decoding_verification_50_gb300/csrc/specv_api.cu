@@ -268,6 +268,26 @@ bool persistent_path() {
   return v == 1;
 }
 
+// Test hook, off unless SPECV_TEST_STALL is set: "A:<i>" makes the first
+// ring stage of row-statistics item i (staged path) wait for 16 bytes that no
+// copy brings, "B:<b>" the first residual stage of batch row b in the decision
+// kernel; the bounded wait then runs out (about a second) and the row comes
+// back flagged SPECV_ROW_DEVICE_TIMEOUT.  Returns 1 + that index for kernel
+// `which`, else 0.
+int test_stall(char which) {
+  static int v = -2;
+  static char k = 0;
+  if (v == -2) {
+    v = -1;
+    const char* e = getenv("SPECV_TEST_STALL");
+    if (e && (e[0] == 'A' || e[0] == 'B') && e[1] == ':') {
+      k = e[0];
+      v = atoi(e + 2);
+    }
+  }
+  return (v >= 0 && k == which) ? v + 1 : 0;
+}
+
 template <int MODE>
 cudaError_t launch_stats(int dtype, bool vec, int64_t items, cudaStream_t s, const StatsParams& p) {
   const size_t ring_smem = static_cast<size_t>(p.stages) * 2 * kTripBytes;
@@ -422,6 +442,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
                 ? pl.iters / 2 : 0;
   sp.cu = a->cu_num_draft_tokens;
   sp.ntok = a->num_draft_tokens;
+  sp.stall = test_stall('A');
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t items = units * pl.nchunk;
   cudaError_t e = mode == kModeSsd      ? launch_stats<kModeSsd>(a->dtype, vec, items, s, sp)
@@ -472,6 +493,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   const bool fits = pl.chunk <= static_cast<int64_t>(kDrawTiles) * kThreads * vec_width(a->dtype);
   dp.local_draw = fits && (env_local >= 0 ? env_local != 0 : pl.chunk < pl.L);
   dp.half = sp.half;
+  dp.stall = test_stall('B');
   for (int k = 0; k <= K; ++k) dp.fk[k] = fanout ? fanout[k] : F;
   // Aligned rows stream the residual slice through a ring placed after the
   // segment sums in dynamic shared memory.

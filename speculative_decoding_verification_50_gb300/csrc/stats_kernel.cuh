@@ -79,6 +79,8 @@ struct StatsParams {
   int32_t half;       // sampler rows: trips in a chunk's first half, recorded apart (0: none)
   const int32_t* cu;  // per-row draft counts (inclusive prefix sums), or null
   int32_t ntok;       // with cu: packed draft rows the buffers hold
+  int32_t stall;      // test hook: 1 + the item whose first stage waits for 16
+                      // bytes no copy brings, so its wait runs out (0: none)
 };
 
 // Where batch row b's logit rows, draft tokens and uniforms live: the strided
@@ -755,10 +757,12 @@ __device__ __forceinline__ int64_t covered_end(const Chunk& C) {
 // half > 0: after `half` trips the draft row's running statistics move to
 // snap[threadIdx.x] and start again, so the chunk's first half is recorded
 // apart (all of it if the chunk is that short).
+// stall (test hook): stage 0 also waits for 16 bytes that no copy brings.
 template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* ring, int S2,
                                                     const Chunk& C, float c, Acc<Elem<DT>::VW>& A,
-                                                    int half = 0, float2* snap = nullptr) {
+                                                    bool stall, int half = 0,
+                                                    float2* snap = nullptr) {
   const int ntr = ring_trips(C.nv);
   const int64_t covered = covered_end<DT>(C);
   // A chunk of a single row (a draft row alone, or a target row with no
@@ -770,6 +774,7 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&R.full[s], 1);
     fence_mbar_init();
+    if (stall) mbar_expect_tx(&R.full[0], 16);
     for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C, one);
   }
   __syncthreads();
@@ -839,8 +844,9 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? 4 : 5) stats_kernel(const 
   if (VEC) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ RingBars R;
-    ok = greedy ? stream_chunk_staged<DT, true, kT, kTopF>(R, ring, P.stages, C, c, A)
-                : stream_chunk_staged<DT, false, kT, kTopF>(R, ring, P.stages, C, c, A,
+    const bool stall = P.stall == static_cast<int64_t>(blockIdx.x) + 1;
+    ok = greedy ? stream_chunk_staged<DT, true, kT, kTopF>(R, ring, P.stages, C, c, A, stall)
+                : stream_chunk_staged<DT, false, kT, kTopF>(R, ring, P.stages, C, c, A, stall,
                                                             halves ? P.half : 0, snap);
   } else if (greedy) {
     stream_chunk<DT, false, true, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
