@@ -52,7 +52,7 @@ int vec_width(int32_t dtype) { return dtype == SPECV_BF16 ? 8 : 4; }
 // it, for tuning runs.
 int sm_count();
 
-int pick_cluster(int32_t B, int32_t V, int vw, int min_c = 1) {
+int pick_cluster(int32_t B, int32_t V, int vw, int min_c = 1, int max_c = 16) {
   static int env = -2;
   if (env == -2) {
     const char* s = getenv("SPECV_CLUSTER");
@@ -64,6 +64,7 @@ int pick_cluster(int32_t B, int32_t V, int vw, int min_c = 1) {
   const int want = 4 * sm_count();
   int c = (want + B - 1) / (B > 0 ? B : 1);
   if (c < min_c) c = min_c;
+  if (c > max_c) c = max_c;
   if (c > 16) c = 16;
   while (c & (c - 1)) c &= c - 1;
   const int tiles = static_cast<int>((static_cast<int64_t>(V) + kThreads * vw - 1) / (kThreads * vw));
@@ -148,7 +149,7 @@ int sm_count() {
 // trips (kernel A 258 -> 215 us on 2304 rows of 152064 fp32); the decision
 // kernel's chunk-local draw reads up to 16 trips.
 Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int min_cb = 1,
-               int iters0 = 8) {
+               int iters0 = 8, int max_cb = 16) {
   Plan pl;
   const int vw = vec_width(dtype);
   const int64_t units = static_cast<int64_t>(B > 0 ? B : 0) * (K + 1);
@@ -185,7 +186,7 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
       }
     }
   }
-  pl.CB = pick_cluster(B, V, vw, min_cb);
+  pl.CB = pick_cluster(B, V, vw, min_cb, max_cb);
   pl.L = slice_len(V, pl.CB, vw);
   const int64_t ntiles = ((pl.L / vw) + kThreads - 1) / kThreads;
   pl.smemB = static_cast<size_t>(ntiles) * kWarps * sizeof(float);
@@ -394,8 +395,13 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   const int32_t B = a->B, K = a->K, V = a->V;
   const int32_t Ka = mode == kModeMss ? 0 : K;  // positions per row in the statistics kernel
   const bool cands = mode == kModeSsd || mode == kModeSample;
-  const Plan pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, mode == kModeMss ? 2 : 1,
-                            mode == kModeSample ? 16 : 8);
+  Plan pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, mode == kModeMss ? 2 : 1,
+                      mode == kModeSample ? 16 : 8);
+  // The sampler's rows draw from one chunk each (the chunk-local draw) when a
+  // chunk is shorter than the row: the other CTAs of a cluster would only
+  // wait, so its rows take one CTA each.
+  if (mode == kModeSample && pl.CB > 1 && pl.chunk < V)
+    pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, 1, 16, 1);
   if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need)
