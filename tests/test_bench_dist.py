@@ -87,6 +87,8 @@ def test_reference_arm_prints_one_line_on_rank0():
     assert line["metric"] == bench.METRIC and line["unit"] == "rows/s"
     assert line["value"] > 0 and line["higher_is_better"] is True
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    # the threads it reports are the ones that had a batch row to work on
+    assert line["cpu_baseline"]["cores"] <= max(1, line["config"]["sample_rows_per_step"])
     assert line["e2e"] == {"value": line["value"], "unit": "rows/s",
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
