@@ -133,6 +133,51 @@ def check_softmax_library(lib):
     assert np.max(np.abs(p - ref)) < 1e-15
 
 
+def check_verify_library(lib):
+    """The whole verification of random rows against library routines: p and q
+    from scipy softmax (fp64), the accept test u <= p(x)/q(x) up to the first
+    rejection, and the bonus as numpy searchsorted (side="right") of U[K] * R
+    on the cumulative residual max(p_n - q_n, 0), or on p_K after K
+    acceptances.  Rows the oracle flags as boundary cases are skipped."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(41)
+    B, K, V = 300, 3, 40
+    zt = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    zd = (zt[:, :K] + rng.standard_normal((B, K, V)) * rng.uniform(0.2, 2.0, (B, 1, 1))).astype(np.float32)
+    temps = rng.choice(np.array([0.6, 1.0, 1.7], np.float32), B)
+    tok = np.empty((B, K), np.int32)
+    for b in range(B):
+        for i in range(K):
+            q = softmax(zd[b, i].astype(np.float64) / temps[b])
+            tok[b, i] = rng.choice(V, p=q)
+    u = rng.random((B, K + 1), dtype=np.float32)
+    out = oracle.verify(zt, zd, tok, temps, u, nthreads=0, lib=lib)
+    checked = 0
+    for b in range(B):
+        T = float(temps[b])
+        p = [softmax(zt[b, i].astype(np.float64) / T) for i in range(K + 1)]
+        q = [softmax(zd[b, i].astype(np.float64) / T) for i in range(K)]
+        n = K
+        for i in range(K):
+            x = tok[b, i]
+            if not (q[i][x] > 0 and p[i][x] / q[i][x] >= u[b, i]):
+                n = i
+                break
+        r = np.maximum(p[n] - q[n], 0.0) if n < K else p[K]
+        t = int(np.searchsorted(np.cumsum(r), float(u[b, K]) * r.sum(), side="right"))
+        np.testing.assert_allclose(out["p"][b], [p[i][tok[b, i]] for i in range(K)], rtol=1e-6)
+        np.testing.assert_allclose(out["q"][b], [q[i][tok[b, i]] for i in range(K)], rtol=1e-6)
+        if out["boundary"][b]:
+            continue
+        checked += 1
+        assert out["accept_len"][b] == n, (b, out["accept_len"][b], n)
+        assert out["out_tokens"][b, n] == t, (b, out["out_tokens"][b, n], t)
+        assert (out["out_tokens"][b, :n] == tok[b, :n]).all() and (out["out_tokens"][b, n + 1:] == -1).all()
+    assert checked > 0.9 * B
+    assert 0 < (out["accept_len"] < K).sum() < B  # both a residual and a p_K draw occur
+    assert (out["accept_len"] == K).any()
+
+
 def check_thm1_overlap(lib):
     """[SSD] Theorem 1: alpha = sum min(p, q) = 1 - 0.5 * ||p - q||_1."""
     rng = np.random.default_rng(11)
@@ -953,6 +998,7 @@ def check_mss_bad_inputs(lib):
 
 ALL_CHECKS = {
     "softmax_library": check_softmax_library,
+    "verify_library": check_verify_library,
     "thm1_overlap": check_thm1_overlap,
     "exercise_1": check_exercise_1,
     "section_2_3": check_section_2_3,

@@ -17,28 +17,28 @@ MUTATIONS = {
     "wrong_method_a": (
         "for (int v = 0; v < V; ++v) { r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0; R += r[v]; }",
         "for (int v = 0; v < V; ++v) { r[v] = p[v]; R += r[v]; (void)q; }",
-        ["exact_enumeration", "wrong_method_a_is_biased", "chisq_0.3"]),
+        ["exact_enumeration", "wrong_method_a_is_biased", "chisq_0.3", "verify_library"]),
     # residual max(q - p, 0), the garbled form on the survey blog
     "swapped_residual": (
         "r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;",
         "r[v] = q[v] > p[v] ? q[v] - p[v] : 0.0;",
-        ["exact_enumeration"]),
+        ["exact_enumeration", "verify_library"]),
     "ratio_inverted": (
         "accept = ratio >= (double)U[i];",
         "accept = 1.0 / ratio >= (double)U[i];",
-        ["exercise_1", "exact_enumeration"]),
+        ["exercise_1", "exact_enumeration", "verify_library"]),
     "accept_uses_bonus_uniform": (
         "accept = ratio >= (double)U[i];",
         "accept = ratio >= (double)U[K];",
-        ["exact_enumeration"]),
+        ["exact_enumeration", "verify_library"]),
     "cdf_off_by_one": (
         "if (cum > tau) { tstar = v; break; }",
         "if (cum > tau) { tstar = v > 0 ? v - 1 : v; break; }",
-        ["exact_enumeration", "section_2_3"]),
+        ["exact_enumeration", "section_2_3", "verify_library"]),
     "temperature_ignored": (
         "p[v] = exp((load_logit(base, dtype, off + v) - m) / T);",
         "p[v] = exp(load_logit(base, dtype, off + v) - m);",
-        ["softmax_library", "exact_enumeration_T07"]),
+        ["softmax_library", "exact_enumeration_T07", "verify_library"]),
     "greedy_last_max": (
         "if (z > m) { m = z; am = v; }",
         "if (z >= m) { m = z; am = v; }",
@@ -46,11 +46,11 @@ MUTATIONS = {
     "no_stop_at_first_rejection": (
         "if (!accept) { n = i; break; }",
         "if (!accept) { n = i; }",
-        ["exact_enumeration"]),
+        ["exact_enumeration", "verify_library"]),
     "bonus_from_wrong_row": (
         "const double* p = pt + (int64_t)n * V;",
         "const double* p = pt + (int64_t)(n > 0 ? n - 1 : 0) * V;",
-        ["exact_enumeration"]),
+        ["exact_enumeration", "verify_library"]),
     "overlap_uses_max": (
         "a += (p[v] < q[v]) ? p[v] : q[v];",
         "a += (p[v] > q[v]) ? p[v] : q[v];",
