@@ -78,12 +78,13 @@ class SpecvError(RuntimeError):
 
 
 _lib = None
+_lib_path = None
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load libspecv.so (built by __graft_entry__.build()); raise if absent."""
-    global _lib
-    if _lib is not None:
+    global _lib, _lib_path
+    if _lib is not None and path == _lib_path:
         return _lib
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
@@ -123,7 +124,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specv_last_launch_count.argtypes = []
     lib.specv_set_split_event.restype = None
     lib.specv_set_split_event.argtypes = [_P]
-    _lib = lib
+    _lib, _lib_path = lib, path
     return lib
 
 

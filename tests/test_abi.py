@@ -304,3 +304,17 @@ def test_mss_arguments_are_checked(lib):
     a.flags = sv.SPECV_MSS_NAIVE
     assert lib.specv_mss_verify(ctypes.byref(a), None, 0, None) == sv.SPECV_OK
     assert lib.specv_mss_verify(None, None, 0, None) == sv.SPECV_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly():
+    """Without libspecv.so the product raises: there is no CPU fallback."""
+    import subprocess
+    import sys
+    code = ("import torch, speculative_decoding_verification_50_gb300 as sv\n"
+            "sv.load_library.__defaults__ = ('/nonexistent/libspecv.so',)\n"
+            "z = torch.zeros(1, 2, 8); t = torch.zeros(1, 1, dtype=torch.int32)\n"
+            "sv.specv_verify(z, z[:, :1], t, torch.ones(1), torch.zeros(1, 2))\n")
+    p = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert p.returncode != 0
+    assert "libspecv.so is missing" in p.stderr, p.stderr[-1000:]
