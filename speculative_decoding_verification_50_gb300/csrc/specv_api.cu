@@ -400,8 +400,10 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   // The sampler's rows draw from one chunk each (the chunk-local draw) when a
   // chunk is shorter than the row: the other CTAs of a cluster would only
   // wait, so its rows take one CTA each.
-  if (mode == kModeSample && pl.CB > 1 && pl.chunk < V)
-    pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, 1, 16, 1);
+  if (mode == kModeSample && pl.CB > 1 && pl.chunk < V) {
+    const Plan one = make_plan(B, Ka, V, cands ? F : 0, a->dtype, 1, 16, 1);
+    if (one.smemB <= kMaxSegSmem) pl = one;  // (a very long row keeps its cluster)
+  }
   if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
   const size_t need = plan_workspace(pl);
   if (!workspace || workspace_bytes < need)

@@ -77,6 +77,27 @@ def test_sampler_matches_oracle(sv, olib, V, dtype, F, C):
     assert (g["tokens"][~ok] == -1).all()
 
 
+@pytest.mark.parametrize("V", [6_000_000, 8_000_000])
+def test_sampler_long_rows_few_batch_rows(sv, olib, V):
+    """Two rows of millions of logits: one CTA per row while its segment table
+    fits in shared memory (V = 6e6), a cluster per row beyond (V = 8e6)."""
+    rng = np.random.default_rng(V // 1000)
+    z = rng.normal(0, 2.0, (2, V)).astype(np.float32)
+    z[1, :6] = 20.0  # the top keys hold most of row 1's mass: the whole-row pass
+    T = np.array([1.0, 0.8], np.float32)
+    U = np.array([0.37, 0.81], np.float32)
+    g = sv.specv_saguaro_sample(to_dev(z), to_dev(T), 6, 0.3, to_dev(U))
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in g.items()}
+    o = oracle.saguaro_sample(z, T, 6, 0.3, U, lib=olib)
+    assert (g["row_status"] & oracle.ROW_ERRORS == 0).all()
+    for b in range(2):
+        if g["tokens"][b] != o["tokens"][b]:
+            assert near_boundary(z[b], float(T[b]), 6, 0.3, float(U[b]), int(o["tokens"][b]), olib)
+        else:
+            assert abs(g["q"][b] - o["q"][b]) <= PROB_TOL
+
+
 def test_sampler_law_small_vocab(sv, olib):
     """Empirical law of GPU draws on V = 6 with C = 0.2, F = 2 against sigma
     (chi-square over 60k draws across many rows of one logit vector)."""
