@@ -178,6 +178,40 @@ def check_verify_library(lib):
     assert (out["accept_len"] == K).any()
 
 
+def check_boundary_flags(lib):
+    """The boundary flag (spec: a uniform within 1e-6 of a ratio or a CDF
+    step) is set exactly where the definition puts it.  Constructed rows at
+    T = 1: p_0 = (.5, .3, .2), q_0 = (.25, .5, .25), p_1 = (.2, .3, .5); the
+    draft x = 1 has p/q = 0.6.  On random rows the flag is rare."""
+    P = [[0.5, 0.3, 0.2], [0.2, 0.3, 0.5]]
+    Q = [[0.25, 0.5, 0.25]]
+    cases = [  # (x, U_0, U_1, accept length, boundary)
+        (1, 0.6 + 5e-7, 0.5, 0, 1),    # U_0 just past the ratio: rejected, on the boundary
+        (1, 0.6 - 5e-7, 0.7, 1, 1),    # just below it: accepted, on the boundary
+        (1, 0.59, 0.2 + 5e-7, 1, 1),   # accepted; U_1 just past the step 0.2 of p_1
+        (1, 0.59, 0.5 - 4e-7, 1, 1),   # accepted; U_1 just below the step 0.5 of p_1
+        (1, 0.59, 0.35, 1, 0),         # clear of every ratio and step
+        (1, 0.9, 0.5, 0, 0),           # rejected; residual (.25, 0, 0): U_1 * R clear of 0 and R
+        (0, 0.999, 0.2 + 5e-7, 1, 1),  # p/q = 2: always accepted; the bonus on a step
+    ]
+    tok = np.array([[c[0]] for c in cases], np.int32)
+    u = np.array([[c[1], c[2]] for c in cases], np.float32)
+    Pf = [[Fr(x).limit_denominator(1000) for x in row] for row in P]
+    Qf = [[Fr(x).limit_denominator(1000) for x in row] for row in Q]
+    out = run_verify(lib, Pf, Qf, tok, u)
+    for k, c in enumerate(cases):
+        assert out["accept_len"][k] == c[3], (k, out["accept_len"][k])
+        assert out["boundary"][k] == c[4], (k, out["boundary"][k])
+    rng = np.random.default_rng(43)
+    B, K, V = 400, 3, 50
+    zt = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    zd = (zt[:, :K] + rng.standard_normal((B, K, V))).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    o = oracle.verify(zt, zd, tok, np.ones(B, np.float32), rng.random((B, K + 1), dtype=np.float32),
+                      nthreads=0, lib=lib)
+    assert o["boundary"].sum() <= 2, o["boundary"].sum()
+
+
 def check_thm1_overlap(lib):
     """[SSD] Theorem 1: alpha = sum min(p, q) = 1 - 0.5 * ||p - q||_1."""
     rng = np.random.default_rng(11)
@@ -999,6 +1033,7 @@ def check_mss_bad_inputs(lib):
 ALL_CHECKS = {
     "softmax_library": check_softmax_library,
     "verify_library": check_verify_library,
+    "boundary_flags": check_boundary_flags,
     "thm1_overlap": check_thm1_overlap,
     "exercise_1": check_exercise_1,
     "section_2_3": check_section_2_3,

@@ -136,6 +136,19 @@ MUTATIONS = {
         "*tok_out = icdf_draw(p, V, (double)U[M], &fb, boundary);\n    for (int j = 0; j < m; ++j)",
         "*tok_out = icdf_draw(q, V, (double)U[M], &fb, boundary);\n    for (int j = 0; j < m; ++j)",
         ["mss_naive_and_greedy"]),
+    # the boundary band dropped, widened, or checked on one side of the step only
+    "boundary_never": (
+        "#define BOUNDARY_EPS 1e-6",
+        "#define BOUNDARY_EPS 0.0",
+        ["boundary_flags"]),
+    "boundary_too_wide": (
+        "#define BOUNDARY_EPS 1e-6",
+        "#define BOUNDARY_EPS 1e-2",
+        ["boundary_flags"]),
+    "boundary_one_side": (
+        "} else if (fabs(tau - prev) < BOUNDARY_EPS * R || fabs(cum - tau) < BOUNDARY_EPS * R) {",
+        "} else if (fabs(cum - tau) < BOUNDARY_EPS * R) {",
+        ["boundary_flags"]),
     "hit_wrong_length": (
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
