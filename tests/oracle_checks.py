@@ -1011,6 +1011,34 @@ def check_mss_naive_and_greedy(lib):
                 assert (o["accept_prob"][b] == 0).all()
 
 
+def check_mss_boundary_flags(lib):
+    """MSS and naive sampling flag a node as a boundary case where the
+    definition puts it: a candidate's uniform within 1e-6 of its acceptance
+    ratio, or the draw's U * R within 1e-6 * R of a CDF step.  One node with
+    p = (.5, .3, .2), q = (.25, .5, .25) at T = 1; candidate 1 has p/q = 0.6."""
+    lp = np.log(np.array([0.5, 0.3, 0.2]))
+    lq = np.log(np.array([0.25, 0.5, 0.25]))
+    zt = np.tile(lp, (6, 1)).astype(np.float32)
+    zq = np.tile(lq, (6, 1)).astype(np.float32)
+    x = np.array([[1], [1], [1], [1], [1], [1]], np.int32)
+    T = np.ones(6, np.float32)
+    U = np.array([[0.6 + 5e-7, 0.5],     # rejected on the boundary of the ratio
+                  [0.6 - 5e-7, 0.5],     # accepted on it
+                  [0.59, 0.5],           # accepted, clear
+                  [0.9, 0.5],            # rejected; residual (.25, 0, 0): draw clear of its steps
+                  [0.9, 0.0 + 3e-7],     # rejected; U * R within 1e-6 * R of the step at 0
+                  [0.9, 0.5]], np.float32)
+    o = oracle.mss(zt, zq, x, T, U, lib=lib)
+    assert o["accepted"].tolist() == [-1, 0, 0, -1, -1, -1], o["accepted"]
+    assert o["boundary"].tolist() == [1, 1, 0, 0, 1, 0], o["boundary"]
+    # naive sampling: the draw from p itself, steps at 0.5 and 0.8
+    Un = np.array([[0.0, 0.5 + 5e-7], [0.0, 0.8 - 5e-7], [0.0, 0.65],
+                   [0.0, 0.3], [0.0, 0.9], [0.0, 0.1]], np.float32)
+    o = oracle.mss(zt, zq, x, T, Un, naive=True, lib=lib)
+    assert o["token"].tolist() == [1, 1, 1, 0, 2, 0], o["token"]
+    assert o["boundary"].tolist() == [1, 1, 0, 0, 0, 0], o["boundary"]
+
+
 def check_mss_bad_inputs(lib):
     """Out-of-range candidates (ROW_BAD_TOKEN), counts outside [0, M]
     (ROW_BAD_COUNT) and bad temperatures flag the node and produce no token."""
@@ -1065,5 +1093,6 @@ ALL_CHECKS = {
     "mss_topk_misuse": check_mss_topk_misuse,
     "mss_single_candidate": check_mss_single_candidate_is_sd,
     "mss_naive_and_greedy": check_mss_naive_and_greedy,
+    "mss_boundary_flags": check_mss_boundary_flags,
     "mss_bad_inputs": check_mss_bad_inputs,
 }

@@ -149,6 +149,14 @@ MUTATIONS = {
         "} else if (fabs(tau - prev) < BOUNDARY_EPS * R || fabs(cum - tau) < BOUNDARY_EPS * R) {",
         "} else if (fabs(cum - tau) < BOUNDARY_EPS * R) {",
         ["boundary_flags"]),
+    "mss_draw_boundary_one_side": (
+        "      if (fabs(tau - prev) < BOUNDARY_EPS * R || fabs(cum - tau) < BOUNDARY_EPS * R) *bd = 1;",
+        "      if (fabs(cum - tau) < BOUNDARY_EPS * R) *bd = 1;",
+        ["mss_boundary_flags"]),
+    "mss_ratio_boundary_dropped": (
+        "    if (qx > 0.0 && fabs((double)U[j] - ratio) < BOUNDARY_EPS) *boundary = 1;",
+        "",
+        ["mss_boundary_flags"]),
     "hit_wrong_length": (
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
