@@ -128,7 +128,10 @@ def check_softmax_library(lib):
     assert p.tolist() == [0.0, 1.0, 0.0, 0.0, 0.0], p  # first maximum wins
     # bf16 bit patterns decode exactly: 1.0, 0.0, -2.0, -inf
     bits = np.array([0x3F80, 0x0000, 0xC000, 0xFF80], np.uint16).view(np.int16)
-    p = oracle.row_probs(bits, 1.0, lib=lib)
+    try:
+        p = oracle.row_probs(bits, 1.0, lib=lib)
+    except ValueError as e:  # a valid row refused
+        raise AssertionError(f"bf16 row refused: {e}")
     ref = softmax(np.array([1.0, 0.0, -2.0, -np.inf]))
     assert np.max(np.abs(p - ref)) < 1e-15
 

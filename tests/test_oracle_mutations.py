@@ -157,6 +157,21 @@ MUTATIONS = {
         "    if (qx > 0.0 && fabs((double)U[j] - ratio) < BOUNDARY_EPS) *boundary = 1;",
         "",
         ["mss_boundary_flags"]),
+    # bf16 bits widened to the wrong place
+    "bf16_decode_shift": (
+        "uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;",
+        "uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 15;",
+        ["softmax_library"]),
+    # NaN logits not flagged
+    "nan_not_flagged": (
+        "    if (isnan(z) || z == INFINITY) return ROW_NONFINITE;\n    if (z > m) { m = z; am = v; }",
+        "    if (z == INFINITY) return ROW_NONFINITE;\n    if (z > m) { m = z; am = v; }",
+        ["bad_inputs"]),
+    # packed rows: uniforms without the per-row bonus slot
+    "ragged_uniform_offset": (
+        "tokens + c0, (double)temperature[b], uniforms + c0 + b, no_draft, 0, 1.0,",
+        "tokens + c0, (double)temperature[b], uniforms + c0, no_draft, 0, 1.0,",
+        ["ragged_rows"]),
     "hit_wrong_length": (
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + n) * F;",
         "const int32_t* kk = keys + ((int64_t)b * (K + 1) + 0) * F;",
