@@ -52,12 +52,16 @@ int vec_width(int32_t dtype) { return dtype == SPECV_BF16 ? 8 : 4; }
 // it, for tuning runs.
 int sm_count();
 
+// A SPECV_* tuning variable as an integer (dflt when unset), read once per
+// process: callers keep it in a function-local static, whose initialisation
+// C++ makes thread-safe.
+int env_int(const char* name, int dflt) {
+  const char* e = getenv(name);
+  return e ? atoi(e) : dflt;
+}
+
 int pick_cluster(int32_t B, int32_t V, int vw, int min_c = 1, int max_c = 16) {
-  static int env = -2;
-  if (env == -2) {
-    const char* s = getenv("SPECV_CLUSTER");
-    env = s ? atoi(s) : -1;
-  }
+  static const int env = env_int("SPECV_CLUSTER", -1);
   if (env >= 1 && env <= 16) return env;
   // About four CTAs per SM over the whole grid, rounded down to a power of
   // two: clusters of 2^k CTAs pack onto the GPCs without gaps.
@@ -131,13 +135,13 @@ struct Plan {
 };
 
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
+  static const int n = [] {
+    int dev = 0, c = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 152;
-  }
+        cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+      c = 152;
+    return c;
+  }();
   return n;
 }
 
@@ -156,11 +160,7 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
   // Loop trips per kernel-A CTA: long chunks amortise the per-CTA reductions;
   // halve them while there would be fewer than four chunks per SM.
   // SPECV_ITERS (1..64) fixes the trip count, for tuning runs.
-  static int env_iters = -2;
-  if (env_iters == -2) {
-    const char* e = getenv("SPECV_ITERS");
-    env_iters = e ? atoi(e) : -1;
-  }
+  static const int env_iters = env_int("SPECV_ITERS", -1);
   pl.iters = (env_iters >= 1 && env_iters <= 64) ? env_iters : iters0;
   const int64_t want = 4LL * sm_count();
   for (;;) {
@@ -213,26 +213,16 @@ cudaError_t launch_plain(Kern k, int64_t blocks, size_t smem, cudaStream_t s, co
 // Stages of the persistent path's ring (SPECV_STAGES = 2..8 fixes the count,
 // for tuning runs).
 int ring_stages() {
-  static int n = 0;
-  if (n == 0) {
-    const char* e = getenv("SPECV_STAGES");
-    const int v = e ? atoi(e) : 0;
-    n = (v >= 2 && v <= kMaxStages) ? v : 2;
-  }
-  return n;
+  static const int v = env_int("SPECV_STAGES", 0);
+  return (v >= 2 && v <= kMaxStages) ? v : 2;
 }
 
 // Stages of the decision kernel's residual ring (SPECV_STAGES_B = 2..8 fixes
 // the count, for tuning runs).  Its grid is small (B x cluster CTAs), so each
 // CTA keeps more of its slice in flight than a row-statistics CTA does.
 int ring_stages_b() {
-  static int n = 0;
-  if (n == 0) {
-    const char* e = getenv("SPECV_STAGES_B");
-    const int v = e ? atoi(e) : 0;
-    n = (v >= 2 && v <= kMaxStages) ? v : 2;
-  }
-  return n;
+  static const int v = env_int("SPECV_STAGES_B", 0);
+  return (v >= 2 && v <= kMaxStages) ? v : 2;
 }
 
 // Persistent row-statistics kernel: as many CTAs as are resident at once on
@@ -261,11 +251,7 @@ cudaError_t launch_ring(int64_t items, cudaStream_t s, const StatsParams& p) {
 // default, the persistent path when SPECV_PERSIST=1 (for tuning runs); the
 // register path for any other layout.
 bool persistent_path() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("SPECV_PERSIST");
-    v = (e && atoi(e) == 1) ? 1 : 0;
-  }
+  static const int v = env_int("SPECV_PERSIST", 0);
   return v == 1;
 }
 
@@ -276,17 +262,16 @@ bool persistent_path() {
 // back flagged SPECV_ROW_DEVICE_TIMEOUT.  Returns 1 + that index for kernel
 // `which`, else 0.
 int test_stall(char which) {
-  static int v = -2;
-  static char k = 0;
-  if (v == -2) {
-    v = -1;
+  struct Stall {
+    char k;
+    int v;
+  };
+  static const Stall st = [] {
     const char* e = getenv("SPECV_TEST_STALL");
-    if (e && (e[0] == 'A' || e[0] == 'B') && e[1] == ':') {
-      k = e[0];
-      v = atoi(e + 2);
-    }
-  }
-  return (v >= 0 && k == which) ? v + 1 : 0;
+    if (e && (e[0] == 'A' || e[0] == 'B') && e[1] == ':') return Stall{e[0], atoi(e + 2)};
+    return Stall{0, -1};
+  }();
+  return (st.v >= 0 && st.k == which) ? st.v + 1 : 0;
 }
 
 template <int MODE>
@@ -493,11 +478,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   // A draw from a whole row reads one chunk on rank 0 instead of a slice on
   // every CTA of the cluster: worth it when the chunk is the shorter read.
   // SPECV_LOCAL_DRAW=0/1 overrides, for tuning runs.
-  static int env_local = -2;
-  if (env_local == -2) {
-    const char* e = getenv("SPECV_LOCAL_DRAW");
-    env_local = e ? atoi(e) : -1;
-  }
+  static const int env_local = env_int("SPECV_LOCAL_DRAW", -1);
   const bool fits = pl.chunk <= static_cast<int64_t>(kDrawTiles) * kThreads * vec_width(a->dtype);
   dp.local_draw = fits && (env_local >= 0 ? env_local != 0 : pl.chunk < pl.L);
   dp.half = sp.half;
