@@ -749,25 +749,27 @@ def check_saguaro_thm19(lib):
     C = 47/147 becomes (.47,.47,.03,.03); the acceptance rate against
     p_t = (.48,.48,.02,.02) is 0.98 with either; after a rejection the bonus
     lands in the cache (top-2 of the draft) always with Saguaro, never without."""
-    zd = np.log(np.array([0.49, 0.49, 0.01, 0.01])).astype(np.float32)
-    zt = np.log(np.array([0.48, 0.48, 0.02, 0.02])).astype(np.float32)
-    q = oracle.saguaro_probs(zd, 1.0, 2, 47 / 147, lib=lib)
-    np.testing.assert_allclose(q, [0.47, 0.47, 0.03, 0.03], atol=2e-7)
+    g = golden("ssd_theorem19.json")
+    F, C = g["F"], g["C_num"] / g["C_den"]
+    zd = np.log(np.array(g["p_draft"])).astype(np.float32)
+    zt = np.log(np.array(g["p_target"])).astype(np.float32)
+    q = oracle.saguaro_probs(zd, 1.0, F, C, lib=lib)
+    np.testing.assert_allclose(q, g["p_draft_saguaro"], atol=2e-7)
     # sampling from it: inverse CDF at U
-    s = oracle.saguaro_sample(np.stack([zd] * 4), np.ones(4, np.float32), 2, 47 / 147,
+    s = oracle.saguaro_sample(np.stack([zd] * 4), np.ones(4, np.float32), F, C,
                               np.array([0.2, 0.6, 0.95, 0.99], np.float32), lib=lib)
     assert list(s["tokens"]) == [0, 1, 2, 3]
-    np.testing.assert_allclose(s["q"], [0.47, 0.47, 0.03, 0.03], atol=2e-7)
+    np.testing.assert_allclose(s["q"], g["p_draft_saguaro"], atol=2e-7)
     B = 64
     rng = np.random.default_rng(19)
     U = rng.uniform(0, 1, (B, 2)).astype(np.float32)
     U[:, 0] = 0.999  # reject whenever p/q < 1
     tgt = np.broadcast_to(np.stack([zt, zt])[None], (B, 2, 4))
     dft = np.broadcast_to(zd[None, None], (B, 1, 4))
-    for sg, tok, in_cache in (((2, 47 / 147), 2, True), (None, 0, False)):
+    for sg, tok, in_cache in (((F, C), 2, True), (None, 0, False)):
         toks = np.full((B, 1), tok, np.int32)
         o = oracle.verify(tgt, dft, toks, np.ones(B, np.float32), U, lib=lib, saguaro=sg)
-        np.testing.assert_allclose(o["alpha"][:, 0], 0.98, atol=2e-7)
+        np.testing.assert_allclose(o["alpha"][:, 0], g["acceptance_rate_both"], atol=2e-7)
         assert (o["accept_len"] == 0).all()  # p/q = 2/3 (Saguaro) or 0.98 (plain) < 0.999
         bonus = o["out_tokens"][:, 0]
         assert (np.isin(bonus, [0, 1]) == in_cache).all(), (sg, bonus)
