@@ -84,3 +84,29 @@ def test_no_draft_and_mss_layouts():
     lay = bench.lay_out(data, spec, "mss")
     assert lay["tokens"].shape == (5, bench.MSS_M["cfg5-mss"]) and lay["rows"] == 5
     assert lay["bytes"] == 2 * 5 * spec.V * spec.elem_bytes
+
+
+def test_clock_summary_reports_median_and_throttle_reasons():
+    """The clocks object of the bench line from nvidia-smi's CSV samples:
+    median SM clock under load, the maximum, and every throttle reason seen
+    active (a rejected run shows hw_slowdown or a thermal slowdown)."""
+    class Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s = bench.ClockSampler(None)
+    s.proc = Done()
+    s.lines = [
+        "0, 2070, 2070, 900.1, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.0, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1100.0, Active, Not Active, Not Active, Not Active",
+        "garbled line",
+        "0, [N/A], 2070, 0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    c = s.stop()
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0 and c["samples"] == 3
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler(None).stop()["reasons"] == ["nvidia-smi unavailable"]
