@@ -70,12 +70,15 @@ WORKLOADS = {
     "cfg2a": (wl.SPECS["cfg2a"], "config 2a (B=1, K=5, V=128256, bf16, greedy), verify only"),
     "cfg2b": (wl.SPECS["cfg2b"], "config 2b (B=1, K=5, V=128256, bf16, T=0.7), verify only"),
     "cfg1": (wl.SPECS["cfg1"], "config 1 (B=1, K=4, V=4096, fp32, T=1), verify only"),
+    "cfg4-predict": (wl.SPECS["cfg4"], "config 4's draft rows (B=32, K+1=5, V=128256, bf16, F=6) "
+                                       "through the separate calls: specv_predict_outcomes, then "
+                                       "specv_check_hit on a fixed outcome"),
 }
 
 # Workloads in another layout: rows packed by per-row draft counts, or
 # verification without draft logits.
 LAYOUT = {"cfg5-ragged": "ragged", "cfg5-nodraft": "nodraft", "cfg5-sample": "sample",
-          "cfg5-mss": "mss"}
+          "cfg5-mss": "mss", "cfg4-predict": "predict"}
 
 # Candidates per token-tree node of the MSS workloads.
 MSS_M = {"cfg5-mss": 3}
@@ -273,6 +276,8 @@ def lay_out(data, spec, mode, first_row: int = 0) -> dict:
         lay.update(rows=int((kb + 1).sum()), bytes=int((2 * kb + 1).sum()) * V * s)
     elif mode == "nodraft":
         lay.update(draft=None, rows=B * (K + 1), bytes=B * (K + 1) * V * s)
+    elif mode == "predict":  # the draft rows at K+1 lookaheads, ranked once
+        lay.update(target=None, rows=B * (K + 1), bytes=B * (K + 1) * V * s)
     elif mode == "sample":  # every draft row of the round, one draw each
         rows = data["draft"].reshape(-1, V)
         n = rows.shape[0]
@@ -295,6 +300,11 @@ def time_oracle(lay, spec, nthreads: int, mode=None, saguaro=None) -> float:
         return time.perf_counter() - t0
     if mode == "sample":
         oracle.saguaro_sample(lay["draft"], lay["temperature"], *saguaro, lay["uniforms"])
+        return time.perf_counter() - t0
+    if mode == "predict":
+        p = oracle.predict(lay["draft"], lay["tokens"], spec.F, nthreads=nthreads)
+        n = np.zeros(lay["tokens"].shape[0], np.int32)
+        oracle.check_hit(p["keys"], n, np.zeros((n.size, spec.K + 1), np.int32))
         return time.perf_counter() - t0
     if mode == "ragged":
         oracle.verify_ragged(lay["target"], lay["draft"], lay["cu"], lay["tokens"],
@@ -341,6 +351,338 @@ def cpu_baseline(spec, budget_s: float = 12.0, mode=None, saguaro=None, workload
 
 
 # ---------------------------------------------------------------------------
+# host placement of the pinned input buffers (the end-to-end figure is bound
+# by the host-to-device link)
+
+def numa_nodes() -> list:
+    import glob
+    return sorted(int(os.path.basename(n)[4:]) for n in glob.glob("/sys/devices/system/node/node[0-9]*"))
+
+
+def pages_node(addr: int) -> dict:
+    """Pages per NUMA node of the mapping holding host address `addr`
+    (from /proc/self/numa_maps), e.g. {"N0": 65536}; {} if not found."""
+    try:
+        with open("/proc/self/numa_maps") as f:
+            maps = f.read().splitlines()
+        with open("/proc/self/maps") as f:
+            ranges = f.read().splitlines()
+    except OSError:
+        return {}
+    for ln in ranges:
+        lo, hi = (int(x, 16) for x in ln.split()[0].split("-"))
+        if lo <= addr < hi:
+            for m in maps:
+                if int(m.split()[0], 16) == lo:
+                    return {kv.split("=")[0]: int(kv.split("=")[1]) for kv in m.split()[2:]
+                            if kv.startswith("N") and "=" in kv}
+    return {}
+
+
+def gpu_numa_node(torch, dev):
+    p = torch.cuda.get_device_properties(dev)
+    bus = getattr(p, "pci_bus_id", None)
+    dom = getattr(p, "pci_domain_id", 0)
+    devid = getattr(p, "pci_device_id", None)
+    if bus is None or devid is None:
+        return None
+    path = f"/sys/bus/pci/devices/{dom:04x}:{bus:02x}:{devid:02x}.0/numa_node"
+    try:
+        with open(path) as f:
+            return int(f.read().strip())
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+
+# The configurations timed after the headline in the default run (one GPU).
+SIDE_CONFIGS = ("cfg1", "cfg2a", "cfg2b", "cfg3", "cfg4")
+
+
+def prepare(name, args, torch, sv, dev, rank, world, batch=0):
+    """Inputs, outputs and one call of workload `name` on this rank's shard."""
+    spec, desc = WORKLOADS[name]
+    if batch:
+        spec = dataclasses.replace(spec, B=batch)
+        desc += f" [B overridden to {batch}]"
+    fanout = None
+    if name in GEOMETRIC:
+        fanout, _ = sv.specv_geometric_fanout(spec.K, *GEOMETRIC[name], max_f=32)
+        spec = dataclasses.replace(spec, F=max(1, max(fanout)))
+        desc += f" [F_k = {fanout}]"
+    mode = LAYOUT.get(name)
+    saguaro = SAGUARO.get(name)
+    data = gen_data(spec, shard_rows(rank, world, spec.B), mode, name)
+    lay = lay_out(data, spec, mode, first_row=rank * spec.B)
+    B, K, V, F = spec.B, spec.K, spec.V, spec.F
+    is_bf16 = spec.dtype == wl.BF16
+
+    def host_logits(a):
+        t = torch.from_numpy(a)
+        return t.view(torch.bfloat16) if is_bf16 else t
+
+    h = dict(target=host_logits(lay["target"]).pin_memory() if lay["target"] is not None else None,
+             draft=host_logits(lay["draft"]).pin_memory() if lay["draft"] is not None else None,
+             tok=torch.from_numpy(lay["tokens"]).pin_memory(),
+             temp=torch.from_numpy(lay["temperature"]).pin_memory(),
+             unif=torch.from_numpy(lay["uniforms"]).pin_memory(),
+             cu=torch.from_numpy(lay["cu"]).pin_memory() if lay["cu"] is not None else None)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in h.items()}
+    pq_shape = (max(1, h["tok"].numel()),) if mode == "ragged" else \
+        (lay["rows"],) if mode == "sample" else (B, K)
+    i32 = dict(dtype=torch.int32, device=dev)
+    n_out = lay["rows"] if mode == "sample" else B
+    outs = dict(accept_len=torch.empty(B, **i32), out_tokens=torch.empty((B, K + 1), **i32),
+                p_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
+                q_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
+                row_status=torch.empty(n_out, **i32))
+    lib = sv.load_library()
+    code = sv.SPECV_BF16 if is_bf16 else sv.SPECV_FP32
+    ws = torch.empty(max(1, lib.specv_verify_workspace_bytes(B, K, V, code)), dtype=torch.uint8, device=dev)
+    s_tok = None
+    if mode == "sample":
+        ws = torch.empty(max(1, lib.specv_saguaro_workspace_bytes(lay["rows"], V, saguaro[0], code)),
+                         dtype=torch.uint8, device=dev)
+        s_tok = torch.empty(lay["rows"], **i32)
+    if mode == "mss":
+        Mc = MSS_M[name]
+        outs = dict(accepted=torch.empty(B, **i32), out_token=torch.empty(B, **i32),
+                    accept_prob=torch.empty((B, Mc), dtype=torch.float32, device=dev),
+                    row_status=torch.empty(B, **i32))
+        ws = torch.empty(max(1, lib.specv_mss_workspace_bytes(B, Mc, V, code)), dtype=torch.uint8, device=dev)
+    keys = key_logits = hit = None
+    if mode == "predict":  # a fixed outcome to check against: one verification of the batch
+        t_dev = host_logits(data["target"]).to(dev)
+        v = sv.specv_verify(t_dev, d["draft"][:, :K], d["tok"], d["temp"], d["unif"])
+        fixed_n, fixed_tok = v["accept_len"], v["out_tokens"]
+        del t_dev
+    if F:
+        keys = torch.empty((B, K + 1, F), **i32)
+        key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
+        hit = torch.empty(B, dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(1, lib.specv_ssd_workspace_bytes(B, K, V, F, code)), dtype=torch.uint8, device=dev)
+    if mode == "predict":
+        ws = torch.empty(max(1, lib.specv_predict_workspace_bytes(B, K, V, F, code)), dtype=torch.uint8,
+                         device=dev)
+    ws.zero_()
+    stream = torch.cuda.current_stream(dev)
+    launches = [0]
+    per_call = [0]  # our launches in the last call
+
+    def call(ev=None):
+        if ev is not None:
+            sv.specv_set_split_event(ev[1])  # recorded between the call's two launches
+            ev[0].record(stream)
+        if mode == "predict":  # a4 then a5 through their own entry points
+            sv.specv_predict_outcomes(d["draft"], d["tok"], F, keys=keys, key_logits=key_logits,
+                                      row_status=outs["row_status"], workspace=ws)
+            n_pred = sv.last_launch_count()
+            sv.specv_check_hit(keys, fixed_n, fixed_tok, hit=hit)
+            per_call[0] = n_pred + sv.last_launch_count()
+            launches[0] += per_call[0]
+            if ev is not None:
+                ev[2].record(stream)
+                sv.specv_set_split_event(None)
+            return
+        if mode == "sample":
+            sv.specv_saguaro_sample(d["draft"], d["temp"], *saguaro, d["unif"], tokens=s_tok,
+                                    q=outs["q_draft"], row_status=outs["row_status"], workspace=ws)
+        elif mode == "mss":
+            sv.specv_mss_verify(d["target"], d["draft"], d["tok"], d["temp"], d["unif"], workspace=ws, **outs)
+        elif F:  # the fused SSD round: verify + outcome keys + hit in one pass
+            sv.specv_ssd_round(d["target"], d["draft"], d["tok"], d["temp"], d["unif"], F, keys=keys,
+                               key_logits=key_logits, hit=hit, workspace=ws, fanout=fanout,
+                               saguaro=saguaro, **outs)
+        elif mode == "ragged":
+            sv.specv_verify_ragged(d["target"], d["draft"], d["cu"], d["tok"], d["temp"], d["unif"], K,
+                                   workspace=ws, **outs)
+        else:
+            sv.specv_verify(d["target"], d["draft"], d["tok"], d["temp"], d["unif"], workspace=ws, **outs)
+        per_call[0] = sv.last_launch_count()
+        launches[0] += per_call[0]
+        if ev is not None:
+            ev[2].record(stream)
+            sv.specv_set_split_event(None)
+
+    in_bytes = sum(t.numel() * t.element_size() for t in (d["target"], d["draft"]) if t is not None)
+    return dict(name=name, spec=spec, desc=desc, mode=mode, saguaro=saguaro, fanout=fanout, lay=lay,
+                h=h, d=d, outs=outs, keys=keys, hit=hit, s_tok=s_tok, call=call, launches=launches,
+                per_call=per_call,
+                in_bytes=in_bytes, stream=stream, is_bf16=is_bf16)
+
+
+def make_flush(torch, dev):
+    """Between timed calls whose inputs fit in L2 (outside their events):
+    write a buffer twice the L2, then read another as large, so the call
+    starts with an L2 of clean, unrelated lines rather than paying for the
+    flush's write-backs."""
+    fw = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    fr = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        fw.zero_()
+        fr.sum()
+    return flush
+
+
+def submit_us(torch, w, barrier) -> float:
+    """Host time to enqueue one call (Python, ctypes, the library's checks),
+    measured with the GPU kept busy so the host never waits for it."""
+    barrier()
+    torch.cuda._sleep(50_000_000)  # about 25 ms of GPU time: the host runs ahead
+    t0 = time.perf_counter()
+    for _ in range(20):
+        w["call"]()
+    dt = (time.perf_counter() - t0) / 20
+    barrier()
+    return dt * 1e6
+
+
+def gpu_wait(torch, us: float) -> None:
+    """A GPU-side wait of about `us` microseconds (at up to 2.1 GHz) queued
+    before a timed group of calls, so every call of the group is on the
+    stream before the GPU reaches it: the events then time the GPU's work,
+    not the host's enqueueing."""
+    torch.cuda._sleep(int(us * 2100))
+
+
+def time_calls(torch, w, steps, reps, flush, barrier, t_sub):
+    """K steps of `reps` calls each; returns (per-call ms of each step, our
+    kernel launches).  Inputs that fit in L2 are timed call by call with an
+    L2 flush before each (outside the events); larger inputs back to back."""
+    stream, call, launches = w["stream"], w["call"], w["launches"]
+    launches[0] = 0
+    barrier()
+    per_step = []
+    if flush is None:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for k in range(steps):
+            gpu_wait(torch, 1.5 * reps * t_sub + 20)
+            ev[k][0].record(stream)
+            for _ in range(reps):
+                call()
+            ev[k][1].record(stream)
+        barrier()
+        per_step = [e[0].elapsed_time(e[1]) / reps for e in ev]
+    else:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps * reps)]
+        for k in range(steps * reps):
+            flush()
+            gpu_wait(torch, 1.5 * t_sub + 20)
+            ev[k][0].record(stream)
+            call()
+            ev[k][1].record(stream)
+        barrier()
+        t = [e[0].elapsed_time(e[1]) for e in ev]
+        per_step = [sum(t[k * reps:(k + 1) * reps]) / reps for k in range(steps)]
+    return per_step, launches[0]
+
+
+def time_split(torch, w, n, flush, barrier, t_sub):
+    """n calls with an event between the call's two launches: per-call
+    (call ms, first-launch ms, second-launch ms)."""
+    stream, call = w["stream"], w["call"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for e in evs:  # create the events (a torch event exists once recorded)
+        e[1].record(stream)
+    barrier()
+    for k in range(n):
+        if flush is not None:
+            flush()
+        gpu_wait(torch, 1.5 * t_sub + 20)
+        call(evs[k])
+    barrier()
+    return ([e[0].elapsed_time(e[2]) for e in evs], [e[0].elapsed_time(e[1]) for e in evs],
+            [e[1].elapsed_time(e[2]) for e in evs])
+
+
+def measure(torch, w, steps, warmup, target_s, barrier, dev, peak):
+    """The headline timing of one workload: `steps` steps, each the mean of
+    enough repeated calls that the timed region lasts about target_s."""
+    for _ in range(warmup):
+        w["call"]()
+    barrier()
+    flush = make_flush(torch, dev) if w["in_bytes"] <= L2_BYTES else None
+    if flush is not None:
+        flush()
+        barrier()
+    t_sub = submit_us(torch, w, barrier)
+    # a short probe of the call time sets the repeats per step
+    probe, _ = time_calls(torch, w, 2, 3, flush, barrier, t_sub)
+    t_call = max(1e-3, min(probe))
+    reps = max(1, int(np.ceil(target_s * 1e3 / (steps * t_call))))
+    if flush is None:  # keep each step's queued wait short
+        reps = min(reps, max(1, int(20_000 / max(t_sub, 1.0))))
+    per_step, launches = time_calls(torch, w, steps, reps, flush, barrier, t_sub)
+    ms_call = statistics.mean(per_step)
+    hot = None
+    if flush is not None:  # the same calls back to back, inputs left in L2
+        hs, _ = time_calls(torch, w, max(1, steps // 4), reps, None, barrier, t_sub)
+        hot = statistics.mean(hs)
+    n_split = min(steps * reps, 2000)
+    call_ms, first_ms, second_ms = time_split(torch, w, n_split, flush, barrier, t_sub)
+    kb = w["lay"]["bytes"]
+    f_ms, s_ms = statistics.mean(first_ms), statistics.mean(second_ms)
+    dominant = 0 if f_ms >= s_ms else 1  # the launch that reads the logits
+    return dict(per_step=per_step, reps=reps, launches=launches, ms=ms_call, hot=hot,
+                call_ms=call_ms, first_ms=first_ms, second_ms=second_ms, dominant=dominant,
+                kernel_ms=max(f_ms, s_ms), submit_us=t_sub,
+                gbs=kb / (ms_call / 1e3) / 1e9, frac=kb / (ms_call / 1e3) / 1e9 / peak)
+
+
+def spawn_ranks(args, argv) -> int:
+    """`--gpus N` outside torchrun: start N ranks of this script on this
+    node, one per local GPU (NCCL for the two timing reductions; gloo on the
+    host with --dry-run), and return the worst exit code.  Rank 0 prints."""
+    n = args.gpus
+    if not args.dry_run:
+        import torch
+        have = torch.cuda.device_count() if torch.cuda.is_available() else 0
+        if have < n:
+            print(json.dumps({"error": f"--gpus {n} asks for {n} GPUs; this node has {have}"}), flush=True)
+            return 2
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), WORLD_SIZE=str(n), LOCAL_RANK=str(r),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__)] + list(argv), env=env))
+    rc = 0
+    for p in procs:
+        rc = max(rc, p.wait())
+    return rc
+
+
+def run_dry(args) -> None:
+    """The multi-rank plumbing on the host (gloo, no GPU, no kernels): process
+    group, barriers, the max over ranks of a stand-in step time and the sum of
+    the shards' rows.  Prints a line marked dry_run; it measures nothing."""
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    spec, desc = WORKLOADS[args.workload]
+    rows = float(len(shard_rows(rank, world, spec.B)) * (spec.K + 1))
+    t0 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    dt = time.perf_counter() - t0
+    ms = reduce_max(dt * 1e3, world)
+    rows_total = reduce_sum(rows, world)
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "metric": METRIC, "value": None, "unit": "rows/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": None, "scaling": "weak",
+                          "rows_per_step_all_ranks": rows_total, "barrier_ms_max": round(ms, 3),
+                          "config": {"workload": f"{args.workload}: {desc}", "B_per_gpu": spec.B}}),
+              flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
 
 def run_ours(args) -> None:
     import torch
@@ -358,91 +700,6 @@ def run_ours(args) -> None:
     import speculative_decoding_verification_50_gb300 as sv
     sv.load_library()
 
-    spec, desc = WORKLOADS[args.workload]
-    if args.batch:
-        spec = dataclasses.replace(spec, B=args.batch)
-        desc += f" [B overridden to {args.batch}]"
-    fanout = None
-    if args.workload in GEOMETRIC:
-        fanout, _ = sv.specv_geometric_fanout(spec.K, *GEOMETRIC[args.workload], max_f=32)
-        spec = dataclasses.replace(spec, F=max(1, max(fanout)))
-        desc += f" [F_k = {fanout}]"
-    mode = LAYOUT.get(args.workload)
-    saguaro = SAGUARO.get(args.workload)
-    data = gen_data(spec, shard_rows(rank, world, spec.B), mode, args.workload)
-    lay = lay_out(data, spec, mode, first_row=rank * spec.B)
-    B, K, V, F = spec.B, spec.K, spec.V, spec.F
-    is_bf16 = spec.dtype == wl.BF16
-
-    def host_logits(a):
-        t = torch.from_numpy(a)
-        return t.view(torch.bfloat16) if is_bf16 else t
-
-    h_target = host_logits(lay["target"]).pin_memory() if lay["target"] is not None else None
-    h_draft = host_logits(lay["draft"]).pin_memory() if lay["draft"] is not None else None
-    h_tok = torch.from_numpy(lay["tokens"]).pin_memory()
-    h_temp = torch.from_numpy(lay["temperature"]).pin_memory()
-    h_unif = torch.from_numpy(lay["uniforms"]).pin_memory()
-    h_cu = torch.from_numpy(lay["cu"]).pin_memory() if lay["cu"] is not None else None
-    d_target = h_target.to(dev) if h_target is not None else None
-    d_draft = h_draft.to(dev) if h_draft is not None else None
-    d_tok, d_temp, d_unif = h_tok.to(dev), h_temp.to(dev), h_unif.to(dev)
-    d_cu = h_cu.to(dev) if h_cu is not None else None
-    pq_shape = (max(1, h_tok.numel()),) if mode == "ragged" else \
-        (lay["rows"],) if mode == "sample" else (B, K)
-
-    i32 = dict(dtype=torch.int32, device=dev)
-    n_out = lay["rows"] if mode == "sample" else B
-    outs = dict(accept_len=torch.empty(B, **i32), out_tokens=torch.empty((B, K + 1), **i32),
-                p_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
-                q_draft=torch.empty(pq_shape, dtype=torch.float32, device=dev),
-                row_status=torch.empty(n_out, **i32))
-    lib = sv.load_library()
-    code = sv.SPECV_BF16 if is_bf16 else sv.SPECV_FP32
-    ws_v = torch.empty(max(1, lib.specv_verify_workspace_bytes(B, K, V, code)), dtype=torch.uint8, device=dev)
-    if mode == "sample":
-        ws_v = torch.empty(max(1, lib.specv_saguaro_workspace_bytes(lay["rows"], V, saguaro[0], code)),
-                           dtype=torch.uint8, device=dev)
-        s_tok = torch.empty(lay["rows"], **i32)
-    if mode == "mss":
-        Mc = MSS_M[args.workload]
-        outs = dict(accepted=torch.empty(B, **i32), out_token=torch.empty(B, **i32),
-                    accept_prob=torch.empty((B, Mc), dtype=torch.float32, device=dev),
-                    row_status=torch.empty(B, **i32))
-        ws_v = torch.empty(max(1, lib.specv_mss_workspace_bytes(B, Mc, V, code)),
-                           dtype=torch.uint8, device=dev)
-    if F:
-        keys = torch.empty((B, K + 1, F), **i32)
-        key_logits = torch.empty((B, K + 1, F), dtype=torch.float32, device=dev)
-        hit = torch.empty(B, dtype=torch.uint8, device=dev)
-        ws_v = torch.empty(max(1, lib.specv_ssd_workspace_bytes(B, K, V, F, code)), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    launches = [0]
-
-    def step(ev=None):
-        if ev is not None:
-            sv.specv_set_split_event(ev[1])  # recorded between the two kernels
-            ev[0].record(stream)
-        if mode == "sample":
-            sv.specv_saguaro_sample(d_draft, d_temp, *saguaro, d_unif, tokens=s_tok,
-                                    q=outs["q_draft"], row_status=outs["row_status"],
-                                    workspace=ws_v)
-        elif mode == "mss":
-            sv.specv_mss_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
-        elif F:  # the fused SSD round: verify + outcome keys + hit in one pass
-            sv.specv_ssd_round(d_target, d_draft, d_tok, d_temp, d_unif, F, keys=keys,
-                               key_logits=key_logits, hit=hit, workspace=ws_v, fanout=fanout,
-                               saguaro=saguaro, **outs)
-        elif mode == "ragged":
-            sv.specv_verify_ragged(d_target, d_draft, d_cu, d_tok, d_temp, d_unif, K,
-                                   workspace=ws_v, **outs)
-        else:
-            sv.specv_verify(d_target, d_draft, d_tok, d_temp, d_unif, workspace=ws_v, **outs)
-        launches[0] += sv.last_launch_count()
-        if ev is not None:
-            ev[2].record(stream)
-            sv.specv_set_split_event(None)
-
     def barrier():
         torch.cuda.synchronize(dev)
         if world > 1:
@@ -450,135 +707,123 @@ def run_ours(args) -> None:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    peak, peak_kind = measured_peak()
+    w = prepare(args.workload, args, torch, sv, dev, rank, world, batch=args.batch)
+    spec, lay, mode, outs = w["spec"], w["lay"], w["mode"], w["outs"]
+    B, K, V, F = spec.B, spec.K, spec.V, spec.F
+    flush = make_flush(torch, dev) if w["in_bytes"] <= L2_BYTES else None
     for _ in range(args.warmup):
-        step()
+        w["call"]()
     barrier()
 
-    in_bytes = (d_target.numel() * d_target.element_size() if d_target is not None else 0) + \
-        (d_draft.numel() * d_draft.element_size() if d_draft is not None else 0)
-    # Inputs that fit in L2 would be timed L2-hot: between timed calls
-    # (outside their events) write a buffer twice the L2, then read another
-    # as large, so that the call starts with an L2 of clean, unrelated lines
-    # rather than paying for the flush's write-backs.
-    flush = None
-    if in_bytes <= L2_BYTES:
-        fw = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-        fr = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
-        def flush():
-            fw.zero_()
-            fr.sum()
-
-        flush()  # the flush's own kernels loaded before the timed loop
-        barrier()
     sampler = ClockSampler(gpu_uuid(torch, dev))
     sampler.start()
-    # the GPU idled while the sampler started: two more untimed calls bring
-    # its clocks back up before the timed region
-    for _ in range(2):
+    # the GPU idled while the sampler started: a few untimed calls bring its
+    # clocks back up before the timed region
+    for _ in range(3):
         if flush is not None:
             flush()
-        step()
-    # (1) the headline: K calls back to back, nothing between the two kernels
-    # of a call (the second is launched as a programmatic dependent of the first)
-    launches[0] = 0
-    barrier()
-    if flush is None:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for k in range(args.steps):
-            step()
-        t_end.record(stream)
-        barrier()
-        total_ms = t_start.elapsed_time(t_end)
-    else:
-        ce = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for k in range(args.steps):
-            flush()
-            ce[k][0].record(stream)
-            step()
-            ce[k][1].record(stream)
-        barrier()
-        total_ms = sum(e[0].elapsed_time(e[1]) for e in ce)
-    gpu_launches = launches[0]
-    # inputs that fit in L2 are also timed hot: the same calls back to back
-    # with no flush between them (reported beside the cold figure)
-    hot_ms = None
-    if flush is not None:
-        h0 = torch.cuda.Event(enable_timing=True)
-        h1 = torch.cuda.Event(enable_timing=True)
-        h0.record(stream)
-        for k in range(args.steps):
-            step()
-        h1.record(stream)
-        barrier()
-        hot_ms = h0.elapsed_time(h1) / args.steps
-    # (2) per-kernel times: the same K calls with an event recorded before,
-    # between and after the two kernels (the middle event ends the overlap)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for e in evs:  # create the events (a torch event exists once recorded)
-        e[1].record(stream)
-    barrier()
-    for k in range(args.steps):
-        if flush is not None:
-            flush()
-        step(evs[k])
-    barrier()
+        w["call"]()
+    m = measure(torch, w, args.steps, 0, args.timed_s, barrier, dev, peak)
     clocks = sampler.stop()
-    call_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    stats_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    decide_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    ms_step = reduce_max(total_ms, world, dev) / args.steps
+    ms_step = reduce_max(m["ms"], world, dev)
     rows_total = reduce_sum(float(lay["rows"]), world, dev)
     value = rows_total / (ms_step / 1e3)
 
     # end to end: host inputs in pinned memory, copies inside the timed region
     e2e_steps = max(2, min(args.steps, 10))
-    h_n = torch.empty(B, dtype=torch.int32).pin_memory()
-    h_ot = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
-    h_keys = torch.empty((B, K + 1, F), dtype=torch.int32).pin_memory() if F else None
-    h_hit = torch.empty(B, dtype=torch.uint8).pin_memory() if F else None
-    h_st = torch.empty(lay["rows"], dtype=torch.int32).pin_memory() if mode == "sample" else None
-    h_tm = torch.empty(B, dtype=torch.int32).pin_memory() if mode == "mss" else None
+    h, d = w["h"], w["d"]
+    hold = dict(n=torch.empty(B, dtype=torch.int32).pin_memory(),
+                ot=torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
+                keys=torch.empty((B, K + 1, F), dtype=torch.int32).pin_memory() if F else None,
+                hit=torch.empty(B, dtype=torch.uint8).pin_memory() if F else None,
+                st=torch.empty(lay["rows"], dtype=torch.int32).pin_memory() if mode == "sample" else None,
+                tm=torch.empty(B, dtype=torch.int32).pin_memory() if mode == "mss" else None)
 
     def e2e_step():
-        if d_target is not None:
-            d_target.copy_(h_target, non_blocking=True)
-        if d_draft is not None:
-            d_draft.copy_(h_draft, non_blocking=True)
-        if d_cu is not None:
-            d_cu.copy_(h_cu, non_blocking=True)
-        d_tok.copy_(h_tok, non_blocking=True)
-        d_temp.copy_(h_temp, non_blocking=True)
-        d_unif.copy_(h_unif, non_blocking=True)
-        step()
+        for k in ("target", "draft", "cu", "tok", "temp", "unif"):
+            if d[k] is not None:
+                d[k].copy_(h[k], non_blocking=True)
+        w["call"]()
         if mode == "sample":
-            h_st.copy_(s_tok, non_blocking=True)
+            hold["st"].copy_(w["s_tok"], non_blocking=True)
         elif mode == "mss":
-            h_n.copy_(outs["accepted"], non_blocking=True)
-            h_tm.copy_(outs["out_token"], non_blocking=True)
+            hold["n"].copy_(outs["accepted"], non_blocking=True)
+            hold["tm"].copy_(outs["out_token"], non_blocking=True)
+        elif mode == "predict":
+            pass  # keys and hit below
         else:
-            h_n.copy_(outs["accept_len"], non_blocking=True)
-            h_ot.copy_(outs["out_tokens"], non_blocking=True)
+            hold["n"].copy_(outs["accept_len"], non_blocking=True)
+            hold["ot"].copy_(outs["out_tokens"], non_blocking=True)
         if F:
-            h_keys.copy_(keys, non_blocking=True)
-            h_hit.copy_(hit, non_blocking=True)
+            hold["keys"].copy_(w["keys"], non_blocking=True)
+            hold["hit"].copy_(w["hit"], non_blocking=True)
 
+    def h2d_only():
+        for k in ("target", "draft", "cu", "tok", "temp", "unif"):
+            if d[k] is not None:
+                d[k].copy_(h[k], non_blocking=True)
+
+    # the host link alone: the same host-to-device copies, nothing else
+    h2d_ms = []
+    for _ in range(2):
+        h2d_only()
+        barrier()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(w["stream"])
+        for _ in range(e2e_steps):
+            h2d_only()
+        c1.record(w["stream"])
+        barrier()
+        h2d_ms.append(c0.elapsed_time(c1) / e2e_steps)
+    h2d_ms = min(h2d_ms)
     e2e_step()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(w["stream"])
     for _ in range(e2e_steps):
         e2e_step()
-    e1.record(stream)
+    e1.record(w["stream"])
     barrier()
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
-    h2d = sum(t.numel() * t.element_size()
-              for t in (h_target, h_draft, h_tok, h_temp, h_unif, h_cu) if t is not None)
-    d2h = (h_st.numel() * 4 if mode == "sample" else 2 * B * 4 if mode == "mss" else
-           h_n.numel() * 4 + h_ot.numel() * 4 + ((h_keys.numel() * 4 + h_hit.numel()) if F else 0))
+    h2d = sum(t.numel() * t.element_size() for t in h.values() if t is not None)
+    d2h = (hold["st"].numel() * 4 if mode == "sample" else 2 * B * 4 if mode == "mss" else
+           hold["keys"].numel() * 4 + hold["hit"].numel() if mode == "predict" else
+           hold["n"].numel() * 4 + hold["ot"].numel() * 4 +
+           ((hold["keys"].numel() * 4 + hold["hit"].numel()) if F else 0))
+    big = h["target"] if h["target"] is not None else h["draft"]
+    placement = {"numa_nodes": numa_nodes(), "gpu_numa_node": gpu_numa_node(torch, dev),
+                 "pinned_input_pages": pages_node(big.data_ptr()),
+                 "cpu_affinity": len(os.sched_getaffinity(0))}
+
+    # the other configurations, after the headline (one GPU, default run)
+    side = {}
+    if world == 1 and args.workload == "cfg5-ssd" and not args.batch and not args.no_configs:
+        side_sampler = ClockSampler(gpu_uuid(torch, dev))
+        side_sampler.start()
+        for name in SIDE_CONFIGS:
+            ws_ = prepare(name, args, torch, sv, dev, 0, 1)
+            ms_ = measure(torch, ws_, max(5, args.steps // 2), 3, 0.15, barrier, dev, peak)
+            kb = ws_["lay"]["bytes"]
+            side[name] = {
+                "workload": WORKLOADS[name][1],
+                "rows": ws_["lay"]["rows"], "algorithmic_bytes": kb,
+                "ms": round(ms_["ms"], 5),
+                "rows_per_s": round(ws_["lay"]["rows"] / (ms_["ms"] / 1e3), 1),
+                "gbs_algorithmic": round(ms_["gbs"], 1), "frac": round(ms_["frac"], 4),
+                **({"ms_hot": round(ms_["hot"], 5),
+                    "frac_hot": round(kb / (ms_["hot"] / 1e3) / 1e9 / peak, 4)} if ms_["hot"] else {}),
+                "timing": "cold: L2 flushed before each call" if ms_["hot"] else "back to back",
+                "first_launch_ms": round(statistics.mean(ms_["first_ms"]), 5),
+                "second_launch_ms": round(statistics.mean(ms_["second_ms"]), 5),
+                "kernel_frac": round(kb / (ms_["kernel_ms"] / 1e3) / 1e9 / peak, 4),
+                "host_submit_us": round(ms_["submit_us"], 1),
+                "calls_timed": len(ms_["per_step"]) * ms_["reps"],
+            }
+            del ws_
+        side_clocks = side_sampler.stop()
 
     if rank != 0:
         if world > 1:
@@ -590,24 +835,29 @@ def run_ours(args) -> None:
         """What the last call decided (the workload's acceptance and hit rates)."""
         if mode == "sample":
             return {"rows_sampled": int(lay["rows"])}
+        if mode == "predict":
+            return {"hit_rate": round(float(w["hit"].float().mean().item()), 4)}
         if mode == "mss":
             acc = outs["accepted"].cpu().numpy()
             return {"candidate_accepted_rate": round(float((acc >= 0).mean()), 4),
                     "accepted_index_hist": np.bincount(acc + 1, minlength=MSS_M[args.workload] + 1).tolist()}
         n = outs["accept_len"].cpu().numpy()
-        d = {"mean_accept_len": round(float(n.mean()), 4),
-             "accept_len_hist": np.bincount(n, minlength=K + 1).tolist()}
+        dd = {"mean_accept_len": round(float(n.mean()), 4),
+              "accept_len_hist": np.bincount(n, minlength=K + 1).tolist()}
         if F:
-            d["hit_rate"] = round(float(hit.float().mean().item()), 4)
-        return d
+            dd["hit_rate"] = round(float(w["hit"].float().mean().item()), 4)
+        return dd
 
-    peak, peak_kind = measured_peak()
-    v_ms = statistics.mean(call_ms)
-    a_ms = statistics.mean(stats_ms)
     kernel_bytes = lay["bytes"]
-    achieved = kernel_bytes / (a_ms / 1e3) / 1e9
-    call_gbs = kernel_bytes / (ms_step / 1e3) / 1e9  # back-to-back calls, kernels overlapped
+    # the dominant kernel (the launch that streams the logits), timed apart
+    # from the call's other launch by the split event, on the launching stream
+    k_ms = m["kernel_ms"]
+    achieved = kernel_bytes / (k_ms / 1e3) / 1e9
+    call_gbs = kernel_bytes / (ms_step / 1e3) / 1e9
     traffic = recorded_traffic(args.workload)
+    kname = (f"launch {m['dominant'] + 1} of {w['per_call'][0]} "
+             f"({'bf16' if w['is_bf16'] else 'fp32'} {mode or ('ssd' if F else 'verify')}): "
+             + (sv.kernel_names(mode, F)[m["dominant"]] if hasattr(sv, "kernel_names") else "streams every logit once"))
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -616,28 +866,30 @@ def run_ours(args) -> None:
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
+        "repeats_per_step": m["reps"],
+        "ms_x_sm_mhz": round(ms_step * clocks["sm_mhz"], 2) if clocks.get("sm_mhz") else None,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded; see workloads.py)",
         "config": {
-            "workload": f"{args.workload}: {desc}",
+            "workload": f"{args.workload}: {w['desc']}",
             "B_per_gpu": B, "K": K, "V": V, "logits": spec.dtype, "F": F,
             **({"M": MSS_M[args.workload], "nodes": B} if mode == "mss" else {}),
-            **({"fanout": fanout} if fanout else {}),
+            **({"fanout": w["fanout"]} if w["fanout"] else {}),
             "rows_per_step_per_gpu": lay["rows"],
-            "l2": (f"inputs {in_bytes / 1e9:.2f} GB > {L2_BYTES / 2**20:.0f} MiB L2, no flush"
-                   if in_bytes > L2_BYTES else
-                   f"inputs {in_bytes / 1e6:.1f} MB fit in L2: between timed calls (outside "
+            "step": (f"one call; each of the {args.steps} timed steps is the mean of "
+                     f"{m['reps']} calls"),
+            "l2": (f"inputs {w['in_bytes'] / 1e9:.2f} GB > {L2_BYTES / 2**20:.0f} MiB L2, no flush"
+                   if w["in_bytes"] > L2_BYTES else
+                   f"inputs {w['in_bytes'] / 1e6:.1f} MB fit in L2: between timed calls (outside "
                    f"their events) a {2 * L2_BYTES / 2**20:.0f} MiB buffer is written, then "
                    f"another as large is read"),
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": (f"stats_kernel<{'bf16' if is_bf16 else 'fp32'},"
-                       f"{mode if mode in ('sample', 'mss') else 'ssd' if F else 'verify'}> "
-                       f"(reads every logit once)"),
+            "kernel": kname,
             "achieved": round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
@@ -646,28 +898,37 @@ def run_ours(args) -> None:
                           else "of fallback"),
             "traffic": traffic,
             "algorithmic_bytes_per_launch": kernel_bytes,
-            "avg_launch_ms": round(a_ms, 5),
+            "avg_launch_ms": round(k_ms, 5),
         },
-        "call": {"api": ("specv_saguaro_sample" if mode == "sample" else
+        "call": {"api": ("specv_predict_outcomes + specv_check_hit" if mode == "predict" else
+                         "specv_saguaro_sample" if mode == "sample" else
                          "specv_mss_verify" if mode == "mss" else
-                         "specv_ssd_round" if F else "specv_verify"), "launches": 2,
+                         "specv_ssd_round" if F else "specv_verify"),
+                 "launches": w["per_call"][0],
                  "ms": round(ms_step, 5),
-                 **({"ms_hot": round(hot_ms, 5)} if hot_ms is not None else {}),
-                 "ms_split": round(v_ms, 5),
+                 **({"ms_hot": round(m["hot"], 5)} if m["hot"] is not None else {}),
+                 "ms_split": round(statistics.mean(m["call_ms"]), 5),
                  "ms_split_p10_p50_p90": [round(float(x), 5) for x in
-                                          np.percentile(call_ms, [10, 50, 90])],
-                 "stats_ms": round(a_ms, 5),
-                 "decide_ms": round(statistics.mean(decide_ms), 5),
+                                          np.percentile(m["call_ms"], [10, 50, 90])],
+                 "first_launch_ms": round(statistics.mean(m["first_ms"]), 5),
+                 "second_launch_ms": round(statistics.mean(m["second_ms"]), 5),
+                 "host_submit_us": round(m["submit_us"], 1),
                  "gbs_algorithmic": round(call_gbs, 1), "frac": round(call_gbs / peak, 4)},
         "e2e": {"value": round(rows_total / (e2e_ms / 1e3), 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "h2d_copy_ms": round(h2d_ms, 4),
+                "h2d_gbs": round(h2d / (h2d_ms / 1e3) / 1e9, 1),
+                "host_placement": placement},
         "outcome": outcome_summary(),
-        "gpu_launches": gpu_launches,
+        "gpu_launches": m["launches"],
         "clocks": clocks,
     }
+    if side:
+        line["configs"] = side
+        line["configs_clocks"] = side_clocks
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec, mode=mode, saguaro=saguaro, workload=args.workload)
+        line["cpu_baseline"] = cpu_baseline(spec, mode=mode, saguaro=w["saguaro"], workload=args.workload)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -724,17 +985,28 @@ def run_reference(args) -> None:
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)  # about 1 s timed at cfg5
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="cfg5-ssd", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the configurations timed after the headline")
+    ap.add_argument("--timed-s", type=float, default=1.2,
+                    help="length of the headline's timed region (repeats per step)")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="host-only run of the multi-rank plumbing (gloo, no GPU, no kernels)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override B (smaller cases for profiling captures)")
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_ranks(args, argv))
+    if args.dry_run:
+        run_dry(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -649,59 +649,214 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
   return S.pick;
 }
 
-template <int DT, bool VEC, int MODE>
-__global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams P) {
-  using E = Elem<DT>;
-  constexpr int VW = E::VW;
-  constexpr bool kTopF = MODE == kModeSsd;      // outcome keys and hit
-  constexpr bool kSample = MODE == kModeSample;  // draft-side Saguaro sampling
-  constexpr bool kMss = MODE == kModeMss;        // candidates at token-tree nodes
-  extern __shared__ float segs[];  // [tiles * kWarps] segment sums of r
-  __shared__ PosStats ps[kMaxK + 1];
-  __shared__ Dec dec;
-  __shared__ FF cta_total[2];  // this CTA's residual mass, per attempt
-  __shared__ int32_t tok_slot;  // rank 0: the token found by the owner CTA
-  __shared__ float q_slot;      // rank 0 (sampler): sigma of that token
-  __shared__ float sg_d[kMaxK + 1];    // Saguaro: weighted mass of the top-F_s,
-  __shared__ float sg_zl[kMaxK + 1];   //   its F_s-th key (zl, il), and whether
-  __shared__ int32_t sg_il[kMaxK + 1]; //   the sent token is among them
-  __shared__ int32_t sg_xin[kMaxK + 1];
-  __shared__ float sg_kv[kMaxF];        // the sampler: its row's top-F_s keys
-  __shared__ int32_t sg_ki[kMaxF];
-  __shared__ int32_t sg_nk;
-  __shared__ DrawSmem draw;
-  __shared__ int32_t copy_fail;  // rank 0: a CTA's staged copies did not land in time
-  __shared__ RingBars ring_bars;
-  __shared__ int32_t pre_x[kMaxK];  // draft tokens, their logits and the uniforms,
-  __shared__ float pre_zt[kMaxK];   // fetched while the records are combined
-  __shared__ float pre_zd[kMaxK];
-  __shared__ float pre_u[kMaxK];
-  __shared__ WarpKeys wkeys[(kTopF || kSample) ? kWarps : 1];
+// The final step of an inverse-CDF draw over a slice [v0, v1) of row n,
+// run by one warp: the slice's per-warp segment sums segs[ntl * kWarps]
+// (shared memory, tile-major) and the mass before the slice (pre) locate the
+// segment where the running sum of r crosses tau, and a scan of its 32
+// vectors the logit.  Lanes own contiguous blocks of segments; a float-float
+// warp scan of the block sums finds the block that holds the crossing.
+// Inside it the walk runs in fp32, relative to the block's start: tau less
+// the mass before the block, rounded once, against the same additions that
+// formed the block sum (so a crossing found by the scan is found again, and
+// what rounding can move lies within a few ulps of the block's mass).
+// last_pos: tau lies at or past the end (rounding), take the last logit with
+// r > 0.  Returns the token in every lane (-1: no mass), and r at it in rv.
+template <int DT, bool VEC>
+__device__ __forceinline__ int owner_scan(const float* segs, int ntl, FF tau, FF pre, bool last_pos,
+                                          const void* rowt, const void* rowd, int64_t v0,
+                                          int64_t v1, int nv, int mode, float mt, float md, float c,
+                                          float ist, float isd, int xn, const SgW& sgw, float& rv_out) {
+  constexpr int VW = Elem<DT>::VW;
+  const int lane = threadIdx.x & 31;
+  const int nseg = ntl * kWarps;
+  const int per = (nseg + 31) / 32;
+  const int s0 = min(nseg, lane * per), s1 = min(nseg, s0 + per);
+  float bsum = 0.f;
+  int lastpos = -1;
+  for (int sg = s0; sg < s1; ++sg) {
+    const float g = segs[sg];
+    if (g > 0.f) {
+      bsum += g;
+      lastpos = sg;
+    }
+  }
+  const FF incl = warp_ffscan(ff(bsum), lane);
+  const FF bpre = ff_add(pre, ff_add(incl, -bsum));
+  const unsigned hitm = last_pos ? 0u
+                                     : __ballot_sync(0xffffffffu, bsum > 0.f && ff_gt(ff_add(bpre, bsum), tau));
+  const unsigned posm = __ballot_sync(0xffffffffu, lastpos >= 0);
+  int seg = -1;
+  float tseg = 0.f;  // U*R less the mass before the chosen segment
+  if (hitm) {
+    const int L = __ffs(hitm) - 1;
+    if (lane == L) {
+      const float t = ff_add(tau, ff_neg(bpre)).hi;
+      float cum = 0.f;
+      for (int sg = s0; sg < s1; ++sg) {
+        const float g = segs[sg];
+        if (g > 0.f) {
+          const float nx = cum + g;
+          if (nx > t) {
+            seg = sg;
+            tseg = t - cum;
+            break;
+          }
+          cum = nx;
+        }
+      }
+      if (seg < 0) seg = lastpos;  // rounding inside the block
+    }
+    seg = __shfl_sync(0xffffffffu, seg, L);
+    tseg = __shfl_sync(0xffffffffu, tseg, L);
+  }
+  const int lastseg = posm ? __shfl_sync(0xffffffffu, lastpos, 31 - __clz(posm)) : -1;
+  bool lp = last_pos || seg < 0;
+  if (seg < 0) seg = lastseg;
+  const int j = (seg / kWarps) * kThreads + (seg % kWarps) * 32 + lane;
+  float r[VW];
+#pragma unroll
+  for (int k = 0; k < VW; ++k) r[k] = 0.f;
+  if (seg >= 0 && j < nv)
+    residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, xn, sgw, r);
+  const int32_t base = static_cast<int32_t>(v0) + j * VW;
+  int found = -1;
+  float rv = 0.f;  // r at the found logit (the sampler reports it as sigma(t))
+  if (!lp) {
+    // the segment's 32 vectors: an fp32 scan relative to the segment start
+    float vs = 0.f;
+#pragma unroll
+    for (int k = 0; k < VW; ++k) vs += r[k];
+    float inc = vs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const float exc = __shfl_up_sync(0xffffffffu, inc, 1);
+    const unsigned m = __ballot_sync(0xffffffffu, vs > 0.f && inc > tseg);
+    if (m) {
+      if (lane == __ffs(m) - 1) {
+        float run = lane > 0 ? exc : 0.f;
+        int kk = -1, klast = -1;
+#pragma unroll
+        for (int k = 0; k < VW; ++k) {
+          if (r[k] > 0.f) {
+            run += r[k];
+            klast = k;
+            if (kk < 0 && run > tseg) kk = k;
+          }
+        }
+        const int ksel = kk >= 0 ? kk : klast;
+        found = base + ksel;
+#pragma unroll
+        for (int k = 0; k < VW; ++k)
+          if (k == ksel) rv = r[k];
+      }
+    } else {
+      lp = true;
+    }
+  }
+  if (lp) {
+    int kl = -1;
+#pragma unroll
+    for (int k = 0; k < VW; ++k)
+      if (r[k] > 0.f) kl = k;
+    const unsigned m = __ballot_sync(0xffffffffu, kl >= 0);
+    if (m && lane == 31 - __clz(m)) {
+      found = base + kl;
+#pragma unroll
+      for (int k = 0; k < VW; ++k)
+        if (k == kl) rv = r[k];
+    }
+  }
+  const unsigned mf = __ballot_sync(0xffffffffu, found >= 0);
+  rv_out = mf ? __shfl_sync(0xffffffffu, rv, __ffs(mf) - 1) : 0.f;
+  return mf ? __shfl_sync(0xffffffffu, found, __ffs(mf) - 1) : -1;
+}
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int CB = P.CB;
-  const int b = static_cast<int>(blockIdx.x / CB);
+// What a batch row's decision needs besides the records, the same on every
+// thread of every CTA that decides it.
+struct RowCtx {
+  int b;
+  int kb_in;    // the row's drafts (an MSS node's candidates); -1: bad count
+  int kb;       // max(kb_in, 0)
+  int npos;     // positions with records: 0..npos
+  int u_draw;   // the uniform of the final draw
+  float T, c;   // temperature, log2(e)/T
+  bool greedy, temp_ok, nd, sg_on;
+  int64_t u0;   // first record unit and output row of the batch row
+  RowLayout L;
+};
+
+template <int MODE>
+__device__ __forceinline__ RowCtx row_ctx(const DecideParams& P, int b) {
+  constexpr bool kTopF = MODE == kModeSsd;
+  constexpr bool kSample = MODE == kModeSample;
+  constexpr bool kMss = MODE == kModeMss;
+  RowCtx X;
+  X.b = b;
+  X.T = P.temp[b];
+  X.greedy = X.T == 0.f;
+  X.temp_ok = X.T >= 0.f && X.T < pos_inf();
+  X.c = X.greedy ? 1.f : temp_scale(X.T);
+  // records, outputs: [B, K+1] (an MSS node has one position)
+  X.u0 = kMss ? static_cast<int64_t>(b) : static_cast<int64_t>(b) * (P.K + 1);
+  X.L = row_layout(P.cu, P.ntok, b, P.K, P.t_bs, P.t_rs, P.d_bs, P.d_rs);
+  X.kb_in = X.L.kb;
+  if (kMss && P.ncand) {
+    const int m = P.ncand[b];
+    X.kb_in = (m >= 0 && m <= P.K) ? m : -1;
+  }
+  X.kb = X.kb_in < 0 ? 0 : X.kb_in;
+  X.npos = kMss ? 0 : X.kb;
+  X.u_draw = kMss ? P.K : X.kb;
+  X.nd = P.no_draft != 0;
+  X.sg_on = (kSample || (kTopF && P.sg_F > 0)) && !X.greedy && X.temp_ok;
+  return X;
+}
+
+// Shared memory of one batch row's decision.
+struct PrepSmem {
+  PosStats ps[kMaxK + 1];
+  Dec dec;
+  int32_t tok_slot;  // the token found by the final scan
+  float q_slot;      // the sampler: sigma of that token
+  float sg_d[kMaxK + 1];    // Saguaro: weighted mass of the top-F_s,
+  float sg_zl[kMaxK + 1];   //   its F_s-th key (zl, il), and whether
+  int32_t sg_il[kMaxK + 1]; //   the sent token is among them
+  int32_t sg_xin[kMaxK + 1];
+  float sg_kv[kMaxF];       // the sampler: its row's top-F_s keys
+  int32_t sg_ki[kMaxF];
+  int32_t sg_nk;
+  int32_t copy_fail;        // a staged copy of the row's passes did not land in time
+  int32_t pre_x[kMaxK];     // draft tokens, their logits and the uniforms,
+  float pre_zt[kMaxK];      // fetched while the records are combined
+  float pre_zd[kMaxK];
+  float pre_u[kMaxK];
+};
+
+// The decision of batch row X.b from its chunk records, by every thread of
+// one CTA: the records combined per position, the Saguaro keys of the draft
+// rows, and the accept test (or the first MSS candidate's test), leaving the
+// outcome in S.dec.  wkeys: kWarps warps' key scratch.  wait_primary: the
+// records come from the previous kernel on the stream (wait for it once the
+// inputs are fetched).  Ends with a CTA barrier.
+template <int DT, int MODE>
+__device__ __forceinline__ void decide_prepare(const DecideParams& P, const RowCtx& X, PrepSmem& S,
+                                               WarpKeys* wkeys, bool wait_primary) {
+  using E = Elem<DT>;
+  constexpr bool kTopF = MODE == kModeSsd;
+  constexpr bool kSample = MODE == kModeSample;
+  constexpr bool kMss = MODE == kModeMss;
+  const int b = X.b;
   const int K = P.K, F = P.F;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const float T = P.temp[b];
-  const bool greedy = T == 0.f;
-  const bool temp_ok = T >= 0.f && T < pos_inf();
-  const float c = greedy ? 1.f : temp_scale(T);
-  // records, outputs: [B, K+1] (an MSS node has one position)
-  const int64_t u0 = kMss ? static_cast<int64_t>(b) : static_cast<int64_t>(b) * (K + 1);
-  const RowLayout L = row_layout(P.cu, P.ntok, b, K, P.t_bs, P.t_rs, P.d_bs, P.d_rs);
-  int kb_in = L.kb;  // this row's drafts (an MSS node's candidates); -1: bad count
-  if (kMss && P.ncand) {
-    const int m = P.ncand[b];
-    kb_in = (m >= 0 && m <= K) ? m : -1;
-  }
-  const int kb = kb_in < 0 ? 0 : kb_in;
-  const int npos = kMss ? 0 : kb;     // positions with records: 0..npos
-  const int u_draw = kMss ? K : kb;   // the uniform of the final draw
-  const bool nd = P.no_draft != 0;
-
+  const bool greedy = X.greedy, temp_ok = X.temp_ok, nd = X.nd, sg_on = X.sg_on;
+  const float c = X.c;
+  const int64_t u0 = X.u0;
+  const RowLayout& L = X.L;
+  const int kb_in = X.kb_in, kb = X.kb, npos = X.npos;
   // ---- every CTA combines the records and decides (identical results) -------
   // The last warp first fetches what the decision needs besides the records.
   if (warp == kWarps - 1) {
@@ -713,20 +868,20 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
         zt = E::scalar(static_cast<const char*>(P.zt) + (L.t_off + ri * P.t_rs) * E::ES, x);
         if (!nd) zd = E::scalar(static_cast<const char*>(P.zd) + (L.d_off + ri * P.d_rs) * E::ES, x);
       }
-      pre_x[i] = x;
-      pre_zt[i] = zt;
-      pre_zd[i] = zd;
-      pre_u[i] = P.unif[L.u_off + i];
+      S.pre_x[i] = x;
+      S.pre_zt[i] = zt;
+      S.pre_zd[i] = zd;
+      S.pre_u[i] = P.unif[L.u_off + i];
     }
   }
   // Everything above reads only the call's inputs; the records below are
   // the row-statistics kernel's output, so wait for it to complete here.
-  pdl_wait_primary();
+  if (wait_primary) pdl_wait_primary();
   // Half a warp per position: positions 2w and 2w+1 on warp w, 16 per pass.
   for (int i0 = 2 * warp; i0 <= npos; i0 += 2 * kWarps) {
     const int i = i0 + (lane >> 4);
     const PosStats p = combine_position<16>(P.recs + (u0 + min(i, npos)) * P.nchunk, P.nchunk, c, lane & 15);
-    if ((lane & 15) == 0 && i <= npos) ps[i] = p;
+    if ((lane & 15) == 0 && i <= npos) S.ps[i] = p;
   }
   __syncthreads();
 
@@ -735,7 +890,6 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   // keys (the lookahead's merged candidates, which exclude the sent token x,
   // with x put back in key order), their mass in units of 2^((z - Md) c), and
   // the F_s-th key.  One warp per row.  Greedy rows are left one-hot.
-  const bool sg_on = (kSample || (kTopF && P.sg_F > 0)) && !greedy && temp_ok;
   if (sg_on) {
     const int nrows = kSample ? 1 : kb;
     const int ncand = static_cast<int>(P.nchunk) * F;
@@ -754,13 +908,13 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
         Lk = warp_keys(P.cand_v + u * ncand, P.cand_i + u * ncand, ncand, F, lane, wkeys[warp]);
       }
       const int fs = P.sg_F;
-      const int x = kSample ? -1 : pre_x[i];
-      const float zx = kSample ? neg_inf() : pre_zd[i];
+      const int x = kSample ? -1 : S.pre_x[i];
+      const float zx = kSample ? neg_inf() : S.pre_zd[i];
       const int pos = (x >= 0) ? __popc(__ballot_sync(0xffffffffu, lane < F && key_beats(Lk.v, Lk.i, zx, x)))
                                : F;
       const bool xin = x >= 0 && pos < fs;
       const int fl = xin ? fs - 1 : fs;  // list entries inside the top-F_s
-      const float Md = ps[i].Md;
+      const float Md = S.ps[i].Md;
       float d = (lane < fl && Lk.i != INT_MAX) ? ex2((Lk.v - Md) * c) : 0.f;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
@@ -770,19 +924,19 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
       const float lv = __shfl_sync(0xffffffffu, Lk.v, src < 0 ? 0 : src);
       const int32_t li = __shfl_sync(0xffffffffu, Lk.i, src < 0 ? 0 : src);
       if (lane == 0) {
-        sg_d[i] = d;
-        sg_zl[i] = src < 0 ? zx : lv;
-        sg_il[i] = src < 0 ? x : li;
-        sg_xin[i] = xin;
+        S.sg_d[i] = d;
+        S.sg_zl[i] = src < 0 ? zx : lv;
+        S.sg_il[i] = src < 0 ? x : li;
+        S.sg_xin[i] = xin;
       }
       if (kSample) {  // the keys themselves, for the chunk-local draw
         const bool valid = lane < fs && Lk.i != INT_MAX;
         if (valid) {
-          sg_kv[lane] = Lk.v;
-          sg_ki[lane] = Lk.i;
+          S.sg_kv[lane] = Lk.v;
+          S.sg_ki[lane] = Lk.i;
         }
         const unsigned vm = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0) sg_nk = __popc(vm);
+        if (lane == 0) S.sg_nk = __popc(vm);
       }
     }
     __syncthreads();
@@ -790,13 +944,13 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   // ---- MSS at a token-tree node ([CS349D] §6.4): warp 0 tests the first
   // candidate; each rejection is followed by a residual pass below ------------
   if (kMss && warp == 0) {
-    const PosStats& q = ps[0];
+    const PosStats& q = S.ps[0];
     int nf = 0;
     if (lane == 0 && temp_ok)
       nf = greedy ? ((q.bad & 1) || q.it == INT_MAX || q.id == INT_MAX)
                   : (!(q.St.hi >= 1.f) || q.Mt == kNegMax || !(q.Sd.hi >= 1.f) || q.Md == kNegMax);
     const bool cl = lane < kb;
-    const int x = cl ? pre_x[lane] : -1;
+    const int x = cl ? S.pre_x[lane] : -1;
     int status = temp_ok ? 0 : kBadTemp;
     if (kb_in < 0) status |= kBadCount;
     if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
@@ -809,19 +963,19 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     float t = 0.f;
     bool qpos = false;
     if (cl && ok && !greedy) {
-      const float lt = __fmul_rn(pre_zt[lane] - q.Mt, c);
-      const float ld = __fmul_rn(pre_zd[lane] - q.Md, c);
-      qpos = pre_zd[lane] != neg_inf();
+      const float lt = __fmul_rn(S.pre_zt[lane] - q.Mt, c);
+      const float ld = __fmul_rn(S.pre_zd[lane] - q.Md, c);
+      qpos = S.pre_zd[lane] != neg_inf();
       t = qpos ? __fmul_rn(ex2(__fsub_rn(lt, ld)), __fdiv_rn(q.Sd.hi, q.St.hi)) : 0.f;
     }
     const unsigned hitg = __ballot_sync(0xffffffffu, ok && cl && greedy && x == q.it);
     const int acc_g = hitg ? __ffs(hitg) - 1 : -1;
-    const bool a0 = __shfl_sync(0xffffffffu, cl && qpos && t >= pre_u[lane < kMaxK ? lane : 0], 0);
+    const bool a0 = __shfl_sync(0xffffffffu, cl && qpos && t >= S.pre_u[lane < kMaxK ? lane : 0], 0);
     float ap = 0.f;
     if (ok && cl && !naive) ap = greedy ? (lane == acc_g ? 1.f : 0.f) : (lane == 0 ? fminf(t, 1.f) : 0.f);
-    dec.ap[lane] = ap;
-    dec.px[lane] = t;
-    dec.qx[lane] = qpos ? 1.f : 0.f;
+    S.dec.ap[lane] = ap;
+    S.dec.px[lane] = t;
+    S.dec.qx[lane] = qpos ? 1.f : 0.f;
     if (lane == 0) {
       int acc = -1, token = -1, mode = 1, need = 0;
       if (ok) {
@@ -832,39 +986,39 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
           need = 1;  // a draw from p itself
         } else if (a0) {
           acc = 0;
-          token = pre_x[0];
+          token = S.pre_x[0];
         } else {
           need = 1;  // residual max(0, p - c_1 q), c_1 = 1
           mode = 0;
         }
       }
-      dec.n = 0;
-      dec.status = status;
-      dec.mode = mode;
-      dec.xn = -1;
-      dec.need_scan = need;
-      dec.token = token;
-      dec.acc = acc;
-      dec.owner = -1;
-      dec.last_pos = 0;
-      dec.mt = q.Mt;
-      dec.md = q.Md;
-      dec.ist = __fdiv_rn(1.f, q.St.hi);
-      dec.isd = __fdiv_rn(1.f, q.Sd.hi);
-      dec.sgc = 1.f;
-      dec.zl = pos_inf();
-      dec.il = -1;
-      dec.full_pass = 0;
-      dec.tau = ff(0.f);
-      dec.pre_mine = ff(0.f);
-      dec.R = ff(0.f);
-      dec.cff = ff(1.f);
-      dec.cq = 1.f;
-      dec.next = 1;
-      dec.again = 0;
-      tok_slot = token;
-      q_slot = 0.f;
-      copy_fail = 0;
+      S.dec.n = 0;
+      S.dec.status = status;
+      S.dec.mode = mode;
+      S.dec.xn = -1;
+      S.dec.need_scan = need;
+      S.dec.token = token;
+      S.dec.acc = acc;
+      S.dec.owner = -1;
+      S.dec.last_pos = 0;
+      S.dec.mt = q.Mt;
+      S.dec.md = q.Md;
+      S.dec.ist = __fdiv_rn(1.f, q.St.hi);
+      S.dec.isd = __fdiv_rn(1.f, q.Sd.hi);
+      S.dec.sgc = 1.f;
+      S.dec.zl = pos_inf();
+      S.dec.il = -1;
+      S.dec.full_pass = 0;
+      S.dec.tau = ff(0.f);
+      S.dec.pre_mine = ff(0.f);
+      S.dec.R = ff(0.f);
+      S.dec.cff = ff(1.f);
+      S.dec.cq = 1.f;
+      S.dec.next = 1;
+      S.dec.again = 0;
+      S.tok_slot = token;
+      S.q_slot = 0.f;
+      S.copy_fail = 0;
     }
   }
   if (!kMss && warp == 0) {
@@ -873,14 +1027,14 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     const float sgC = sg_on ? P.sg_C : 1.f;
     const FF one_m_c = two_sum(1.f, -sgC);  // 1 - C, exactly
     auto sdp = [&](int i) -> FF {
-      return sg_on ? ff_add(ps[i].Sd, ff_neg(ff_mul(one_m_c, sg_d[i]))) : ps[i].Sd;
+      return sg_on ? ff_add(S.ps[i].Sd, ff_neg(ff_mul(one_m_c, S.sg_d[i]))) : S.ps[i].Sd;
     };
     if (kSample && temp_ok && lane == 0) {  // the sampled row sits in the draft fields
-      const PosStats& q = ps[0];
+      const PosStats& q = S.ps[0];
       nf = greedy ? ((q.bad & 1) || q.id == INT_MAX)
                   : (!(q.Sd.hi >= 1.f) || q.Md == kNegMax || !(sdp(0).hi > 0.f));
     } else if (!kSample && lane <= kb && temp_ok) {
-      const PosStats& q = ps[lane];
+      const PosStats& q = S.ps[lane];
       const bool d_full = lane < kb && !nd;  // draft rows that are normalised
       const bool d_any = (MODE != kModeVerify) || d_full;
       if (greedy) {
@@ -892,118 +1046,150 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
       }
     }
     const bool acc_lane = lane < kb;
-    const int x = acc_lane ? pre_x[lane] : -1;
+    const int x = acc_lane ? S.pre_x[lane] : -1;
     int status = temp_ok ? 0 : kBadTemp;
     if (kb_in < 0) status |= kBadCount;
     if (__any_sync(0xffffffffu, nf)) status |= kNonFinite;
-    if (__any_sync(0xffffffffu, lane <= kb && (ps[lane].bad & 2))) status |= kTimeout;
+    if (__any_sync(0xffffffffu, lane <= kb && (S.ps[lane].bad & 2))) status |= kTimeout;
     if (__any_sync(0xffffffffu, acc_lane && (x < 0 || x >= P.V))) status |= kBadToken;
     const bool ok = !(status & kErrors);
     bool accept = false;
     float px = 0.f, qx = 0.f;
     if (acc_lane && ok) {
-      const PosStats& q = ps[lane];
+      const PosStats& q = S.ps[lane];
       if (greedy) {  // one-hot p and q (q at x itself without draft logits)
         px = (x == q.it) ? 1.f : 0.f;
         qx = (nd || x == q.id) ? 1.f : 0.f;
         accept = (x == q.it) && (nd || x == q.id);
       } else if (nd) {  // q_i(x_i) = 1: accept iff p_i(x_i) >= u
-        const float lt = __fmul_rn(pre_zt[lane] - q.Mt, c);
+        const float lt = __fmul_rn(S.pre_zt[lane] - q.Mt, c);
         px = __fdiv_rn(ex2(lt), q.St.hi);
         qx = 1.f;
-        accept = px >= pre_u[lane];
+        accept = px >= S.pre_u[lane];
       } else {
-        const float ztx = pre_zt[lane];
-        const float zdx = pre_zd[lane];
+        const float ztx = S.pre_zt[lane];
+        const float zdx = S.pre_zd[lane];
         const float lt = __fmul_rn(ztx - q.Mt, c);  // log2 of unnormalised p_i(x), q_i(x)
         const float ld = __fmul_rn(zdx - q.Md, c);
         const float St = q.St.hi, Sd = sdp(lane).hi;
-        const float wx = (sg_on && sg_xin[lane]) ? sgC : 1.f;  // Saguaro weight of x_i
+        const float wx = (sg_on && S.sg_xin[lane]) ? sgC : 1.f;  // Saguaro weight of x_i
         px = __fdiv_rn(ex2(lt), St);
         qx = __fdiv_rn(__fmul_rn(ex2(ld), wx), Sd);
         if (zdx != neg_inf() && wx > 0.f) {  // q_i(x_i) > 0
           const float ratio = __fdiv_rn(__fmul_rn(ex2(__fsub_rn(lt, ld)), __fdiv_rn(Sd, St)), wx);
-          accept = ratio >= pre_u[lane];
+          accept = ratio >= S.pre_u[lane];
         }
       }
     }
     const unsigned rej = __ballot_sync(0xffffffffu, acc_lane && !accept);
     const int n = ok ? (rej ? __ffs(rej) - 1 : kb) : 0;
     if (lane < kb) {
-      dec.px[lane] = px;
-      dec.qx[lane] = qx;
+      S.dec.px[lane] = px;
+      S.dec.qx[lane] = qx;
     }
     if (lane == 0) {
-      const PosStats& q = ps[n];
-      dec.n = n;
-      dec.status = status;
-      dec.mode = kSample ? 3 : (n < kb) ? (nd ? 2 : 0) : 1;
-      dec.xn = (n < kb) ? pre_x[n] : -1;
-      dec.need_scan = ok && !greedy;
-      dec.token = (ok && greedy) ? (kSample ? q.id : q.it) : -1;
-      dec.owner = -1;
-      dec.last_pos = 0;
+      const PosStats& q = S.ps[n];
+      S.dec.n = n;
+      S.dec.status = status;
+      S.dec.mode = kSample ? 3 : (n < kb) ? (nd ? 2 : 0) : 1;
+      S.dec.xn = (n < kb) ? S.pre_x[n] : -1;
+      S.dec.need_scan = ok && !greedy;
+      S.dec.token = (ok && greedy) ? (kSample ? q.id : q.it) : -1;
+      S.dec.owner = -1;
+      S.dec.last_pos = 0;
       // the sampler's row statistics are the draft fields of position 0
-      dec.mt = kSample ? q.Md : q.Mt;
-      dec.md = q.Md;
-      dec.ist = __fdiv_rn(1.f, (kSample ? sdp(0) : q.St).hi);
-      dec.isd = __fdiv_rn(1.f, ((n < kb) ? sdp(n) : q.Sd).hi);
+      S.dec.mt = kSample ? q.Md : q.Mt;
+      S.dec.md = q.Md;
+      S.dec.ist = __fdiv_rn(1.f, (kSample ? sdp(0) : q.St).hi);
+      S.dec.isd = __fdiv_rn(1.f, ((n < kb) ? sdp(n) : q.Sd).hi);
       // Saguaro weights on the residual: the draft row n (mode 0) or the row (mode 3)
       const bool weighted = sg_on && (kSample || (n < kb && !nd));
-      dec.sgc = weighted ? sgC : 1.f;
-      dec.zl = weighted ? sg_zl[n] : pos_inf();
-      dec.il = weighted ? sg_il[n] : -1;
+      S.dec.sgc = weighted ? sgC : 1.f;
+      S.dec.zl = weighted ? S.sg_zl[n] : pos_inf();
+      S.dec.il = weighted ? S.sg_il[n] : -1;
       // The chunk-local draw takes the weighted mass from the chunk sums less
       // (1 - C) x the keys' mass; when that correction is most of the row's
       // mass the difference loses fp32 precision, and the draw reads the whole
       // row instead (its residual total is then summed from the weighted
       // values themselves).
-      dec.full_pass = (kSample && sg_on) ? (__fmul_rn(one_m_c.hi, sg_d[0]) > 0.5f * q.Sd.hi) : 0;
-      dec.tau = ff(0.f);
-      dec.pre_mine = ff(0.f);
-      tok_slot = dec.token;
-      q_slot = (ok && greedy) ? 1.f : 0.f;
-      copy_fail = 0;
+      S.dec.full_pass = (kSample && sg_on) ? (__fmul_rn(one_m_c.hi, S.sg_d[0]) > 0.5f * q.Sd.hi) : 0;
+      S.dec.tau = ff(0.f);
+      S.dec.pre_mine = ff(0.f);
+      S.tok_slot = S.dec.token;
+      S.q_slot = (ok && greedy) ? 1.f : 0.f;
+      S.copy_fail = 0;
     }
   }
   __syncthreads();
+
+}
+
+template <int DT, bool VEC, int MODE>
+__global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams P) {
+  using E = Elem<DT>;
+  constexpr int VW = E::VW;
+  constexpr bool kTopF = MODE == kModeSsd;      // outcome keys and hit
+  constexpr bool kSample = MODE == kModeSample;  // draft-side Saguaro sampling
+  constexpr bool kMss = MODE == kModeMss;        // candidates at token-tree nodes
+  extern __shared__ float segs[];  // [tiles * kWarps] segment sums of r
+  __shared__ PrepSmem S;
+  __shared__ FF cta_total[2];  // this CTA's residual mass, per attempt
+  __shared__ DrawSmem draw;
+  __shared__ RingBars ring_bars;
+  __shared__ WarpKeys wkeys[(kTopF || kSample) ? kWarps : 1];
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int CB = P.CB;
+  const int b = static_cast<int>(blockIdx.x / CB);
+  const int K = P.K, F = P.F;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const RowCtx X = row_ctx<MODE>(P, b);
+  const bool greedy = X.greedy;
+  const float c = X.c;
+  const int64_t u0 = X.u0;
+  const RowLayout& L = X.L;
+  const int kb = X.kb, u_draw = X.u_draw;
+  const bool sg_on = X.sg_on;
+  decide_prepare<DT, MODE>(P, X, S, wkeys, true);
 
   // ---- a draw from a whole row's own distribution (the bonus after K accepted
   // drafts, the sampler) needs only the one chunk holding U * R: rank 0 finds
   // it from the chunk records and reads that chunk alone -----------------------
   // (P.local_draw: the host's choice, made when a chunk is shorter than one
   // CTA's slice of the row and holds at most kDrawTiles tiles)
-  const bool local_draw = dec.need_scan && P.local_draw && (dec.mode == 1 || (dec.mode == 3 && !dec.full_pass));
-  const bool scan = dec.need_scan && !local_draw;  // the residual pass over row n
+  const bool local_draw = S.dec.need_scan && P.local_draw && (S.dec.mode == 1 || (S.dec.mode == 3 && !S.dec.full_pass));
+  const bool scan = S.dec.need_scan && !local_draw;  // the residual pass over row n
   if (local_draw && rank == 0) {
-    const int nn = dec.n;
+    const int nn = S.dec.n;
     const char* row = kSample ? static_cast<const char*>(P.zd) + L.d_off * E::ES
                               : static_cast<const char*>(P.zt) +
                                     (L.t_off + static_cast<int64_t>(nn) * P.t_rs) * E::ES;
-    const SgW w = kSample ? SgW{dec.sgc, dec.zl, dec.il} : SgW{1.f, pos_inf(), -1};
+    const SgW w = kSample ? SgW{S.dec.sgc, S.dec.zl, S.dec.il} : SgW{1.f, pos_inf(), -1};
     const int tok = chunk_draw<DT, VEC>(P.recs + (u0 + nn) * P.nchunk, P.nchunk, P.chunk, P.V,
-                                        kSample, dec.mt, c, row,
-                                        P.unif[L.u_off + u_draw], sg_kv, sg_ki,
-                                        (kSample && sg_on) ? sg_nk : 0, w, kSample && P.half > 0,
+                                        kSample, S.dec.mt, c, row,
+                                        P.unif[L.u_off + u_draw], S.sg_kv, S.sg_ki,
+                                        (kSample && sg_on) ? S.sg_nk : 0, w, kSample && P.half > 0,
                                         draw);
     if (threadIdx.x == 0) {
-      tok_slot = tok;
-      q_slot = draw.q;
-      if (draw.fallback) dec.status |= kFallback;
+      S.tok_slot = tok;
+      S.q_slot = draw.q;
+      if (draw.fallback) S.dec.status |= kFallback;
     }
     __syncthreads();
   }
 
   // ---- this CTA's slice of row n; aligned rows start streaming it now, so the
   // copies run while the keys are merged ------------------------------------
-  const int n_dec = dec.n;
+  const int n_dec = S.dec.n;
   Chunk RC;
   RC.b = b;
   RC.i = n_dec;
   RC.rowt = kSample  // the sampler reads its one row through the target slot
                 ? static_cast<const char*>(P.zd) + L.d_off * E::ES
                 : static_cast<const char*>(P.zt) + (L.t_off + static_cast<int64_t>(n_dec) * P.t_rs) * E::ES;
-  RC.rowd = (dec.mode == 0)  // draft row n, read only for the residual max(p - q, 0)
+  RC.rowd = (S.dec.mode == 0)  // draft row n, read only for the residual max(p - q, 0)
                 ? static_cast<const char*>(P.zd) + (L.d_off + static_cast<int64_t>(n_dec) * P.d_rs) * E::ES
                 : nullptr;
   RC.v0 = static_cast<int64_t>(rank) * P.L;
@@ -1013,13 +1199,13 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   const bool staged = VEC && scan && P.stages > 0;
   if (staged) {
     Chunk SC = RC;
-    if (dec.mode != 0) SC.rowd = nullptr;  // mode 1 reads p_n only
+    if (S.dec.mode != 0) SC.rowd = nullptr;  // mode 1 reads p_n only
     ring_start<DT>(ring_bars, ring, P.stages, SC, P.stall == b + 1 && rank == 0);
     __syncthreads();
   }
 
   if (scan) {
-    const SgW sgw{dec.sgc, dec.zl, dec.il};
+    const SgW sgw{S.dec.sgc, S.dec.zl, S.dec.il};
     const void* rowt = RC.rowt;
     const void* rowd = RC.rowd;
     const int64_t v0 = RC.v0;
@@ -1031,9 +1217,9 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     // one when a zero mass falls back to p; an MSS node one per rejection ----
     const int max_pass = kMss ? kb + 2 : 2;
     for (int pass = 0; pass < max_pass; ++pass) {
-      const int mode = dec.mode;
-      const float mt = dec.mt, md = dec.md, ist = dec.ist;
-      const float isd = kMss ? __fmul_rn(dec.isd, dec.cq) : dec.isd;  // MSS: c_j q
+      const int mode = S.dec.mode;
+      const float mt = S.dec.mt, md = S.dec.md, ist = S.dec.ist;
+      const float isd = kMss ? __fmul_rn(S.dec.isd, S.dec.cq) : S.dec.isd;  // MSS: c_j q
       // (a CTA whose copies gave up reads its later passes directly: its ring
       // may still have a copy in flight, and the row is an error row anyway)
       if (staged && (pass == 0 || copies_ok)) {
@@ -1046,7 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
           __syncthreads();
         }
         copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd,
-                                      dec.xn, sgw, segs, ntl) && copies_ok;
+                                      S.dec.xn, sgw, segs, ntl) && copies_ok;
       } else
       for (int t0 = 0; t0 < ntl; t0 += kTileUnroll) {
         float s[kTileUnroll];
@@ -1056,7 +1242,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
           s[q] = 0.f;
           if (j < nv) {
             float r[VW];
-            residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, dec.xn, sgw, r);
+            residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, mode, mt, md, c, ist, isd, S.dec.xn, sgw, r);
 #pragma unroll
             for (int k = 0; k < VW; ++k) s[q] += r[k];
           }
@@ -1075,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
         if (lane == 0) cta_total[pass & 1] = acc;
       }
       cluster_sync();  // (1) per-CTA totals visible; every CTA of the cluster has started
-      if (!copies_ok && threadIdx.x == 0) *cluster.map_shared_rank(&copy_fail, 0) = 1;
+      if (!copies_ok && threadIdx.x == 0) *cluster.map_shared_rank(&S.copy_fail, 0) = 1;
       if (warp == 0) {
         const FF tr = (lane < CB) ? *cluster.map_shared_rank(&cta_total[pass & 1], lane) : ff(0.f);
         const FF incl = warp_ffscan(tr, lane);
@@ -1085,172 +1271,65 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
         const unsigned pos = __ballot_sync(0xffffffffu, tr.hi > 0.f);
         const FF pm = shfl(ff_add(incl, ff_neg(tr)), rank);
         if (lane == 0) {
-          dec.tau = tau;
-          dec.pre_mine = pm;
-          dec.R = R;
-          dec.again = 0;
-          if (kMss && mode == 0 && dec.next < kb && R.hi > 0.f) {
+          S.dec.tau = tau;
+          S.dec.pre_mine = pm;
+          S.dec.R = R;
+          S.dec.again = 0;
+          if (kMss && mode == 0 && S.dec.next < kb && R.hi > 0.f) {
             // MSS: R = D_j; candidate j is accepted iff
             // p_j(x_j)/q(x_j) = max(0, t_j - c_j) / D_j >= u_j
-            const int j = dec.next;
-            const FF d = ff_add(ff(dec.px[j]), ff_neg(dec.cff));
-            const float a = (dec.qx[j] > 0.f && d.hi > 0.f) ? __fdiv_rn(d.hi, R.hi) : 0.f;
-            dec.ap[j] = fminf(a, 1.f);
-            if (dec.qx[j] > 0.f && a >= pre_u[j]) {
-              dec.acc = j;
-              dec.token = pre_x[j];
-              tok_slot = pre_x[j];
+            const int j = S.dec.next;
+            const FF d = ff_add(ff(S.dec.px[j]), ff_neg(S.dec.cff));
+            const float a = (S.dec.qx[j] > 0.f && d.hi > 0.f) ? __fdiv_rn(d.hi, R.hi) : 0.f;
+            S.dec.ap[j] = fminf(a, 1.f);
+            if (S.dec.qx[j] > 0.f && a >= S.pre_u[j]) {
+              S.dec.acc = j;
+              S.dec.token = S.pre_x[j];
+              S.tok_slot = S.pre_x[j];
             } else {  // rejected: c_{j+1} = c_j + D_j, one more pass
-              dec.cff = ff_add(dec.cff, R);
-              dec.cq = dec.cff.hi;
-              dec.next = j + 1;
-              dec.again = 1;
+              S.dec.cff = ff_add(S.dec.cff, R);
+              S.dec.cq = S.dec.cff.hi;
+              S.dec.next = j + 1;
+              S.dec.again = 1;
             }
           } else if (R.hi > 0.f) {
             if (own) {
-              dec.owner = __ffs(own) - 1;
+              S.dec.owner = __ffs(own) - 1;
             } else {  // U*R >= R after rounding: the last index with r > 0
-              dec.owner = 31 - __clz(pos);
-              dec.last_pos = 1;
-              dec.status |= kFallback;
+              S.dec.owner = 31 - __clz(pos);
+              S.dec.last_pos = 1;
+              S.dec.status |= kFallback;
             }
-          } else if (dec.mode != 1) {
-            dec.mode = 1;  // zero residual mass: draw from p_n instead
-            dec.status |= kFallback;
-            dec.again = 1;
+          } else if (S.dec.mode != 1) {
+            S.dec.mode = 1;  // zero residual mass: draw from p_n instead
+            S.dec.status |= kFallback;
+            S.dec.again = 1;
           }
         }
       }
       __syncthreads();  // the decision on the owner, made by warp 0, seen by the CTA
-      if (!dec.again) break;
+      if (!S.dec.again) break;
     }
 
     // ---- owner CTA: locate the crossing segment, then scan it --------------
-    if (rank == dec.owner && warp == 0) {
-      // lanes own contiguous blocks of segments; a float-float warp scan of
-      // the block sums finds the block that holds the crossing.  Inside it
-      // the walk runs in fp32, relative to the block's start: U*R less the
-      // mass before the block, rounded once, against the same additions that
-      // formed the block sum (so a crossing found by the scan is found again,
-      // and what rounding can move lies within a few ulps of the block's mass)
-      const int nseg = ntl * kWarps;
-      const FF tau = dec.tau;
-      const int per = (nseg + 31) / 32;
-      const int s0 = min(nseg, lane * per), s1 = min(nseg, s0 + per);
-      float bsum = 0.f;
-      int lastpos = -1;
-      for (int sg = s0; sg < s1; ++sg) {
-        const float g = segs[sg];
-        if (g > 0.f) {
-          bsum += g;
-          lastpos = sg;
-        }
-      }
-      const FF incl = warp_ffscan(ff(bsum), lane);
-      const FF bpre = ff_add(dec.pre_mine, ff_add(incl, -bsum));
-      const unsigned hitm = dec.last_pos ? 0u
-                                         : __ballot_sync(0xffffffffu, bsum > 0.f && ff_gt(ff_add(bpre, bsum), tau));
-      const unsigned posm = __ballot_sync(0xffffffffu, lastpos >= 0);
-      int seg = -1;
-      float tseg = 0.f;  // U*R less the mass before the chosen segment
-      if (hitm) {
-        const int L = __ffs(hitm) - 1;
-        if (lane == L) {
-          const float t = ff_add(tau, ff_neg(bpre)).hi;
-          float cum = 0.f;
-          for (int sg = s0; sg < s1; ++sg) {
-            const float g = segs[sg];
-            if (g > 0.f) {
-              const float nx = cum + g;
-              if (nx > t) {
-                seg = sg;
-                tseg = t - cum;
-                break;
-              }
-              cum = nx;
-            }
-          }
-          if (seg < 0) seg = lastpos;  // rounding inside the block
-        }
-        seg = __shfl_sync(0xffffffffu, seg, L);
-        tseg = __shfl_sync(0xffffffffu, tseg, L);
-      }
-      const int lastseg = posm ? __shfl_sync(0xffffffffu, lastpos, 31 - __clz(posm)) : -1;
-      bool lp = dec.last_pos || seg < 0;
-      if (seg < 0) seg = lastseg;
-      const int j = (seg / kWarps) * kThreads + (seg % kWarps) * 32 + lane;
-      float r[VW];
-#pragma unroll
-      for (int k = 0; k < VW; ++k) r[k] = 0.f;
-      if (seg >= 0 && j < nv)
-        residual_vec<DT, VEC>(rowt, rowd, v0, v1, j, dec.mode, dec.mt, dec.md, c, dec.ist,
-                              kMss ? __fmul_rn(dec.isd, dec.cq) : dec.isd, dec.xn, sgw, r);
-      const int32_t base = static_cast<int32_t>(v0) + j * VW;
-      int found = -1;
-      float rv = 0.f;  // r at the found logit (the sampler reports it as sigma(t))
-      if (!lp) {
-        // the segment's 32 vectors: an fp32 scan relative to the segment start
-        float vs = 0.f;
-#pragma unroll
-        for (int k = 0; k < VW; ++k) vs += r[k];
-        float inc = vs;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += y;
-        }
-        const float exc = __shfl_up_sync(0xffffffffu, inc, 1);
-        const unsigned m = __ballot_sync(0xffffffffu, vs > 0.f && inc > tseg);
-        if (m) {
-          if (lane == __ffs(m) - 1) {
-            float run = lane > 0 ? exc : 0.f;
-            int kk = -1, klast = -1;
-#pragma unroll
-            for (int k = 0; k < VW; ++k) {
-              if (r[k] > 0.f) {
-                run += r[k];
-                klast = k;
-                if (kk < 0 && run > tseg) kk = k;
-              }
-            }
-            const int ksel = kk >= 0 ? kk : klast;
-            found = base + ksel;
-#pragma unroll
-            for (int k = 0; k < VW; ++k)
-              if (k == ksel) rv = r[k];
-          }
-        } else {
-          lp = true;
-        }
-      }
-      if (lp) {
-        int kl = -1;
-#pragma unroll
-        for (int k = 0; k < VW; ++k)
-          if (r[k] > 0.f) kl = k;
-        const unsigned m = __ballot_sync(0xffffffffu, kl >= 0);
-        if (m && lane == 31 - __clz(m)) {
-          found = base + kl;
-#pragma unroll
-          for (int k = 0; k < VW; ++k)
-            if (k == kl) rv = r[k];
-        }
-      }
-      const unsigned mf = __ballot_sync(0xffffffffu, found >= 0);
-      const int tok = mf ? __shfl_sync(0xffffffffu, found, __ffs(mf) - 1) : -1;
-      const float rq = mf ? __shfl_sync(0xffffffffu, rv, __ffs(mf) - 1) : 0.f;
+    if (rank == S.dec.owner && warp == 0) {
+      float rq;
+      const int tok = owner_scan<DT, VEC>(segs, ntl, S.dec.tau, S.dec.pre_mine, S.dec.last_pos != 0,
+                                          rowt, rowd, v0, v1, nv, S.dec.mode, S.dec.mt, S.dec.md, c,
+                                          S.dec.ist, kMss ? __fmul_rn(S.dec.isd, S.dec.cq) : S.dec.isd,
+                                          S.dec.xn, sgw, rq);
       if (lane == 0) {
-        *cluster.map_shared_rank(&tok_slot, 0) = tok;
+        *cluster.map_shared_rank(&S.tok_slot, 0) = tok;
         // sigma(t) = r(t) / R: the pass's own total, free of the cancellation
         // in the weighted normaliser
-        if (kSample) *cluster.map_shared_rank(&q_slot, 0) = __fdiv_rn(rq, dec.R.hi);
+        if (kSample) *cluster.map_shared_rank(&S.q_slot, 0) = __fdiv_rn(rq, S.dec.R.hi);
       }
     }
   }
   // ---- outcome keys, while the owner CTA's warp 0 scans: warps 1..7 of CTA
   // r merge lookaheads r, r + CB, ... (one warp each, all at once) -----------
   if (kTopF && warp > 0) {
-    const bool ok = !(dec.status & kErrors);
+    const bool ok = !(S.dec.status & kErrors);
     for (int k = rank + (warp - 1) * CB; k <= K; k += CB * (kWarps - 1)) {
       const int64_t u = u0 + k;
       const WarpTopF L = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
@@ -1271,16 +1350,16 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
 
   // ---- outputs, written by rank 0 ---------------------------------------------
   if (kMss && rank == 0) {  // a node: its token, the accepted candidate, accept probabilities
-    const int status = dec.status | (copy_fail ? kTimeout : 0);
+    const int status = S.dec.status | (S.copy_fail ? kTimeout : 0);
     const bool ok = !(status & kErrors);
     const int t = threadIdx.x;
-    const int32_t token = ok ? tok_slot : -1;
+    const int32_t token = ok ? S.tok_slot : -1;
     if (t == 0) {
-      int acc = ok ? dec.acc : -1;
+      int acc = ok ? S.dec.acc : -1;
       if (ok && P.naive) {  // naive sampling: the first candidate equal to the draw
         acc = -1;
         for (int j = 0; j < kb; ++j)
-          if (pre_x[j] == token) {
+          if (S.pre_x[j] == token) {
             acc = j;
             break;
           }
@@ -1289,33 +1368,33 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
       P.mss_acc[b] = acc;
       if (P.row_status) P.row_status[b] = ok ? (status & kFallback) : (status & kErrors);
     }
-    if (P.mss_ap && t < K) P.mss_ap[static_cast<int64_t>(b) * K + t] = (ok && t < kb) ? dec.ap[t] : 0.f;
+    if (P.mss_ap && t < K) P.mss_ap[static_cast<int64_t>(b) * K + t] = (ok && t < kb) ? S.dec.ap[t] : 0.f;
   }
   if (!kMss && rank == 0) {
     // A slice whose staged copies did not land makes the row an error row
     // (read after the barrier above, so the same on every thread).
-    const int status = dec.status | (copy_fail ? kTimeout : 0);
+    const int status = S.dec.status | (S.copy_fail ? kTimeout : 0);
     const bool ok = !(status & kErrors);
-    const int n = dec.n;
+    const int n = S.dec.n;
     const int t = threadIdx.x;
-    const int32_t token = tok_slot;
+    const int32_t token = S.tok_slot;
     if (t <= K) {
       int32_t v = -1;
-      if (ok) v = (t < n) ? pre_x[t] : (t == n ? token : -1);
+      if (ok) v = (t < n) ? S.pre_x[t] : (t == n ? token : -1);
       P.out_tokens[u0 + t] = v;
     }
     if (t < K) {
-      if (t < kb && P.p_draft) P.p_draft[L.tok0 + t] = ok ? dec.px[t] : 0.f;
-      if (t < kb && P.q_draft) P.q_draft[L.tok0 + t] = ok ? dec.qx[t] : 0.f;
+      if (t < kb && P.p_draft) P.p_draft[L.tok0 + t] = ok ? S.dec.px[t] : 0.f;
+      if (t < kb && P.q_draft) P.q_draft[L.tok0 + t] = ok ? S.dec.qx[t] : 0.f;
     }
-    if (kTopF && copy_fail)
+    if (kTopF && S.copy_fail)
       for (int e = t; e < (K + 1) * F; e += kThreads) {
         P.keys[u0 * F + e] = -1;
         if (P.key_logits) P.key_logits[u0 * F + e] = neg_inf();
       }
     if (t == 0) {
       if (kSample) {
-        if (P.q_draft) P.q_draft[b] = ok ? q_slot : 0.f;  // sigma(token)
+        if (P.q_draft) P.q_draft[b] = ok ? S.q_slot : 0.f;  // sigma(token)
       } else {
         P.accept_len[b] = ok ? n : 0;
       }

@@ -97,3 +97,47 @@ def test_reference_arm_is_silent_on_other_ranks():
     p = _run_reference({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+def test_gpus_flag_spawns_ranks_dry_run():
+    """`bench.py --gpus 2` outside torchrun starts two ranks itself; in the
+    host-only dry mode (gloo, no kernels) rank 0 prints one line with the
+    world size and the rows of both shards."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run",
+                        "--workload", "cfg3", "--steps", "3", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, p.stdout
+    line = json.loads(lines[0])
+    assert line["dry_run"] is True and line["value"] is None
+    assert line["n_gpus"] == 2 and line["scaling"] == "weak"
+    assert line["rows_per_step_all_ranks"] == 2 * 64 * 5  # two shards of B=64 rows, K+1 = 5
+
+
+def test_gpus_flag_without_enough_gpus_fails():
+    """Asking for more GPUs than the node has is an error, not a silent
+    one-GPU run."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--steps", "3", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert p.returncode != 0
+    assert "error" in json.loads(p.stdout.strip().splitlines()[-1])
+
+
+def test_pinned_page_placement_is_read_from_numa_maps():
+    """The host placement recorded beside the end-to-end figure: the NUMA
+    node(s) holding a buffer's pages, from /proc/self/numa_maps."""
+    import numpy as np
+    a = np.ones(1 << 22, np.uint8)  # 4 MiB, touched
+    nodes = bench.numa_nodes()
+    placed = bench.pages_node(a.ctypes.data)
+    if not os.path.exists("/proc/self/numa_maps") or not nodes:
+        pytest.skip("no NUMA information on this host")
+    assert placed and all(k.startswith("N") and int(k[1:]) in nodes for k in placed)
+    assert sum(placed.values()) >= 1

@@ -2,9 +2,13 @@
 configuration bench.py times (inputs laid out by bench.py's own code):
 the Saguaro sampler over the 2304 draft rows of a round (16-trip chunks, the
 32-tile chunk-local draw), per-row draft counts over packed rows, and
-verification without draft logits.  Sampled rows against the oracle, the
-same bars as the smaller cases (tokens and accept lengths exact except
-boundary rows, probabilities within 1e-5, error bits exact)."""
+verification without draft logits.  Every row against the oracle, the same
+bars as the smaller cases (tokens and accept lengths exact except boundary
+rows, probabilities within 1e-5, error bits exact).  The oracle flags a row
+as a boundary case when a uniform lies within 1e-6 of a ratio or CDF step;
+config 5's Zipf-like tail puts many draws from p on steps narrower than that,
+so the flagged rows are counted and reported, and the rows where the GPU and
+the oracle differ (every one of them flagged) are bounded: at most 2%."""
 import dataclasses
 
 import numpy as np
@@ -46,7 +50,7 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def test_sampler_full_size_sampled(sv, olib, bench):
+def test_sampler_full_size(sv, olib, bench):
     spec, _ = bench.WORKLOADS["cfg5-sample"]
     F, C = bench.SAGUARO["cfg5-sample"]
     lay = bench.lay_out(wl.generate(spec), spec, "sample")
@@ -57,20 +61,36 @@ def test_sampler_full_size_sampled(sv, olib, bench):
     n = z.shape[0]
     assert n == 2304 and (g["row_status"] & oracle.ROW_ERRORS == 0).all()
     assert ((g["tokens"] >= 0) & (g["tokens"] < spec.V)).all()
-    rows = np.random.default_rng(11).choice(n, 32, replace=False)
-    o = oracle.saguaro_sample(z[rows], T[rows], F, C, U[rows], lib=olib)
-    for k, b in enumerate(rows):
-        if g["tokens"][b] == o["tokens"][k]:
-            assert abs(g["q"][b] - o["q"][k]) <= PROB_TOL, (b, g["q"][b], o["q"][k])
-            continue
+    o = oracle.saguaro_sample(z, T, F, C, U, lib=olib)
+    same = g["tokens"] == o["tokens"]
+    assert np.abs(g["q"][same] - o["q"][same]).max(initial=0.0) <= PROB_TOL
+    boundary = 0
+    for b in np.flatnonzero(~same):
+        # a differing token must sit on a CDF step within 1e-6 of the uniform
         q = oracle.saguaro_probs(z[b], float(T[b]), F, C, lib=olib)
         cs = np.cumsum(q)
-        t = int(o["tokens"][k])
+        t = int(o["tokens"][b])
         lo = cs[t - 1] if t > 0 else 0.0
         assert min(abs(U[b] - lo), abs(cs[t] - U[b])) < 1e-6, (b, g["tokens"][b], t)
+        boundary += 1
+    print(f"sampler cfg5: differing rows {boundary}/{n} (each on a CDF step within 1e-6)")
+    assert boundary <= max(1, n // 50)
 
 
-def test_ragged_full_size_sampled(sv, olib, bench):
+def _ragged_rows(data, kb, rows):
+    """The packed inputs of `rows` alone (their own prefix sums)."""
+    sub = {k: data[k][rows] for k in ("target", "draft", "tokens", "temperature", "uniforms")}
+    kr = kb[rows]
+    cu_s = np.cumsum(kr).astype(np.int32)
+    tgt = np.concatenate([sub["target"][i, :kr[i] + 1] for i in range(len(rows))])
+    dft = np.concatenate([sub["draft"][i, :kr[i]] for i in range(len(rows))])
+    tok = np.concatenate([sub["tokens"][i, :kr[i]] for i in range(len(rows))]).astype(np.int32)
+    uni = np.concatenate([np.append(sub["uniforms"][i, :kr[i]], sub["uniforms"][i, -1])
+                          for i in range(len(rows))]).astype(np.float32)
+    return tgt, dft, cu_s, tok, sub["temperature"], uni
+
+
+def test_ragged_full_size(sv, olib, bench):
     spec, _ = bench.WORKLOADS["cfg5-ragged"]
     data = wl.generate(spec)
     lay = bench.lay_out(data, spec, "ragged")
@@ -82,27 +102,26 @@ def test_ragged_full_size_sampled(sv, olib, bench):
     g = {k: v.cpu().numpy() for k, v in g.items()}
     kb = np.diff(np.concatenate([[0], cu]))
     assert (g["accept_len"] <= kb).all() and (g["row_status"] & oracle.ROW_ERRORS == 0).all()
-    rows = np.sort(np.random.default_rng(12).choice(B, 16, replace=False))
-    sub = {k: data[k][rows] for k in ("target", "draft", "tokens", "temperature", "uniforms")}
-    kr = kb[rows]
-    cu_s = np.cumsum(kr).astype(np.int32)
-    tgt = np.concatenate([sub["target"][i, :kr[i] + 1] for i in range(len(rows))])
-    dft = np.concatenate([sub["draft"][i, :kr[i]] for i in range(len(rows))])
-    tok = np.concatenate([sub["tokens"][i, :kr[i]] for i in range(len(rows))]).astype(np.int32)
-    uni = np.concatenate([np.append(sub["uniforms"][i, :kr[i]], sub["uniforms"][i, -1])
-                          for i in range(len(rows))]).astype(np.float32)
-    o = oracle.verify_ragged(tgt, dft, cu_s, tok, sub["temperature"], uni, K, nthreads=0, lib=olib)
+    # the oracle on the packed rows exactly as laid out for the GPU
+    o = oracle.verify_ragged(lay["target"], lay["draft"], cu, lay["tokens"], lay["temperature"],
+                             lay["uniforms"], K, nthreads=0, lib=olib)
     ok = o["boundary"] == 0
-    assert np.array_equal(g["accept_len"][rows][ok], o["accept_len"][ok])
-    assert np.array_equal(g["out_tokens"][rows][ok], o["out_tokens"][ok])
-    c0 = np.concatenate([[0], cu[:-1]])
-    gp = np.concatenate([g["p_draft"][c0[b]:cu[b]] for b in rows])
-    gq = np.concatenate([g["q_draft"][c0[b]:cu[b]] for b in rows])
-    assert np.abs(gp - o["p"]).max(initial=0) <= PROB_TOL
-    assert np.abs(gq - o["q"]).max(initial=0) <= PROB_TOL
+    assert np.array_equal(g["accept_len"][ok], o["accept_len"][ok])
+    assert np.array_equal(g["out_tokens"][ok], o["out_tokens"][ok])
+    assert np.abs(g["p_draft"] - o["p"]).max(initial=0) <= PROB_TOL
+    assert np.abs(g["q_draft"] - o["q"]).max(initial=0) <= PROB_TOL
+    nb = int((~ok).sum())
+    nd = int(((g["accept_len"] != o["accept_len"]) | (g["out_tokens"] != o["out_tokens"]).any(axis=1)).sum())
+    print(f"ragged cfg5: boundary rows {nb}/{B}, differing rows {nd}")
+    assert nd <= max(1, B // 50)
+    # the same rows packed on their own give the same outcome (prefix sums)
+    rows = np.arange(0, B, 37)
+    o2 = oracle.verify_ragged(*_ragged_rows(data, kb, rows), K, nthreads=0, lib=olib)
+    assert np.array_equal(o2["accept_len"], o["accept_len"][rows])
+    assert np.array_equal(o2["out_tokens"], o["out_tokens"][rows])
 
 
-def test_no_draft_full_size_sampled(sv, olib, bench):
+def test_no_draft_full_size(sv, olib, bench):
     spec, _ = bench.WORKLOADS["cfg5-nodraft"]
     data = wl.generate(spec)
     g = sv.specv_verify(dev(data["target"]), None, dev(data["tokens"]),
@@ -110,11 +129,14 @@ def test_no_draft_full_size_sampled(sv, olib, bench):
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in g.items()}
     assert (g["row_status"] & oracle.ROW_ERRORS == 0).all()
-    rows = np.random.default_rng(13).choice(spec.B, 16, replace=False)
-    o = oracle.verify(data["target"][rows], None, data["tokens"][rows], data["temperature"][rows],
-                      data["uniforms"][rows], nthreads=0, lib=olib, no_draft=True)
+    o = oracle.verify(data["target"], None, data["tokens"], data["temperature"],
+                      data["uniforms"], nthreads=0, lib=olib, no_draft=True)
     ok = o["boundary"] == 0
-    assert np.array_equal(g["accept_len"][rows][ok], o["accept_len"][ok])
-    assert np.array_equal(g["out_tokens"][rows][ok], o["out_tokens"][ok])
-    assert np.abs(g["p_draft"][rows] - o["p"]).max() <= PROB_TOL
+    assert np.array_equal(g["accept_len"][ok], o["accept_len"][ok])
+    assert np.array_equal(g["out_tokens"][ok], o["out_tokens"][ok])
+    assert np.abs(g["p_draft"] - o["p"]).max() <= PROB_TOL
     assert (g["q_draft"] == 1.0).all()
+    nb = int((~ok).sum())
+    nd = int(((g["accept_len"] != o["accept_len"]) | (g["out_tokens"] != o["out_tokens"]).any(axis=1)).sum())
+    print(f"no-draft cfg5: boundary rows {nb}/{spec.B}, differing rows {nd}")
+    assert nd <= max(1, spec.B // 50)
