@@ -34,6 +34,12 @@
  *     batch row gets accept length 0 and tokens -1 (and, in an SSD round, -1
  *     keys and no hit); specv_predict_outcomes gives -1 keys at the lookaheads
  *     whose draft row or sent token is invalid.
+ *   - Launches.  specv_verify, specv_ssd_round, specv_saguaro_sample and
+ *     specv_mss_verify are two kernels: one streaming pass over every logit
+ *     (per-chunk statistics and candidates into the workspace), then one
+ *     decision per batch row (launched as a programmatic dependent of the
+ *     first).  The workspace needs no initialisation: everything a call
+ *     reads from it is written earlier in the same call.
  *   - Limits: 1 <= K <= 32, 0 <= B, 1 <= F <= 32, 1 <= V < 2^31 (in practice
  *     up to about 10^8: beyond that a CTA's table of partial sums no longer
  *     fits in shared memory and the call returns SPECV_ERR_UNSUPPORTED).
@@ -160,15 +166,22 @@ specv_status specv_verify(const specv_verify_args* args, void* workspace,
  * Its scratch is a fixed array of SPECV_NOALLOC_SCRATCH_BYTES bytes of device
  * memory built into the library; every GPU that loads the library holds one
  * copy until the process exits.  A call whose specv_verify_workspace_bytes()
- * exceeds it returns SPECV_ERR_UNSUPPORTED before any launch (8 MiB covers,
- * e.g., B = 256, K = 8, V = 152064 fp32 with a wide margin).
+ * exceeds it returns SPECV_ERR_UNSUPPORTED before any launch.  With the
+ * default chunk sizes 8 MiB covers, e.g., B = 256, K = 8, V = 152064 fp32
+ * (about 1.1 MB); the tuning variable SPECV_ITERS changes the chunk size,
+ * hence the scratch a call needs, and a call it pushes past the limit is
+ * refused the same way.
  *
  * The first call on a device looks up the scratch's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  All calls on a device share the one
- * scratch array, which keeps the last call's contents (nothing in it needs to
- * start at zero): calls that can overlap on the GPU -- other streams, other
- * host threads -- race and corrupt each other's results, so serialise them.
+ * (cudaGetSymbolAddress, with that device current) and caches it per device
+ * index for the life of the process; make that first call before any stream
+ * capture.  The cache assumes one (primary) CUDA context per device that is
+ * not reset: after cudaDeviceReset, or from a second context on the same
+ * device, the cached address is stale -- do not call this entry point there.
+ * All calls on a device share the one scratch array, which keeps the last
+ * call's contents (nothing in it needs to start at zero): calls that can overlap on the GPU
+ * -- other streams, other host threads -- race and corrupt each other's
+ * results, so serialise them.
  */
 #define SPECV_NOALLOC_SCRATCH_BYTES (8u << 20)
 specv_status specv_verify_noalloc(const specv_verify_args* args, void* stream);

@@ -33,21 +33,39 @@ def _stale(out: str) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, out: str = LIB) -> str:
+    """Each translation unit compiled to an object in parallel (one per kernel
+    mode), then linked into the shared library."""
     if not force and not _stale(out):
         return out
     nvcc = _nvcc()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
-    cmd = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-I" + INCLUDE, "-cudart", "shared", "-Xlinker", "-rpath," + cuda_lib,
-           "-o", out + ".tmp"] + sources()
+    objdir = os.path.join(PKG, "_build")
+    os.makedirs(objdir, exist_ok=True)
+    common = [nvcc, ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
+        common.insert(1, "-Xptxas=-v")
+    procs = []
+    for src in sources():
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
+        procs.append((src, obj, subprocess.Popen(common + ["-c", src, "-o", obj],
+                                                 stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                                 text=True)))
+    logs, failed = [], []
+    for src, obj, p in procs:
+        o, e = p.communicate()
+        logs.append(o + e)
+        if p.returncode != 0:
+            failed.append(src)
+    if failed:
+        raise RuntimeError("nvcc failed on " + ", ".join(failed) + ":\n" + "".join(logs))
+    link = [nvcc, ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath," + cuda_lib,
+            "-o", out + ".tmp"] + [obj for _, obj, _ in procs]
+    res = subprocess.run(link, capture_output=True, text=True)
     if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+        raise RuntimeError("nvcc link failed:\n" + res.stdout + res.stderr)
     os.replace(out + ".tmp", out)
     if verbose:
-        print(res.stdout + res.stderr)
+        print("".join(logs))
     return out
 
 

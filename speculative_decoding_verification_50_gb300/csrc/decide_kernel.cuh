@@ -111,7 +111,7 @@ __device__ __forceinline__ PosStats combine_position(const ChunkRec* R, int nchu
   at.init();
   ad.init();
   for (int q = sub; q < nchunk; q += W) {
-    const ChunkRec r = R[q];
+    const ChunkRec r = ld_rec(R + q);
     soft_merge(mt, s_t, r.mt, r.st, c);
     soft_merge(md, s_d, r.md, r.sd, c);
     at.merge(r.bt, r.it, r.bad);
@@ -155,9 +155,53 @@ __device__ __forceinline__ WarpTopF warp_keys(const float* cv, const int32_t* ci
                                               int lane, WarpKeys& S) {
   if (ncand > kWarpCand) return merge_candidates(cv, ci, ncand, F, lane);
   for (int e = lane; e < ncand; e += 32) {
-    S.v[e] = cv[e];
-    S.i[e] = ci[e];
+    S.v[e] = __ldcg(cv + e);
+    S.i[e] = __ldcg(ci + e);
   }
+  __syncwarp();
+  WarpTopF L;
+  L.init();
+  const int nl = ncand / F;  // the chunks' lists, F entries each in key order
+  if (nl <= 32) {
+    // merge by their heads: lane l follows list l; F rounds of a warp
+    // argmax, the winning lane stepping to its list's next entry (indices are
+    // distinct across chunks; empty entries (-inf, INT_MAX) come last)
+    int ptr = 0;
+    float hv = neg_inf();
+    int32_t hi = INT_MAX;
+    if (lane < nl) {
+      hv = S.v[lane * F];
+      hi = S.i[lane * F];
+    }
+    for (int f = 0; f < F; ++f) {
+      float bv = hv;
+      int32_t bi = hi;
+      int bl = lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+        if (key_beats(ov, oi, bv, bi) || (ov == bv && oi == bi && ol < bl)) {
+          bv = ov;
+          bi = oi;
+          bl = ol;
+        }
+      }
+      if (lane == f) {
+        L.v = bv;
+        L.i = bi;
+      }
+      if (lane == bl && bi != INT_MAX) {
+        ++ptr;
+        hv = ptr < F ? S.v[lane * F + ptr] : neg_inf();
+        hi = ptr < F ? S.i[lane * F + ptr] : INT_MAX;
+      }
+    }
+    __syncwarp();  // the scratch may be reused by this warp's next row
+    return L;
+  }
+  // more lists than lanes: rank every candidate by counting
   if (lane < F) {
     S.ov[lane] = neg_inf();
     S.oi[lane] = INT_MAX;
@@ -175,8 +219,6 @@ __device__ __forceinline__ WarpTopF warp_keys(const float* cv, const int32_t* ci
     }
   }
   __syncwarp();
-  WarpTopF L;
-  L.init();
   if (lane < F) {
     L.v = S.ov[lane];
     L.i = S.oi[lane];
@@ -193,8 +235,8 @@ __device__ __forceinline__ void cta_rank_keys(const float* cv, const int32_t* ci
                                               WarpKeys& S) {
   const int t = threadIdx.x;
   if (t < ncand) {
-    S.v[t] = cv[t];
-    S.i[t] = ci[t];
+    S.v[t] = __ldcg(cv + t);
+    S.i[t] = __ldcg(ci + t);
   }
   if (t < F) {
     S.ov[t] = neg_inf();
@@ -229,8 +271,8 @@ __device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int3
     float z = neg_inf();
     int32_t vi = INT_MAX;
     if (idx < ncand) {
-      z = cv[idx];
-      vi = ci[idx];
+      z = __ldcg(cv + idx);
+      vi = __ldcg(ci + idx);
     }
     unsigned m = __ballot_sync(0xffffffffu, vi != INT_MAX && key_beats(z, vi, L.tv, L.ti));
     while (m) {
@@ -469,11 +511,11 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
     auto mass = [&](int j) -> FF {
       FF x;
       if (halves) {  // piece j is half j % 2 of chunk j / 2; the second is the rest
-        const ChunkRec r = recs[j >> 1];
+        const ChunkRec r = ld_rec(recs + (j >> 1));
         const FF first = ff_mul(r.st, ex2((r.mt - M) * c));
         x = (j & 1) ? ff_add(ff_mul(r.sd, ex2((r.md - M) * c)), ff_neg(first)) : first;
       } else {
-        const ChunkRec r = recs[j];
+        const ChunkRec r = ld_rec(recs + j);
         const float m = draft_fields ? r.md : r.mt, sm = draft_fields ? r.sd : r.st;
         x = ff_mul(sm, ex2((m - M) * c));
       }
@@ -838,18 +880,17 @@ struct PrepSmem {
 // The decision of batch row X.b from its chunk records, by every thread of
 // one CTA: the records combined per position, the Saguaro keys of the draft
 // rows, and the accept test (or the first MSS candidate's test), leaving the
-// outcome in S.dec.  wkeys: kWarps warps' key scratch.  wait_primary: the
+// outcome in S.dec.  wkeys: key scratch of the first nkw warps (the others
+// take no part in the key merges; nkw >= 1).  wait_primary: the
 // records come from the previous kernel on the stream (wait for it once the
 // inputs are fetched).  Ends with a CTA barrier.
 template <int DT, int MODE>
 __device__ __forceinline__ void decide_prepare(const DecideParams& P, const RowCtx& X, PrepSmem& S,
-                                               WarpKeys* wkeys, bool wait_primary) {
+                                               WarpKeys* wkeys, int nkw, bool wait_primary) {
   using E = Elem<DT>;
-  constexpr bool kTopF = MODE == kModeSsd;
   constexpr bool kSample = MODE == kModeSample;
   constexpr bool kMss = MODE == kModeMss;
-  const int b = X.b;
-  const int K = P.K, F = P.F;
+  const int F = P.F;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const bool greedy = X.greedy, temp_ok = X.temp_ok, nd = X.nd, sg_on = X.sg_on;
@@ -895,7 +936,7 @@ __device__ __forceinline__ void decide_prepare(const DecideParams& P, const RowC
     const int ncand = static_cast<int>(P.nchunk) * F;
     const bool cta_rank = kSample && ncand <= kWarpCand;  // the sampler: all warps rank
     if (cta_rank) cta_rank_keys(P.cand_v + u0 * ncand, P.cand_i + u0 * ncand, ncand, F, wkeys[0]);
-    for (int i = warp; i < nrows; i += kWarps) {
+    for (int i = warp; warp < nkw && i < nrows; i += nkw) {
       const int64_t u = u0 + i;
       WarpTopF Lk;
       if (cta_rank) {
@@ -1146,13 +1187,12 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const RowCtx X = row_ctx<MODE>(P, b);
-  const bool greedy = X.greedy;
   const float c = X.c;
   const int64_t u0 = X.u0;
   const RowLayout& L = X.L;
   const int kb = X.kb, u_draw = X.u_draw;
   const bool sg_on = X.sg_on;
-  decide_prepare<DT, MODE>(P, X, S, wkeys, true);
+  decide_prepare<DT, MODE>(P, X, S, wkeys, (kTopF || kSample) ? kWarps : 1, true);
 
   // ---- a draw from a whole row's own distribution (the bonus after K accepted
   // drafts, the sampler) needs only the one chunk holding U * R: rank 0 finds
@@ -1423,55 +1463,5 @@ struct PredictKeysParams {
   int32_t B, K, V, F, nchunk;
   int32_t fk[kMaxK + 1];  // keys kept at lookahead k
 };
-
-__global__ void __launch_bounds__(kThreads) predict_keys_kernel(const PredictKeysParams P) {
-  __shared__ int32_t status_all;
-  __shared__ WarpKeys wkeys[kWarps];
-  const int b = blockIdx.x;
-  const int K = P.K, F = P.F;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int64_t u0 = static_cast<int64_t>(b) * (K + 1);
-  if (threadIdx.x == 0) status_all = 0;
-  pdl_wait_primary();  // records and candidates come from the row-statistics kernel
-  __syncthreads();
-  for (int k = warp; k <= K; k += kWarps) {
-    const int64_t u = u0 + k;
-    int bad = 0;
-    for (int q = lane; q < P.nchunk; q += 32) bad |= P.recs[u * P.nchunk + q].bad;
-    bad = __reduce_or_sync(0xffffffffu, bad);
-    const int x = (k < K) ? P.tokens[static_cast<int64_t>(b) * K + k] : 0;
-    const int status = ((bad & 1) ? kNonFinite : 0) | ((bad & 2) ? kTimeout : 0) |
-                       ((x < 0 || x >= P.V) ? kBadToken : 0);
-    const WarpTopF L = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
-                                 P.nchunk * F, F, lane, wkeys[warp]);
-    if (lane < F) {
-      const bool good = status == 0 && lane < P.fk[k] && L.i != INT_MAX;
-      P.keys[u * F + lane] = good ? L.i : -1;
-      if (P.key_logits) P.key_logits[u * F + lane] = good ? L.v : neg_inf();
-    }
-    if (lane == 0 && status) atomicOr(&status_all, status);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && P.row_status) P.row_status[b] = status_all;
-}
-
-__global__ void check_hit_kernel(int B, int K, int F, const int32_t* __restrict__ keys,
-                                 const int32_t* __restrict__ accept_len,
-                                 const int32_t* __restrict__ out_tokens,
-                                 uint8_t* __restrict__ hit) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  const int n = accept_len[b];
-  uint8_t h = 0;
-  if (n >= 0 && n <= K) {
-    const int t = out_tokens[static_cast<int64_t>(b) * (K + 1) + n];
-    if (t >= 0) {
-      const int32_t* kk = keys + (static_cast<int64_t>(b) * (K + 1) + n) * F;
-      for (int f = 0; f < F; ++f) h |= (kk[f] == t);
-    }
-  }
-  hit[b] = h;
-}
 
 }  // namespace specv

@@ -10,7 +10,7 @@
 #include <string>
 
 #include "specv.h"
-#include "decide_kernel.cuh"
+#include "launch.cuh"
 
 using namespace specv;
 
@@ -87,40 +87,6 @@ bool vec_ok(const void* base, int64_t bs, int64_t rs, int es) {
   return aligned(base, 16) && ((bs * es) % 16 == 0) && ((rs * es) % 16 == 0);
 }
 
-template <typename Kern>
-cudaError_t allow_cluster(Kern k, int C) {
-  if (C <= 8) return cudaSuccess;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-}
-
-template <typename Kern, typename Params>
-cudaError_t launch_clustered(Kern k, int C, int64_t units, size_t smem, cudaStream_t stream,
-                             const Params& p) {
-  cudaError_t e = allow_cluster(k, C);
-  if (e != cudaSuccess) return e;
-  if (smem > 0) {  // static + dynamic shared memory may pass the 48 KB default
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units * C), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  // The kernel waits (griddepcontrol.wait) for the one before it on the
-  // stream, so it may be scheduled while that one drains.
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k, p);
-}
-
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Sizes of one call: kernel A chunks, kernel B cluster and slices, workspace.
@@ -162,6 +128,7 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
   // SPECV_ITERS (1..64) fixes the trip count, for tuning runs.
   static const int env_iters = env_int("SPECV_ITERS", -1);
   pl.iters = (env_iters >= 1 && env_iters <= 64) ? env_iters : iters0;
+  const int64_t slots = static_cast<int64_t>(sm_count()) * (dtype == SPECV_BF16 ? 4 : 5);
   const int64_t want = 4LL * sm_count();
   for (;;) {
     pl.chunk = static_cast<int64_t>(pl.iters) * kVecs * kThreads * vw;
@@ -173,7 +140,6 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
   // bf16) leaves a few chunks to run after the rest: lengthen the chunks (up
   // to 16 trips) until they fit in one wave.  Config 4 (B=32, K=4, V=128256
   // bf16): 640 chunks of 8 trips -> 480 of 11, 0.0525 -> 0.0485 ms per call.
-  const int64_t slots = static_cast<int64_t>(sm_count()) * (dtype == SPECV_BF16 ? 4 : 5);
   if (env_iters < 1 && units * pl.nchunk > slots && 4 * units * pl.nchunk <= 5 * slots) {
     for (int it = pl.iters + 1; it <= 16; ++it) {
       const int64_t ch = static_cast<int64_t>(it) * kVecs * kThreads * vw;
@@ -195,20 +161,11 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
   return pl;
 }
 
-size_t plan_workspace(const Plan& pl) { return pl.recs_bytes + 2 * pl.cand_bytes; }
+size_t plan_workspace_split(const Plan& pl) { return pl.recs_bytes + 2 * pl.cand_bytes; }
+
+size_t plan_workspace(const Plan& pl) { return plan_workspace_split(pl); }
 
 constexpr size_t kMaxSegSmem = 200 * 1024;
-
-template <typename Kern, typename Params>
-cudaError_t launch_plain(Kern k, int64_t blocks, size_t smem, cudaStream_t s, const Params& p) {
-  if (smem > 0) {  // static + dynamic shared memory may pass the 48 KB default
-    const cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  k<<<static_cast<unsigned>(blocks), kThreads, smem, s>>>(p);
-  return cudaGetLastError();
-}
 
 // Stages of the persistent path's ring (SPECV_STAGES = 2..8 fixes the count,
 // for tuning runs).
@@ -223,28 +180,6 @@ int ring_stages() {
 int ring_stages_b() {
   static const int v = env_int("SPECV_STAGES_B", 0);
   return (v >= 2 && v <= kMaxStages) ? v : 2;
-}
-
-// Persistent row-statistics kernel: as many CTAs as are resident at once on
-// the GPU (at most one per work item), each with the ring in dynamic shared
-// memory.  The occupancy query is made once per kernel and ring size.
-template <int DT, int MODE>
-cudaError_t launch_ring(int64_t items, cudaStream_t s, const StatsParams& p) {
-  auto k = stats_ring_kernel<DT, MODE>;
-  const size_t smem = static_cast<size_t>(p.stages) * 2 * kTripBytes;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  static std::atomic<int> occ_cache[kMaxStages + 1];
-  int occ = occ_cache[p.stages].load(std::memory_order_relaxed);
-  if (occ <= 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kRingThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-    occ_cache[p.stages].store(occ, std::memory_order_relaxed);
-  }
-  const int64_t grid = std::min<int64_t>(items, static_cast<int64_t>(occ) * sm_count());
-  k<<<static_cast<unsigned>(grid), kRingThreads, smem, s>>>(p);
-  return cudaGetLastError();
 }
 
 // Kernel A for 16-byte aligned layouts: the staged path (one CTA per item) by
@@ -272,29 +207,6 @@ int test_stall(char which) {
     return Stall{0, -1};
   }();
   return (st.v >= 0 && st.k == which) ? st.v + 1 : 0;
-}
-
-template <int MODE>
-cudaError_t launch_stats(int dtype, bool vec, int64_t items, cudaStream_t s, const StatsParams& p) {
-  const size_t ring_smem = static_cast<size_t>(p.stages) * 2 * kTripBytes;
-  if (dtype == SPECV_BF16) {
-    if (!vec) return launch_plain(stats_kernel<0, false, MODE>, items, 0, s, p);
-    return persistent_path() ? launch_ring<0, MODE>(items, s, p)
-                             : launch_plain(stats_kernel<0, true, MODE>, items, ring_smem, s, p);
-  }
-  if (!vec) return launch_plain(stats_kernel<1, false, MODE>, items, 0, s, p);
-  return persistent_path() ? launch_ring<1, MODE>(items, s, p)
-                           : launch_plain(stats_kernel<1, true, MODE>, items, ring_smem, s, p);
-}
-
-template <int MODE>
-cudaError_t launch_decide(int dtype, bool vec, int CB, int64_t B, size_t smem, cudaStream_t s,
-                          const DecideParams& p) {
-  if (dtype == SPECV_BF16)
-    return vec ? launch_clustered(decide_kernel<0, true, MODE>, CB, B, smem, s, p)
-               : launch_clustered(decide_kernel<0, false, MODE>, CB, B, smem, s, p);
-  return vec ? launch_clustered(decide_kernel<1, true, MODE>, CB, B, smem, s, p)
-             : launch_clustered(decide_kernel<1, false, MODE>, CB, B, smem, s, p);
 }
 
 // Checks shared by specv_verify and specv_ssd_round.
@@ -380,6 +292,13 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   const int32_t B = a->B, K = a->K, V = a->V;
   const int32_t Ka = mode == kModeMss ? 0 : K;  // positions per row in the statistics kernel
   const bool cands = mode == kModeSsd || mode == kModeSample;
+  const int es = elem_bytes(a->dtype);
+  // Packed rows have no batch stride: row alignment follows from the row stride.
+  const bool packed = a->cu_num_draft_tokens != nullptr;
+  const bool nd = (a->flags & SPECV_NO_DRAFT_PROBS) != 0;
+  const bool vec =
+      vec_ok(a->target_logits, packed ? 0 : a->target_batch_stride, a->target_row_stride, es) &&
+      (nd || vec_ok(a->draft_logits, packed ? 0 : a->draft_batch_stride, a->draft_row_stride, es));
   Plan pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, mode == kModeMss ? 2 : 1,
                       mode == kModeSample ? 16 : 8);
   // The sampler's rows draw from one chunk each (the chunk-local draw) when a
@@ -397,13 +316,6 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   const int64_t units = static_cast<int64_t>(B) * (Ka + 1);
   if (units * pl.nchunk > 0x7fffffffLL || static_cast<int64_t>(B) * pl.CB > 0x7fffffffLL)
     return fail(SPECV_ERR_UNSUPPORTED, "B*(K+1) too large");
-  const int es = elem_bytes(a->dtype);
-  // Packed rows have no batch stride: row alignment follows from the row stride.
-  const bool packed = a->cu_num_draft_tokens != nullptr;
-  const bool nd = (a->flags & SPECV_NO_DRAFT_PROBS) != 0;
-  const bool vec =
-      vec_ok(a->target_logits, packed ? 0 : a->target_batch_stride, a->target_row_stride, es) &&
-      (nd || vec_ok(a->draft_logits, packed ? 0 : a->draft_batch_stride, a->draft_row_stride, es));
   char* ws = static_cast<char*>(workspace);
   ChunkRec* recs = reinterpret_cast<ChunkRec*>(ws);
   float* cand_v = pl.cand_bytes ? reinterpret_cast<float*>(ws + pl.recs_bytes) : nullptr;
@@ -438,10 +350,11 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.stall = test_stall('A');
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t items = units * pl.nchunk;
-  cudaError_t e = mode == kModeSsd      ? launch_stats<kModeSsd>(a->dtype, vec, items, s, sp)
-                  : mode == kModeSample ? launch_stats<kModeSample>(a->dtype, vec, items, s, sp)
-                  : mode == kModeMss    ? launch_stats<kModeMss>(a->dtype, vec, items, s, sp)
-                                        : launch_stats<kModeVerify>(a->dtype, vec, items, s, sp);
+  cudaError_t e =
+      mode == kModeSsd      ? launch_stats<kModeSsd>(a->dtype, vec, persistent_path(), sm_count(), items, s, sp)
+      : mode == kModeSample ? launch_stats<kModeSample>(a->dtype, vec, persistent_path(), sm_count(), items, s, sp)
+      : mode == kModeMss    ? launch_stats<kModeMss>(a->dtype, vec, persistent_path(), sm_count(), items, s, sp)
+                            : launch_stats<kModeVerify>(a->dtype, vec, persistent_path(), sm_count(), items, s, sp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
   e = record_split(s);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "split event: %s", cudaGetErrorString(e));
@@ -562,7 +475,7 @@ specv_status specv_ssd_round(const specv_ssd_args* a, void* workspace, size_t wo
 
 size_t specv_predict_workspace_bytes(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype) {
   if (B <= 0 || K < 1 || V < 1 || F < 1) return 0;
-  return plan_workspace(make_plan(B, K, V, F, dtype));
+  return plan_workspace_split(make_plan(B, K, V, F, dtype));
 }
 
 specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace,
@@ -591,7 +504,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   if (B > 1 && a->draft_batch_stride < K * a->draft_row_stride + V)
     return fail(SPECV_ERR_INVALID_ARG, "batch stride too small for K+1 draft rows");
   const Plan pl = make_plan(B, K, V, F, a->dtype);
-  const size_t need = plan_workspace(pl);
+  const size_t need = plan_workspace_split(pl);
   if (!workspace || workspace_bytes < need)
     return fail(SPECV_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
   if (!aligned(workspace, 256)) return fail(SPECV_ERR_WORKSPACE, "workspace not 256-byte aligned");
@@ -616,7 +529,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   sp.iters = pl.iters;
   sp.stages = ring_stages();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_stats<kModePredict>(a->dtype, vec, units * pl.nchunk, s, sp);
+  cudaError_t e = launch_stats<kModePredict>(a->dtype, vec, persistent_path(), sm_count(), units * pl.nchunk, s, sp);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "row-statistics launch: %s", cudaGetErrorString(e));
   e = record_split(s);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "split event: %s", cudaGetErrorString(e));
@@ -634,18 +547,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   kp.F = F;
   kp.nchunk = static_cast<int32_t>(pl.nchunk);
   for (int k = 0; k <= K; ++k) kp.fk[k] = a->fanout ? a->fanout[k] : F;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, predict_keys_kernel, kp);
-  }
+  e = launch_predict_keys(kp, B, s);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "keys launch: %s", cudaGetErrorString(e));
   g_launches = 2;
@@ -701,7 +603,7 @@ specv_status specv_saguaro_sample(const specv_saguaro_args* a, void* workspace,
 }
 
 size_t specv_mss_workspace_bytes(int32_t B, int32_t M, int32_t V, int32_t dtype) {
-  if (B <= 0 || M < 1 || V < 1) return 0;
+  if (B <= 0 || M < 1 || V < 1 || M > 32) return 0;
   return plan_workspace(make_plan(B, 0, V, 0, dtype, 2));
 }
 
@@ -808,8 +710,7 @@ specv_status specv_check_hit(int32_t B, int32_t K, int32_t F, const int32_t* key
   if (!aligned(keys, 4) || !aligned(accept_len, 4) || !aligned(out_tokens, 4))
     return fail(SPECV_ERR_INVALID_ARG, "a pointer is not aligned to its element size");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  check_hit_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, K, F, keys, accept_len, out_tokens, hit);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_check_hit(B, K, F, keys, accept_len, out_tokens, hit, s);
   if (e != cudaSuccess) return fail(SPECV_ERR_CUDA, "check_hit launch: %s", cudaGetErrorString(e));
   g_launches = 1;
   return ok();

@@ -64,6 +64,19 @@ struct ChunkRec {        // 48 bytes per (unit, chunk)
 };
 static_assert(sizeof(ChunkRec) == 48, "ChunkRec layout");
 
+// A record written by another CTA, possibly of the same launch: read through
+// L2 (ld.global.cg), never from a line this SM may hold from before.
+__device__ __forceinline__ ChunkRec ld_rec(const ChunkRec* p) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+  const float4 a = __ldcg(q), b = __ldcg(q + 1), c = __ldcg(q + 2);
+  ChunkRec r;
+  r.mt = a.x; r.st = a.y; r.md = a.z; r.sd = a.w;
+  r.bt = b.x; r.bd = b.y; r.it = __float_as_int(b.z); r.id = __float_as_int(b.w);
+  r.bad = __float_as_int(c.x); r.pad[0] = __float_as_int(c.y); r.pad[1] = __float_as_int(c.z);
+  r.pad[2] = __float_as_int(c.w);
+  return r;
+}
+
 struct StatsParams {
   const void* zt;
   int64_t t_bs, t_rs;

@@ -53,7 +53,7 @@ def _numpy(out):
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls(sv):
     cases = [
         wl.generate(wl.SPECS["cfg3"]),  # bf16, mixed greedy / temperature rows
-        wl.generate(wl.SPECS["cfg5"], rows=range(48)),  # fp32, K=8, V=152064
+        wl.generate(wl.SPECS["cfg5"]),  # fp32, B=256, K=8, V=152064: the size the header cites
     ]
     for data in cases:
         args = _dev(data)
@@ -64,6 +64,13 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(sv):
             assert np.array_equal(got[k], ref[k]), k
         for k in ("p_draft", "q_draft"):
             assert np.abs(got[k] - ref[k]).max() <= PROB_TOL, k
+
+
+def test_noalloc_covers_config5_at_full_size(sv):
+    """The header's size claim: B=256, K=8, V=152064 fp32 fits the scratch."""
+    lib = sv.load_library()
+    need = lib.specv_verify_workspace_bytes(256, 8, 152064, sv.SPECV_FP32)
+    assert 0 < need <= (8 << 20), need
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(sv):
