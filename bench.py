@@ -740,11 +740,12 @@ def run_ours(args) -> None:
                 st=torch.empty(lay["rows"], dtype=torch.int32).pin_memory() if mode == "sample" else None,
                 tm=torch.empty(B, dtype=torch.int32).pin_memory() if mode == "mss" else None)
 
-    def e2e_step():
+    def h2d_only():
         for k in ("target", "draft", "cu", "tok", "temp", "unif"):
             if d[k] is not None:
                 d[k].copy_(h[k], non_blocking=True)
-        w["call"]()
+
+    def d2h_reads():
         if mode == "sample":
             hold["st"].copy_(w["s_tok"], non_blocking=True)
         elif mode == "mss":
@@ -759,10 +760,10 @@ def run_ours(args) -> None:
             hold["keys"].copy_(w["keys"], non_blocking=True)
             hold["hit"].copy_(w["hit"], non_blocking=True)
 
-    def h2d_only():
-        for k in ("target", "draft", "cu", "tok", "temp", "unif"):
-            if d[k] is not None:
-                d[k].copy_(h[k], non_blocking=True)
+    def e2e_step():
+        h2d_only()
+        w["call"]()
+        d2h_reads()
 
     # the host link alone: the same host-to-device copies, nothing else
     h2d_ms = []
@@ -788,6 +789,23 @@ def run_ours(args) -> None:
     e1.record(w["stream"])
     barrier()
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev) / e2e_steps
+    # the same steps again with an event between their phases (host-to-device
+    # copies, the call, the device-to-host reads): where a slow step's time goes
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(e2e_steps)]
+    barrier()
+    for ev in ph:
+        ev[0].record(w["stream"])
+        h2d_only()
+        ev[1].record(w["stream"])
+        w["call"]()
+        ev[2].record(w["stream"])
+        d2h_reads()
+        ev[3].record(w["stream"])
+    barrier()
+    phases = {name: round(statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ph), 4)
+              for i, name in enumerate(("h2d_ms", "call_ms", "d2h_ms"))}
+    h2d_each = [e[0].elapsed_time(e[1]) for e in ph]
+    phases["h2d_ms_min_max"] = [round(min(h2d_each), 4), round(max(h2d_each), 4)]
     h2d = sum(t.numel() * t.element_size() for t in h.values() if t is not None)
     d2h = (hold["st"].numel() * 4 if mode == "sample" else 2 * B * 4 if mode == "mss" else
            hold["keys"].numel() * 4 + hold["hit"].numel() if mode == "predict" else
@@ -926,6 +944,7 @@ def run_ours(args) -> None:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "h2d_copy_ms": round(h2d_ms, 4),
+                "phases_in_step": phases,
                 "h2d_gbs": round(h2d / (h2d_ms / 1e3) / 1e9, 1),
                 "host_placement": placement},
         "outcome": outcome_summary(),

@@ -359,7 +359,9 @@ __device__ __forceinline__ void residual_vec(const void* rowt, const void* rowd,
 // consumes them and writes the per-warp segment sums of r, tile-major, as the
 // register path does.  Returns false if a wait gave up (after a bounded wait
 // for the copies still in flight).  With `stall` (a test hook) stage 0 also
-// waits for 16 bytes that no copy brings.
+// waits for 16 bytes that no copy brings.  `stream`: the copies are marked
+// evict-first (a row read once); an MSS node, whose later passes read the
+// same two rows again, keeps the default policy.
 // Invalidates the ring's barriers, before ring_start arms them for another
 // pass (every wait on them has ended and every copy has landed).
 __device__ __forceinline__ void ring_reset(RingBars& R, int S) {
@@ -370,20 +372,21 @@ __device__ __forceinline__ void ring_reset(RingBars& R, int S) {
 
 template <int DT>
 __device__ __forceinline__ void ring_start(RingBars& R, unsigned char* ring, int S, const Chunk& C,
-                                           bool stall = false) {
+                                           bool stall = false, bool stream = true) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&R.full[s], 1);
     fence_mbar_init();
     if (stall) mbar_expect_tx(&R.full[0], 16);
     const int ntr = ring_trips(C.nv);
-    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C);
+    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C, false, stream);
   }
 }
 
 template <int DT>
 __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, int S, const Chunk& C,
                                               int mode, float mt, float md, float c, float ist,
-                                              float isd, int xn, const SgW& w, float* segs, int ntl) {
+                                              float isd, int xn, const SgW& w, float* segs, int ntl,
+                                              bool stream = true) {
   using E = Elem<DT>;
   using Vec = typename E::Vec;
   constexpr int VW = E::VW;
@@ -457,7 +460,7 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
     }
     if (threadIdx.x == 0 && t + S < ntr) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      ring_issue<DT>(&R.full[s], ring, s, t + S, C);
+      ring_issue<DT>(&R.full[s], ring, s, t + S, C, false, stream);
     }
     if (++s == S) {
       s = 0;
@@ -1240,7 +1243,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   if (staged) {
     Chunk SC = RC;
     if (S.dec.mode != 0) SC.rowd = nullptr;  // mode 1 reads p_n only
-    ring_start<DT>(ring_bars, ring, P.stages, SC, P.stall == b + 1 && rank == 0);
+    ring_start<DT>(ring_bars, ring, P.stages, SC, P.stall == b + 1 && rank == 0, !kMss);
     __syncthreads();
   }
 
@@ -1268,11 +1271,11 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
         if (pass > 0) {  // another pass over the slice (an MSS rejection, a fallback)
           __syncthreads();
           ring_reset(ring_bars, P.stages);
-          ring_start<DT>(ring_bars, ring, P.stages, SC);
+          ring_start<DT>(ring_bars, ring, P.stages, SC, false, !kMss);
           __syncthreads();
         }
         copies_ok = ring_residual<DT>(ring_bars, ring, P.stages, SC, mode, mt, md, c, ist, isd,
-                                      S.dec.xn, sgw, segs, ntl) && copies_ok;
+                                      S.dec.xn, sgw, segs, ntl, !kMss) && copies_ok;
       } else
       for (int t0 = 0; t0 < ntl; t0 += kTileUnroll) {
         float s[kTileUnroll];

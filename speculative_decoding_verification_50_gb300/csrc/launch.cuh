@@ -17,6 +17,10 @@ cudaError_t launch_stats(int dtype, bool vec, bool persistent, int sms, int64_t 
 template <int MODE>
 cudaError_t launch_decide(int dtype, bool vec, int CB, int64_t B, size_t smem, cudaStream_t s,
                           const DecideParams& p);
+// The sampler's decision with one warp per row (aligned rows whose records
+// carry their first halves): ceil(rows / 8) CTAs, `smem` bytes of segment
+// sums for the CTA-wide pass over a whole row.
+cudaError_t launch_sample_rows(int dtype, int64_t rows, size_t smem, cudaStream_t s, const DecideParams& p);
 cudaError_t launch_predict_keys(const PredictKeysParams& kp, int B, cudaStream_t s);
 cudaError_t launch_check_hit(int B, int K, int F, const int32_t* keys, const int32_t* accept_len,
                              const int32_t* out_tokens, uint8_t* hit, cudaStream_t s);

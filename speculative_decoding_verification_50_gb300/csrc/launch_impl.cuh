@@ -43,6 +43,28 @@ cudaError_t launch_clustered(Kern k, int C, int64_t units, size_t smem, cudaStre
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
+// One launch that may be scheduled while the kernel before it on the stream
+// drains (it waits for that kernel with griddepcontrol.wait).
+template <typename Kern, typename Params>
+cudaError_t launch_dependent(Kern k, int64_t blocks, size_t smem, cudaStream_t stream, const Params& p) {
+  if (smem > 0) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
 template <typename Kern, typename Params>
 cudaError_t launch_plain(Kern k, int64_t blocks, size_t smem, cudaStream_t s, const Params& p) {
   if (smem > 0) {  // static + dynamic shared memory may pass the 48 KB default

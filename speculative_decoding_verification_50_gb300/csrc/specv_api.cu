@@ -178,6 +178,11 @@ size_t plan_workspace(const Plan& pl) { return plan_workspace_split(pl); }
 
 constexpr size_t kMaxSegSmem = 200 * 1024;
 
+// Sampled rows per SM from which the sampler's decision runs one warp per row
+// (fewer rows keep one CTA per row, whose eight warps read a row's half
+// chunk faster than one warp can).
+constexpr int kWarpRowsPerSm = 8;
+
 // Stages of the persistent path's ring (SPECV_STAGES = 2..8 fixes the count,
 // for tuning runs).
 int ring_stages() {
@@ -429,7 +434,16 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
     dp.mss_acc = mx->acc;
     dp.mss_ap = mx->ap;
   }
-  e = mode == kModeSsd      ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, smemB, s, dp)
+  // The sampler's rows on one warp each, when they are many and their records
+  // carry first halves (aligned rows, chunks of an even trip count).
+  // SPECV_SAMPLE_WARP=0/1 overrides the row count, for tuning runs.
+  static const int env_warp = env_int("SPECV_SAMPLE_WARP", -1);
+  const int64_t nv_row = (static_cast<int64_t>(V) + vec_width(a->dtype) - 1) / vec_width(a->dtype);
+  const size_t smem_row = static_cast<size_t>((nv_row + kThreads - 1) / kThreads) * kWarps * sizeof(float);
+  const bool warp_rows = mode == kModeSample && vec && sp.half > 0 && smem_row <= kMaxSegSmem &&
+                         (env_warp >= 0 ? env_warp != 0 : B >= kWarpRowsPerSm * sm_count());
+  e = warp_rows             ? launch_sample_rows(a->dtype, B, smem_row, s, dp)
+      : mode == kModeSsd    ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, smemB, s, dp)
       : mode == kModeSample ? launch_decide<kModeSample>(a->dtype, vec, pl.CB, B, smemB, s, dp)
       : mode == kModeMss    ? launch_decide<kModeMss>(a->dtype, vec, pl.CB, B, smemB, s, dp)
                             : launch_decide<kModeVerify>(a->dtype, vec, pl.CB, B, smemB, s, dp);

@@ -656,7 +656,7 @@ __device__ __forceinline__ int ring_trips(int nv) {
 // that row alone, so the same ring carries twice as many trips.
 template <int DT>
 __device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, int s, int t,
-                                           const Chunk& C, bool one = false) {
+                                           const Chunk& C, bool one = false, bool stream = true) {
   using E = Elem<DT>;
   const int64_t off = static_cast<int64_t>(t) * kTripBytes;
   int64_t bytes = (C.v1 - C.v0) * E::ES - off;
@@ -668,11 +668,12 @@ __device__ __forceinline__ void ring_issue(uint64_t* full, unsigned char* ring, 
   if (b32) {
     const int64_t src = C.v0 * E::ES + off;
     if (one) {
-      bulk_load(ring + static_cast<int64_t>(s) * kTripBytes, (C.rowt ? C.rowt : C.rowd) + src, b32, full);
+      bulk_load(ring + static_cast<int64_t>(s) * kTripBytes, (C.rowt ? C.rowt : C.rowd) + src, b32, full,
+                stream);
     } else {
       unsigned char* base = ring + static_cast<int64_t>(s) * 2 * kTripBytes;
-      if (C.rowt) bulk_load(base, C.rowt + src, b32, full);
-      if (C.rowd) bulk_load(base + kTripBytes, C.rowd + src, b32, full);
+      if (C.rowt) bulk_load(base, C.rowt + src, b32, full, stream);
+      if (C.rowd) bulk_load(base + kTripBytes, C.rowd + src, b32, full, stream);
     }
   }
 }
@@ -788,7 +789,7 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
     for (int s = 0; s < S; ++s) mbar_init(&R.full[s], 1);
     fence_mbar_init();
     if (stall) mbar_expect_tx(&R.full[0], 16);
-    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C, one);
+    for (int t = 0; t < ntr && t < S; ++t) ring_issue<DT>(&R.full[t], ring, t, t, C, one, !TOPF);
   }
   __syncthreads();
   bool ok = true;
@@ -821,7 +822,7 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
     }
     if (threadIdx.x == 0 && t + S < ntr) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      ring_issue<DT>(&R.full[s], ring, s, t + S, C, one);
+      ring_issue<DT>(&R.full[s], ring, s, t + S, C, one, !TOPF);
     }
     if (++s == S) {
       s = 0;
