@@ -139,7 +139,7 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
   // SPECV_ITERS (1..64) fixes the trip count, for tuning runs.
   static const int env_iters = env_int("SPECV_ITERS", -1);
   pl.iters = (env_iters >= 1 && env_iters <= 64) ? env_iters : iters0;
-  const int64_t slots = static_cast<int64_t>(sm_count()) * (dtype == SPECV_BF16 ? 4 : 5);
+  const int64_t slots = static_cast<int64_t>(sm_count()) * ((dtype == SPECV_BF16 && F > 0) ? 4 : 5);
   const int64_t want = 4LL * sm_count();
   for (;;) {
     pl.chunk = static_cast<int64_t>(pl.iters) * kVecs * kThreads * vw;

@@ -836,10 +836,17 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
   return ok;
 }
 
+// Resident CTAs per SM: 5 (48 registers), but 4 for bf16 rows with top-F
+// candidates and for bf16 rows on the register path, which would spill at 48.
+template <int DT, bool VEC, int MODE>
+constexpr int stats_ctas_per_sm() {
+  return (DT == 0 && (mode_has_topf(MODE) || !VEC)) ? 4 : 5;
+}
+
 // Register path (VEC = false: any layout) or staged path (VEC = true: 16-byte
 // aligned rows, P.stages stages of dynamic shared memory); one CTA per item.
 template <int DT, bool VEC, int MODE>
-__global__ void __launch_bounds__(kThreads, DT == 0 ? 4 : 5) stats_kernel(const StatsParams P) {
+__global__ void __launch_bounds__(kThreads, (stats_ctas_per_sm<DT, VEC, MODE>())) stats_kernel(const StatsParams P) {
   constexpr bool kT = mode_has_target(MODE);
   constexpr bool kTopF = mode_has_topf(MODE);
   __shared__ EpiSmem S;
