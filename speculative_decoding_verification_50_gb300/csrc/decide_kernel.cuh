@@ -92,7 +92,7 @@ struct DecideParams {
   int32_t sg_F;      // Saguaro sampling: the drafts came from sigma_{sg_F, sg_C}
   float sg_C;        //   (0: plain softmax drafts); the sampler's own F and C
   int32_t local_draw;  // draws from a whole row read only the chunk holding U * R
-  int32_t half;        // the sampler's records carry each chunk's first half apart
+  int32_t pieces;      // the sampler's records carry each chunk's pieces apart (2 or 4; 0: none)
   int32_t stall;       // test hook: 1 + the batch row whose first residual stage (rank 0)
                        // waits for 16 bytes no copy brings, so its wait runs out (0: none)
   // MSS (K = M candidates per node, one target and one draft row each)
@@ -470,7 +470,23 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
   return ok;
 }
 
-constexpr int kDrawTiles = 16 * kVecs;  // 256-vector tiles in the longest chunk (16 trips)
+// Mass of piece p of a sampled row's chunk record (the chunk split in
+// `pieces`), in units of 2^((z - M) c): the first pieces from their own
+// fields, the last the chunk's less the others (float-float; may round to
+// slightly below 0, which the callers clamp).
+__device__ __forceinline__ FF piece_mass(const ChunkRec& r, int p, int pieces, float M, float c) {
+  auto part = [&](int k) -> FF {
+    const float m = k == 0 ? r.mt : k == 1 ? r.bt : __int_as_float(r.it);
+    const float z = k == 0 ? r.st : k == 1 ? r.bd : __int_as_float(r.id);
+    return ff_mul(z, ex2((m - M) * c));
+  };
+  if (p < pieces - 1) return part(p);
+  FF x = ff_mul(r.sd, ex2((r.md - M) * c));
+  for (int k = 0; k < pieces - 1; ++k) x = ff_add(x, ff_neg(part(k)));
+  return x;
+}
+
+constexpr int kDrawTiles = 16 * kVecs;  // 256-vector tiles in the longest piece read (16 trips)
 static_assert(kDrawTiles <= 32, "one lane per tile");
 
 struct DrawSmem {
@@ -498,14 +514,15 @@ struct DrawSmem {
 template <int DT, bool VEC>
 __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V, bool draft_fields,
                           float M, float c, const char* row, float U, const float* kv,
-                          const int32_t* ki, int nk, const SgW& w, bool halves, DrawSmem& S) {
+                          const int32_t* ki, int nk, const SgW& w, int pieces, DrawSmem& S) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  // With halves the records also carry each chunk's first half (the sampler's
-  // chunks, in the target fields): the draw then locates and reads a half.
-  const int nloc = halves ? 2 * nchunk : nchunk;
-  const int32_t span = halves ? chunk / 2 : chunk;  // logits per located piece
+  // With pieces the records also carry each piece of their chunk (the
+  // sampler's chunks): the draw then locates and reads one piece.
+  const bool halves = pieces > 1;
+  const int nloc = halves ? pieces * nchunk : nchunk;
+  const int32_t span = halves ? chunk / pieces : chunk;  // logits per located piece
   // ---- warp 0: chunk masses, lanes over contiguous blocks of chunks --------
   if (warp == 0) {
     const FF one_m_c = two_sum(1.f, -w.C);
@@ -513,10 +530,8 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
     const int j0 = min(nloc, lane * per), j1 = min(nloc, j0 + per);
     auto mass = [&](int j) -> FF {
       FF x;
-      if (halves) {  // piece j is half j % 2 of chunk j / 2; the second is the rest
-        const ChunkRec r = ld_rec(recs + (j >> 1));
-        const FF first = ff_mul(r.st, ex2((r.mt - M) * c));
-        x = (j & 1) ? ff_add(ff_mul(r.sd, ex2((r.md - M) * c)), ff_neg(first)) : first;
+      if (halves) {  // piece j % pieces of chunk j / pieces
+        x = piece_mass(ld_rec(recs + j / pieces), j % pieces, pieces, M, c);
       } else {
         const ChunkRec r = ld_rec(recs + j);
         const float m = draft_fields ? r.md : r.mt, sm = draft_fields ? r.sd : r.st;
@@ -1213,7 +1228,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     const int tok = chunk_draw<DT, VEC>(P.recs + (u0 + nn) * P.nchunk, P.nchunk, P.chunk, P.V,
                                         kSample, S.dec.mt, c, row,
                                         P.unif[L.u_off + u_draw], S.sg_kv, S.sg_ki,
-                                        (kSample && sg_on) ? S.sg_nk : 0, w, kSample && P.half > 0,
+                                        (kSample && sg_on) ? S.sg_nk : 0, w, kSample ? P.pieces : 0,
                                         draw);
     if (threadIdx.x == 0) {
       S.tok_slot = tok;

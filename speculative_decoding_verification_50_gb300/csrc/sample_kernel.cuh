@@ -4,25 +4,26 @@
 // inverse CDF of U, §2.1).
 //
 // The row-statistics kernel has already read every row once and left, per
-// chunk, its record (the chunk's max and sum of 2^((z - max) c), its first
-// half's apart) and its top-F candidates.  A row's draw then needs only the
-// half chunk that holds U * R.  One warp per row does every step of it:
+// chunk, its record (the chunk's max and sum of 2^((z - max) c), and the same
+// for each of its pieces: quarters of 32-trip chunks) and its top-F
+// candidates.  A row's draw then needs only the piece that holds U * R.  One
+// warp per row does every step of it:
 //   1. combine the row's chunk records (one lane per chunk),
 //   2. merge the chunks' candidate lists into the row's top-F_s keys,
 //   3. the weighted mass R = S - (1 - C) x (the keys' mass) and the checks,
-//   4. a float-float scan over the half-chunk masses (the key corrections
-//      subtracted from the halves that hold them) finds the half holding U*R,
-//   5. that half is read in batches of 16 warp tiles (32 16-byte vectors
+//   4. a float-float scan over the pieces' masses (the key corrections
+//      subtracted from the pieces that hold them) finds the piece holding U*R,
+//   5. that piece is read in batches of 16 warp tiles (32 16-byte vectors
 //      each, coalesced) and summed unweighted in paired fp32 steps; a
 //      butterfly leaves one tile's sum in each lane, the keys' weights are
 //      applied per tile, a float-float scan over the tiles finds the tile, an
 //      fp32 scan over its lanes (weighted values, recomputed) the vector, and
 //      the crossing lane walks its elements.
 // All rows of a launch are in flight at once (8 per CTA, two CTAs per SM), so
-// the half chunks stream at HBM rate, where one CTA per row left most of its
+// the pieces stream at HBM rate, where one CTA per row left most of its
 // warps waiting at barriers.
 //
-// Rows whose keys hold so much of the mass that the half-chunk masses lose
+// Rows whose keys hold so much of the mass that the pieces' masses lose
 // fp32 precision to the correction (the same test as the CTA-per-row kernel)
 // are left to a CTA-wide pass over the whole row at the end of the CTA: its
 // eight warps sum the row's weighted values tile by tile, and warp 0 locates
@@ -51,7 +52,7 @@ struct PendRow {  // a row left for the CTA-wide pass, as its warp decided it
 // q and `fb` set when rounding left U * R at or past the end of what was
 // located (the last logit with r > 0 is then taken).
 template <int DT>
-__device__ __forceinline__ int warp_half_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V,
+__device__ __forceinline__ int warp_piece_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int pieces, int V,
                                               float M, float c, const char* row, float U,
                                               const float* kv, const int32_t* ki, int nk,
                                               const SgW& w, float& q, bool& fb) {
@@ -59,17 +60,15 @@ __device__ __forceinline__ int warp_half_draw(const ChunkRec* recs, int nchunk, 
   using Vec = typename E::Vec;
   constexpr int VW = E::VW;
   const int lane = threadIdx.x & 31;
-  const int nloc = 2 * nchunk;
-  const int32_t span = chunk / 2;  // logits per half chunk
+  const int nloc = pieces * nchunk;
+  const int32_t span = chunk / pieces;  // logits per piece
   const FF one_m_c = two_sum(1.f, -w.C);
   // ---- step 4: lanes over contiguous runs of halves ---------------------------
   const int per = (nloc + 31) / 32;
   const int j0 = min(nloc, lane * per), j1 = min(nloc, j0 + per);
-  auto mass = [&](int j) -> FF {  // half j % 2 of chunk j / 2; the second is the rest
-    const ChunkRec r = ld_rec(recs + (j >> 1));
-    const FF first = ff_mul(r.st, ex2((r.mt - M) * c));
-    FF x = (j & 1) ? ff_add(ff_mul(r.sd, ex2((r.md - M) * c)), ff_neg(first)) : first;
-    for (int k = 0; k < nk; ++k)  // the weighted keys of this half
+  auto mass = [&](int j) -> FF {  // piece j % pieces of chunk j / pieces
+    FF x = piece_mass(ld_rec(recs + j / pieces), j % pieces, pieces, M, c);
+    for (int k = 0; k < nk; ++k)  // the weighted keys of this piece
       if (ki[k] / span == j) x = ff_add(x, ff_neg(ff_mul(one_m_c, ex2((kv[k] - M) * c))));
     return x.hi > 0.f ? x : ff(0.f);
   };
@@ -86,7 +85,7 @@ __device__ __forceinline__ int warp_half_draw(const ChunkRec* recs, int nchunk, 
   fb = last;
   if (owner < 0) return -1;  // no mass at all (the caller's checks flag such rows)
   int pick = -1;
-  FF tin = ff(0.f);  // U * R less the mass before the chosen half
+  FF tin = ff(0.f);  // U * R less the mass before the chosen piece
   if (lane == owner) {
     FF run = ff_add(incl, ff_neg(mine));
     for (int j = j0; j < j1; ++j) {
@@ -98,7 +97,7 @@ __device__ __forceinline__ int warp_half_draw(const ChunkRec* recs, int nchunk, 
           tin = ff_add(tau, ff_neg(run));
           break;
         }
-        pick = j;  // the last half with mass so far
+        pick = j;  // the last piece with mass so far
         tin = x;
         run = nx;
       }
@@ -107,12 +106,12 @@ __device__ __forceinline__ int warp_half_draw(const ChunkRec* recs, int nchunk, 
   pick = __shfl_sync(0xffffffffu, pick, owner);
   tin = shfl(tin, owner);
 
-  // ---- step 5: the chosen half, tile by tile ----------------------------------
+  // ---- step 5: the chosen piece, tile by tile ---------------------------------
   const int64_t e0 = static_cast<int64_t>(pick) * span;
   const int64_t e1 = min(static_cast<int64_t>(V), e0 + span);
   const int nvc = static_cast<int>((e1 - e0 + VW - 1) / VW);
   const int ntile = (nvc + 31) / 32;
-  // The keys inside this half: lane k < nk holds key k's tile and (1 - C) x
+  // The keys inside this piece: lane k < nk holds key k's tile and (1 - C) x
   // its mass, subtracted from that tile's sum of 2^((z - M) c) below (the
   // loop sums every logit unweighted: identical to summing the weighted
   // values, up to rounding, since the keys are exactly the logits C weighs).
@@ -206,7 +205,7 @@ __device__ __forceinline__ int warp_half_draw(const ChunkRec* recs, int nchunk, 
     }
     run = ff_add(run, shfl(inc, 31));
   }
-  if (tsel < 0) {  // rounding: U * R at or past the end of the half
+  if (tsel < 0) {  // rounding: U * R at or past the end of the piece
     last = true;
     tsel = tlast;
     tw = twlast;
@@ -271,7 +270,7 @@ __device__ __forceinline__ void sample_write(const DecideParams& P, int b, int64
 }
 
 // One warp per sampled row (rows 8 x blockIdx.x + warp); aligned rows whose
-// records carry their first halves (P.half > 0).  Dynamic shared memory: the
+// records carry their chunks' pieces (P.pieces > 0).  Dynamic shared memory: the
 // segment sums of one whole row for the CTA-wide pass.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecideParams P) {
@@ -315,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecidePa
       const int32_t il = __shfl_sync(0xffffffffu, Lk.i, fs > 0 ? fs - 1 : 0);
       w = fs > 0 ? SgW{P.sg_C, zl, il} : SgW{P.sg_C, neg_inf(), -1};
       const bool valid = lane < fs && Lk.i != INT_MAX;
-      if (valid) {  // the keys, for the half masses (after the merge's last use of the scratch)
+      if (valid) {  // the keys, for the pieces' masses (after the merge's last use of the scratch)
         wkeys[warp].ov[lane] = Lk.v;
         wkeys[warp].oi[lane] = Lk.i;
       }
@@ -341,10 +340,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecidePa
         pend[warp] = PendRow{row, ps.Md, X.c, __fdiv_rn(1.f, sdp.hi), U, w, status, b};
       }
     } else {
-      // ---- 4-5. the half chunk holding U * R ------------------------------------
+      // ---- 4-5. the piece holding U * R -----------------------------------------
       float q;
       bool fb;
-      const int tok = warp_half_draw<DT>(P.recs + X.u0 * P.nchunk, P.nchunk, P.chunk, P.V, ps.Md, X.c,
+      const int tok = warp_piece_draw<DT>(P.recs + X.u0 * P.nchunk, P.nchunk, P.chunk, P.pieces, P.V, ps.Md, X.c,
                                          row, U, wkeys[warp].ov, wkeys[warp].oi, nk, w, q, fb);
       if (lane == 0) sample_write(P, b, X.u0, status | (fb ? kFallback : 0), tok, q);
     }

@@ -178,9 +178,15 @@ size_t plan_workspace(const Plan& pl) { return plan_workspace_split(pl); }
 
 constexpr size_t kMaxSegSmem = 200 * 1024;
 
+// Loop trips per chunk of the Saguaro sampler's rows: long chunks amortise the
+// per-chunk top-F epilogue (2304 rows of 152064 fp32: kernel A 0.2233 ms at
+// 16 trips, 0.2114 at 32), and the records carry each chunk's quarters, so the
+// draw still reads 8 trips' worth (64 KB of fp32).
+constexpr int kSampleIters = 32;
+
 // Sampled rows per SM from which the sampler's decision runs one warp per row
-// (fewer rows keep one CTA per row, whose eight warps read a row's half
-// chunk faster than one warp can).
+// (fewer rows keep one CTA per row, whose eight warps read a row's piece of
+// a chunk faster than one warp can).
 constexpr int kWarpRowsPerSm = 8;
 
 // Stages of the persistent path's ring (SPECV_STAGES = 2..8 fixes the count,
@@ -316,12 +322,12 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
       vec_ok(a->target_logits, packed ? 0 : a->target_batch_stride, a->target_row_stride, es) &&
       (nd || vec_ok(a->draft_logits, packed ? 0 : a->draft_batch_stride, a->draft_row_stride, es));
   Plan pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, mode == kModeMss ? 2 : 1,
-                      mode == kModeSample ? 16 : 8);
+                      mode == kModeSample ? kSampleIters : 8);
   // The sampler's rows draw from one chunk each (the chunk-local draw) when a
   // chunk is shorter than the row: the other CTAs of a cluster would only
   // wait, so its rows take one CTA each.
   if (mode == kModeSample && pl.CB > 1 && pl.chunk < V) {
-    const Plan one = make_plan(B, Ka, V, cands ? F : 0, a->dtype, 1, 16, 1);
+    const Plan one = make_plan(B, Ka, V, cands ? F : 0, a->dtype, 1, kSampleIters, 1);
     if (one.smemB <= kMaxSegSmem) pl = one;  // (a very long row keeps its cluster)
   }
   if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
@@ -357,10 +363,13 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.chunk = static_cast<int32_t>(pl.chunk);
   sp.iters = pl.iters;
   sp.stages = ring_stages();
-  // The sampler's staged chunks record their first half apart, so its draw
-  // reads half a chunk (two equal halves: an even trip count).
-  sp.half = (mode == kModeSample && vec && !persistent_path() && pl.iters >= 2 && pl.iters % 2 == 0)
-                ? pl.iters / 2 : 0;
+  // The sampler's staged chunks record their pieces apart (quarters when the
+  // trip count divides by 4, else halves when it is even), so its draw reads
+  // one piece.
+  if (mode == kModeSample && vec && !persistent_path()) {
+    sp.pieces = pl.iters % 4 == 0 ? 4 : pl.iters % 2 == 0 ? 2 : 0;
+    sp.piece = sp.pieces ? pl.iters / sp.pieces : 0;
+  }
   sp.cu = a->cu_num_draft_tokens;
   sp.ntok = a->num_draft_tokens;
   sp.stall = test_stall('A');
@@ -408,9 +417,10 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   // every CTA of the cluster: worth it when the chunk is the shorter read.
   // SPECV_LOCAL_DRAW=0/1 overrides, for tuning runs.
   static const int env_local = env_int("SPECV_LOCAL_DRAW", -1);
-  const bool fits = pl.chunk <= static_cast<int64_t>(kDrawTiles) * kThreads * vec_width(a->dtype);
+  const int64_t span = sp.pieces ? pl.chunk / sp.pieces : pl.chunk;  // what the draw reads
+  const bool fits = span <= static_cast<int64_t>(kDrawTiles) * kThreads * vec_width(a->dtype);
   dp.local_draw = fits && (env_local >= 0 ? env_local != 0 : pl.chunk < pl.L);
-  dp.half = sp.half;
+  dp.pieces = sp.pieces;
   dp.stall = test_stall('B');
   for (int k = 0; k <= K; ++k) dp.fk[k] = fanout ? fanout[k] : F;
   // Aligned rows stream the residual slice through a ring placed after the
@@ -440,7 +450,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   static const int env_warp = env_int("SPECV_SAMPLE_WARP", -1);
   const int64_t nv_row = (static_cast<int64_t>(V) + vec_width(a->dtype) - 1) / vec_width(a->dtype);
   const size_t smem_row = static_cast<size_t>((nv_row + kThreads - 1) / kThreads) * kWarps * sizeof(float);
-  const bool warp_rows = mode == kModeSample && vec && sp.half > 0 && smem_row <= kMaxSegSmem &&
+  const bool warp_rows = mode == kModeSample && vec && sp.pieces > 0 && smem_row <= kMaxSegSmem &&
                          (env_warp >= 0 ? env_warp != 0 : B >= kWarpRowsPerSm * sm_count());
   e = warp_rows             ? launch_sample_rows(a->dtype, B, smem_row, s, dp)
       : mode == kModeSsd    ? launch_decide<kModeSsd>(a->dtype, vec, pl.CB, B, smemB, s, dp)
@@ -581,7 +591,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
 
 size_t specv_saguaro_workspace_bytes(int32_t B, int32_t V, int32_t F, int32_t dtype) {
   if (B <= 0 || V < 1 || F < 0 || F > 32) return 0;
-  return plan_workspace(make_plan(B, 0, V, F > 0 ? F : 1, dtype, 1, 16));
+  return plan_workspace(make_plan(B, 0, V, F > 0 ? F : 1, dtype, 1, kSampleIters));
 }
 
 // Saguaro sampling runs the verification pipeline with no drafts (K = 0):

@@ -53,11 +53,14 @@ constexpr int kMaxStages = 8;
 constexpr int kTripBytes = kVecs * kThreads * 16;  // one row's share of a trip (8 KB)
 
 struct ChunkRec {        // 48 bytes per (unit, chunk)
-  float mt, st, md, sd;  // temperature rows: max and sum of 2^((z-max)c); a
-                         // sampler chunk split in halves keeps its first
-                         // half's draft statistics in mt, st
+  float mt, st, md, sd;  // temperature rows: max and sum of 2^((z-max)c)
   float bt, bd;          // greedy rows: best logit
   int32_t it, id;        // greedy rows: first index of the best logit
+                         // A sampled row's chunk split in pieces (2 or 4)
+                         // keeps its draft statistics (max, sum) per piece:
+                         // piece 0 in (mt, st), piece 1 in (bt, bd), piece 2
+                         // in (it, id) as float bits; the last piece is the
+                         // chunk's (md, sd) less the others.
   int32_t bad;           // bit 0: NaN or +inf seen in a greedy row (T > 0: shows
                          // as a NaN sum); bit 1: a staged copy did not land in time
   int32_t pad[3];
@@ -89,7 +92,8 @@ struct StatsParams {
   int32_t* cand_i;
   int32_t B, K, V, F, nchunk, chunk, iters;  // chunk = iters * kVecs * 256 * VW logits
   int32_t stages;     // ring stages of the staged paths, 2..kMaxStages
-  int32_t half;       // sampler rows: trips in a chunk's first half, recorded apart (0: none)
+  int32_t piece;      // sampler rows: trips per recorded piece of a chunk (0: none)
+  int32_t pieces;     //   and pieces per chunk (2 or 4)
   const int32_t* cu;  // per-row draft counts (inclusive prefix sums), or null
   int32_t ntok;       // with cu: packed draft rows the buffers hold
   int32_t stall;      // test hook: 1 + the item whose first stage waits for 16
@@ -410,7 +414,8 @@ __device__ __forceinline__ void push_key(KeyScratch& KS, float v, int32_t i) {
 template <int DT, bool VEC, int MODE>
 __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& C, int64_t item,
                                              bool greedy, float c, Acc<Elem<DT>::VW>& A, bool ok,
-                                             EpiSmem& S, int excl, const float2* snap = nullptr) {
+                                             EpiSmem& S, int excl, const float2* snap = nullptr,
+                                             int npieces = 0) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   constexpr bool kTopF = mode_has_topf(MODE);
@@ -428,17 +433,33 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     }
   } else {  // (a row the chunk does not have keeps its empty statistics)
     float mt = A.st.m, s_t = A.st.total(), md = A.sd.m, s_d = A.sd.total();
-    if (snap) {  // the draft's first half in the target slots, the whole chunk in the draft's
-      const float2 h = snap[threadIdx.x];
-      mt = h.x;
-      s_t = h.y;
-      const float M = fmaxf(mt, md);
-      s_d = s_t * ex2((mt - M) * c) + s_d * ex2((md - M) * c);
-      md = M;
-    }
-    if (C.rowt || snap) warp_soft_all(mt, s_t, c);
-    if (C.rowd) warp_soft_all(md, s_d, c);
+    if (C.rowt) warp_soft_all(mt, s_t, c);
+    if (C.rowd) warp_soft_all(md, s_d, c);  // with pieces: the last one
     if (lane == 0) {
+      if (snap) {
+        // the warp's earlier pieces (snap[k * kWarps + warp]) in the fields a
+        // sampled row leaves free, and with the last one the whole chunk
+        float2 pk[3] = {make_float2(kNegMax, 0.f), make_float2(kNegMax, 0.f), make_float2(kNegMax, 0.f)};
+        float M = md;
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          if (k < npieces - 1) {
+            pk[k] = snap[k * kWarps + warp];
+            M = fmaxf(M, pk[k].x);
+          }
+        float tot = s_d * ex2((md - M) * c);
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          if (k < npieces - 1) tot += pk[k].y * ex2((pk[k].x - M) * c);
+        md = M;
+        s_d = tot;
+        mt = pk[0].x;
+        s_t = pk[0].y;
+        S.wrec[warp].bt = pk[1].x;
+        S.wrec[warp].bd = pk[1].y;
+        S.wrec[warp].it = __float_as_int(pk[2].x);
+        S.wrec[warp].id = __float_as_int(pk[2].y);
+      }
       S.wrec[warp].mt = mt; S.wrec[warp].st = s_t; S.wrec[warp].md = md; S.wrec[warp].sd = s_d;
     }
   }
@@ -499,12 +520,22 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
       r.bad = __any_sync(0xffffffffu, bad);
     } else {
       float mt = kNegMax, s_t = 0.f, md = kNegMax, s_d = 0.f;
+      float m1 = kNegMax, s1 = 0.f, m2 = kNegMax, s2 = 0.f;
       if (lane < kWarps) {
         mt = S.wrec[lane].mt; s_t = S.wrec[lane].st; md = S.wrec[lane].md; s_d = S.wrec[lane].sd;
+        if (snap) {
+          m1 = S.wrec[lane].bt; s1 = S.wrec[lane].bd;
+          m2 = __int_as_float(S.wrec[lane].it); s2 = __int_as_float(S.wrec[lane].id);
+        }
       }
       if (C.rowt || snap) warp_soft_all<kWarps>(mt, s_t, c);
       if (C.rowd) warp_soft_all<kWarps>(md, s_d, c);
       r.mt = mt; r.st = s_t; r.md = md; r.sd = s_d;
+      if (snap && npieces > 2) {
+        warp_soft_all<kWarps>(m1, s1, c);
+        warp_soft_all<kWarps>(m2, s2, c);
+        r.bt = m1; r.bd = s1; r.it = __float_as_int(m2); r.id = __float_as_int(s2);
+      }
     }
     if (copy_bad) r.bad |= 2;
     if (lane == 0) P.recs[item] = r;
@@ -768,14 +799,16 @@ __device__ __forceinline__ int64_t covered_end(const Chunk& C) {
 // refills a stage after the CTA barrier that closes its consumption.  Returns
 // false (on every thread) if a wait gave up; the copies then in flight get a
 // bounded wait before returning.
-// half > 0: after `half` trips the draft row's running statistics move to
-// snap[threadIdx.x] and start again, so the chunk's first half is recorded
-// apart (all of it if the chunk is that short).
+// piece > 0: every `piece` trips, up to the chunk's last piece, the draft
+// row's running statistics, reduced over the warp, move to
+// snap[k * kWarps + warp] (piece k) and start again, so the chunk's pieces
+// are recorded apart (a short chunk fills the first pieces; the others stay
+// empty).
 // stall (test hook): stage 0 also waits for 16 bytes that no copy brings.
 template <int DT, bool GREEDY, bool KT, bool TOPF>
 __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* ring, int S2,
                                                     const Chunk& C, float c, Acc<Elem<DT>::VW>& A,
-                                                    bool stall, int half = 0,
+                                                    bool stall, int piece = 0, int npieces = 0,
                                                     float2* snap = nullptr) {
   const int ntr = ring_trips(C.nv);
   const int64_t covered = covered_end<DT>(C);
@@ -796,14 +829,21 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
   int s = 0;
   uint32_t ph = 0;
   const int nwhole = whole_trips<DT>(C, covered);
+  // the trip that ends the next recorded piece, and that piece
+  int snap_at = (!GREEDY && piece > 0 && npieces > 1) ? piece : -1;
+  int snap_k = 0;
   for (int t = 0; t < ntr; ++t) {
     if (!mbar_wait_bounded(&R.full[s], ph)) ok = false;
     const unsigned char* base = ring + static_cast<int64_t>(s) * sb;
     if (t < nwhole) consume_stage_whole<DT, GREEDY, KT, TOPF>(base, t, C, c, A, doff);
     else consume_stage<DT, GREEDY, KT, TOPF>(base, t, C, covered, c, A, doff);
-    if (!GREEDY && half > 0 && t + 1 == half) {
-      snap[threadIdx.x] = make_float2(A.sd.m, A.sd.total());
+    if (t + 1 == snap_at) {
+      float m = A.sd.m, z = A.sd.total();
+      warp_soft_all(m, z, c);
+      if ((threadIdx.x & 31) == 0) snap[snap_k * kWarps + (threadIdx.x >> 5)] = make_float2(m, z);
       A.sd.init();
+      ++snap_k;
+      snap_at = snap_k < npieces - 1 ? snap_at + piece : -1;
     }
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
@@ -829,9 +869,18 @@ __device__ __forceinline__ bool stream_chunk_staged(RingBars& R, unsigned char* 
       ph ^= 1u;
     }
   }
-  if (!GREEDY && half > 0 && ntr < half) {  // a short chunk: all of it is the first half
-    snap[threadIdx.x] = make_float2(A.sd.m, A.sd.total());
-    A.sd.init();
+  if (!GREEDY && piece > 0) {  // a short chunk: the rest is the next piece, the others empty
+    const int taken = snap_k;
+    for (int k = taken; k < npieces - 1; ++k) {
+      float m = kNegMax, z = 0.f;
+      if (k == taken) {
+        m = A.sd.m;
+        z = A.sd.total();
+        warp_soft_all(m, z, c);
+        A.sd.init();
+      }
+      if ((threadIdx.x & 31) == 0) snap[k * kWarps + (threadIdx.x >> 5)] = make_float2(m, z);
+    }
   }
   return ok;
 }
@@ -859,16 +908,16 @@ __global__ void __launch_bounds__(kThreads, (stats_ctas_per_sm<DT, VEC, MODE>())
   Acc<Elem<DT>::VW> A;
   A.init();
   bool ok = true;
-  // the sampler's chunks may record their first half apart (staged path)
-  __shared__ float2 snap[MODE == kModeSample ? kThreads : 1];
-  const bool halves = MODE == kModeSample && VEC && !greedy && P.half > 0;
+  // the sampler's chunks may record their pieces apart (staged path)
+  __shared__ float2 snap[MODE == kModeSample ? 3 * kWarps : 1];
+  const bool halves = MODE == kModeSample && VEC && !greedy && P.piece > 0;
   if (VEC) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ RingBars R;
     const bool stall = P.stall == static_cast<int64_t>(blockIdx.x) + 1;
     ok = greedy ? stream_chunk_staged<DT, true, kT, kTopF>(R, ring, P.stages, C, c, A, stall)
                 : stream_chunk_staged<DT, false, kT, kTopF>(R, ring, P.stages, C, c, A, stall,
-                                                            halves ? P.half : 0, snap);
+                                                            halves ? P.piece : 0, P.pieces, snap);
   } else if (greedy) {
     stream_chunk<DT, false, true, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
                                              P.iters, c, A);
@@ -876,7 +925,8 @@ __global__ void __launch_bounds__(kThreads, (stats_ctas_per_sm<DT, VEC, MODE>())
     stream_chunk<DT, false, false, kT, kTopF>(C.rowt, C.rowd, C.rowd != nullptr, C.v0, C.v1, C.nv,
                                               P.iters, c, A);
   }
-  chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S, excl, halves ? snap : nullptr);
+  chunk_finish<DT, VEC, MODE>(P, C, blockIdx.x, greedy, c, A, ok, S, excl, halves ? snap : nullptr,
+                              P.pieces);
 }
 
 // ---- persistent path ------------------------------------------------------------
