@@ -30,7 +30,6 @@
 
 namespace specv {
 
-constexpr int kMaxK = 32;
 constexpr int kTileUnroll = 8;  // tiles of r per loop trip in the residual pass
 
 struct PosStats {  // one position's combined row statistics

@@ -362,6 +362,9 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   sp.nchunk = static_cast<int32_t>(pl.nchunk);
   sp.chunk = static_cast<int32_t>(pl.chunk);
   sp.iters = pl.iters;
+  // Candidates per chunk at each position: the fan-out (F when uniform), and
+  // never fewer than the Saguaro F_s the draft rows' weights need.
+  for (int k = 0; k <= Ka; ++k) sp.fk[k] = max(fanout ? fanout[k] : F, sg_F);
   sp.stages = ring_stages();
   // The sampler's staged chunks record their pieces apart (quarters when the
   // trip count divides by 4, else halves when it is even), so its draw reads
@@ -562,6 +565,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
   sp.nchunk = static_cast<int32_t>(pl.nchunk);
   sp.chunk = static_cast<int32_t>(pl.chunk);
   sp.iters = pl.iters;
+  for (int k = 0; k <= K; ++k) sp.fk[k] = a->fanout ? a->fanout[k] : F;
   sp.stages = ring_stages();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_stats<kModePredict>(a->dtype, vec, persistent_path(), sm_count(), units * pl.nchunk, s, sp);

@@ -10,6 +10,7 @@
 namespace specv {
 
 constexpr int kMaxF = 32;
+constexpr int kMaxK = 32;  // drafts per row (K + 1 positions)
 
 template <int VW>
 struct Soft {  // online (max, sum) with VW partial sums for accuracy

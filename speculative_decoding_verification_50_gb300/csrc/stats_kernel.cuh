@@ -91,6 +91,8 @@ struct StatsParams {
   float* cand_v;      // [units * nchunk * F] (predict / ssd)
   int32_t* cand_i;
   int32_t B, K, V, F, nchunk, chunk, iters;  // chunk = iters * kVecs * 256 * VW logits
+  int32_t fk[kMaxK + 1];  // candidates a chunk at position k keeps (<= F; the rest of its
+                          // F slots padded): the fan-out, at least the Saguaro F_s
   int32_t stages;     // ring stages of the staged paths, 2..kMaxStages
   int32_t piece;      // sampler rows: trips per recorded piece of a chunk (0: none)
   int32_t pieces;     //   and pieces per chunk (2 or 4)
@@ -472,7 +474,8 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     // bound on the chunk's top-F without it.
     float s = A.kd.m1;  // this thread's draft maximum
     float tw, tf;
-    if (P.F < kWarps) {
+    const int Fu = P.fk[C.i];  // candidates this chunk keeps
+    if (Fu < kWarps) {
       // g = 1: the warp's largest maximum.  A warp with no finite maximum
       // (a short chunk) leaves the bound unset and the chunk takes the exact
       // path below.
@@ -490,10 +493,10 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
           s = take_max ? fmaxf(s, o) : fminf(s, o);
         }
       }
-      tw = __shfl_sync(0xffffffffu, s, (P.F + kWarps) / kWarps - 1);
+      tw = __shfl_sync(0xffffffffu, s, (Fu + kWarps) / kWarps - 1);
       // Fallback when some warp holds fewer than g finite maxima (a short last
       // chunk): the largest, over warps, of a warp's (F+1)-th largest maximum.
-      tf = (P.F < 32) ? __shfl_sync(0xffffffffu, s, P.F) : neg_inf();
+      tf = (Fu < 32) ? __shfl_sync(0xffffffffu, s, Fu) : neg_inf();
     }
     if (lane == 0) {
       S.wthr[warp] = tw;
@@ -551,7 +554,7 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     // fetches vector l, l+32, ... of the list (candidate, vector k).  Too many
     // qualifiers (ties at the bound), or no finite bound at all (masked rows,
     // chunks with fewer than F+1 finite logits), take the exact warp-list path.
-    const int F = P.F;
+    const int F = P.fk[C.i];  // candidates kept; the output holds P.F slots
     float thr = S.wthr[0], thr_f = S.wthr_f[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) {
@@ -607,8 +610,8 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     if (!bounded && threadIdx.x == 0) S.KS.count = kCandCap + 1;  // exact path below
     cons_sync();
     const int m = S.KS.count;
-    float* outv = P.cand_v + item * F;
-    int32_t* outi = P.cand_i + item * F;
+    float* outv = P.cand_v + item * P.F;
+    int32_t* outi = P.cand_i + item * P.F;
     if (m <= kCandCap) {
       // distinct indices: the ranks are 0..m-1, each written once; slots
       // m..F-1 (fewer candidates than F) are padded
@@ -622,7 +625,7 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
           outi[rank] = ii;
         }
       }
-      if (threadIdx.x >= m && threadIdx.x < F) {
+      if (threadIdx.x >= min(m, F) && threadIdx.x < P.F) {
         outv[threadIdx.x] = neg_inf();
         outi[threadIdx.x] = INT_MAX;
       }
@@ -659,7 +662,13 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
         S.wl_i[warp][lane] = L.i;
       }
       cons_sync();
-      if (warp == 0) merge_lists(S.wl_v, S.wl_i, kWarps, F, lane, outv, outi);
+      if (warp == 0) {
+        merge_lists(S.wl_v, S.wl_i, kWarps, F, lane, outv, outi);
+        if (lane >= F && lane < P.F) {
+          outv[lane] = neg_inf();
+          outi[lane] = INT_MAX;
+        }
+      }
     }
   }
   cons_sync();
