@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecidePa
   __shared__ int32_t npend[kWarps];
   __shared__ FF total;
   __shared__ FF tau_s;
-  __shared__ int32_t pass_again, last_pos, mode_s;
+  __shared__ int32_t pass_again, mode_s;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int b = static_cast<int>(blockIdx.x) * kWarps + warp;
@@ -356,10 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecidePa
   for (int pw = 0; pw < kWarps; ++pw) {
     if (!npend[pw]) continue;  // (the same in every thread)
     const PendRow& R = pend[pw];
-    if (threadIdx.x == 0) {
-      mode_s = 3;
-      last_pos = 0;
-    }
+    if (threadIdx.x == 0) mode_s = 3;
     __syncthreads();
     for (int pass = 0; pass < 2; ++pass) {
       const int mode = mode_s;
