@@ -91,7 +91,8 @@ struct DecideParams {
   int32_t sg_F;      // Saguaro sampling: the drafts came from sigma_{sg_F, sg_C}
   float sg_C;        //   (0: plain softmax drafts); the sampler's own F and C
   int32_t local_draw;  // draws from a whole row read only the chunk holding U * R
-  int32_t pieces;      // the sampler's records carry each chunk's pieces apart (2 or 4; 0: none)
+  int32_t pieces;      // the sampler's chunks are split in pieces (2, 4 or 8; 0: none)
+  const float2* piece_stats;  // their (max, sum), kMaxPieces entries per chunk
   int32_t stall;       // test hook: 1 + the batch row whose first residual stage (rank 0)
                        // waits for 16 bytes no copy brings, so its wait runs out (0: none)
   // MSS (K = M candidates per node, one target and one draft row each)
@@ -469,20 +470,11 @@ __device__ __forceinline__ bool ring_residual(RingBars& R, unsigned char* ring, 
   return ok;
 }
 
-// Mass of piece p of a sampled row's chunk record (the chunk split in
-// `pieces`), in units of 2^((z - M) c): the first pieces from their own
-// fields, the last the chunk's less the others (float-float; may round to
-// slightly below 0, which the callers clamp).
-__device__ __forceinline__ FF piece_mass(const ChunkRec& r, int p, int pieces, float M, float c) {
-  auto part = [&](int k) -> FF {
-    const float m = k == 0 ? r.mt : k == 1 ? r.bt : __int_as_float(r.it);
-    const float z = k == 0 ? r.st : k == 1 ? r.bd : __int_as_float(r.id);
-    return ff_mul(z, ex2((m - M) * c));
-  };
-  if (p < pieces - 1) return part(p);
-  FF x = ff_mul(r.sd, ex2((r.md - M) * c));
-  for (int k = 0; k < pieces - 1; ++k) x = ff_add(x, ff_neg(part(k)));
-  return x;
+// Mass of piece p of a sampled row's chunk, in units of 2^((z - M) c), from
+// the row-statistics kernel's table (read through L2: another kernel wrote it).
+__device__ __forceinline__ FF piece_mass(const float2* stats, int p, float M, float c) {
+  const float2 h = __ldcg(stats + p);
+  return ff_mul(h.y, ex2((h.x - M) * c));
 }
 
 constexpr int kDrawTiles = 16 * kVecs;  // 256-vector tiles in the longest piece read (16 trips)
@@ -513,15 +505,17 @@ struct DrawSmem {
 template <int DT, bool VEC>
 __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V, bool draft_fields,
                           float M, float c, const char* row, float U, const float* kv,
-                          const int32_t* ki, int nk, const SgW& w, int pieces, DrawSmem& S) {
+                          const int32_t* ki, int nk, const SgW& w, int pieces,
+                          const float2* piece_stats, DrawSmem& S) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  // With pieces the records also carry each piece of their chunk (the
-  // sampler's chunks): the draw then locates and reads one piece.
-  const bool halves = pieces > 1;
-  const int nloc = halves ? pieces * nchunk : nchunk;
-  const int32_t span = halves ? chunk / pieces : chunk;  // logits per located piece
+  // With pieces the row-statistics kernel also wrote the statistics of each
+  // piece of a chunk (the sampler's chunks): the draw then locates and reads
+  // one piece.
+  const bool split = pieces > 1;
+  const int nloc = split ? pieces * nchunk : nchunk;
+  const int32_t span = split ? chunk / pieces : chunk;  // logits per located piece
   // ---- warp 0: chunk masses, lanes over contiguous blocks of chunks --------
   if (warp == 0) {
     const FF one_m_c = two_sum(1.f, -w.C);
@@ -529,8 +523,8 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
     const int j0 = min(nloc, lane * per), j1 = min(nloc, j0 + per);
     auto mass = [&](int j) -> FF {
       FF x;
-      if (halves) {  // piece j % pieces of chunk j / pieces
-        x = piece_mass(ld_rec(recs + j / pieces), j % pieces, pieces, M, c);
+      if (split) {  // piece j % pieces of chunk j / pieces
+        x = piece_mass(piece_stats + static_cast<int64_t>(j / pieces) * kMaxPieces, j % pieces, M, c);
       } else {
         const ChunkRec r = ld_rec(recs + j);
         const float m = draft_fields ? r.md : r.mt, sm = draft_fields ? r.sd : r.st;
@@ -1228,6 +1222,8 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
                                         kSample, S.dec.mt, c, row,
                                         P.unif[L.u_off + u_draw], S.sg_kv, S.sg_ki,
                                         (kSample && sg_on) ? S.sg_nk : 0, w, kSample ? P.pieces : 0,
+                                        (kSample && P.pieces) ? P.piece_stats + (u0 + nn) * P.nchunk * kMaxPieces
+                                                              : nullptr,
                                         draw);
     if (threadIdx.x == 0) {
       S.tok_slot = tok;

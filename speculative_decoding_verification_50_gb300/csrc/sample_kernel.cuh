@@ -4,8 +4,8 @@
 // inverse CDF of U, §2.1).
 //
 // The row-statistics kernel has already read every row once and left, per
-// chunk, its record (the chunk's max and sum of 2^((z - max) c), and the same
-// for each of its pieces: quarters of 32-trip chunks) and its top-F
+// chunk, its record (the chunk's max and sum of 2^((z - max) c)), the same
+// for each of its pieces (eighths of 32-trip chunks) and its top-F
 // candidates.  A row's draw then needs only the piece that holds U * R.  One
 // warp per row does every step of it:
 //   1. combine the row's chunk records (one lane per chunk),
@@ -45,14 +45,14 @@ struct PendRow {  // a row left for the CTA-wide pass, as its warp decided it
   int32_t b;
 };
 
-// Steps 4-5 for one row by one warp.  recs: the row's chunk records; row: the
+// Steps 4-5 for one row by one warp.  piece_stats: the row's piece table; row: the
 // row's logits; M, c: its max and log2(e)/T; U: its uniform; keys: its top-F_s
 // keys (value, index) in the warp's shared scratch, nk of them; w: the
 // weights.  Returns the token in every lane (-1: no mass), with r(t) / R in
 // q and `fb` set when rounding left U * R at or past the end of what was
 // located (the last logit with r > 0 is then taken).
 template <int DT>
-__device__ __forceinline__ int warp_piece_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int pieces, int V,
+__device__ __forceinline__ int warp_piece_draw(const float2* piece_stats, int nchunk, int32_t chunk, int pieces, int V,
                                               float M, float c, const char* row, float U,
                                               const float* kv, const int32_t* ki, int nk,
                                               const SgW& w, float& q, bool& fb) {
@@ -67,7 +67,7 @@ __device__ __forceinline__ int warp_piece_draw(const ChunkRec* recs, int nchunk,
   const int per = (nloc + 31) / 32;
   const int j0 = min(nloc, lane * per), j1 = min(nloc, j0 + per);
   auto mass = [&](int j) -> FF {  // piece j % pieces of chunk j / pieces
-    FF x = piece_mass(ld_rec(recs + j / pieces), j % pieces, pieces, M, c);
+    FF x = piece_mass(piece_stats + static_cast<int64_t>(j / pieces) * kMaxPieces, j % pieces, M, c);
     for (int k = 0; k < nk; ++k)  // the weighted keys of this piece
       if (ki[k] / span == j) x = ff_add(x, ff_neg(ff_mul(one_m_c, ex2((kv[k] - M) * c))));
     return x.hi > 0.f ? x : ff(0.f);
@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecidePa
       // ---- 4-5. the piece holding U * R -----------------------------------------
       float q;
       bool fb;
-      const int tok = warp_piece_draw<DT>(P.recs + X.u0 * P.nchunk, P.nchunk, P.chunk, P.pieces, P.V, ps.Md, X.c,
+      const int tok = warp_piece_draw<DT>(P.piece_stats + X.u0 * P.nchunk * kMaxPieces, P.nchunk, P.chunk,
+                                          P.pieces, P.V, ps.Md, X.c,
                                          row, U, wkeys[warp].ov, wkeys[warp].oi, nk, w, q, fb);
       if (lane == 0) sample_write(P, b, X.u0, status | (fb ? kFallback : 0), tok, q);
     }

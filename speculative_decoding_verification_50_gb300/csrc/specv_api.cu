@@ -109,6 +109,7 @@ struct Plan {
   int64_t L;       // kernel-B slice per CTA
   size_t smemB;    // kernel-B dynamic shared memory (segment sums)
   size_t recs_bytes, cand_bytes;
+  size_t piece_bytes;  // the sampler's piece table (kMaxPieces entries per chunk), or 0
 };
 
 int sm_count() {
@@ -130,7 +131,7 @@ int sm_count() {
 // trips (kernel A 258 -> 215 us on 2304 rows of 152064 fp32); the decision
 // kernel's chunk-local draw reads up to 16 trips.
 Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int min_cb = 1,
-               int iters0 = 8, int max_cb = 16) {
+               int iters0 = 8, int max_cb = 16, bool piece_table = false) {
   Plan pl;
   const int vw = vec_width(dtype);
   const int64_t units = static_cast<int64_t>(B > 0 ? B : 0) * (K + 1);
@@ -169,10 +170,12 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
   pl.smemB = static_cast<size_t>(ntiles) * kWarps * sizeof(float);
   pl.recs_bytes = round_up(static_cast<size_t>(units * pl.nchunk) * sizeof(ChunkRec), 256);
   pl.cand_bytes = F > 0 ? round_up(static_cast<size_t>(units * pl.nchunk * F) * 4, 256) : 0;
+  pl.piece_bytes =
+      piece_table ? round_up(static_cast<size_t>(units * pl.nchunk) * kMaxPieces * sizeof(float2), 256) : 0;
   return pl;
 }
 
-size_t plan_workspace_split(const Plan& pl) { return pl.recs_bytes + 2 * pl.cand_bytes; }
+size_t plan_workspace_split(const Plan& pl) { return pl.recs_bytes + 2 * pl.cand_bytes + pl.piece_bytes; }
 
 size_t plan_workspace(const Plan& pl) { return plan_workspace_split(pl); }
 
@@ -180,8 +183,8 @@ constexpr size_t kMaxSegSmem = 200 * 1024;
 
 // Loop trips per chunk of the Saguaro sampler's rows: long chunks amortise the
 // per-chunk top-F epilogue (2304 rows of 152064 fp32: kernel A 0.2233 ms at
-// 16 trips, 0.2114 at 32), and the records carry each chunk's quarters, so the
-// draw still reads 8 trips' worth (64 KB of fp32).
+// 16 trips, 0.2114 at 32), and each chunk's eighths are recorded, so the draw
+// reads 4 trips' worth (32 KB of fp32).
 constexpr int kSampleIters = 32;
 
 // Sampled rows per SM from which the sampler's decision runs one warp per row
@@ -322,12 +325,12 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
       vec_ok(a->target_logits, packed ? 0 : a->target_batch_stride, a->target_row_stride, es) &&
       (nd || vec_ok(a->draft_logits, packed ? 0 : a->draft_batch_stride, a->draft_row_stride, es));
   Plan pl = make_plan(B, Ka, V, cands ? F : 0, a->dtype, mode == kModeMss ? 2 : 1,
-                      mode == kModeSample ? kSampleIters : 8);
+                      mode == kModeSample ? kSampleIters : 8, 16, mode == kModeSample);
   // The sampler's rows draw from one chunk each (the chunk-local draw) when a
   // chunk is shorter than the row: the other CTAs of a cluster would only
   // wait, so its rows take one CTA each.
   if (mode == kModeSample && pl.CB > 1 && pl.chunk < V) {
-    const Plan one = make_plan(B, Ka, V, cands ? F : 0, a->dtype, 1, kSampleIters, 1);
+    const Plan one = make_plan(B, Ka, V, cands ? F : 0, a->dtype, 1, kSampleIters, 1, true);
     if (one.smemB <= kMaxSegSmem) pl = one;  // (a very long row keeps its cluster)
   }
   if (pl.smemB > kMaxSegSmem) return fail(SPECV_ERR_UNSUPPORTED, "V=%d too large", V);
@@ -342,6 +345,8 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   ChunkRec* recs = reinterpret_cast<ChunkRec*>(ws);
   float* cand_v = pl.cand_bytes ? reinterpret_cast<float*>(ws + pl.recs_bytes) : nullptr;
   int32_t* cand_i = pl.cand_bytes ? reinterpret_cast<int32_t*>(ws + pl.recs_bytes + pl.cand_bytes) : nullptr;
+  float2* piece_stats =
+      pl.piece_bytes ? reinterpret_cast<float2*>(ws + pl.recs_bytes + 2 * pl.cand_bytes) : nullptr;
 
   StatsParams sp = {};
   sp.zt = a->target_logits;
@@ -366,12 +371,13 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   // never fewer than the Saguaro F_s the draft rows' weights need.
   for (int k = 0; k <= Ka; ++k) sp.fk[k] = max(fanout ? fanout[k] : F, sg_F);
   sp.stages = ring_stages();
-  // The sampler's staged chunks record their pieces apart (quarters when the
-  // trip count divides by 4, else halves when it is even), so its draw reads
-  // one piece.
-  if (mode == kModeSample && vec && !persistent_path()) {
-    sp.pieces = pl.iters % 4 == 0 ? 4 : pl.iters % 2 == 0 ? 2 : 0;
+  // The sampler's staged chunks record their pieces apart (eighths when the
+  // trip count divides by 8, else quarters or halves), so its draw reads one
+  // piece.
+  if (mode == kModeSample && vec && !persistent_path() && piece_stats) {
+    sp.pieces = pl.iters % 8 == 0 ? 8 : pl.iters % 4 == 0 ? 4 : pl.iters % 2 == 0 ? 2 : 0;
     sp.piece = sp.pieces ? pl.iters / sp.pieces : 0;
+    sp.piece_stats = piece_stats;
   }
   sp.cu = a->cu_num_draft_tokens;
   sp.ntok = a->num_draft_tokens;
@@ -424,6 +430,7 @@ specv_status run_verify(const specv_verify_args* a, void* workspace, size_t work
   const bool fits = span <= static_cast<int64_t>(kDrawTiles) * kThreads * vec_width(a->dtype);
   dp.local_draw = fits && (env_local >= 0 ? env_local != 0 : pl.chunk < pl.L);
   dp.pieces = sp.pieces;
+  dp.piece_stats = sp.piece_stats;
   dp.stall = test_stall('B');
   for (int k = 0; k <= K; ++k) dp.fk[k] = fanout ? fanout[k] : F;
   // Aligned rows stream the residual slice through a ring placed after the
@@ -595,7 +602,7 @@ specv_status specv_predict_outcomes(const specv_predict_args* a, void* workspace
 
 size_t specv_saguaro_workspace_bytes(int32_t B, int32_t V, int32_t F, int32_t dtype) {
   if (B <= 0 || V < 1 || F < 0 || F > 32) return 0;
-  return plan_workspace(make_plan(B, 0, V, F > 0 ? F : 1, dtype, 1, kSampleIters));
+  return plan_workspace(make_plan(B, 0, V, F > 0 ? F : 1, dtype, 1, kSampleIters, 16, true));
 }
 
 // Saguaro sampling runs the verification pipeline with no drafts (K = 0):

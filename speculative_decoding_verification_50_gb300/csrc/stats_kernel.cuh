@@ -56,11 +56,6 @@ struct ChunkRec {        // 48 bytes per (unit, chunk)
   float mt, st, md, sd;  // temperature rows: max and sum of 2^((z-max)c)
   float bt, bd;          // greedy rows: best logit
   int32_t it, id;        // greedy rows: first index of the best logit
-                         // A sampled row's chunk split in pieces (2 or 4)
-                         // keeps its draft statistics (max, sum) per piece:
-                         // piece 0 in (mt, st), piece 1 in (bt, bd), piece 2
-                         // in (it, id) as float bits; the last piece is the
-                         // chunk's (md, sd) less the others.
   int32_t bad;           // bit 0: NaN or +inf seen in a greedy row (T > 0: shows
                          // as a NaN sum); bit 1: a staged copy did not land in time
   int32_t pad[3];
@@ -80,6 +75,11 @@ __device__ __forceinline__ ChunkRec ld_rec(const ChunkRec* p) {
   return r;
 }
 
+// A sampled row's chunk may be split in up to kMaxPieces equal pieces, whose
+// draft statistics (max, sum of 2^((z-max)c)) the kernel also writes, to a
+// table of kMaxPieces entries per chunk.
+constexpr int kMaxPieces = 8;
+
 struct StatsParams {
   const void* zt;
   int64_t t_bs, t_rs;
@@ -95,7 +95,8 @@ struct StatsParams {
                           // F slots padded): the fan-out, at least the Saguaro F_s
   int32_t stages;     // ring stages of the staged paths, 2..kMaxStages
   int32_t piece;      // sampler rows: trips per recorded piece of a chunk (0: none)
-  int32_t pieces;     //   and pieces per chunk (2 or 4)
+  int32_t pieces;     //   and pieces per chunk (2, 4 or 8)
+  float2* piece_stats;  // [units * nchunk * kMaxPieces] (max, sum) of each piece
   const int32_t* cu;  // per-row draft counts (inclusive prefix sums), or null
   int32_t ntok;       // with cu: packed draft rows the buffers hold
   int32_t stall;      // test hook: 1 + the item whose first stage waits for 16
@@ -416,7 +417,7 @@ __device__ __forceinline__ void push_key(KeyScratch& KS, float v, int32_t i) {
 template <int DT, bool VEC, int MODE>
 __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& C, int64_t item,
                                              bool greedy, float c, Acc<Elem<DT>::VW>& A, bool ok,
-                                             EpiSmem& S, int excl, const float2* snap = nullptr,
+                                             EpiSmem& S, int excl, float2* snap = nullptr,
                                              int npieces = 0) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
@@ -437,31 +438,19 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
     float mt = A.st.m, s_t = A.st.total(), md = A.sd.m, s_d = A.sd.total();
     if (C.rowt) warp_soft_all(mt, s_t, c);
     if (C.rowd) warp_soft_all(md, s_d, c);  // with pieces: the last one
-    if (lane == 0) {
-      if (snap) {
-        // the warp's earlier pieces (snap[k * kWarps + warp]) in the fields a
-        // sampled row leaves free, and with the last one the whole chunk
-        float2 pk[3] = {make_float2(kNegMax, 0.f), make_float2(kNegMax, 0.f), make_float2(kNegMax, 0.f)};
-        float M = md;
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-          if (k < npieces - 1) {
-            pk[k] = snap[k * kWarps + warp];
-            M = fmaxf(M, pk[k].x);
-          }
-        float tot = s_d * ex2((md - M) * c);
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-          if (k < npieces - 1) tot += pk[k].y * ex2((pk[k].x - M) * c);
-        md = M;
-        s_d = tot;
-        mt = pk[0].x;
-        s_t = pk[0].y;
-        S.wrec[warp].bt = pk[1].x;
-        S.wrec[warp].bd = pk[1].y;
-        S.wrec[warp].it = __float_as_int(pk[2].x);
-        S.wrec[warp].id = __float_as_int(pk[2].y);
+    if (snap) {  // the warp's last piece joins the others; the chunk is their sum (lane k: piece k)
+      if (lane == 0) snap[(npieces - 1) * kWarps + warp] = make_float2(md, s_d);
+      __syncwarp();
+      md = kNegMax;
+      s_d = 0.f;
+      if (lane < npieces) {
+        const float2 h = snap[lane * kWarps + warp];
+        md = h.x;
+        s_d = h.y;
       }
+      warp_soft_all(md, s_d, c);
+    }
+    if (lane == 0) {
       S.wrec[warp].mt = mt; S.wrec[warp].st = s_t; S.wrec[warp].md = md; S.wrec[warp].sd = s_d;
     }
   }
@@ -523,25 +512,25 @@ __device__ __forceinline__ void chunk_finish(const StatsParams& P, const Chunk& 
       r.bad = __any_sync(0xffffffffu, bad);
     } else {
       float mt = kNegMax, s_t = 0.f, md = kNegMax, s_d = 0.f;
-      float m1 = kNegMax, s1 = 0.f, m2 = kNegMax, s2 = 0.f;
       if (lane < kWarps) {
         mt = S.wrec[lane].mt; s_t = S.wrec[lane].st; md = S.wrec[lane].md; s_d = S.wrec[lane].sd;
-        if (snap) {
-          m1 = S.wrec[lane].bt; s1 = S.wrec[lane].bd;
-          m2 = __int_as_float(S.wrec[lane].it); s2 = __int_as_float(S.wrec[lane].id);
-        }
       }
-      if (C.rowt || snap) warp_soft_all<kWarps>(mt, s_t, c);
+      if (C.rowt) warp_soft_all<kWarps>(mt, s_t, c);
       if (C.rowd) warp_soft_all<kWarps>(md, s_d, c);
       r.mt = mt; r.st = s_t; r.md = md; r.sd = s_d;
-      if (snap && npieces > 2) {
-        warp_soft_all<kWarps>(m1, s1, c);
-        warp_soft_all<kWarps>(m2, s2, c);
-        r.bt = m1; r.bd = s1; r.it = __float_as_int(m2); r.id = __float_as_int(s2);
-      }
     }
     if (copy_bad) r.bad |= 2;
     if (lane == 0) P.recs[item] = r;
+  }
+  if (snap && !greedy && warp < npieces) {  // warp k: piece k over the CTA
+    float m = kNegMax, z = 0.f;
+    if (lane < kWarps) {
+      const float2 h = snap[warp * kWarps + lane];
+      m = h.x;
+      z = h.y;
+    }
+    warp_soft_all<kWarps>(m, z, c);
+    if (lane == 0) P.piece_stats[item * kMaxPieces + warp] = make_float2(m, z);
   }
 
   if (kTopF) {
@@ -918,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, (stats_ctas_per_sm<DT, VEC, MODE>())
   A.init();
   bool ok = true;
   // the sampler's chunks may record their pieces apart (staged path)
-  __shared__ float2 snap[MODE == kModeSample ? 3 * kWarps : 1];
+  __shared__ float2 snap[MODE == kModeSample ? kMaxPieces * kWarps : 1];
   const bool halves = MODE == kModeSample && VEC && !greedy && P.piece > 0;
   if (VEC) {
     extern __shared__ __align__(128) unsigned char ring[];
