@@ -21,9 +21,9 @@
 // R and the CTA whose range holds U_K * R; that CTA walks its segments and one
 // warp scans the one segment that holds the crossing (a re-read of 32
 // vectors).  A draw from a whole row's own distribution reads only the chunk
-// (or half-chunk) holding U * R instead.  Meanwhile warps 1..7 of every CTA
-// merge the chunk candidate lists into the outcome keys (one warp per
-// lookahead).  Rank 0 writes the outputs.
+// (or, for the sampler, the piece of a chunk) holding U * R instead.
+// Meanwhile warps 1..7 of every CTA merge the chunk candidate lists into the
+// outcome keys (one warp per lookahead).  Rank 0 writes the outputs.
 #pragma once
 
 #include "stats_kernel.cuh"
