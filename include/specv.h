@@ -39,7 +39,9 @@
  *     (per-chunk statistics and candidates into the workspace), then one
  *     decision per batch row (launched as a programmatic dependent of the
  *     first).  The workspace needs no initialisation: everything a call
- *     reads from it is written earlier in the same call.
+ *     reads from it is written earlier in the same call.  A call only
+ *     enqueues kernels on the given stream, so it can be captured in a CUDA
+ *     graph and replayed (on new inputs written into the same buffers).
  *   - Limits: 1 <= K <= 32, 0 <= B, 1 <= F <= 32, 1 <= V < 2^31 (in practice
  *     up to about 10^8: beyond that a CTA's table of partial sums no longer
  *     fits in shared memory and the call returns SPECV_ERR_UNSUPPORTED).
