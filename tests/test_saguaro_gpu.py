@@ -113,10 +113,13 @@ def test_sampler_law_small_vocab(sv, olib):
     assert chisquare(counts, q * n).pvalue > 1e-3
 
 
-@pytest.mark.parametrize("Fs,C", [(1, 0.3), (4, 47 / 147), (6, 0.0)])
-def test_ssd_round_with_saguaro_drafts(sv, olib, Fs, C):
+@pytest.mark.parametrize("Fs,C,fanout", [(1, 0.3, None), (4, 47 / 147, None), (6, 0.0, None),
+                                         (6, 0.3, [6, 4, 2, 1, 0])])
+def test_ssd_round_with_saguaro_drafts(sv, olib, Fs, C, fanout):
     """Config 4 with drafts from sigma_{Fs,C}: accept lengths, tokens, p/q,
-    keys and hit against the oracle's verify(saguaro=...) + predict + hit."""
+    keys and hit against the oracle's verify(saguaro=...) + predict + hit.
+    With a fan-out whose later lookaheads keep fewer keys than F_s, the
+    statistics kernel must still keep F_s candidates there for the weights."""
     spec = wl.SPECS["cfg4"]
     data = wl.generate(spec)
     F = spec.F
@@ -130,12 +133,12 @@ def test_ssd_round_with_saguaro_drafts(sv, olib, Fs, C):
         tok[:, i] = np.where(s["tokens"] >= 0, s["tokens"], tok[:, i])
     out = sv.specv_ssd_round(to_dev(data["target"], spec.dtype), to_dev(data["draft"], spec.dtype),
                              to_dev(tok), to_dev(data["temperature"]), to_dev(data["uniforms"]), F,
-                             saguaro=(Fs, C))
+                             saguaro=(Fs, C), fanout=fanout)
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in out.items()}
     o = oracle.verify(data["target"], data["draft"], tok, data["temperature"], data["uniforms"],
                       nthreads=0, lib=olib, saguaro=(Fs, C))
-    op = oracle.predict(data["draft"], tok, F, nthreads=0, lib=olib)
+    op = oracle.predict(data["draft"], tok, F, nthreads=0, lib=olib, fanout=fanout)
     status = o["status"] | op["status"]
     err = status & oracle.ROW_ERRORS
     assert np.array_equal(g["row_status"] & oracle.ROW_ERRORS, err)
