@@ -23,6 +23,7 @@ CASES = [
     (313, 128256, wl.BF16, 1, 0.25),
     (257, 50000, wl.FP32, 32, 0.0),
     (67, 152064, wl.FP32, 0, 1.0),
+    (130, 50001, wl.FP32, 6, 0.3),  # rows padded to 50004: a ragged last vector
 ]
 
 
@@ -52,7 +53,13 @@ def run_case(rows, V, dtype, F, C, olib, seed):
     U = rng.uniform(0, 1, rows).astype(np.float32)
     bf16 = dtype == wl.BF16
     zz = wl.f32_to_bf16_bits(z) if bf16 else z
-    g = sv.specv_saguaro_sample(dev(zz, bf16), dev(T), F, C, dev(U))
+    zdev = dev(zz, bf16)
+    pad = (-V) % (8 if bf16 else 4)
+    if pad:  # the same rows in a buffer whose rows start 16-byte aligned
+        buf = torch.zeros((rows, V + pad), dtype=zdev.dtype, device=zdev.device)
+        buf[:, :V] = zdev
+        zdev = buf[:, :V]
+    g = sv.specv_saguaro_sample(zdev, dev(T), F, C, dev(U))
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in g.items()}
     o = oracle.saguaro_sample(zz, T, F, C, U, lib=olib)
