@@ -3,7 +3,8 @@ decision paths, run in a fresh process so that the library reads this
 environment's SPECV_SAMPLE_WARP (one warp per row when 1, one CTA per row
 when 0; the variable is read once per process).  Each case mixes greedy
 rows, rows whose top keys hold most of the mass (the whole-row pass), a row
-with a bad temperature and a row holding NaN, and ends on a partial CTA.
+with a bad temperature and a row holding NaN, and ends on a partial CTA; one
+case's rows are padded (16-byte aligned rows whose last vector is ragged).
 Prints "sampler case ok <rows>" or raises.  Run by
 tests/test_sampler_warp_gpu.py as `python -m tests._sampler_case`.
 """
