@@ -867,6 +867,20 @@ def run_ours(args) -> None:
             dd["hit_rate"] = round(float(w["hit"].float().mean().item()), 4)
         return dd
 
+    def decision_reread() -> int | None:
+        """Logit bytes the decision kernel reads again in the last call: a
+        sampled batch row that rejected draft n reads target and draft row n,
+        one that accepted all K drafts at most target row K (less when its draw
+        is chunk-local); greedy rows read none.  Strided verification and SSD
+        rounds only."""
+        if mode is not None or d["draft"] is None:
+            return None
+        n = outs["accept_len"].cpu().numpy()
+        T = np.asarray(lay["temperature"]).reshape(-1)[:len(n)]
+        es = d["target"].element_size()
+        rows = np.where(T > 0, np.where(n < K, 2, 1), 0)
+        return int(rows.sum()) * V * es
+
     kernel_bytes = lay["bytes"]
     # The roofline's kernel is launch 1, the one that streams every logit once
     # (its algorithmic bytes are the logits), timed apart from the call's
@@ -881,6 +895,15 @@ def run_ours(args) -> None:
              f"({'bf16' if w['is_bf16'] else 'fp32'} {mode or ('ssd' if F else 'verify')}): "
              "streams every logit once")
     f_mean, s_mean = statistics.mean(m["first_ms"]), statistics.mean(m["second_ms"])
+    # the decision kernel's own bytes and rate (launch 2, split event)
+    reread = decision_reread()
+    decision_line = None
+    if reread is not None and s_mean > 0:
+        dgbs = reread / (s_mean / 1e3) / 1e9
+        decision_line = {"reread_bytes": reread, "ms": round(s_mean, 5), "gbs": round(dgbs, 1),
+                         "frac": round(dgbs / peak, 4),
+                         "note": "rows of the rejected position read again (at most one row "
+                                 "after a full acceptance); records and candidates not counted"}
     dominant = {"launch": "1" if m["dominant"] == 0 else f"2..{w['per_call'][0]}",
                 "share_of_split_call": round(max(f_mean, s_mean) / (f_mean + s_mean), 4)}
     line = {
@@ -948,6 +971,7 @@ def run_ours(args) -> None:
                 "h2d_gbs": round(h2d / (h2d_ms / 1e3) / 1e9, 1),
                 "host_placement": placement},
         "outcome": outcome_summary(),
+        **({"decision": decision_line} if decision_line else {}),
         "gpu_launches": m["launches"],
         "clocks": clocks,
     }
