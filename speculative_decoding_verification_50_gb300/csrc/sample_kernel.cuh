@@ -43,6 +43,7 @@ struct PendRow {  // a row left for the CTA-wide pass, as its warp decided it
   SgW w;
   int32_t status;
   int32_t b;
+  int64_t u0;  // its output slot
 };
 
 // Steps 4-5 for one row by one warp.  piece_stats: the row's piece table; row: the
@@ -63,7 +64,7 @@ __device__ __forceinline__ int warp_piece_draw(const float2* piece_stats, int nc
   const int nloc = pieces * nchunk;
   const int32_t span = chunk / pieces;  // logits per piece
   const FF one_m_c = two_sum(1.f, -w.C);
-  // ---- step 4: lanes over contiguous runs of halves ---------------------------
+  // ---- step 4: lanes over contiguous runs of pieces ---------------------------
   const int per = (nloc + 31) / 32;
   const int j0 = min(nloc, lane * per), j1 = min(nloc, j0 + per);
   auto mass = [&](int j) -> FF {  // piece j % pieces of chunk j / pieces
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecidePa
       // the keys hold most of the mass: the CTA-wide pass over the whole row
       if (lane == 0) {
         npend[warp] = 1;
-        pend[warp] = PendRow{row, ps.Md, X.c, __fdiv_rn(1.f, sdp.hi), U, w, status, b};
+        pend[warp] = PendRow{row, ps.Md, X.c, __fdiv_rn(1.f, sdp.hi), U, w, status, b, X.u0};
       }
     } else {
       // ---- 4-5. the piece holding U * R -----------------------------------------
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const DecidePa
                                    R.mt, R.c, R.ist, R.ist, -1, R.w, rq);
       }
       if (lane == 0)
-        sample_write(P, R.b, static_cast<int64_t>(R.b) * (P.K + 1), status, tok,
+        sample_write(P, R.b, R.u0, status, tok,
                      Rt.hi > 0.f ? __fdiv_rn(rq, Rt.hi) : 0.f);
     }
     __syncthreads();

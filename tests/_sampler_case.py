@@ -2,7 +2,8 @@
 decision paths, run in a fresh process so that the library reads this
 environment's SPECV_SAMPLE_WARP (one warp per row when 1, one CTA per row
 when 0; the variable is read once per process).  Each case mixes greedy
-rows, rows whose top keys hold most of the mass (the whole-row pass), a row
+rows, rows whose top keys hold most of the mass (the whole-row pass; two of them
+share a CTA), a row
 with a bad temperature and a row holding NaN, and ends on a partial CTA; one
 case's rows are padded (16-byte aligned rows whose last vector is ragged).
 Prints "sampler case ok <rows>" or raises.  Run by
@@ -45,12 +46,13 @@ def near_boundary(z, T, F, C, U, tok, olib):
 def run_case(rows, V, dtype, F, C, olib, seed):
     rng = np.random.default_rng(seed)
     z = rng.normal(0, 2.5, (rows, V)).astype(np.float32)
-    for b in (3, rows // 2, rows - 1):  # the keys hold most of the mass
+    heavy = (3, 16, 17, rows // 2, rows - 1)  # the keys hold most of the mass (16, 17: one CTA)
+    for b in heavy:
         z[b, rng.choice(V, 6, replace=False)] += 16.0
     z[9, 1234] = np.nan
     T = rng.choice([0.0, 0.7, 1.0, 1.3], rows).astype(np.float32)
     T[5] = -1.0
-    T[3] = T[rows // 2] = T[rows - 1] = 1.0
+    T[list(heavy)] = 1.0
     U = rng.uniform(0, 1, rows).astype(np.float32)
     bf16 = dtype == wl.BF16
     zz = wl.f32_to_bf16_bits(z) if bf16 else z

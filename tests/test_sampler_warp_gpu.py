@@ -1,5 +1,5 @@
 """The Saguaro sampler's two decision kernels against the oracle: one warp
-per row (the default from two rows per SM on) and one CTA per row, each
+per row (the default from eight rows per SM on) and one CTA per row, each
 forced on every case of tests/_sampler_case.py (greedy rows, whole-row passes,
 error rows, partial CTAs; fp32 and bf16) in a fresh process."""
 import os
