@@ -26,6 +26,8 @@ CASES = [
     (257, 50000, wl.FP32, 32, 0.0),
     (67, 152064, wl.FP32, 0, 1.0),
     (130, 50001, wl.FP32, 6, 0.3),  # rows padded to 50004: a ragged last vector
+    (70, 4096, wl.FP32, 6, 0.3),    # short rows: one chunk, most pieces empty
+    (70, 1000, wl.BF16, 3, 0.5),
 ]
 
 
@@ -49,7 +51,7 @@ def run_case(rows, V, dtype, F, C, olib, seed):
     heavy = (3, 16, 17, rows // 2, rows - 1)  # the keys hold most of the mass (16, 17: one CTA)
     for b in heavy:
         z[b, rng.choice(V, 6, replace=False)] += 16.0
-    z[9, 1234] = np.nan
+    z[9, min(1234, V - 1)] = np.nan
     T = rng.choice([0.0, 0.7, 1.0, 1.3], rows).astype(np.float32)
     T[5] = -1.0
     T[list(heavy)] = 1.0
