@@ -7,7 +7,9 @@ one-wave rule, the kernel-B cluster size and slice, the chunk-local draw,
 ring or direct residual pass) meet combinations nobody picked: batch sizes
 from 1 to 1216 across the cluster-size thresholds, K from 1 to 12, V from 1
 to 152064, both dtypes, the three logit recipes, mixed temperatures and
-F from 1 to 12.  Same bars as tests/test_parity_gpu.py: every row the oracle
+F from 1 to 12 (and 24 MSS shapes, 16 sampler shapes below, with the bars
+of tests/test_mss_gpu.py and tests/_sampler_case.py).  Same bars as
+tests/test_parity_gpu.py: every row the oracle
 does not flag is exact, and at most 2 % of the rows (at least one) differ.
 The flagged rows themselves are only counted: a flat row of 152064 logits
 has many tokens of probability below 2e-6, and a draw of such a token is
@@ -93,3 +95,98 @@ def test_sweep_matches_oracle(sv, olib, shape):
         compare_verify(g, o, data["temperature"], _id(shape))
     nd = differing_rows(g, o)
     assert nd <= max(1, shape["B"] // 50), nd
+
+
+# ---- MSS nodes and the Saguaro sampler over seeded shapes -------------------
+
+def _mss_shapes(n=24, seed=20261203):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        B = int(rng.choice([1, 3, 40, 300, 1300]))
+        M = int(rng.integers(1, 9))
+        band = int(rng.integers(0, 4))
+        V = int([rng.integers(1, 300), rng.integers(300, 8000), rng.integers(8000, 70000), 152064][band])
+        if 2 * B * V > 40_000_000:
+            continue
+        dtype = wl.FP32 if rng.integers(0, 2) else wl.BF16
+        temps = tuple(sorted(set(float(t) for t in rng.choice([0.0, 0.6, 1.0, 1.4], int(rng.integers(1, 4))))))
+        out.append(dict(B=B, M=M, V=V, dtype=dtype, temps=temps, naive=bool(rng.random() < 0.2),
+                        ragged=bool(rng.random() < 0.3), seed=wl.SEED_BASE + 13000 + len(out)))
+    return out
+
+
+def _mss_id(s):
+    return (f"mss-B{s['B']}-M{s['M']}-V{s['V']}-{s['dtype']}" + ("-naive" if s["naive"] else "") +
+            ("-ragged" if s["ragged"] else ""))
+
+
+@pytest.mark.parametrize("shape", _mss_shapes(), ids=_mss_id)
+def test_sweep_mss_matches_oracle(sv, olib, shape):
+    from tests.test_mss_gpu import compare, run_pair
+    spec = wl.custom(_mss_id(shape), B=shape["B"], K=1, V=shape["V"], dtype=shape["dtype"],
+                     temps=shape["temps"], sigma_d=(0.3, 2.5), seed=shape["seed"])
+    data = wl.generate_mss(spec, shape["M"])
+    nc = None
+    if shape["ragged"]:  # per-node candidate counts 0..M
+        nc = np.random.default_rng(shape["seed"]).integers(0, shape["M"] + 1, shape["B"]).astype(np.int32)
+    g, o = run_pair(sv, olib, data, shape["dtype"] == wl.BF16, naive=shape["naive"], num_candidates=nc)
+    compare(g, o, data, _mss_id(shape))
+
+
+def _sampler_shapes(n=16, seed=20261204):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        rows = int(rng.choice([1, 5, 100, 1216, 2000]))
+        band = int(rng.integers(0, 4))
+        V = int([rng.integers(1, 300), rng.integers(300, 8000), rng.integers(8000, 70000), 152064][band])
+        dtype = wl.FP32 if rng.integers(0, 2) else wl.BF16
+        if dtype == wl.BF16:
+            V += (-V) % 8  # contiguous rows stay 16-byte aligned (the vector paths)
+        else:
+            V += (-V) % 4
+        if rows * V > 60_000_000:
+            continue
+        F = int(rng.integers(0, 17))
+        C = float(np.round(rng.uniform(0.0, 1.0), 3)) if F else 1.0
+        out.append(dict(rows=rows, V=V, dtype=dtype, F=F, C=C, sigma=float(rng.choice([1.0, 2.5, 4.0])),
+                        seed=wl.SEED_BASE + 14000 + len(out)))
+    return out
+
+
+def _sampler_id(s):
+    return f"sample-R{s['rows']}-V{s['V']}-{s['dtype']}-F{s['F']}-C{s['C']}"
+
+
+@pytest.mark.parametrize("shape", _sampler_shapes(), ids=_sampler_id)
+def test_sweep_sampler_matches_oracle(sv, olib, shape):
+    """specv_saguaro_sample (one warp per row from 1216 rows, one CTA per row
+    below) against the oracle: error bits exact, tokens exact except draws
+    within 1e-6 of a CDF step, sigma(token) within 1e-5."""
+    from tests._sampler_case import near_boundary
+    rng = np.random.default_rng(shape["seed"])
+    rows, V, F, C = shape["rows"], shape["V"], shape["F"], shape["C"]
+    z = (rng.standard_normal((rows, V)) * shape["sigma"]).astype(np.float32)
+    T = rng.choice([0.0, 0.7, 1.0, 1.3], rows).astype(np.float32)
+    U = rng.uniform(0, 1, rows).astype(np.float32)
+    bf16 = shape["dtype"] == wl.BF16
+    zz = wl.f32_to_bf16_bits(z) if bf16 else z
+    zt = torch.from_numpy(np.ascontiguousarray(zz))
+    zdev = (zt.view(torch.bfloat16) if bf16 else zt).cuda()
+    g = sv.specv_saguaro_sample(zdev, torch.from_numpy(T).cuda(), F, C, torch.from_numpy(U).cuda())
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in g.items()}
+    o = oracle.saguaro_sample(zz, T, F, C, U, lib=olib)
+    err = o["status"] & oracle.ROW_ERRORS
+    assert np.array_equal(g["row_status"] & oracle.ROW_ERRORS, err)
+    differ = 0
+    for b in np.nonzero(err == 0)[0]:
+        if g["tokens"][b] != o["tokens"][b]:
+            assert near_boundary(zz[b], float(T[b]), F, C, float(U[b]), int(o["tokens"][b]), olib), \
+                (b, g["tokens"][b], o["tokens"][b], T[b])
+            differ += 1
+        else:
+            assert abs(g["q"][b] - o["q"][b]) <= 1e-5, (b, g["q"][b], o["q"][b])
+    assert differ <= max(1, rows // 50), differ
+    print(f"[{_sampler_id(shape)}] differing rows {differ}/{rows}")
