@@ -445,6 +445,28 @@ def test_ssd_round_ragged(sv, olib, B, K, V, dtype, F):
 
 
 @pytest.mark.parametrize("dtype", [wl.FP32, wl.BF16])
+@pytest.mark.parametrize("V", [1000, 4101, 40000])
+def test_ssd_round_padded_and_sliced_layouts(sv, olib, dtype, V):
+    """The fused SSD round on row stride > V (16-byte aligned rows, a ragged
+    tail) and on a slice of a wider tensor (unaligned rows: the element path
+    of both kernels, the keys from the register path's candidates)."""
+    spec = wl.custom(f"ssdpad{V}", B=6, K=3, V=V, dtype=dtype, temps=(0.0, 0.9), ssd=True, F=6,
+                     sigma_d=(0.3, 2.0), seed=wl.SEED_BASE + 8500 + V)
+    data = wl.generate(spec)
+    pad = (-V) % 16 + 16
+    for layout in ("padded", "offset"):
+        lo, w = (0, V + pad) if layout == "padded" else (1, V + 1)
+        t = np.zeros(data["target"].shape[:2] + (w,), data["target"].dtype)
+        d = np.zeros(data["draft"].shape[:2] + (w,), data["draft"].dtype)
+        t[..., lo:lo + V] = data["target"]
+        d[..., lo:lo + V] = data["draft"]
+        tt, dd = to_dev(t, dtype)[..., lo:lo + V], to_dev(d, dtype)[..., lo:lo + V]
+        g = gpu_ssd(sv, data, spec.F, tt, dd)
+        o, keys, kl = oracle_ssd(olib, data, spec.F)
+        compare_ssd(olib, g, o, keys, kl, data["temperature"], f"ssd {layout} V={V}")
+
+
+@pytest.mark.parametrize("dtype", [wl.FP32, wl.BF16])
 def test_ssd_round_edge_cases(sv, olib, dtype):
     base = _edge_batch(wl.FP32)
     zt, zd = base["target"], base["draft"]

@@ -160,10 +160,12 @@ def _sampler_id(s):
 
 
 @pytest.mark.parametrize("shape", _sampler_shapes(), ids=_sampler_id)
-def test_sweep_sampler_matches_oracle(sv, olib, shape):
-    """specv_saguaro_sample (one warp per row from 1216 rows, one CTA per row
-    below) against the oracle: error bits exact, tokens exact except draws
-    within 1e-6 of a CDF step, sigma(token) within 1e-5."""
+@pytest.mark.parametrize("layout", ["contiguous", "offset"])
+def test_sweep_sampler_matches_oracle(sv, olib, shape, layout):
+    """specv_saguaro_sample (one warp per row from 1216 rows of aligned rows,
+    one CTA per row otherwise) against the oracle, on contiguous rows and on
+    unaligned rows (one element into a wider buffer): error bits exact, tokens
+    exact except draws within 1e-6 of a CDF step, sigma(token) within 1e-5."""
     from tests._sampler_case import near_boundary
     rng = np.random.default_rng(shape["seed"])
     rows, V, F, C = shape["rows"], shape["V"], shape["F"], shape["C"]
@@ -172,8 +174,15 @@ def test_sweep_sampler_matches_oracle(sv, olib, shape):
     U = rng.uniform(0, 1, rows).astype(np.float32)
     bf16 = shape["dtype"] == wl.BF16
     zz = wl.f32_to_bf16_bits(z) if bf16 else z
-    zt = torch.from_numpy(np.ascontiguousarray(zz))
+    if layout == "offset":  # rows one element into a wider buffer: unaligned, the element paths
+        wide = np.zeros((rows, V + 1), zz.dtype)
+        wide[:, 1:] = zz
+        zt = torch.from_numpy(wide)
+    else:
+        zt = torch.from_numpy(np.ascontiguousarray(zz))
     zdev = (zt.view(torch.bfloat16) if bf16 else zt).cuda()
+    if layout == "offset":
+        zdev = zdev[:, 1:]
     g = sv.specv_saguaro_sample(zdev, torch.from_numpy(T).cuda(), F, C, torch.from_numpy(U).cuda())
     torch.cuda.synchronize()
     g = {k: v.cpu().numpy() for k, v in g.items()}
@@ -189,4 +198,4 @@ def test_sweep_sampler_matches_oracle(sv, olib, shape):
         else:
             assert abs(g["q"][b] - o["q"][b]) <= 1e-5, (b, g["q"][b], o["q"][b])
     assert differ <= max(1, rows // 50), differ
-    print(f"[{_sampler_id(shape)}] differing rows {differ}/{rows}")
+    print(f"[{_sampler_id(shape)} {layout}] differing rows {differ}/{rows}")
