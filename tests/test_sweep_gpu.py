@@ -7,8 +7,9 @@ one-wave rule, the kernel-B cluster size and slice, the chunk-local draw,
 ring or direct residual pass) meet combinations nobody picked: batch sizes
 from 1 to 1216 across the cluster-size thresholds, K from 1 to 12, V from 1
 to 152064, both dtypes, the three logit recipes, mixed temperatures and
-F from 1 to 12 (and 24 MSS shapes, 16 sampler shapes below, with the bars
-of tests/test_mss_gpu.py and tests/_sampler_case.py).  Same bars as
+F from 1 to 12 (and below: 24 MSS shapes and 16 sampler shapes, with the
+bars of tests/test_mss_gpu.py and tests/_sampler_case.py, and 16 outcome
+prediction shapes with fan-outs and ties, keys exact).  Same bars as
 tests/test_parity_gpu.py: every row the oracle
 does not flag is exact, and at most 2 % of the rows (at least one) differ.
 The flagged rows themselves are only counted: a flat row of 152064 logits
@@ -199,3 +200,60 @@ def test_sweep_sampler_matches_oracle(sv, olib, shape, layout):
             assert abs(g["q"][b] - o["q"][b]) <= 1e-5, (b, g["q"][b], o["q"][b])
     assert differ <= max(1, rows // 50), differ
     print(f"[{_sampler_id(shape)} {layout}] differing rows {differ}/{rows}")
+
+
+def _predict_shapes(n=16, seed=20261205):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        B = int(rng.choice([1, 3, 32, 100, 700]))
+        K = int(rng.integers(1, 13))
+        band = int(rng.integers(0, 4))
+        V = int([rng.integers(1, 300), rng.integers(300, 8000), rng.integers(8000, 70000), 152064][band])
+        if B * (K + 1) * V > 40_000_000:
+            continue
+        dtype = wl.FP32 if rng.integers(0, 2) else wl.BF16
+        F = int(rng.integers(1, 33))
+        fan = None
+        if rng.random() < 0.4:  # a per-lookahead fan-out (any counts in 0..F)
+            fan = [int(x) for x in rng.integers(0, F + 1, K + 1)]
+        out.append(dict(B=B, K=K, V=V, dtype=dtype, F=F, fan=fan, grid=bool(rng.random() < 0.3),
+                        seed=wl.SEED_BASE + 15000 + len(out)))
+    return out
+
+
+def _predict_id(s):
+    return (f"predict-B{s['B']}-K{s['K']}-V{s['V']}-{s['dtype']}-F{s['F']}" +
+            ("-fan" if s["fan"] else "") + ("-ties" if s["grid"] else ""))
+
+
+@pytest.mark.parametrize("shape", _predict_shapes(), ids=_predict_id)
+def test_sweep_predict_matches_oracle(sv, olib, shape):
+    """specv_predict_outcomes (keys and key logits exact, ties included: some
+    shapes draw logits on a coarse grid) and specv_check_hit on random
+    outcomes against those keys."""
+    rng = np.random.default_rng(shape["seed"])
+    B, K, V, F = shape["B"], shape["K"], shape["V"], shape["F"]
+    if shape["grid"]:
+        z = (rng.integers(-4, 5, (B, K + 1, V)) * 0.5).astype(np.float32)
+    else:
+        z = (rng.standard_normal((B, K + 1, V)) * 2.0).astype(np.float32)
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    zz = wl.f32_to_bf16_bits(z) if shape["dtype"] == wl.BF16 else z
+    t = torch.from_numpy(np.ascontiguousarray(zz))
+    dft = (t.view(torch.bfloat16) if shape["dtype"] == wl.BF16 else t).cuda()
+    pr = sv.specv_predict_outcomes(dft, torch.from_numpy(tok).cuda(), F, fanout=shape["fan"])
+    torch.cuda.synchronize()
+    op = oracle.predict(zz, tok, F, nthreads=0, lib=olib, fanout=shape["fan"])
+    keys = pr["keys"].cpu().numpy()
+    assert np.array_equal(keys, op["keys"])
+    assert np.array_equal(pr["key_logits"].cpu().numpy(), op["key_logits"])
+    assert np.array_equal(pr["row_status"].cpu().numpy(), op["status"])
+    n = rng.integers(-1, K + 2, B).astype(np.int32)
+    outs = rng.integers(-1, V, (B, K + 1)).astype(np.int32)
+    for b in range(0, B, 3):  # some outcomes that are keys
+        if 0 <= n[b] <= K:
+            outs[b, n[b]] = keys[b, n[b], 0]
+    h = sv.specv_check_hit(pr["keys"], torch.from_numpy(n).cuda(), torch.from_numpy(outs).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(h.cpu().numpy(), oracle.check_hit(op["keys"], n, outs, lib=olib))
