@@ -1,7 +1,7 @@
 """The benchmark's other config 5 workloads at full size, in the launch
 configuration bench.py times (inputs laid out by bench.py's own code):
-the Saguaro sampler over the 2304 draft rows of a round (16-trip chunks, the
-32-tile chunk-local draw), per-row draft counts over packed rows, and
+the Saguaro sampler over the 2304 draft rows of a round (32-trip chunks
+recorded in eighths, one warp per row for the draw), per-row draft counts over packed rows, and
 verification without draft logits.  Every row against the oracle, the same
 bars as the smaller cases (tokens and accept lengths exact except boundary
 rows, probabilities within 1e-5, error bits exact).  The oracle flags a row
