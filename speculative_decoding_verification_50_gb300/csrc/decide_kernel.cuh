@@ -45,7 +45,8 @@ struct Dec {  // a batch row's decision (the same in every CTA of its cluster)
   float mt, md, ist, isd;
   float sgc, zl;  // residual weights: C on the keys at or above (zl, il)
   int32_t il;
-  int32_t full_pass;  // the sampler's draw reads the whole row (see below)
+  int32_t full_pass;  // a chunk-local draw reads the whole row instead (see below)
+  float zx;      // without draft probabilities: the target logit of the rejected token
   FF R;          // total residual mass (the sampler normalises its q by it)
   FF tau, pre_mine;
   float px[kMaxK], qx[kMaxK];
@@ -495,7 +496,9 @@ struct DrawSmem {
 // A draw from a whole row's own distribution, r(v) = w(v) 2^((z_v - M) c) with
 // w = C on the row's top-F_s keys (the sampler) or 1 (the bonus after all K
 // drafts are accepted), by inverse CDF of U ("Speculative Speculative
-// Decoding" §2.1; §4.2.1).  The row-statistics kernel's chunk records give
+// Decoding" §2.1; §4.2.1); with xex >= 0, w(xex) = 0 (the residual
+// max(p - q, 0) when q is one-hot at the rejected token xex, whose logit is
+// zex: "Speculative Decoding" dl-note, Appendix, NO_DRAFT_PROBS).  The row-statistics kernel's chunk records give
 // every chunk's mass, so the prefix over chunks finds the chunk holding U * R
 // and only that chunk is read again: its 256-vector tiles give per-warp sums,
 // a scan over tiles and then warps narrows U * R to 32 vectors, and a warp
@@ -506,7 +509,7 @@ template <int DT, bool VEC>
 __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V, bool draft_fields,
                           float M, float c, const char* row, float U, const float* kv,
                           const int32_t* ki, int nk, const SgW& w, int pieces,
-                          const float2* piece_stats, DrawSmem& S) {
+                          const float2* piece_stats, int32_t xex, float zex, DrawSmem& S) {
   using E = Elem<DT>;
   constexpr int VW = E::VW;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -532,6 +535,7 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
       }
       for (int k = 0; k < nk; ++k)  // the weighted keys of this piece
         if (ki[k] / span == j) x = ff_add(x, ff_neg(ff_mul(one_m_c, ex2((kv[k] - M) * c))));
+      if (xex >= 0 && xex / span == j) x = ff_add(x, ff(-ex2((zex - M) * c)));  // the excluded token
       return x.hi > 0.f ? x : ff(0.f);
     };
     FF mine = ff(0.f);
@@ -585,8 +589,9 @@ __device__ int chunk_draw(const ChunkRec* recs, int nchunk, int32_t chunk, int V
     E::unpack(v, z);
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
+      const int64_t e = e0 + static_cast<int64_t>(j) * VW + k;
       const float p = ex2((z[k] - M) * c);
-      r[k] = w.in(z[k], e0 + static_cast<int64_t>(j) * VW + k) ? __fmul_rn(p, w.C) : p;
+      r[k] = e == xex ? 0.f : (w.in(z[k], e) ? __fmul_rn(p, w.C) : p);
     }
   };
   auto rvals = [&](int j, float (&r)[VW]) { rfrom(load_vec<DT, VEC>(row, e0, e1, j), j, r); };
@@ -1165,6 +1170,12 @@ __device__ __forceinline__ void decide_prepare(const DecideParams& P, const RowC
       // row instead (its residual total is then summed from the weighted
       // values themselves).
       S.dec.full_pass = (kSample && sg_on) ? (__fmul_rn(one_m_c.hi, S.sg_d[0]) > 0.5f * q.Sd.hi) : 0;
+      // Without draft probabilities the residual at a rejection is p_n less
+      // its rejected token: the same draw with that token's mass taken from
+      // its chunk, or the whole row when the token holds most of the mass.
+      S.dec.zx = (n < kb && nd) ? S.pre_zt[n] : 0.f;
+      if (!kSample && n < kb && nd)
+        S.dec.full_pass = ex2(__fmul_rn(S.dec.zx - q.Mt, c)) > 0.5f * q.St.hi;
       S.dec.tau = ff(0.f);
       S.dec.pre_mine = ff(0.f);
       S.tok_slot = S.dec.token;
@@ -1210,7 +1221,8 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
   // it from the chunk records and reads that chunk alone -----------------------
   // (P.local_draw: the host's choice, made when a chunk is shorter than one
   // CTA's slice of the row and holds at most kDrawTiles tiles)
-  const bool local_draw = S.dec.need_scan && P.local_draw && (S.dec.mode == 1 || (S.dec.mode == 3 && !S.dec.full_pass));
+  const bool local_draw = S.dec.need_scan && P.local_draw &&
+                          (S.dec.mode == 1 || ((S.dec.mode == 3 || S.dec.mode == 2) && !S.dec.full_pass));
   const bool scan = S.dec.need_scan && !local_draw;  // the residual pass over row n
   if (local_draw && rank == 0) {
     const int nn = S.dec.n;
@@ -1224,7 +1236,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
                                         (kSample && sg_on) ? S.sg_nk : 0, w, kSample ? P.pieces : 0,
                                         (kSample && P.pieces) ? P.piece_stats + (u0 + nn) * P.nchunk * kMaxPieces
                                                               : nullptr,
-                                        draw);
+                                        S.dec.mode == 2 ? S.dec.xn : -1, S.dec.zx, draw);
     if (threadIdx.x == 0) {
       S.tok_slot = tok;
       S.q_slot = draw.q;

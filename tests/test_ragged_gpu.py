@@ -175,3 +175,52 @@ def test_ragged_cfg3_sizes(sv, olib):
     data = wl.generate(spec)
     kb = np.random.default_rng(3).integers(0, spec.K + 1, spec.B)
     run_pair(sv, olib, data, kb, spec.K, spec.dtype, False, "ragged cfg3")
+
+
+def test_no_draft_rejections_draw_from_one_chunk(sv, olib):
+    """Without draft probabilities a rejection's residual is p_n less the
+    rejected token; at B=300, V=50000 fp32 (clusters of 2, chunks shorter
+    than a CTA's slice) it is drawn from the one chunk that holds U * R, the
+    token's mass taken from its chunk.  Rows whose rejected token holds most
+    of the mass (p = 0.8, drafted and rejected by u = 0.95) read the whole
+    row instead; at p = 0.3 the chunk's mass loses 0.3 of the row's to the
+    correction.  Every row against the oracle."""
+    B, K, V = 300, 3, 50000
+    spec = wl.custom("ndlocal", B=B, K=K, V=V, dtype=wl.FP32, temps=(0.7, 1.0),
+                     sigma_d=(0.3, 2.0), seed=wl.SEED_BASE + 9600)
+    data = wl.generate(spec)
+    zt = data["target"].copy()
+    tok = data["tokens"].copy()
+    u = data["uniforms"].copy()
+    rng = np.random.default_rng(96)
+    dom = rng.choice(B, 60, replace=False)
+    for i, b in enumerate(dom):  # a drafted token of p = 0.8 (or 0.3) at position 0, rejected
+        x = int(rng.integers(0, V))
+        T = float(data["temperature"][b])
+        others = np.delete(zt[b, 0].astype(np.float64), x) / T
+        lse = others.max() + np.log(np.exp(others - others.max()).sum())
+        pt = 0.8 if i % 2 == 0 else 0.3
+        zt[b, 0, x] = np.float32(T * (lse + np.log(pt / (1.0 - pt))))
+        tok[b, 0] = x
+        u[b, 0] = 0.95
+    g = sv.specv_verify(to_dev(zt), None, to_dev(tok), to_dev(data["temperature"]), to_dev(u))
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in g.items()}
+    o = oracle.verify(zt, None, tok, data["temperature"], u, nthreads=0, lib=olib, no_draft=True)
+    err = o["status"] & oracle.ROW_ERRORS
+    assert np.array_equal(g["row_status"] & oracle.ROW_ERRORS, err)
+    ok = ~o["boundary"].astype(bool)
+    assert np.array_equal(g["accept_len"][ok], o["accept_len"][ok])
+    assert np.array_equal(g["out_tokens"][ok], o["out_tokens"][ok])
+    fb = ok & (err == 0)
+    assert np.array_equal(g["row_status"][fb] & oracle.ROW_FALLBACK, o["status"][fb] & oracle.ROW_FALLBACK)
+    assert np.abs(g["p_draft"] - o["p"]).max() <= PROB_TOL
+    differ = int(((g["accept_len"] != o["accept_len"]) | (g["out_tokens"] != o["out_tokens"]).any(axis=1)).sum())
+    assert differ <= max(1, B // 50), differ
+    rej = (o["accept_len"][dom] == 0).mean()
+    assert rej > 0.9, rej  # the dominant rows do reject at position 0
+    for b in range(B):
+        n = g["accept_len"][b]
+        if n < K:
+            assert g["out_tokens"][b, n] != tok[b, n]
+    print(f"no-draft local draw: boundary rows {int(o['boundary'].sum())}/{B}, differing {differ}")

@@ -6,7 +6,8 @@ host's choices that depend on the sizes (chunk length and count, the
 one-wave rule, the kernel-B cluster size and slice, the chunk-local draw,
 ring or direct residual pass) meet combinations nobody picked: batch sizes
 from 1 to 1216 across the cluster-size thresholds, K from 1 to 12, V from 1
-to 152064, both dtypes, the three logit recipes, mixed temperatures and
+to 152064, both dtypes, the three logit recipes, mixed temperatures,
+drafts without probabilities (a third of the verification shapes) and
 F from 1 to 12 (and below: 24 MSS shapes and 16 sampler shapes, with the
 bars of tests/test_mss_gpu.py and tests/_sampler_case.py, and 16 outcome
 prediction shapes with fan-outs and ties, keys exact).  Same bars as
@@ -48,7 +49,8 @@ def _shapes(n=64, seed=20261202):
         temps = tuple(sorted(set(float(t) for t in rng.choice([0.0, 0.5, 0.8, 1.0, 1.5],
                                                               int(rng.integers(1, 4))))))
         F = int(rng.integers(1, 13)) if ssd else 0
-        out.append(dict(B=B, K=K, V=V, dtype=dtype, kind=kind, temps=temps, ssd=ssd, F=F,
+        nd = not ssd and len(out) % 3 == 1  # a third of the verification shapes: no draft logits
+        out.append(dict(B=B, K=K, V=V, dtype=dtype, kind=kind, temps=temps, ssd=ssd, F=F, nd=nd,
                         seed=wl.SEED_BASE + 12000 + len(out)))
     return out
 
@@ -73,7 +75,7 @@ def olib():
 
 
 def _id(s):
-    mode = f"ssdF{s['F']}" if s["ssd"] else "verify"
+    mode = f"ssdF{s['F']}" if s["ssd"] else ("verify-nodraft" if s["nd"] else "verify")
     return f"{mode}-B{s['B']}-K{s['K']}-V{s['V']}-{s['dtype']}-{s['kind']}"
 
 
@@ -90,6 +92,17 @@ def test_sweep_matches_oracle(sv, olib, shape):
         g = gpu_ssd(sv, data, shape["F"])
         o, keys, kl = oracle_ssd(olib, data, shape["F"])
         compare_ssd(olib, g, o, keys, kl, data["temperature"], _id(shape))
+    elif shape["nd"]:  # q one-hot at each draft token (NO_DRAFT_PROBS)
+        t = torch.from_numpy(np.ascontiguousarray(data["target"]))
+        tgt = (t.view(torch.bfloat16) if shape["dtype"] == wl.BF16 else t).cuda()
+        out = sv.specv_verify(tgt, None, torch.from_numpy(data["tokens"]).cuda(),
+                              torch.from_numpy(data["temperature"]).cuda(),
+                              torch.from_numpy(data["uniforms"]).cuda())
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy() for k, v in out.items()}
+        o = oracle.verify(data["target"], None, data["tokens"], data["temperature"], data["uniforms"],
+                          nthreads=0, lib=olib, no_draft=True)
+        compare_verify(g, o, data["temperature"], _id(shape))
     else:
         g = gpu_verify(sv, data)
         o = oracle_verify(olib, data)
