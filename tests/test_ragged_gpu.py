@@ -89,6 +89,7 @@ def run_pair(sv, olib, data, kb, K, dtype, no_draft, label):
     (8, 4, 4097, wl.BF16),
     (5, 6, 20001, wl.FP32),
     (4, 8, 131071, wl.BF16),
+    (300, 4, 50000, wl.FP32),  # clusters of 2: bonus and no-draft draws from one chunk
 ])
 @pytest.mark.parametrize("no_draft", [False, True])
 def test_ragged_rows(sv, olib, B, K, V, dtype, no_draft):
