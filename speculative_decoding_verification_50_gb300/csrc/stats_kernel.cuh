@@ -179,9 +179,11 @@ struct SoftG {
     m = kNegMax;
     s0 = s1 = f2(0.f, 0.f);
   }
-  __device__ __forceinline__ void add(const float (&z)[N], float c) {
+  __device__ __forceinline__ void add(const float (&z)[N], float c) { add_max(z, c, group_max(z, m)); }
+  // mn: max(m, the group's max), NaN ignored (taken once per group when the
+  // outcome-prediction tracking needs the group's own max as well)
+  __device__ __forceinline__ void add_max(const float (&z)[N], float c, float mn) {
     static_assert(N % 4 == 0, "groups of whole pairs of pairs");
-    const float mn = group_max(z, m);
     const float f = ex2(__fmul_rn(__fsub_rn(m, mn), c));  // exactly 1 when m is unchanged
     const uint64_t ff = f2(f, f);
     s0 = f2_mul(s0, ff);
@@ -247,7 +249,10 @@ struct BestGroup {
     for (int k = 0; k < N; ++k) z[k] = neg_inf();
   }
   __device__ __forceinline__ void add(const float (&zz)[N], int t) {
-    const float vm = group_max(zz, neg_inf());  // NaN ignored
+    add_max(zz, t, group_max(zz, neg_inf()));  // NaN ignored
+  }
+  // vm: the group's max, NaN ignored
+  __device__ __forceinline__ void add_max(const float (&zz)[N], int t, float vm) {
     const bool nb = vm > m1;
     m2 = nb ? m1 : fmaxf(m2, vm);
     t1 = nb ? t : t1;
@@ -274,6 +279,12 @@ struct Acc {
   template <bool GREEDY, bool DRAFT, bool TOPF>
   __device__ __forceinline__ void add(const float (&z)[N], const int32_t (&base)[kVecs], float c,
                                       int t) {
+    if (!GREEDY && DRAFT && TOPF) {  // one group max serves both (max is exact)
+      const float gz = group_max(z, neg_inf());
+      sd.add_max(z, c, fmaxf(sd.m, gz));
+      kd.add_max(z, t, gz);
+      return;
+    }
     if (GREEDY) (DRAFT ? ad : at).template add<VW>(z, base);
     else (DRAFT ? sd : st).add(z, c);
     if (DRAFT && TOPF) kd.add(z, t);
