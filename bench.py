@@ -92,7 +92,9 @@ GEOMETRIC = {"cfg5-ssd-geo": (0.5, 1.0, 54)}
 
 KERNEL_DIR = os.path.join(ROOT, "speculative_decoding_verification_50_gb300", "csrc")
 # Sources of the row-statistics kernel, the one the roofline reports on.
-KERNEL_SRCS = ("stats_kernel.cuh", "specv_device.cuh", "specv_common.cuh")
+# kernel A's sources and the host code that sizes its chunks: a recorded DRAM
+# traffic figure holds only for the code it was captured with
+KERNEL_SRCS = ("stats_kernel.cuh", "specv_device.cuh", "specv_common.cuh", "specv_api.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 

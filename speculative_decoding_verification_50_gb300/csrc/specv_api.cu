@@ -112,6 +112,17 @@ struct Plan {
   size_t piece_bytes;  // the sampler's piece table (kMaxPieces entries per chunk), or 0
 };
 
+// Loop trips per chunk of rows that carry top-F candidates (outcome keys),
+// on grids of at least four waves: the per-chunk selection and its ramp are
+// paid fewer times than at 8 trips.
+// cfg5-ssd (256 x 9 items of 152064 fp32) per call: 8 trips 0.4583 ms, 10
+// 0.4531, 11 0.4551, 12 0.4528, 13 0.4543, 14 0.4622, 15 0.4654 (longer
+// chunks leave more threads with two groups above the candidate bound, whose
+// whole share is read again); the geometric fan-out and Saguaro rounds the
+// same way (0.4729 -> 0.4642, 0.4640 -> 0.4584).  Verification alone stays
+// at 8 (12: 0.4140 -> 0.4152 ms).
+constexpr int kTopFIters = 12;
+
 int sm_count() {
   static const int n = [] {
     int dev = 0, c = 0;
@@ -127,9 +138,11 @@ int sm_count() {
 // rejection, and two CTAs per node halve each pass (measured best at 2048
 // nodes of 152064 fp32 logits: 1 -> 0.69 ms, 2 -> 0.58, 4 -> 0.60, 8 -> 0.61).
 // iters0: loop trips per chunk before halving.  The sampler's rows all carry
-// top-F candidates, whose per-chunk selection is worth amortising over 16
-// trips (kernel A 258 -> 215 us on 2304 rows of 152064 fp32); the decision
-// kernel's chunk-local draw reads up to 16 trips.
+// top-F candidates, whose per-chunk selection is worth amortising over longer
+// chunks (kernel A 258 -> 215 us on 2304 rows of 152064 fp32 at 16 trips; 32
+// with its pieces); the decision kernel's chunk-local draw reads up to 16
+// trips.  Other rows with top-F candidates take kTopFIters trips when their
+// grid spans several waves (below).
 Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int min_cb = 1,
                int iters0 = 8, int max_cb = 16, bool piece_table = false) {
   Plan pl;
@@ -163,6 +176,24 @@ Plan make_plan(int32_t B, int32_t K, int32_t V, int32_t F, int32_t dtype, int mi
         break;
       }
     }
+  }
+  // Rows with top-F candidates over a grid of several waves: longer chunks
+  // (kTopFIters trips), so each chunk's selection is paid fewer times.
+  if (env_iters < 1 && F > 0 && !piece_table && pl.iters < kTopFIters && units * pl.nchunk >= 4 * slots) {
+    pl.iters = kTopFIters;
+    pl.chunk = static_cast<int64_t>(pl.iters) * kVecs * kThreads * vw;
+    pl.nchunk = (static_cast<int64_t>(V) + pl.chunk - 1) / pl.chunk;
+  }
+  // In a single wave the longest chunk sets the kernel's time: the same
+  // number of chunks, each as short as that allows (config 4's rows of 31.3
+  // trips: 12 + 12 + 7.3 -> 11 + 11 + 9.3).  Not for the sampler, whose
+  // pieces are eighths of its chunks.
+  if (env_iters < 1 && !piece_table && units * pl.nchunk <= slots && pl.nchunk > 1) {
+    const int64_t trip = static_cast<int64_t>(kVecs) * kThreads * vw;
+    const int64_t trips = (static_cast<int64_t>(V) + trip - 1) / trip;
+    pl.iters = static_cast<int>((trips + pl.nchunk - 1) / pl.nchunk);
+    pl.chunk = static_cast<int64_t>(pl.iters) * trip;
+    pl.nchunk = (static_cast<int64_t>(V) + pl.chunk - 1) / pl.chunk;
   }
   pl.CB = pick_cluster(B, V, vw, min_cb, max_cb);
   pl.L = slice_len(V, pl.CB, vw);
