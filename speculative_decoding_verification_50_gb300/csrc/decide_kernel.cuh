@@ -138,13 +138,16 @@ __device__ __forceinline__ PosStats combine_position(const ChunkRec* R, int nchu
 
 // Top-F keys of one draft row from its per-chunk candidate lists, by one warp
 // (lanes < F end with the keys of rank `lane`; (-inf, INT_MAX) where the row
-// has fewer than F).  Up to kWarpCand candidates are staged in the warp's
-// shared scratch and ranked by counting (independent comparisons); larger sets
-// are merged by warp insertion.
+// has fewer than F).  Up to kStageCand candidates are staged in the warp's
+// shared scratch and merged by the lists' heads (or ranked by counting when
+// there are more lists than lanes); larger sets are merged by warp
+// insertion.  The sampler's CTA ranks up to kWarpCand candidates with all
+// its threads (four per candidate).
 constexpr int kWarpCand = 64;
+constexpr int kStageCand = 128;  // a fan-out's widest lookahead: 7 chunks x 16 keys
 struct WarpKeys {
-  float v[kWarpCand];
-  int32_t i[kWarpCand];
+  float v[kStageCand];
+  int32_t i[kStageCand];
   float ov[kMaxF];
   int32_t oi[kMaxF];
 };
@@ -152,9 +155,10 @@ struct WarpKeys {
 __device__ __forceinline__ WarpTopF merge_candidates(const float* cv, const int32_t* ci, int ncand,
                                                      int F, int lane);
 
+// nkeep <= F: only the first nkeep keys are wanted (a fan-out's lookahead).
 __device__ __forceinline__ WarpTopF warp_keys(const float* cv, const int32_t* ci, int ncand, int F,
-                                              int lane, WarpKeys& S) {
-  if (ncand > kWarpCand) return merge_candidates(cv, ci, ncand, F, lane);
+                                              int lane, WarpKeys& S, int nkeep = kMaxF) {
+  if (ncand > kStageCand) return merge_candidates(cv, ci, ncand, F, lane);
   for (int e = lane; e < ncand; e += 32) {
     S.v[e] = __ldcg(cv + e);
     S.i[e] = __ldcg(ci + e);
@@ -174,7 +178,8 @@ __device__ __forceinline__ WarpTopF warp_keys(const float* cv, const int32_t* ci
       hv = S.v[lane * F];
       hi = S.i[lane * F];
     }
-    for (int f = 0; f < F; ++f) {
+    const int rounds = min(F, nkeep);
+    for (int f = 0; f < rounds; ++f) {
       float bv = hv;
       int32_t bi = hi;
       int bl = lane;
@@ -1398,7 +1403,7 @@ __global__ void __launch_bounds__(kThreads, 4) decide_kernel(const DecideParams 
     for (int k = rank + (warp - 1) * CB; k <= K; k += CB * (kWarps - 1)) {
       const int64_t u = u0 + k;
       const WarpTopF L = warp_keys(P.cand_v + u * P.nchunk * F, P.cand_i + u * P.nchunk * F,
-                                   static_cast<int>(P.nchunk) * F, F, lane, wkeys[warp]);
+                                   static_cast<int>(P.nchunk) * F, F, lane, wkeys[warp], P.fk[k]);
       if (lane < F) {
         const bool good = ok && lane < P.fk[k] && L.i != INT_MAX;
         P.keys[u * F + lane] = good ? L.i : -1;
